@@ -1,0 +1,325 @@
+/*
+ * bi.h — C ABI of the batch-invariant decoder forward library (libbi.so, sm_103a).
+ *
+ * What it computes: a pre-norm decoder forward (RMSNorm, GEMMs, RoPE, paged-KV
+ * causal GQA attention with a fixed KV split, SwiGLU FFN or a top-k MoE FFN)
+ * that ends in each sampled token's logprob.  Every row's result depends only
+ * on that row's own inputs and absolute position, so a token gets the same
+ * bits in a decode step, in a prefill chunk of any size and in any batch.
+ *
+ * Sources: "vLLM Achieves Bitwise-Consistent RL Training: Eliminating Numerical
+ * Drift to Zero KL Divergence on DeepSeek-V4-Flash at 91% Throughput" (the
+ * Article), §2 (requirements: kernel determinism, batch independence, phase
+ * consistency, same numerical contract, same discrete choices), §3.1 (training
+ * forward calls the inference kernels), §4.1-4.6 (per-operator choices); and the
+ * zero-mismatch-rl README ("Key features": fixed-split attention, fixed slot
+ * order MoE combine).
+ *
+ * Conventions (all calls):
+ *  - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous; bf16 tensors are passed as void*.  The library never frees
+ *    caller memory and allocates no device memory in any call (the model
+ *    handle holds only host-side data).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream).  No call synchronises or reads device data
+ *    back to the host, so calls can be captured into a CUDA graph once the
+ *    same call has run once eagerly (first use configures kernel attributes).
+ *  - Shapes are int64_t.  Invalid shapes or NULL required pointers return
+ *    BI_ERR_INVALID_ARG (or BI_ERR_UNSUPPORTED_SHAPE for legal but
+ *    unimplemented shapes) before anything is launched; bi_last_error() then
+ *    describes the problem (thread-local string).
+ *  - `mode` is BI_INVARIANT (the batch-invariant path) or BI_FAST, the same
+ *    kernels with batch-dependent choices (split-K chosen from M, attention
+ *    split size chosen from the batch, vocab split across CTAs) used as the
+ *    non-invariant comparison baseline ([Article] §1: the >= 70% bar is
+ *    measured against an equally optimised baseline).  BI_FAST results are NOT
+ *    batch invariant.
+ *  - Device-side waits are bounded; a kernel that gives up, or that sees an
+ *    out-of-range index, records a code that bi_device_status() reports as
+ *    BI_ERR_TIMEOUT / BI_ERR_DEVICE_CHECK.  Nothing traps.
+ */
+#ifndef BI_H_
+#define BI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BI_OK = 0,
+  BI_ERR_INVALID_ARG = 1,
+  BI_ERR_UNSUPPORTED_SHAPE = 2,
+  BI_ERR_CUDA = 3,
+  BI_ERR_DEVICE_CHECK = 4,
+  BI_ERR_TIMEOUT = 5
+} bi_status;
+
+typedef enum { BI_INVARIANT = 0, BI_FAST = 1 } bi_mode;
+typedef enum { BI_DTYPE_BF16 = 0, BI_DTYPE_FP32 = 1 } bi_dtype;
+typedef enum { BI_EPI_NONE = 0, BI_EPI_SWIGLU = 1 } bi_epilogue;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int bi_version(void);
+/* Description of the last error returned on this host thread ("" if none). */
+const char* bi_last_error(void);
+/* Number of kernel launches this library has issued from the host in this
+ * process (a CUDA graph replay re-runs captured launches without counting). */
+int64_t bi_launch_count(void);
+/* Synchronises the current device, then returns BI_OK, BI_ERR_TIMEOUT (a
+ * bounded device wait gave up) or BI_ERR_DEVICE_CHECK (a kernel saw an
+ * out-of-range index) and clears the device status word. */
+bi_status bi_device_status(void);
+
+/* ------------------------------------------------------------------ RMSNorm
+ * [Article] §3.1 (RMSNorm is one of the forward operators whose values come
+ * from the inference kernel), §2 (batch independence).
+ * y[r] = bf16( s[r] * (1 / sqrt(sum_i s[r,i]^2 / d + eps)) * gamma ), fp32 math,
+ * where s = bf16(residual + x) if `residual` is non-NULL (and s is written back
+ * into `residual`), else s = x.  One CTA per row; the sum of squares uses a fixed
+ * per-thread stride, a fixed xor-butterfly warp tree and a fixed cross-warp order,
+ * so a row's bits never depend on `rows`.
+ * x, y: bf16 [rows, d]; residual: bf16 [rows, d] or NULL; gamma: bf16 [d].
+ * d % 8 == 0, 8 <= d <= 16384, pointers 16-byte aligned.  y may alias x. */
+bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, int64_t rows,
+                     int64_t d, float eps, int mode, void* stream);
+
+/* --------------------------------------------------------------------- GEMM
+ * [Article] §4.1 "Dense GEMM: one accumulation order for every M".
+ * C[m, n] = sum_k A[m, k] * W[n, k] with bf16 inputs and fp32 accumulation on
+ * the tcgen05 tensor cores (TMEM accumulator, TMA-fed 128B-swizzled tiles).
+ * In BI_INVARIANT mode the tile is 128 x BN x 64 with BN a function of (N, K,
+ * epilogue) only, K is consumed in ascending 16-wide steps, never split: the
+ * bits of row m do not depend on M or on the other rows.
+ * A: bf16 [M, K]; W: bf16 [N, K] (nn.Linear layout); C: bf16 or fp32 [M, N]
+ * (c_dtype), or for BI_EPI_SWIGLU: W holds 2F rows (gate rows then up rows)
+ * and C is bf16 [M, F] with C = bf16( silu(bf16(g)) * bf16(u) ) computed in
+ * fp32 and rounded once ([Article] §4.4, condition 3).
+ * K % 64 == 0, N % 8 == 0 (F % 8 == 0 for SwiGLU), pointers 16-byte aligned.
+ * `workspace` (may be NULL when bi_gemm_workspace_size() returns 0) holds the
+ * fp32 split-K partials of BI_FAST mode. M == 0 is a no-op. */
+bi_status bi_gemm(const void* A, int64_t M, int64_t K, const void* W, int64_t N, void* C, int c_dtype,
+                  int epilogue, int mode, void* workspace, size_t ws_bytes, void* stream);
+size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int epilogue, int mode);
+/* The N tile width bi_gemm uses for a weight of shape (N, K) (diagnostic). */
+int bi_gemm_tile_n(int64_t N, int64_t K, int epilogue);
+
+/* Grouped GEMM over 128-row tiles, each tile owned by one expert
+ * ([Article] §4.4 "Expert GEMM: two layouts, same row result").
+ * A: bf16 [M_rows, K] in a padded layout whose 128-row tile t belongs to
+ * expert tile_expert[t] (device int32 [M_rows/128]; -1 = empty tile, skipped);
+ * W: bf16 [E, N, K]; C: [M_rows, N] (or [M_rows, N/2] for SwiGLU).  Works for
+ * the contiguous (packed by expert, padded to 128) and the masked (fixed
+ * capacity per expert) layouts alike; a row's bits do not depend on the layout.
+ * M_rows % 128 == 0. */
+bi_status bi_grouped_gemm(const void* A, int64_t M_rows, int64_t K, const void* W, int64_t E, int64_t N,
+                          const int32_t* tile_expert, void* C, int c_dtype, int epilogue, void* stream);
+
+/* ------------------------------------------------------- RoPE + paged KV write
+ * [Article] §4.2 (prefill, decode and training share one KV write and read
+ * path; training writes into a private cache the same way).
+ * For the T rows of a call, grouped into P "pieces" (consecutive tokens of one
+ * sequence): piece p covers rows piece_row0[p] .. piece_row0[p+1]-1 of
+ * sequence piece_seq[p] at absolute positions piece_pos0[p] + i.
+ * qkv: bf16 [T, (Hq + 2 Hkv) hd] (q heads, k heads, v heads);
+ * q_out: bf16 [T, Hq, hd] = rope(q); k_cache / v_cache: bf16
+ * [n_blocks, Hkv, 64, hd] (one layer) receive rope(k) and v at
+ * block_table[seq, pos / 64], slot pos % 64.  rope_table: fp32 [max_pos, hd]
+ * (cos for i < hd/2 in the first half of each row, sin in the second), filled by
+ * bi_rope_table().  Rotate-half pairs (i, i + hd/2), applied in fp32, rounded
+ * once to bf16. max_q_len bounds the piece lengths (host value). */
+bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                           const float* rope_table, int64_t max_pos, const int32_t* block_table,
+                           int64_t max_blocks_per_seq, int64_t n_blocks, void* q_out, void* k_cache,
+                           void* v_cache, void* stream);
+/* rope_table[p, i] = cos(p * theta^(-2i/hd)), rope_table[p, hd/2 + i] = sin(...),
+ * angles and functions evaluated in fp64 on the device, rounded to fp32. */
+bi_status bi_rope_table(float* rope_table, int64_t max_pos, int hd, double theta, void* stream);
+
+/* ---------------------------------------------------------------- attention
+ * [Article] §4.2 (one read path for prefill and decode; decode's default
+ * batch-dependent partition is given up) and the zero-mismatch-rl README
+ * ("fixed-split attention").
+ * Causal GQA over the paged cache.  Row (token t, q head h) at position p
+ * attends to keys 0..p of its sequence through kv head h / (Hq/Hkv).  Keys are
+ * processed in splits of `kv_split` absolute positions (512 by default, a
+ * multiple of 64) and, inside a split, in tiles of 64 (one cache block) in
+ * ascending order with an fp32 online softmax (scores and P in bf16 MMA, P
+ * rounded to bf16).  The per-split partials (m, l, acc) are merged in
+ * ascending split order:  M = max m_s, L = sum l_s 2^(m_s - M),
+ * O = sum acc_s 2^(m_s - M), out = bf16(O / L).  Split and tile boundaries are
+ * absolute positions, so a decode row reproduces its prefill row exactly.
+ * q: bf16 [T, Hq, hd] (pieces as in bi_rope_kv_write); out: bf16 [T, Hq * hd].
+ * hd in {64, 128}; Hq % Hkv == 0; 64 % (Hq/Hkv) == 0.  max_ctx (host value)
+ * bounds every sequence's context length in this call.  workspace must hold
+ * bi_attention_workspace_size(T, Hq, hd, max_ctx, kv_split) bytes.
+ * In BI_FAST mode the split size is chosen from the batch (flash-decoding
+ * heuristic) and results are not batch invariant. */
+bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                       const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale, void* workspace,
+                       size_t ws_bytes, void* out, int mode, void* stream);
+size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ctx, int kv_split);
+
+/* ---------------------------------------------------------- embed / logprob
+ * Row gather: out[t] = table[ids[t]] (bf16 [V, d] -> bf16 [T, d]).  Ids outside
+ * [0, V) write zeros and record BI_ERR_DEVICE_CHECK. */
+bi_status bi_embed(const int32_t* ids, int64_t T, const void* table, int64_t V, int64_t d, void* out,
+                   void* stream);
+
+/* [Article] §2 (diff is defined on each sampled token's logprob), §3.1 ("the
+ * final logprob").  For each row t of fp32 logits [T, V]:
+ *   lse = m + log(sum_v exp(x_v - m)),   lp[t] = x[t, id_t] - lse
+ * with one CTA per row, a single pass keeping an online (max, sum) per thread
+ * over a fixed index stride, and a fixed butterfly / cross-warp merge order.
+ * ids: device int32 [T] or NULL (greedy: id = argmax, ties to the lowest id).
+ * argmax_out: device int32 [T] or NULL.  V >= 1, V % 4 == 0.
+ * BI_FAST splits the vocab across CTAs when T is small (not batch invariant);
+ * it then needs bi_logprob_workspace_size() bytes of workspace. */
+bi_status bi_logprob_gather(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
+                            int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes, void* stream);
+size_t bi_logprob_workspace_size(int64_t T, int64_t V, int mode);
+
+/* ---------------------------------------------------------------------- MoE
+ * Router: [Article] §2 "the same discrete choices", §4.4 (router output fp32
+ * at every batch size).  For each token, the k largest of E fp32 logits
+ * (ties to the lower expert id), slot 0 = best; weights = softmax over the k
+ * selected logits in slot order.  ids: int32 [T, k], weights: fp32 [T, k].
+ * E <= 64, k <= E. */
+bi_status bi_moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* weights,
+                            void* stream);
+
+/* Contiguous expert layout ([Article] §4.4, training side): a stable counting
+ * sort of the T*k (token, slot) pairs by expert, each expert's rows padded to a
+ * multiple of 128.  Outputs: row_of_slot int32 [T*k] (row in the padded layout
+ * of pair (t, s)), tile_expert int32 [max_rows/128] (-1 for unused tiles) and
+ * expert_offsets int32 [E+1].  max_rows >= T*k + 128*E rounded to 128.
+ * workspace: bi_moe_permute_workspace_size(T, k, E) bytes. */
+bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t max_rows, int32_t* row_of_slot,
+                         int32_t* tile_expert, int32_t* expert_offsets, void* workspace, size_t ws_bytes,
+                         void* stream);
+size_t bi_moe_permute_workspace_size(int64_t T, int k, int E);
+/* Masked expert layout ([Article] §4.4, rollout side): expert e owns rows
+ * [e*capacity, (e+1)*capacity); pairs beyond an expert's capacity are an error
+ * (BI_ERR_DEVICE_CHECK).  capacity % 128 == 0. */
+bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int64_t capacity,
+                                int32_t* row_of_slot, int32_t* tile_expert, void* workspace, size_t ws_bytes,
+                                void* stream);
+/* xp[row_of_slot[t*k+s]] = x[t] for every (t, s) (bf16 rows of length d). */
+bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, int k, int64_t d, void* xp,
+                        void* stream);
+/* [Article] §4.5 ("accumulated in FP32 in top-k slot order") and the README
+ * ("fixed slot order"): out[t] = bf16( sum_{s=0..k-1} w[t,s] * y[row_of_slot[t*k+s]] ),
+ * fp32, slots summed sequentially.  y: bf16 [rows, d]; out: bf16 [T, d].
+ * BI_FAST uses fp32 atomics (order not fixed) and needs
+ * bi_moe_combine_workspace_size() bytes. */
+bi_status bi_moe_combine(const void* y, const int32_t* row_of_slot, const float* w, int64_t T, int k, int64_t d,
+                         void* out, int mode, void* workspace, size_t ws_bytes, void* stream);
+size_t bi_moe_combine_workspace_size(int64_t T, int64_t d, int mode);
+
+/* Whole MoE FFN layer: route, permute (contiguous layout), gather, grouped
+ * gate_up GEMM with SwiGLU, grouped down GEMM, slot-order combine.
+ * x: bf16 [T, d]; router_logits fp32 [T, E]; w13 bf16 [E, 2F, d]; w2 bf16 [E, d, F];
+ * out bf16 [T, d].  workspace: bi_moe_layer_workspace_size() bytes. */
+bi_status bi_moe_layer(const void* x, const float* router_logits, int64_t T, int64_t d, int E, int k, int64_t F,
+                       const void* w13, const void* w2, void* out, int mode, void* workspace, size_t ws_bytes,
+                       void* stream);
+size_t bi_moe_layer_workspace_size(int64_t T, int64_t d, int E, int k, int64_t F, int mode);
+
+/* ------------------------------------------------------------- model driver
+ * [Article] §3.1: the training forward calls the inference kernels; here both
+ * the rollout (decode) and the training recompute (chunked prefill) call the
+ * same entry points below, which call the same kernels. */
+typedef struct {
+  int64_t n_layers, d, n_heads_q, n_heads_kv, head_dim, ffn, vocab;
+  float eps;          /* RMSNorm epsilon (1e-6) */
+  float rope_theta;   /* 10000 */
+  int64_t kv_block;   /* tokens per cache block: must be 64 */
+  int64_t kv_split;   /* attention KV split, multiple of 64 (512) */
+  int64_t max_pos;    /* rows of the RoPE table = maximum context length */
+} bi_model_config;
+
+typedef struct {
+  const void* attn_norm; /* bf16 [d] */
+  const void* wqkv;      /* bf16 [(Hq + 2 Hkv) hd, d] */
+  const void* wo;        /* bf16 [d, Hq hd] */
+  const void* ffn_norm;  /* bf16 [d] */
+  const void* w13;       /* bf16 [2F, d]: gate rows, then up rows */
+  const void* w2;        /* bf16 [d, F] */
+} bi_layer_weights;
+
+typedef struct {
+  const void* embed;              /* bf16 [V, d] */
+  const void* final_norm;         /* bf16 [d] */
+  const void* lm_head;            /* bf16 [V, d] */
+  const bi_layer_weights* layers; /* host array [n_layers] (copied) */
+  float* rope_table;              /* device fp32 [max_pos, hd], caller-allocated; filled by bi_model_create */
+} bi_weights;
+
+typedef struct bi_model bi_model;
+
+/* Validates the config, copies the weight pointers (weights stay owned by the
+ * caller and may be overwritten in place between calls: [Article] §4.6,
+ * conflict 3) and fills the RoPE table on `stream`. */
+bi_status bi_model_create(const bi_model_config* cfg, const bi_weights* w, void* stream, bi_model** out);
+void bi_model_destroy(bi_model* m);
+
+/* Paged KV cache of one model: k_cache and v_cache are bf16
+ * [n_layers, n_blocks, Hkv, 64, hd]; block_table is int32 [B, max_blocks_per_seq]. */
+size_t bi_kv_cache_bytes(const bi_model_config* cfg, int64_t n_blocks);
+
+/* Workspace for bi_forward_prefill / bi_forward_decode: sized only by limits
+ * (max_tokens rows per layer pass, max_pieces sequences per pass, max_ctx
+ * context, max_logit_rows lm_head rows per launch), never by the batch of a
+ * particular call ([Article] §4.6, conflict 2). */
+size_t bi_forward_workspace_size(const bi_model_config* cfg, int64_t max_tokens, int64_t max_pieces,
+                                 int64_t max_ctx, int64_t max_logit_rows, int mode);
+
+/* Chunked, packed prefill (rollout prompt processing and training recompute).
+ * tokens: device int32 [T], sequences packed back to back; cu_seqlens (HOST
+ * int64 [B+1]) gives sequence b's rows; start_pos (HOST int64 [B]) is how many
+ * tokens of sequence b are already in the cache (its first row sits at that
+ * position).  Rows are processed in chunks of at most `chunk` tokens per
+ * sequence and passes of at most `max_tokens` rows (the workspace limit).
+ * logit_from (HOST int64 [B] or NULL = every row): the first in-call row index
+ * of sequence b whose logprob is wanted; rows from there to the sequence end
+ * get logits.  target_ids: device int32 [T] (target of each row) or NULL for
+ * greedy (argmax).  logprob_out (fp32 [T]) and sampled_out (int32 [T], may be
+ * NULL) are written for rows with logits only.  block_table: device int32
+ * [B, max_blocks_per_seq]. */
+bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* target_ids,
+                             const int64_t* cu_seqlens, const int64_t* start_pos, const int64_t* logit_from,
+                             int64_t B, int64_t chunk, const int32_t* block_table, int64_t max_blocks_per_seq,
+                             void* k_cache, void* v_cache, int64_t n_blocks, float* logprob_out,
+                             int32_t* sampled_out, void* workspace, size_t ws_bytes, int64_t max_tokens,
+                             int64_t max_ctx, int64_t max_logit_rows, int mode, void* stream);
+
+/* One greedy decode step for B sequences: token b (device int32 [B]) sits at
+ * position pos[b] (device int32 [B]); its K/V are written to the cache, and the
+ * argmax of the next-token distribution and its logprob are written to
+ * sampled_out / logprob_out (device [B]).  max_ctx is a static upper bound on
+ * pos[b] + 1 (a graph captured with it stays valid while the bound holds).
+ * No host reads: capturable into a CUDA graph. */
+bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* pos, int64_t B,
+                            const int32_t* block_table, int64_t max_blocks_per_seq, void* k_cache, void* v_cache,
+                            int64_t n_blocks, int64_t max_ctx, int32_t* sampled_out, float* logprob_out,
+                            void* workspace, size_t ws_bytes, int mode, void* stream);
+
+/* Rollout bookkeeping after a decode step (device only, capturable):
+ * hist_ids[step, b] = sampled[b], hist_lp[step, b] = logprob[b] with
+ * step = *step_counter; then tokens[b] = sampled[b], pos[b] += 1, and
+ * *step_counter += 1.  hist_*: [max_steps, B]; steps beyond max_steps are
+ * dropped and recorded as BI_ERR_DEVICE_CHECK. */
+bi_status bi_decode_advance(const int32_t* sampled, const float* logprob, int32_t* tokens, int32_t* pos,
+                            int64_t B, int32_t* step_counter, int32_t* hist_ids, float* hist_lp,
+                            int64_t max_steps, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BI_H_ */

@@ -1,0 +1,479 @@
+// RoPE + paged KV write, fixed-split paged attention and the ascending-order split merge.
+//
+// "vLLM Achieves Bitwise-Consistent RL Training ..." §4.2 ("FP8 KV cache: keep
+// FP8 storage, unify the read path"): decode gives up its own batch-partitioned
+// kernel and goes through prefill's algorithm, and training writes and reads a
+// private cache the same way.  The zero-mismatch-rl README lists "fixed-split
+// attention" for the hybrid model.  Here there is one attention kernel for
+// prefill chunks and decode steps alike:
+//   * a CTA owns (piece, 64-row query tile, kv head, split); rows are
+//     (token, q head of the group) pairs;
+//   * splits cover ABSOLUTE positions [s*S, (s+1)*S), S = kv_split, and inside a
+//     split 64-key tiles (one cache block each) are taken in ascending order;
+//   * scores and P*V run on bf16 mma.sync tensor-core tiles (row-independent),
+//     the online softmax is fp32 with masking by select, so a key tile that is
+//     fully masked for a row leaves that row's (m, l, acc) bit-for-bit unchanged;
+//   * keys beyond the CTA's last query position are zero-filled, so stale cache
+//     contents never reach the arithmetic;
+//   * partials (m, l, acc) are merged per row in ascending split order.
+// A decode row therefore reproduces its prefill row exactly.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace bi {
+
+// ------------------------------------------------------------------ RoPE table
+__global__ void rope_table_kernel(float* table, int64_t max_pos, int hd, double theta) {
+  const int half = hd / 2;
+  const int64_t total = max_pos * half;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t p = idx / half;
+    const int i = (int)(idx % half);
+    const double inv_freq = pow(theta, -2.0 * (double)i / (double)hd);
+    const double ang = (double)p * inv_freq;
+    table[p * hd + i] = (float)cos(ang);
+    table[p * hd + half + i] = (float)sin(ang);
+  }
+}
+
+// ------------------------------------------------------ RoPE + KV cache write
+struct PieceMeta {
+  const int32_t* seq;   // [P] sequence of each piece
+  const int32_t* row0;  // [P+1] first row of each piece (row0[P] = T)
+  const int32_t* pos0;  // [P] absolute position of each piece's first row
+};
+
+__global__ void rope_kv_write_kernel(const __nv_bfloat16* __restrict__ qkv, PieceMeta pm, int Hq, int Hkv, int hd,
+                                     const float* __restrict__ table, int64_t max_pos,
+                                     const int32_t* __restrict__ block_table, int64_t max_blk, int64_t n_blocks,
+                                     __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ k_cache,
+                                     __nv_bfloat16* __restrict__ v_cache, int* status) {
+  const int p = blockIdx.y;
+  const int i = blockIdx.x;
+  const int row0 = pm.row0[p];
+  if (i >= pm.row0[p + 1] - row0) return;
+  const int64_t row = row0 + i;
+  const int64_t pos = (int64_t)pm.pos0[p] + i;
+  const int seq = pm.seq[p];
+  const int half = hd / 2;
+  const int nqkv = (Hq + 2 * Hkv) * hd;
+  const __nv_bfloat16* src = qkv + row * nqkv;
+  if (pos < 0 || pos >= max_pos) {
+    report(status, DEV_BAD_INDEX);
+    return;
+  }
+  const bool tab_ok = pos / 64 < max_blk;
+  const int32_t blk = tab_ok ? block_table[(int64_t)seq * max_blk + pos / 64] : -1;
+  const bool blk_ok = blk >= 0 && blk < n_blocks;
+  if (!blk_ok && threadIdx.x == 0) report(status, DEV_BAD_INDEX);
+  const float* cs = table + pos * hd;
+  const int slot = (int)(pos % 64);
+  // q and k heads: rotate pairs (j, j + hd/2)
+  for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {
+    const int h = idx / half;
+    const int j = idx % half;
+    const float x1 = bf2f(src[h * hd + j]);
+    const float x2 = bf2f(src[h * hd + j + half]);
+    const float c = cs[j], s = cs[half + j];
+    const __nv_bfloat16 o1 = f2bf(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
+    const __nv_bfloat16 o2 = f2bf(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
+    if (h < Hq) {
+      __nv_bfloat16* dst = q_out + (row * Hq + h) * hd;
+      dst[j] = o1;
+      dst[j + half] = o2;
+    } else if (blk_ok) {
+      const int kh = h - Hq;
+      __nv_bfloat16* dst = k_cache + (((int64_t)blk * Hkv + kh) * 64 + slot) * hd;
+      dst[j] = o1;
+      dst[j + half] = o2;
+    }
+  }
+  if (blk_ok) {
+    for (int idx = threadIdx.x; idx < Hkv * hd; idx += blockDim.x) {
+      const int kh = idx / hd, j = idx % hd;
+      v_cache[(((int64_t)blk * Hkv + kh) * 64 + slot) * hd + j] = src[(Hq + Hkv) * hd + idx];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ attention
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16 bf16) * B(16x8 bf16) + D, fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+struct AttnArgs {
+  const __nv_bfloat16* q;  // [T, Hq, hd]
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;  // [n_blocks, Hkv, 64, hd]
+  const int32_t* block_table;
+  float* part_o;  // [T, Hq, nsplit, hd]
+  float* part_ml; // [T, Hq, nsplit, 2]
+  int* status;
+  PieceMeta pm;
+  int64_t max_blk, n_blocks;
+  int Hq, Hkv, group, nsplit, split;  // split = positions per split
+  float scale_log2;
+};
+
+constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
+constexpr int kKeys = 64;   // keys per tile = cache block
+
+template <int HD>
+__global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
+  constexpr int CH = HD / 8;  // 16-byte chunks per key row
+  constexpr int TILE_BYTES = kKeys * HD * 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  // [stage][K|V][64][HD] bf16, chunk-swizzled
+  const int p = blockIdx.y;
+  const int kvh = blockIdx.z % a.Hkv;
+  const int s = blockIdx.z / a.Hkv;
+  const int row0 = a.pm.row0[p];
+  const int n_tok = a.pm.row0[p + 1] - row0;
+  const int tok_per_tile = kRows / a.group;
+  const int tok0 = blockIdx.x * tok_per_tile;
+  if (tok0 >= n_tok) return;
+  const int pos_first = a.pm.pos0[p];
+  const int tok_last = min(n_tok, tok0 + tok_per_tile) - 1;
+  const int max_pos = pos_first + tok_last;  // last query position in this CTA
+  const int kv_begin = s * a.split;
+  if (kv_begin > max_pos) return;  // split entirely in the future of every row here
+  const int kv_end = min(kv_begin + a.split, max_pos + 1);  // exclusive
+  const int t_begin = kv_begin / kKeys;
+  const int n_tiles = (kv_end - t_begin * kKeys + kKeys - 1) / kKeys;
+  const int seq = a.pm.seq[p];
+  const int32_t* bt = a.block_table + (int64_t)seq * a.max_blk;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, tq = lane & 3;
+
+  // rows of this thread: r_lo = warp*16 + g, r_hi = r_lo + 8
+  int row_pos[2], row_tok[2], row_head[2];
+  bool row_valid[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = warp * 16 + g + h * 8;
+    const int ti = tok0 + r / a.group;
+    row_valid[h] = ti < n_tok && (r / a.group) < tok_per_tile;
+    row_tok[h] = row0 + ti;
+    row_pos[h] = pos_first + ti;
+    row_head[h] = kvh * a.group + (r % a.group);
+  }
+  // Q fragments for this warp's 16 rows: HD/16 k-steps x 4 registers
+  uint32_t qf[HD / 16][4];
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat16* qr = a.q + ((int64_t)row_tok[h] * a.Hq + row_head[h]) * HD + kk * 16 + tq * 2;
+      qf[kk][h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+      qf[kk][2 + h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+    }
+  }
+
+  auto load_tile = [&](int t, int stage) {
+    const int key0 = (t_begin + t) * kKeys;
+    const bool tab_ok = key0 / kKeys < a.max_blk;
+    const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
+    const bool blk_ok = blk >= 0 && blk < a.n_blocks;
+    if (!blk_ok && tid == 0) report(a.status, DEV_BAD_INDEX);
+    const int64_t base = ((int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh) * kKeys * HD;
+    uint8_t* sk = smem + stage * 2 * TILE_BYTES;
+    uint8_t* sv = sk + TILE_BYTES;
+    for (int c = tid; c < kKeys * CH; c += 128) {
+      const int key = c / CH, ch = c % CH;
+      const bool valid = blk_ok && (key0 + key) <= max_pos;
+      const int off = (key * CH + (ch ^ (key & 7))) * 16;
+      const int64_t src = base + (int64_t)key * HD + ch * 8;
+      cp_async16(sk + off, a.k_cache + (valid ? src : 0), valid);
+      cp_async16(sv + off, a.v_cache + (valid ? src : 0), valid);
+    }
+    cp_async_commit();
+  };
+
+  float m[2] = {-INFINITY, -INFINITY};
+  float l[2] = {0.f, 0.f};
+  float acc[HD / 8][4];
+#pragma unroll
+  for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+  load_tile(0, 0);
+  for (int t = 0; t < n_tiles; ++t) {
+    const int stage = t & 1;
+    if (t + 1 < n_tiles) {
+      load_tile(t + 1, stage ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t sk = smem_u32(smem + stage * 2 * TILE_BYTES);
+    const uint32_t sv = sk + TILE_BYTES;
+    const int key0 = (t_begin + t) * kKeys;
+
+    // S = Q K^T for 16 rows x 64 keys
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; kk += 2) {
+        const int key = j * 8 + (lane & 7);
+        const int ch = kk * 2 + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+        mma_bf16_16816(sc[j], qf[kk], b0, b1);
+        mma_bf16_16816(sc[j], qf[kk + 1], b2, b3);
+      }
+    }
+    // online softmax (fp32), masking by select
+    float pr[8][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kp = key0 + j * 8 + tq * 2 + e;
+          const bool ok = row_valid[h] && kp <= row_pos[h];
+          const float v = ok ? __fmul_rn(sc[j][h * 2 + e], a.scale_log2) : -INFINITY;
+          sc[j][h * 2 + e] = v;
+          tmax = fmaxf(tmax, v);
+        }
+      }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m[h], tmax);
+      const float alpha = (m_new == m[h]) ? 1.0f : exp2f(__fsub_rn(m[h], m_new));
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float v = sc[j][h * 2 + e];
+          const float pv = (v == -INFINITY) ? 0.f : exp2f(__fsub_rn(v, m_new));
+          pr[j][h * 2 + e] = pv;
+          rs = __fadd_rn(rs, pv);
+        }
+      }
+      rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 1));
+      rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 2));
+      l[h] = __fadd_rn(__fmul_rn(l[h], alpha), rs);
+      m[h] = m_new;
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        acc[j][h * 2] = __fmul_rn(acc[j][h * 2], alpha);
+        acc[j][h * 2 + 1] = __fmul_rn(acc[j][h * 2 + 1], alpha);
+      }
+    }
+    // O += P V  (P rounded to bf16)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
+      pa[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
+      pa[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+      pa[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+#pragma unroll
+      for (int j = 0; j < HD / 8; j += 2) {
+        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int ch = j + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+        mma_bf16_16816(acc[j], pa, b0, b1);
+        mma_bf16_16816(acc[j + 1], pa, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // write partials for rows that own this split
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (!row_valid[h] || row_pos[h] < kv_begin) continue;
+    const int64_t pidx = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
+    float* po = a.part_o + pidx * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      *reinterpret_cast<float2*>(po + j * 8 + tq * 2) = make_float2(acc[j][h * 2], acc[j][h * 2 + 1]);
+    }
+    if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(m[h], l[h]);
+  }
+}
+
+// Merge of the split partials in ascending split order, one token per CTA.
+__global__ void attention_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                                       PieceMeta pm, int Hq, int hd, int nsplit, int split,
+                                       __nv_bfloat16* __restrict__ out, int* status) {
+  const int p = blockIdx.y;
+  const int i = blockIdx.x;
+  const int row0 = pm.row0[p];
+  if (i >= pm.row0[p + 1] - row0) return;
+  const int64_t row = row0 + i;
+  const int pos = pm.pos0[p] + i;
+  int ns = pos / split + 1;
+  if (ns > nsplit) {  // a position beyond the call's max_ctx bound
+    if (threadIdx.x == 0) report(status, DEV_BAD_INDEX);
+    ns = nsplit;
+  }
+  for (int idx = threadIdx.x; idx < Hq * hd; idx += blockDim.x) {
+    const int h = idx / hd, d = idx % hd;
+    const int64_t base = (row * Hq + h) * nsplit;
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
+    float L = 0.f, O = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float w = exp2f(__fsub_rn(part_ml[(base + s) * 2], M));
+      L = __fadd_rn(L, __fmul_rn(part_ml[(base + s) * 2 + 1], w));
+      O = __fadd_rn(O, __fmul_rn(part_o[(base + s) * hd + d], w));
+    }
+    out[row * (int64_t)Hq * hd + idx] = f2bf(__fdiv_rn(O, L));
+  }
+}
+
+static int attn_smem_bytes(int hd) { return 2 * 2 * kKeys * hd * 2; }
+
+// Positions per split: the fixed kv_split, or (BI_FAST) a size chosen from the
+// batch so that the decode grid fills the GPU (flash-decoding heuristic).
+static int choose_split(int mode, int kv_split, int64_t P, int64_t max_q_len, int Hkv, int group, int64_t max_ctx) {
+  if (mode != BI_FAST || max_q_len * group > kRows) return kv_split;
+  const int64_t qtiles = 1;
+  const int64_t ctas = P * Hkv * qtiles;
+  const int64_t want = std::max<int64_t>(1, cdiv(2 * (int64_t)num_sms(), std::max<int64_t>(ctas, 1)));
+  int64_t sz = cdiv(std::max<int64_t>(max_ctx, 1), want);
+  sz = std::max<int64_t>(64, cdiv(sz, 64) * 64);
+  return (int)std::min<int64_t>(sz, kv_split);
+}
+
+static int64_t n_splits(int64_t max_ctx, int split) { return std::max<int64_t>(1, cdiv(max_ctx, split)); }
+
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_rope_table(float* rope_table, int64_t max_pos, int hd, double theta, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(rope_table, "null table");
+  BI_REQUIRE(max_pos > 0 && hd > 0 && hd % 2 == 0, "bad shape");
+  const int64_t total = max_pos * (hd / 2);
+  const int blocks = (int)std::min<int64_t>(cdiv(total, 256), 4096);
+  rope_table_kernel<<<blocks, 256, 0, as_stream(stream)>>>(rope_table, max_pos, hd, theta);
+  return check_launch("bi_rope_table");
+}
+
+bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                           const float* rope_table, int64_t max_pos, const int32_t* block_table,
+                           int64_t max_blocks_per_seq, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache,
+                           void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
+  if (T == 0 || P == 0) return BI_OK;
+  BI_REQUIRE(qkv && piece_seq && piece_row0 && piece_pos0 && rope_table && block_table && q_out && k_cache && v_cache,
+             "null pointer");
+  BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0 && hd > 0 && hd % 2 == 0, "bad heads");
+  BI_REQUIRE(max_q_len > 0 && max_q_len <= 65535 && P <= 65535, "bad max_q_len / P");
+  BI_REQUIRE(max_blocks_per_seq > 0 && n_blocks > 0, "bad cache shape");
+  PieceMeta pm{piece_seq, piece_row0, piece_pos0};
+  dim3 grid((unsigned)max_q_len, (unsigned)P);
+  rope_kv_write_kernel<<<grid, 128, 0, as_stream(stream)>>>(
+      static_cast<const __nv_bfloat16*>(qkv), pm, Hq, Hkv, hd, rope_table, max_pos, block_table, max_blocks_per_seq,
+      n_blocks, static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(k_cache),
+      static_cast<__nv_bfloat16*>(v_cache), device_status_ptr());
+  return check_launch("bi_rope_kv_write");
+}
+
+size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ctx, int kv_split) {
+  if (max_T <= 0 || Hq <= 0 || hd <= 0 || max_ctx <= 0 || kv_split < 64) return 0;
+  // BI_FAST may shrink the split down to 64 positions for decode-sized calls;
+  // size for the invariant split and for 64 and take the larger.
+  const int64_t ns = std::max(bi::n_splits(max_ctx, kv_split), std::min<int64_t>(bi::n_splits(max_ctx, 64),
+                                                                                   bi::n_splits(max_ctx, kv_split) * 8));
+  const size_t per = (size_t)max_T * Hq * ns;
+  return per * hd * sizeof(float) + per * 2 * sizeof(float) + 256;
+}
+
+bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                       const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale, void* workspace,
+                       size_t ws_bytes, void* out, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
+  if (T == 0 || P == 0) return BI_OK;
+  BI_REQUIRE(q && piece_seq && piece_row0 && piece_pos0 && k_cache && v_cache && block_table && out && workspace,
+             "null pointer");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
+  BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  const int group = Hq / Hkv;
+  BI_REQUIRE_SHAPE(kRows % group == 0, "64 must be a multiple of Hq/Hkv");
+  BI_REQUIRE(kv_split >= 64 && kv_split % 64 == 0, "kv_split must be a positive multiple of 64");
+  BI_REQUIRE(max_ctx > 0 && max_q_len > 0, "bad max_ctx / max_q_len");
+  BI_REQUIRE(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(workspace) && aligned16(out),
+             "pointers must be 16-byte aligned");
+  const int split = choose_split(mode, kv_split, P, max_q_len, Hkv, group, max_ctx);
+  const int64_t ns = n_splits(max_ctx, split);
+  const size_t per = (size_t)T * Hq * ns;
+  const size_t need = per * hd * sizeof(float) + per * 2 * sizeof(float);
+  BI_REQUIRE(ws_bytes >= need, "attention workspace too small (bi_attention_workspace_size)");
+  float* part_o = static_cast<float*>(workspace);
+  float* part_ml = part_o + per * hd;
+  const int64_t qtiles = cdiv(max_q_len * group, kRows);
+  BI_REQUIRE(qtiles <= 0x7fffffff && P <= 65535 && Hkv * ns <= 65535, "grid too large");
+  AttnArgs args;
+  args.q = static_cast<const __nv_bfloat16*>(q);
+  args.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  args.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  args.block_table = block_table;
+  args.part_o = part_o;
+  args.part_ml = part_ml;
+  args.status = device_status_ptr();
+  args.pm = PieceMeta{piece_seq, piece_row0, piece_pos0};
+  args.max_blk = max_blocks_per_seq;
+  args.n_blocks = 1ll << 40;  // the caller's cache size is checked by the writer
+  args.Hq = Hq;
+  args.Hkv = Hkv;
+  args.group = group;
+  args.nsplit = (int)ns;
+  args.split = split;
+  args.scale_log2 = scale * 1.4426950408889634f;
+  dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
+  const int smem = attn_smem_bytes(hd);
+  cudaStream_t st = as_stream(stream);
+  if (hd == 64) {
+    attention_kernel<64><<<grid, 128, smem, st>>>(args);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      attr = true;
+    }
+    attention_kernel<128><<<grid, 128, smem, st>>>(args);
+  }
+  BI_TRY(check_launch("attention_kernel"));
+  dim3 mgrid((unsigned)max_q_len, (unsigned)P);
+  attention_merge_kernel<<<mgrid, 256, 0, st>>>(part_o, part_ml, args.pm, Hq, hd, (int)ns, split,
+                                               static_cast<__nv_bfloat16*>(out), args.status);
+  return check_launch("attention_merge_kernel");
+}
+
+}  // extern "C"

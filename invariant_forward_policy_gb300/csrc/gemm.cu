@@ -1,0 +1,482 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// "vLLM Achieves Bitwise-Consistent RL Training ..." §4.1 "Dense GEMM: keep
+// FP8, one accumulation order for every M": the inference engine's M-dependent
+// kernel switch is removed so a request's row never changes with the batch.
+// Here the invariant path runs ONE kernel for every M: a 128 x BN x 64 CTA
+// tile (BN fixed by the weight's (N, K) and the epilogue), K consumed in
+// ascending 16-wide tcgen05.mma steps into a single fp32 TMEM accumulator, no
+// split-K.  A row's bits therefore depend only on that row of A and on W.
+//
+// §4.4 "Expert GEMM: two layouts, same row result": the grouped variant maps
+// each 128-row tile to one expert; row results do not depend on the layout.
+//
+// CTA = 4 warps.  Warp 0 lane 0 issues TMA loads into a STAGES-deep ring
+// (full/empty mbarriers), warp 1 lane 0 issues tcgen05.mma and commits each
+// stage back to its empty barrier, then all four warps drain TMEM (warp w owns
+// TMEM lanes 32w..32w+31 = tile rows) through the epilogue.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace bi {
+
+enum EpiKind : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU = 2, EPI_PARTIAL = 3, EPI_PARTIAL_SWIGLU = 4 };
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kATileBytes = kBM * kBK * 2;
+
+template <int BN>
+struct GemmSmem {
+  static constexpr int kBTileBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kBytes = 1024 + kStages * kStageBytes + 256;
+};
+
+struct GemmArgs {
+  void* C;
+  float* partial;           // split-K partials [splits, M, ldp]
+  const int32_t* tile_expert;
+  int* status;
+  int M, K, ldc;            // ldc = output columns
+  int n_out;                // valid output columns (N, or F for SwiGLU)
+  int w_rows_per_expert;    // rows of W per expert (grouped); 0 for dense
+  int up_offset;            // SwiGLU: row offset of the up half inside one expert's W
+  int k_blocks_per_split;
+  int ldp;                  // partial row length
+};
+
+__device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                         const __grid_constant__ CUtensorMap tmB,
+                                                         const __grid_constant__ CUtensorMap tmB2,
+                                                         const GemmArgs args) {
+  using S = GemmSmem<BN>;
+  constexpr bool kSwiglu = (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * S::kBTileBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accb = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* consumed = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tile = blockIdx.x, m_tile = blockIdx.y, split = blockIdx.z;
+  int expert = 0;
+  if (args.tile_expert) {
+    expert = args.tile_expert[m_tile];
+    if (expert < 0) return;  // whole CTA leaves before touching barriers or TMEM
+  }
+  const int m0 = m_tile * kBM;
+  const int nk = args.k_blocks_per_split;
+  const int kb0 = split * nk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accb, 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, BN);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (kSwiglu) prefetch_tmap(&tmB2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_d = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    const int wbase = expert * args.w_rows_per_expert;
+    int issued = 0;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1;
+      if (!mbar_wait(&empty[s], ph ^ 1) || *abort_flag) {
+        report(args.status, DEV_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+      const int kc = (kb0 + kb) * kBK;
+      tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], kc, m0);
+      if (kSwiglu) {
+        const int j0 = n_tile * (BN / 2);
+        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
+        tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc,
+                    wbase + args.up_offset + j0);
+      } else {
+        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
+      }
+      ++issued;
+    }
+    if (*abort_flag) {
+      // let every copy this CTA started land before the CTA can exit
+      for (int kb = *consumed; kb < issued; ++kb) mbar_wait(&full[kb % kStages], (kb / kStages) & 1);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1;
+      if (!mbar_wait(&full[s], ph) || *abort_flag) {
+        report(args.status, DEV_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      *consumed = kb + 1;
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
+      const uint32_t b_addr = smem_u32(sB + s * S::kBTileBytes);
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        tc_mma_bf16(tmem_d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
+                    (kb | k) != 0 ? 1u : 0u);
+      }
+      tc_commit(&empty[s]);
+    }
+    tc_commit(accb);  // fires once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> registers -> global
+  const bool acc_ok = mbar_wait(accb, 0);
+  tc_fence_after();
+  if (!acc_ok) report(args.status, DEV_TIMEOUT);
+  const bool do_store = acc_ok && !*abort_flag;
+  const int row = m0 + warp * 32 + lane;
+  const bool row_ok = row < args.M;
+  const uint32_t t_row = tmem_d + ((uint32_t)(warp * 32) << 16);
+
+  if (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU) {
+    const int j0 = n_tile * (BN / 2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld_32x32b_x32(t_row + c, g);
+      tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
+      tmem_ld_wait();
+      if (!(do_store && row_ok)) continue;
+      if (EPI == EPI_SWIGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.C) + (size_t)row * args.ldc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = j0 + c + q * 8;
+          if (col >= args.n_out) break;
+          uint4 v;
+          uint32_t* pv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float a2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int i = q * 8 + e * 2 + h;
+              const float gb = bf2f(f2bf(__uint_as_float(g[i])));
+              const float ub = bf2f(f2bf(__uint_as_float(u[i])));
+              a2[h] = __fmul_rn(silu_f(gb), ub);
+            }
+            pv[e] = pack_bf16x2(a2[0], a2[1]);
+          }
+          *reinterpret_cast<uint4*>(out + col) = v;
+        }
+      } else {
+        float* pg = args.partial + ((size_t)split * args.M + row) * args.ldp;
+        float* pu = pg + args.n_out;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int col = j0 + c + q * 4;
+          if (col >= args.n_out) break;
+          *reinterpret_cast<float4*>(pg + col) =
+              make_float4(__uint_as_float(g[q * 4]), __uint_as_float(g[q * 4 + 1]), __uint_as_float(g[q * 4 + 2]),
+                          __uint_as_float(g[q * 4 + 3]));
+          *reinterpret_cast<float4*>(pu + col) =
+              make_float4(__uint_as_float(u[q * 4]), __uint_as_float(u[q * 4 + 1]), __uint_as_float(u[q * 4 + 2]),
+                          __uint_as_float(u[q * 4 + 3]));
+        }
+      }
+    }
+  } else {
+    const int n0 = n_tile * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_ld_wait();
+      if (!(do_store && row_ok)) continue;
+      if (EPI == EPI_BF16) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.C) + (size_t)row * args.ldc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = n0 + c + q * 8;
+          if (col >= args.n_out) break;
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]), __uint_as_float(r[q * 8 + 1]));
+          v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]), __uint_as_float(r[q * 8 + 3]));
+          v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]), __uint_as_float(r[q * 8 + 5]));
+          v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]), __uint_as_float(r[q * 8 + 7]));
+          *reinterpret_cast<uint4*>(out + col) = v;
+        }
+      } else {
+        float* out = (EPI == EPI_F32) ? static_cast<float*>(args.C) + (size_t)row * args.ldc
+                                      : args.partial + ((size_t)split * args.M + row) * args.ldp;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int col = n0 + c + q * 4;
+          if (col >= args.n_out) break;
+          *reinterpret_cast<float4*>(out + col) =
+              make_float4(__uint_as_float(r[q * 4]), __uint_as_float(r[q * 4 + 1]), __uint_as_float(r[q * 4 + 2]),
+                          __uint_as_float(r[q * 4 + 3]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_d, BN);
+  }
+}
+
+// Split-K reduction of the non-invariant path: sums partials in split order.
+template <int EPI>
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int n_out, int ldp,
+                                     void* C) {
+  const int64_t total = (int64_t)M * n_out;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / n_out;
+    const int n = (int)(i % n_out);
+    float a = 0.f, b = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float* p = part + ((int64_t)s * M + m) * ldp;
+      a += p[n];
+      if (EPI == EPI_SWIGLU) b += p[n_out + n];
+    }
+    if (EPI == EPI_BF16) {
+      static_cast<__nv_bfloat16*>(C)[i] = f2bf(a);
+    } else if (EPI == EPI_F32) {
+      static_cast<float*>(C)[i] = a;
+    } else {
+      const float gb = bf2f(f2bf(a)), ub = bf2f(f2bf(b));
+      static_cast<__nv_bfloat16*>(C)[i] = f2bf(__fmul_rn(silu_f(gb), ub));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host side
+template <int BN, int EPI>
+static bi_status launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmArgs& args,
+                           dim3 grid, cudaStream_t st) {
+  constexpr int smem = GemmSmem<BN>::kBytes;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess) return fail(BI_ERR_CUDA, std::string("gemm smem attribute: ") + cudaGetErrorString(attr_err));
+  gemm_tc_kernel<BN, EPI><<<grid, 128, smem, st>>>(a, b, b2, args);
+  return check_launch("gemm_tc_kernel");
+}
+
+template <int EPI>
+static bi_status dispatch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                             const GemmArgs& args, dim3 grid, cudaStream_t st) {
+  switch (bn) {
+    case 64: return launch_tc<64, EPI>(a, b, b2, args, grid, st);
+    case 128: return launch_tc<128, EPI>(a, b, b2, args, grid, st);
+    case 256: return launch_tc<256, EPI>(a, b, b2, args, grid, st);
+  }
+  return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad tile width");
+}
+
+static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
+                              const GemmArgs& args, dim3 grid, cudaStream_t st) {
+  switch (epi) {
+    case EPI_BF16: return dispatch_bn<EPI_BF16>(bn, a, b, b2, args, grid, st);
+    case EPI_F32: return dispatch_bn<EPI_F32>(bn, a, b, b2, args, grid, st);
+    case EPI_SWIGLU: return dispatch_bn<EPI_SWIGLU>(bn, a, b, b2, args, grid, st);
+    case EPI_PARTIAL: return dispatch_bn<EPI_PARTIAL>(bn, a, b, b2, args, grid, st);
+    case EPI_PARTIAL_SWIGLU: return dispatch_bn<EPI_PARTIAL_SWIGLU>(bn, a, b, b2, args, grid, st);
+  }
+  return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad epilogue");
+}
+
+// Accumulator tile width for a weight: a function of (N, K, epilogue) only.
+static int tile_n_for(int64_t n_rows_w, int64_t /*K*/, bool swiglu) {
+  if (swiglu) return n_rows_w >= 4096 ? 128 : 64;
+  if (n_rows_w >= 32768) return 256;
+  if (n_rows_w >= 4096) return 128;
+  return 64;
+}
+
+// Non-invariant choices (BI_FAST): tile width and split count chosen from M.
+static void fast_plan(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, int* bn, int* splits) {
+  *bn = tile_n_for(n_rows_w, K, swiglu);
+  *splits = 1;
+  if (M > 128) return;
+  *bn = 64;
+  const int64_t n_cols = swiglu ? n_rows_w / 2 : n_rows_w;
+  const int64_t tiles = cdiv(n_cols, swiglu ? 32 : 64);
+  const int64_t kblocks = K / kBK;
+  int64_t s = cdiv((int64_t)num_sms(), tiles);
+  s = std::min<int64_t>(s, kblocks / 2 > 0 ? kblocks / 2 : 1);
+  while (s > 1 && kblocks % s) --s;
+  *splits = (int)std::max<int64_t>(s, 1);
+}
+
+struct GemmCall {
+  const void* A;
+  int64_t M, K;
+  const void* W;
+  int64_t n_rows_w;        // rows of W per expert (2F for SwiGLU)
+  int64_t E;               // number of experts (1 = dense)
+  const int32_t* tile_expert;
+  void* C;
+  int c_dtype, epilogue, mode;
+  void* ws;
+  size_t ws_bytes;
+};
+
+static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
+  return splits > 1 ? (size_t)splits * M * n_rows_w * sizeof(float) : 0;
+}
+
+static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
+  const bool swiglu = g.epilogue == BI_EPI_SWIGLU;
+  const int64_t n_out = swiglu ? g.n_rows_w / 2 : g.n_rows_w;
+  int bn = tile_n_for(g.n_rows_w, g.K, swiglu), splits = 1;
+  if (g.mode == BI_FAST && g.E == 1) fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
+  const int64_t kblocks = g.K / kBK;
+
+  CUtensorMap ta, tb, tb2;
+  if (!encode_tmap_2d_bf16(&ta, g.A, g.K, g.M, g.K * 2, kBK, kBM, true))
+    return fail(BI_ERR_CUDA, "gemm: TMA descriptor for A failed");
+  const uint32_t box_b = swiglu ? bn / 2 : bn;
+  if (g.E == 1 && swiglu) {
+    const char* w = static_cast<const char*>(g.W);
+    if (!encode_tmap_2d_bf16(&tb, w, g.K, n_out, g.K * 2, kBK, box_b, true) ||
+        !encode_tmap_2d_bf16(&tb2, w + n_out * g.K * 2, g.K, n_out, g.K * 2, kBK, box_b, true))
+      return fail(BI_ERR_CUDA, "gemm: TMA descriptor for W failed");
+  } else {
+    if (!encode_tmap_2d_bf16(&tb, g.W, g.K, g.n_rows_w * g.E, g.K * 2, kBK, box_b, true))
+      return fail(BI_ERR_CUDA, "gemm: TMA descriptor for W failed");
+    tb2 = tb;
+  }
+
+  GemmArgs args;
+  args.C = g.C;
+  args.partial = nullptr;
+  args.tile_expert = g.tile_expert;
+  args.status = device_status_ptr();
+  args.M = (int)g.M;
+  args.K = (int)g.K;
+  args.ldc = (int)n_out;
+  args.n_out = (int)n_out;
+  args.w_rows_per_expert = g.E > 1 || g.tile_expert ? (int)g.n_rows_w : 0;
+  args.up_offset = (g.E == 1 && !g.tile_expert) ? 0 : (int)n_out;
+  args.k_blocks_per_split = (int)(kblocks / splits);
+  args.ldp = (int)g.n_rows_w;
+
+  const int64_t n_tiles = swiglu ? cdiv(n_out, bn / 2) : cdiv(n_out, bn);
+  dim3 grid((unsigned)n_tiles, (unsigned)cdiv(g.M, kBM), (unsigned)splits);
+  int epi;
+  if (splits > 1) {
+    if (g.ws_bytes < partial_bytes(g.M, g.n_rows_w, splits) || !g.ws)
+      return fail(BI_ERR_INVALID_ARG, "bi_gemm: BI_FAST split-K needs workspace (bi_gemm_workspace_size)");
+    args.partial = static_cast<float*>(g.ws);
+    epi = swiglu ? EPI_PARTIAL_SWIGLU : EPI_PARTIAL;
+  } else {
+    epi = swiglu ? EPI_SWIGLU : (g.c_dtype == BI_DTYPE_FP32 ? EPI_F32 : EPI_BF16);
+  }
+  BI_TRY(dispatch_epi(epi, bn, ta, tb, tb2, args, grid, st));
+  if (splits > 1) {
+    const int64_t total = g.M * n_out;
+    const int blocks = (int)std::min<int64_t>(cdiv(total, 256), 4 * (int64_t)num_sms());
+    if (swiglu)
+      splitk_reduce_kernel<EPI_SWIGLU><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
+                                                                (int)g.n_rows_w, g.C);
+    else if (g.c_dtype == BI_DTYPE_FP32)
+      splitk_reduce_kernel<EPI_F32><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
+                                                             (int)g.n_rows_w, g.C);
+    else
+      splitk_reduce_kernel<EPI_BF16><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
+                                                              (int)g.n_rows_w, g.C);
+    BI_TRY(check_launch("splitk_reduce_kernel"));
+  }
+  return BI_OK;
+}
+
+}  // namespace bi
+
+extern "C" {
+
+int bi_gemm_tile_n(int64_t N, int64_t K, int epilogue) { return bi::tile_n_for(N, K, epilogue == BI_EPI_SWIGLU); }
+
+size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int epilogue, int mode) {
+  if (mode != BI_FAST || M <= 0 || K % bi::kBK) return 0;
+  int bn, splits;
+  bi::fast_plan(M, N, K, epilogue == BI_EPI_SWIGLU, &bn, &splits);
+  return bi::partial_bytes(M, N, splits);
+}
+
+bi_status bi_gemm(const void* A, int64_t M, int64_t K, const void* W, int64_t N, void* C, int c_dtype, int epilogue,
+                  int mode, void* workspace, size_t ws_bytes, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(M >= 0 && N > 0 && K > 0, "bad shape");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(A && W && C, "null pointer");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  BI_REQUIRE(epilogue == BI_EPI_NONE || epilogue == BI_EPI_SWIGLU, "bad epilogue");
+  BI_REQUIRE(c_dtype == BI_DTYPE_BF16 || c_dtype == BI_DTYPE_FP32, "bad c_dtype");
+  BI_REQUIRE(epilogue != BI_EPI_SWIGLU || c_dtype == BI_DTYPE_BF16, "SwiGLU output is bf16");
+  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(C), "pointers must be 16-byte aligned");
+  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
+  BI_REQUIRE_SHAPE(N % 8 == 0, "N must be a multiple of 8");
+  BI_REQUIRE_SHAPE(epilogue != BI_EPI_SWIGLU || (N % 16 == 0), "SwiGLU needs N = 2F with F % 8 == 0");
+  BI_REQUIRE_SHAPE(M < (1ll << 31) && N < (1ll << 31) && K < (1ll << 31), "shape too large");
+  GemmCall g{A, M, K, W, N, 1, nullptr, C, c_dtype, epilogue, mode, workspace, ws_bytes};
+  return run_gemm(g, as_stream(stream));
+}
+
+bi_status bi_grouped_gemm(const void* A, int64_t M_rows, int64_t K, const void* W, int64_t E, int64_t N,
+                          const int32_t* tile_expert, void* C, int c_dtype, int epilogue, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(M_rows >= 0 && N > 0 && K > 0 && E > 0, "bad shape");
+  if (M_rows == 0) return BI_OK;
+  BI_REQUIRE(A && W && C && tile_expert, "null pointer");
+  BI_REQUIRE(M_rows % 128 == 0, "M_rows must be a multiple of 128");
+  BI_REQUIRE(epilogue == BI_EPI_NONE || epilogue == BI_EPI_SWIGLU, "bad epilogue");
+  BI_REQUIRE(c_dtype == BI_DTYPE_BF16 || c_dtype == BI_DTYPE_FP32, "bad c_dtype");
+  BI_REQUIRE(epilogue != BI_EPI_SWIGLU || c_dtype == BI_DTYPE_BF16, "SwiGLU output is bf16");
+  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(C), "pointers must be 16-byte aligned");
+  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
+  const bool swiglu = epilogue == BI_EPI_SWIGLU;
+  const int bn = tile_n_for(N, K, swiglu);
+  BI_REQUIRE_SHAPE(swiglu ? (N / 2) % (bn / 2) == 0 : N % bn == 0,
+                   "grouped GEMM needs the per-expert N to be a multiple of the tile width");
+  BI_REQUIRE_SHAPE(M_rows < (1ll << 31) && N * E < (1ll << 31), "shape too large");
+  GemmCall g{A, M_rows, K, W, N, E, tile_expert, C, c_dtype, epilogue, BI_INVARIANT, nullptr, 0};
+  return run_gemm(g, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,388 @@
+// MoE FFN: top-k router, expert layouts, gather, grouped expert GEMMs, slot-order combine.
+//
+// "vLLM Achieves Bitwise-Consistent RL Training ..." §4.4 ("Expert GEMM: two
+// layouts, same row result"): the rollout side feeds the expert GEMM a masked
+// layout (fixed capacity per expert) and the training side a contiguous layout
+// packed by expert; a row's result must not depend on which.  §4.5: expert
+// outputs are "accumulated in FP32 in top-k slot order" on the token's owner.
+// §2: routing is a discrete choice whose tie-break must be fixed.
+//
+// Layout construction is a stable counting sort: the rank of (token, slot)
+// inside its expert is its order in the (token, slot) sequence, computed with
+// a fixed per-thread chunking and a block scan, so the layout is a pure
+// function of the routing.  Row results do not depend on the layout anyway
+// because the grouped GEMM is row-invariant.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace bi {
+
+// ------------------------------------------------------------------ router
+__global__ void route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids,
+                                  float* __restrict__ weights) {
+  const int64_t t = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* x = logits + t * E;
+  float v0 = lane < E ? x[lane] : -INFINITY;
+  float v1 = lane + 32 < E ? x[lane + 32] : -INFINITY;
+  bool taken0 = lane >= E, taken1 = lane + 32 >= E;
+  float sel_v[64];
+  int sel_i[64];
+  for (int s = 0; s < k; ++s) {
+    // lane candidate: larger logit, ties to the lower expert id
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    if (!taken0) { bv = v0; bi = lane; }
+    if (!taken1 && (v1 > bv || bi == 0x7fffffff)) { bv = v1; bi = lane + 32; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    sel_v[s] = bv;
+    sel_i[s] = bi;
+    if (bi == lane) taken0 = true;
+    if (bi == lane + 32) taken1 = true;
+  }
+  if (lane == 0) {
+    float e[64];
+    float den = 0.f;
+    for (int s = 0; s < k; ++s) {
+      e[s] = expf(__fsub_rn(sel_v[s], sel_v[0]));
+      den = __fadd_rn(den, e[s]);
+    }
+    for (int s = 0; s < k; ++s) {
+      ids[t * k + s] = sel_i[s];
+      weights[t * k + s] = __fdiv_rn(e[s], den);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ layouts
+// rank[pair] = number of earlier pairs (in (token, slot) order) routed to the
+// same expert; counts[e] = pairs of expert e.  One CTA per expert.
+constexpr int kPermThreads = 1024;
+__global__ void __launch_bounds__(kPermThreads) expert_rank_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
+                                                                   int32_t* __restrict__ rank,
+                                                                   int32_t* __restrict__ counts, int* status) {
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t per = (n + kPermThreads - 1) / kPermThreads;
+  const int64_t b = tid * per, en = min(n, b + per);
+  int c = 0;
+  for (int64_t i = b; i < en; ++i) {
+    const int32_t x = ids[i];
+    if (x == e) ++c;
+    if (e == 0 && (x < 0 || x >= E)) report(status, DEV_BAD_INDEX);
+  }
+  // exclusive block scan of c in thread order
+  __shared__ int warp_tot[32];
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if ((tid & 31) >= o) incl += y;
+  }
+  if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
+  __syncthreads();
+  if (tid < 32) {
+    int w = warp_tot[tid];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (tid >= o) wi += y;
+    }
+    warp_tot[tid] = wi - w;  // exclusive prefix over warps
+    if (tid == 31) counts[e] = wi;
+  }
+  __syncthreads();
+  int r = warp_tot[tid >> 5] + incl - c;
+  for (int64_t i = b; i < en; ++i)
+    if (ids[i] == e) rank[i] = r++;
+}
+
+// Contiguous layout: expert offsets padded to 128 rows, and the tile owner map.
+__global__ void expert_offsets_kernel(const int32_t* __restrict__ counts, int E, int64_t max_tiles,
+                                      int32_t* __restrict__ offsets, int32_t* __restrict__ tile_expert, int* status) {
+  __shared__ int32_t off[1025];
+  if (threadIdx.x == 0) {
+    int32_t o = 0;
+    for (int e = 0; e < E; ++e) {
+      off[e] = o;
+      o += (counts[e] + 127) / 128 * 128;
+    }
+    off[E] = o;
+    if ((int64_t)o > max_tiles * 128) report(status, DEV_BAD_INDEX);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
+  for (int64_t t = threadIdx.x; t < max_tiles; t += blockDim.x) {
+    const int64_t r = t * 128;
+    int owner = -1;
+    if (r < off[E]) {
+      int lo = 0, hi = E - 1;  // last e with off[e] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (off[mid] <= r) lo = mid; else hi = mid - 1;
+      }
+      owner = lo;
+    }
+    tile_expert[t] = owner;
+  }
+}
+
+__global__ void row_of_slot_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, int64_t n,
+                                   const int32_t* __restrict__ offsets, int64_t capacity, int64_t max_rows,
+                                   int32_t* __restrict__ row_of_slot, int* status) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int32_t e = ids[i];
+  int64_t row;
+  if (capacity > 0) {  // masked layout
+    row = (rank[i] < capacity) ? e * capacity + rank[i] : -1;
+  } else {
+    row = offsets[e] + rank[i];
+  }
+  if (row < 0 || row >= max_rows) {
+    report(status, DEV_BAD_INDEX);
+    row = -1;
+  }
+  row_of_slot[i] = (int32_t)row;
+}
+
+__global__ void masked_tiles_kernel(int32_t* tile_expert, int64_t n_tiles, int64_t tiles_per_expert) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t < n_tiles) tile_expert[t] = (int32_t)(t / tiles_per_expert);
+}
+
+__global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of_slot, int k,
+                                  int64_t d, __nv_bfloat16* __restrict__ xp) {
+  const int64_t pair = blockIdx.x;
+  const int32_t row = row_of_slot[pair];
+  if (row < 0) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (pair / k) * d);
+  uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)row * d);
+  for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) dst[v] = src[v];
+}
+
+// out[t] = bf16( sum_s w[t,s] * y[row(t,s)] ), slots in order, fp32.
+__global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of_slot,
+                                   const float* __restrict__ w, int k, int64_t d, __nv_bfloat16* __restrict__ out) {
+  const int64_t t = blockIdx.x;
+  for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int32_t row = row_of_slot[t * k + s];
+      if (row < 0) continue;
+      const float ws = w[t * k + s];
+      const uint4 yv = reinterpret_cast<const uint4*>(y + (int64_t)row * d)[v];
+      const uint32_t* py = reinterpret_cast<const uint32_t*>(&yv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(ws, bf16lo(py[j])));
+        acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(ws, bf16hi(py[j])));
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(out + t * d)[v] = o;
+  }
+}
+
+// BI_FAST combine: fp32 atomics in arrival order (not deterministic).
+__global__ void moe_combine_atomic_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of_slot,
+                                          const float* __restrict__ w, int k, int64_t d, float* __restrict__ acc) {
+  const int64_t pair = blockIdx.x;
+  const int32_t row = row_of_slot[pair];
+  if (row < 0) return;
+  const float ws = w[pair];
+  float* dst = acc + (pair / k) * d;
+  for (int64_t i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(dst + i, ws * bf2f(y[(int64_t)row * d + i]));
+}
+__global__ void zero_f32_kernel(float* p, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0.f;
+}
+__global__ void f32_to_bf16_kernel(const float* p, int64_t n, __nv_bfloat16* out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = f2bf(p[i]);
+}
+
+static int64_t contiguous_rows(int64_t T, int k, int E) { return cdiv(T * k + 127ll * E, 128) * 128; }
+
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* weights,
+                            void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0, "T < 0");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(logits && ids && weights, "null pointer");
+  BI_REQUIRE_SHAPE(E >= 1 && E <= 64, "E must be in [1, 64]");
+  BI_REQUIRE(k >= 1 && k <= E, "k must be in [1, E]");
+  const int warps = 8;
+  route_topk_kernel<<<(unsigned)cdiv(T, warps), warps * 32, 0, as_stream(stream)>>>(logits, T, E, k, ids, weights);
+  return check_launch("bi_moe_route_topk");
+}
+
+size_t bi_moe_permute_workspace_size(int64_t T, int k, int E) {
+  if (T <= 0 || k <= 0 || E <= 0) return 0;
+  return ((size_t)T * k + (size_t)E + 64) * sizeof(int32_t);
+}
+
+static bi_status permute_common(const int32_t* ids, int64_t T, int k, int E, void* workspace, size_t ws_bytes,
+                                int32_t** rank, int32_t** counts, cudaStream_t st) {
+  using namespace bi;
+  BI_REQUIRE(workspace && ws_bytes >= bi_moe_permute_workspace_size(T, k, E), "permute workspace too small");
+  BI_REQUIRE(E >= 1 && E <= 1024, "E must be in [1, 1024]");
+  *rank = static_cast<int32_t*>(workspace);
+  *counts = *rank + T * k;
+  expert_rank_kernel<<<E, kPermThreads, 0, st>>>(ids, T * k, E, *rank, *counts, device_status_ptr());
+  return check_launch("expert_rank_kernel");
+}
+
+bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t max_rows, int32_t* row_of_slot,
+                         int32_t* tile_expert, int32_t* expert_offsets, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && k >= 1, "bad shape");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(ids && row_of_slot && tile_expert && expert_offsets, "null pointer");
+  BI_REQUIRE(max_rows % 128 == 0 && max_rows >= contiguous_rows(T, k, E), "max_rows too small");
+  cudaStream_t st = as_stream(stream);
+  int32_t *rank, *counts;
+  BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
+  expert_offsets_kernel<<<1, 256, 0, st>>>(counts, E, max_rows / 128, expert_offsets, tile_expert,
+                                           device_status_ptr());
+  BI_TRY(check_launch("expert_offsets_kernel"));
+  row_of_slot_kernel<<<(unsigned)cdiv(T * k, 256), 256, 0, st>>>(ids, rank, T * k, expert_offsets, 0, max_rows,
+                                                                   row_of_slot, device_status_ptr());
+  return check_launch("row_of_slot_kernel");
+}
+
+bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int64_t capacity, int32_t* row_of_slot,
+                                int32_t* tile_expert, void* workspace, size_t ws_bytes, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && k >= 1, "bad shape");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(ids && row_of_slot && tile_expert, "null pointer");
+  BI_REQUIRE(capacity > 0 && capacity % 128 == 0, "capacity must be a positive multiple of 128");
+  cudaStream_t st = as_stream(stream);
+  int32_t *rank, *counts;
+  BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
+  const int64_t n_tiles = E * capacity / 128;
+  masked_tiles_kernel<<<(unsigned)cdiv(n_tiles, 256), 256, 0, st>>>(tile_expert, n_tiles, capacity / 128);
+  BI_TRY(check_launch("masked_tiles_kernel"));
+  row_of_slot_kernel<<<(unsigned)cdiv(T * k, 256), 256, 0, st>>>(ids, rank, T * k, nullptr, capacity, E * capacity,
+                                                                   row_of_slot, device_status_ptr());
+  return check_launch("row_of_slot_kernel");
+}
+
+bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, int k, int64_t d, void* xp,
+                        void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && k >= 1, "bad shape");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(x && row_of_slot && xp, "null pointer");
+  BI_REQUIRE(d % 8 == 0 && aligned16(x) && aligned16(xp), "d % 8 and 16-byte alignment required");
+  moe_gather_kernel<<<(unsigned)(T * k), 128, 0, as_stream(stream)>>>(static_cast<const __nv_bfloat16*>(x),
+                                                                      row_of_slot, k, d,
+                                                                      static_cast<__nv_bfloat16*>(xp));
+  return check_launch("bi_moe_gather");
+}
+
+size_t bi_moe_combine_workspace_size(int64_t T, int64_t d, int mode) {
+  return mode == BI_FAST && T > 0 ? (size_t)T * d * sizeof(float) : 0;
+}
+
+bi_status bi_moe_combine(const void* y, const int32_t* row_of_slot, const float* w, int64_t T, int k, int64_t d,
+                         void* out, int mode, void* workspace, size_t ws_bytes, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && k >= 1, "bad shape");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(y && row_of_slot && w && out, "null pointer");
+  BI_REQUIRE(d % 8 == 0 && aligned16(y) && aligned16(out), "d % 8 and 16-byte alignment required");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  cudaStream_t st = as_stream(stream);
+  if (mode == BI_FAST) {
+    BI_REQUIRE(workspace && ws_bytes >= (size_t)T * d * sizeof(float), "BI_FAST combine needs workspace");
+    float* acc = static_cast<float*>(workspace);
+    const int blocks = (int)std::min<int64_t>(cdiv(T * d, 256), 8 * (int64_t)num_sms());
+    zero_f32_kernel<<<blocks, 256, 0, st>>>(acc, T * d);
+    BI_TRY(check_launch("zero_f32_kernel"));
+    moe_combine_atomic_kernel<<<(unsigned)(T * k), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y), row_of_slot,
+                                                                  w, k, d, acc);
+    BI_TRY(check_launch("moe_combine_atomic_kernel"));
+    f32_to_bf16_kernel<<<blocks, 256, 0, st>>>(acc, T * d, static_cast<__nv_bfloat16*>(out));
+    return check_launch("f32_to_bf16_kernel");
+  }
+  const int thr = (int)std::min<int64_t>(256, std::max<int64_t>(32, d / 8));
+  moe_combine_kernel<<<(unsigned)T, thr, 0, st>>>(static_cast<const __nv_bfloat16*>(y), row_of_slot, w, k, d,
+                                                  static_cast<__nv_bfloat16*>(out));
+  return check_launch("bi_moe_combine");
+}
+
+size_t bi_moe_layer_workspace_size(int64_t T, int64_t d, int E, int k, int64_t F, int mode) {
+  if (T <= 0) return 0;
+  const int64_t rows = bi::contiguous_rows(T, k, E);
+  size_t b = 0;
+  auto add = [&](size_t n) { b += (n + 255) / 256 * 256; };
+  add((size_t)T * k * 4);                        // ids
+  add((size_t)T * k * 4);                        // weights
+  add((size_t)T * k * 4);                        // row_of_slot
+  add((size_t)(rows / 128) * 4);                 // tile_expert
+  add((size_t)(E + 1) * 4);                      // offsets
+  add(bi_moe_permute_workspace_size(T, k, E));   // rank + counts
+  add((size_t)rows * d * 2);                     // gathered x
+  add((size_t)rows * F * 2);                     // activation
+  add((size_t)rows * d * 2);                     // expert outputs
+  add(bi_moe_combine_workspace_size(T, d, mode));
+  return b;
+}
+
+bi_status bi_moe_layer(const void* x, const float* router_logits, int64_t T, int64_t d, int E, int k, int64_t F,
+                       const void* w13, const void* w2, void* out, int mode, void* workspace, size_t ws_bytes,
+                       void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0, "T < 0");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(x && router_logits && w13 && w2 && out && workspace, "null pointer");
+  BI_REQUIRE(ws_bytes >= bi_moe_layer_workspace_size(T, d, E, k, F, mode), "MoE workspace too small");
+  const int64_t rows = contiguous_rows(T, k, E);
+  uint8_t* p = static_cast<uint8_t*>(workspace);
+  auto take = [&](size_t n) {
+    void* r = p;
+    p += (n + 255) / 256 * 256;
+    return r;
+  };
+  auto* ids = static_cast<int32_t*>(take((size_t)T * k * 4));
+  auto* wts = static_cast<float*>(take((size_t)T * k * 4));
+  auto* ros = static_cast<int32_t*>(take((size_t)T * k * 4));
+  auto* tiles = static_cast<int32_t*>(take((size_t)(rows / 128) * 4));
+  auto* offs = static_cast<int32_t*>(take((size_t)(E + 1) * 4));
+  const size_t pws = bi_moe_permute_workspace_size(T, k, E);
+  void* perm_ws = take(pws);
+  void* xp = take((size_t)rows * d * 2);
+  void* act = take((size_t)rows * F * 2);
+  void* y = take((size_t)rows * d * 2);
+  void* cws = take(bi_moe_combine_workspace_size(T, d, mode));
+  BI_TRY(bi_moe_route_topk(router_logits, T, E, k, ids, wts, stream));
+  BI_TRY(bi_moe_permute(ids, T, k, E, rows, ros, tiles, offs, perm_ws, pws, stream));
+  BI_TRY(bi_moe_gather(x, ros, T, k, d, xp, stream));
+  BI_TRY(bi_grouped_gemm(xp, rows, d, w13, E, 2 * F, tiles, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, stream));
+  BI_TRY(bi_grouped_gemm(act, rows, F, w2, E, d, tiles, y, BI_DTYPE_BF16, BI_EPI_NONE, stream));
+  return bi_moe_combine(y, ros, wts, T, k, d, out, mode, cws, bi_moe_combine_workspace_size(T, d, mode), stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// RMSNorm with optional fused residual add: one CTA per row, fixed reduction tree.
+//
+// Batch-invariance source: "vLLM Achieves Bitwise-Consistent RL Training ..."
+// §2 (batch independence: the row result may not depend on batch-mates) and
+// §3.1 (RMSNorm is a forward operator whose values come from this kernel on
+// both the rollout and the training side).
+#include "common.cuh"
+
+namespace bi {
+
+// Threads per row: d/8 (one 16-byte vector each) capped at 256; a thread walks
+// its vectors with stride 8*blockDim, so the per-thread order depends on d only.
+static int norm_threads(int64_t d) {
+  int64_t t = d / 8;
+  if (t > 256) t = 256;
+  if (t < 32) t = 32;
+  return (int)((t + 31) / 32 * 32);
+}
+
+template <bool kResidual>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
+                                                      __nv_bfloat16* __restrict__ residual,
+                                                      const __nv_bfloat16* __restrict__ gamma,
+                                                      __nv_bfloat16* __restrict__ y, int d, float eps) {
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int nvec = d / 8;
+  constexpr int kMaxVec = 8;  // d <= 16384 -> at most 8 vectors per thread with 256 threads
+  uint4 sv[kMaxVec];
+  float ss = 0.f;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
+  uint4* rr = reinterpret_cast<uint4*>(residual + row * d);
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int v = tid + i * nthr;
+    if (v < nvec) {
+      uint4 a = xr[v];
+      if (kResidual) {
+        uint4 b = rr[v];
+        uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
+        const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float lo = __fadd_rn(bf16lo(pb[j]), bf16lo(pa[j]));
+          float hi = __fadd_rn(bf16hi(pb[j]), bf16hi(pa[j]));
+          pa[j] = pack_bf16x2(lo, hi);
+        }
+        rr[v] = a;
+      }
+      sv[i] = a;
+      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&a);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo = bf16lo(pa[j]), hi = bf16hi(pa[j]);
+        ss = __fmaf_rn(lo, lo, ss);
+        ss = __fmaf_rn(hi, hi, ss);
+      }
+    }
+  }
+  // fixed xor-butterfly inside the warp, then warps summed in index order
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  __shared__ float warp_ss[8];
+  __shared__ float s_inv;
+  if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nthr / 32; ++w) t += warp_ss[w];
+    const float ms = __fdiv_rn(t, (float)d);
+    s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  }
+  __syncthreads();
+  const float inv = s_inv;
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * d);
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int v = tid + i * nthr;
+    if (v < nvec) {
+      const uint4 g = gr[v];
+      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&sv[i]);
+      const uint32_t* pg = reinterpret_cast<const uint32_t*>(&g);
+      uint4 o;
+      uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo = __fmul_rn(__fmul_rn(bf16lo(pa[j]), inv), bf16lo(pg[j]));
+        float hi = __fmul_rn(__fmul_rn(bf16hi(pa[j]), inv), bf16hi(pg[j]));
+        po[j] = pack_bf16x2(lo, hi);
+      }
+      yr[v] = o;
+    }
+  }
+}
+
+}  // namespace bi
+
+extern "C" bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d,
+                                float eps, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(rows >= 0, "rows < 0");
+  if (rows == 0) return BI_OK;
+  BI_REQUIRE(x && gamma && y, "null pointer");
+  BI_REQUIRE(d >= 8 && d <= 16384 && d % 8 == 0, "d must be a multiple of 8 in [8, 16384]");
+  BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y) && (!residual || aligned16(residual)),
+             "pointers must be 16-byte aligned");
+  BI_REQUIRE(rows <= 0x7fffffff, "rows too large");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  const int thr = norm_threads(d);
+  auto* xp = static_cast<const __nv_bfloat16*>(x);
+  auto* rp = static_cast<__nv_bfloat16*>(residual);
+  auto* gp = static_cast<const __nv_bfloat16*>(gamma);
+  auto* yp = static_cast<__nv_bfloat16*>(y);
+  if (residual)
+    rmsnorm_kernel<true><<<(unsigned)rows, thr, 0, as_stream(stream)>>>(xp, rp, gp, yp, (int)d, eps);
+  else
+    rmsnorm_kernel<false><<<(unsigned)rows, thr, 0, as_stream(stream)>>>(xp, rp, gp, yp, (int)d, eps);
+  return check_launch("bi_rmsnorm");
+}

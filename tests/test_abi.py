@@ -1,0 +1,85 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_forward_policy_gb300 as bi
+from invariant_forward_policy_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "bi.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bi_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = _declared()
+    assert len(names) >= 30
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_version_and_no_error(lib):
+    assert bi.bi_version() == 100
+    assert isinstance(bi.bi_last_error(), str)
+
+
+def test_validation_rejects_bad_arguments_without_launching(lib):
+    # null pointers, bad shapes and bad modes are refused before any CUDA call
+    assert lib.bi_rmsnorm(None, None, None, None, 4, 64, 1e-6, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert "null" in bi.bi_last_error()
+    assert lib.bi_rmsnorm(16, None, 16, 16, 4, 63, 1e-6, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm(16, None, 16, 16, 4, 64, 1e-6, 7, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm(16, 4, 100, 16, 64, 16, 0, 0, 0, None, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_gemm(16, 4, 64, 16, 64, 16, 0, 5, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_gemm(17, 4, 64, 16, 64, 16, 0, 0, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG  # misaligned
+    assert lib.bi_logprob_gather(16, None, 4, 6, 16, None, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_moe_route_topk(16, 4, 65, 8, 16, 16, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_moe_route_topk(16, 4, 64, 65, 16, 16, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 96, 16, 16, 16, 1, 64, 512, 0.1, 16, 1 << 20, 16, 0,
+                            None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 1, 64, 500, 0.1, 16, 1 << 20, 16, 0,
+                            None) == bi.BI_ERR_INVALID_ARG
+    # empty inputs are no-ops
+    assert lib.bi_rmsnorm(None, None, None, None, 0, 64, 1e-6, 0, None) == bi.BI_OK
+    assert lib.bi_gemm(None, 0, 64, None, 64, None, 0, 0, 0, None, 0, None) == bi.BI_OK
+
+
+def test_model_config_validation(lib):
+    cfg = _lib.bi_model_config(n_layers=2, d=128, n_heads_q=4, n_heads_kv=2, head_dim=64, ffn=256, vocab=512, eps=1e-6,
+                               rope_theta=1e4, kv_block=32, kv_split=512, max_pos=256)
+    w = _lib.bi_weights()
+    h = ctypes.c_void_p()
+    create = lambda: lib.bi_model_create(ctypes.byref(cfg), ctypes.byref(w), None, ctypes.byref(h))
+    assert create() == bi.BI_ERR_UNSUPPORTED_SHAPE
+    cfg.kv_block = 64
+    cfg.kv_split = 100
+    assert create() == bi.BI_ERR_INVALID_ARG
+    cfg.kv_split = 512
+    assert create() == bi.BI_ERR_INVALID_ARG   # null weight pointers
+    assert "null" in bi.bi_last_error()
+
+
+def test_workspace_queries_are_limit_sized(lib):
+    cfg = _lib.bi_model_config(n_layers=4, d=512, n_heads_q=8, n_heads_kv=8, head_dim=64, ffn=1408, vocab=32000,
+                               eps=1e-6, rope_theta=1e4, kv_block=64, kv_split=512, max_pos=1024)
+    a = _lib.bi_forward_workspace_size(cfg, 1024, 16, 768, 512)
+    b = _lib.bi_forward_workspace_size(cfg, 2048, 16, 768, 512)
+    assert 0 < a < b
+    assert _lib.bi_kv_cache_bytes(cfg, 10) == 4 * 10 * 8 * 64 * 64 * 2
+    # invariant GEMM tile width depends on the weight shape only
+    assert bi.bi_gemm_tile_n(32000, 512) == bi.bi_gemm_tile_n(32000, 512)
+    assert bi.bi_gemm_workspace_size(16, 1536, 512, 0, bi.BI_INVARIANT) == 0
+    assert bi.bi_gemm_workspace_size(16, 1536, 512, 0, bi.BI_FAST) > 0

@@ -1,0 +1,337 @@
+"""Per-kernel parity with the CPU oracle and bitwise batch invariance, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import invariant_forward_policy_gb300 as bi
+from oracle import moe as omoe
+from oracle import ops
+from synthetic import bits_to_f32, make_moe_layer, normal_bf16
+from tests.gpu_util import bf16_close, dev_bf16, host_f32, same_bits
+
+pytestmark = pytest.mark.gpu
+F32 = np.float32
+
+
+def rng_bf16(rng, shape, std=1.0):
+    b = normal_bf16(rng, shape, std)
+    return b, bits_to_f32(b)
+
+
+# ---------------------------------------------------------------------------- RMSNorm
+@pytest.mark.parametrize("rows,d", [(1, 256), (7, 512), (130, 2048), (33, 4096), (5, 520)])
+@pytest.mark.parametrize("residual", [False, True])
+def test_rmsnorm_parity_and_residual(rows, d, residual):
+    rng = np.random.default_rng(rows * d)
+    xb, xf = rng_bf16(rng, (rows, d), 2.0)
+    rb, rf = rng_bf16(rng, (rows, d))
+    gb, gf = rng_bf16(rng, (d,), 0.2)
+    gb = normal_bf16(np.random.default_rng(1), (d,), 0.2)
+    gf = bits_to_f32(gb) + F32(0)
+    x, g = dev_bf16(xb), dev_bf16(gb)
+    res = dev_bf16(rb) if residual else None
+    y = torch.empty_like(x)
+    bi.bi_rmsnorm(x, res, g, y, rows, d, 1e-6)
+    want, r_want = ops.rmsnorm(xf, gf, 1e-6, residual=rf if residual else None)
+    bf16_close(host_f32(y), want, ulps=1, frac_exact=0.97)
+    if residual:
+        assert np.array_equal(host_f32(res), r_want)
+
+
+def test_rmsnorm_rows_do_not_depend_on_batch():
+    rng = np.random.default_rng(3)
+    d = 2048
+    xb, _ = rng_bf16(rng, (300, d))
+    g = dev_bf16(normal_bf16(rng, (d,), 1.0))
+    x = dev_bf16(xb)
+    y = torch.empty_like(x)
+    bi.bi_rmsnorm(x, None, g, y, 300, d)
+    perm = torch.from_numpy(rng.permutation(300)).cuda()
+    xp = x[perm].contiguous()
+    yp = torch.empty_like(xp)
+    bi.bi_rmsnorm(xp, None, g, yp, 300, d)
+    assert same_bits(yp, y[perm])
+    for r in (0, 17, 299):
+        y1 = torch.empty_like(x[r:r + 1])
+        bi.bi_rmsnorm(x[r:r + 1].contiguous(), None, g, y1, 1, d)
+        assert same_bits(y1, y[r:r + 1])
+
+
+# ---------------------------------------------------------------------------- GEMM
+GEMM_SHAPES = [(1, 64, 64), (5, 1536, 512), (128, 512, 512), (129, 4096, 256), (300, 200, 576), (17, 32000, 512),
+               (260, 2816, 512)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_bf16_and_fp32_parity(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    ab, af = rng_bf16(rng, (M, K))
+    wb, wf = rng_bf16(rng, (N, K), 0.05)
+    A, W = dev_bf16(ab), dev_bf16(wb)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm(A, M, K, W, N, C)
+    bf16_close(host_f32(C), ops.linear(af, wf, "bf16"), ulps=1, frac_exact=0.97)
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    bi.bi_gemm(A, M, K, W, N, C32, bi.BI_DTYPE_FP32)
+    want = ops.linear(af, wf, "fp32")
+    scale = np.sqrt(np.abs(af) @ np.abs(wf).T ** 2 + 1e-30)
+    assert np.max(np.abs(host_f32(C32) - want) / (np.abs(af) @ np.abs(wf).T + 1e-30)) < 1e-5, scale.shape
+
+
+@pytest.mark.parametrize("M,F,K", [(3, 1408, 512), (200, 64, 128), (129, 5632, 256)])
+def test_gemm_swiglu_epilogue(M, F, K):
+    rng = np.random.default_rng(M * F)
+    ab, af = rng_bf16(rng, (M, K))
+    wb, wf = rng_bf16(rng, (2 * F, K), 0.08)
+    C = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm(dev_bf16(ab), M, K, dev_bf16(wb), 2 * F, C, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
+    want = ops.silu_mul(ops.linear(af, wf[:F]), ops.linear(af, wf[F:]))
+    bf16_close(host_f32(C), want, ulps=2, frac_exact=0.9, atol=1e-6)
+
+
+@pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408)])
+def test_gemm_rows_invariant_to_M_and_order(N, K):
+    rng = np.random.default_rng(N)
+    ab, _ = rng_bf16(rng, (300, K))
+    wb, _ = rng_bf16(rng, (N, K), 0.02)
+    A, W = dev_bf16(ab), dev_bf16(wb)
+    full = torch.empty((300, N), dtype=torch.float32, device="cuda")
+    bi.bi_gemm(A, 300, K, W, N, full, bi.BI_DTYPE_FP32)
+    for M in (1, 2, 7, 16, 64, 127, 128, 129, 255):
+        part = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        off = 300 - M
+        bi.bi_gemm(A[off:].contiguous(), M, K, W, N, part, bi.BI_DTYPE_FP32)
+        assert same_bits(part, full[off:]), M
+    perm = torch.from_numpy(rng.permutation(300)).cuda()
+    outp = torch.empty_like(full)
+    bi.bi_gemm(A[perm].contiguous(), 300, K, W, N, outp, bi.BI_DTYPE_FP32)
+    assert same_bits(outp, full[perm])
+
+
+def test_gemm_fast_mode_is_close_but_split():
+    rng = np.random.default_rng(9)
+    M, N, K = 16, 1536, 512
+    ab, af = rng_bf16(rng, (M, K))
+    wb, wf = rng_bf16(rng, (N, K), 0.05)
+    ws = torch.empty(bi.bi_gemm_workspace_size(M, N, K, 0, bi.BI_FAST), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    bi.bi_gemm(dev_bf16(ab), M, K, dev_bf16(wb), N, C, bi.BI_DTYPE_FP32, 0, bi.BI_FAST, ws)
+    want = ops.linear(af, wf, "fp32")
+    assert np.max(np.abs(host_f32(C) - want)) < 1e-4
+
+
+# ---------------------------------------------------------------------------- logprob
+@pytest.mark.parametrize("T,V", [(37, 4096), (16, 32000), (3, 129280)])
+def test_logprob_gather_parity(T, V):
+    rng = np.random.default_rng(T + V)
+    x = (rng.standard_normal((T, V)) * 3).astype(F32)
+    ids = rng.integers(0, V, T).astype(np.int32)
+    xl = torch.from_numpy(x).cuda()
+    lp = torch.empty(T, dtype=torch.float32, device="cuda")
+    am = torch.empty(T, dtype=torch.int32, device="cuda")
+    bi.bi_logprob_gather(xl, torch.from_numpy(ids).cuda(), T, V, lp, am)
+    assert np.max(np.abs(lp.cpu().numpy() - ops.logprob(x, ids))) < 5e-5
+    assert np.array_equal(am.cpu().numpy(), ops.argmax_lowest(x))
+    bi.bi_logprob_gather(xl, None, T, V, lp, am)   # greedy: logprob of the argmax
+    assert np.max(np.abs(lp.cpu().numpy() - ops.logprob(x, ops.argmax_lowest(x)))) < 5e-5
+
+
+def test_logprob_argmax_ties_lowest_id_and_row_invariance():
+    V = 32000
+    x = np.random.default_rng(5).standard_normal((64, V)).astype(F32)
+    x[:, [7, 19000, 31999]] = 9.0
+    xl = torch.from_numpy(x).cuda()
+    lp = torch.empty(64, dtype=torch.float32, device="cuda")
+    am = torch.empty(64, dtype=torch.int32, device="cuda")
+    bi.bi_logprob_gather(xl, None, 64, V, lp, am)
+    assert (am.cpu().numpy() == 7).all()
+    for T in (1, 5, 33):
+        lp1 = torch.empty(T, dtype=torch.float32, device="cuda")
+        bi.bi_logprob_gather(xl[-T:].contiguous(), None, T, V, lp1)
+        assert same_bits(lp1, lp[-T:])
+
+
+# ---------------------------------------------------------------------------- RoPE + attention
+def _paged_setup(seq_lens, Hq, Hkv, hd, rng, n_blocks_extra=3):
+    max_blk = max(math.ceil(n / 64) for n in seq_lens)
+    n_blocks = len(seq_lens) * max_blk + n_blocks_extra
+    perm = rng.permutation(n_blocks)[: len(seq_lens) * max_blk].astype(np.int32)
+    bt = torch.from_numpy(perm.reshape(len(seq_lens), max_blk)).cuda()
+    kc = torch.full((n_blocks, Hkv, 64, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full((n_blocks, Hkv, 64, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    return bt, kc, vc, max_blk, n_blocks
+
+
+def _pieces(pieces):
+    """pieces: list of (seq, pos0, n) -> device metadata arrays."""
+    seq = torch.tensor([p[0] for p in pieces], dtype=torch.int32, device="cuda")
+    row0 = torch.tensor(np.concatenate([[0], np.cumsum([p[2] for p in pieces])]), dtype=torch.int32, device="cuda")
+    pos0 = torch.tensor([p[1] for p in pieces], dtype=torch.int32, device="cuda")
+    return seq, row0, pos0
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd", [(8, 8, 64), (16, 4, 128), (4, 1, 64)])
+def test_rope_kv_write_and_attention_prefill_parity(Hq, Hkv, hd):
+    rng = np.random.default_rng(Hq * hd)
+    seq_lens = [70, 600, 1100]
+    bt, kc, vc, max_blk, n_blocks = _paged_setup(seq_lens, Hq, Hkv, hd, rng)
+    max_pos = 2048
+    table = torch.empty((max_pos, hd), dtype=torch.float32, device="cuda")
+    bi.bi_rope_table(table, max_pos, hd, 10000.0)
+    nq = (Hq + 2 * Hkv) * hd
+    T = sum(seq_lens)
+    qkvb, qkvf = rng_bf16(rng, (T, nq))
+    seq, row0, pos0 = _pieces([(b, 0, n) for b, n in enumerate(seq_lens)])
+    q = torch.empty((T, Hq, hd), dtype=torch.bfloat16, device="cuda")
+    bi.bi_rope_kv_write(dev_bf16(qkvb), T, seq, row0, pos0, len(seq_lens), max(seq_lens), Hq, Hkv, hd, table, max_pos,
+                        bt, max_blk, n_blocks, q, kc, vc)
+    out = torch.empty((T, Hq * hd), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(bi.bi_attention_workspace_size(T, Hq, hd, max(seq_lens), 512), dtype=torch.uint8, device="cuda")
+    bi.bi_attention(q, T, seq, row0, pos0, len(seq_lens), max(seq_lens), Hq, Hkv, hd, kc, vc, bt, max_blk,
+                    max(seq_lens), 512, 1.0 / math.sqrt(hd), ws, out)
+    got_q, got_o = host_f32(q), host_f32(out)
+    r0 = 0
+    for b, n in enumerate(seq_lens):
+        f = qkvf[r0:r0 + n]
+        pos = np.arange(n)
+        qo = ops.rope(f[:, : Hq * hd].reshape(n, Hq, hd), pos)
+        ko = ops.rope(f[:, Hq * hd:(Hq + Hkv) * hd].reshape(n, Hkv, hd), pos)
+        vo = f[:, (Hq + Hkv) * hd:].reshape(n, Hkv, hd)
+        bf16_close(got_q[r0:r0 + n], qo, ulps=1, frac_exact=0.99)
+        # cache contents at the sequence's blocks
+        blocks = bt[b].cpu().numpy()
+        kg = host_f32(kc)[blocks].transpose(0, 2, 1, 3).reshape(-1, Hkv, hd)[:n]
+        vg = host_f32(vc)[blocks].transpose(0, 2, 1, 3).reshape(-1, Hkv, hd)[:n]
+        bf16_close(kg, ko, ulps=1, frac_exact=0.99)
+        assert np.array_equal(vg, vo)
+        want = ops.attention(qo, ko, vo, pos).reshape(n, Hq * hd)
+        err = np.abs(got_o[r0:r0 + n] - want)
+        assert err.max() < 2e-2 and err.mean() < 2e-3, (err.max(), err.mean())
+        r0 += n
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd", [(8, 8, 64), (16, 4, 128)])
+def test_attention_decode_rows_equal_prefill_rows_bitwise(Hq, Hkv, hd):
+    """A decode call (one token per sequence) reproduces the prefill rows exactly,
+    and so does any chunking of the prefill."""
+    rng = np.random.default_rng(11 + hd)
+    seq_lens = [1100, 513, 64, 1]
+    bt, kc, vc, max_blk, n_blocks = _paged_setup(seq_lens, Hq, Hkv, hd, rng)
+    max_pos = 2048
+    table = torch.empty((max_pos, hd), dtype=torch.float32, device="cuda")
+    bi.bi_rope_table(table, max_pos, hd, 10000.0)
+    nq = (Hq + 2 * Hkv) * hd
+    T = sum(seq_lens)
+    qkv = dev_bf16(normal_bf16(rng, (T, nq), 1.0))
+    scale = 1.0 / math.sqrt(hd)
+
+    def run(pieces, rows_qkv, max_ctx, mode=bi.BI_INVARIANT):
+        seq, row0, pos0 = _pieces(pieces)
+        Tn = rows_qkv.shape[0]
+        mq = max(p[2] for p in pieces)
+        q = torch.empty((Tn, Hq, hd), dtype=torch.bfloat16, device="cuda")
+        bi.bi_rope_kv_write(rows_qkv, Tn, seq, row0, pos0, len(pieces), mq, Hq, Hkv, hd, table, max_pos, bt, max_blk,
+                            n_blocks, q, kc, vc)
+        out = torch.empty((Tn, Hq * hd), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(bi.bi_attention_workspace_size(Tn, Hq, hd, max_ctx, 512), dtype=torch.uint8, device="cuda")
+        bi.bi_attention(q, Tn, seq, row0, pos0, len(pieces), mq, Hq, Hkv, hd, kc, vc, bt, max_blk, max_ctx, 512,
+                        scale, ws, out, mode)
+        return out
+
+    offs = np.concatenate([[0], np.cumsum(seq_lens)])
+    full = run([(b, 0, n) for b, n in enumerate(seq_lens)], qkv, max(seq_lens))
+    # chunked prefill: chunks of 97 then of 64
+    for ch in (97, 64, 512):
+        outs = []
+        for b, n in enumerate(seq_lens):
+            for s0 in range(0, n, ch):
+                e = min(n, s0 + ch)
+                outs.append((offs[b] + s0, run([(b, s0, e - s0)], qkv[offs[b] + s0: offs[b] + e].contiguous(),
+                                               max(seq_lens))))
+        for r, o in outs:
+            assert same_bits(o, full[r:r + o.shape[0]]), ch
+    # decode: every sequence's rows at a few positions, as one batch of single tokens
+    for pos in (0, 63, 64, 511, 512, 1099):
+        pcs, rows = [], []
+        for b, n in enumerate(seq_lens):
+            if pos < n:
+                pcs.append((b, pos, 1))
+                rows.append(offs[b] + pos)
+        if not pcs:
+            continue
+        o = run(pcs, qkv[torch.tensor(rows, device="cuda")].contiguous(), 2048)
+        assert same_bits(o, full[torch.tensor(rows, device="cuda")]), pos
+
+
+# ---------------------------------------------------------------------------- MoE
+def _moe_dev(T, d, F, E, seed):
+    inp = make_moe_layer(T, d, F, E, 0.05, seed)
+    return inp, dev_bf16(inp["x"]), torch.from_numpy(inp["router_logits"]).cuda(), dev_bf16(inp["w13"]), \
+        dev_bf16(inp["w2"])
+
+
+def test_moe_route_topk_matches_oracle_and_ties():
+    rng = np.random.default_rng(2)
+    T, E, k = 500, 64, 8
+    x = rng.standard_normal((T, E)).astype(F32)
+    x[:50] = np.round(x[:50])   # many exact ties
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    bi.bi_moe_route_topk(torch.from_numpy(x).cuda(), T, E, k, ids, w)
+    oi, ow = omoe.route_topk(x, k)
+    assert np.array_equal(ids.cpu().numpy(), oi)
+    assert np.max(np.abs(w.cpu().numpy() - ow)) < 1e-6
+
+
+@pytest.mark.parametrize("T", [1, 37, 512])
+def test_moe_layer_parity(T):
+    d, F, E, k = 256, 128, 16, 4
+    inp, x, lg, w13, w2 = _moe_dev(T, d, F, E, seed=T)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(bi.bi_moe_layer_workspace_size(T, d, E, k, F), dtype=torch.uint8, device="cuda")
+    bi.bi_moe_layer(x, lg, T, d, E, k, F, w13, w2, out, bi.BI_INVARIANT, ws)
+    want, _, _ = omoe.moe_layer(bits_to_f32(inp["x"]), inp["router_logits"], bits_to_f32(inp["w13"]),
+                                bits_to_f32(inp["w2"]), k)
+    got = host_f32(out)
+    err = np.abs(got - want)
+    assert np.all(err <= 2 * 2.0 ** -7 * np.abs(want) + 2e-3), err.max()
+
+
+def test_moe_rows_invariant_to_batching_and_layout():
+    T, d, F, E, k = 600, 256, 128, 16, 4
+    inp, x, lg, w13, w2 = _moe_dev(T, d, F, E, seed=77)
+
+    def layer(xs, ls):
+        n = xs.shape[0]
+        out = torch.empty((n, d), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(bi.bi_moe_layer_workspace_size(n, d, E, k, F), dtype=torch.uint8, device="cuda")
+        bi.bi_moe_layer(xs, ls, n, d, E, k, F, w13, w2, out, bi.BI_INVARIANT, ws)
+        return out
+
+    full = layer(x, lg)
+    rng = np.random.default_rng(0)
+    perm = torch.from_numpy(rng.permutation(T)).cuda()
+    assert same_bits(layer(x[perm].contiguous(), lg[perm].contiguous()), full[perm])
+    for a, b in ((0, 1), (5, 200), (300, 600)):
+        assert same_bits(layer(x[a:b].contiguous(), lg[a:b].contiguous()), full[a:b])
+    # masked layout (fixed capacity per expert) gives the same rows as the contiguous one
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    bi.bi_moe_route_topk(lg, T, E, k, ids, w)
+    cap = 128 * math.ceil(T * k / E / 128 + 2)
+    ros = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    tiles = torch.empty(E * cap // 128, dtype=torch.int32, device="cuda")
+    pws = torch.empty(bi.bi_moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+    bi.bi_moe_permute_masked(ids, T, k, E, cap, ros, tiles, pws)
+    xp = torch.zeros((E * cap, d), dtype=torch.bfloat16, device="cuda")
+    bi.bi_moe_gather(x, ros, T, k, d, xp)
+    act = torch.empty((E * cap, F), dtype=torch.bfloat16, device="cuda")
+    bi.bi_grouped_gemm(xp, E * cap, d, w13, E, 2 * F, tiles, act, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
+    y = torch.empty((E * cap, d), dtype=torch.bfloat16, device="cuda")
+    bi.bi_grouped_gemm(act, E * cap, F, w2, E, d, tiles, y)
+    out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    bi.bi_moe_combine(y, ros, w, T, k, d, out)
+    assert same_bits(out, full)
