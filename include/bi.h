@@ -268,6 +268,17 @@ typedef struct bi_model bi_model;
 bi_status bi_model_create(const bi_model_config* cfg, const bi_weights* w, void* stream, bi_model** out);
 void bi_model_destroy(bi_model* m);
 
+/* Layer-by-layer dump for locating the first divergent layer ([Article] §5:
+ * "on a mismatch, compare layer by layer for the first divergent layer").
+ * While set, every forward pass of at most max_rows rows writes into
+ * dump (device bf16 [n_layers + 2, max_rows, d]): slot l < n_layers the residual
+ * stream entering layer l, slot n_layers the residual after the last layer,
+ * slot n_layers + 1 the final-norm output, rows in pass order (for a prefill
+ * processed in one pass, i.e. T <= max_tokens and chunk >= every sequence
+ * length, that is the call's row order).  Passes longer than max_rows are not
+ * dumped.  NULL disables it.  Adds copies to the stream; results are unchanged. */
+bi_status bi_model_set_dump(bi_model* m, void* dump, int64_t max_rows);
+
 /* Paged KV cache of one model: k_cache and v_cache are bf16
  * [n_layers, n_blocks, Hkv, 64, hd]; block_table is int32 [B, max_blocks_per_seq]. */
 size_t bi_kv_cache_bytes(const bi_model_config* cfg, int64_t n_blocks);

@@ -87,6 +87,7 @@ _SIGS = {
     "bi_model_create": (_int, [ctypes.POINTER(bi_model_config), ctypes.POINTER(bi_weights), _vp,
                                ctypes.POINTER(_vp)]),
     "bi_model_destroy": (None, [_vp]),
+    "bi_model_set_dump": (_int, [_vp, _vp, _i64]),
     "bi_kv_cache_bytes": (_sz, [ctypes.POINTER(bi_model_config), _i64]),
     "bi_forward_workspace_size": (_sz, [ctypes.POINTER(bi_model_config), _i64, _i64, _i64, _i64, _int]),
     "bi_forward_prefill": (_int, [_vp, _vp, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64),
@@ -271,6 +272,10 @@ def bi_model_create(cfg: bi_model_config, weights: bi_weights, stream=None) -> i
 
 def bi_model_destroy(handle: int):
     load().bi_model_destroy(handle)
+
+
+def bi_model_set_dump(handle: int, dump, max_rows: int):
+    _check(load().bi_model_set_dump(handle, _p(dump), max_rows))
 
 
 def bi_kv_cache_bytes(cfg: bi_model_config, n_blocks: int) -> int:

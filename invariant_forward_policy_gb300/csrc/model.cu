@@ -20,6 +20,8 @@ struct bi_model {
   const void* lm_head;
   float* rope_table;
   std::vector<bi_layer_weights> layers;
+  void* dump = nullptr;       // optional per-layer residual dump (bf16 [n_layers + 2, dump_rows, d])
+  int64_t dump_rows = 0;
 };
 
 namespace bi {
@@ -209,7 +211,17 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
   void* gws = L.gemm_ws_bytes ? at<void>(ws, L.gemm_ws) : nullptr;
   const size_t layer_cache = (size_t)n_blocks * Hkv * 64 * hd * 2;
 
+  const bool dumping = m->dump && T <= m->dump_rows;
+  const size_t slot_bytes = (size_t)m->dump_rows * c.d * 2;
+  auto dump_slot = [&](int64_t l) { return static_cast<uint8_t*>(m->dump) + l * slot_bytes; };
+  auto dump_copy = [&](int64_t l, const void* src) -> bi_status {
+    if (!dumping) return BI_OK;
+    cudaMemcpyAsync(dump_slot(l), src, (size_t)T * c.d * 2, cudaMemcpyDeviceToDevice, as_stream(stream));
+    return check_launch("dump copy");
+  };
+
   BI_TRY(bi_embed(at<int32_t>(ws, L.ids), T, m->embed, c.vocab, c.d, h, stream));
+  BI_TRY(dump_copy(0, h));
   BI_TRY(bi_rmsnorm(h, nullptr, m->layers[0].attn_norm, x, T, c.d, c.eps, mode, stream));
   for (int64_t li = 0; li < c.n_layers; ++li) {
     const bi_layer_weights& lw = m->layers[li];
@@ -226,8 +238,16 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     BI_TRY(bi_gemm(x, T, c.d, lw.w13, 2 * c.ffn, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, mode, gws, L.gemm_ws_bytes,
                    stream));
     BI_TRY(bi_gemm(act, T, c.ffn, lw.w2, c.d, tmp, BI_DTYPE_BF16, BI_EPI_NONE, mode, gws, L.gemm_ws_bytes, stream));
-    if (li + 1 < c.n_layers)
+    if (li + 1 < c.n_layers) {
       BI_TRY(bi_rmsnorm(tmp, h, m->layers[li + 1].attn_norm, x, T, c.d, c.eps, mode, stream));
+      BI_TRY(dump_copy(li + 1, h));
+    }
+  }
+  if (dumping) {
+    // residual after the last layer and the final-norm output of every row
+    BI_TRY(dump_copy(c.n_layers, h));
+    BI_TRY(bi_rmsnorm(tmp, dump_slot(c.n_layers), m->final_norm, dump_slot(c.n_layers + 1), T, c.d, c.eps, mode,
+                      stream));
   }
   // final residual add + norm only on the rows whose logits are wanted
   const cudaStream_t st = as_stream(stream);
@@ -300,6 +320,14 @@ bi_status bi_model_create(const bi_model_config* cfg, const bi_weights* w, void*
 }
 
 void bi_model_destroy(bi_model* m) { delete m; }
+
+bi_status bi_model_set_dump(bi_model* m, void* dump, int64_t max_rows) {
+  BI_REQUIRE(m, "null model");
+  BI_REQUIRE(!dump || (max_rows > 0 && bi::aligned16(dump)), "dump needs max_rows > 0 and 16-byte alignment");
+  m->dump = dump;
+  m->dump_rows = dump ? max_rows : 0;
+  return BI_OK;
+}
 
 size_t bi_kv_cache_bytes(const bi_model_config* cfg, int64_t n_blocks) {
   if (!cfg || n_blocks <= 0) return 0;

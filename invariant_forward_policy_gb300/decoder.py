@@ -92,8 +92,11 @@ class Decoder:
     # ------------------------------------------------------------ calls
     def prefill(self, seqs, cache: KVCache, block_table: torch.Tensor, start_pos=None, logit_from=None,
                 targets=None, chunk=2048, max_tokens=8192, max_ctx=None, max_logit_rows=2048,
-                mode=L.BI_INVARIANT, workspace=None, tokens_dev=None):
-        """Packed prefill of a list of token arrays; returns (logprob [T], sampled [T]) over the packed rows."""
+                mode=L.BI_INVARIANT, workspace=None, tokens_dev=None, dump=None):
+        """Packed prefill of a list of token arrays; returns (logprob [T], sampled [T]) over the packed rows.
+
+        `dump` (bf16 [n_layers + 2, rows, d]) receives the per-layer residual
+        stream of a single-pass call (see bi_model_set_dump)."""
         lens = [len(x) for x in seqs]
         B = len(seqs)
         cu = np.zeros(B + 1, dtype=np.int64)
@@ -111,9 +114,15 @@ class Decoder:
         sm = torch.full((T,), -1, dtype=torch.int32, device=self.device)
         if workspace is None:
             workspace = self.workspace(max_tokens, min(B, 128), max_ctx, max_logit_rows, mode)
-        L.bi_forward_prefill(self.handle, tokens_dev, tgt, cu, start_pos, logit_from, B, chunk, block_table,
-                             block_table.shape[1], cache.k, cache.v, cache.n_blocks, lp, sm, workspace, max_tokens,
-                             max_ctx, max_logit_rows, mode)
+        if dump is not None:
+            L.bi_model_set_dump(self.handle, dump, dump.shape[1])
+        try:
+            L.bi_forward_prefill(self.handle, tokens_dev, tgt, cu, start_pos, logit_from, B, chunk, block_table,
+                                 block_table.shape[1], cache.k, cache.v, cache.n_blocks, lp, sm, workspace, max_tokens,
+                                 max_ctx, max_logit_rows, mode)
+        finally:
+            if dump is not None:
+                L.bi_model_set_dump(self.handle, None, 0)
         return lp, sm, cu
 
     def decode(self, tokens: torch.Tensor, pos: torch.Tensor, cache: KVCache, block_table: torch.Tensor, max_ctx: int,

@@ -24,7 +24,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import ops
-from .bf16 import bf16_bits_to_f32
+from .bf16 import bf16_bits_to_f32, round_bf16
 
 F32 = np.float32
 
@@ -36,36 +36,44 @@ def weights_to_f32(w_bits: dict) -> dict:
     return out
 
 
+def layer(lw: dict, shape, r, pos):
+    """One decoder layer on the residual stream r [L, d] of ONE sequence whose
+    rows sit at positions ``pos`` (0 .. L-1, every earlier key is in r).
+    Returns the residual stream after the layer, bf16(r + attn + ffn) with the
+    two adds rounded separately."""
+    L = r.shape[0]
+    hq, hkv, hd, F = shape.n_heads_q, shape.n_heads_kv, shape.head_dim, shape.ffn
+    x, _ = ops.rmsnorm(r, lw["attn_norm"], shape.eps)
+    qkv = ops.linear(x, lw["wqkv"])
+    q = qkv[:, : hq * hd].reshape(L, hq, hd)
+    k = qkv[:, hq * hd: (hq + hkv) * hd].reshape(L, hkv, hd)
+    v = qkv[:, (hq + hkv) * hd:].reshape(L, hkv, hd)
+    q = ops.rope(q, pos, shape.rope_theta)
+    k = ops.rope(k, pos, shape.rope_theta)
+    a = ops.attention(q, k, v, pos).reshape(L, hq * hd)
+    o = ops.linear(a, lw["wo"])
+    x, r = ops.rmsnorm(o, lw["ffn_norm"], shape.eps, residual=r)
+    g = ops.linear(x, lw["w13"][:F])
+    u = ops.linear(x, lw["w13"][F:])
+    dn = ops.linear(ops.silu_mul(g, u), lw["w2"])
+    return round_bf16(r + dn)
+
+
 def hidden_states(w: dict, shape, tokens, return_layers: bool = False):
     """Final-norm output for every position of one sequence, fp32 [L, d] (bf16 values).
 
     ``shape`` carries n_heads_q, n_heads_kv, head_dim, ffn, eps, rope_theta.
-    With ``return_layers`` also returns the residual stream after every layer.
+    With ``return_layers`` also returns the residual stream entering every
+    layer and leaving the last one (n_layers + 1 arrays).
     """
     tokens = np.asarray(tokens, dtype=np.int64)
-    L = tokens.shape[0]
-    hq, hkv, hd, F = shape.n_heads_q, shape.n_heads_kv, shape.head_dim, shape.ffn
-    pos = np.arange(L)
+    pos = np.arange(tokens.shape[0])
     r = w["embed"][tokens]
-    x, _ = ops.rmsnorm(r, w["layers"][0]["attn_norm"], shape.eps)
-    per_layer = []
-    for li, lw in enumerate(w["layers"]):
-        qkv = ops.linear(x, lw["wqkv"])
-        q = qkv[:, : hq * hd].reshape(L, hq, hd)
-        k = qkv[:, hq * hd: (hq + hkv) * hd].reshape(L, hkv, hd)
-        v = qkv[:, (hq + hkv) * hd:].reshape(L, hkv, hd)
-        q = ops.rope(q, pos, shape.rope_theta)
-        k = ops.rope(k, pos, shape.rope_theta)
-        a = ops.attention(q, k, v, pos).reshape(L, hq * hd)
-        o = ops.linear(a, lw["wo"])
-        x, r = ops.rmsnorm(o, lw["ffn_norm"], shape.eps, residual=r)
-        g = ops.linear(x, lw["w13"][:F])
-        u = ops.linear(x, lw["w13"][F:])
-        y = ops.silu_mul(g, u)
-        dn = ops.linear(y, lw["w2"])
-        nxt = w["layers"][li + 1]["attn_norm"] if li + 1 < len(w["layers"]) else w["final_norm"]
-        x, r = ops.rmsnorm(dn, nxt, shape.eps, residual=r)
-        per_layer.append(r.copy())
+    per_layer = [r]
+    for lw in w["layers"]:
+        r = layer(lw, shape, r, pos)
+        per_layer.append(r)
+    x, _ = ops.rmsnorm(r, w["final_norm"], shape.eps)
     if return_layers:
         return x, per_layer
     return x

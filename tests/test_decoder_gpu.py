@@ -13,9 +13,68 @@ from invariant_forward_policy_gb300.decoder import Decoder
 from oracle import model as omodel
 from oracle import ops
 from synthetic import C2, DecoderShape, make_decoder_weights, make_prompts
-from tests.gpu_util import same_bits
+from tests.gpu_util import bf16_close, host_f32, same_bits
 
 pytestmark = pytest.mark.gpu
+
+# Free-running tolerance on the end-to-end logprob.  Two implementations of
+# the same numerical contract (fp32 accumulation, bf16 at the same boundaries)
+# that only sum in a different order already differ by up to ~8e-3 (mean
+# ~2e-3) on these models: the oracle against its own fp64-accumulation
+# variant on the dense-decoder workload gives max 7.5e-3, mean 2.2e-3, because
+# one-ulp bf16 flips in the residual stream propagate.  So the free-running
+# bound is max 2e-2 / mean 5e-3, and the strict check is the layer-anchored one
+# below (every layer from the GPU's own input; logprob from its final norm).
+E2E_MAX, E2E_MEAN = 2e-2, 5e-3
+
+
+def e2e_close(got, want):
+    err = np.abs(np.asarray(got, np.float64) - want)
+    assert err.max() < E2E_MAX and err.mean() < E2E_MEAN, (err.max(), err.mean())
+    return err
+
+
+def anchored_parity(dec, wb, shape, seqs, seed=0):
+    """Prefill `seqs` in one pass with the layer dump on, then check each layer
+    against the oracle applied to the GPU's own layer input, the final norm, and
+    the logprobs against the oracle's lm_head + log-softmax of the GPU's
+    final-norm rows.  Returns the worst errors seen."""
+    W = omodel.weights_to_f32(wb)
+    T = sum(len(s) for s in seqs)
+    L_ = shape.n_layers
+    mb = max(-(-len(s) // 64) for s in seqs)
+    cache = dec.alloc_cache(len(seqs) * mb)
+    bt = dec.block_table(len(seqs), mb, seed=seed)
+    dump = torch.zeros((L_ + 2, T, shape.d), dtype=torch.bfloat16, device="cuda")
+    rng = np.random.default_rng(seed)
+    targets = [rng.integers(0, shape.vocab, len(s)).astype(np.int32) for s in seqs]
+    lp, _, cu = dec.prefill(seqs, cache, bt, targets=targets, chunk=max(len(s) for s in seqs), max_tokens=T,
+                            max_logit_rows=T, dump=dump)
+    D = host_f32(dump)
+    lp = lp.cpu().numpy()
+    worst = {"layer_max_rel_update": 0.0, "layer_frac_exact_min": 1.0, "lp": 0.0}
+    for b, s in enumerate(seqs):
+        rows = slice(int(cu[b]), int(cu[b + 1]))
+        pos = np.arange(len(s))
+        assert np.array_equal(D[0][rows], W["embed"][np.asarray(s)])
+        for l in range(L_):
+            r_in = D[l][rows]
+            want = omodel.layer(W["layers"][l], shape, r_in, pos)
+            got = D[l + 1][rows]
+            upd = np.abs(want - r_in)
+            bf16_close(got, want, ulps=1, frac_exact=0.8, atol=2.0 ** -4 * upd + 1e-6)
+            worst["layer_max_rel_update"] = max(worst["layer_max_rel_update"],
+                                                float(np.max(np.abs(got - want) / (upd + 1e-3))))
+            worst["layer_frac_exact_min"] = min(worst["layer_frac_exact_min"], float(np.mean(got == want)))
+        xf = ops.rmsnorm(D[L_][rows], W["final_norm"], shape.eps)[0]
+        bf16_close(D[L_ + 1][rows], xf, ulps=1, frac_exact=0.97)
+        logits = ops.linear(D[L_ + 1][rows], W["lm_head"], "fp32")
+        want_lp = ops.logprob(logits, targets[b])
+        e = float(np.max(np.abs(lp[rows] - want_lp)))
+        worst["lp"] = max(worst["lp"], e)
+        assert e < 1e-4, e
+    print("anchored parity", worst)
+    return worst
 
 
 def _decoder(shape, seed, max_pos, w_std=0.05):
@@ -87,7 +146,8 @@ def test_small_decoder_rollout_equals_recompute_and_oracle():
     W = omodel.weights_to_f32(wb)
     for b in range(5):
         _, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
-        assert np.max(np.abs(lp_g[b].cpu().numpy() - want)) < 5e-3
+        e2e_close(lp_g[b].cpu().numpy(), want)
+    anchored_parity(dec, wb, shape, [np.concatenate([prompts[b], gens[b][:-1]]) for b in range(5)])
 
 
 def test_gqa_decoder_rollout_equals_recompute_long_context():
@@ -107,7 +167,8 @@ def test_gqa_decoder_rollout_equals_recompute_long_context():
     assert same_bits(lp_t, lp)
     W = omodel.weights_to_f32(wb)
     _, want, _ = omodel.score_generation(W, shape, prompts[0], gens[0])
-    assert np.max(np.abs(lp[0].cpu().numpy() - want)) < 5e-3
+    e2e_close(lp[0].cpu().numpy(), want)
+    anchored_parity(dec, wb, shape, [np.concatenate([prompts[b], gens[b][:-1]]) for b in (0, 2)], seed=3)
 
 
 @pytest.mark.slow
@@ -142,7 +203,12 @@ def test_c2_dense_decoder_diff_zero_all_schedules():
         assert s == {"max": 0.0, "mean": 0.0, "std": 0.0, "k3": 0.0}, s
         assert same_bits(lt, lp)
     W = omodel.weights_to_f32(wb)
+    errs = []
     for b in (0, 5, 10, 15):
         _, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
-        assert np.max(np.abs(lp[b].cpu().numpy() - want)) < 5e-3
+        errs.append(e2e_close(lp[b].cpu().numpy(), want))
+    errs = np.concatenate(errs)
+    print("C2 free-running oracle error: max %.2e mean %.2e p99 %.2e" % (errs.max(), errs.mean(),
+                                                                         np.quantile(errs, 0.99)))
+    anchored_parity(dec, wb, shape, [np.concatenate([prompts[b], gens[b][:-1]]) for b in (0, 5, 10, 15)], seed=4)
     assert bi.bi_device_status() == 0

@@ -72,12 +72,15 @@ def test_gemm_bf16_and_fp32_parity(M, N, K):
     A, W = dev_bf16(ab), dev_bf16(wb)
     C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     bi.bi_gemm(A, M, K, W, N, C)
-    bf16_close(host_f32(C), ops.linear(af, wf, "bf16"), ulps=1, frac_exact=0.97)
+    # fp32 dot products in a different order differ by a small multiple of
+    # 2^-24 * sum|a||w|; after rounding both to bf16 the gap is at most one bf16
+    # ulp plus that amount.
+    absdot = np.abs(af) @ np.abs(wf).T
+    bf16_close(host_f32(C), ops.linear(af, wf, "bf16"), ulps=1, frac_exact=0.97, atol=1e-5 * absdot)
     C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
     bi.bi_gemm(A, M, K, W, N, C32, bi.BI_DTYPE_FP32)
     want = ops.linear(af, wf, "fp32")
-    scale = np.sqrt(np.abs(af) @ np.abs(wf).T ** 2 + 1e-30)
-    assert np.max(np.abs(host_f32(C32) - want) / (np.abs(af) @ np.abs(wf).T + 1e-30)) < 1e-5, scale.shape
+    assert np.max(np.abs(host_f32(C32) - want) / (absdot + 1e-30)) < 1e-5
 
 
 @pytest.mark.parametrize("M,F,K", [(3, 1408, 512), (200, 64, 128), (129, 5632, 256)])
@@ -88,7 +91,8 @@ def test_gemm_swiglu_epilogue(M, F, K):
     C = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
     bi.bi_gemm(dev_bf16(ab), M, K, dev_bf16(wb), 2 * F, C, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
     want = ops.silu_mul(ops.linear(af, wf[:F]), ops.linear(af, wf[F:]))
-    bf16_close(host_f32(C), want, ulps=2, frac_exact=0.9, atol=1e-6)
+    absdot = np.maximum(np.abs(af) @ np.abs(wf[:F]).T, np.abs(af) @ np.abs(wf[F:]).T)
+    bf16_close(host_f32(C), want, ulps=2, frac_exact=0.9, atol=2e-2 * absdot * 2.0 ** -7)
 
 
 @pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408)])
