@@ -192,15 +192,19 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def timed(e, k, keep):
+    def timed(e, k, keep, tag):
         times = []
         for i in range(k):
             flush.zero_()
             s0 = torch.cuda.Event(enable_timing=True)
             s1 = torch.cuda.Event(enable_timing=True)
+            if i == 0:
+                torch.cuda.nvtx.range_push(f"step_{tag}")   # lets ncu capture one whole step
             s0.record(stream)
             ids, lp_r, lp_t = e.run(prompt_dev)
             s1.record(stream)
+            if i == 0:
+                torch.cuda.nvtx.range_pop()
             if keep is not None:
                 keep.append((ids.clone(), lp_r.clone(), lp_t.clone()))
             times.append((s0, s1))
@@ -227,8 +231,8 @@ def run_ours(args):
     barrier()
     with Clocks(os.path.join(ROOT, "gpurun_out", "clocks_bench.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
                 else "/tmp/clocks_bench.csv") as ck:
-        t_inv = timed(ep, args.steps, results)
-        t_fast = timed(ep_fast, args.steps, None)
+        t_inv = timed(ep, args.steps, results, "invariant")
+        t_fast = timed(ep_fast, args.steps, None, "fast")
     barrier()
     clocks = ck.summary()
     ms_inv = sum(t_inv) / len(t_inv)

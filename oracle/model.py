@@ -36,11 +36,12 @@ def weights_to_f32(w_bits: dict) -> dict:
     return out
 
 
-def layer(lw: dict, shape, r, pos):
+def layer(lw: dict, shape, r, pos, return_parts: bool = False):
     """One decoder layer on the residual stream r [L, d] of ONE sequence whose
     rows sit at positions ``pos`` (0 .. L-1, every earlier key is in r).
     Returns the residual stream after the layer, bf16(r + attn + ffn) with the
-    two adds rounded separately."""
+    two adds rounded separately (and, with ``return_parts``, the attention
+    output projection o and the FFN output dn that were added)."""
     L = r.shape[0]
     hq, hkv, hd, F = shape.n_heads_q, shape.n_heads_kv, shape.head_dim, shape.ffn
     x, _ = ops.rmsnorm(r, lw["attn_norm"], shape.eps)
@@ -56,7 +57,8 @@ def layer(lw: dict, shape, r, pos):
     g = ops.linear(x, lw["w13"][:F])
     u = ops.linear(x, lw["w13"][F:])
     dn = ops.linear(ops.silu_mul(g, u), lw["w2"])
-    return round_bf16(r + dn)
+    out = round_bf16(r + dn)
+    return (out, o, dn) if return_parts else out
 
 
 def hidden_states(w: dict, shape, tokens, return_layers: bool = False):

@@ -59,10 +59,18 @@ def anchored_parity(dec, wb, shape, seqs, seed=0):
         assert np.array_equal(D[0][rows], W["embed"][np.asarray(s)])
         for l in range(L_):
             r_in = D[l][rows]
-            want = omodel.layer(W["layers"][l], shape, r_in, pos)
+            want, o, dn = omodel.layer(W["layers"][l], shape, r_in, pos, return_parts=True)
             got = D[l + 1][rows]
-            upd = np.abs(want - r_in)
-            bf16_close(got, want, ulps=1, frac_exact=0.8, atol=2.0 ** -4 * upd + 1e-6)
+            # two residual roundings (r + o, then + dn) may each flip by one ulp of
+            # the residual; o and dn carry rounding flips of their dot-product
+            # inputs, i.e. errors on the scale of their row's typical size.
+            # (Checked on the CPU: the oracle's fp64-accumulation variant and a
+            # bf16-P attention variant stay below half of this bound; a 5% error
+            # in the attention scale exceeds it.)
+            upd = np.abs(o) + np.abs(dn)
+            rms = np.sqrt(np.mean(o.astype(np.float64) ** 2, -1, keepdims=True)) + \
+                np.sqrt(np.mean(dn.astype(np.float64) ** 2, -1, keepdims=True))
+            bf16_close(got, want, ulps=2, frac_exact=0.8, atol=2.0 ** -5 * (upd + rms) + 1e-6)
             worst["layer_max_rel_update"] = max(worst["layer_max_rel_update"],
                                                 float(np.max(np.abs(got - want) / (upd + 1e-3))))
             worst["layer_frac_exact_min"] = min(worst["layer_frac_exact_min"], float(np.mean(got == want)))
