@@ -165,6 +165,32 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
                        size_t ws_bytes, void* out, int mode, void* stream);
 size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ctx, int kv_split);
 
+/* Same computation and kernels as bi_attention (bitwise the same output), for
+ * callers that cannot provide a device workspace: code that must not allocate
+ * device memory on its hot path (a serving loop whose memory is reserved up
+ * front, an allocator owned by another framework that this code cannot call),
+ * plugins that a host application gives no scratch buffer, or runtimes with a
+ * fixed memory budget.  The pages have no counterpart for this entry point.
+ *  - The split partials go to a scratch array compiled into the library, 32 MiB
+ *    on every GPU that loads the library, held until the process exits.  A call
+ *    whose partials, T * Hq * ceil(max_ctx / split) * (hd + 2) * 4 bytes, exceed
+ *    32 MiB returns BI_ERR_INVALID_ARG with the sizes in bi_last_error().
+ *  - It allocates nothing: no cudaMalloc / cudaFree, no library allocator.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array and the array keeps the last
+ *    call's contents; nothing in it needs to start at zero, because every
+ *    partial that the merge reads is written earlier in the same call.  Calls
+ *    that may run at the same time on the GPU (different streams, or several
+ *    host threads) race on the array: serialise them.
+ * Arguments are those of bi_attention without the workspace. */
+bi_status bi_attention_static_scratch(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                                      const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv,
+                                      int hd, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                      int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale,
+                                      void* out, int mode, void* stream);
+
 /* ---------------------------------------------------------- embed / logprob
  * Row gather: out[t] = table[ids[t]] (bf16 [V, d] -> bf16 [T, d]).  Ids outside
  * [0, V) write zeros and record BI_ERR_DEVICE_CHECK. */

@@ -18,6 +18,8 @@
 //   * partials (m, l, acc) are merged per row in ascending split order.
 // A decode row therefore reproduces its prefill row exactly.
 #include <algorithm>
+#include <mutex>
+#include <string>
 
 #include "common.cuh"
 
@@ -477,3 +479,62 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
 }
 
 }  // extern "C"
+
+// ------------------------------------------------- attention, library scratch
+// For callers that cannot hand the library a workspace: the split partials go
+// to a fixed array that lives in this module on every device that loads it.
+namespace bi {
+
+constexpr size_t kAttnStaticScratchBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_attn_static_scratch[kAttnStaticScratchBytes];
+
+// Device address of the array on the current device, looked up once per device.
+static bi_status attn_static_scratch_addr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(BI_ERR_CUDA, std::string("bi_attention_static_scratch: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(BI_ERR_CUDA, "bi_attention_static_scratch: device index out of range");
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(BI_ERR_CUDA, std::string("bi_attention_static_scratch: cudaGetSymbolAddress failed: ") +
+                                   cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return BI_OK;
+}
+
+}  // namespace bi
+
+extern "C" bi_status bi_attention_static_scratch(const void* q, int64_t T, const int32_t* piece_seq,
+                                                 const int32_t* piece_row0, const int32_t* piece_pos0, int64_t P,
+                                                 int64_t max_q_len, int Hq, int Hkv, int hd, const void* k_cache,
+                                                 const void* v_cache, const int32_t* block_table,
+                                                 int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split,
+                                                 float scale, void* out, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
+  if (T == 0 || P == 0) return BI_OK;
+  BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  BI_REQUIRE(hd > 0 && kv_split >= 64 && kv_split % 64 == 0 && max_ctx > 0 && max_q_len > 0,
+             "bad head_dim / kv_split / max_ctx / max_q_len");
+  // the partials this call needs, computed the way bi_attention sizes them
+  const int split = choose_split(mode, kv_split, P, max_q_len, Hkv, Hq / Hkv, max_ctx);
+  const size_t per = (size_t)T * Hq * n_splits(max_ctx, split);
+  const size_t need = per * hd * sizeof(float) + per * 2 * sizeof(float);
+  if (need > kAttnStaticScratchBytes)
+    return fail(BI_ERR_INVALID_ARG, "bi_attention_static_scratch: this call needs " + std::to_string(need) +
+                                        " bytes of split partials but the static scratch array holds " +
+                                        std::to_string(kAttnStaticScratchBytes) +
+                                        " bytes; use bi_attention with a caller workspace");
+  void* scratch = nullptr;
+  BI_TRY(attn_static_scratch_addr(&scratch));
+  return bi_attention(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,
+                      block_table, max_blocks_per_seq, max_ctx, kv_split, scale, scratch, kAttnStaticScratchBytes, out,
+                      mode, stream);
+}
