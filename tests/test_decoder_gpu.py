@@ -66,11 +66,15 @@ def anchored_parity(dec, wb, shape, seqs, seed=0):
             # inputs, i.e. errors on the scale of their row's typical size.
             # (Checked on the CPU: the oracle's fp64-accumulation variant and a
             # bf16-P attention variant stay below half of this bound; a 5% error
-            # in the attention scale exceeds it.)
+            # in the attention scale exceeds it.)  The kernel rounds P to bf16
+            # before P.V; the oracle keeps it fp32.  On the CPU that one change
+            # leaves only about a third of layer-0 outputs bit-equal (0.34 on the
+            # dense-decoder workload, rising to 0.67 by layer 3), so the
+            # bit-equal floor here is 0.25.
             upd = np.abs(o) + np.abs(dn)
             rms = np.sqrt(np.mean(o.astype(np.float64) ** 2, -1, keepdims=True)) + \
                 np.sqrt(np.mean(dn.astype(np.float64) ** 2, -1, keepdims=True))
-            bf16_close(got, want, ulps=2, frac_exact=0.8, atol=2.0 ** -5 * (upd + rms) + 1e-6)
+            bf16_close(got, want, ulps=2, frac_exact=0.25, atol=2.0 ** -5 * (upd + rms) + 1e-6)
             worst["layer_max_rel_update"] = max(worst["layer_max_rel_update"],
                                                 float(np.max(np.abs(got - want) / (upd + 1e-3))))
             worst["layer_frac_exact_min"] = min(worst["layer_frac_exact_min"], float(np.mean(got == want)))
