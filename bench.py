@@ -338,8 +338,48 @@ def roofline_probe(dec, ep, args):
             "note": "weights are L2-resident across decode steps (58.5 MB model < 129 MB L2)"}
 
 
+def run_kernel_case(name: str, reps: int):
+    """Launch one kernel of the step at its step shape `reps` times (profiling aid)."""
+    import torch
+    import invariant_forward_policy_gb300 as bi
+    torch.manual_seed(0)
+    dev = torch.device("cuda")
+    if name in ("gemm_decode_qkv", "gemm_decode_lm_head", "gemm_prefill"):
+        M, N, K, dt = {"gemm_decode_qkv": (16, 1536, 512, bi.BI_DTYPE_BF16),
+                       "gemm_decode_lm_head": (16, 32000, 512, bi.BI_DTYPE_FP32),
+                       "gemm_prefill": (8192, 5632 * 2, 2048, bi.BI_DTYPE_BF16)}[name]
+        A = (0.5 * torch.randn((M, K), device=dev)).to(torch.bfloat16)
+        W = (0.02 * torch.randn((N, K), device=dev)).to(torch.bfloat16)
+        C = torch.empty((M, N), device=dev, dtype=torch.float32 if dt == bi.BI_DTYPE_FP32 else torch.bfloat16)
+        for _ in range(reps):
+            bi.bi_gemm(A, M, K, W, N, C, dt)
+    elif name == "attention_decode":
+        B, Hq, Hkv, hd, ctx = 16, 8, 8, 64, 700
+        max_blk = -(-ctx // 64)
+        kc = (0.5 * torch.randn((B * max_blk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+        vc = (0.5 * torch.randn((B * max_blk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+        bt = torch.arange(B * max_blk, dtype=torch.int32, device=dev).view(B, max_blk)
+        q = (0.5 * torch.randn((B, Hq, hd), device=dev)).to(torch.bfloat16)
+        seq = torch.arange(B, dtype=torch.int32, device=dev)
+        row0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        pos0 = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
+        out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, ctx, 512), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, ctx, 512, 0.125, ws, out)
+    else:
+        raise SystemExit(f"unknown kernel case {name}")
+    torch.cuda.synchronize()
+    assert bi.bi_device_status() == 0
+    print(json.dumps({"kernel_case": name, "reps": reps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel-case", default=None,
+                    help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
+                         "attention_decode) and exit; for profiling")
+    ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
@@ -347,6 +387,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args.kernel_case, args.reps)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

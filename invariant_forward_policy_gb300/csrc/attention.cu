@@ -27,6 +27,8 @@ namespace bi {
 
 // ------------------------------------------------------------------ RoPE table
 __global__ void rope_table_kernel(float* table, int64_t max_pos, int hd, double theta) {
+  pdl_trigger();
+  pdl_wait();
   const int half = hd / 2;
   const int64_t total = max_pos * half;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -52,6 +54,8 @@ __global__ void rope_kv_write_kernel(const __nv_bfloat16* __restrict__ qkv, Piec
                                      const int32_t* __restrict__ block_table, int64_t max_blk, int64_t n_blocks,
                                      __nv_bfloat16* __restrict__ q_out, __nv_bfloat16* __restrict__ k_cache,
                                      __nv_bfloat16* __restrict__ v_cache, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int p = blockIdx.y;
   const int i = blockIdx.x;
   const int row0 = pm.row0[p];
@@ -137,12 +141,16 @@ struct AttnArgs {
 constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
 constexpr int kKeys = 64;   // keys per tile = cache block
 
-template <int HD>
+// STAGES = depth of the cp.async ring of (K, V) tiles.  It changes only when
+// loads are issued, never the arithmetic, so every depth gives the same bits.
+template <int HD, int STAGES>
 __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
   extern __shared__ __align__(128) uint8_t smem[];
   // [stage][K|V][64][HD] bf16, chunk-swizzled
+  pdl_trigger();
+  pdl_wait();
   const int p = blockIdx.y;
   const int kvh = blockIdx.z % a.Hkv;
   const int s = blockIdx.z / a.Hkv;
@@ -215,15 +223,17 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  load_tile(0, 0);
+  // keep STAGES - 1 tiles in flight; one commit group per tile (empty past the end)
+#pragma unroll
+  for (int t = 0; t < STAGES - 1; ++t) {
+    if (t < n_tiles) load_tile(t, t);
+    else cp_async_commit();
+  }
   for (int t = 0; t < n_tiles; ++t) {
-    const int stage = t & 1;
-    if (t + 1 < n_tiles) {
-      load_tile(t + 1, stage ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int stage = t % STAGES;
+    if (t + STAGES - 1 < n_tiles) load_tile(t + STAGES - 1, (t + STAGES - 1) % STAGES);
+    else cp_async_commit();
+    cp_async_wait<STAGES - 1>();
     __syncthreads();
     const uint32_t sk = smem_u32(smem + stage * 2 * TILE_BYTES);
     const uint32_t sv = sk + TILE_BYTES;
@@ -325,6 +335,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 __global__ void attention_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                        PieceMeta pm, int Hq, int hd, int nsplit, int split,
                                        __nv_bfloat16* __restrict__ out, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int p = blockIdx.y;
   const int i = blockIdx.x;
   const int row0 = pm.row0[p];
@@ -351,7 +363,20 @@ __global__ void attention_merge_kernel(const float* __restrict__ part_o, const f
   }
 }
 
-static int attn_smem_bytes(int hd) { return 2 * 2 * kKeys * hd * 2; }
+static int attn_smem_bytes(int hd, int stages) { return stages * 2 * kKeys * hd * 2; }
+
+template <int HD, int STAGES>
+static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t st) {
+  const int smem = attn_smem_bytes(HD, STAGES);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [smem] {
+    attr_err = cudaFuncSetAttribute(attention_kernel<HD, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
+  return launched(launch_pdl(attention_kernel<HD, STAGES>, grid, dim3(128), smem, st, args), "attention_kernel");
+}
 
 // Positions per split: the fixed kv_split, or (BI_FAST) a size chosen from the
 // batch so that the decode grid fills the GPU (flash-decoding heuristic).
@@ -377,8 +402,9 @@ bi_status bi_rope_table(float* rope_table, int64_t max_pos, int hd, double theta
   BI_REQUIRE(max_pos > 0 && hd > 0 && hd % 2 == 0, "bad shape");
   const int64_t total = max_pos * (hd / 2);
   const int blocks = (int)std::min<int64_t>(cdiv(total, 256), 4096);
-  rope_table_kernel<<<blocks, 256, 0, as_stream(stream)>>>(rope_table, max_pos, hd, theta);
-  return check_launch("bi_rope_table");
+  return launched(launch_pdl(rope_table_kernel, dim3(blocks), dim3(256), 0, as_stream(stream), rope_table, max_pos, hd,
+                             theta),
+                  "bi_rope_table");
 }
 
 bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
@@ -396,11 +422,12 @@ bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq,
   BI_REQUIRE(max_blocks_per_seq > 0 && n_blocks > 0, "bad cache shape");
   PieceMeta pm{piece_seq, piece_row0, piece_pos0};
   dim3 grid((unsigned)max_q_len, (unsigned)P);
-  rope_kv_write_kernel<<<grid, 128, 0, as_stream(stream)>>>(
-      static_cast<const __nv_bfloat16*>(qkv), pm, Hq, Hkv, hd, rope_table, max_pos, block_table, max_blocks_per_seq,
-      n_blocks, static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(k_cache),
-      static_cast<__nv_bfloat16*>(v_cache), device_status_ptr());
-  return check_launch("bi_rope_kv_write");
+  return launched(launch_pdl(rope_kv_write_kernel, grid, dim3(128), 0, as_stream(stream),
+                             static_cast<const __nv_bfloat16*>(qkv), pm, Hq, Hkv, hd, rope_table, max_pos, block_table,
+                             max_blocks_per_seq, n_blocks, static_cast<__nv_bfloat16*>(q_out),
+                             static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache),
+                             device_status_ptr()),
+                  "bi_rope_kv_write");
 }
 
 size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ctx, int kv_split) {
@@ -459,23 +486,19 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   args.split = split;
   args.scale_log2 = scale * 1.4426950408889634f;
   dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
-  const int smem = attn_smem_bytes(hd);
   cudaStream_t st = as_stream(stream);
-  if (hd == 64) {
-    attention_kernel<64><<<grid, 128, smem, st>>>(args);
-  } else {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(attention_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      attr = true;
-    }
-    attention_kernel<128><<<grid, 128, smem, st>>>(args);
-  }
-  BI_TRY(check_launch("attention_kernel"));
+  // a query tile that fits one warp (decode steps) is latency bound: keep more
+  // key tiles in flight; larger tiles keep two so that more CTAs share an SM
+  const bool deep = max_q_len * group <= 16;
+  if (hd == 64)
+    BI_TRY(deep ? launch_attention<64, 8>(args, grid, st) : launch_attention<64, 2>(args, grid, st));
+  else
+    BI_TRY(deep ? launch_attention<128, 4>(args, grid, st) : launch_attention<128, 2>(args, grid, st));
   dim3 mgrid((unsigned)max_q_len, (unsigned)P);
-  attention_merge_kernel<<<mgrid, 256, 0, st>>>(part_o, part_ml, args.pm, Hq, hd, (int)ns, split,
-                                               static_cast<__nv_bfloat16*>(out), args.status);
-  return check_launch("attention_merge_kernel");
+  return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(256), 0, st, (const float*)part_o,
+                             (const float*)part_ml, args.pm, Hq, hd, (int)ns, split, static_cast<__nv_bfloat16*>(out),
+                             args.status),
+                  "attention_merge_kernel");
 }
 
 }  // extern "C"

@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "../../include/bi.h"
 
@@ -31,9 +32,9 @@ bi_status check_launch(const char* what);
     if (!(cond)) return ::bi::fail(BI_ERR_UNSUPPORTED_SHAPE, std::string(__func__) + ": " + (msg)); \
   } while (0)
 
-#define BI_TRY(expr)                                                             \
+#define BI_TRY(...)                                                              \
   do {                                                                           \
-    bi_status _st = (expr);                                                      \
+    bi_status _st = (__VA_ARGS__);                                               \
     if (_st != BI_OK) return _st;                                                \
   } while (0)
 
@@ -48,13 +49,59 @@ int num_sms();
 enum DeviceCode : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 int* device_status_ptr();  // device address of the status word (current device)
 
+// Internal launchers shared between translation units (same kernels as the
+// public entry points, with a row indirection the model driver uses).
+// RMSNorm of rows idx[0..rows) of x / residual into the compact y[0..rows).
+bi_status rmsnorm_rows(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d, float eps,
+                       const int32_t* idx, void* stream);
+// Logprob / argmax of each logits row, written to out index dst[row] (dst may be NULL).
+bi_status logprob_gather_to(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
+                            int32_t* argmax_out, const int32_t* dst, int mode, void* workspace, size_t ws_bytes,
+                            void* stream);
+
 // TMA descriptor encode (driver entry point looked up through the runtime).
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool swizzle128);
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while its predecessor in the stream is still finishing; it must execute
+// pdl_wait() (below) before touching anything the predecessor writes or reads.
+// Every kernel of this library calls pdl_trigger() and pdl_wait() in all of its
+// CTAs, so completion stays transitive along the stream.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Status of a launch: its own return code, then the runtime's sticky error.
+inline bi_status launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(BI_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+  }
+  return check_launch(what);
+}
+
 // ---------------------------------------------------------------- device side
 #define BI_DEV __device__ __forceinline__
+
+// Let the next kernel in the stream start its launch (its CTAs then wait in pdl_wait).
+BI_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding kernel has completed and its memory is visible
+// (returns at once when the kernel was launched without the attribute).
+BI_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Bounded waits give up after this many nanoseconds (global timer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

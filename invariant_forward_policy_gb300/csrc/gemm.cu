@@ -69,10 +69,12 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* consumed = abort_flag + 1;
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tile = blockIdx.x, m_tile = blockIdx.y, split = blockIdx.z;
   int expert = 0;
   if (args.tile_expert) {
+    pdl_wait();  // the tile owner map comes from the preceding kernel
     expert = args.tile_expert[m_tile];
     if (expert < 0) return;  // whole CTA leaves before touching barriers or TMEM
   }
@@ -107,8 +109,27 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer
     const int wbase = expert * args.w_rows_per_expert;
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
+    auto load_w = [&](int kb, int s) {
+      const int kc = (kb0 + kb) * kBK;
+      if (kSwiglu) {
+        const int j0 = n_tile * (BN / 2);
+        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
+        tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc, wbase + args.up_offset + j0);
+      } else {
+        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
+      }
+    };
+    // The weights are not written by the preceding kernel: fetch the first
+    // stages' weight tiles while it finishes, then wait for it before reading A.
+    const int pre = nk < kStages ? nk : kStages;
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
+      load_w(kb, kb);
+    }
+    pdl_wait();
+    for (int kb = 0; kb < pre; ++kb) tma_load_2d(sA + kb * kATileBytes, &tmA, &full[kb], (kb0 + kb) * kBK, m0);
+    int issued = pre;
+    for (int kb = pre; kb < nk; ++kb) {
       const int s = kb % kStages;
       const uint32_t ph = (kb / kStages) & 1;
       if (!mbar_wait(&empty[s], ph ^ 1) || *abort_flag) {
@@ -117,16 +138,8 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
         break;
       }
       mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-      const int kc = (kb0 + kb) * kBK;
-      tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], kc, m0);
-      if (kSwiglu) {
-        const int j0 = n_tile * (BN / 2);
-        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
-        tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc,
-                    wbase + args.up_offset + j0);
-      } else {
-        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
-      }
+      tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], (kb0 + kb) * kBK, m0);
+      load_w(kb, s);
       ++issued;
     }
     if (*abort_flag) {
@@ -262,6 +275,8 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
 template <int EPI>
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int n_out, int ldp,
                                      void* C) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t total = (int64_t)M * n_out;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t m = i / n_out;
@@ -294,8 +309,7 @@ static bi_status launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUt
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return fail(BI_ERR_CUDA, std::string("gemm smem attribute: ") + cudaGetErrorString(attr_err));
-  gemm_tc_kernel<BN, EPI><<<grid, 128, smem, st>>>(a, b, b2, args);
-  return check_launch("gemm_tc_kernel");
+  return launched(launch_pdl(gemm_tc_kernel<BN, EPI>, grid, dim3(128), smem, st, a, b, b2, args), "gemm_tc_kernel");
 }
 
 template <int EPI>
@@ -412,16 +426,11 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   if (splits > 1) {
     const int64_t total = g.M * n_out;
     const int blocks = (int)std::min<int64_t>(cdiv(total, 256), 4 * (int64_t)num_sms());
-    if (swiglu)
-      splitk_reduce_kernel<EPI_SWIGLU><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
-                                                                (int)g.n_rows_w, g.C);
-    else if (g.c_dtype == BI_DTYPE_FP32)
-      splitk_reduce_kernel<EPI_F32><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
-                                                             (int)g.n_rows_w, g.C);
-    else
-      splitk_reduce_kernel<EPI_BF16><<<blocks, 256, 0, st>>>(args.partial, splits, (int)g.M, (int)n_out,
-                                                              (int)g.n_rows_w, g.C);
-    BI_TRY(check_launch("splitk_reduce_kernel"));
+    auto* kern = swiglu ? splitk_reduce_kernel<EPI_SWIGLU>
+                        : (g.c_dtype == BI_DTYPE_FP32 ? splitk_reduce_kernel<EPI_F32> : splitk_reduce_kernel<EPI_BF16>);
+    BI_TRY(launched(launch_pdl(kern, dim3(blocks), dim3(256), 0, st, (const float*)args.partial, splits, (int)g.M,
+                               (int)n_out, (int)g.n_rows_w, g.C),
+                    "splitk_reduce_kernel"));
   }
   return BI_OK;
 }

@@ -15,6 +15,8 @@ namespace bi {
 
 __global__ void embed_kernel(const int32_t* __restrict__ ids, const __nv_bfloat16* __restrict__ table, int64_t V,
                              int64_t d, __nv_bfloat16* __restrict__ out, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t t = blockIdx.x;
   const int32_t id = ids[t];
   const bool ok = id >= 0 && id < V;
@@ -92,11 +94,14 @@ __device__ __forceinline__ LseState lse_block_reduce(LseState st) {
 
 __device__ __forceinline__ LseState lse_init() { return LseState{-INFINITY, 0.f, -INFINITY, 0x7fffffff}; }
 
-// One CTA per row (invariant path).
+// One CTA per row (invariant path).  Results go to index dst[row] (or row).
 template <int NT>
 __global__ void __launch_bounds__(NT) logprob_kernel(const float* __restrict__ logits, const int32_t* __restrict__ ids,
                                                      int64_t V, float* __restrict__ lp_out,
-                                                     int32_t* __restrict__ argmax_out, int* status) {
+                                                     int32_t* __restrict__ argmax_out, const int32_t* __restrict__ dst,
+                                                     int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const float4* x4 = reinterpret_cast<const float4*>(logits + row * V);
   const int64_t n4 = V / 4;
@@ -113,8 +118,9 @@ __global__ void __launch_bounds__(NT) logprob_kernel(const float* __restrict__ l
       }
     }
     const float xid = logits[row * V + id];
-    lp_out[row] = __fsub_rn(__fsub_rn(xid, st.m), logf(st.s));
-    if (argmax_out) argmax_out[row] = st.idx;
+    const int64_t o = dst ? (int64_t)dst[row] : row;
+    lp_out[o] = __fsub_rn(__fsub_rn(xid, st.m), logf(st.s));
+    if (argmax_out) argmax_out[o] = st.idx;
   }
 }
 
@@ -123,6 +129,8 @@ __global__ void __launch_bounds__(NT) logprob_kernel(const float* __restrict__ l
 template <int NT>
 __global__ void __launch_bounds__(NT) logprob_partial_kernel(const float* __restrict__ logits, int64_t V, int chunks,
                                                              LseState* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x / chunks;
   const int c = blockIdx.x % chunks;
   const int64_t n4 = V / 4;
@@ -137,7 +145,9 @@ __global__ void __launch_bounds__(NT) logprob_partial_kernel(const float* __rest
 
 __global__ void logprob_combine_kernel(const float* __restrict__ logits, const int32_t* __restrict__ ids, int64_t V,
                                        int chunks, const LseState* __restrict__ part, float* __restrict__ lp_out,
-                                       int32_t* __restrict__ argmax_out, int64_t T) {
+                                       int32_t* __restrict__ argmax_out, const int32_t* __restrict__ dst, int64_t T) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (row >= T) return;
   LseState st = part[row * chunks];
@@ -147,8 +157,9 @@ __global__ void logprob_combine_kernel(const float* __restrict__ logits, const i
     id = ids[row];
     if (id < 0 || id >= V) id = st.idx;
   }
-  lp_out[row] = __fsub_rn(__fsub_rn(logits[row * V + id], st.m), logf(st.s));
-  if (argmax_out) argmax_out[row] = st.idx;
+  const int64_t o = dst ? (int64_t)dst[row] : row;
+  lp_out[o] = __fsub_rn(__fsub_rn(logits[row * V + id], st.m), logf(st.s));
+  if (argmax_out) argmax_out[o] = st.idx;
 }
 
 static int fast_chunks(int64_t T, int64_t V) {
@@ -158,51 +169,33 @@ static int fast_chunks(int64_t T, int64_t V) {
   return (int)std::max<int64_t>(c, 1);
 }
 
+// One CTA: record the step, feed the sampled tokens back, advance positions and the step counter.
 __global__ void decode_advance_kernel(const int32_t* __restrict__ sampled, const float* __restrict__ lp,
                                       int32_t* __restrict__ tokens, int32_t* __restrict__ pos, int64_t B,
                                       int32_t* __restrict__ step_counter, int32_t* __restrict__ hist_ids,
                                       float* __restrict__ hist_lp, int64_t max_steps, int* status) {
-  const int64_t b = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   const int32_t step = *step_counter;
-  if (b < B) {
-    if (step >= 0 && step < max_steps) {
+  const bool in_range = step >= 0 && step < max_steps;
+  for (int64_t b = threadIdx.x; b < B; b += blockDim.x) {
+    if (in_range) {
       hist_ids[(int64_t)step * B + b] = sampled[b];
       hist_lp[(int64_t)step * B + b] = lp[b];
-    } else if (b == 0) {
-      report(status, DEV_BAD_INDEX);
     }
     tokens[b] = sampled[b];
     pos[b] = pos[b] + 1;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!in_range) report(status, DEV_BAD_INDEX);
+    *step_counter = step + 1;
+  }
 }
 
-__global__ void step_increment_kernel(int32_t* step_counter) { *step_counter += 1; }
-
-}  // namespace bi
-
-extern "C" {
-
-bi_status bi_embed(const int32_t* ids, int64_t T, const void* table, int64_t V, int64_t d, void* out, void* stream) {
-  using namespace bi;
-  BI_REQUIRE(T >= 0, "T < 0");
-  if (T == 0) return BI_OK;
-  BI_REQUIRE(ids && table && out, "null pointer");
-  BI_REQUIRE(V > 0 && d > 0 && d % 8 == 0, "d must be a multiple of 8");
-  BI_REQUIRE(aligned16(table) && aligned16(out), "pointers must be 16-byte aligned");
-  BI_REQUIRE(T <= 0x7fffffff, "T too large");
-  embed_kernel<<<(unsigned)T, 128, 0, as_stream(stream)>>>(ids, static_cast<const __nv_bfloat16*>(table), V, d,
-                                                           static_cast<__nv_bfloat16*>(out), device_status_ptr());
-  return check_launch("bi_embed");
-}
-
-size_t bi_logprob_workspace_size(int64_t T, int64_t V, int mode) {
-  if (mode != BI_FAST || T <= 0) return 0;
-  return (size_t)T * bi::fast_chunks(T, V) * sizeof(bi::LseState);
-}
-
-bi_status bi_logprob_gather(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
-                            int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes, void* stream) {
-  using namespace bi;
+bi_status logprob_gather_to(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
+                            int32_t* argmax_out, const int32_t* dst, int mode, void* workspace, size_t ws_bytes,
+                            void* stream) {
   BI_REQUIRE(T >= 0, "T < 0");
   if (T == 0) return BI_OK;
   BI_REQUIRE(logits && logprob_out, "null pointer");
@@ -216,17 +209,48 @@ bi_status bi_logprob_gather(const float* logits, const int32_t* ids, int64_t T, 
     BI_REQUIRE(workspace && ws_bytes >= (size_t)T * chunks * sizeof(LseState),
                "BI_FAST logprob needs workspace (bi_logprob_workspace_size)");
     auto* part = static_cast<LseState*>(workspace);
-    logprob_partial_kernel<256><<<(unsigned)(T * chunks), 256, 0, st>>>(logits, V, chunks, part);
-    BI_TRY(check_launch("logprob_partial_kernel"));
-    logprob_combine_kernel<<<(unsigned)cdiv(T, 128), 128, 0, st>>>(logits, ids, V, chunks, part, logprob_out,
-                                                                    argmax_out, T);
-    return check_launch("logprob_combine_kernel");
+    BI_TRY(launched(launch_pdl(logprob_partial_kernel<256>, dim3((unsigned)(T * chunks)), dim3(256), 0, st, logits,
+                               V, chunks, part),
+                    "logprob_partial_kernel"));
+    return launched(launch_pdl(logprob_combine_kernel, dim3((unsigned)cdiv(T, 128)), dim3(128), 0, st, logits, ids, V,
+                               chunks, (const LseState*)part, logprob_out, argmax_out, dst, T),
+                    "logprob_combine_kernel");
   }
   if (V <= 16384)
-    logprob_kernel<256><<<(unsigned)T, 256, 0, st>>>(logits, ids, V, logprob_out, argmax_out, device_status_ptr());
-  else
-    logprob_kernel<512><<<(unsigned)T, 512, 0, st>>>(logits, ids, V, logprob_out, argmax_out, device_status_ptr());
-  return check_launch("logprob_kernel");
+    return launched(launch_pdl(logprob_kernel<256>, dim3((unsigned)T), dim3(256), 0, st, logits, ids, V, logprob_out,
+                               argmax_out, dst, device_status_ptr()),
+                    "logprob_kernel");
+  return launched(launch_pdl(logprob_kernel<512>, dim3((unsigned)T), dim3(512), 0, st, logits, ids, V, logprob_out,
+                             argmax_out, dst, device_status_ptr()),
+                  "logprob_kernel");
+}
+
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_embed(const int32_t* ids, int64_t T, const void* table, int64_t V, int64_t d, void* out, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(T >= 0, "T < 0");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(ids && table && out, "null pointer");
+  BI_REQUIRE(V > 0 && d > 0 && d % 8 == 0, "d must be a multiple of 8");
+  BI_REQUIRE(aligned16(table) && aligned16(out), "pointers must be 16-byte aligned");
+  BI_REQUIRE(T <= 0x7fffffff, "T too large");
+  return launched(launch_pdl(embed_kernel, dim3((unsigned)T), dim3(128), 0, as_stream(stream), ids,
+                             static_cast<const __nv_bfloat16*>(table), V, d, static_cast<__nv_bfloat16*>(out),
+                             device_status_ptr()),
+                  "bi_embed");
+}
+
+size_t bi_logprob_workspace_size(int64_t T, int64_t V, int mode) {
+  if (mode != BI_FAST || T <= 0) return 0;
+  return (size_t)T * bi::fast_chunks(T, V) * sizeof(bi::LseState);
+}
+
+bi_status bi_logprob_gather(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
+                            int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes, void* stream) {
+  return bi::logprob_gather_to(logits, ids, T, V, logprob_out, argmax_out, nullptr, mode, workspace, ws_bytes, stream);
 }
 
 bi_status bi_decode_advance(const int32_t* sampled, const float* logprob, int32_t* tokens, int32_t* pos, int64_t B,
@@ -237,12 +261,9 @@ bi_status bi_decode_advance(const int32_t* sampled, const float* logprob, int32_
   if (B == 0) return BI_OK;
   BI_REQUIRE(sampled && logprob && tokens && pos && step_counter && hist_ids && hist_lp, "null pointer");
   BI_REQUIRE(max_steps > 0, "max_steps <= 0");
-  cudaStream_t st = as_stream(stream);
-  decode_advance_kernel<<<(unsigned)cdiv(B, 128), 128, 0, st>>>(sampled, logprob, tokens, pos, B, step_counter,
-                                                                 hist_ids, hist_lp, max_steps, device_status_ptr());
-  BI_TRY(check_launch("decode_advance_kernel"));
-  step_increment_kernel<<<1, 1, 0, st>>>(step_counter);
-  return check_launch("step_increment_kernel");
+  return launched(launch_pdl(decode_advance_kernel, dim3(1), dim3(256), 0, as_stream(stream), sampled, logprob, tokens,
+                             pos, B, step_counter, hist_ids, hist_lp, max_steps, device_status_ptr()),
+                  "decode_advance_kernel");
 }
 
 }  // extern "C"

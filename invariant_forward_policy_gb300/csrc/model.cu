@@ -50,6 +50,8 @@ struct DevMeta {
 
 __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ tokens,
                                  const int32_t* __restrict__ targets, DevMeta dm) {
+  pdl_trigger();
+  pdl_wait();
   if (blockIdx.x == 0) {
     for (int p = threadIdx.x; p < pm.n_pieces; p += blockDim.x) {
       dm.piece_seq[p] = pm.seq[p];
@@ -77,48 +79,30 @@ __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ 
   }
 }
 
-__global__ void decode_meta_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ pos, int B,
-                                   DevMeta dm) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b == 0) dm.piece_row0[B] = B;
-  if (b >= B) return;
-  dm.piece_seq[b] = b;
-  dm.piece_row0[b] = b;
-  dm.piece_pos0[b] = pos[b];
-  dm.ids[b] = tokens[b];
-  dm.logit_src[b] = b;
-  dm.logit_dst[b] = b;
-  dm.logit_tgt[b] = -1;
-}
-
-// Gather two bf16 row sets by an index list (final residual add + norm on logit rows only).
-__global__ void gather_rows2_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b,
-                                    const int32_t* __restrict__ src, int64_t d, __nv_bfloat16* __restrict__ oa,
-                                    __nv_bfloat16* __restrict__ ob) {
-  const int64_t j = blockIdx.x;
-  const int64_t r = src[j];
-  const uint4* pa = reinterpret_cast<const uint4*>(a + r * d);
-  const uint4* pb = reinterpret_cast<const uint4*>(b + r * d);
-  uint4* qa = reinterpret_cast<uint4*>(oa + j * d);
-  uint4* qb = reinterpret_cast<uint4*>(ob + j * d);
-  for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) {
-    qa[v] = pa[v];
-    qb[v] = pb[v];
+// Decode step metadata (one piece per sequence, one row each) fused with the
+// embedding gather of that row.
+__global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ pos, int B,
+                                    DevMeta dm, const __nv_bfloat16* __restrict__ table, int64_t V, int64_t d,
+                                    __nv_bfloat16* __restrict__ h, int* status) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const int32_t id = tokens[b];
+  if (threadIdx.x == 0) {
+    if (b == 0) dm.piece_row0[B] = B;
+    dm.piece_seq[b] = b;
+    dm.piece_row0[b] = b;
+    dm.piece_pos0[b] = pos[b];
+    dm.ids[b] = id;
+    dm.logit_src[b] = b;
+    dm.logit_dst[b] = b;
+    dm.logit_tgt[b] = -1;
   }
-}
-
-__global__ void scatter_results_kernel(const float* __restrict__ lp, const int32_t* __restrict__ am,
-                                       const int32_t* __restrict__ dst, int n, float* __restrict__ lp_out,
-                                       int32_t* __restrict__ sampled_out) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= n) return;
-  lp_out[dst[j]] = lp[j];
-  if (sampled_out) sampled_out[dst[j]] = am[j];
-}
-
-__global__ void copy_targets_kernel(const int32_t* __restrict__ tgt, int n, int32_t* __restrict__ out) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j < n) out[j] = tgt[j];
+  const bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) report(status, DEV_BAD_INDEX);
+  const uint4* src = reinterpret_cast<const uint4*>(table + (int64_t)(ok ? id : 0) * d);
+  uint4* dst = reinterpret_cast<uint4*>(h + (int64_t)b * d);
+  for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) dst[v] = ok ? src[v] : make_uint4(0, 0, 0, 0);
 }
 
 // ------------------------------------------------------------- workspace plan
@@ -185,6 +169,7 @@ static T* at(void* base, size_t off) {
 
 struct PassShape {
   int64_t rows, pieces, max_q_len, max_ctx, n_logit;
+  bool embedded;  // the embedding rows are already in the residual buffer
 };
 
 // The layer stack over the rows of one pass (identical for prefill and decode).
@@ -220,7 +205,7 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     return check_launch("dump copy");
   };
 
-  BI_TRY(bi_embed(at<int32_t>(ws, L.ids), T, m->embed, c.vocab, c.d, h, stream));
+  if (!ps.embedded) BI_TRY(bi_embed(at<int32_t>(ws, L.ids), T, m->embed, c.vocab, c.d, h, stream));
   BI_TRY(dump_copy(0, h));
   BI_TRY(bi_rmsnorm(h, nullptr, m->layers[0].attn_norm, x, T, c.d, c.eps, mode, stream));
   for (int64_t li = 0; li < c.n_layers; ++li) {
@@ -254,27 +239,17 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
   for (int64_t r0 = 0; r0 < ps.n_logit; r0 += Rm) {
     const int64_t R = std::min(Rm, ps.n_logit - r0);
     const int32_t* src = at<int32_t>(ws, L.logit_src) + r0;
-    void* hsel = at<void>(ws, L.hsel);
-    void* tsel = at<void>(ws, L.tsel);
     void* xsel = at<void>(ws, L.xsel);
     float* logits = at<float>(ws, L.logits);
-    gather_rows2_kernel<<<(unsigned)R, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h),
-                                                      static_cast<const __nv_bfloat16*>(tmp), src, c.d,
-                                                      static_cast<__nv_bfloat16*>(hsel),
-                                                      static_cast<__nv_bfloat16*>(tsel));
-    BI_TRY(check_launch("gather_rows2_kernel"));
-    BI_TRY(bi_rmsnorm(tsel, hsel, m->final_norm, xsel, R, c.d, c.eps, mode, stream));
+    // rows src[j] of (down-proj out + residual) -> final norm -> compact row j
+    BI_TRY(rmsnorm_rows(tmp, h, m->final_norm, xsel, R, c.d, c.eps, src, stream));
     BI_TRY(bi_gemm(xsel, R, c.d, m->lm_head, c.vocab, logits, BI_DTYPE_FP32, BI_EPI_NONE, mode, gws,
                    L.gemm_ws_bytes, stream));
     const int32_t* tgt = greedy ? nullptr : at<int32_t>(ws, L.logit_tgt) + r0;
-    float* lp = at<float>(ws, L.lp);
-    int32_t* am = at<int32_t>(ws, L.am);
-    BI_TRY(bi_logprob_gather(logits, tgt, R, c.vocab, lp, am, mode, L.lp_ws_bytes ? at<void>(ws, L.lp_ws) : nullptr,
-                             L.lp_ws_bytes, stream));
-    scatter_results_kernel<<<(unsigned)cdiv(R, 128), 128, 0, st>>>(lp, am, at<int32_t>(ws, L.logit_dst) + r0, (int)R,
-                                                                   logprob_out, sampled_out);
-    BI_TRY(check_launch("scatter_results_kernel"));
+    BI_TRY(logprob_gather_to(logits, tgt, R, c.vocab, logprob_out, sampled_out, at<int32_t>(ws, L.logit_dst) + r0,
+                             mode, L.lp_ws_bytes ? at<void>(ws, L.lp_ws) : nullptr, L.lp_ws_bytes, stream));
   }
+  (void)st;
   return BI_OK;
 }
 
@@ -423,8 +398,9 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
                at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids),
                at<int32_t>(workspace, L.logit_src), at<int32_t>(workspace, L.logit_dst),
                at<int32_t>(workspace, L.logit_tgt)};
-    pass_meta_kernel<<<(unsigned)cdiv(std::max<int64_t>(rows, 1), 256), 256, 0, st>>>(pm, tokens, target_ids, dm);
-    BI_TRY(check_launch("pass_meta_kernel"));
+    BI_TRY(launched(launch_pdl(pass_meta_kernel, dim3((unsigned)cdiv(std::max<int64_t>(rows, 1), 256)), dim3(256), 0,
+                               st, pm, tokens, target_ids, dm),
+                    "pass_meta_kernel"));
     BI_TRY(run_pass(m, workspace, L, ps, max_logit_rows, block_table, max_blocks_per_seq, k_cache, v_cache, n_blocks,
                     target_ids == nullptr, logprob_out, sampled_out, mode, stream));
   }
@@ -451,9 +427,11 @@ bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* p
              at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids), at<int32_t>(workspace, L.logit_src),
              at<int32_t>(workspace, L.logit_dst), at<int32_t>(workspace, L.logit_tgt)};
   const cudaStream_t st = as_stream(stream);
-  decode_meta_kernel<<<(unsigned)cdiv(B, 128), 128, 0, st>>>(tokens, pos, (int)B, dm);
-  BI_TRY(check_launch("decode_meta_kernel"));
-  PassShape ps{B, B, 1, max_ctx, B};
+  BI_TRY(launched(launch_pdl(decode_embed_kernel, dim3((unsigned)B), dim3(128), 0, st, tokens, pos, (int)B, dm,
+                             static_cast<const __nv_bfloat16*>(m->embed), m->cfg.vocab, m->cfg.d,
+                             at<__nv_bfloat16>(workspace, L.h), device_status_ptr()),
+                  "decode_embed_kernel"));
+  PassShape ps{B, B, 1, max_ctx, B, true};
   return run_pass(m, workspace, L, ps, B, block_table, max_blocks_per_seq, k_cache, v_cache, n_blocks, true,
                   logprob_out, sampled_out, mode, stream);
 }

@@ -21,6 +21,8 @@ namespace bi {
 // ------------------------------------------------------------------ router
 __global__ void route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids,
                                   float* __restrict__ weights) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t t = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -68,6 +70,8 @@ constexpr int kPermThreads = 1024;
 __global__ void __launch_bounds__(kPermThreads) expert_rank_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
                                                                    int32_t* __restrict__ rank,
                                                                    int32_t* __restrict__ counts, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int e = blockIdx.x;
   const int tid = threadIdx.x;
   const int64_t per = (n + kPermThreads - 1) / kPermThreads;
@@ -108,6 +112,8 @@ __global__ void __launch_bounds__(kPermThreads) expert_rank_kernel(const int32_t
 // Contiguous layout: expert offsets padded to 128 rows, and the tile owner map.
 __global__ void expert_offsets_kernel(const int32_t* __restrict__ counts, int E, int64_t max_tiles,
                                       int32_t* __restrict__ offsets, int32_t* __restrict__ tile_expert, int* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int32_t off[1025];
   if (threadIdx.x == 0) {
     int32_t o = 0;
@@ -138,6 +144,8 @@ __global__ void expert_offsets_kernel(const int32_t* __restrict__ counts, int E,
 __global__ void row_of_slot_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, int64_t n,
                                    const int32_t* __restrict__ offsets, int64_t capacity, int64_t max_rows,
                                    int32_t* __restrict__ row_of_slot, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= n) return;
   const int32_t e = ids[i];
@@ -155,12 +163,16 @@ __global__ void row_of_slot_kernel(const int32_t* __restrict__ ids, const int32_
 }
 
 __global__ void masked_tiles_kernel(int32_t* tile_expert, int64_t n_tiles, int64_t tiles_per_expert) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t < n_tiles) tile_expert[t] = (int32_t)(t / tiles_per_expert);
 }
 
 __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of_slot, int k,
                                   int64_t d, __nv_bfloat16* __restrict__ xp) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t pair = blockIdx.x;
   const int32_t row = row_of_slot[pair];
   if (row < 0) return;
@@ -172,6 +184,8 @@ __global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int
 // out[t] = bf16( sum_s w[t,s] * y[row(t,s)] ), slots in order, fp32.
 __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of_slot,
                                    const float* __restrict__ w, int k, int64_t d, __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t t = blockIdx.x;
   for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) {
     float acc[8];
@@ -201,6 +215,8 @@ __global__ void moe_combine_kernel(const __nv_bfloat16* __restrict__ y, const in
 // BI_FAST combine: fp32 atomics in arrival order (not deterministic).
 __global__ void moe_combine_atomic_kernel(const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ row_of_slot,
                                           const float* __restrict__ w, int k, int64_t d, float* __restrict__ acc) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t pair = blockIdx.x;
   const int32_t row = row_of_slot[pair];
   if (row < 0) return;
@@ -209,10 +225,14 @@ __global__ void moe_combine_atomic_kernel(const __nv_bfloat16* __restrict__ y, c
   for (int64_t i = threadIdx.x; i < d; i += blockDim.x) atomicAdd(dst + i, ws * bf2f(y[(int64_t)row * d + i]));
 }
 __global__ void zero_f32_kernel(float* p, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     p[i] = 0.f;
 }
 __global__ void f32_to_bf16_kernel(const float* p, int64_t n, __nv_bfloat16* out) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     out[i] = f2bf(p[i]);
 }
@@ -232,8 +252,7 @@ bi_status bi_moe_route_topk(const float* logits, int64_t T, int E, int k, int32_
   BI_REQUIRE_SHAPE(E >= 1 && E <= 64, "E must be in [1, 64]");
   BI_REQUIRE(k >= 1 && k <= E, "k must be in [1, E]");
   const int warps = 8;
-  route_topk_kernel<<<(unsigned)cdiv(T, warps), warps * 32, 0, as_stream(stream)>>>(logits, T, E, k, ids, weights);
-  return check_launch("bi_moe_route_topk");
+  return launched(launch_pdl(route_topk_kernel, dim3((unsigned)cdiv(T, warps)), dim3(warps * 32), 0, as_stream(stream), logits, T, E, k, ids, weights), "bi_moe_route_topk");
 }
 
 size_t bi_moe_permute_workspace_size(int64_t T, int k, int E) {
@@ -248,8 +267,7 @@ static bi_status permute_common(const int32_t* ids, int64_t T, int k, int E, voi
   BI_REQUIRE(E >= 1 && E <= 1024, "E must be in [1, 1024]");
   *rank = static_cast<int32_t*>(workspace);
   *counts = *rank + T * k;
-  expert_rank_kernel<<<E, kPermThreads, 0, st>>>(ids, T * k, E, *rank, *counts, device_status_ptr());
-  return check_launch("expert_rank_kernel");
+  return launched(launch_pdl(expert_rank_kernel, dim3(E), dim3(kPermThreads), 0, st, ids, T * k, E, *rank, *counts, device_status_ptr()), "expert_rank_kernel");
 }
 
 bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t max_rows, int32_t* row_of_slot,
@@ -263,12 +281,10 @@ bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t ma
   cudaStream_t st = as_stream(stream);
   int32_t *rank, *counts;
   BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
-  expert_offsets_kernel<<<1, 256, 0, st>>>(counts, E, max_rows / 128, expert_offsets, tile_expert,
-                                           device_status_ptr());
-  BI_TRY(check_launch("expert_offsets_kernel"));
-  row_of_slot_kernel<<<(unsigned)cdiv(T * k, 256), 256, 0, st>>>(ids, rank, T * k, expert_offsets, 0, max_rows,
-                                                                   row_of_slot, device_status_ptr());
-  return check_launch("row_of_slot_kernel");
+  BI_TRY(launched(launch_pdl(expert_offsets_kernel, dim3(1), dim3(256), 0, st, counts, E, max_rows / 128, expert_offsets, tile_expert,
+                                           device_status_ptr()), "expert_offsets_kernel"));
+  return launched(launch_pdl(row_of_slot_kernel, dim3((unsigned)cdiv(T * k, 256)), dim3(256), 0, st, ids, rank, T * k, expert_offsets, 0, max_rows,
+                                                                   row_of_slot, device_status_ptr()), "row_of_slot_kernel");
 }
 
 bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int64_t capacity, int32_t* row_of_slot,
@@ -282,11 +298,9 @@ bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int
   int32_t *rank, *counts;
   BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
   const int64_t n_tiles = E * capacity / 128;
-  masked_tiles_kernel<<<(unsigned)cdiv(n_tiles, 256), 256, 0, st>>>(tile_expert, n_tiles, capacity / 128);
-  BI_TRY(check_launch("masked_tiles_kernel"));
-  row_of_slot_kernel<<<(unsigned)cdiv(T * k, 256), 256, 0, st>>>(ids, rank, T * k, nullptr, capacity, E * capacity,
-                                                                   row_of_slot, device_status_ptr());
-  return check_launch("row_of_slot_kernel");
+  BI_TRY(launched(launch_pdl(masked_tiles_kernel, dim3((unsigned)cdiv(n_tiles, 256)), dim3(256), 0, st, tile_expert, n_tiles, capacity / 128), "masked_tiles_kernel"));
+  return launched(launch_pdl(row_of_slot_kernel, dim3((unsigned)cdiv(T * k, 256)), dim3(256), 0, st, ids, rank, T * k, nullptr, capacity, E * capacity,
+                                                                   row_of_slot, device_status_ptr()), "row_of_slot_kernel");
 }
 
 bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, int k, int64_t d, void* xp,
@@ -296,10 +310,9 @@ bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, in
   if (T == 0) return BI_OK;
   BI_REQUIRE(x && row_of_slot && xp, "null pointer");
   BI_REQUIRE(d % 8 == 0 && aligned16(x) && aligned16(xp), "d % 8 and 16-byte alignment required");
-  moe_gather_kernel<<<(unsigned)(T * k), 128, 0, as_stream(stream)>>>(static_cast<const __nv_bfloat16*>(x),
+  return launched(launch_pdl(moe_gather_kernel, dim3((unsigned)(T * k)), dim3(128), 0, as_stream(stream), static_cast<const __nv_bfloat16*>(x),
                                                                       row_of_slot, k, d,
-                                                                      static_cast<__nv_bfloat16*>(xp));
-  return check_launch("bi_moe_gather");
+                                                                      static_cast<__nv_bfloat16*>(xp)), "bi_moe_gather");
 }
 
 size_t bi_moe_combine_workspace_size(int64_t T, int64_t d, int mode) {
@@ -319,18 +332,14 @@ bi_status bi_moe_combine(const void* y, const int32_t* row_of_slot, const float*
     BI_REQUIRE(workspace && ws_bytes >= (size_t)T * d * sizeof(float), "BI_FAST combine needs workspace");
     float* acc = static_cast<float*>(workspace);
     const int blocks = (int)std::min<int64_t>(cdiv(T * d, 256), 8 * (int64_t)num_sms());
-    zero_f32_kernel<<<blocks, 256, 0, st>>>(acc, T * d);
-    BI_TRY(check_launch("zero_f32_kernel"));
-    moe_combine_atomic_kernel<<<(unsigned)(T * k), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y), row_of_slot,
-                                                                  w, k, d, acc);
-    BI_TRY(check_launch("moe_combine_atomic_kernel"));
-    f32_to_bf16_kernel<<<blocks, 256, 0, st>>>(acc, T * d, static_cast<__nv_bfloat16*>(out));
-    return check_launch("f32_to_bf16_kernel");
+    BI_TRY(launched(launch_pdl(zero_f32_kernel, dim3(blocks), dim3(256), 0, st, acc, T * d), "zero_f32_kernel"));
+    BI_TRY(launched(launch_pdl(moe_combine_atomic_kernel, dim3((unsigned)(T * k)), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(y), row_of_slot,
+                                                                  w, k, d, acc), "moe_combine_atomic_kernel"));
+    return launched(launch_pdl(f32_to_bf16_kernel, dim3(blocks), dim3(256), 0, st, acc, T * d, static_cast<__nv_bfloat16*>(out)), "f32_to_bf16_kernel");
   }
   const int thr = (int)std::min<int64_t>(256, std::max<int64_t>(32, d / 8));
-  moe_combine_kernel<<<(unsigned)T, thr, 0, st>>>(static_cast<const __nv_bfloat16*>(y), row_of_slot, w, k, d,
-                                                  static_cast<__nv_bfloat16*>(out));
-  return check_launch("bi_moe_combine");
+  return launched(launch_pdl(moe_combine_kernel, dim3((unsigned)T), dim3(thr), 0, st, static_cast<const __nv_bfloat16*>(y), row_of_slot, w, k, d,
+                                                  static_cast<__nv_bfloat16*>(out)), "bi_moe_combine");
 }
 
 size_t bi_moe_layer_workspace_size(int64_t T, int64_t d, int E, int k, int64_t F, int mode) {

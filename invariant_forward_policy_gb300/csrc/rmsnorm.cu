@@ -17,20 +17,25 @@ static int norm_threads(int64_t d) {
   return (int)((t + 31) / 32 * 32);
 }
 
+// Row r of y is the norm of row src(r) of x (+ residual), src(r) = idx ? idx[r] : r.
 template <bool kResidual>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
                                                       __nv_bfloat16* __restrict__ residual,
                                                       const __nv_bfloat16* __restrict__ gamma,
-                                                      __nv_bfloat16* __restrict__ y, int d, float eps) {
+                                                      __nv_bfloat16* __restrict__ y, int d, float eps,
+                                                      const int32_t* __restrict__ idx) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.x;
+  const int64_t src = idx ? (int64_t)idx[row] : row;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   const int nvec = d / 8;
   constexpr int kMaxVec = 8;  // d <= 16384 -> at most 8 vectors per thread with 256 threads
   uint4 sv[kMaxVec];
   float ss = 0.f;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
-  uint4* rr = reinterpret_cast<uint4*>(residual + row * d);
+  const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
+  uint4* rr = reinterpret_cast<uint4*>(residual + src * d);
 #pragma unroll
   for (int i = 0; i < kMaxVec; ++i) {
     const int v = tid + i * nthr;
@@ -95,11 +100,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   }
 }
 
-}  // namespace bi
-
-extern "C" bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d,
-                                float eps, int mode, void* stream) {
-  using namespace bi;
+bi_status rmsnorm_rows(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d, float eps,
+                       const int32_t* idx, void* stream) {
   BI_REQUIRE(rows >= 0, "rows < 0");
   if (rows == 0) return BI_OK;
   BI_REQUIRE(x && gamma && y, "null pointer");
@@ -107,15 +109,26 @@ extern "C" bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma
   BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y) && (!residual || aligned16(residual)),
              "pointers must be 16-byte aligned");
   BI_REQUIRE(rows <= 0x7fffffff, "rows too large");
-  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
   const int thr = norm_threads(d);
   auto* xp = static_cast<const __nv_bfloat16*>(x);
   auto* rp = static_cast<__nv_bfloat16*>(residual);
   auto* gp = static_cast<const __nv_bfloat16*>(gamma);
   auto* yp = static_cast<__nv_bfloat16*>(y);
+  cudaError_t e;
   if (residual)
-    rmsnorm_kernel<true><<<(unsigned)rows, thr, 0, as_stream(stream)>>>(xp, rp, gp, yp, (int)d, eps);
+    e = launch_pdl(rmsnorm_kernel<true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp, yp,
+                   (int)d, eps, idx);
   else
-    rmsnorm_kernel<false><<<(unsigned)rows, thr, 0, as_stream(stream)>>>(xp, rp, gp, yp, (int)d, eps);
-  return check_launch("bi_rmsnorm");
+    e = launch_pdl(rmsnorm_kernel<false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp, yp,
+                   (int)d, eps, idx);
+  return launched(e, "rmsnorm_kernel");
+}
+
+}  // namespace bi
+
+extern "C" bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d,
+                                float eps, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  return rmsnorm_rows(x, residual, gamma, y, rows, d, eps, nullptr, stream);
 }

@@ -85,6 +85,22 @@ class Decoder:
             ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
         return torch.from_numpy(ids.reshape(n_seq, max_blocks)).to(self.device)
 
+    def paged_block_table(self, ctx_lens, max_blocks: int, seed: int | None = None):
+        """Block table giving sequence b only ceil(ctx_lens[b] / 64) physical blocks
+        (entries past that are -1 and never touched), scattered over the cache by a
+        seeded permutation.  Returns (table [n_seq, max_blocks] int32, n_blocks)."""
+        need = [-(-int(n) // 64) for n in ctx_lens]
+        total = int(sum(need))
+        ids = np.arange(total, dtype=np.int32)
+        if seed is not None:
+            ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
+        tab = np.full((len(need), max_blocks), -1, dtype=np.int32)
+        o = 0
+        for b, n in enumerate(need):
+            tab[b, :n] = ids[o:o + n]
+            o += n
+        return torch.from_numpy(tab).to(self.device), total
+
     def workspace(self, max_tokens, max_pieces, max_ctx, max_logit_rows, mode=L.BI_INVARIANT) -> torch.Tensor:
         n = L.bi_forward_workspace_size(self.cfg, max_tokens, max_pieces, max_ctx, max_logit_rows, mode)
         return torch.empty(n, dtype=torch.uint8, device=self.device)
