@@ -13,80 +13,10 @@ from invariant_forward_policy_gb300.decoder import Decoder
 from oracle import model as omodel
 from oracle import ops
 from synthetic import C2, DecoderShape, make_decoder_weights, make_prompts
-from tests.gpu_util import bf16_close, host_f32, same_bits
+from tests.gpu_util import same_bits
+from tests.parity import anchored_parity, e2e_close
 
 pytestmark = pytest.mark.gpu
-
-# Free-running tolerance on the end-to-end logprob.  Two implementations of
-# the same numerical contract (fp32 accumulation, bf16 at the same boundaries)
-# that only sum in a different order already differ by up to ~8e-3 (mean
-# ~2e-3) on these models: the oracle against its own fp64-accumulation
-# variant on the dense-decoder workload gives max 7.5e-3, mean 2.2e-3, because
-# one-ulp bf16 flips in the residual stream propagate.  So the free-running
-# bound is max 2e-2 / mean 5e-3, and the strict check is the layer-anchored one
-# below (every layer from the GPU's own input; logprob from its final norm).
-E2E_MAX, E2E_MEAN = 2e-2, 5e-3
-
-
-def e2e_close(got, want):
-    err = np.abs(np.asarray(got, np.float64) - want)
-    assert err.max() < E2E_MAX and err.mean() < E2E_MEAN, (err.max(), err.mean())
-    return err
-
-
-def anchored_parity(dec, wb, shape, seqs, seed=0):
-    """Prefill `seqs` in one pass with the layer dump on, then check each layer
-    against the oracle applied to the GPU's own layer input, the final norm, and
-    the logprobs against the oracle's lm_head + log-softmax of the GPU's
-    final-norm rows.  Returns the worst errors seen."""
-    W = omodel.weights_to_f32(wb)
-    T = sum(len(s) for s in seqs)
-    L_ = shape.n_layers
-    mb = max(-(-len(s) // 64) for s in seqs)
-    cache = dec.alloc_cache(len(seqs) * mb)
-    bt = dec.block_table(len(seqs), mb, seed=seed)
-    dump = torch.zeros((L_ + 2, T, shape.d), dtype=torch.bfloat16, device="cuda")
-    rng = np.random.default_rng(seed)
-    targets = [rng.integers(0, shape.vocab, len(s)).astype(np.int32) for s in seqs]
-    lp, _, cu = dec.prefill(seqs, cache, bt, targets=targets, chunk=max(len(s) for s in seqs), max_tokens=T,
-                            max_logit_rows=T, dump=dump)
-    D = host_f32(dump)
-    lp = lp.cpu().numpy()
-    worst = {"layer_max_rel_update": 0.0, "layer_frac_exact_min": 1.0, "lp": 0.0}
-    for b, s in enumerate(seqs):
-        rows = slice(int(cu[b]), int(cu[b + 1]))
-        pos = np.arange(len(s))
-        assert np.array_equal(D[0][rows], W["embed"][np.asarray(s)])
-        for l in range(L_):
-            r_in = D[l][rows]
-            want, o, dn = omodel.layer(W["layers"][l], shape, r_in, pos, return_parts=True)
-            got = D[l + 1][rows]
-            # two residual roundings (r + o, then + dn) may each flip by one ulp of
-            # the residual; o and dn carry rounding flips of their dot-product
-            # inputs, i.e. errors on the scale of their row's typical size.
-            # (Checked on the CPU: the oracle's fp64-accumulation variant and a
-            # bf16-P attention variant stay below half of this bound; a 5% error
-            # in the attention scale exceeds it.)  The kernel rounds P to bf16
-            # before P.V; the oracle keeps it fp32.  On the CPU that one change
-            # leaves only about a third of layer-0 outputs bit-equal (0.34 on the
-            # dense-decoder workload, rising to 0.67 by layer 3), so the
-            # bit-equal floor here is 0.25.
-            upd = np.abs(o) + np.abs(dn)
-            rms = np.sqrt(np.mean(o.astype(np.float64) ** 2, -1, keepdims=True)) + \
-                np.sqrt(np.mean(dn.astype(np.float64) ** 2, -1, keepdims=True))
-            bf16_close(got, want, ulps=2, frac_exact=0.25, atol=2.0 ** -5 * (upd + rms) + 1e-6)
-            worst["layer_max_rel_update"] = max(worst["layer_max_rel_update"],
-                                                float(np.max(np.abs(got - want) / (upd + 1e-3))))
-            worst["layer_frac_exact_min"] = min(worst["layer_frac_exact_min"], float(np.mean(got == want)))
-        xf = ops.rmsnorm(D[L_][rows], W["final_norm"], shape.eps)[0]
-        bf16_close(D[L_ + 1][rows], xf, ulps=1, frac_exact=0.97)
-        logits = ops.linear(D[L_ + 1][rows], W["lm_head"], "fp32")
-        want_lp = ops.logprob(logits, targets[b])
-        e = float(np.max(np.abs(lp[rows] - want_lp)))
-        worst["lp"] = max(worst["lp"], e)
-        assert e < 1e-4, e
-    print("anchored parity", worst)
-    return worst
 
 
 def _decoder(shape, seed, max_pos, w_std=0.05):
