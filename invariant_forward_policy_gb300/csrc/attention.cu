@@ -141,14 +141,149 @@ struct AttnArgs {
 constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
 constexpr int kKeys = 64;   // keys per tile = cache block
 
-// STAGES = depth of the cp.async ring of (K, V) tiles.  It changes only when
-// loads are issued, never the arithmetic, so every depth gives the same bits.
-template <int HD, int STAGES>
+// Per-row arithmetic (shared by the decode and the prefill schedule below):
+// a split of S positions is cut into at most four "lanes" of lane_len =
+// roundup(S / 4, 64) positions.  Inside a lane, 64-key tiles are taken in
+// ascending order with an fp32 online softmax from a fresh (m, l, acc); the
+// lane results are then merged in lane order 0, 1, 2, 3 (lanes with no key
+// at or before the row's position are skipped).  The schedule decides only
+// who computes a lane (all four warps in parallel for a decode tile, one warp
+// after another for a prefill tile), never the arithmetic.
+
+// One 64-key tile into the online-softmax state of 16 query rows (one warp).
+template <int HD>
+__device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][4],
+                                          const bool (&row_valid)[2], const int (&row_pos)[2], float scale_log2,
+                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4]) {
+  constexpr int CH = HD / 8;
+  const int tq = lane & 3;
+  // S = Q K^T for 16 rows x 64 keys
+  float sc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; kk += 2) {
+      const int key = j * 8 + (lane & 7);
+      const int ch = kk * 2 + (lane >> 3);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+      mma_bf16_16816(sc[j], qf[kk], b0, b1);
+      mma_bf16_16816(sc[j], qf[kk + 1], b2, b3);
+    }
+  }
+  // online softmax (fp32), masking by select
+  float pr[8][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kp = key0 + j * 8 + tq * 2 + e;
+        const bool ok = row_valid[h] && kp <= row_pos[h];
+        const float v = ok ? __fmul_rn(sc[j][h * 2 + e], scale_log2) : -INFINITY;
+        sc[j][h * 2 + e] = v;
+        tmax = fmaxf(tmax, v);
+      }
+    }
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+    const float m_new = fmaxf(m[h], tmax);
+    const float alpha = (m_new == m[h]) ? 1.0f : exp2f(__fsub_rn(m[h], m_new));
+    float rs = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = sc[j][h * 2 + e];
+        const float pv = (v == -INFINITY) ? 0.f : exp2f(__fsub_rn(v, m_new));
+        pr[j][h * 2 + e] = pv;
+        rs = __fadd_rn(rs, pv);
+      }
+    }
+    rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 1));
+    rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 2));
+    l[h] = __fadd_rn(__fmul_rn(l[h], alpha), rs);
+    m[h] = m_new;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      acc[j][h * 2] = __fmul_rn(acc[j][h * 2], alpha);
+      acc[j][h * 2 + 1] = __fmul_rn(acc[j][h * 2 + 1], alpha);
+    }
+  }
+  // O += P V  (P rounded to bf16)
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
+    pa[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
+    pa[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
+    pa[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+#pragma unroll
+    for (int j = 0; j < HD / 8; j += 2) {
+      const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int ch = j + (lane >> 4);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+      mma_bf16_16816(acc[j], pa, b0, b1);
+      mma_bf16_16816(acc[j + 1], pa, b2, b3);
+    }
+  }
+}
+
+// Per-thread state of one lane, as stored in shared memory between lanes.
+template <int HD>
+struct LaneState {
+  float m[2], l[2];
+  float acc[HD / 8][4];
+};
+
+// P <- P (+) Q for the two rows a thread holds; an empty Q leaves P unchanged,
+// an empty P takes Q as it is.
+template <int HD>
+__device__ __forceinline__ void lane_merge(LaneState<HD>& P, const float (&mq)[2], const float (&lq)[2],
+                                           const float (&accq)[HD / 8][4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (mq[h] == -INFINITY) continue;
+    if (P.m[h] == -INFINITY) {
+      P.m[h] = mq[h];
+      P.l[h] = lq[h];
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) {
+        P.acc[j][h * 2] = accq[j][h * 2];
+        P.acc[j][h * 2 + 1] = accq[j][h * 2 + 1];
+      }
+      continue;
+    }
+    const float M = fmaxf(P.m[h], mq[h]);
+    const float a = (P.m[h] == M) ? 1.0f : exp2f(__fsub_rn(P.m[h], M));
+    const float b = (mq[h] == M) ? 1.0f : exp2f(__fsub_rn(mq[h], M));
+    P.l[h] = __fadd_rn(__fmul_rn(P.l[h], a), __fmul_rn(lq[h], b));
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = h * 2 + e;
+        P.acc[j][c] = __fadd_rn(__fmul_rn(P.acc[j][c], a), __fmul_rn(accq[j][c], b));
+      }
+    }
+    P.m[h] = M;
+  }
+}
+
+// DECODE: the CTA's query tile fits one warp (<= 16 rows); warp w computes lane
+// w of the split from its own K/V buffer, then warp 0 merges lanes 0..3.
+// PREFILL: warp w owns rows 16w..16w+15 and walks the split's tiles in order
+// from a shared two-stage ring, merging at every lane boundary.
+template <int HD, bool DECODE>
 __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  // [stage][K|V][64][HD] bf16, chunk-swizzled
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
@@ -156,7 +291,7 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   const int s = blockIdx.z / a.Hkv;
   const int row0 = a.pm.row0[p];
   const int n_tok = a.pm.row0[p + 1] - row0;
-  const int tok_per_tile = kRows / a.group;
+  const int tok_per_tile = (DECODE ? 16 : kRows) / a.group;
   const int tok0 = blockIdx.x * tok_per_tile;
   if (tok0 >= n_tok) return;
   const int pos_first = a.pm.pos0[p];
@@ -165,27 +300,25 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   const int kv_begin = s * a.split;
   if (kv_begin > max_pos) return;  // split entirely in the future of every row here
   const int kv_end = min(kv_begin + a.split, max_pos + 1);  // exclusive
-  const int t_begin = kv_begin / kKeys;
-  const int n_tiles = (kv_end - t_begin * kKeys + kKeys - 1) / kKeys;
+  const int lane_len = ((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys;
   const int seq = a.pm.seq[p];
   const int32_t* bt = a.block_table + (int64_t)seq * a.max_blk;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, tq = lane & 3;
 
-  // rows of this thread: r_lo = warp*16 + g, r_hi = r_lo + 8
+  // rows of this thread: r = (DECODE ? 0 : 16 * warp) + g + 8h
   int row_pos[2], row_tok[2], row_head[2];
   bool row_valid[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int r = warp * 16 + g + h * 8;
+    const int r = (DECODE ? 0 : warp * 16) + g + h * 8;
     const int ti = tok0 + r / a.group;
     row_valid[h] = ti < n_tok && (r / a.group) < tok_per_tile;
     row_tok[h] = row0 + ti;
     row_pos[h] = pos_first + ti;
     row_head[h] = kvh * a.group + (r % a.group);
   }
-  // Q fragments for this warp's 16 rows: HD/16 k-steps x 4 registers
   uint32_t qf[HD / 16][4];
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
@@ -197,16 +330,14 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     }
   }
 
-  auto load_tile = [&](int t, int stage) {
-    const int key0 = (t_begin + t) * kKeys;
+  // copy one 64-key tile of K and V into (sk, sv), threads t0, t0+nthr, ...
+  auto load_tile = [&](int key0, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
     const bool tab_ok = key0 / kKeys < a.max_blk;
     const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
     const bool blk_ok = blk >= 0 && blk < a.n_blocks;
-    if (!blk_ok && tid == 0) report(a.status, DEV_BAD_INDEX);
+    if (!blk_ok && t0 == 0) report(a.status, DEV_BAD_INDEX);
     const int64_t base = ((int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh) * kKeys * HD;
-    uint8_t* sk = smem + stage * 2 * TILE_BYTES;
-    uint8_t* sv = sk + TILE_BYTES;
-    for (int c = tid; c < kKeys * CH; c += 128) {
+    for (int c = t0; c < kKeys * CH; c += nthr) {
       const int key = c / CH, ch = c % CH;
       const bool valid = blk_ok && (key0 + key) <= max_pos;
       const int off = (key * CH + (ch ^ (key & 7))) * 16;
@@ -223,101 +354,80 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  // keep STAGES - 1 tiles in flight; one commit group per tile (empty past the end)
+  LaneState<HD> P;
+  P.m[0] = P.m[1] = -INFINITY;
+  P.l[0] = P.l[1] = 0.f;
 #pragma unroll
-  for (int t = 0; t < STAGES - 1; ++t) {
-    if (t < n_tiles) load_tile(t, t);
-    else cp_async_commit();
-  }
-  for (int t = 0; t < n_tiles; ++t) {
-    const int stage = t % STAGES;
-    if (t + STAGES - 1 < n_tiles) load_tile(t + STAGES - 1, (t + STAGES - 1) % STAGES);
-    else cp_async_commit();
-    cp_async_wait<STAGES - 1>();
-    __syncthreads();
-    const uint32_t sk = smem_u32(smem + stage * 2 * TILE_BYTES);
-    const uint32_t sv = sk + TILE_BYTES;
-    const int key0 = (t_begin + t) * kKeys;
+  for (int j = 0; j < HD / 8; ++j) P.acc[j][0] = P.acc[j][1] = P.acc[j][2] = P.acc[j][3] = 0.f;
 
-    // S = Q K^T for 16 rows x 64 keys
-    float sc[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; kk += 2) {
-        const int key = j * 8 + (lane & 7);
-        const int ch = kk * 2 + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
-        mma_bf16_16816(sc[j], qf[kk], b0, b1);
-        mma_bf16_16816(sc[j], qf[kk + 1], b2, b3);
-      }
+  if (DECODE) {
+    // ---- lane `warp`, from this warp's own one-tile buffer
+    uint8_t* sk = smem + warp * 2 * TILE_BYTES;
+    uint8_t* sv = sk + TILE_BYTES;
+    const int lb = kv_begin + warp * lane_len;
+    const int le = min(lb + lane_len, kv_end);
+    for (int key0 = lb; key0 < le; key0 += kKeys) {
+      load_tile(key0, sk, sv, lane, 32);
+      cp_async_wait<0>();
+      __syncwarp();
+      attn_tile<HD>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
+      __syncwarp();
     }
-    // online softmax (fp32), masking by select
-    float pr[8][4];
+    // lanes meet in shared memory (each warp reuses its buffer); warp 0 merges 0..3
+    LaneState<HD>* st = reinterpret_cast<LaneState<HD>*>(smem + warp * 2 * TILE_BYTES) + lane;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kp = key0 + j * 8 + tq * 2 + e;
-          const bool ok = row_valid[h] && kp <= row_pos[h];
-          const float v = ok ? __fmul_rn(sc[j][h * 2 + e], a.scale_log2) : -INFINITY;
-          sc[j][h * 2 + e] = v;
-          tmax = fmaxf(tmax, v);
-        }
-      }
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-      const float m_new = fmaxf(m[h], tmax);
-      const float alpha = (m_new == m[h]) ? 1.0f : exp2f(__fsub_rn(m[h], m_new));
-      float rs = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float v = sc[j][h * 2 + e];
-          const float pv = (v == -INFINITY) ? 0.f : exp2f(__fsub_rn(v, m_new));
-          pr[j][h * 2 + e] = pv;
-          rs = __fadd_rn(rs, pv);
-        }
-      }
-      rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 1));
-      rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, 2));
-      l[h] = __fadd_rn(__fmul_rn(l[h], alpha), rs);
-      m[h] = m_new;
-#pragma unroll
-      for (int j = 0; j < HD / 8; ++j) {
-        acc[j][h * 2] = __fmul_rn(acc[j][h * 2], alpha);
-        acc[j][h * 2 + 1] = __fmul_rn(acc[j][h * 2 + 1], alpha);
-      }
+      st->m[h] = m[h];
+      st->l[h] = l[h];
     }
-    // O += P V  (P rounded to bf16)
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
-      pa[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
-      pa[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+    for (int j = 0; j < HD / 8; ++j)
 #pragma unroll
-      for (int j = 0; j < HD / 8; j += 2) {
-        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = j + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
-        mma_bf16_16816(acc[j], pa, b0, b1);
-        mma_bf16_16816(acc[j + 1], pa, b2, b3);
-      }
-    }
+      for (int c = 0; c < 4; ++c) st->acc[j][c] = acc[j][c];
     __syncthreads();
+    if (warp != 0) return;
+    const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
+    for (int w = 0; w < n_lanes; ++w) {
+      const LaneState<HD>* q = reinterpret_cast<const LaneState<HD>*>(smem + w * 2 * TILE_BYTES) + lane;
+      lane_merge<HD>(P, q->m, q->l, q->acc);
+    }
+  } else {
+    // ---- all warps share a two-stage ring; lanes are walked in order
+    LaneState<HD>* run = reinterpret_cast<LaneState<HD>*>(smem + 2 * 2 * TILE_BYTES) + tid;
+    *run = P;
+    const int t_begin = kv_begin / kKeys;
+    const int n_tiles = (kv_end - kv_begin + kKeys - 1) / kKeys;
+    const int tiles_per_lane = lane_len / kKeys;
+    load_tile(t_begin * kKeys, smem, smem + TILE_BYTES, tid, 128);
+    for (int t = 0; t < n_tiles; ++t) {
+      const int stage = t & 1;
+      uint8_t* sk = smem + stage * 2 * TILE_BYTES;
+      if (t + 1 < n_tiles) {
+        uint8_t* nk = smem + (stage ^ 1) * 2 * TILE_BYTES;
+        load_tile((t_begin + t + 1) * kKeys, nk, nk + TILE_BYTES, tid, 128);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      if (t > 0 && t % tiles_per_lane == 0) {  // lane boundary: fold the finished lane in
+        LaneState<HD> r = *run;
+        lane_merge<HD>(r, m, l, acc);
+        *run = r;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      }
+      attn_tile<HD>(smem_u32(sk), smem_u32(sk + TILE_BYTES), (t_begin + t) * kKeys, qf, row_valid, row_pos,
+                    a.scale_log2, lane, m, l, acc);
+      __syncthreads();
+    }
+    P = *run;
+    lane_merge<HD>(P, m, l, acc);
   }
 
-  // write partials for rows that own this split
+  // write the split partial for rows that own this split
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     if (!row_valid[h] || row_pos[h] < kv_begin) continue;
@@ -325,9 +435,9 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     float* po = a.part_o + pidx * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
-      *reinterpret_cast<float2*>(po + j * 8 + tq * 2) = make_float2(acc[j][h * 2], acc[j][h * 2 + 1]);
+      *reinterpret_cast<float2*>(po + j * 8 + tq * 2) = make_float2(P.acc[j][h * 2], P.acc[j][h * 2 + 1]);
     }
-    if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(m[h], l[h]);
+    if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(P.m[h], P.l[h]);
   }
 }
 
@@ -363,19 +473,23 @@ __global__ void attention_merge_kernel(const float* __restrict__ part_o, const f
   }
 }
 
-static int attn_smem_bytes(int hd, int stages) { return stages * 2 * kKeys * hd * 2; }
+template <int HD, bool DECODE>
+constexpr int attn_smem_bytes() {
+  // decode: one K+V tile per warp; prefill: a two-stage ring plus the running lane state
+  return DECODE ? 4 * 2 * kKeys * HD * 2 : 2 * 2 * kKeys * HD * 2 + 128 * (int)sizeof(LaneState<HD>);
+}
 
-template <int HD, int STAGES>
+template <int HD, bool DECODE>
 static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t st) {
-  const int smem = attn_smem_bytes(HD, STAGES);
+  constexpr int smem = attn_smem_bytes<HD, DECODE>();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [smem] {
-    attr_err = cudaFuncSetAttribute(attention_kernel<HD, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attention_kernel<HD, DECODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(attention_kernel<HD, STAGES>, grid, dim3(128), smem, st, args), "attention_kernel");
+  return launched(launch_pdl(attention_kernel<HD, DECODE>, grid, dim3(128), smem, st, args), "attention_kernel");
 }
 
 // Positions per split: the fixed kv_split, or (BI_FAST) a size chosen from the
@@ -485,15 +599,17 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   args.nsplit = (int)ns;
   args.split = split;
   args.scale_log2 = scale * 1.4426950408889634f;
-  dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
   cudaStream_t st = as_stream(stream);
-  // a query tile that fits one warp (decode steps) is latency bound: keep more
-  // key tiles in flight; larger tiles keep two so that more CTAs share an SM
-  const bool deep = max_q_len * group <= 16;
-  if (hd == 64)
-    BI_TRY(deep ? launch_attention<64, 8>(args, grid, st) : launch_attention<64, 2>(args, grid, st));
-  else
-    BI_TRY(deep ? launch_attention<128, 4>(args, grid, st) : launch_attention<128, 2>(args, grid, st));
+  // a query tile of at most 16 rows (decode steps) uses the lane-parallel
+  // schedule; bigger tiles the row-parallel one.  Same bits either way.
+  const bool decode = max_q_len * group <= 16;
+  if (decode) {
+    dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)(Hkv * ns));
+    BI_TRY(hd == 64 ? launch_attention<64, true>(args, grid, st) : launch_attention<128, true>(args, grid, st));
+  } else {
+    dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
+    BI_TRY(hd == 64 ? launch_attention<64, false>(args, grid, st) : launch_attention<128, false>(args, grid, st));
+  }
   dim3 mgrid((unsigned)max_q_len, (unsigned)P);
   return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(256), 0, st, (const float*)part_o,
                              (const float*)part_ml, args.pm, Hq, hd, (int)ns, split, static_cast<__nv_bfloat16*>(out),

@@ -26,11 +26,13 @@ enum EpiKind : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU = 2, EPI_PARTIAL = 3,
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kATileBytes = kBM * kBK * 2;
 
+// TMA ring depth per tile width (about 144-192 KB of stages): deep enough that
+// a decode-size K range is mostly in flight at once.  It never changes results.
 template <int BN>
 struct GemmSmem {
+  static constexpr int kStages = BN == 64 ? 6 : (BN == 128 ? 5 : 4);
   static constexpr int kBTileBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
   static constexpr int kBytes = 1024 + kStages * kStageBytes + 256;
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmB2,
                                                          const GemmArgs args) {
   using S = GemmSmem<BN>;
+  constexpr int kStages = S::kStages;
   constexpr bool kSwiglu = (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -94,6 +94,26 @@ __device__ __forceinline__ LseState lse_block_reduce(LseState st) {
 
 __device__ __forceinline__ LseState lse_init() { return LseState{-INFINITY, 0.f, -INFINITY, 0x7fffffff}; }
 
+// Visit x4[v] for v = v0, v0 + NT, ... < end in that order; the loads of four
+// consecutive visits are issued before any of them is used.
+template <int NT>
+__device__ __forceinline__ void lse_walk(LseState& st, const float4* __restrict__ x4, int64_t v0, int64_t end) {
+  constexpr int U = 4;
+  for (; v0 < end; v0 += (int64_t)NT * U) {
+    float4 xs[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + (int64_t)u * NT;
+      if (v < end) xs[u] = __ldg(x4 + v);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = v0 + (int64_t)u * NT;
+      if (v < end) lse_step4(st, xs[u], (int)(v * 4));
+    }
+  }
+}
+
 // One CTA per row (invariant path).  Results go to index dst[row] (or row).
 template <int NT>
 __global__ void __launch_bounds__(NT) logprob_kernel(const float* __restrict__ logits, const int32_t* __restrict__ ids,
@@ -106,7 +126,7 @@ __global__ void __launch_bounds__(NT) logprob_kernel(const float* __restrict__ l
   const float4* x4 = reinterpret_cast<const float4*>(logits + row * V);
   const int64_t n4 = V / 4;
   LseState st = lse_init();
-  for (int64_t v = threadIdx.x; v < n4; v += NT) lse_step4(st, __ldg(x4 + v), (int)(v * 4));
+  lse_walk<NT>(st, x4, threadIdx.x, n4);
   st = lse_block_reduce<NT>(st);
   if (threadIdx.x == 0) {
     int32_t id = st.idx;
@@ -138,7 +158,7 @@ __global__ void __launch_bounds__(NT) logprob_partial_kernel(const float* __rest
   const int64_t b = c * per, e = min(n4, b + per);
   const float4* x4 = reinterpret_cast<const float4*>(logits + row * V);
   LseState st = lse_init();
-  for (int64_t v = b + threadIdx.x; v < e; v += NT) lse_step4(st, __ldg(x4 + v), (int)(v * 4));
+  lse_walk<NT>(st, x4, b + threadIdx.x, e);
   st = lse_block_reduce<NT>(st);
   if (threadIdx.x == 0) part[blockIdx.x] = st;
 }
