@@ -210,6 +210,23 @@ bi_status bi_logprob_gather(const float* logits, const int32_t* ids, int64_t T, 
                             int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes, void* stream);
 size_t bi_logprob_workspace_size(int64_t T, int64_t V, int mode);
 
+/* Fused lm_head + log-softmax + gather: logprob_out[t] = x[t, id_t] - lse(x[t, :])
+ * with x = X W^T never written to memory.  The GEMM epilogue of each 128 x BN
+ * tile keeps, per row and in column order, an fp32 online (max, sum-exp,
+ * argmax) and the target's logit; the per-tile records are then merged per
+ * row in a fixed order (thread t takes tiles t, t+128, ..., then a fixed
+ * butterfly and warp order).  BN is the weight's invariant tile width, so a
+ * row's bits do not depend on T.  (The article lists "the final logprob" among
+ * the fused forward outputs, [Article] §3.1.)
+ * X: bf16 [T, K]; W: bf16 [V, K]; ids: device int32 [T] or NULL (greedy: the
+ * argmax, ties to the lowest id); argmax_out: int32 [T] or NULL.  K % 64 == 0,
+ * V % 8 == 0.  workspace: bi_lm_head_logprob_workspace_size(T, V, K, mode)
+ * bytes.  BI_FAST narrows the vocab tiles for T <= 128 (not batch invariant). */
+bi_status bi_lm_head_logprob(const void* X, int64_t T, int64_t K, const void* W, int64_t V, const int32_t* ids,
+                             float* logprob_out, int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes,
+                             void* stream);
+size_t bi_lm_head_logprob_workspace_size(int64_t T, int64_t V, int64_t K, int mode);
+
 /* ---------------------------------------------------------------------- MoE
  * Router: [Article] §2 "the same discrete choices", §4.4 (router output fp32
  * at every batch size).  For each token, the k largest of E fp32 logits

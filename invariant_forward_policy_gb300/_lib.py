@@ -77,6 +77,8 @@ _SIGS = {
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
     "bi_logprob_workspace_size": (_sz, [_i64, _i64, _int]),
+    "bi_lm_head_logprob": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _int, _vp, _sz, _vp]),
+    "bi_lm_head_logprob_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "bi_moe_route_topk": (_int, [_vp, _i64, _int, _int, _vp, _vp, _vp]),
     "bi_moe_permute": (_int, [_vp, _i64, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "bi_moe_permute_workspace_size": (_sz, [_i64, _int, _int]),
@@ -234,6 +236,16 @@ def bi_logprob_gather(logits, ids, T, V, logprob_out, argmax_out=None, mode=BI_I
 
 def bi_logprob_workspace_size(T, V, mode=BI_INVARIANT) -> int:
     return load().bi_logprob_workspace_size(T, V, mode)
+
+
+def bi_lm_head_logprob(X, T, K, W, V, ids, logprob_out, argmax_out=None, mode=BI_INVARIANT, workspace=None,
+                       stream=None):
+    _check(load().bi_lm_head_logprob(_p(X), T, K, _p(W), V, _p(ids), _p(logprob_out), _p(argmax_out), mode,
+                                     _p(workspace), _nb(workspace), _s(stream)))
+
+
+def bi_lm_head_logprob_workspace_size(T, V, K, mode=BI_INVARIANT) -> int:
+    return load().bi_lm_head_logprob_workspace_size(T, V, K, mode)
 
 
 def bi_moe_route_topk(logits, T, E, k, ids, weights, stream=None):

@@ -59,6 +59,25 @@ bi_status logprob_gather_to(const float* logits, const int32_t* ids, int64_t T, 
                             int32_t* argmax_out, const int32_t* dst, int mode, void* workspace, size_t ws_bytes,
                             void* stream);
 
+// Per-(row, vocab tile) partial of the fused lm_head + log-softmax: the tile's
+// max, sum of exp(x - max), argmax (value, lowest index) and the target's logit
+// when the target id falls in the tile.
+struct TileLse {
+  float m, s, best, xt;
+  int idx;
+  int pad[3];
+};
+// Merge the n_tiles partials of each of T rows (fixed order) into the logprob
+// of ids[row] (or of the argmax when ids is NULL), written to index dst[row].
+bi_status lse_tiles_merge(const TileLse* part, int64_t T, int n_tiles, int tile_n, const int32_t* ids,
+                          float* logprob_out, int32_t* argmax_out, const int32_t* dst, void* stream);
+
+// Fused lm_head + log-softmax with results at index dst[row]; its workspace size.
+bi_status lm_head_logprob_to(const void* X, int64_t T, int64_t K, const void* W, int64_t V, const int32_t* ids,
+                             float* logprob_out, int32_t* argmax_out, const int32_t* dst, int mode, void* workspace,
+                             size_t ws_bytes, void* stream);
+size_t lm_head_partial_bytes(int64_t T, int64_t V, int64_t K, int mode);
+
 // TMA descriptor encode (driver entry point looked up through the runtime).
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,

@@ -22,7 +22,7 @@
 
 namespace bi {
 
-enum EpiKind : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU = 2, EPI_PARTIAL = 3, EPI_PARTIAL_SWIGLU = 4 };
+enum EpiKind : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU = 2, EPI_PARTIAL = 3, EPI_PARTIAL_SWIGLU = 4, EPI_LSE = 5 };
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -49,7 +49,30 @@ struct GemmArgs {
   int up_offset;            // SwiGLU: row offset of the up half inside one expert's W
   int k_blocks_per_split;
   int ldp;                  // partial row length
+  const int32_t* ids;       // EPI_LSE: target id of each row (NULL = greedy)
+  TileLse* lse;             // EPI_LSE: [M, n_tiles] tile partials
+  int n_tiles;              // EPI_LSE: vocab tiles per row
 };
+
+// Online (max, sum-exp, argmax) over 4 consecutive logits, in column order.
+__device__ __forceinline__ void tile_lse_step4(float& m, float& s, float& best, int& idx, const uint32_t* r,
+                                               int col) {
+  const float x0 = __uint_as_float(r[0]), x1 = __uint_as_float(r[1]);
+  const float x2 = __uint_as_float(r[2]), x3 = __uint_as_float(r[3]);
+  const float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  if (mx > m) {
+    s = (m == -INFINITY) ? 0.f : __fmul_rn(s, expf(__fsub_rn(m, mx)));
+    m = mx;
+  }
+  s = __fadd_rn(s, expf(__fsub_rn(x0, m)));
+  s = __fadd_rn(s, expf(__fsub_rn(x1, m)));
+  s = __fadd_rn(s, expf(__fsub_rn(x2, m)));
+  s = __fadd_rn(s, expf(__fsub_rn(x3, m)));
+  if (x0 > best) { best = x0; idx = col; }
+  if (x1 > best) { best = x1; idx = col + 1; }
+  if (x2 > best) { best = x2; idx = col + 2; }
+  if (x3 > best) { best = x3; idx = col + 3; }
+}
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
@@ -231,6 +254,40 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
         }
       }
     }
+  } else if (EPI == EPI_LSE) {
+    // fp32 logits of this row's BN columns, visited in column order
+    const int n0 = n_tile * BN;
+    const int tgt = (row_ok && args.ids) ? args.ids[row] : -1;
+    float m = -INFINITY, s = 0.f, best = -INFINITY, xt = __int_as_float(0x7fc00000);
+    int idx = 0x7fffffff;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c, r);
+      tmem_ld_wait();
+      if (!(do_store && row_ok)) continue;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = n0 + c + q * 4;
+        if (col < args.n_out) tile_lse_step4(m, s, best, idx, r + q * 4, col);
+      }
+      const int off = tgt - (n0 + c);
+      if (off >= 0 && off < 32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i == off) xt = __uint_as_float(r[i]);
+      }
+    }
+    if (do_store && row_ok) {
+      TileLse t;
+      t.m = m;
+      t.s = s;
+      t.best = best;
+      t.xt = xt;
+      t.idx = idx;
+      t.pad[0] = t.pad[1] = t.pad[2] = 0;
+      args.lse[(size_t)row * args.n_tiles + n_tile] = t;
+    }
   } else {
     const int n0 = n_tile * BN;
 #pragma unroll 1
@@ -334,6 +391,7 @@ static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUten
     case EPI_SWIGLU: return dispatch_bn<EPI_SWIGLU>(bn, a, b, b2, args, grid, st);
     case EPI_PARTIAL: return dispatch_bn<EPI_PARTIAL>(bn, a, b, b2, args, grid, st);
     case EPI_PARTIAL_SWIGLU: return dispatch_bn<EPI_PARTIAL_SWIGLU>(bn, a, b, b2, args, grid, st);
+    case EPI_LSE: return dispatch_bn<EPI_LSE>(bn, a, b, b2, args, grid, st);
   }
   return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad epilogue");
 }
@@ -372,6 +430,8 @@ struct GemmCall {
   int c_dtype, epilogue, mode;
   void* ws;
   size_t ws_bytes;
+  const int32_t* ids = nullptr;  // fused log-softmax: targets (NULL = greedy)
+  TileLse* lse = nullptr;        // fused log-softmax: tile partials (non-NULL selects it)
 };
 
 static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
@@ -382,7 +442,10 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   const bool swiglu = g.epilogue == BI_EPI_SWIGLU;
   const int64_t n_out = swiglu ? g.n_rows_w / 2 : g.n_rows_w;
   int bn = tile_n_for(g.n_rows_w, g.K, swiglu), splits = 1;
-  if (g.mode == BI_FAST && g.E == 1) fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
+  if (g.mode == BI_FAST && g.E == 1) {
+    fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
+    if (g.lse) splits = 1;  // the fused head keeps whole K per tile; FAST narrows the tiles instead
+  }
   const int64_t kblocks = g.K / kBK;
 
   CUtensorMap ta, tb, tb2;
@@ -413,11 +476,17 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   args.up_offset = (g.E == 1 && !g.tile_expert) ? 0 : (int)n_out;
   args.k_blocks_per_split = (int)(kblocks / splits);
   args.ldp = (int)g.n_rows_w;
+  args.ids = g.ids;
+  args.lse = g.lse;
 
   const int64_t n_tiles = swiglu ? cdiv(n_out, bn / 2) : cdiv(n_out, bn);
+  args.n_tiles = (int)n_tiles;
   dim3 grid((unsigned)n_tiles, (unsigned)cdiv(g.M, kBM), (unsigned)splits);
   int epi;
-  if (splits > 1) {
+  if (g.lse) {
+    if (splits != 1) return fail(BI_ERR_INVALID_ARG, "fused log-softmax cannot run split-K");
+    epi = EPI_LSE;
+  } else if (splits > 1) {
     if (g.ws_bytes < partial_bytes(g.M, g.n_rows_w, splits) || !g.ws)
       return fail(BI_ERR_INVALID_ARG, "bi_gemm: BI_FAST split-K needs workspace (bi_gemm_workspace_size)");
     args.partial = static_cast<float*>(g.ws);
@@ -489,6 +558,59 @@ bi_status bi_grouped_gemm(const void* A, int64_t M_rows, int64_t K, const void* 
   BI_REQUIRE_SHAPE(M_rows < (1ll << 31) && N * E < (1ll << 31), "shape too large");
   GemmCall g{A, M_rows, K, W, N, E, tile_expert, C, c_dtype, epilogue, BI_INVARIANT, nullptr, 0};
   return run_gemm(g, as_stream(stream));
+}
+
+}  // extern "C"
+
+// ----------------------------------------------- fused lm_head + log-softmax
+namespace bi {
+
+// Vocab tile width of the fused head: the invariant width of the weight, or
+// (BI_FAST, at most 128 rows) the narrow width that spreads the vocab over more CTAs.
+static int lm_head_tile_n(int64_t T, int64_t V, int64_t K, int mode) {
+  int bn = tile_n_for(V, K, false), splits = 1;
+  if (mode == BI_FAST) fast_plan(T, V, K, false, &bn, &splits);
+  return bn;
+}
+
+size_t lm_head_partial_bytes(int64_t T, int64_t V, int64_t K, int mode) {
+  if (T <= 0 || V <= 0) return 0;
+  return (size_t)T * cdiv(V, lm_head_tile_n(T, V, K, mode)) * sizeof(TileLse);
+}
+
+bi_status lm_head_logprob_to(const void* X, int64_t T, int64_t K, const void* W, int64_t V, const int32_t* ids,
+                             float* logprob_out, int32_t* argmax_out, const int32_t* dst, int mode, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  BI_REQUIRE(T >= 0 && V > 0 && K > 0, "bad shape");
+  if (T == 0) return BI_OK;
+  BI_REQUIRE(X && W && logprob_out && workspace, "null pointer");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  BI_REQUIRE(aligned16(X) && aligned16(W) && aligned16(workspace), "pointers must be 16-byte aligned");
+  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
+  BI_REQUIRE_SHAPE(V % 8 == 0, "V must be a multiple of 8");
+  BI_REQUIRE_SHAPE(T < (1ll << 31) && V < (1ll << 31), "shape too large");
+  BI_REQUIRE(ws_bytes >= lm_head_partial_bytes(T, V, K, mode), "workspace too small (bi_lm_head_logprob_workspace_size)");
+  const int bn = lm_head_tile_n(T, V, K, mode);
+  GemmCall g{X, T, K, W, V, 1, nullptr, nullptr, BI_DTYPE_FP32, BI_EPI_NONE, mode, nullptr, 0};
+  g.ids = ids;
+  g.lse = static_cast<TileLse*>(workspace);
+  BI_TRY(run_gemm(g, as_stream(stream)));
+  return lse_tiles_merge(g.lse, T, (int)cdiv(V, bn), bn, ids, logprob_out, argmax_out, dst, stream);
+}
+
+}  // namespace bi
+
+extern "C" {
+
+size_t bi_lm_head_logprob_workspace_size(int64_t T, int64_t V, int64_t K, int mode) {
+  return bi::lm_head_partial_bytes(T, V, K, mode);
+}
+
+bi_status bi_lm_head_logprob(const void* X, int64_t T, int64_t K, const void* W, int64_t V, const int32_t* ids,
+                             float* logprob_out, int32_t* argmax_out, int mode, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  return bi::lm_head_logprob_to(X, T, K, W, V, ids, logprob_out, argmax_out, nullptr, mode, workspace, ws_bytes,
+                                stream);
 }
 
 }  // extern "C"

@@ -182,6 +182,47 @@ __global__ void logprob_combine_kernel(const float* __restrict__ logits, const i
   if (argmax_out) argmax_out[o] = st.idx;
 }
 
+// Fused head: merge the vocab-tile partials of one row, thread t taking tiles
+// t, t + 128, ... in order, then the fixed butterfly / warp-order tree.
+__global__ void __launch_bounds__(128) lse_tiles_merge_kernel(const TileLse* __restrict__ part, int n_tiles,
+                                                              int tile_n, const int32_t* __restrict__ ids,
+                                                              float* __restrict__ lp_out,
+                                                              int32_t* __restrict__ argmax_out,
+                                                              const int32_t* __restrict__ dst, int* status) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  const TileLse* pr = part + row * n_tiles;
+  LseState st = lse_init();
+  for (int t = threadIdx.x; t < n_tiles; t += 128) {
+    const TileLse q = pr[t];
+    st = lse_merge(st, LseState{q.m, q.s, q.best, q.idx});
+  }
+  st = lse_block_reduce<128>(st);
+  if (threadIdx.x == 0) {
+    float xt = st.best;
+    if (ids) {
+      int32_t id = ids[row];
+      if (id < 0 || id / tile_n >= n_tiles) {
+        report(status, DEV_BAD_INDEX);
+      } else {
+        xt = pr[id / tile_n].xt;
+      }
+    }
+    const int64_t o = dst ? (int64_t)dst[row] : row;
+    lp_out[o] = __fsub_rn(__fsub_rn(xt, st.m), logf(st.s));
+    if (argmax_out) argmax_out[o] = st.idx;
+  }
+}
+
+bi_status lse_tiles_merge(const TileLse* part, int64_t T, int n_tiles, int tile_n, const int32_t* ids,
+                          float* logprob_out, int32_t* argmax_out, const int32_t* dst, void* stream) {
+  if (T == 0) return BI_OK;
+  return launched(launch_pdl(lse_tiles_merge_kernel, dim3((unsigned)T), dim3(128), 0, as_stream(stream), part, n_tiles,
+                             tile_n, ids, logprob_out, argmax_out, dst, device_status_ptr()),
+                  "lse_tiles_merge_kernel");
+}
+
 static int fast_chunks(int64_t T, int64_t V) {
   if (T >= num_sms()) return 1;
   int64_t c = cdiv(2 * (int64_t)num_sms(), T);

@@ -108,7 +108,7 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
 // ------------------------------------------------------------- workspace plan
 struct FwdLayout {
   size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt;
-  size_t h, x, qkv, q, ao, tmp, act, attn_ws, hsel, tsel, xsel, logits, lp, am, gemm_ws, lp_ws;
+  size_t h, x, qkv, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
   size_t attn_ws_bytes, gemm_ws_bytes, lp_ws_bytes;
   size_t total;
 };
@@ -139,12 +139,12 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   L.act = take(Tm * c.ffn * 2);
   L.attn_ws_bytes = bi_attention_workspace_size(Tm, (int)c.n_heads_q, (int)c.head_dim, max_ctx, (int)c.kv_split);
   L.attn_ws = take(L.attn_ws_bytes);
-  L.hsel = take(Rm * c.d * 2);
-  L.tsel = take(Rm * c.d * 2);
   L.xsel = take(Rm * c.d * 2);
-  L.logits = take(Rm * c.vocab * 4);
-  L.lp = take(Rm * 4);
-  L.am = take(Rm * 4);
+  // fused lm_head + log-softmax: per-(row, vocab tile) records, no logits
+  const size_t head_bytes = std::max(lm_head_partial_bytes(Rm, c.vocab, c.d, mode),
+                                     lm_head_partial_bytes(std::min<int64_t>(Rm, 128), c.vocab, c.d, mode));
+  L.logits = take(head_bytes);
+  L.lp_ws_bytes = head_bytes;
   size_t g = 0;
   if (mode == BI_FAST) {
     const int64_t m = std::min<int64_t>(std::max(Tm, Rm), 128);
@@ -152,12 +152,9 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
     g = std::max(g, bi_gemm_workspace_size(m, c.d, hq, BI_EPI_NONE, mode));
     g = std::max(g, bi_gemm_workspace_size(m, 2 * c.ffn, c.d, BI_EPI_SWIGLU, mode));
     g = std::max(g, bi_gemm_workspace_size(m, c.d, c.ffn, BI_EPI_NONE, mode));
-    g = std::max(g, bi_gemm_workspace_size(m, c.vocab, c.d, BI_EPI_NONE, mode));
   }
   L.gemm_ws_bytes = g;
   L.gemm_ws = take(g);
-  L.lp_ws_bytes = bi_logprob_workspace_size(Rm, c.vocab, mode);
-  L.lp_ws = take(L.lp_ws_bytes);
   L.total = off + 256;
   return L;
 }
@@ -240,14 +237,12 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     const int64_t R = std::min(Rm, ps.n_logit - r0);
     const int32_t* src = at<int32_t>(ws, L.logit_src) + r0;
     void* xsel = at<void>(ws, L.xsel);
-    float* logits = at<float>(ws, L.logits);
     // rows src[j] of (down-proj out + residual) -> final norm -> compact row j
     BI_TRY(rmsnorm_rows(tmp, h, m->final_norm, xsel, R, c.d, c.eps, src, stream));
-    BI_TRY(bi_gemm(xsel, R, c.d, m->lm_head, c.vocab, logits, BI_DTYPE_FP32, BI_EPI_NONE, mode, gws,
-                   L.gemm_ws_bytes, stream));
+    // lm_head + log-softmax + gather fused; results land at the call's row index
     const int32_t* tgt = greedy ? nullptr : at<int32_t>(ws, L.logit_tgt) + r0;
-    BI_TRY(logprob_gather_to(logits, tgt, R, c.vocab, logprob_out, sampled_out, at<int32_t>(ws, L.logit_dst) + r0,
-                             mode, L.lp_ws_bytes ? at<void>(ws, L.lp_ws) : nullptr, L.lp_ws_bytes, stream));
+    BI_TRY(lm_head_logprob_to(xsel, R, c.d, m->lm_head, c.vocab, tgt, logprob_out, sampled_out,
+                              at<int32_t>(ws, L.logit_dst) + r0, mode, at<void>(ws, L.logits), L.lp_ws_bytes, stream));
   }
   (void)st;
   return BI_OK;

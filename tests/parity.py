@@ -7,6 +7,9 @@ in the residual stream propagate.  Measured with the oracle against its own
 fp64-accumulation variant (same tokens, teacher forced):
   dense decoder (4 layers, d 512):            max 7.5e-3, mean 2.2e-3
   long-context GQA decoder (8 layers, d 2048): max 3.8e-2, mean 1.0e-2
+  small 2-layer test models (d 128 / 256):     max 6.7e-3, mean 2.6e-3
+and rounding P to bf16 before P.V (the kernel does, the oracle does not) adds
+about 3e-3 to the mean on the small models (max 7.9e-3, mean 3.0e-3 alone).
 The free-running bounds are about twice those floors; the strict check is the
 layer-anchored one (every layer from the GPU's own input; the logprob from its
 final norm within 1e-4).
@@ -18,7 +21,8 @@ from oracle import model as omodel
 from oracle import ops
 from tests.gpu_util import bf16_close, host_f32
 
-E2E_MAX, E2E_MEAN = 2e-2, 5e-3            # dense decoder and the small test models
+E2E_MAX, E2E_MEAN = 2e-2, 5e-3            # dense decoder workload
+E2E_MAX_SMALL, E2E_MEAN_SMALL = 3e-2, 1e-2  # small 2-layer test models
 E2E_MAX_LONG, E2E_MEAN_LONG = 8e-2, 2.5e-2  # 8-layer d-2048 long-context decoder
 
 

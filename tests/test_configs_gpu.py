@@ -130,6 +130,30 @@ def test_large_vocab_logprob_two_partitions_k3_zero():
                                   norm=False)
     err = np.abs(lp_a.cpu().numpy()[sub] - want)
     assert err.max() < 2e-4, err.max()
+    # the fused lm_head + log-softmax (no logits in memory): same two partitions
+    d = c["d"]
+
+    def fused(hh, ii):
+        n = hh.shape[0]
+        out = torch.empty(n, dtype=torch.float32, device="cuda")
+        ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(n, c["vocab"], d), dtype=torch.uint8, device="cuda")
+        bi.bi_lm_head_logprob(hh, n, d, W, c["vocab"], ii, out, None, bi.BI_INVARIANT, ws)
+        return out
+
+    fa = fused(h, ids)
+    fb = torch.empty_like(fa)
+    rng = np.random.default_rng(c["seed"] + 2)
+    perm = rng.permutation(T)
+    i = 0
+    while i < T:
+        n = int(rng.integers(1, 4097))
+        r = torch.from_numpy(perm[i:i + n]).cuda()
+        fb[r] = fused(h[r].contiguous(), ids[r].contiguous())
+        i += n
+    s = ops.diff_stats(fa.cpu().numpy(), fb.cpu().numpy())
+    assert s == {"max": 0.0, "mean": 0.0, "std": 0.0, "k3": 0.0}, s
+    errf = np.abs(fa.cpu().numpy()[sub] - want)
+    assert errf.max() < 2e-4, errf.max()
 
 
 # ----------------------------------------------------------------------------- long-context GQA

@@ -158,6 +158,40 @@ def test_logprob_argmax_ties_lowest_id_and_row_invariance():
         assert same_bits(lp1, lp[-T:])
 
 
+def _fused_head(X, W, ids, mode=bi.BI_INVARIANT):
+    T, K = X.shape
+    V = W.shape[0]
+    lp = torch.full((T,), float("nan"), dtype=torch.float32, device="cuda")
+    am = torch.full((T,), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(T, V, K, mode), dtype=torch.uint8, device="cuda")
+    bi.bi_lm_head_logprob(X, T, K, W, V, ids, lp, am, mode, ws)
+    return lp, am
+
+
+@pytest.mark.parametrize("T,K,V", [(1, 512, 32000), (37, 256, 4096), (130, 512, 32000), (5, 1024, 129280)])
+def test_fused_lm_head_logprob_parity_and_row_invariance(T, K, V):
+    rng = np.random.default_rng(T * 7 + V)
+    xb, xf = rng_bf16(rng, (T, K))
+    wb, wf = rng_bf16(rng, (V, K), 0.05)
+    ids = rng.integers(0, V, T).astype(np.int32)
+    X, W, I = dev_bf16(xb), dev_bf16(wb), torch.from_numpy(ids).cuda()
+    lp, am = _fused_head(X, W, I)
+    logits = ops.linear(xf, wf, "fp32")
+    assert np.max(np.abs(lp.cpu().numpy() - ops.logprob(logits, ids))) < 1e-4
+    o_am = ops.argmax_lowest(logits)
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > 1e-4
+    assert np.array_equal(am.cpu().numpy()[clear], o_am[clear])
+    lpg, amg = _fused_head(X, W, None)                        # greedy
+    assert torch.equal(amg, am)
+    assert np.max(np.abs(lpg.cpu().numpy() - ops.logprob(logits, amg.cpu().numpy()))) < 1e-4
+    for t0 in (0, T // 2, T - 1):                              # rows alone give the same bits
+        l1, a1 = _fused_head(X[t0:t0 + 1].contiguous(), W, I[t0:t0 + 1].contiguous())
+        assert same_bits(l1, lp[t0:t0 + 1]) and torch.equal(a1, am[t0:t0 + 1])
+    lf, _ = _fused_head(X, W, I, bi.BI_FAST)                   # the non-invariant path agrees closely
+    assert np.max(np.abs(lf.cpu().numpy() - lp.cpu().numpy())) < 1e-4
+
+
 # ---------------------------------------------------------------------------- RoPE + attention
 def _paged_setup(seq_lens, Hq, Hkv, hd, rng, n_blocks_extra=3):
     max_blk = max(math.ceil(n / 64) for n in seq_lens)
