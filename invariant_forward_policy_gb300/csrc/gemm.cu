@@ -52,6 +52,7 @@ struct GemmArgs {
   const int32_t* ids;       // EPI_LSE: target id of each row (NULL = greedy)
   TileLse* lse;             // EPI_LSE: [M, n_tiles] tile partials
   int n_tiles;              // EPI_LSE: vocab tiles per row
+  int m_tiles, n_tiles_grid, splits;  // tile space walked by the persistent CTAs
 };
 
 // Online (max, sum-exp, argmax) over 4 consecutive logits, in column order.
@@ -76,137 +77,11 @@ __device__ __forceinline__ void tile_lse_step4(float& m, float& s, float& best, 
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
+// Epilogue of one 128 x BN accumulator tile: this warp drains TMEM lanes
+// 32q..32q+31 (tile rows) from column base t_row and writes its rows.
 template <int BN, int EPI>
-__global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                                                         const __grid_constant__ CUtensorMap tmB,
-                                                         const __grid_constant__ CUtensorMap tmB2,
-                                                         const GemmArgs args) {
-  using S = GemmSmem<BN>;
-  constexpr int kStages = S::kStages;
-  constexpr bool kSwiglu = (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU);
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kATileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * S::kBTileBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* accb = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* consumed = abort_flag + 1;
-
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tile = blockIdx.x, m_tile = blockIdx.y, split = blockIdx.z;
-  int expert = 0;
-  if (args.tile_expert) {
-    pdl_wait();  // the tile owner map comes from the preceding kernel
-    expert = args.tile_expert[m_tile];
-    if (expert < 0) return;  // whole CTA leaves before touching barriers or TMEM
-  }
-  const int m0 = m_tile * kBM;
-  const int nk = args.k_blocks_per_split;
-  const int kb0 = split * nk;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(accb, 1);
-    *abort_flag = 0;
-    *consumed = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, BN);
-    tmem_relinquish();
-  }
-  if (threadIdx.x == 32) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    if (kSwiglu) prefetch_tmap(&tmB2);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_d = *tmem_slot;
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    const int wbase = expert * args.w_rows_per_expert;
-    auto load_w = [&](int kb, int s) {
-      const int kc = (kb0 + kb) * kBK;
-      if (kSwiglu) {
-        const int j0 = n_tile * (BN / 2);
-        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
-        tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc, wbase + args.up_offset + j0);
-      } else {
-        tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
-      }
-    };
-    // The weights are not written by the preceding kernel: fetch the first
-    // stages' weight tiles while it finishes, then wait for it before reading A.
-    const int pre = nk < kStages ? nk : kStages;
-    for (int kb = 0; kb < pre; ++kb) {
-      mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
-      load_w(kb, kb);
-    }
-    pdl_wait();
-    for (int kb = 0; kb < pre; ++kb) tma_load_2d(sA + kb * kATileBytes, &tmA, &full[kb], (kb0 + kb) * kBK, m0);
-    int issued = pre;
-    for (int kb = pre; kb < nk; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1) || *abort_flag) {
-        report(args.status, DEV_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      mbar_arrive_expect_tx(&full[s], S::kStageBytes);
-      tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], (kb0 + kb) * kBK, m0);
-      load_w(kb, s);
-      ++issued;
-    }
-    if (*abort_flag) {
-      // let every copy this CTA started land before the CTA can exit
-      for (int kb = *consumed; kb < issued; ++kb) mbar_wait(&full[kb % kStages], (kb / kStages) & 1);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1;
-      if (!mbar_wait(&full[s], ph) || *abort_flag) {
-        report(args.status, DEV_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      *consumed = kb + 1;
-      tc_fence_after();
-      const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
-      const uint32_t b_addr = smem_u32(sB + s * S::kBTileBytes);
-#pragma unroll
-      for (int k = 0; k < kBK / 16; ++k) {
-        tc_mma_bf16(tmem_d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
-                    (kb | k) != 0 ? 1u : 0u);
-      }
-      tc_commit(&empty[s]);
-    }
-    tc_commit(accb);  // fires once every MMA issued above has completed
-  }
-  __syncwarp();
-
-  // ---------------- epilogue: TMEM -> registers -> global
-  const bool acc_ok = mbar_wait(accb, 0);
-  tc_fence_after();
-  if (!acc_ok) report(args.status, DEV_TIMEOUT);
-  const bool do_store = acc_ok && !*abort_flag;
-  const int row = m0 + warp * 32 + lane;
-  const bool row_ok = row < args.M;
-  const uint32_t t_row = tmem_d + ((uint32_t)(warp * 32) << 16);
-
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_row, int row, bool row_ok,
+                                              bool do_store, int n_tile, int split) {
   if (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU) {
     const int j0 = n_tile * (BN / 2);
 #pragma unroll 1
@@ -323,11 +198,224 @@ __global__ void __launch_bounds__(128, 1) gemm_tc_kernel(const __grid_constant__
       }
     }
   }
+}
+
+// Persistent warp-specialized kernel: one CTA per SM walks its tiles
+// (t = blockIdx.x, blockIdx.x + gridDim.x, ...).  Warp 0 lane 0 = TMA producer,
+// warp 1 = TMEM owner and (lane 0) MMA issuer, warps 2..5 = epilogue.  The fp32
+// accumulator is double-buffered in TMEM so the epilogue of tile i overlaps
+// the mainloop of tile i+1.  Each tile's MMAs, K order and epilogue are the
+// same as for a lone tile: the schedule never changes results.
+struct TileCoord {
+  int m_tile, n_tile, split;
+};
+
+// Grouped rasterisation: kGroupM M-tiles at a time, N-tiles within the group,
+// so that concurrently running tiles share their A and W tiles in L2.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ TileCoord tile_coord(int t, int m_tiles, int n_tiles) {
+  TileCoord c;
+  const int per_split = m_tiles * n_tiles;
+  c.split = t / per_split;
+  t -= c.split * per_split;
+  const int per_group = kGroupM * n_tiles;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int gm = min(kGroupM, m_tiles - g * kGroupM);
+  c.n_tile = r / gm;
+  c.m_tile = g * kGroupM + (r - c.n_tile * gm);
+  return c;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                         const __grid_constant__ CUtensorMap tmB,
+                                                         const __grid_constant__ CUtensorMap tmB2,
+                                                         const GemmArgs args) {
+  using S = GemmSmem<BN>;
+  constexpr int kStages = S::kStages;
+  constexpr bool kSwiglu = (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU);
+  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulator buffers
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * S::kBTileBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;   // [2] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA (4 warp arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = args.m_tiles, n_tiles = args.n_tiles_grid;
+  const int total = m_tiles * n_tiles * args.splits;
+  const int nk = args.k_blocks_per_split;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (kSwiglu) prefetch_tmap(&tmB2);
+  }
   tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // expert of an M-tile (grouped GEMM); -1 tiles are skipped by every role alike
+  auto tile_expert = [&](int m_tile) { return args.tile_expert ? args.tile_expert[m_tile] : 0; };
+
   if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      auto load_w = [&](int expert, int n_tile, int kc, int s) {
+        const int wbase = expert * args.w_rows_per_expert;
+        if (kSwiglu) {
+          const int j0 = n_tile * (BN / 2);
+          tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
+          tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc,
+                      wbase + args.up_offset + j0);
+        } else {
+          tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
+        }
+      };
+      int kb_total = 0;  // ring position across tiles
+      bool first = true;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, m_tiles, n_tiles);
+        int expert = 0;
+        int pre = 0;
+        if (first && !args.tile_expert) {
+          // weights never come from the preceding kernel: start fetching them
+          // while it finishes; A is read only after the dependency wait
+          pre = nk < kStages ? nk : kStages;
+          for (int kb = 0; kb < pre; ++kb) {
+            mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
+            load_w(0, tc.n_tile, (tc.split * nk + kb) * kBK, kb);
+          }
+        }
+        if (first) pdl_wait();
+        first = false;
+        if (args.tile_expert) {
+          expert = tile_expert(tc.m_tile);
+          if (expert < 0) continue;
+        }
+        for (int kb = 0; kb < pre; ++kb)
+          tma_load_2d(sA + kb * kATileBytes, &tmA, &full[kb], (tc.split * nk + kb) * kBK, tc.m_tile * kBM);
+        kb_total += pre;
+        for (int kb = pre; kb < nk; ++kb, ++kb_total) {
+          const int s = kb_total % kStages;
+          const uint32_t ph = (kb_total / kStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1) || *abort_flag) {
+            report(args.status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+          const int kc = (tc.split * nk + kb) * kBK;
+          tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], kc, tc.m_tile * kBM);
+          load_w(expert, tc.n_tile, kc, s);
+        }
+      }
+      if (first) pdl_wait();  // no tile for this CTA: still order after the predecessor
+      // let the last copies this CTA started land before it can exit
+      for (int i = 0; i < kStages && i < kb_total; ++i) {
+        const int kb = kb_total - 1 - i;
+        mbar_wait(&full[kb % kStages], (kb / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      pdl_wait();
+      int kb_total = 0, local = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, m_tiles, n_tiles);
+        if (args.tile_expert && tile_expert(tc.m_tile) < 0) continue;
+        const int b = local & 1;
+        const uint32_t bph = (local >> 1) & 1;
+        if (!mbar_wait(&acc_empty[b], bph ^ 1)) {
+          report(args.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + b * BN;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++kb_total) {
+          const int s = kb_total % kStages;
+          const uint32_t ph = (kb_total / kStages) & 1;
+          if (!mbar_wait(&full[s], ph) || *abort_flag) {
+            report(args.status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
+          const uint32_t b_addr = smem_u32(sB + s * S::kBTileBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            tc_mma_bf16(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        tc_commit(&acc_full[b]);  // fires once this tile's MMAs have completed
+        ++local;
+        if (!ok) break;
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5: TMEM lane quarter q = warp % 4
+    const int q = warp & 3;
+    int local = 0;
+    pdl_wait();
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const TileCoord tc = tile_coord(t, m_tiles, n_tiles);
+      if (args.tile_expert && tile_expert(tc.m_tile) < 0) continue;
+      const int b = local & 1;
+      const uint32_t bph = (local >> 1) & 1;
+      const bool acc_ok = mbar_wait(&acc_full[b], bph);
+      tc_fence_after();
+      if (!acc_ok) {
+        report(args.status, DEV_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const int row = tc.m_tile * kBM + q * 32 + lane;
+      epilogue_tile<BN, EPI>(args, tmem_base + b * BN + ((uint32_t)(q * 32) << 16), row, row < args.M,
+                             !*abort_flag, tc.n_tile, tc.split);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
+      ++local;
+      if (*abort_flag) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_d, BN);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -369,7 +457,7 @@ static bi_status launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUt
     attr_err = cudaFuncSetAttribute(gemm_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess) return fail(BI_ERR_CUDA, std::string("gemm smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(gemm_tc_kernel<BN, EPI>, grid, dim3(128), smem, st, a, b, b2, args), "gemm_tc_kernel");
+  return launched(launch_pdl(gemm_tc_kernel<BN, EPI>, grid, dim3(192), smem, st, a, b, b2, args), "gemm_tc_kernel");
 }
 
 template <int EPI>
@@ -481,7 +569,12 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
 
   const int64_t n_tiles = swiglu ? cdiv(n_out, bn / 2) : cdiv(n_out, bn);
   args.n_tiles = (int)n_tiles;
-  dim3 grid((unsigned)n_tiles, (unsigned)cdiv(g.M, kBM), (unsigned)splits);
+  args.m_tiles = (int)cdiv(g.M, kBM);
+  args.n_tiles_grid = (int)n_tiles;
+  args.splits = splits;
+  const int64_t tiles = (int64_t)args.m_tiles * n_tiles * splits;
+  BI_REQUIRE_SHAPE(tiles < (1ll << 31), "too many tiles");
+  dim3 grid((unsigned)std::min<int64_t>(tiles, num_sms()));
   int epi;
   if (g.lse) {
     if (splits != 1) return fail(BI_ERR_INVALID_ARG, "fused log-softmax cannot run split-K");
