@@ -273,6 +273,7 @@ def run_ours(args):
 
     # roofline of the dominant kernel (timed live, same shapes as in the step)
     roof = roofline_probe(dec, ep, args)
+    kernels = kernel_table(args) if not args.no_kernels else None
 
     # CPU oracle baseline on a bounded sample (rank 0, N = 1 only), also a parity spot check
     cpu = None
@@ -296,6 +297,7 @@ def run_ours(args):
                 "non_invariant": {"value": fast_value, "ms_per_step": ms_fast,
                                   "invariant_fraction": value / fast_value},
                 "roofline": roof,
+                "kernels": kernels,
                 "cpu_baseline": cpu,
                 "oracle_max_abs_err": parity,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(prompt_host.numel() * 4),
@@ -307,35 +309,159 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def _graph_us(fn, n=20, reps=10):
+    """Per-launch device time of `fn` replayed from a CUDA graph of n launches (CUDA events)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1000.0 / (n * reps)
+
+
 def roofline_probe(dec, ep, args):
-    """Time the lm_head GEMM of a decode step (M = 16 rows, N = 32000, K = 512, fp32
-    out) the way the step launches it, L2 state as in decode (weights resident)."""
+    """Roofline of the step's dominant kernel class, the decode-size tcgen05 GEMMs
+    (QKV, O, gate/up+SwiGLU, down of every layer and the fused lm_head+logprob):
+    each is launched at its decode shape (M = 16) from a CUDA graph, the way the
+    decode step runs it, and timed with CUDA events.  achieved = the algorithmic
+    bytes of one decode step's GEMMs (weights + activations in + out) / their
+    summed launch time.  The weights are L2-resident across decode steps (the
+    58.5 MB model fits the 129 MB L2): these launches are latency-bound."""
     import torch
     import invariant_forward_policy_gb300 as bi
     hbm, tf, tf_s, src = _peaks()
     s = dec.shape
-    M, N, K = ep.B, s.vocab, s.d
+    B, d, F, V = ep.B, s.d, s.ffn, s.vocab
+    nqkv = (s.n_heads_q + 2 * s.n_heads_kv) * s.head_dim
+    hq = s.n_heads_q * s.head_dim
     dev = dec.device
-    A = torch.randn((M, K), device=dev).to(torch.bfloat16)
-    C = torch.empty((M, N), dtype=torch.float32, device=dev)
-    W = dec.w["lm_head"]
-    for _ in range(5):
-        bi.bi_gemm(A, M, K, W, N, C, bi.BI_DTYPE_FP32)
-    n = 200
-    st = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(n):
-        bi.bi_gemm(A, M, K, W, N, C, bi.BI_DTYPE_FP32)
-    e1.record(st)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1000.0 / n
-    algo_bytes = N * K * 2 + M * K * 2 + M * N * 4
-    achieved = algo_bytes / (us * 1e-6) / 1e9
-    return {"kernel": "gemm_tc_kernel (lm_head, decode M=16, N=32000, K=512, fp32 out)", "bound": "hbm",
-            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
-            "us_per_launch": us, "algorithmic_bytes": algo_bytes, "peak_source": src,
-            "note": "weights are L2-resident across decode steps (58.5 MB model < 129 MB L2)"}
+    lw = dec.layers[0]
+    x = (0.5 * torch.randn((B, max(d, hq, F)), device=dev)).to(torch.bfloat16)
+    outs = torch.empty((B, max(nqkv, d, F)), dtype=torch.bfloat16, device=dev)
+    lp = torch.empty(B, dtype=torch.float32, device=dev)
+    am = torch.empty(B, dtype=torch.int32, device=dev)
+    wsh = torch.empty(bi.bi_lm_head_logprob_workspace_size(B, V, d), dtype=torch.uint8, device=dev)
+    xd, xh, xf = x[:, :d].contiguous(), x[:, :hq].contiguous(), x[:, :F].contiguous()
+    shapes = [
+        ("qkv", lambda: bi.bi_gemm(xd, B, d, lw["wqkv"], nqkv, outs), nqkv * d * 2 + B * d * 2 + B * nqkv * 2),
+        ("o", lambda: bi.bi_gemm(xh, B, hq, lw["wo"], d, outs), d * hq * 2 + B * hq * 2 + B * d * 2),
+        ("gate_up_swiglu", lambda: bi.bi_gemm(xd, B, d, lw["w13"], 2 * F, outs, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU),
+         2 * F * d * 2 + B * d * 2 + B * F * 2),
+        ("down", lambda: bi.bi_gemm(xf, B, F, lw["w2"], d, outs), d * F * 2 + B * F * 2 + B * d * 2),
+    ]
+    per_step_us, per_step_bytes, detail = 0.0, 0, {}
+    for name, fn, nbytes in shapes:
+        us = _graph_us(fn)
+        detail[name] = round(us, 2)
+        per_step_us += s.n_layers * us
+        per_step_bytes += s.n_layers * nbytes
+    us = _graph_us(lambda: bi.bi_lm_head_logprob(xd, B, d, dec.w["lm_head"], V, None, lp, am, bi.BI_INVARIANT, wsh))
+    detail["lm_head_logprob_fused"] = round(us, 2)
+    per_step_us += us
+    per_step_bytes += V * d * 2 + B * d * 2 + B * 8
+    achieved = per_step_bytes / (per_step_us * 1e-6) / 1e9
+    return {"kernel": "gemm_tc_kernel, decode-size launches of one decode step (M 16: QKV, O, gate/up+SwiGLU, "
+                      "down per layer; fused lm_head + log-softmax)",
+            "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": None, "us_per_decode_step": round(per_step_us, 2), "us_per_launch": detail,
+            "algorithmic_bytes_per_decode_step": per_step_bytes, "peak_source": src,
+            "note": "weights L2-resident across decode steps; launches are latency-bound (one 128-row tile, "
+                    "16 valid rows); frac of the HBM copy peak"}
+
+
+def kernel_table(args):
+    """Achieved rates of the other kernels at their workload shapes (CUDA events,
+    warm L2 unless stated): decode attention of the long-context decoder (HBM),
+    vocab-wide logprob (HBM), RMSNorm (HBM), and the large GEMMs (tensor)."""
+    import torch
+    import invariant_forward_policy_gb300 as bi
+    from synthetic import C5, make_c5_prompt_lengths
+    hbm, tf, tf_s, src = _peaks()
+    dev = torch.device("cuda")
+    out = {}
+    # decode attention, long-context GQA shape: 64 sequences, contexts 1K-32K log-uniform, 4 kv heads x 128
+    lens = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"])
+    B, Hq, Hkv, hd = len(lens), 16, 4, 128
+    mb = int(-(-lens.max() // 64))
+    nblk = int(sum(-(-int(n) // 64) for n in lens))
+    kc = (0.5 * torch.randn((nblk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+    vc = (0.5 * torch.randn((nblk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+    tab = torch.full((B, mb), -1, dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(lens):
+        k = -(-int(n) // 64)
+        tab[b, :k] = torch.arange(o, o + k, dtype=torch.int32)
+        o += k
+    bt = tab.to(dev)
+    q = (0.5 * torch.randn((B, Hq, hd), device=dev)).to(torch.bfloat16)
+    seq = torch.arange(B, dtype=torch.int32, device=dev)
+    row0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+    pos0 = torch.from_numpy((lens - 1).astype("int32")).to(dev)
+    ao = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
+    max_ctx = int(lens.max())
+    ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, max_ctx, 512), dtype=torch.uint8, device=dev)
+    us = _graph_us(lambda: bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, mb, max_ctx, 512,
+                                           hd ** -0.5, ws, ao), n=5, reps=5)
+    nbytes = int(lens.sum()) * Hkv * hd * 2 * 2
+    out["attention_decode_long_context"] = {"shape": f"64 seqs, ctx {int(lens.min())}-{max_ctx} (sum {int(lens.sum())}), "
+                                            "16/4 heads x 128, split 512", "us": round(us, 1),
+                                            "GB/s": round(nbytes / us / 1e3, 1), "frac": round(nbytes / us / 1e3 / hbm, 3),
+                                            "bound": "hbm", "note": "KV (1.2 GB) exceeds L2"}
+    del kc, vc
+    # vocab-wide logprob, large-vocab shape (8.47 GB of fp32 logits, > L2)
+    T, Vv = 16384, 129280
+    logits = torch.randn((T, Vv), device=dev)
+    lp = torch.empty(T, device=dev)
+    ids = torch.randint(0, Vv, (T,), dtype=torch.int32, device=dev)
+    us = _graph_us(lambda: bi.bi_logprob_gather(logits, ids, T, Vv, lp), n=2, reps=3)
+    out["logprob_16384x129280"] = {"us": round(us, 1), "GB/s": round(T * Vv * 4 / us / 1e3, 1),
+                                   "frac": round(T * Vv * 4 / us / 1e3 / hbm, 3), "bound": "hbm"}
+    del logits
+    # RMSNorm with residual add, 65536 rows x 2048 (read x, residual, write residual, y: 4 x 268 MB)
+    Rr, dd = 65536, 2048
+    xx = torch.randn((Rr, dd), device=dev).to(torch.bfloat16)
+    rr = torch.randn((Rr, dd), device=dev).to(torch.bfloat16)
+    yy = torch.empty_like(xx)
+    gg = torch.ones(dd, device=dev).to(torch.bfloat16)
+    us = _graph_us(lambda: bi.bi_rmsnorm(xx, rr, gg, yy, Rr, dd), n=5, reps=5)
+    out["rmsnorm_residual_65536x2048"] = {"us": round(us, 1), "GB/s": round(4 * Rr * dd * 2 / us / 1e3, 1),
+                                          "frac": round(4 * Rr * dd * 2 / us / 1e3 / hbm, 3), "bound": "hbm"}
+    del xx, rr, yy
+    # tensor-bound GEMMs: fused large-vocab lm_head + log-softmax, prefill FFN
+    def gemm_rate(M, N, K, fn_builder, tag):
+        fn, flops = fn_builder(M, N, K)
+        us = _graph_us(fn, n=2, reps=3)
+        out[tag] = {"us": round(us, 1), "TFLOP/s": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / tf, 3),
+                    "bound": "tensor"}
+
+    def fused_head(M, N, K):
+        X = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        W = (0.01 * torch.randn((N, K), device=dev)).to(torch.bfloat16)
+        I = torch.randint(0, N, (M,), dtype=torch.int32, device=dev)
+        L = torch.empty(M, device=dev)
+        Wk = torch.empty(bi.bi_lm_head_logprob_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+        return (lambda: bi.bi_lm_head_logprob(X, M, K, W, N, I, L, None, bi.BI_INVARIANT, Wk)), 2.0 * M * N * K
+
+    def ffn_gate_up(M, N, K):
+        X = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        W = (0.02 * torch.randn((N, K), device=dev)).to(torch.bfloat16)
+        C = torch.empty((M, N // 2), device=dev, dtype=torch.bfloat16)
+        return (lambda: bi.bi_gemm(X, M, K, W, N, C, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)), 2.0 * M * N * K
+
+    gemm_rate(16384, 129280, 4096, fused_head, "lm_head_logprob_fused_16384x129280x4096")
+    gemm_rate(16384, 11264, 2048, ffn_gate_up, "gate_up_swiglu_16384x11264x2048")
+    out["peak_source"] = src
+    return out
 
 
 def run_kernel_case(name: str, reps: int):
@@ -385,6 +511,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-kernels", action="store_true", help="skip the per-kernel rate table")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.kernel_case:

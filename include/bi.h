@@ -135,6 +135,19 @@ bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq,
                            const float* rope_table, int64_t max_pos, const int32_t* block_table,
                            int64_t max_blocks_per_seq, int64_t n_blocks, void* q_out, void* k_cache,
                            void* v_cache, void* stream);
+/* QKV projection with RoPE and the paged K/V write fused into the GEMM
+ * epilogue: x [T, K] x Wqkv [(Hq + 2 Hkv) hd, K]^T, each q/k/v value rounded to
+ * bf16 as bi_gemm would, then q and k rotated and everything written exactly as
+ * bi_rope_kv_write does for row t at (row_seq[t], row_pos[t]) (device int32
+ * [T]).  Same bits as the two calls, without the bf16 qkv round trip.  The
+ * GEMM tile width is a multiple of hd (a tile holds whole heads).  The caller
+ * guarantees 0 <= row_seq[t] < rows of block_table; a position outside
+ * [0, max_pos) or a block id outside [0, n_blocks) skips that row's writes and
+ * sets the device status (bi_device_status). */
+bi_status bi_qkv_rope_kv_write(const void* x, int64_t T, int64_t K, const void* wqkv, int Hq, int Hkv, int hd,
+                               const int32_t* row_seq, const int32_t* row_pos, const float* rope_table,
+                               int64_t max_pos, const int32_t* block_table, int64_t max_blocks_per_seq,
+                               int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int mode, void* stream);
 /* rope_table[p, i] = cos(p * theta^(-2i/hd)), rope_table[p, hd/2 + i] = sin(...),
  * angles and functions evaluated in fp64 on the device, rounded to fp32. */
 bi_status bi_rope_table(float* rope_table, int64_t max_pos, int hd, double theta, void* stream);

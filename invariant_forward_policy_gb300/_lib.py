@@ -69,6 +69,8 @@ _SIGS = {
     "bi_rope_kv_write": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _i64, _vp, _i64, _i64,
                                 _vp, _vp, _vp, _vp]),
     "bi_rope_table": (_int, [_vp, _i64, _int, _f64, _vp]),
+    "bi_qkv_rope_kv_write": (_int, [_vp, _i64, _i64, _vp, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
+                                    _vp, _vp, _int, _vp]),
     "bi_attention": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _i64, _int,
                             _f32, _vp, _sz, _vp, _int, _vp]),
     "bi_attention_workspace_size": (_sz, [_i64, _int, _int, _i64, _int]),
@@ -190,6 +192,13 @@ def bi_gemm_tile_n(N, K, epilogue=BI_EPI_NONE) -> int:
 def bi_grouped_gemm(A, M_rows, K, W, E, N, tile_expert, C, c_dtype=BI_DTYPE_BF16, epilogue=BI_EPI_NONE, stream=None):
     _check(load().bi_grouped_gemm(_p(A), M_rows, K, _p(W), E, N, _p(tile_expert), _p(C), c_dtype, epilogue,
                                   _s(stream)))
+
+
+def bi_qkv_rope_kv_write(x, T, K, wqkv, Hq, Hkv, hd, row_seq, row_pos, rope_table, max_pos, block_table,
+                         max_blocks_per_seq, n_blocks, q_out, k_cache, v_cache, mode=BI_INVARIANT, stream=None):
+    _check(load().bi_qkv_rope_kv_write(_p(x), T, K, _p(wqkv), Hq, Hkv, hd, _p(row_seq), _p(row_pos), _p(rope_table),
+                                       max_pos, _p(block_table), max_blocks_per_seq, n_blocks, _p(q_out), _p(k_cache),
+                                       _p(v_cache), mode, _s(stream)))
 
 
 def bi_rope_table(table, max_pos, hd, theta=10000.0, stream=None):

@@ -77,6 +77,13 @@ bi_status lm_head_logprob_to(const void* X, int64_t T, int64_t K, const void* W,
                              float* logprob_out, int32_t* argmax_out, const int32_t* dst, int mode, void* workspace,
                              size_t ws_bytes, void* stream);
 size_t lm_head_partial_bytes(int64_t T, int64_t V, int64_t K, int mode);
+// QKV projection whose epilogue applies RoPE (q, k) and writes k, v into the
+// paged cache at each row's (row_seq, row_pos): the same values as bi_gemm
+// followed by bi_rope_kv_write, without the bf16 qkv round trip.
+bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int64_t N, const int32_t* row_seq,
+                        const int32_t* row_pos, const float* rope_table, int64_t max_pos, const int32_t* block_table,
+                        int64_t max_blk, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int Hq, int Hkv,
+                        int hd, int mode, void* stream);
 
 // TMA descriptor encode (driver entry point looked up through the runtime).
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

@@ -22,7 +22,28 @@
 
 namespace bi {
 
-enum EpiKind : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_SWIGLU = 2, EPI_PARTIAL = 3, EPI_PARTIAL_SWIGLU = 4, EPI_LSE = 5 };
+enum EpiKind : int {
+  EPI_BF16 = 0,
+  EPI_F32 = 1,
+  EPI_SWIGLU = 2,
+  EPI_PARTIAL = 3,
+  EPI_PARTIAL_SWIGLU = 4,
+  EPI_LSE = 5,
+  EPI_ROPE = 6
+};
+
+// Operands of the QKV epilogue that applies RoPE and writes K/V into the paged cache.
+struct RopeKvArgs {
+  const int32_t* row_seq;   // [M] sequence of each row
+  const int32_t* row_pos;   // [M] absolute position of each row
+  const float* table;       // [max_pos, hd]: cos | sin
+  const int32_t* block_table;
+  __nv_bfloat16* q_out;     // [M, Hq, hd]
+  __nv_bfloat16* k_cache;   // [n_blocks, Hkv, 64, hd] (one layer)
+  __nv_bfloat16* v_cache;
+  int64_t max_pos, max_blk, n_blocks;
+  int Hq, Hkv, hd;
+};
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -53,6 +74,7 @@ struct GemmArgs {
   TileLse* lse;             // EPI_LSE: [M, n_tiles] tile partials
   int n_tiles;              // EPI_LSE: vocab tiles per row
   int m_tiles, n_tiles_grid, splits;  // tile space walked by the persistent CTAs
+  RopeKvArgs rope;                    // EPI_ROPE only
 };
 
 // Online (max, sum-exp, argmax) over 4 consecutive logits, in column order.
@@ -126,6 +148,82 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
           *reinterpret_cast<float4*>(pu + col) =
               make_float4(__uint_as_float(u[q * 4]), __uint_as_float(u[q * 4 + 1]), __uint_as_float(u[q * 4 + 2]),
                           __uint_as_float(u[q * 4 + 3]));
+        }
+      }
+    }
+  } else if (EPI == EPI_ROPE) {
+    // q/k heads: rotate-half pairs (j, j + hd/2) of bf16(acc) in fp32, rounded
+    // to bf16; q to q_out, k and v into the paged cache at the row's position.
+    const RopeKvArgs& ra = args.rope;
+    const int hd = ra.hd, half = hd / 2;
+    const int n0 = n_tile * BN;
+    bool ok = do_store && row_ok;
+    int64_t pos = 0, blk = -1;
+    if (ok) {
+      const int seq = ra.row_seq[row];
+      pos = ra.row_pos[row];
+      if (pos < 0 || pos >= ra.max_pos) {
+        report(args.status, DEV_BAD_INDEX);
+        ok = false;
+      } else {
+        const int32_t b = (pos / 64 < ra.max_blk) ? ra.block_table[(int64_t)seq * ra.max_blk + pos / 64] : -1;
+        if (b >= 0 && b < ra.n_blocks) blk = b;
+        else report(args.status, DEV_BAD_INDEX);
+      }
+    }
+    const int slot = (int)(pos % 64);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int n = n0 + c;
+      const int h = n / hd, j0 = n % hd;
+      if (h < ra.Hq + ra.Hkv) {
+        if (j0 >= half) continue;  // done together with its partner chunk
+        uint32_t x1[32], x2[32];
+        tmem_ld_32x32b_x32(t_row + c, x1);
+        tmem_ld_32x32b_x32(t_row + c + half, x2);
+        tmem_ld_wait();
+        if (!ok) continue;
+        __nv_bfloat16* dst;
+        if (h < ra.Hq) dst = ra.q_out + ((int64_t)row * ra.Hq + h) * hd;
+        else if (blk >= 0) dst = ra.k_cache + (((int64_t)blk * ra.Hkv + (h - ra.Hq)) * 64 + slot) * hd;
+        else continue;
+        const float* cs = ra.table + pos * hd;
+        uint32_t o1[16], o2[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float a1[2], a2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float v1 = bf2f(f2bf(__uint_as_float(x1[i + e])));
+            const float v2 = bf2f(f2bf(__uint_as_float(x2[i + e])));
+            const float cc = cs[j0 + i + e], ss = cs[half + j0 + i + e];
+            a1[e] = __fsub_rn(__fmul_rn(v1, cc), __fmul_rn(v2, ss));
+            a2[e] = __fadd_rn(__fmul_rn(v2, cc), __fmul_rn(v1, ss));
+          }
+          o1[i / 2] = pack_bf16x2(a1[0], a1[1]);
+          o2[i / 2] = pack_bf16x2(a2[0], a2[1]);
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          reinterpret_cast<uint4*>(dst + j0)[v] = make_uint4(o1[4 * v], o1[4 * v + 1], o1[4 * v + 2], o1[4 * v + 3]);
+          reinterpret_cast<uint4*>(dst + j0 + half)[v] =
+              make_uint4(o2[4 * v], o2[4 * v + 1], o2[4 * v + 2], o2[4 * v + 3]);
+        }
+      } else {
+        uint32_t x[32];
+        tmem_ld_32x32b_x32(t_row + c, x);
+        tmem_ld_wait();
+        if (!ok || blk < 0) continue;
+        __nv_bfloat16* dst =
+            ra.v_cache + (((int64_t)blk * ra.Hkv + (h - ra.Hq - ra.Hkv)) * 64 + slot) * hd + j0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(x[8 * v + 0]), __uint_as_float(x[8 * v + 1]));
+          w.y = pack_bf16x2(__uint_as_float(x[8 * v + 2]), __uint_as_float(x[8 * v + 3]));
+          w.z = pack_bf16x2(__uint_as_float(x[8 * v + 4]), __uint_as_float(x[8 * v + 5]));
+          w.w = pack_bf16x2(__uint_as_float(x[8 * v + 6]), __uint_as_float(x[8 * v + 7]));
+          reinterpret_cast<uint4*>(dst)[v] = w;
         }
       }
     }
@@ -480,6 +578,7 @@ static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUten
     case EPI_PARTIAL: return dispatch_bn<EPI_PARTIAL>(bn, a, b, b2, args, grid, st);
     case EPI_PARTIAL_SWIGLU: return dispatch_bn<EPI_PARTIAL_SWIGLU>(bn, a, b, b2, args, grid, st);
     case EPI_LSE: return dispatch_bn<EPI_LSE>(bn, a, b, b2, args, grid, st);
+    case EPI_ROPE: return dispatch_bn<EPI_ROPE>(bn, a, b, b2, args, grid, st);
   }
   return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad epilogue");
 }
@@ -520,6 +619,7 @@ struct GemmCall {
   size_t ws_bytes;
   const int32_t* ids = nullptr;  // fused log-softmax: targets (NULL = greedy)
   TileLse* lse = nullptr;        // fused log-softmax: tile partials (non-NULL selects it)
+  const RopeKvArgs* rope = nullptr;  // fused RoPE + paged KV write (non-NULL selects it)
 };
 
 static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
@@ -532,7 +632,12 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   int bn = tile_n_for(g.n_rows_w, g.K, swiglu), splits = 1;
   if (g.mode == BI_FAST && g.E == 1) {
     fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
-    if (g.lse) splits = 1;  // the fused head keeps whole K per tile; FAST narrows the tiles instead
+    if (g.lse || g.rope) splits = 1;  // fused epilogues keep whole K per tile; FAST narrows the tiles instead
+  }
+  if (g.rope) {
+    // a tile must hold whole heads so that rotate-half pairs meet in one thread
+    while (bn < g.rope->hd) bn *= 2;
+    if (bn % g.rope->hd) return fail(BI_ERR_UNSUPPORTED_SHAPE, "QKV tile width must be a multiple of head_dim");
   }
   const int64_t kblocks = g.K / kBK;
 
@@ -566,6 +671,7 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   args.ldp = (int)g.n_rows_w;
   args.ids = g.ids;
   args.lse = g.lse;
+  if (g.rope) args.rope = *g.rope;
 
   const int64_t n_tiles = swiglu ? cdiv(n_out, bn / 2) : cdiv(n_out, bn);
   args.n_tiles = (int)n_tiles;
@@ -579,6 +685,8 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   if (g.lse) {
     if (splits != 1) return fail(BI_ERR_INVALID_ARG, "fused log-softmax cannot run split-K");
     epi = EPI_LSE;
+  } else if (g.rope) {
+    epi = EPI_ROPE;
   } else if (splits > 1) {
     if (g.ws_bytes < partial_bytes(g.M, g.n_rows_w, splits) || !g.ws)
       return fail(BI_ERR_INVALID_ARG, "bi_gemm: BI_FAST split-K needs workspace (bi_gemm_workspace_size)");
@@ -707,3 +815,41 @@ bi_status bi_lm_head_logprob(const void* X, int64_t T, int64_t K, const void* W,
 }
 
 }  // extern "C"
+
+// ------------------------------------------- fused QKV + RoPE + paged KV write
+namespace bi {
+
+bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int64_t N, const int32_t* row_seq,
+                        const int32_t* row_pos, const float* rope_table, int64_t max_pos, const int32_t* block_table,
+                        int64_t max_blk, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int Hq, int Hkv,
+                        int hd, int mode, void* stream) {
+  BI_REQUIRE(M >= 0 && K > 0 && N > 0, "bad shape");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(A && W && row_seq && row_pos && rope_table && block_table && q_out && k_cache && v_cache, "null pointer");
+  BI_REQUIRE(N == (int64_t)(Hq + 2 * Hkv) * hd, "N must be (Hq + 2 Hkv) * head_dim");
+  BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
+  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
+  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache),
+             "pointers must be 16-byte aligned");
+  RopeKvArgs ra{row_seq, row_pos, rope_table, block_table, static_cast<__nv_bfloat16*>(q_out),
+                static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), max_pos, max_blk,
+                n_blocks, Hq, Hkv, hd};
+  GemmCall g{A, M, K, W, N, 1, nullptr, q_out, BI_DTYPE_BF16, BI_EPI_NONE, mode, nullptr, 0};
+  g.rope = &ra;
+  return run_gemm(g, as_stream(stream));
+}
+
+}  // namespace bi
+
+extern "C" bi_status bi_qkv_rope_kv_write(const void* x, int64_t T, int64_t K, const void* wqkv, int Hq, int Hkv,
+                                          int hd, const int32_t* row_seq, const int32_t* row_pos,
+                                          const float* rope_table, int64_t max_pos, const int32_t* block_table,
+                                          int64_t max_blocks_per_seq, int64_t n_blocks, void* q_out, void* k_cache,
+                                          void* v_cache, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0, "bad heads");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  BI_REQUIRE(max_pos > 0 && max_blocks_per_seq > 0 && n_blocks > 0, "bad table / cache shape");
+  return gemm_qkv_rope(x, T, K, wqkv, (int64_t)(Hq + 2 * Hkv) * hd, row_seq, row_pos, rope_table, max_pos,
+                       block_table, max_blocks_per_seq, n_blocks, q_out, k_cache, v_cache, Hq, Hkv, hd, mode, stream);
+}

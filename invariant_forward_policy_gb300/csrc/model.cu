@@ -46,6 +46,8 @@ struct DevMeta {
   int32_t* logit_src;  // pass row of each logit row
   int32_t* logit_dst;  // call row of each logit row
   int32_t* logit_tgt;  // target id of each logit row (or -1)
+  int32_t* row_seq;    // sequence of every pass row
+  int32_t* row_pos;    // absolute position of every pass row
 };
 
 __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ tokens,
@@ -71,6 +73,8 @@ __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ 
   const int i = r - pm.row0[p];
   const int tok = pm.tok0[p] + i;
   dm.ids[r] = tokens[tok];
+  dm.row_seq[r] = pm.seq[p];
+  dm.row_pos[r] = pm.pos0[p] + i;
   if (i >= pm.lfirst[p]) {
     const int j = pm.loff[p] + (i - pm.lfirst[p]);
     dm.logit_src[j] = r;
@@ -94,6 +98,8 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
     dm.piece_row0[b] = b;
     dm.piece_pos0[b] = pos[b];
     dm.ids[b] = id;
+    dm.row_seq[b] = b;
+    dm.row_pos[b] = pos[b];
     dm.logit_src[b] = b;
     dm.logit_dst[b] = b;
     dm.logit_tgt[b] = -1;
@@ -107,8 +113,8 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
 
 // ------------------------------------------------------------- workspace plan
 struct FwdLayout {
-  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt;
-  size_t h, x, qkv, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
+  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos;
+  size_t h, x, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
   size_t attn_ws_bytes, gemm_ws_bytes, lp_ws_bytes;
   size_t total;
 };
@@ -130,9 +136,11 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   L.logit_src = take(std::max(Tm, Rm) * 4);
   L.logit_dst = take(std::max(Tm, Rm) * 4);
   L.logit_tgt = take(std::max(Tm, Rm) * 4);
+  L.row_seq = take(Tm * 4);
+  L.row_pos = take(Tm * 4);
   L.h = take(Tm * c.d * 2);
   L.x = take(Tm * c.d * 2);
-  L.qkv = take(Tm * nqkv * 2);
+
   L.q = take(Tm * hq * 2);
   L.ao = take(Tm * hq * 2);
   L.tmp = take(Tm * c.d * 2);
@@ -185,7 +193,7 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
   auto* piece_pos0 = at<int32_t>(ws, L.piece_pos0);
   void* h = at<void>(ws, L.h);
   void* x = at<void>(ws, L.x);
-  void* qkv = at<void>(ws, L.qkv);
+
   void* q = at<void>(ws, L.q);
   void* ao = at<void>(ws, L.ao);
   void* tmp = at<void>(ws, L.tmp);
@@ -209,9 +217,10 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     const bi_layer_weights& lw = m->layers[li];
     void* kc = static_cast<uint8_t*>(k_cache) + li * layer_cache;
     void* vc = static_cast<uint8_t*>(v_cache) + li * layer_cache;
-    BI_TRY(bi_gemm(x, T, c.d, lw.wqkv, nqkv, qkv, BI_DTYPE_BF16, BI_EPI_NONE, mode, gws, L.gemm_ws_bytes, stream));
-    BI_TRY(bi_rope_kv_write(qkv, T, piece_seq, piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq, Hkv, hd,
-                            m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, stream));
+    // QKV projection with RoPE and the paged K/V write fused into its epilogue
+    BI_TRY(gemm_qkv_rope(x, T, c.d, lw.wqkv, nqkv, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos),
+                         m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd, mode,
+                         stream));
     BI_TRY(bi_attention(q, T, piece_seq, piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq, Hkv, hd, kc, vc,
                         block_table, max_blk, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
                         L.attn_ws_bytes, ao, mode, stream));
@@ -392,7 +401,8 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
     DevMeta dm{at<int32_t>(workspace, L.piece_seq), at<int32_t>(workspace, L.piece_row0),
                at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids),
                at<int32_t>(workspace, L.logit_src), at<int32_t>(workspace, L.logit_dst),
-               at<int32_t>(workspace, L.logit_tgt)};
+               at<int32_t>(workspace, L.logit_tgt), at<int32_t>(workspace, L.row_seq),
+               at<int32_t>(workspace, L.row_pos)};
     BI_TRY(launched(launch_pdl(pass_meta_kernel, dim3((unsigned)cdiv(std::max<int64_t>(rows, 1), 256)), dim3(256), 0,
                                st, pm, tokens, target_ids, dm),
                     "pass_meta_kernel"));
@@ -420,7 +430,8 @@ bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* p
   BI_REQUIRE(ws_bytes >= L.total, "forward workspace too small (bi_forward_workspace_size(cfg, B, B, max_ctx, B))");
   DevMeta dm{at<int32_t>(workspace, L.piece_seq), at<int32_t>(workspace, L.piece_row0),
              at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids), at<int32_t>(workspace, L.logit_src),
-             at<int32_t>(workspace, L.logit_dst), at<int32_t>(workspace, L.logit_tgt)};
+             at<int32_t>(workspace, L.logit_dst), at<int32_t>(workspace, L.logit_tgt),
+             at<int32_t>(workspace, L.row_seq), at<int32_t>(workspace, L.row_pos)};
   const cudaStream_t st = as_stream(stream);
   BI_TRY(launched(launch_pdl(decode_embed_kernel, dim3((unsigned)B), dim3(128), 0, st, tokens, pos, (int)B, dm,
                              static_cast<const __nv_bfloat16*>(m->embed), m->cfg.vocab, m->cfg.d,

@@ -373,3 +373,39 @@ def test_moe_rows_invariant_to_batching_and_layout():
     out = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     bi.bi_moe_combine(y, ros, w, T, k, d, out)
     assert same_bits(out, full)
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd", [(8, 8, 64), (16, 4, 128)])
+def test_fused_qkv_rope_kv_write_equals_gemm_then_rope(Hq, Hkv, hd):
+    """The QKV GEMM with RoPE + paged K/V write in its epilogue gives the same q
+    and cache bits as bi_gemm followed by bi_rope_kv_write."""
+    rng = np.random.default_rng(Hq + hd)
+    seq_lens = [130, 1, 77]
+    T, K = sum(seq_lens), 512
+    N = (Hq + 2 * Hkv) * hd
+    xb, _ = rng_bf16(rng, (T, K))
+    wb, _ = rng_bf16(rng, (N, K), 0.05)
+    X, W = dev_bf16(xb), dev_bf16(wb)
+    max_pos = 1024
+    table = torch.empty((max_pos, hd), dtype=torch.float32, device="cuda")
+    bi.bi_rope_table(table, max_pos, hd, 10000.0)
+    starts = [3, 0, 200]                      # rows sit at positions start + i
+    bt, kc1, vc1, max_blk, n_blocks = _paged_setup([s + n for s, n in zip(starts, seq_lens)], Hq, Hkv, hd, rng)
+    kc1.zero_()
+    vc1.zero_()
+    kc2, vc2 = torch.zeros_like(kc1), torch.zeros_like(vc1)
+    seq, row0, pos0 = _pieces([(b, starts[b], n) for b, n in enumerate(seq_lens)])
+    qkv = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm(X, T, K, W, N, qkv)
+    q1 = torch.empty((T, Hq, hd), dtype=torch.bfloat16, device="cuda")
+    bi.bi_rope_kv_write(qkv, T, seq, row0, pos0, len(seq_lens), max(seq_lens), Hq, Hkv, hd, table, max_pos, bt,
+                        max_blk, n_blocks, q1, kc1, vc1)
+    row_seq = torch.tensor(np.repeat(np.arange(len(seq_lens)), seq_lens), dtype=torch.int32, device="cuda")
+    row_pos = torch.tensor(np.concatenate([starts[b] + np.arange(n) for b, n in enumerate(seq_lens)]),
+                           dtype=torch.int32, device="cuda")
+    q2 = torch.empty_like(q1)
+    bi.bi_qkv_rope_kv_write(X, T, K, W, Hq, Hkv, hd, row_seq, row_pos, table, max_pos, bt, max_blk, n_blocks, q2,
+                            kc2, vc2)
+    assert same_bits(q2, q1)
+    assert same_bits(kc2, kc1) and same_bits(vc2, vc1)
+    assert bi.bi_device_status() == 0
