@@ -410,7 +410,7 @@ def kernel_table(args):
     ao = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
     max_ctx = int(lens.max())
     ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, max_ctx, 512), dtype=torch.uint8, device=dev)
-    us = _graph_us(lambda: bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, mb, max_ctx, 512,
+    us = _graph_us(lambda: bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, mb, nblk, max_ctx, 512,
                                            hd ** -0.5, ws, ao), n=5, reps=5)
     nbytes = int(lens.sum()) * Hkv * hd * 2 * 2
     out["attention_decode_long_context"] = {"shape": f"64 seqs, ctx {int(lens.min())}-{max_ctx} (sum {int(lens.sum())}), "
@@ -492,7 +492,8 @@ def run_kernel_case(name: str, reps: int):
         out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, ctx, 512), dtype=torch.uint8, device=dev)
         for _ in range(reps):
-            bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, ctx, 512, 0.125, ws, out)
+            bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, B * max_blk, ctx, 512, 0.125,
+                            ws, out)
     else:
         raise SystemExit(f"unknown kernel case {name}")
     torch.cuda.synchronize()

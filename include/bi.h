@@ -166,16 +166,18 @@ bi_status bi_rope_table(float* rope_table, int64_t max_pos, int hd, double theta
  * O = sum acc_s 2^(m_s - M), out = bf16(O / L).  Split and tile boundaries are
  * absolute positions, so a decode row reproduces its prefill row exactly.
  * q: bf16 [T, Hq, hd] (pieces as in bi_rope_kv_write); out: bf16 [T, Hq * hd].
- * hd in {64, 128}; Hq % Hkv == 0; 64 % (Hq/Hkv) == 0.  max_ctx (host value)
- * bounds every sequence's context length in this call.  workspace must hold
+ * hd in {64, 128}; Hq % Hkv == 0; 64 % (Hq/Hkv) == 0.  k_cache / v_cache
+ * hold n_blocks pages of [Hkv, 64, hd] bf16; a block id outside [0, n_blocks)
+ * is skipped and sets the device status.  max_ctx (host value) bounds every
+ * sequence's context length in this call.  workspace must hold
  * bi_attention_workspace_size(T, Hq, hd, max_ctx, kv_split) bytes.
  * In BI_FAST mode the split size is chosen from the batch (flash-decoding
  * heuristic) and results are not batch invariant. */
 bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
                        const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
                        const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale, void* workspace,
-                       size_t ws_bytes, void* out, int mode, void* stream);
+                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split, float scale,
+                       void* workspace, size_t ws_bytes, void* out, int mode, void* stream);
 size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ctx, int kv_split);
 
 /* Same computation and kernels as bi_attention (bitwise the same output), for
@@ -201,8 +203,8 @@ size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ct
 bi_status bi_attention_static_scratch(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
                                       const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv,
                                       int hd, const void* k_cache, const void* v_cache, const int32_t* block_table,
-                                      int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale,
-                                      void* out, int mode, void* stream);
+                                      int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split,
+                                      float scale, void* out, int mode, void* stream);
 
 /* ---------------------------------------------------------- embed / logprob
  * Row gather: out[t] = table[ids[t]] (bf16 [V, d] -> bf16 [T, d]).  Ids outside

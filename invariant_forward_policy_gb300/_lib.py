@@ -71,11 +71,11 @@ _SIGS = {
     "bi_rope_table": (_int, [_vp, _i64, _int, _f64, _vp]),
     "bi_qkv_rope_kv_write": (_int, [_vp, _i64, _i64, _vp, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _i64, _i64, _vp,
                                     _vp, _vp, _int, _vp]),
-    "bi_attention": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _i64, _int,
-                            _f32, _vp, _sz, _vp, _int, _vp]),
+    "bi_attention": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _i64, _i64, _i64,
+                            _int, _f32, _vp, _sz, _vp, _int, _vp]),
     "bi_attention_workspace_size": (_sz, [_i64, _int, _int, _i64, _int]),
     "bi_attention_static_scratch": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp,
-                                           _i64, _i64, _int, _f32, _vp, _int, _vp]),
+                                           _i64, _i64, _i64, _int, _f32, _vp, _int, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
     "bi_logprob_workspace_size": (_sz, [_i64, _i64, _int]),
@@ -213,19 +213,20 @@ def bi_rope_kv_write(qkv, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq
 
 
 def bi_attention(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache, block_table,
-                 max_blocks_per_seq, max_ctx, kv_split, scale, workspace, out, mode=BI_INVARIANT, stream=None):
+                 max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, workspace, out, mode=BI_INVARIANT,
+                 stream=None):
     _check(load().bi_attention(_p(q), T, _p(piece_seq), _p(piece_row0), _p(piece_pos0), P, max_q_len, Hq, Hkv, hd,
-                               _p(k_cache), _p(v_cache), _p(block_table), max_blocks_per_seq, max_ctx, kv_split, scale,
-                               _p(workspace), _nb(workspace), _p(out), mode, _s(stream)))
+                               _p(k_cache), _p(v_cache), _p(block_table), max_blocks_per_seq, n_blocks, max_ctx,
+                               kv_split, scale, _p(workspace), _nb(workspace), _p(out), mode, _s(stream)))
 
 
 def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,
-                                block_table, max_blocks_per_seq, max_ctx, kv_split, scale, out, mode=BI_INVARIANT,
-                                stream=None):
+                                block_table, max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, out,
+                                mode=BI_INVARIANT, stream=None):
     """bi_attention without a caller workspace (the library's own static scratch array)."""
     _check(load().bi_attention_static_scratch(_p(q), T, _p(piece_seq), _p(piece_row0), _p(piece_pos0), P, max_q_len,
                                               Hq, Hkv, hd, _p(k_cache), _p(v_cache), _p(block_table),
-                                              max_blocks_per_seq, max_ctx, kv_split, scale, _p(out), mode,
+                                              max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, _p(out), mode,
                                               _s(stream)))
 
 

@@ -150,15 +150,21 @@ constexpr int kKeys = 64;   // keys per tile = cache block
 // who computes a lane (all four warps in parallel for a decode tile, one warp
 // after another for a prefill tile), never the arithmetic.
 
-// One 64-key tile into the online-softmax state of 16 query rows (one warp).
+// Shared-memory byte offset of 16-byte chunk `ch` of key row `key` inside a
+// 64-key tile: HD/64 boxes of 64 keys x 128 bytes, the chunks of each row
+// XOR-swizzled by (key mod 8).  This is the layout a TMA copy with 128-byte
+// swizzle writes for a 64x64 bf16 box at a 1024-byte aligned address, and the
+// one the cp.async loader below reproduces; ldmatrix reads of 8 consecutive
+// keys at one chunk hit 8 different bank groups.
 template <int HD>
-__device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][4],
-                                          const bool (&row_valid)[2], const int (&row_pos)[2], float scale_log2,
-                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4]) {
-  constexpr int CH = HD / 8;
-  const int tq = lane & 3;
-  // S = Q K^T for 16 rows x 64 keys
-  float sc[8][4];
+__device__ __forceinline__ uint32_t kv_off(int key, int ch) {
+  return (uint32_t)((ch >> 3) * (kKeys * 128) + key * 128 + (((ch & 7) ^ (key & 7)) << 4));
+}
+
+// S = Q K^T for the warp's 16 query rows and one 64-key tile (fp32, unscaled).
+template <int HD>
+__device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD / 16][4], int lane,
+                                            float (&sc)[8][4]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
@@ -168,12 +174,20 @@ __device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, co
       const int key = j * 8 + (lane & 7);
       const int ch = kk * 2 + (lane >> 3);
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(sk + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+      ldsm_x4(sk + kv_off<HD>(key, ch), b0, b1, b2, b3);
       mma_bf16_16816(sc[j], qf[kk], b0, b1);
       mma_bf16_16816(sc[j], qf[kk + 1], b2, b3);
     }
   }
-  // online softmax (fp32), masking by select
+}
+
+// Fold one tile's scores into the online-softmax state of the warp's rows:
+// masking by select, fp32 rescaling, then O += P V with P rounded to bf16.
+template <int HD>
+__device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int key0, const bool (&row_valid)[2],
+                                            const int (&row_pos)[2], float scale_log2, int lane, float (&m)[2],
+                                            float (&l)[2], float (&acc)[HD / 8][4]) {
+  const int tq = lane & 3;
   float pr[8][4];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -214,7 +228,6 @@ __device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, co
       acc[j][h * 2 + 1] = __fmul_rn(acc[j][h * 2 + 1], alpha);
     }
   }
-  // O += P V  (P rounded to bf16)
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
     uint32_t pa[4];
@@ -227,11 +240,21 @@ __device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, co
       const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
       const int ch = j + (lane >> 4);
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(sv + (key * CH + (ch ^ (key & 7))) * 16, b0, b1, b2, b3);
+      ldsm_x4_t(sv + kv_off<HD>(key, ch), b0, b1, b2, b3);
       mma_bf16_16816(acc[j], pa, b0, b1);
       mma_bf16_16816(acc[j + 1], pa, b2, b3);
     }
   }
+}
+
+// One 64-key tile into the online-softmax state of 16 query rows (one warp).
+template <int HD>
+__device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][4],
+                                          const bool (&row_valid)[2], const int (&row_pos)[2], float scale_log2,
+                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4]) {
+  float sc[8][4];
+  attn_scores<HD>(sk, qf, lane, sc);
+  attn_update<HD>(sv, sc, key0, row_valid, row_pos, scale_log2, lane, m, l, acc);
 }
 
 // Per-thread state of one lane, as stored in shared memory between lanes.
@@ -275,15 +298,51 @@ __device__ __forceinline__ void lane_merge(LaneState<HD>& P, const float (&mq)[2
   }
 }
 
-// DECODE: the CTA's query tile fits one warp (<= 16 rows); warp w computes lane
-// w of the split from its own K/V buffer, then warp 0 merges lanes 0..3.
-// PREFILL: warp w owns rows 16w..16w+15 and walks the split's tiles in order
-// from a shared two-stage ring, merging at every lane boundary.
+// Split partial of one row pair (the two rows a thread holds) to the workspace.
+template <int HD>
+__device__ __forceinline__ void write_partial(const AttnArgs& a, const LaneState<HD>& P, const bool (&row_valid)[2],
+                                              const int (&row_pos)[2], const int (&row_tok)[2],
+                                              const int (&row_head)[2], int kv_begin, int s, int tq) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (!row_valid[h] || row_pos[h] < kv_begin) continue;
+    const int64_t pidx = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
+    float* po = a.part_o + pidx * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      *reinterpret_cast<float2*>(po + j * 8 + tq * 2) = make_float2(P.acc[j][h * 2], P.acc[j][h * 2 + 1]);
+    }
+    if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(P.m[h], P.l[h]);
+  }
+}
+
+// Query fragments (mma A layout) of the two rows a thread holds; zero for invalid rows.
+template <int HD>
+__device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row_valid)[2], const int (&row_tok)[2],
+                                             const int (&row_head)[2], int tq, uint32_t (&qf)[HD / 16][4]) {
+#pragma unroll
+  for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat16* qr = a.q + ((int64_t)row_tok[h] * a.Hq + row_head[h]) * HD + kk * 16 + tq * 2;
+      qf[kk][h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+      qf[kk][2 + h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+    }
+  }
+}
+
+// One CTA per (piece, query tile, kv head, split), two schedules:
+// PREFILL (64-row query tiles): warp w owns rows 16w..16w+15 and walks the
+// split's tiles in order from a shared two-stage cp.async ring, folding each
+// finished lane into a running state at every lane boundary.
+// DECODE (query tiles of at most 16 rows, short contexts): warp w computes
+// lane w of the split from its own one-tile buffer, then warp 0 merges the
+// lanes in order.
 template <int HD, bool DECODE>
 __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
@@ -320,17 +379,10 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     row_head[h] = kvh * a.group + (r % a.group);
   }
   uint32_t qf[HD / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __nv_bfloat16* qr = a.q + ((int64_t)row_tok[h] * a.Hq + row_head[h]) * HD + kk * 16 + tq * 2;
-      qf[kk][h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-      qf[kk][2 + h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
-    }
-  }
+  load_q_frags<HD>(a, row_valid, row_tok, row_head, tq, qf);
 
-  // copy one 64-key tile of K and V into (sk, sv), threads t0, t0+nthr, ...
+  // copy one 64-key tile of K and V into (sk, sv) with threads t0, t0 + nthr, ...;
+  // keys after max_pos are zero-filled
   auto load_tile = [&](int key0, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
     const bool tab_ok = key0 / kKeys < a.max_blk;
     const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
@@ -340,7 +392,7 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     for (int c = t0; c < kKeys * CH; c += nthr) {
       const int key = c / CH, ch = c % CH;
       const bool valid = blk_ok && (key0 + key) <= max_pos;
-      const int off = (key * CH + (ch ^ (key & 7))) * 16;
+      const int off = (int)kv_off<HD>(key, ch);
       const int64_t src = base + (int64_t)key * HD + ch * 8;
       cp_async16(sk + off, a.k_cache + (valid ? src : 0), valid);
       cp_async16(sv + off, a.v_cache + (valid ? src : 0), valid);
@@ -426,51 +478,364 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     P = *run;
     lane_merge<HD>(P, m, l, acc);
   }
+  write_partial<HD>(a, P, row_valid, row_pos, row_tok, row_head, kv_begin, s, tq);
+}
 
-  // write the split partial for rows that own this split
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if (!row_valid[h] || row_pos[h] < kv_begin) continue;
-    const int64_t pidx = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
-    float* po = a.part_o + pidx * HD;
-#pragma unroll
-    for (int j = 0; j < HD / 8; ++j) {
-      *reinterpret_cast<float2*>(po + j * 8 + tq * 2) = make_float2(P.acc[j][h * 2], P.acc[j][h * 2 + 1]);
+// ----------------------------------------------------------- decode schedule
+// Persistent DECODE schedule, for query tiles of at most 16 rows over long
+// contexts: the same per-row arithmetic as above, with the four lanes of a
+// split computed in parallel by four warps and merged in lane order by warp 0.
+// The kernel is
+// persistent (one or two CTAs per SM walk the work items (piece, split, kv
+// head) with a grid stride; each CTA first counts every piece's live splits
+// into a prefix table in shared memory) and warp-specialised:
+//   * warp 4 reads block-table entries and issues 128-byte-swizzled TMA copies
+//     of each 64-key K and V page into a kDecSlots-deep ring per consumer warp,
+//     running ahead across work items;
+//   * warps 0..3 compute lane w of each item from ring w: scores from the K
+//     page, then softmax and P*V from the V page, releasing each slot as soon
+//     as it is read;
+//   * at the end of an item warps 1..3 hand their lane state to warp 0 through
+//     shared memory (named barriers 1 and 2), and warp 0 merges and writes the
+//     split partial.
+// TMA copies whole pages, so V rows after the item's last position (slots not
+// yet written in the cache) are zeroed in shared memory before P*V; K rows
+// there only feed scores that the select-mask replaces with -inf.
+constexpr int kDecMaxPieces = 1024;      // larger decode calls take the per-CTA schedule (same bits)
+constexpr int kDecPersistentSplits = 4;  // shorter contexts take the per-CTA schedule (same bits)
+
+template <int HD>
+struct DecLayout {
+  // ring depth per consumer warp: three 16 KB pages at hd 128 (one CTA per
+  // SM); two 8 KB pages at hd 64, so that two CTAs share an SM
+  static constexpr int kDecSlots = HD == 64 ? 2 : 3;
+  static constexpr int kTile = kKeys * HD * 2;                       // one K or V page
+  static constexpr int kRing = 4 * kDecSlots * kTile;                // four rings
+  static constexpr int kStates = kRing;                              // lane states of warps 1..3
+  static constexpr int kTable = kStates + 3 * 32 * (int)sizeof(LaneState<HD>);  // int [kDecMaxPieces + 1]
+  static constexpr int kBars = kTable + (kDecMaxPieces + 2) * 4;
+  static constexpr int kAbort = kBars + 2 * 4 * kDecSlots * 8;       // full[4][S], empty[4][S]
+  static constexpr int kBytes = kAbort + 16 + 1024;                  // + alignment slack
+};
+
+// Work items are (piece, split, kv head) with the split at or before the
+// piece's last position, numbered piece by piece: item j belongs to the last
+// piece p with first[p] <= j, and j - first[p] = split * Hkv + kv head.
+struct DecItem {
+  int p, s, kvh, n_tok, row0, pos_first, max_pos, kv_begin, kv_end, seq;
+};
+
+__device__ __forceinline__ DecItem dec_item(const AttnArgs& a, const int* first, int j, int P) {
+  int lo = 0, hi = P - 1;  // first[lo] <= j < first[P]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (first[mid] <= j) lo = mid;
+    else hi = mid - 1;
+  }
+  DecItem it;
+  it.p = lo;
+  const int r = j - first[lo];
+  it.s = r / a.Hkv;
+  it.kvh = r % a.Hkv;
+  it.row0 = a.pm.row0[it.p];
+  it.n_tok = a.pm.row0[it.p + 1] - it.row0;
+  it.pos_first = a.pm.pos0[it.p];
+  it.seq = a.pm.seq[it.p];
+  it.max_pos = it.pos_first + it.n_tok - 1;
+  it.kv_begin = it.s * a.split;
+  it.kv_end = min(it.kv_begin + a.split, it.max_pos + 1);
+  return it;
+}
+
+// Bounded mbarrier wait that also gives up once another warp has set *abort.
+__device__ __forceinline__ bool dec_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      report(status, DEV_TIMEOUT);
+      *abort = 1;
+      return false;
     }
-    if (tq == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(P.m[h], P.l[h]);
   }
 }
 
-// Merge of the split partials in ascending split order, one token per CTA.
-__global__ void attention_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                       PieceMeta pm, int Hq, int hd, int nsplit, int split,
-                                       __nv_bfloat16* __restrict__ out, int* status) {
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
+    attention_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                            const __grid_constant__ CUtensorMap tmv, int P) {
+  using Lay = DecLayout<HD>;
+  constexpr int kDecSlots = Lay::kDecSlots;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);  // [4][kDecSlots]
+  uint64_t* empty = full + 4 * kDecSlots;                           // [4][kDecSlots]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kAbort);
+  int* first = reinterpret_cast<int*>(smem + Lay::kTable);          // [P + 1]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < 4 * kDecSlots; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (tid == 128) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  pdl_trigger();
+  pdl_wait();  // q, the cache pages and the piece positions come from preceding kernels
+  // items per piece: splits 0 .. last position / split (at most nsplit) times Hkv
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int n_tok = a.pm.row0[p + 1] - a.pm.row0[p];
+    const int max_pos = a.pm.pos0[p] + n_tok - 1;
+    first[p] = (n_tok > 0 && max_pos >= 0) ? min(a.nsplit, max_pos / a.split + 1) * a.Hkv : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix sum, in order
+    int run = 0;
+    for (int base = 0; base < P; base += 32) {
+      const int i = base + lane;
+      const int v = i < P ? first[i] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      if (i < P) first[i] = run + inc - v;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) first[P] = run;
+  }
+  __syncthreads();
+  const int n_items = first[P];
+  const int lane_len = ((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys;
+  const int tpl = lane_len / kKeys;  // tiles per lane
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    int issued[4] = {0, 0, 0, 0};
+    for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+      const DecItem it = dec_item(a, first, item, P);
+      const int32_t* bt = a.block_table + (int64_t)it.seq * a.max_blk;
+      // tiles in (t, w) order: index i = 4 t + w
+      for (int base = 0; base < 4 * tpl && !*abort_flag; base += 32) {
+        const int i = base + lane;
+        const int t = i >> 2, w = i & 3;
+        const int lb = it.kv_begin + w * lane_len;
+        const int le = min(lb + lane_len, it.kv_end);
+        const int key0 = lb + t * kKeys;
+        const bool need = i < 4 * tpl && key0 < le;
+        int blk = -1;
+        if (need) {
+          blk = (key0 / kKeys < a.max_blk) ? bt[key0 / kKeys] : -1;
+          if (blk < 0 || blk >= a.n_blocks) {
+            report(a.status, DEV_BAD_INDEX);
+            blk = -1;
+          }
+        }
+        const unsigned need_mask = __ballot_sync(0xffffffffu, need);
+        for (int j = 0; j < 32; ++j) {
+          if (!((need_mask >> j) & 1u)) continue;
+          const int bj = __shfl_sync(0xffffffffu, blk, j);
+          const int wj = (base + j) & 3;
+          int nok = 0;  // pages of this tile issued (K, then V)
+          if (lane == 0) {
+            for (int kv = 0; kv < 2; ++kv) {
+              const int n = issued[wj] + kv;
+              const int slot = wj * kDecSlots + n % kDecSlots;
+              if (!dec_wait(&empty[slot], ((n / kDecSlots) & 1) ^ 1, abort_flag, a.status)) break;
+              uint8_t* dst = smem + slot * Lay::kTile;
+              if (bj >= 0) {
+                mbar_arrive_expect_tx(&full[slot], Lay::kTile);
+                const int y = (bj * a.Hkv + it.kvh) * kKeys;
+#pragma unroll
+                for (int bx = 0; bx < HD / 64; ++bx)
+                  tma_load_2d(dst + bx * kKeys * 128, kv ? &tmv : &tmk, &full[slot], bx * 64, y);
+              } else {
+                mbar_arrive(&full[slot]);  // bad block (reported): the page is left as it was
+              }
+              ++nok;
+            }
+          }
+          nok = __shfl_sync(0xffffffffu, nok, 0);
+          issued[wj] += nok;
+          if (nok < 2) break;
+        }
+      }
+    }
+    // let every copy this CTA started land before it can exit
+    if (lane == 0) {
+      for (int w = 0; w < 4; ++w)
+        for (int i = 0; i < kDecSlots && i < issued[w]; ++i) {
+          const int n = issued[w] - 1 - i;
+          mbar_wait(&full[w * kDecSlots + n % kDecSlots], (n / kDecSlots) & 1);
+        }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int g = lane >> 2, tq = lane & 3;
+  LaneState<HD>* states = reinterpret_cast<LaneState<HD>*>(smem + Lay::kStates);  // [3][32]
+  int used = 0;  // objects taken from this warp's ring
+  bool handed = false;
+  DecItem nxt;
+  if (blockIdx.x < n_items) nxt = dec_item(a, first, blockIdx.x, P);
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const DecItem it = nxt;
+    // the next item's metadata loads overlap this item's pages
+    if (item + (int)gridDim.x < n_items) nxt = dec_item(a, first, item + gridDim.x, P);
+    int row_pos[2], row_tok[2], row_head[2];
+    bool row_valid[2];
+    const int tok_per_tile = 16 / a.group;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = g + h * 8;
+      const int ti = r / a.group;
+      row_valid[h] = ti < it.n_tok && (r / a.group) < tok_per_tile;
+      row_tok[h] = it.row0 + ti;
+      row_pos[h] = it.pos_first + ti;
+      row_head[h] = it.kvh * a.group + (r % a.group);
+    }
+    uint32_t qf[HD / 16][4];
+    load_q_frags<HD>(a, row_valid, row_tok, row_head, tq, qf);
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
+    float acc[HD / 8][4];
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+
+    const int lb = it.kv_begin + warp * lane_len;
+    const int le = min(lb + lane_len, it.kv_end);
+    for (int key0 = lb; key0 < le; key0 += kKeys) {
+      float sc[8][4];
+      // K page
+      int slot = warp * kDecSlots + used % kDecSlots;
+      bool ok = dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+      if (ok) attn_scores<HD>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++used;
+      // V page
+      slot = warp * kDecSlots + used % kDecSlots;
+      ok = ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+      if (ok) {
+        uint8_t* sv = smem + slot * Lay::kTile;
+        const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
+        if (n_keys < kKeys) {
+          for (int c = n_keys * (HD / 8) + lane; c < kKeys * (HD / 8); c += 32) {
+            const int key = c / (HD / 8), ch = c % (HD / 8);
+            *reinterpret_cast<uint4*>(sv + kv_off<HD>(key, ch)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+        attn_update<HD>(smem_u32(sv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
+        fence_proxy_async();  // generic writes above before the next TMA write of this slot
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++used;
+    }
+
+    // lanes meet: warps 1..3 hand over, warp 0 merges in lane order
+    if (warp != 0) {
+      if (handed) named_bar_sync(2, 128);  // warp 0 has read the previous item's states
+      LaneState<HD>* st = states + (warp - 1) * 32 + lane;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        st->m[h] = m[h];
+        st->l[h] = l[h];
+      }
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st->acc[j][c] = acc[j][c];
+      named_bar_arrive(1, 128);
+      handed = true;
+    } else {
+      LaneState<HD> Pm;
+      Pm.m[0] = Pm.m[1] = -INFINITY;
+      Pm.l[0] = Pm.l[1] = 0.f;
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j) Pm.acc[j][0] = Pm.acc[j][1] = Pm.acc[j][2] = Pm.acc[j][3] = 0.f;
+      lane_merge<HD>(Pm, m, l, acc);
+      named_bar_sync(1, 128);
+#pragma unroll 1
+      for (int w = 1; w < 4; ++w) {
+        const LaneState<HD>* q = states + (w - 1) * 32 + lane;
+        lane_merge<HD>(Pm, q->m, q->l, q->acc);
+      }
+      named_bar_arrive(2, 128);
+      write_partial<HD>(a, Pm, row_valid, row_pos, row_tok, row_head, it.kv_begin, it.s, tq);
+    }
+  }
+  if (warp != 0 && handed) named_bar_sync(2, 128);  // pairs with warp 0's last hand-back
+}
+
+// Merge of the split partials in ascending split order.  One thread per
+// output element (row, head, d), 128 per CTA; the split records are loaded in
+// batches of kMergeBatch ahead of the in-order accumulation, so a row with many
+// splits is bound by bandwidth rather than by one load latency per split.
+constexpr int kMergeBatch = 8;
+
+__global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ part_o,
+                                                              const float* __restrict__ part_ml, PieceMeta pm,
+                                                              int Hq, int hd, int nsplit, int split,
+                                                              __nv_bfloat16* __restrict__ out, int* status) {
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
   const int i = blockIdx.x;
   const int row0 = pm.row0[p];
   if (i >= pm.row0[p + 1] - row0) return;
+  const int idx = blockIdx.z * 128 + threadIdx.x;
+  if (idx >= Hq * hd) return;
   const int64_t row = row0 + i;
   const int pos = pm.pos0[p] + i;
   int ns = pos / split + 1;
   if (ns > nsplit) {  // a position beyond the call's max_ctx bound
-    if (threadIdx.x == 0) report(status, DEV_BAD_INDEX);
+    if (idx == 0) report(status, DEV_BAD_INDEX);
     ns = nsplit;
   }
-  for (int idx = threadIdx.x; idx < Hq * hd; idx += blockDim.x) {
-    const int h = idx / hd, d = idx % hd;
-    const int64_t base = (row * Hq + h) * nsplit;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, part_ml[(base + s) * 2]);
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = exp2f(__fsub_rn(part_ml[(base + s) * 2], M));
-      L = __fadd_rn(L, __fmul_rn(part_ml[(base + s) * 2 + 1], w));
-      O = __fadd_rn(O, __fmul_rn(part_o[(base + s) * hd + d], w));
+  const int h = idx / hd, d = idx % hd;
+  const int64_t base = (row * Hq + h) * nsplit;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + base;
+  const float* po = part_o + base * hd + d;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
+  float L = 0.f, O = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
+    float2 r[kMergeBatch];
+    float o[kMergeBatch];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const bool in = s0 + k < ns;
+      r[k] = in ? ml[s0 + k] : make_float2(-INFINITY, 0.f);
+      o[k] = in ? po[(int64_t)(s0 + k) * hd] : 0.f;
     }
-    out[row * (int64_t)Hq * hd + idx] = f2bf(__fdiv_rn(O, L));
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      if (s0 + k >= ns) break;
+      const float w = exp2f(__fsub_rn(r[k].x, M));
+      L = __fadd_rn(L, __fmul_rn(r[k].y, w));
+      O = __fadd_rn(O, __fmul_rn(o[k], w));
+    }
   }
+  out[row * (int64_t)Hq * hd + idx] = f2bf(__fdiv_rn(O, L));
 }
 
 template <int HD, bool DECODE>
@@ -490,6 +855,34 @@ static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t 
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
   return launched(launch_pdl(attention_kernel<HD, DECODE>, grid, dim3(128), smem, st, args), "attention_kernel");
+}
+
+// Persistent decode launch: as many CTAs as fit on the GPU at once (at most
+// one per work item).  K and V are viewed as 2-D bf16 tensors [n_blocks * Hkv
+// * 64 rows, hd] read in 64 x 64 boxes with 128-byte swizzle.
+template <int HD>
+static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaStream_t st) {
+  constexpr int smem = DecLayout<HD>::kBytes;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int per_sm = 1;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attention_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD>, 160, smem);
+    if (per_sm < 1) per_sm = 1;
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("attention decode attributes: ") + cudaGetErrorString(attr_err));
+  const uint64_t rows = (uint64_t)args.n_blocks * args.Hkv * kKeys;
+  CUtensorMap tmk, tmv;
+  if (!encode_tmap_2d_bf16(&tmk, args.k_cache, HD, rows, HD * 2, 64, kKeys, true) ||
+      !encode_tmap_2d_bf16(&tmv, args.v_cache, HD, rows, HD * 2, 64, kKeys, true))
+    return fail(BI_ERR_CUDA, "attention decode: cuTensorMapEncodeTiled failed for the K/V cache");
+  const int64_t grid = std::min<int64_t>(P * args.Hkv * args.nsplit, (int64_t)num_sms() * per_sm);
+  return launched(launch_pdl(attention_decode_kernel<HD>, dim3((unsigned)grid), dim3(160), smem, st, args, tmk, tmv,
+                             (int)P),
+                  "attention_decode_kernel");
 }
 
 // Positions per split: the fixed kv_split, or (BI_FAST) a size chosen from the
@@ -557,8 +950,8 @@ size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ct
 bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
                        const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
                        const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split, float scale, void* workspace,
-                       size_t ws_bytes, void* out, int mode, void* stream) {
+                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split, float scale,
+                       void* workspace, size_t ws_bytes, void* out, int mode, void* stream) {
   using namespace bi;
   BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
   if (T == 0 || P == 0) return BI_OK;
@@ -571,6 +964,8 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   BI_REQUIRE_SHAPE(kRows % group == 0, "64 must be a multiple of Hq/Hkv");
   BI_REQUIRE(kv_split >= 64 && kv_split % 64 == 0, "kv_split must be a positive multiple of 64");
   BI_REQUIRE(max_ctx > 0 && max_q_len > 0, "bad max_ctx / max_q_len");
+  BI_REQUIRE(max_blocks_per_seq > 0 && n_blocks > 0 && n_blocks * Hkv * 64 < (int64_t(1) << 32),
+             "bad cache shape (max_blocks_per_seq, n_blocks)");
   BI_REQUIRE(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(workspace) && aligned16(out),
              "pointers must be 16-byte aligned");
   const int split = choose_split(mode, kv_split, P, max_q_len, Hkv, group, max_ctx);
@@ -592,7 +987,7 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   args.status = device_status_ptr();
   args.pm = PieceMeta{piece_seq, piece_row0, piece_pos0};
   args.max_blk = max_blocks_per_seq;
-  args.n_blocks = 1ll << 40;  // the caller's cache size is checked by the writer
+  args.n_blocks = n_blocks;
   args.Hq = Hq;
   args.Hkv = Hkv;
   args.group = group;
@@ -600,18 +995,25 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   args.split = split;
   args.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = as_stream(stream);
-  // a query tile of at most 16 rows (decode steps) uses the lane-parallel
-  // schedule; bigger tiles the row-parallel one.  Same bits either way.
+  // Three schedules with the same per-row arithmetic (so the same bits):
+  // query tiles of at most 16 rows (decode steps) take the lane-parallel
+  // schedule, persistent with TMA page streaming once contexts span more than
+  // kDecPersistentSplits splits (and the call has at most kDecMaxPieces
+  // sequences), one CTA per (sequence, kv head, split) otherwise; bigger query
+  // tiles take the row-parallel schedule.
   const bool decode = max_q_len * group <= 16;
-  if (decode) {
+  if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
+    BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
+    BI_TRY(hd == 64 ? launch_attention_decode<64>(args, P, st) : launch_attention_decode<128>(args, P, st));
+  } else if (decode) {
     dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)(Hkv * ns));
     BI_TRY(hd == 64 ? launch_attention<64, true>(args, grid, st) : launch_attention<128, true>(args, grid, st));
   } else {
     dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
     BI_TRY(hd == 64 ? launch_attention<64, false>(args, grid, st) : launch_attention<128, false>(args, grid, st));
   }
-  dim3 mgrid((unsigned)max_q_len, (unsigned)P);
-  return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(256), 0, st, (const float*)part_o,
+  dim3 mgrid((unsigned)max_q_len, (unsigned)P, (unsigned)cdiv(Hq * hd, 128));
+  return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(128), 0, st, (const float*)part_o,
                              (const float*)part_ml, args.pm, Hq, hd, (int)ns, split, static_cast<__nv_bfloat16*>(out),
                              args.status),
                   "attention_merge_kernel");
@@ -654,8 +1056,8 @@ extern "C" bi_status bi_attention_static_scratch(const void* q, int64_t T, const
                                                  const int32_t* piece_row0, const int32_t* piece_pos0, int64_t P,
                                                  int64_t max_q_len, int Hq, int Hkv, int hd, const void* k_cache,
                                                  const void* v_cache, const int32_t* block_table,
-                                                 int64_t max_blocks_per_seq, int64_t max_ctx, int kv_split,
-                                                 float scale, void* out, int mode, void* stream) {
+                                                 int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx,
+                                                 int kv_split, float scale, void* out, int mode, void* stream) {
   using namespace bi;
   BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
   if (T == 0 || P == 0) return BI_OK;
@@ -674,6 +1076,6 @@ extern "C" bi_status bi_attention_static_scratch(const void* q, int64_t T, const
   void* scratch = nullptr;
   BI_TRY(attn_static_scratch_addr(&scratch));
   return bi_attention(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,
-                      block_table, max_blocks_per_seq, max_ctx, kv_split, scale, scratch, kAttnStaticScratchBytes, out,
-                      mode, stream);
+                      block_table, max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, scratch,
+                      kAttnStaticScratchBytes, out, mode, stream);
 }

@@ -222,7 +222,7 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
                          m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd, mode,
                          stream));
     BI_TRY(bi_attention(q, T, piece_seq, piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq, Hkv, hd, kc, vc,
-                        block_table, max_blk, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
+                        block_table, max_blk, n_blocks, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
                         L.attn_ws_bytes, ao, mode, stream));
     BI_TRY(bi_gemm(ao, T, hq, lw.wo, c.d, tmp, BI_DTYPE_BF16, BI_EPI_NONE, mode, gws, L.gemm_ws_bytes, stream));
     BI_TRY(bi_rmsnorm(tmp, h, lw.ffn_norm, x, T, c.d, c.eps, mode, stream));

@@ -48,9 +48,9 @@ def test_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.bi_logprob_gather(16, None, 4, 6, 16, None, 0, None, 0, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_moe_route_topk(16, 4, 65, 8, 16, 16, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_moe_route_topk(16, 4, 64, 65, 16, 16, None) == bi.BI_ERR_INVALID_ARG
-    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 96, 16, 16, 16, 1, 64, 512, 0.1, 16, 1 << 20, 16, 0,
+    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 96, 16, 16, 16, 1, 1, 64, 512, 0.1, 16, 1 << 20, 16, 0,
                             None) == bi.BI_ERR_UNSUPPORTED_SHAPE
-    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 1, 64, 500, 0.1, 16, 1 << 20, 16, 0,
+    assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 1, 1, 64, 500, 0.1, 16, 1 << 20, 16, 0,
                             None) == bi.BI_ERR_INVALID_ARG
     # empty inputs are no-ops
     assert lib.bi_rmsnorm(None, None, None, None, 0, 64, 1e-6, 0, None) == bi.BI_OK

@@ -229,7 +229,7 @@ def test_rope_kv_write_and_attention_prefill_parity(Hq, Hkv, hd):
     out = torch.empty((T, Hq * hd), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(bi.bi_attention_workspace_size(T, Hq, hd, max(seq_lens), 512), dtype=torch.uint8, device="cuda")
     bi.bi_attention(q, T, seq, row0, pos0, len(seq_lens), max(seq_lens), Hq, Hkv, hd, kc, vc, bt, max_blk,
-                    max(seq_lens), 512, 1.0 / math.sqrt(hd), ws, out)
+                    kc.shape[0], max(seq_lens), 512, 1.0 / math.sqrt(hd), ws, out)
     got_q, got_o = host_f32(q), host_f32(out)
     r0 = 0
     for b, n in enumerate(seq_lens):
@@ -275,8 +275,8 @@ def test_attention_decode_rows_equal_prefill_rows_bitwise(Hq, Hkv, hd):
                             n_blocks, q, kc, vc)
         out = torch.empty((Tn, Hq * hd), dtype=torch.bfloat16, device="cuda")
         ws = torch.empty(bi.bi_attention_workspace_size(Tn, Hq, hd, max_ctx, 512), dtype=torch.uint8, device="cuda")
-        bi.bi_attention(q, Tn, seq, row0, pos0, len(pieces), mq, Hq, Hkv, hd, kc, vc, bt, max_blk, max_ctx, 512,
-                        scale, ws, out, mode)
+        bi.bi_attention(q, Tn, seq, row0, pos0, len(pieces), mq, Hq, Hkv, hd, kc, vc, bt, max_blk, kc.shape[0], max_ctx,
+                        512, scale, ws, out, mode)
         return out
 
     offs = np.concatenate([[0], np.cumsum(seq_lens)])
@@ -300,8 +300,48 @@ def test_attention_decode_rows_equal_prefill_rows_bitwise(Hq, Hkv, hd):
                 rows.append(offs[b] + pos)
         if not pcs:
             continue
-        o = run(pcs, qkv[torch.tensor(rows, device="cuda")].contiguous(), 2048)
-        assert same_bits(o, full[torch.tensor(rows, device="cuda")]), pos
+        # max_ctx 2048: one CTA per (sequence, kv head, split); 8192: the persistent schedule
+        for max_ctx in (2048, 8192):
+            o = run(pcs, qkv[torch.tensor(rows, device="cuda")].contiguous(), max_ctx)
+            assert same_bits(o, full[torch.tensor(rows, device="cuda")]), (pos, max_ctx)
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd,B", [(8, 8, 64, 300), (16, 4, 128, 200), (8, 1, 64, 1100)])
+def test_attention_decode_schedules_agree(Hq, Hkv, hd, B):
+    """Decode rows are bitwise the same whichever decode schedule runs: per-CTA
+    (max_ctx 2048 = 4 splits) or persistent with TMA page streaming (max_ctx
+    16384; more than 1024 sequences fall back to per-CTA).  Cache slots after
+    each sequence's last position hold NaN, which must never reach the output."""
+    rng = np.random.default_rng(B * 3 + hd)
+    ctx = rng.integers(1, 2049, B)
+    max_blk = 32
+    n_blocks = B * max_blk
+    bt = torch.from_numpy(rng.permutation(n_blocks).astype(np.int32).reshape(B, max_blk)).cuda()
+    kc = (0.5 * torch.randn((n_blocks, Hkv, 64, hd), device="cuda")).to(torch.bfloat16)
+    vc = (0.5 * torch.randn((n_blocks, Hkv, 64, hd), device="cuda")).to(torch.bfloat16)
+    stale = np.zeros((n_blocks, 64), dtype=bool)
+    tab = bt.cpu().numpy()
+    for b in range(B):
+        last = (ctx[b] - 1) // 64
+        stale[tab[b, last], ctx[b] - last * 64:] = True
+        stale[tab[b, last + 1:]] = True
+    m = torch.from_numpy(stale).cuda()
+    kc.permute(0, 2, 1, 3)[m] = float("nan")
+    vc.permute(0, 2, 1, 3)[m] = float("nan")
+    q = (0.5 * torch.randn((B, Hq, hd), device="cuda")).to(torch.bfloat16)
+    seq = torch.arange(B, dtype=torch.int32, device="cuda")
+    row0 = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    pos0 = torch.from_numpy((ctx - 1).astype(np.int32)).cuda()
+    outs = []
+    for max_ctx in (2048, 16384):
+        out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, max_ctx, 512), dtype=torch.uint8, device="cuda")
+        bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, n_blocks, max_ctx, 512,
+                        hd ** -0.5, ws, out)
+        outs.append(out)
+    assert bi.bi_device_status() == 0
+    assert not torch.isnan(outs[0].float()).any()
+    assert same_bits(outs[1], outs[0])
 
 
 # ---------------------------------------------------------------------------- MoE

@@ -53,8 +53,8 @@ def _with_workspace(pb):
     ws = torch.empty(bi.bi_attention_workspace_size(pb["T"], pb["Hq"], pb["hd"], pb["max_ctx"], 512),
                      dtype=torch.uint8, device="cuda")
     bi.bi_attention(pb["q"], pb["T"], pb["seq"], pb["row0"], pb["pos0"], pb["P"], pb["max_q_len"], pb["Hq"],
-                    pb["Hkv"], pb["hd"], pb["kc"], pb["vc"], pb["bt"], pb["max_blk"], pb["max_ctx"], 512,
-                    1.0 / math.sqrt(pb["hd"]), ws, out)
+                    pb["Hkv"], pb["hd"], pb["kc"], pb["vc"], pb["bt"], pb["max_blk"], pb["kc"].shape[0],
+                    pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), ws, out)
     return out
 
 
@@ -62,7 +62,7 @@ def _static(pb):
     out = torch.full((pb["T"], pb["Hq"] * pb["hd"]), float("nan"), dtype=torch.bfloat16, device="cuda")
     bi.bi_attention_static_scratch(pb["q"], pb["T"], pb["seq"], pb["row0"], pb["pos0"], pb["P"], pb["max_q_len"],
                                    pb["Hq"], pb["Hkv"], pb["hd"], pb["kc"], pb["vc"], pb["bt"], pb["max_blk"],
-                                   pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), out)
+                                   pb["kc"].shape[0], pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), out)
     return out
 
 
@@ -84,6 +84,7 @@ def test_static_scratch_refuses_calls_larger_than_the_array():
     with pytest.raises(bi.BiError) as e:
         # T rows whose partials would exceed 32 MiB: 20000 * 16 * 8 splits * 130 * 4 bytes
         bi.bi_attention_static_scratch(pb["q"], 20000, pb["seq"], pb["row0"], pb["pos0"], 1, 64, 16, 4, 128,
-                                       pb["kc"], pb["vc"], pb["bt"], pb["max_blk"], 4096, 512, 0.088, pb["q"])
+                                       pb["kc"], pb["vc"], pb["bt"], pb["max_blk"],
+                                       pb["kc"].shape[0], 4096, 512, 0.088, pb["q"])
     assert e.value.status == bi.BI_ERR_INVALID_ARG
     assert "static scratch array holds" in str(e.value)
