@@ -274,6 +274,7 @@ def run_ours(args):
     # roofline of the dominant kernel (timed live, same shapes as in the step)
     roof = roofline_probe(dec, ep, args)
     kernels = kernel_table(args) if not args.no_kernels else None
+    configs = config_table(args) if not args.no_configs else None
 
     # CPU oracle baseline on a bounded sample (rank 0, N = 1 only), also a parity spot check
     cpu = None
@@ -282,8 +283,8 @@ def run_ours(args):
         gens = results[0][0].cpu().numpy()
         v, n, dt, outs = oracle_sample(budget_s=args.cpu_budget, gens=gens)
         cpu = {"value": v, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
-               "sample": f"teacher-forced oracle scoring of {len(outs)} of {B} sequences ({n} sampled-token logprobs) "
-                         f"in {dt:.1f} s"}
+               "sample": f"teacher-forced oracle scoring of {len(outs)} sequences, cycling over the {B} of the "
+                         f"workload with the GPU's sampled ids ({n} sampled-token logprobs) in {dt:.1f} s"}
         lr0 = results[0][1].cpu().numpy()
         parity = max(float(np.max(np.abs(lr0[b] - lp))) for b, lp in outs)
 
@@ -298,6 +299,7 @@ def run_ours(args):
                                   "invariant_fraction": value / fast_value},
                 "roofline": roof,
                 "kernels": kernels,
+                "configs": configs,
                 "cpu_baseline": cpu,
                 "oracle_max_abs_err": parity,
                 "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": int(prompt_host.numel() * 4),
@@ -464,6 +466,134 @@ def kernel_table(args):
     return out
 
 
+def config_table(args):
+    """Timed unit of each other configuration of the scope table, invariant and
+    non-invariant (BI_FAST, the same kernels with batch-dependent choices), with
+    the roofline of its dominant work.  CUDA events around CUDA-graph replays.
+      logprob head: 512 rows x 256 -> RMSNorm -> lm_head 4096 -> log-softmax + gather
+        (latency-bound; inputs fit L2);
+      MoE layer: 4096 tokens x 2048, 64 experts top-8, F 1024: route, permute,
+        grouped gate/up + SwiGLU and down GEMMs, slot-order combine (805 MB of
+        expert weights > L2);
+      large-vocab logprob: 16384 x 4096 -> lm_head 129280 -> log-softmax + gather,
+        fused (1.06 GB of weights > L2);
+      long-context GQA decode: one decode step of the 8-layer d 2048 model over 64
+        sequences with contexts 1K-32K (KV 8.6 GB > L2), replayed at fixed positions.
+    Inputs of the MoE and large-vocab cases are drawn on the device with torch's
+    seeded normal generator (the recipe's distributions); the others come from
+    the seeded numpy generators."""
+    import torch
+    import invariant_forward_policy_gb300 as bi
+    from invariant_forward_policy_gb300.decoder import Decoder
+    from synthetic import C1, C3, C4, C5, make_c5_prompt_lengths, make_decoder_weights, make_logprob_head
+    hbm, tf, tf_s, src = _peaks()
+    dev = torch.device("cuda")
+    out = {"peak_source": src}
+
+    def both(build, n, reps):
+        r = {}
+        for mode, tag in ((bi.BI_INVARIANT, "invariant"), (bi.BI_FAST, "non_invariant")):
+            r[tag] = _graph_us(build(mode), n=n, reps=reps)
+        return r
+
+    def row(name, units, unit, t, extra):
+        v_inv, v_fast = units / (t["invariant"] * 1e-6), units / (t["non_invariant"] * 1e-6)
+        out[name] = {"value": round(v_inv, 1), "unit": unit, "us": round(t["invariant"], 1),
+                     "non_invariant": round(v_fast, 1), "invariant_fraction": round(v_inv / v_fast, 3), **extra}
+
+    # logprob head
+    h = make_logprob_head(C1["n_seq"] * C1["seq_len"], C1["d"], C1["vocab"], C1["w_std"], C1["seed"])
+    R, d, V = h["h"].shape[0], C1["d"], C1["vocab"]
+    X = torch.from_numpy(h["h"].view(np.int16)).to(dev).view(torch.bfloat16)
+    W = torch.from_numpy(h["w"].view(np.int16)).to(dev).view(torch.bfloat16)
+    g = torch.from_numpy(h["gain"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(h["ids"]).to(dev)
+    Y = torch.empty_like(X)
+    lp = torch.empty(R, device=dev)
+
+    def head(mode):
+        ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(R, V, d, mode), dtype=torch.uint8, device=dev)
+        return lambda: (bi.bi_rmsnorm(X, None, g, Y, R, d, 1e-6, mode),
+                        bi.bi_lm_head_logprob(Y, R, d, W, V, ids, lp, None, mode, ws))
+    t = both(head, 20, 10)
+    row("logprob_head_512x256x4096", R, "logprobs/s", t, {"bound": "latency", "note": "2 launches, inputs in L2"})
+    del X, W, Y
+
+    # MoE layer
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(C3["seed"])
+    T, dm, E, k, F = C3["n_tokens"], C3["d"], C3["n_experts"], C3["top_k"], C3["ffn"]
+    x = torch.randn((T, dm), device=dev, generator=gen).to(torch.bfloat16)
+    lg = torch.randn((T, E), device=dev, generator=gen)
+    w13 = (C3["w_std"] * torch.randn((E, 2 * F, dm), device=dev, generator=gen)).to(torch.bfloat16)
+    w2 = (C3["w_std"] * torch.randn((E, dm, F), device=dev, generator=gen)).to(torch.bfloat16)
+    y = torch.empty((T, dm), dtype=torch.bfloat16, device=dev)
+
+    def moe(mode):
+        ws = torch.empty(bi.bi_moe_layer_workspace_size(T, dm, E, k, F, mode), dtype=torch.uint8, device=dev)
+        return lambda: bi.bi_moe_layer(x, lg, T, dm, E, k, F, w13, w2, y, mode, ws)
+    t = both(moe, 3, 5)
+    fl = 2.0 * T * k * (2 * F * dm + dm * F)
+    row("moe_layer_4096x2048_e64_top8", T, "tokens/s", t,
+        {"bound": "tensor", "TFLOP/s": round(fl / t["invariant"] / 1e6, 1),
+         "frac": round(fl / t["invariant"] / 1e6 / tf, 3)})
+    del x, lg, w13, w2, y
+
+    # large-vocab logprob
+    gen.manual_seed(C4["seed"])
+    T4, d4, V4 = C4["n_tokens"], C4["d"], C4["vocab"]
+    H4 = torch.randn((T4, d4), device=dev, generator=gen).to(torch.bfloat16)
+    W4 = (C4["w_std"] * torch.randn((V4, d4), device=dev, generator=gen)).to(torch.bfloat16)
+    I4 = torch.randint(0, V4, (T4,), dtype=torch.int32, device=dev, generator=gen)
+    L4 = torch.empty(T4, device=dev)
+
+    def big(mode):
+        ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(T4, V4, d4, mode), dtype=torch.uint8, device=dev)
+        return lambda: bi.bi_lm_head_logprob(H4, T4, d4, W4, V4, I4, L4, None, mode, ws)
+    t = both(big, 2, 3)
+    fl = 2.0 * T4 * V4 * d4
+    row("large_vocab_logprob_16384x4096x129280", T4, "logprobs/s", t,
+        {"bound": "tensor", "TFLOP/s": round(fl / t["invariant"] / 1e6, 1),
+         "frac": round(fl / t["invariant"] / 1e6 / tf, 3)})
+    del H4, W4, I4, L4
+    torch.cuda.empty_cache()
+
+    # long-context GQA decode step
+    shape = C5["shape"]
+    lens = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"])
+    B = len(lens)
+    wb = make_decoder_weights(shape, seed=C5["seed"], w_std=C5["w_std"])
+    max_ctx = int(lens.max()) + 1
+    dec = Decoder(shape, wb, max_pos=max_ctx + 64)
+    mb = -(-max_ctx // 64)
+    bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
+    cache = dec.alloc_cache(nb)
+    rng = np.random.default_rng(C5["seed"] + 3)
+    prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
+    _, sm, cu = dec.prefill(prompts, cache, bt, logit_from=[int(n) - 1 for n in lens], chunk=C5["chunk"],
+                            max_tokens=16384, max_ctx=max_ctx, max_logit_rows=B)
+    tok = sm[torch.from_numpy(cu[1:] - 1).to(dev)].contiguous()
+    pos = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    smp = torch.empty(B, dtype=torch.int32, device=dev)
+    lpd = torch.empty(B, device=dev)
+
+    def step(mode):
+        ws = dec.workspace(B, B, max_ctx, B, mode)
+        return lambda: dec.decode(tok, pos, cache, bt, max_ctx, smp, lpd, ws, mode)
+    t = both(step, 3, 5)
+    kv = float(sum(int(n) + 1 for n in lens)) * shape.n_layers * shape.n_heads_kv * shape.head_dim * 2 * 2
+    wbytes = sum(a.nbytes for lw in wb["layers"] for a in lw.values()) + wb["lm_head"].nbytes + wb["final_norm"].nbytes
+    row("long_context_gqa_decode_step_64seq", B, "logprobs/s", t,
+        {"bound": "hbm", "GB/s": round((kv + wbytes) / t["invariant"] / 1e3, 1),
+         "frac": round((kv + wbytes) / t["invariant"] / 1e3 / hbm, 3),
+         "bytes_per_step": int(kv + wbytes),
+         "note": "KV of every context + all layer and lm_head weights read once per step (embedding rows excluded)"})
+    dec.close()
+    del cache
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_kernel_case(name: str, reps: int):
     """Launch one kernel of the step at its step shape `reps` times (profiling aid)."""
     import torch
@@ -513,6 +643,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip the per-kernel rate table")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' timed units")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     args = ap.parse_args()
     if args.kernel_case:
