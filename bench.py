@@ -490,11 +490,15 @@ def config_table(args):
     dev = torch.device("cuda")
     out = {"peak_source": src}
 
-    def both(build, n, reps):
-        r = {}
-        for mode, tag in ((bi.BI_INVARIANT, "invariant"), (bi.BI_FAST, "non_invariant")):
-            r[tag] = _graph_us(build(mode), n=n, reps=reps)
-        return r
+    def both(build, n, reps, rounds=3):
+        # the two arms alternate and each reports its median, so clock and
+        # power drift over the measurement favour neither
+        fns = {tag: build(mode) for mode, tag in ((bi.BI_INVARIANT, "invariant"), (bi.BI_FAST, "non_invariant"))}
+        ts = {tag: [] for tag in fns}
+        for _ in range(rounds):
+            for tag, fn in fns.items():
+                ts[tag].append(_graph_us(fn, n=n, reps=reps))
+        return {tag: float(np.median(v)) for tag, v in ts.items()}
 
     def row(name, units, unit, t, extra):
         v_inv, v_fast = units / (t["invariant"] * 1e-6), units / (t["non_invariant"] * 1e-6)

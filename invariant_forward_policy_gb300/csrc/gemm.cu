@@ -74,6 +74,7 @@ struct GemmArgs {
   TileLse* lse;             // EPI_LSE: [M, n_tiles] tile partials
   int n_tiles;              // EPI_LSE: vocab tiles per row
   int m_tiles, n_tiles_grid, splits;  // tile space walked by the persistent CTAs
+  int a_box_rows;                     // rows of A one TMA copy brings in (128, or M rounded up to 8 when M < 128)
   RopeKvArgs rope;                    // EPI_ROPE only
 };
 
@@ -394,6 +395,10 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + n_tile * BN);
         }
       };
+      // bytes of one stage: the A rows the copy brings (a decode-size A leaves the
+      // tile's other rows as they are; MMA rows never mix and rows >= M are
+      // never stored) plus the W tile
+      const uint32_t stage_bytes = (uint32_t)args.a_box_rows * kBK * 2 + S::kBTileBytes;
       int kb_total = 0;  // ring position across tiles
       bool first = true;
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
@@ -405,7 +410,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           // while it finishes; A is read only after the dependency wait
           pre = nk < kStages ? nk : kStages;
           for (int kb = 0; kb < pre; ++kb) {
-            mbar_arrive_expect_tx(&full[kb], S::kStageBytes);
+            mbar_arrive_expect_tx(&full[kb], stage_bytes);
             load_w(0, tc.n_tile, (tc.split * nk + kb) * kBK, kb);
           }
         }
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             *abort_flag = 1;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], S::kStageBytes);
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
           const int kc = (tc.split * nk + kb) * kBK;
           tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], kc, tc.m_tile * kBM);
           load_w(expert, tc.n_tile, kc, s);
@@ -583,12 +588,16 @@ static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUten
   return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad epilogue");
 }
 
-// Accumulator tile width for a weight: a function of (N, K, epilogue) only.
-static int tile_n_for(int64_t n_rows_w, int64_t /*K*/, bool swiglu) {
-  if (swiglu) return n_rows_w >= 4096 ? 128 : 64;
-  if (n_rows_w >= 32768) return 256;
-  if (n_rows_w >= 4096) return 128;
-  return 64;
+// Accumulator tile width for a weight: a function of its shape (N, K) only,
+// never of M.  Small weights (under 2M elements) take 64-wide tiles, so that a
+// decode-size call spreads over many CTAs; larger ones 128, and weights of
+// 16M+ elements or 32K+ rows 256, where the tensor pipe rather than shared
+// memory bandwidth bounds a prefill-size call.
+static int tile_n_for(int64_t n_rows_w, int64_t K, bool /*swiglu*/) {
+  const int64_t elems = n_rows_w * K;
+  if (elems < (int64_t(1) << 21)) return 64;
+  if (elems < (int64_t(1) << 24) && n_rows_w < 32768) return 128;
+  return 256;
 }
 
 // Non-invariant choices (BI_FAST): tile width and split count chosen from M.
@@ -642,7 +651,10 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   const int64_t kblocks = g.K / kBK;
 
   CUtensorMap ta, tb, tb2;
-  if (!encode_tmap_2d_bf16(&ta, g.A, g.K, g.M, g.K * 2, kBK, kBM, true))
+  // a dense call with M < 128 copies only its M rows (rounded up to 8) of A per stage
+  const int a_box_rows = (g.M < kBM && g.E == 1 && !g.tile_expert) ? (int)std::max<int64_t>(8, cdiv(g.M, 8) * 8)
+                                                                    : kBM;
+  if (!encode_tmap_2d_bf16(&ta, g.A, g.K, g.M, g.K * 2, kBK, (uint32_t)a_box_rows, true))
     return fail(BI_ERR_CUDA, "gemm: TMA descriptor for A failed");
   const uint32_t box_b = swiglu ? bn / 2 : bn;
   if (g.E == 1 && swiglu) {
@@ -678,6 +690,7 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   args.m_tiles = (int)cdiv(g.M, kBM);
   args.n_tiles_grid = (int)n_tiles;
   args.splits = splits;
+  args.a_box_rows = a_box_rows;
   const int64_t tiles = (int64_t)args.m_tiles * n_tiles * splits;
   BI_REQUIRE_SHAPE(tiles < (1ll << 31), "too many tiles");
   dim3 grid((unsigned)std::min<int64_t>(tiles, num_sms()));

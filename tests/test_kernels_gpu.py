@@ -60,8 +60,9 @@ def test_rmsnorm_rows_do_not_depend_on_batch():
 
 
 # ---------------------------------------------------------------------------- GEMM
+# tile widths: 64 below 2M weight elements, 128 below 16M (and N < 32768), else 256
 GEMM_SHAPES = [(1, 64, 64), (5, 1536, 512), (128, 512, 512), (129, 4096, 256), (300, 200, 576), (17, 32000, 512),
-               (260, 2816, 512)]
+               (260, 2816, 512), (131, 3072, 1024), (200, 8192, 2048), (3, 40000, 128)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -83,7 +84,7 @@ def test_gemm_bf16_and_fp32_parity(M, N, K):
     assert np.max(np.abs(host_f32(C32) - want) / (absdot + 1e-30)) < 1e-5
 
 
-@pytest.mark.parametrize("M,F,K", [(3, 1408, 512), (200, 64, 128), (129, 5632, 256)])
+@pytest.mark.parametrize("M,F,K", [(3, 1408, 512), (200, 64, 128), (129, 5632, 256), (70, 4096, 2048)])
 def test_gemm_swiglu_epilogue(M, F, K):
     rng = np.random.default_rng(M * F)
     ab, af = rng_bf16(rng, (M, K))
@@ -95,7 +96,7 @@ def test_gemm_swiglu_epilogue(M, F, K):
     bf16_close(host_f32(C), want, ulps=2, frac_exact=0.9, atol=2e-2 * absdot * 2.0 ** -7)
 
 
-@pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408)])
+@pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408), (3072, 2048), (8192, 2048)])
 def test_gemm_rows_invariant_to_M_and_order(N, K):
     rng = np.random.default_rng(N)
     ab, _ = rng_bf16(rng, (300, K))
