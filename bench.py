@@ -628,6 +628,34 @@ def run_kernel_case(name: str, reps: int):
         for _ in range(reps):
             bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, B * max_blk, ctx, 512, 0.125,
                             ws, out)
+    elif name == "step":
+        # the timed unit of the default run: rollout + recompute of the dense-decoder workload
+        from invariant_forward_policy_gb300.decoder import Decoder, Episode
+        from synthetic import C2, make_decoder_weights, make_prompts
+        shape = C2["shape"]
+        wb = make_decoder_weights(shape, seed=C2["seed"], w_std=C2["w_std"])
+        prompts = make_prompts(C2["batch"], C2["prompt_min"], C2["prompt_max"], shape.vocab, C2["seed"])
+        dec = Decoder(shape, wb, max_pos=1024, device=dev)
+        ep = Episode(dec, [len(p) for p in prompts], C2["gen"], mode=bi.BI_INVARIANT)
+        pd = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
+        for _ in range(reps):
+            ep.run(pd)
+    elif name == "attention_decode_long":
+        # persistent decode schedule: 32 sequences x 4096 context, 16/4 heads x 128 (268 MB of KV > L2)
+        B, Hq, Hkv, hd, ctx = 32, 16, 4, 128, 4096
+        max_blk = ctx // 64
+        kc = (0.5 * torch.randn((B * max_blk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+        vc = (0.5 * torch.randn((B * max_blk, Hkv, 64, hd), device=dev)).to(torch.bfloat16)
+        bt = torch.arange(B * max_blk, dtype=torch.int32, device=dev).view(B, max_blk)
+        q = (0.5 * torch.randn((B, Hq, hd), device=dev)).to(torch.bfloat16)
+        seq = torch.arange(B, dtype=torch.int32, device=dev)
+        row0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        pos0 = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
+        out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, ctx, 512), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, B * max_blk, ctx, 512,
+                            hd ** -0.5, ws, out)
     else:
         raise SystemExit(f"unknown kernel case {name}")
     torch.cuda.synchronize()
@@ -639,7 +667,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
-                         "attention_decode) and exit; for profiling")
+                         "attention_decode, attention_decode_long) or the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
