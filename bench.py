@@ -98,6 +98,22 @@ def _dist():
     return ws, rank
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest replica sets the job's time).
+    `dist` is torch.distributed (or None for a single process)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(n_replicas, units_per_replica, ms):
+    """Units every replica processed in one step, divided by the step time (ms)."""
+    return n_replicas * units_per_replica / (ms / 1000.0)
+
+
 def _cpu_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -237,13 +253,10 @@ def run_ours(args):
     clocks = ck.summary()
     ms_inv = sum(t_inv) / len(t_inv)
     ms_fast = sum(t_fast) / len(t_fast)
-    if dist is not None:
-        t = torch.tensor([ms_inv, ms_fast], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_inv, ms_fast = float(t[0]), float(t[1])
+    ms_inv, ms_fast = max_over_ranks([ms_inv, ms_fast], dist, device=dev)
     tokens = B * G
-    value = ws_n * tokens / (ms_inv / 1000.0)
-    fast_value = ws_n * tokens / (ms_fast / 1000.0)
+    value = whole_job_rate(ws_n, tokens, ms_inv)
+    fast_value = whole_job_rate(ws_n, tokens, ms_fast)
 
     # diff = 0 in every timed step (rollout vs recompute) and identical across steps
     from oracle.ops import diff_stats  # host-side acceptance statistics
