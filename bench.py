@@ -452,6 +452,22 @@ def kernel_table(args):
     out["rmsnorm_residual_65536x2048"] = {"us": round(us, 1), "GB/s": round(4 * Rr * dd * 2 / us / 1e3, 1),
                                           "frac": round(4 * Rr * dd * 2 / us / 1e3 / hbm, 3), "bound": "hbm"}
     del xx, rr, yy
+    # deterministic Top-K (sparse-attention indexer budget K = 2048): one decode step of the
+    # long-context batch (64 rows, contexts 1K-32K) and one 2048-row prefill chunk at 30K-32K
+    for tag, nv in (("topk_decode_64rows_ctx1k-32k_k2048", lens.astype(np.int32)),
+                    ("topk_prefill_2048rows_ctx30k-32k_k2048", np.arange(30721, 32769, dtype=np.int32))):
+        T, ld = len(nv), int(nv.max())
+        S = torch.randn((T, ld), device=dev)
+        nvd = torch.from_numpy(nv).to(dev)
+        idx = torch.empty((T, 2048), dtype=torch.int32, device=dev)
+        us_i = _graph_us(lambda: bi.bi_topk(S, T, ld, nvd, 2048, idx, bi.BI_INVARIANT), n=5, reps=5)
+        us_f = _graph_us(lambda: bi.bi_topk(S, T, ld, nvd, 2048, idx, bi.BI_FAST), n=5, reps=5)
+        nbytes = float(nv.astype(np.int64).sum()) * 4
+        out[tag] = {"us": round(us_i, 1), "GB/s": round(nbytes / us_i / 1e3, 1),
+                    "frac": round(nbytes / us_i / 1e3 / hbm, 3), "bound": "hbm",
+                    "non_invariant_us": round(us_f, 1), "invariant_fraction": round(us_f / us_i, 3),
+                    "note": "algorithmic bytes = the scores read once; 4 radix passes + 1 ordered pass re-read them"}
+        del S
     # tensor-bound GEMMs: fused large-vocab lm_head + log-softmax, prefill FFN
     def gemm_rate(M, N, K, fn_builder, tag):
         fn, flops = fn_builder(M, N, K)

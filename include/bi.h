@@ -206,6 +206,23 @@ bi_status bi_attention_static_scratch(const void* q, int64_t T, const int32_t* p
                                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split,
                                       float scale, void* out, int mode, void* stream);
 
+/* ------------------------------------------------------- deterministic Top-K
+ * [Article] §4.3 ("Top-K in sparse attention: fix ties and order").
+ * Row t of `scores` (device fp32, row stride ld elements) scores the candidate
+ * positions 0 .. n_valid[t] - 1 (in-request positions; device int32 [T]).  The
+ * K candidates that come first in the order (score descending, then position
+ * descending) -- the unique key "score bits, then position bits" -- are
+ * selected and written to idx_out[t, 0 .. K) (device int32 [T, K]) in
+ * descending position order, followed by -1 when n_valid[t] < K.  Scores
+ * compare as numbers (-0 ties +0; -inf is a score); NaN is outside the
+ * contract.  K in [1, 4096].  A row with n_valid outside [0, ld] is clamped and
+ * sets the device status.
+ * BI_FAST: ties at the threshold score go to whichever candidates claim a slot
+ * first and the selection is left unsorted (the non-deterministic default the
+ * pages replace; same set of scores, not the same positions). */
+bi_status bi_topk(const float* scores, int64_t T, int64_t ld, const int32_t* n_valid, int K, int32_t* idx_out,
+                  int mode, void* stream);
+
 /* ---------------------------------------------------------- embed / logprob
  * Row gather: out[t] = table[ids[t]] (bf16 [V, d] -> bf16 [T, d]).  Ids outside
  * [0, V) write zeros and record BI_ERR_DEVICE_CHECK. */

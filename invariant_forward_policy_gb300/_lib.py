@@ -76,6 +76,7 @@ _SIGS = {
     "bi_attention_workspace_size": (_sz, [_i64, _int, _int, _i64, _int]),
     "bi_attention_static_scratch": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp,
                                            _i64, _i64, _i64, _int, _f32, _vp, _int, _vp]),
+    "bi_topk": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _int, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
     "bi_logprob_workspace_size": (_sz, [_i64, _i64, _int]),
@@ -232,6 +233,10 @@ def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_
 
 def bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split) -> int:
     return load().bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split)
+
+
+def bi_topk(scores, T, ld, n_valid, K, idx_out, mode=BI_INVARIANT, stream=None):
+    _check(load().bi_topk(_p(scores), T, ld, _p(n_valid), K, _p(idx_out), mode, _s(stream)))
 
 
 def bi_embed(ids, T, table, V, d, out, stream=None):

@@ -52,8 +52,13 @@ def test_validation_rejects_bad_arguments_without_launching(lib):
                             None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 1, 1, 64, 500, 0.1, 16, 1 << 20, 16, 0,
                             None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_topk(16, 4, 64, 16, 0, 16, 0, None) == bi.BI_ERR_INVALID_ARG       # K < 1
+    assert lib.bi_topk(16, 4, 64, 16, 4097, 16, 0, None) == bi.BI_ERR_INVALID_ARG    # K > 4096
+    assert lib.bi_topk(None, 4, 64, 16, 8, 16, 0, None) == bi.BI_ERR_INVALID_ARG     # null scores
+    assert lib.bi_topk(16, 4, 64, 16, 8, 16, 3, None) == bi.BI_ERR_INVALID_ARG       # bad mode
     # empty inputs are no-ops
     assert lib.bi_rmsnorm(None, None, None, None, 0, 64, 1e-6, 0, None) == bi.BI_OK
+    assert lib.bi_topk(None, 0, 64, None, 8, None, 0, None) == bi.BI_OK
     assert lib.bi_gemm(None, 0, 64, None, 64, None, 0, 0, 0, None, 0, None) == bi.BI_OK
 
 
