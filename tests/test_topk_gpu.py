@@ -86,3 +86,19 @@ def test_topk_fast_selects_the_same_scores():
         # the same multiset of scores (compared as numbers: -0 == +0), possibly other tie positions
         assert np.array_equal(np.sort(S[t][inv[t]]), np.sort(S[t][fast[t]]))
         assert len(set(fast[t].tolist())) == K and fast[t].min() >= 0 and fast[t].max() < n[t]
+
+
+def test_topk_row_and_cluster_schedules_agree():
+    """400 rows take one CTA per row, 64 or fewer a cluster per row: every row is
+    bitwise the same either way, and both equal the oracle."""
+    rng = np.random.default_rng(23)
+    T, ld, K = 400, 3000, 256
+    S = _scores(rng, T, ld, "bf16_ties")
+    n = rng.integers(0, ld + 1, T)
+    full = _run(S, n, K)
+    assert np.array_equal(full, otk.topk(S, n, K))
+    for a in (0, 150, 336):
+        assert np.array_equal(_run(S[a:a + 64], n[a:a + 64], K), full[a:a + 64])
+    fast = _run(S, n, K, bi.BI_FAST)
+    for t in range(0, T, 37):
+        assert np.array_equal(np.sort(S[t][full[t][full[t] >= 0]]), np.sort(S[t][fast[t][fast[t] >= 0]]))
