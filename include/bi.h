@@ -206,6 +206,31 @@ bi_status bi_attention_static_scratch(const void* q, int64_t T, const int32_t* p
                                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split,
                                       float scale, void* out, int mode, void* stream);
 
+/* ------------------------------------------------------------- block FP8
+ * [Article] §4.1 ("Dense GEMM: keep FP8, one accumulation order for every M"):
+ * block-FP8 W8A8, the training forward quantising its bf16 master weights by
+ * the deployment rule.  Readings (the pages give no block sizes or scale
+ * format): e4m3 "fn" codes, round to nearest even, saturating at 448, sign of
+ * zero kept; 128 x 128 weight blocks and 1 x 128 activation blocks; scale of a
+ * block = the smallest power of two s with 448 s >= amax (1 when amax = 0), so
+ * a code times its scale is exact.
+ *
+ * bi_quantize_fp8: x bf16 [R, C] (device, row-major, C % 128 == 0) ->
+ * q uint8 [R, C] (e4m3 codes of x / s) and scales fp32 [ceil(R / block_rows),
+ * C / 128]; block_rows = 1 (activations) or 128 (weights).  Deterministic:
+ * every block depends on its own elements only. */
+bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, void* q, float* scales,
+                          void* stream);
+/* bi_gemm_fp8: C = dequant(Aq) dequant(Wq)^T.  Aq uint8 [M, K] with sa fp32
+ * [M, K/128] (1 x 128 blocks); Wq uint8 [N, K] with sw fp32 [N/128, K/128]
+ * (128 x 128 blocks); C [M, N] bf16 or fp32 (c_dtype).  N and K multiples of
+ * 128; Aq, Wq, C 16-byte aligned.  Per 128-wide K block the e4m3 products are
+ * summed by tcgen05 MMAs in TMEM, then added in fp32, times the exact scale
+ * product, in ascending block order: one tile shape and K order for every M
+ * (BI_FAST runs the same kernel). */
+bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, const void* Wq, const float* sw,
+                      int64_t N, void* C, int c_dtype, int mode, void* stream);
+
 /* ------------------------------------------------------- deterministic Top-K
  * [Article] §4.3 ("Top-K in sparse attention: fix ties and order").
  * Row t of `scores` (device fp32, row stride ld elements) scores the candidate

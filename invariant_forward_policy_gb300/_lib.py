@@ -77,6 +77,8 @@ _SIGS = {
     "bi_attention_static_scratch": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp,
                                            _i64, _i64, _i64, _int, _f32, _vp, _int, _vp]),
     "bi_topk": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _int, _vp]),
+    "bi_quantize_fp8": (_int, [_vp, _i64, _i64, _int, _vp, _vp, _vp]),
+    "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
     "bi_logprob_workspace_size": (_sz, [_i64, _i64, _int]),
@@ -233,6 +235,14 @@ def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_
 
 def bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split) -> int:
     return load().bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split)
+
+
+def bi_quantize_fp8(x, R, C, block_rows, q, scales, stream=None):
+    _check(load().bi_quantize_fp8(_p(x), R, C, block_rows, _p(q), _p(scales), _s(stream)))
+
+
+def bi_gemm_fp8(Aq, sa, M, K, Wq, sw, N, C, c_dtype=BI_DTYPE_BF16, mode=BI_INVARIANT, stream=None):
+    _check(load().bi_gemm_fp8(_p(Aq), _p(sa), M, K, _p(Wq), _p(sw), N, _p(C), c_dtype, mode, _s(stream)))
 
 
 def bi_topk(scores, T, ld, n_valid, K, idx_out, mode=BI_INVARIANT, stream=None):

@@ -89,6 +89,9 @@ bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int6
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool swizzle128);
+// 8-bit elements (fp8 codes), 128-byte swizzle.
+bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_outer);
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // while its predecessor in the stream is still finishing; it must execute
@@ -216,6 +219,14 @@ BI_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, e4m3 inputs (K = 32 per instruction), fp32 accumulate.
+BI_DEV void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
 BI_DEV void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -246,6 +257,11 @@ BI_DEV uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   d |= (uint64_t)1 << 46;                           // version
   d |= (uint64_t)2 << 61;                           // SWIZZLE_128B
   return d;
+}
+
+// Instruction descriptor: kind::f8f6f4, A = B = e4m3 (format 0), D = fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.

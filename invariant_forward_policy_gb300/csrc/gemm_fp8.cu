@@ -1,0 +1,306 @@
+// Block-FP8 (e4m3) quantisation and the W8A8 tcgen05 GEMM.
+//
+// "vLLM Achieves Bitwise-Consistent RL Training ..." §4.1 ("Dense GEMM: keep
+// FP8, one accumulation order for every M"): the deployment GEMM is block-FP8
+// W8A8 and every training forward quantises the bf16 master weights to block
+// FP8 by the deployment rule, then calls the same GEMM.  The pages fix neither
+// the block sizes nor the scale format; this file takes 128 x 128 weight
+// blocks, 1 x 128 activation blocks and power-of-two scales
+// s = 2^ceil(log2(amax / 448)), which make dequantisation exact.
+//
+// GEMM: C[m, n] = sum over K blocks kb of sa[m, kb] sw[n/128, kb] P_kb[m, n],
+// P_kb the e4m3 product over the 128 K of block kb.  One persistent CTA per
+// SM walks 128 x 128 output tiles: warp 0 streams A and W tiles of 128 x 128
+// bytes with TMA, warp 1 issues four tcgen05 kind::f8f6f4 MMAs (K = 32 each)
+// per K block into one of two TMEM partial buffers, and warps 2..5 add each
+// finished partial, times the exact power-of-two scale product, to an fp32
+// accumulator held in registers, in ascending kb.  The tile shape and the K
+// order are the same for every M, so every row's result is batch invariant.
+#include <cuda_fp8.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace bi {
+
+constexpr int kF8Block = 128;  // K block = weight block rows = output tile width
+constexpr int kF8Stages = 6;
+constexpr int kF8TileBytes = 128 * kF8Block;  // 128 rows x 128 fp8
+constexpr int kF8SmemBytes = 1024 + kF8Stages * 2 * kF8TileBytes + 256;
+
+// Smallest power of two s with 448 s >= amax (1 for amax = 0), exactly.
+__device__ __forceinline__ int fp8_scale_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = ilogbf(amax);  // amax in [2^e, 2^(e+1))
+  return amax <= ldexpf(1.75f, e) ? e - 8 : e - 7;
+}
+
+// One CTA per block of block_rows x 128 (grid x: row blocks, y: column blocks):
+// amax, power-of-two scale, e4m3 codes.
+__global__ void __launch_bounds__(128) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t R, int64_t C,
+                                                           int block_rows, uint8_t* __restrict__ q,
+                                                           float* __restrict__ scales) {
+  __shared__ float wmax[4];
+  pdl_trigger();
+  pdl_wait();
+  const int64_t col = (int64_t)blockIdx.y * kF8Block + threadIdx.x;
+  const int64_t r0 = (int64_t)blockIdx.x * block_rows;
+  const int64_t r1 = R < r0 + block_rows ? R : r0 + block_rows;
+  float m = 0.f;
+  for (int64_t r = r0; r < r1; ++r) m = fmaxf(m, fabsf(bf2f(x[r * C + col])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  const int e = fp8_scale_exp(amax);
+  if (threadIdx.x == 0) scales[(int64_t)blockIdx.x * (C / kF8Block) + blockIdx.y] = ldexpf(1.f, e);
+  for (int64_t r = r0; r < r1; ++r) {
+    const float v = ldexpf(bf2f(x[r * C + col]), -e);  // exact: a power-of-two scaling
+    q[r * C + col] = (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
+struct F8Args {
+  const float* sa;  // [M, nkb]
+  const float* sw;  // [N / 128, nkb]
+  void* C;
+  int* status;
+  int M, N, nkb, m_tiles, n_tiles, a_box_rows, c_fp32;
+};
+
+__global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                          const __grid_constant__ CUtensorMap tmB, const F8Args args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kF8Stages * kF8TileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kF8Stages * kF8TileBytes);
+  uint64_t* empty = full + kF8Stages;
+  uint64_t* pfull = empty + kF8Stages;   // [2] MMA -> epilogue: a K block's partial is in TMEM
+  uint64_t* pempty = pfull + 2;          // [2] epilogue -> MMA (4 warp arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  constexpr uint32_t kTmemCols = 2 * kF8Block;
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = args.m_tiles * args.n_tiles;
+  const int nk = args.nkb;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kF8Stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // tiles walk M fastest, so consecutive CTAs share a weight tile in L2
+  auto tile_mn = [&](int t, int& mt, int& nt) {
+    mt = t % args.m_tiles;
+    nt = t / args.m_tiles;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      pdl_wait();
+      const uint32_t stage_bytes = (uint32_t)args.a_box_rows * kF8Block + kF8TileBytes;
+      int kb_total = 0;
+      for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+        int mt, nt;
+        tile_mn(t, mt, nt);
+        for (int kb = 0; kb < nk; ++kb, ++kb_total) {
+          const int s = kb_total % kF8Stages;
+          const uint32_t ph = (kb_total / kF8Stages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1) || *abort_flag) {
+            report(args.status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(sA + s * kF8TileBytes, &tmA, &full[s], kb * kF8Block, mt * 128);
+          tma_load_2d(sB + s * kF8TileBytes, &tmB, &full[s], kb * kF8Block, nt * kF8Block);
+        }
+      }
+      for (int i = 0; i < kF8Stages && i < kb_total; ++i) {  // let the last copies land
+        const int kb = kb_total - 1 - i;
+        mbar_wait(&full[kb % kF8Stages], (kb / kF8Stages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: one TMEM partial per K block, two buffers
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, kF8Block);
+      int kb_total = 0, pb = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok && !*abort_flag; t += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb, ++kb_total, ++pb) {
+          const int j = pb & 1;
+          const int s = kb_total % kF8Stages;
+          if (!mbar_wait(&pempty[j], ((pb >> 1) & 1) ^ 1) ||
+              !mbar_wait(&full[s], (kb_total / kF8Stages) & 1) || *abort_flag) {
+            report(args.status, DEV_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + s * kF8TileBytes);
+          const uint32_t b_addr = smem_u32(sB + s * kF8TileBytes);
+          const uint32_t d = tmem_base + j * kF8Block;
+#pragma unroll
+          for (int k = 0; k < kF8Block / 32; ++k)
+            tc_mma_f8(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
+                      k != 0 ? 1u : 0u);
+          tc_commit(&empty[s]);
+          tc_commit(&pfull[j]);
+        }
+      }
+    }
+  } else {
+    // ---------------- promotion and store: warps 2..5, TMEM lane quarter q = warp % 4
+    const int q = warp & 3;
+    pdl_wait();
+    int pb = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      int mt, nt;
+      tile_mn(t, mt, nt);
+      const int row = mt * 128 + q * 32 + lane;
+      const bool valid = row < args.M;
+      float acc[kF8Block];
+#pragma unroll
+      for (int c = 0; c < kF8Block; ++c) acc[c] = 0.f;
+      for (int kb = 0; kb < nk; ++kb, ++pb) {
+        const int j = pb & 1;
+        const float sc = (valid ? args.sa[(int64_t)row * nk + kb] : 0.f) * args.sw[(int64_t)nt * nk + kb];
+        if (!mbar_wait(&pfull[j], (pb >> 1) & 1)) {
+          report(args.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + j * kF8Block + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+        for (int c = 0; c < kF8Block / 32; ++c) {
+          uint32_t p[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, p);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            acc[c * 32 + i] = __fadd_rn(acc[c * 32 + i], __fmul_rn(__uint_as_float(p[i]), sc));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty[j]);
+      }
+      if (!ok || !valid || *abort_flag) continue;
+      const int64_t base = (int64_t)row * args.N + (int64_t)nt * kF8Block;
+      if (args.c_fp32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.C) + base);
+#pragma unroll
+        for (int v = 0; v < kF8Block / 4; ++v)
+          dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.C) + base);
+#pragma unroll
+        for (int v = 0; v < kF8Block / 8; ++v)
+          dst[v] = make_uint4(pack_bf16x2(acc[8 * v], acc[8 * v + 1]), pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
+                              pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
+                              pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, void* q, float* scales,
+                          void* stream) {
+  using namespace bi;
+  BI_REQUIRE(R >= 0 && C >= 0, "bad shape");
+  BI_REQUIRE(block_rows == 1 || block_rows == 128, "block_rows must be 1 (activations) or 128 (weights)");
+  BI_REQUIRE_SHAPE(C % kF8Block == 0, "columns must be a multiple of 128");
+  if (R == 0 || C == 0) return BI_OK;
+  BI_REQUIRE(x && q && scales, "null pointer");
+  const int64_t rb = cdiv(R, block_rows);
+  BI_REQUIRE(rb <= 0x7fffffff && C / kF8Block <= 65535, "too many blocks");
+  return launched(launch_pdl(quantize_fp8_kernel, dim3((unsigned)rb, (unsigned)(C / kF8Block)), dim3(128), 0,
+                             as_stream(stream), static_cast<const __nv_bfloat16*>(x), R, C, block_rows,
+                             static_cast<uint8_t*>(q), scales),
+                  "bi_quantize_fp8");
+}
+
+bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, const void* Wq, const float* sw,
+                      int64_t N, void* C, int c_dtype, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(M >= 0 && N >= 0 && K >= 0, "bad shape");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  BI_REQUIRE(c_dtype == BI_DTYPE_BF16 || c_dtype == BI_DTYPE_FP32, "bad output dtype");
+  BI_REQUIRE_SHAPE(K % kF8Block == 0 && N % kF8Block == 0, "N and K must be multiples of 128");
+  if (M == 0 || N == 0) return BI_OK;
+  BI_REQUIRE(K > 0 && Aq && sa && Wq && sw && C, "null pointer");
+  BI_REQUIRE(aligned16(Aq) && aligned16(Wq) && aligned16(C), "pointers must be 16-byte aligned");
+  BI_REQUIRE(M <= 0x7fffffff && N <= 0x7fffffff, "shape too large");
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8SmemBytes);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("bi_gemm_fp8 smem attribute: ") + cudaGetErrorString(attr_err));
+  // a call with M < 128 copies only its rows of A (rounded up to 8); rows >= M are never stored
+  const int a_rows = M < 128 ? (int)std::max<int64_t>(8, cdiv(M, 8) * 8) : 128;
+  CUtensorMap ta, tb;
+  if (!encode_tmap_2d_u8(&ta, Aq, K, M, K, kF8Block, a_rows) ||
+      !encode_tmap_2d_u8(&tb, Wq, K, N, K, kF8Block, kF8Block))
+    return fail(BI_ERR_CUDA, "bi_gemm_fp8: TMA descriptor failed");
+  F8Args a;
+  a.sa = sa;
+  a.sw = sw;
+  a.C = C;
+  a.status = device_status_ptr();
+  a.M = (int)M;
+  a.N = (int)N;
+  a.nkb = (int)(K / kF8Block);
+  a.m_tiles = (int)cdiv(M, 128);
+  a.n_tiles = (int)(N / kF8Block);
+  a.a_box_rows = a_rows;
+  a.c_fp32 = c_dtype == BI_DTYPE_FP32;
+  const int64_t tiles = (int64_t)a.m_tiles * a.n_tiles;
+  BI_REQUIRE_SHAPE(tiles < (1ll << 31), "too many tiles");
+  return launched(launch_pdl(gemm_fp8_kernel, dim3((unsigned)std::min<int64_t>(tiles, num_sms())), dim3(192),
+                             kF8SmemBytes, as_stream(stream), ta, tb, a),
+                  "bi_gemm_fp8");
+}
+
+}  // extern "C"

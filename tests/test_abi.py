@@ -52,6 +52,10 @@ def test_validation_rejects_bad_arguments_without_launching(lib):
                             None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_attention(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 1, 1, 64, 500, 0.1, 16, 1 << 20, 16, 0,
                             None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_quantize_fp8(16, 4, 100, 1, 16, 16, None) == bi.BI_ERR_UNSUPPORTED_SHAPE   # C % 128
+    assert lib.bi_quantize_fp8(16, 4, 128, 64, 16, 16, None) == bi.BI_ERR_INVALID_ARG        # block rows
+    assert lib.bi_gemm_fp8(16, 16, 4, 100, 16, 16, 128, 16, 0, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_gemm_fp8(16, 16, 4, 128, 16, 16, 128, 16, 7, 0, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_topk(16, 4, 64, 16, 0, 16, 0, None) == bi.BI_ERR_INVALID_ARG       # K < 1
     assert lib.bi_topk(16, 4, 64, 16, 4097, 16, 0, None) == bi.BI_ERR_INVALID_ARG    # K > 4096
     assert lib.bi_topk(None, 4, 64, 16, 8, 16, 0, None) == bi.BI_ERR_INVALID_ARG     # null scores

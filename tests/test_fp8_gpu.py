@@ -1,0 +1,89 @@
+"""Block-FP8 quantisation and the W8A8 tcgen05 GEMM ([Article] §4.1) through the C ABI:
+codes and scales bit-exact against the oracle, the GEMM within fp32 accumulation of
+the oracle's exact product, and every row's result independent of the batch."""
+import numpy as np
+import pytest
+import torch
+
+import invariant_forward_policy_gb300 as bi
+from oracle import fp8 as ofp8
+from synthetic import bits_to_f32, normal_bf16
+from tests.gpu_util import dev_bf16, same_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant(xb, block_rows):
+    R, C = xb.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    s = torch.empty((-(-R // block_rows), C // 128), dtype=torch.float32, device="cuda")
+    bi.bi_quantize_fp8(dev_bf16(xb), R, C, block_rows, q, s)
+    return q, s
+
+
+@pytest.mark.parametrize("R,C,br", [(1, 128, 1), (37, 384, 1), (256, 512, 128), (300, 256, 128), (5, 1024, 128)])
+def test_quantize_matches_oracle_bitwise(R, C, br):
+    rng = np.random.default_rng(R * C + br)
+    xb = normal_bf16(rng, (R, C), 3.0)
+    xf = bits_to_f32(xb).copy()
+    xf[0, :7] = [0.0, -0.0, 1e-38, -3e-39, 6e4, -6e4, 2.0 ** -133]    # zeros, subnormals, large values
+    xf[min(R - 1, 2), 128:256 if C >= 256 else 128] = 0.0              # an all-zero block where there is one
+    from synthetic import to_bf16_bits
+    xb = to_bf16_bits(xf)
+    q, s = _quant(xb, br)
+    want_q, want_s = ofp8.quantize_blocks(bits_to_f32(xb), br)
+    assert np.array_equal(s.cpu().numpy(), want_s)
+    assert np.array_equal(q.cpu().numpy(), want_q)
+
+
+def _fp8_operands(rng, M, N, K, a_std=1.0, w_std=0.05):
+    ab, wb = normal_bf16(rng, (M, K), a_std), normal_bf16(rng, (N, K), w_std)
+    qa, sa = _quant(ab, 1)
+    qw, sw = _quant(wb, 128)
+    return qa, sa, qw, sw
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (5, 256, 512), (130, 384, 256), (300, 1024, 1024), (64, 3072, 2048)])
+def test_gemm_fp8_parity(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    qa, sa, qw, sw = _fp8_operands(rng, M, N, K)
+    C32 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    bi.bi_gemm_fp8(qa, sa, M, K, qw, sw, N, C32, bi.BI_DTYPE_FP32)
+    want = ofp8.gemm_fp8(qa.cpu().numpy(), sa.cpu().numpy(), qw.cpu().numpy(), sw.cpu().numpy())
+    a = ofp8.dequantize_blocks(qa.cpu().numpy(), sa.cpu().numpy(), 1).astype(np.float64)
+    w = ofp8.dequantize_blocks(qw.cpu().numpy(), sw.cpu().numpy(), 128).astype(np.float64)
+    absdot = np.abs(a) @ np.abs(w).T
+    # fp32 accumulation in another order: within a small multiple of 2^-24 sum|a||w|
+    assert np.max(np.abs(C32.cpu().numpy() - want) / (absdot + 1e-30)) < 1e-5
+    Cb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm_fp8(qa, sa, M, K, qw, sw, N, Cb, bi.BI_DTYPE_BF16)
+    # the bf16 output is the fp32 result rounded once
+    assert same_bits(Cb, C32.to(torch.bfloat16))
+    assert bi.bi_device_status() == 0
+
+
+@pytest.mark.parametrize("N,K", [(256, 512), (3072, 2048)])
+def test_gemm_fp8_rows_invariant_to_M_and_order(N, K):
+    rng = np.random.default_rng(N)
+    qa, sa, qw, sw = _fp8_operands(rng, 300, N, K)
+    full = torch.empty((300, N), dtype=torch.float32, device="cuda")
+    bi.bi_gemm_fp8(qa, sa, 300, K, qw, sw, N, full, bi.BI_DTYPE_FP32)
+    for M in (1, 7, 16, 127, 128, 129, 255):
+        off = 300 - M
+        part = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        bi.bi_gemm_fp8(qa[off:].contiguous(), sa[off:].contiguous(), M, K, qw, sw, N, part, bi.BI_DTYPE_FP32)
+        assert same_bits(part, full[off:]), M
+    perm = torch.from_numpy(rng.permutation(300)).cuda()
+    outp = torch.empty_like(full)
+    bi.bi_gemm_fp8(qa[perm].contiguous(), sa[perm].contiguous(), 300, K, qw, sw, N, outp, bi.BI_DTYPE_FP32)
+    assert same_bits(outp, full[perm])
+
+
+def test_training_side_requantisation_is_deterministic():
+    """The training forward requantises the bf16 master weights every call: the
+    codes and scales are bitwise the same each time and match the oracle."""
+    rng = np.random.default_rng(7)
+    wb = normal_bf16(rng, (384, 640), 0.02)
+    q1, s1 = _quant(wb, 128)
+    q2, s2 = _quant(wb, 128)
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
