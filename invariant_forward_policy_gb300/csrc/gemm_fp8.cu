@@ -38,29 +38,68 @@ __device__ __forceinline__ int fp8_scale_exp(float amax) {
   return amax <= ldexpf(1.75f, e) ? e - 8 : e - 7;
 }
 
-// One CTA per block of block_rows x 128 (grid x: row blocks, y: column blocks):
-// amax, power-of-two scale, e4m3 codes.
-__global__ void __launch_bounds__(128) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t R, int64_t C,
-                                                           int block_rows, uint8_t* __restrict__ q,
-                                                           float* __restrict__ scales) {
-  __shared__ float wmax[4];
+// Activations (1 x 128 blocks): one warp per block, 4 consecutive elements per
+// lane, amax by warp shuffles; 8 blocks per CTA.
+__global__ void __launch_bounds__(256) quantize_fp8_rows_kernel(const __nv_bfloat16* __restrict__ x, int64_t R,
+                                                                int64_t C, uint8_t* __restrict__ q,
+                                                                float* __restrict__ scales) {
   pdl_trigger();
   pdl_wait();
-  const int64_t col = (int64_t)blockIdx.y * kF8Block + threadIdx.x;
-  const int64_t r0 = (int64_t)blockIdx.x * block_rows;
-  const int64_t r1 = R < r0 + block_rows ? R : r0 + block_rows;
-  float m = 0.f;
-  for (int64_t r = r0; r < r1; ++r) m = fmaxf(m, fabsf(bf2f(x[r * C + col])));
+  const int64_t nb = C / kF8Block;
+  const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (blk >= R * nb) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = blk / nb, c0 = (blk % nb) * kF8Block + lane * 4;
+  const uint2 raw = *reinterpret_cast<const uint2*>(x + r * C + c0);
+  float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u), __uint_as_float(raw.y << 16),
+                __uint_as_float(raw.y & 0xffff0000u)};
+  float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  const int e = fp8_scale_exp(m);
+  if (lane == 0) scales[blk] = ldexpf(1.f, e);
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    packed |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[i], -e), __NV_SATFINITE, __NV_E4M3) << (8 * i);
+  *reinterpret_cast<uint32_t*>(q + r * C + c0) = packed;
+}
+
+// Weights (128 x 128 blocks): one CTA of 256 threads per block; thread t takes
+// 4 consecutive columns (t % 32) of rows t / 32, t / 32 + 8, ...
+__global__ void __launch_bounds__(256) quantize_fp8_blocks_kernel(const __nv_bfloat16* __restrict__ x, int64_t R,
+                                                                  int64_t C, uint8_t* __restrict__ q,
+                                                                  float* __restrict__ scales) {
+  __shared__ float wmax[8];
+  pdl_trigger();
+  pdl_wait();
+  const int64_t r0 = (int64_t)blockIdx.x * kF8Block;
+  const int64_t c0 = (int64_t)blockIdx.y * kF8Block + (threadIdx.x & 31) * 4;
+  const int rsub = threadIdx.x >> 5;
+  float m = 0.f;
+  for (int i = rsub; i < kF8Block && r0 + i < R; i += 8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + (r0 + i) * C + c0);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(raw.x << 16)), fabsf(__uint_as_float(raw.x & 0xffff0000u))),
+                       fmaxf(fabsf(__uint_as_float(raw.y << 16)), fabsf(__uint_as_float(raw.y & 0xffff0000u)))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[rsub] = m;
   __syncthreads();
-  const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+  float amax = wmax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
   const int e = fp8_scale_exp(amax);
   if (threadIdx.x == 0) scales[(int64_t)blockIdx.x * (C / kF8Block) + blockIdx.y] = ldexpf(1.f, e);
-  for (int64_t r = r0; r < r1; ++r) {
-    const float v = ldexpf(bf2f(x[r * C + col]), -e);  // exact: a power-of-two scaling
-    q[r * C + col] = (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  for (int i = rsub; i < kF8Block && r0 + i < R; i += 8) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(x + (r0 + i) * C + c0);
+    const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
+    uint32_t packed = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      packed |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[k], -e), __NV_SATFINITE, __NV_E4M3) << (8 * k);
+    *reinterpret_cast<uint32_t*>(q + (r0 + i) * C + c0) = packed;
   }
 }
 
@@ -252,11 +291,19 @@ bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, v
   BI_REQUIRE_SHAPE(C % kF8Block == 0, "columns must be a multiple of 128");
   if (R == 0 || C == 0) return BI_OK;
   BI_REQUIRE(x && q && scales, "null pointer");
+  BI_REQUIRE(aligned16(x) && ((uintptr_t)q & 3) == 0, "x must be 16-byte and q 4-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  if (block_rows == 1) {
+    const int64_t blocks = R * (C / kF8Block);
+    BI_REQUIRE(cdiv(blocks, 8) <= 0x7fffffff, "too many blocks");
+    return launched(launch_pdl(quantize_fp8_rows_kernel, dim3((unsigned)cdiv(blocks, 8)), dim3(256), 0, st,
+                               static_cast<const __nv_bfloat16*>(x), R, C, static_cast<uint8_t*>(q), scales),
+                    "bi_quantize_fp8");
+  }
   const int64_t rb = cdiv(R, block_rows);
   BI_REQUIRE(rb <= 0x7fffffff && C / kF8Block <= 65535, "too many blocks");
-  return launched(launch_pdl(quantize_fp8_kernel, dim3((unsigned)rb, (unsigned)(C / kF8Block)), dim3(128), 0,
-                             as_stream(stream), static_cast<const __nv_bfloat16*>(x), R, C, block_rows,
-                             static_cast<uint8_t*>(q), scales),
+  return launched(launch_pdl(quantize_fp8_blocks_kernel, dim3((unsigned)rb, (unsigned)(C / kF8Block)), dim3(256), 0,
+                             st, static_cast<const __nv_bfloat16*>(x), R, C, static_cast<uint8_t*>(q), scales),
                   "bi_quantize_fp8");
 }
 
