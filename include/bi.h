@@ -231,6 +231,29 @@ bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, v
 bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, const void* Wq, const float* sw,
                       int64_t N, void* C, int c_dtype, int mode, void* stream);
 
+/* --------------------------------------------------- Mamba-2 chunked scan
+ * [Article] §6 ("Transfer: Nemotron, a Mamba hybrid architecture + NVFP4"):
+ * decode replays prefill's chunked arithmetic instead of its own single-step
+ * recurrence.  Per head h (group g = h / (H/G) shares B and C):
+ *   state_t = exp(loga_t) state_{t-1} + B_t x_t^T,  y_t = C_t^T state_t,
+ * computed in chunk form over absolute chunks [cQ, cQ + Q): a row uses the
+ * state entering its chunk plus the chunk's earlier rows, and the state is
+ * advanced only when a chunk completes, each sum in ascending index order.  So
+ * a decode step, a prefill over the whole sequence and any chunking of it give
+ * the same bits for every row.
+ * Inputs (device): x bf16 [T, H, P], B and C bf16 [T, G, N], loga fp32 [T, H]
+ * (<= 0); pieces as in bi_attention (piece_seq [pieces], piece_row0
+ * [pieces + 1], piece_pos0 [pieces]): at most one piece per sequence per call,
+ * each sequence's pieces passed in position order over successive calls.
+ * state: fp32, bi_ssd_state_bytes(H, G, P, N, Q) bytes per sequence
+ * (n_seq of them), zeroed by the caller for a new sequence; it holds the state
+ * entering the current chunk and that chunk's earlier inputs.  y: fp32
+ * [T, H, P].  Q <= 64, N <= 128, P <= 128.  BI_FAST runs the same kernel. */
+size_t bi_ssd_state_bytes(int H, int G, int P, int N, int Q);
+bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* loga, const int32_t* piece_seq,
+                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int H, int G,
+                            int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode, void* stream);
+
 /* ------------------------------------------------------- deterministic Top-K
  * [Article] §4.3 ("Top-K in sparse attention: fix ties and order").
  * Row t of `scores` (device fp32, row stride ld elements) scores the candidate

@@ -78,6 +78,9 @@ _SIGS = {
                                            _i64, _i64, _i64, _int, _f32, _vp, _int, _vp]),
     "bi_topk": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _int, _vp]),
     "bi_quantize_fp8": (_int, [_vp, _i64, _i64, _int, _vp, _vp, _vp]),
+    "bi_ssd_state_bytes": (_sz, [_int, _int, _int, _int, _int]),
+    "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _int, _int, _vp, _i64,
+                                 _vp, _int, _vp]),
     "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
@@ -235,6 +238,16 @@ def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_
 
 def bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split) -> int:
     return load().bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split)
+
+
+def bi_ssd_state_bytes(H, G, P, N, Q) -> int:
+    return load().bi_ssd_state_bytes(H, G, P, N, Q)
+
+
+def bi_ssd_chunk_scan(x, B, C, loga, piece_seq, piece_row0, piece_pos0, pieces, H, G, P, N, Q, state, n_seq, y,
+                      mode=BI_INVARIANT, stream=None):
+    _check(load().bi_ssd_chunk_scan(_p(x), _p(B), _p(C), _p(loga), _p(piece_seq), _p(piece_row0), _p(piece_pos0),
+                                    pieces, H, G, P, N, Q, _p(state), n_seq, _p(y), mode, _s(stream)))
 
 
 def bi_quantize_fp8(x, R, C, block_rows, q, scales, stream=None):

@@ -1,0 +1,217 @@
+// Mamba-2 scan in chunked (state-space duality) form, one arithmetic for
+// prefill, chunked prefill and decode.
+//
+// "vLLM Achieves Bitwise-Consistent RL Training ..." §6 ("Transfer: Nemotron,
+// a Mamba hybrid architecture + NVFP4"): Mamba-2 is a linear recurrence, and
+// decode replays prefill's chunked arithmetic instead of its own single-step
+// recurrence.
+//
+// Per head: state_t = a_t state_{t-1} + B_t x_t^T, y_t = C_t^T state_t, with
+// a_t = exp(loga_t).  Chunks are absolute positions [cQ, cQ + Q).  For the row
+// at offset i of chunk c, with H_c the state entering the chunk and
+// L_i = loga_0 + ... + loga_i (offsets of the chunk, summed in order):
+//     y_i = exp(L_i) (C_i^T H_c) + sum_{j = 0..i} (exp(L_i - L_j) (C_i . B_j)) x_j
+// and, once the chunk is complete,
+//     H_{c+1} = exp(L_{Q-1}) H_c + sum_{j = 0..Q-1} (exp(L_{Q-1} - L_j) B_j) x_j^T.
+// Every dot product and sum runs in ascending index order with one fused
+// multiply-add per term.  A call processes one piece (a run of consecutive
+// positions) per sequence; a per-sequence store keeps H_c and the inputs of
+// the chunk's earlier positions (B, x, loga, copied exactly, per head), so a decode step
+// or a prefill chunk that starts mid-chunk computes its rows exactly as a
+// prefill over the whole chunk does.
+#include <algorithm>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace bi {
+
+constexpr int kSsdThreads = 256;
+constexpr int kSsdMaxQ = 64, kSsdMaxN = 128, kSsdMaxP = 128;
+
+struct SsdArgs {
+  const __nv_bfloat16* x;  // [T, H, P]
+  const __nv_bfloat16* B;  // [T, G, N]
+  const __nv_bfloat16* C;  // [T, G, N]
+  const float* loga;       // [T, H]
+  const int32_t* seq;      // [pieces]
+  const int32_t* row0;     // [pieces + 1]
+  const int32_t* pos0;     // [pieces]
+  float* store;            // [n_seq, floats per sequence]
+  float* y;                // [T, H, P]
+  int* status;
+  int64_t n_seq, store_floats;
+  int H, G, P, N, Q;
+};
+
+// Per sequence: entering state [H][N][P], then the open chunk's earlier inputs
+// B [Q][H][N], x [Q][H][P], loga [Q][H].  B is kept per head (not per group) so
+// that each CTA reads and writes only its own slots.
+__host__ __device__ inline int64_t ssd_store_floats(int H, int /*G*/, int P, int N, int Q) {
+  return (int64_t)H * N * P + (int64_t)Q * H * N + (int64_t)Q * H * P + (int64_t)Q * H;
+}
+
+__global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
+  float* Hs = sm;                 // [N][P] state entering the chunk
+  float* Bs = Hs + N * P;         // [Q][N]
+  float* Cs = Bs + Q * N;         // [Q][N]
+  float* xs = Cs + Q * N;         // [Q][P]
+  float* Gm = xs + Q * P;         // [Q][Q] (C_i . B_j) scaled by the decay
+  float* ls = Gm + Q * Q;         // [Q] loga
+  float* Ls = ls + Q;             // [Q] cumulative
+  pdl_trigger();
+  pdl_wait();
+  const int piece = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int g = h / (H / G);
+  const int row0 = a.row0[piece];
+  const int n_tok = a.row0[piece + 1] - row0;
+  if (n_tok <= 0) return;
+  const int s = a.seq[piece];
+  const int64_t p0 = a.pos0[piece], p1 = p0 + n_tok;
+  if (s < 0 || s >= a.n_seq || p0 < 0) {
+    if (tid == 0) report(a.status, DEV_BAD_INDEX);
+    return;
+  }
+  float* st = a.store + (int64_t)s * a.store_floats;
+  float* st_H = st + (int64_t)h * N * P;                       // [H][N][P]
+  float* st_B = st + (int64_t)H * N * P;                       // [Q][H][N]
+  float* st_x = st_B + (int64_t)Q * H * N;                     // [Q][H][P]
+  float* st_l = st_x + (int64_t)Q * H * P;                     // [Q][H]
+
+  for (int i = tid; i < N * P; i += kSsdThreads) Hs[i] = st_H[i];
+  const int64_t c_first = p0 / Q, c_last = (p1 - 1) / Q;
+  for (int64_t c = c_first; c <= c_last; ++c) {
+    const int64_t cs = c * Q;
+    const int i0 = (int)((p0 > cs ? p0 : cs) - cs), i1 = (int)((p1 < cs + Q ? p1 : cs + Q) - cs);
+    // chunk inputs: earlier offsets from the store (first chunk of the call only), new ones from the call
+    for (int e = tid; e < i1 * N; e += kSsdThreads) {
+      const int i = e / N, n = e % N;
+      if (i < i0) {
+        Bs[e] = st_B[((int64_t)i * H + h) * N + n];
+      } else {
+        const int64_t r = row0 + (cs + i - p0);
+        Bs[e] = bf2f(a.B[(r * G + g) * N + n]);
+        Cs[e] = bf2f(a.C[(r * G + g) * N + n]);
+      }
+    }
+    for (int e = tid; e < i1 * P; e += kSsdThreads) {
+      const int i = e / P, p = e % P;
+      xs[e] = i < i0 ? st_x[((int64_t)i * H + h) * P + p]
+                     : bf2f(a.x[((row0 + (cs + i - p0)) * (int64_t)H + h) * P + p]);
+    }
+    for (int i = tid; i < i1; i += kSsdThreads)
+      ls[i] = i < i0 ? st_l[(int64_t)i * H + h] : a.loga[(row0 + (cs + i - p0)) * (int64_t)H + h];
+    __syncthreads();
+    if (tid == 0) {
+      float acc = 0.f;
+      for (int i = 0; i < i1; ++i) {
+        acc = __fadd_rn(acc, ls[i]);
+        Ls[i] = acc;
+      }
+    }
+    __syncthreads();
+    // decay-scaled (C_i . B_j) for the rows this call computes
+    for (int e = tid; e < (i1 - i0) * i1; e += kSsdThreads) {
+      const int i = i0 + e / i1, j = e % i1;
+      if (j > i) continue;
+      float d = 0.f;
+      for (int n = 0; n < N; ++n) d = __fmaf_rn(Cs[i * N + n], Bs[j * N + n], d);
+      Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), d);
+    }
+    __syncthreads();
+    for (int e = tid; e < (i1 - i0) * P; e += kSsdThreads) {
+      const int i = i0 + e / P, p = e % P;
+      float inter = 0.f;
+      for (int n = 0; n < N; ++n) inter = __fmaf_rn(Cs[i * N + n], Hs[n * P + p], inter);
+      float intra = 0.f;
+      for (int j = 0; j <= i; ++j) intra = __fmaf_rn(Gm[i * Q + j], xs[j * P + p], intra);
+      const int64_t r = row0 + (cs + i - p0);
+      a.y[(r * H + h) * P + p] = __fadd_rn(__fmul_rn(expf(Ls[i]), inter), intra);
+    }
+    if (i1 == Q) {
+      // the chunk is complete: its exit state enters the next chunk
+      __syncthreads();
+      const float eL = expf(Ls[Q - 1]);
+      for (int e = tid; e < N * P; e += kSsdThreads) {
+        const int n = e / P, p = e % P;
+        float acc = __fmul_rn(eL, Hs[e]);
+        for (int j = 0; j < Q; ++j)
+          acc = __fmaf_rn(__fmul_rn(expf(__fsub_rn(Ls[Q - 1], Ls[j])), Bs[j * N + n]), xs[j * P + p], acc);
+        Hs[e] = acc;
+      }
+    } else {
+      // the chunk stays open: keep the inputs of the new offsets for the calls that finish it
+      for (int e = tid; e < (i1 - i0) * P; e += kSsdThreads) {
+        const int i = i0 + e / P, p = e % P;
+        st_x[((int64_t)i * H + h) * P + p] = xs[i * P + p];
+      }
+      for (int e = tid; e < (i1 - i0) * N; e += kSsdThreads) {
+        const int i = i0 + e / N, n = e % N;
+        st_B[((int64_t)i * H + h) * N + n] = Bs[i * N + n];
+      }
+      for (int i = i0 + tid; i < i1; i += kSsdThreads) st_l[(int64_t)i * H + h] = ls[i];
+    }
+    __syncthreads();
+  }
+  // the state entering the sequence's next position
+  for (int i = tid; i < N * P; i += kSsdThreads) st_H[i] = Hs[i];
+}
+
+}  // namespace bi
+
+extern "C" {
+
+size_t bi_ssd_state_bytes(int H, int G, int P, int N, int Q) {
+  if (H <= 0 || G <= 0 || P <= 0 || N <= 0 || Q <= 0 || H % G) return 0;
+  return (size_t)bi::ssd_store_floats(H, G, P, N, Q) * sizeof(float);
+}
+
+bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* loga, const int32_t* piece_seq,
+                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int H, int G,
+                            int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(pieces >= 0, "bad shape");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
+  if (pieces == 0) return BI_OK;
+  BI_REQUIRE(x && B && C && loga && piece_seq && piece_row0 && piece_pos0 && state && y, "null pointer");
+  BI_REQUIRE(H > 0 && G > 0 && H % G == 0, "H must be a positive multiple of G");
+  BI_REQUIRE_SHAPE(Q >= 1 && Q <= kSsdMaxQ && N >= 1 && N <= kSsdMaxN && P >= 1 && P <= kSsdMaxP,
+                   "chunk <= 64, state size <= 128 and head size <= 128");
+  BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0, "bad pieces / heads / sequences");
+  const int smem = (int)((size_t)(N * P + 2 * Q * N + Q * P + Q * Q + 2 * Q) * sizeof(float));
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    const int mx = (kSsdMaxN * kSsdMaxP + 2 * kSsdMaxQ * kSsdMaxN + kSsdMaxQ * kSsdMaxP + kSsdMaxQ * kSsdMaxQ +
+                    2 * kSsdMaxQ) * (int)sizeof(float);
+    attr_err = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("bi_ssd_chunk_scan smem attribute: ") + cudaGetErrorString(attr_err));
+  SsdArgs a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.B = static_cast<const __nv_bfloat16*>(B);
+  a.C = static_cast<const __nv_bfloat16*>(C);
+  a.loga = loga;
+  a.seq = piece_seq;
+  a.row0 = piece_row0;
+  a.pos0 = piece_pos0;
+  a.store = static_cast<float*>(state);
+  a.y = y;
+  a.status = device_status_ptr();
+  a.n_seq = n_seq;
+  a.store_floats = ssd_store_floats(H, G, P, N, Q);
+  a.H = H;
+  a.G = G;
+  a.P = P;
+  a.N = N;
+  a.Q = Q;
+  return launched(launch_pdl(ssd_scan_kernel, dim3((unsigned)pieces, (unsigned)H), dim3(kSsdThreads), smem,
+                             as_stream(stream), a),
+                  "bi_ssd_chunk_scan");
+}
+
+}  // extern "C"
