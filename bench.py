@@ -468,6 +468,52 @@ def kernel_table(args):
                     "non_invariant_us": round(us_f, 1), "invariant_fraction": round(us_f / us_i, 3),
                     "note": "algorithmic bytes = the scores read once; 4 radix passes + 1 ordered pass re-read them"}
         del S
+    # Mamba-2 chunked scan (32 heads x 64, state 128, 8 B/C groups, chunk 64): a prefill
+    # of 16 sequences x 2048 and a decode step of 64 sequences at mid-chunk positions.
+    Hs, Gs, Ps, Ns, Qs = 32, 8, 64, 128, 64
+    alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12      # fp32 FMA lanes x 2 FLOP x max SM clock, TFLOP/s
+    for tag, n_seq, per in (("ssd_prefill_16x2048", 16, 2048), ("ssd_decode_64seq", 64, 1)):
+        T = n_seq * per
+        xs = torch.randn((T, Hs, Ps), device=dev).to(torch.bfloat16)
+        Bs = (torch.randn((T, Gs, Ns), device=dev) * Ns ** -0.5).to(torch.bfloat16)
+        Cs = (torch.randn((T, Gs, Ns), device=dev) * Ns ** -0.5).to(torch.bfloat16)
+        la = -torch.rand((T, Hs), device=dev) * 0.2
+        st = torch.zeros((n_seq, bi.bi_ssd_state_bytes(Hs, Gs, Ps, Ns, Qs) // 4), device=dev)
+        ys = torch.empty((T, Hs, Ps), device=dev)
+        sq = torch.arange(n_seq, dtype=torch.int32, device=dev)
+        r0 = torch.arange(0, T + 1, per, dtype=torch.int32, device=dev)
+        p0 = torch.full((n_seq,), 0 if per > 1 else 40, dtype=torch.int32, device=dev)
+        us = _graph_us(lambda: bi.bi_ssd_chunk_scan(xs, Bs, Cs, la, sq, r0, p0, n_seq, Hs, Gs, Ps, Ns, Qs, st, n_seq,
+                                                    ys), n=3, reps=3)
+        if per > 1:   # every chunk complete: rows + exit states
+            fma = n_seq * Hs * (per // Qs) * (Qs * (Qs + 1) / 2 * Ns + Qs * Ps * (Ns + (Qs + 1) / 2) + Ns * Ps * Qs)
+        else:         # one row at offset 40: its chunk row and no exit state
+            fma = n_seq * Hs * (41 * Ns + Ps * (Ns + 41))
+        out[tag] = {"us": round(us, 1), "TFLOP/s": round(2 * fma / us / 1e6, 2),
+                    "frac": round(2 * fma / us / 1e6 / alu_peak, 3), "bound": "alu",
+                    "peak": round(alu_peak, 1), "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 x 2.07 GHz"}
+        del xs, Bs, Cs, la, st, ys
+    # block-FP8 W8A8 GEMM (activation quantisation separate), prefill FFN shape
+    Mf, Nf, Kf = 8192, 11264, 2048
+    Af = torch.randn((Mf, Kf), device=dev).to(torch.bfloat16)
+    Wf = (0.02 * torch.randn((Nf, Kf), device=dev)).to(torch.bfloat16)
+    qa = torch.empty((Mf, Kf), dtype=torch.uint8, device=dev)
+    sa = torch.empty((Mf, Kf // 128), device=dev)
+    qw = torch.empty((Nf, Kf), dtype=torch.uint8, device=dev)
+    sw = torch.empty((Nf // 128, Kf // 128), device=dev)
+    bi.bi_quantize_fp8(Wf, Nf, Kf, 128, qw, sw)
+    bi.bi_quantize_fp8(Af, Mf, Kf, 1, qa, sa)
+    Cf = torch.empty((Mf, Nf), dtype=torch.bfloat16, device=dev)
+    us = _graph_us(lambda: bi.bi_gemm_fp8(qa, sa, Mf, Kf, qw, sw, Nf, Cf), n=3, reps=3)
+    fl = 2.0 * Mf * Nf * Kf
+    out["gemm_fp8_8192x11264x2048"] = {"us": round(us, 1), "TFLOP/s": round(fl / us / 1e6, 1),
+                                       "frac": round(fl / us / 1e6 / (2 * tf), 3), "bound": "tensor",
+                                       "peak_note": "fp8 peak = 2 x the bf16 peak (nominal ratio)"}
+    us_q = _graph_us(lambda: bi.bi_quantize_fp8(Af, Mf, Kf, 1, qa, sa), n=3, reps=3)
+    qbytes = Mf * Kf * 2 + Mf * Kf + Mf * (Kf // 128) * 4
+    out["quantize_fp8_act_8192x2048"] = {"us": round(us_q, 1), "GB/s": round(qbytes / us_q / 1e3, 1),
+                                         "frac": round(qbytes / us_q / 1e3 / hbm, 3), "bound": "hbm"}
+    del Af, Wf, qa, qw, Cf
     # tensor-bound GEMMs: fused large-vocab lm_head + log-softmax, prefill FFN
     def gemm_rate(M, N, K, fn_builder, tag):
         fn, flops = fn_builder(M, N, K)

@@ -248,7 +248,8 @@ bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, con
  * state: fp32, bi_ssd_state_bytes(H, G, P, N, Q) bytes per sequence
  * (n_seq of them), zeroed by the caller for a new sequence; it holds the state
  * entering the current chunk and that chunk's earlier inputs.  y: fp32
- * [T, H, P].  Q <= 64, N <= 128, P <= 128.  BI_FAST runs the same kernel. */
+ * [T, H, P].  Q <= 64, N <= 128, P <= 128, each a multiple of 4.  BI_FAST
+ * runs the same kernel. */
 size_t bi_ssd_state_bytes(int H, int G, int P, int N, int Q);
 bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* loga, const int32_t* piece_seq,
                             const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int H, int G,

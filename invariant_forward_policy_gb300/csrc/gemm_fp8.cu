@@ -10,12 +10,14 @@
 //
 // GEMM: C[m, n] = sum over K blocks kb of sa[m, kb] sw[n/128, kb] P_kb[m, n],
 // P_kb the e4m3 product over the 128 K of block kb.  One persistent CTA per
-// SM walks 128 x 128 output tiles: warp 0 streams A and W tiles of 128 x 128
-// bytes with TMA, warp 1 issues four tcgen05 kind::f8f6f4 MMAs (K = 32 each)
-// per K block into one of two TMEM partial buffers, and warps 2..5 add each
-// finished partial, times the exact power-of-two scale product, to an fp32
-// accumulator held in registers, in ascending kb.  The tile shape and the K
-// order are the same for every M, so every row's result is batch invariant.
+// SM walks 128 x 256 output tiles: warp 0 streams A (128 x 128 bytes) and W
+// (256 x 128 bytes) tiles with TMA, warp 1 issues four tcgen05 kind::f8f6f4
+// MMAs (N = 256, K = 32 each) per K block into one of two 256-column TMEM
+// partial buffers, and warps 2..9 (two per TMEM lane quarter, one per
+// 128-column half, i.e. per weight block) add each finished partial, times
+// the exact power-of-two scale product, to an fp32 accumulator held in
+// registers, in ascending kb.  The tile shape and the K order are the same for
+// every M, so every row's result is batch invariant.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -26,10 +28,13 @@
 
 namespace bi {
 
-constexpr int kF8Block = 128;  // K block = weight block rows = output tile width
-constexpr int kF8Stages = 6;
-constexpr int kF8TileBytes = 128 * kF8Block;  // 128 rows x 128 fp8
-constexpr int kF8SmemBytes = 1024 + kF8Stages * 2 * kF8TileBytes + 256;
+constexpr int kF8Block = 128;   // K block = weight block rows
+constexpr int kF8BN = 256;      // output tile width: two weight blocks
+constexpr int kF8Stages = 4;
+constexpr int kF8TileBytes = 128 * kF8Block;       // A: 128 rows x 128 fp8
+constexpr int kF8BTileBytes = kF8BN * kF8Block;    // W: 256 rows x 128 fp8
+constexpr int kF8Threads = 320;                    // TMA, MMA, 8 promotion warps
+constexpr int kF8SmemBytes = 1024 + kF8Stages * (kF8TileBytes + kF8BTileBytes) + 256;
 
 // Smallest power of two s with 448 s >= amax (1 for amax = 0), exactly.
 __device__ __forceinline__ int fp8_scale_exp(float amax) {
@@ -111,19 +116,19 @@ struct F8Args {
   int M, N, nkb, m_tiles, n_tiles, a_box_rows, c_fp32;
 };
 
-__global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA,
                                                           const __grid_constant__ CUtensorMap tmB, const F8Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kF8Stages * kF8TileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kF8Stages * kF8TileBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kF8Stages * kF8BTileBytes);
   uint64_t* empty = full + kF8Stages;
   uint64_t* pfull = empty + kF8Stages;   // [2] MMA -> epilogue: a K block's partial is in TMEM
-  uint64_t* pempty = pfull + 2;          // [2] epilogue -> MMA (4 warp arrivals)
+  uint64_t* pempty = pfull + 2;          // [2] epilogue -> MMA (8 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  constexpr uint32_t kTmemCols = 2 * kF8Block;
+  constexpr uint32_t kTmemCols = 2 * kF8BN;
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,7 +141,7 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], 4);
+      mbar_init(&pempty[b], 8);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
     if (lane == 0) {
       // ---------------- TMA producer
       pdl_wait();
-      const uint32_t stage_bytes = (uint32_t)args.a_box_rows * kF8Block + kF8TileBytes;
+      const uint32_t stage_bytes = (uint32_t)args.a_box_rows * kF8Block + kF8BTileBytes;
       int kb_total = 0;
       for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
         int mt, nt;
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
           }
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           tma_load_2d(sA + s * kF8TileBytes, &tmA, &full[s], kb * kF8Block, mt * 128);
-          tma_load_2d(sB + s * kF8TileBytes, &tmB, &full[s], kb * kF8Block, nt * kF8Block);
+          tma_load_2d(sB + s * kF8BTileBytes, &tmB, &full[s], kb * kF8Block, nt * kF8BN);
         }
       }
       for (int i = 0; i < kF8Stages && i < kb_total; ++i) {  // let the last copies land
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer: one TMEM partial per K block, two buffers
-      constexpr uint32_t idesc = idesc_e4m3_f32(128, kF8Block);
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, kF8BN);
       int kb_total = 0, pb = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok && !*abort_flag; t += gridDim.x) {
@@ -205,8 +210,8 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + s * kF8TileBytes);
-          const uint32_t b_addr = smem_u32(sB + s * kF8TileBytes);
-          const uint32_t d = tmem_base + j * kF8Block;
+          const uint32_t b_addr = smem_u32(sB + s * kF8BTileBytes);
+          const uint32_t d = tmem_base + j * kF8BN;
 #pragma unroll
           for (int k = 0; k < kF8Block / 32; ++k)
             tc_mma_f8(d, sw128_kmajor_desc(a_addr + k * 32), sw128_kmajor_desc(b_addr + k * 32), idesc,
@@ -217,8 +222,9 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
       }
     }
   } else {
-    // ---------------- promotion and store: warps 2..5, TMEM lane quarter q = warp % 4
-    const int q = warp & 3;
+    // ---------------- promotion and store: warps 2..9; lane quarter q = warp % 4,
+    // column half (= weight block within the tile) hf = (warp - 2) / 4
+    const int q = warp & 3, hf = (warp - 2) >> 2;
     pdl_wait();
     int pb = 0;
     bool ok = true;
@@ -226,13 +232,14 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
       int mt, nt;
       tile_mn(t, mt, nt);
       const int row = mt * 128 + q * 32 + lane;
-      const bool valid = row < args.M;
+      const int wblk = nt * 2 + hf;                       // weight block row of this half
+      const bool valid = row < args.M && wblk * kF8Block < args.N;
       float acc[kF8Block];
 #pragma unroll
       for (int c = 0; c < kF8Block; ++c) acc[c] = 0.f;
       for (int kb = 0; kb < nk; ++kb, ++pb) {
         const int j = pb & 1;
-        const float sc = (valid ? args.sa[(int64_t)row * nk + kb] : 0.f) * args.sw[(int64_t)nt * nk + kb];
+        const float sc = valid ? args.sa[(int64_t)row * nk + kb] * args.sw[(int64_t)wblk * nk + kb] : 0.f;
         if (!mbar_wait(&pfull[j], (pb >> 1) & 1)) {
           report(args.status, DEV_TIMEOUT);
           *abort_flag = 1;
@@ -240,22 +247,22 @@ __global__ void __launch_bounds__(192, 1) gemm_fp8_kernel(const __grid_constant_
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + j * kF8Block + ((uint32_t)(q * 32) << 16);
+        const uint32_t taddr = tmem_base + j * kF8BN + hf * kF8Block + ((uint32_t)(q * 32) << 16);
 #pragma unroll
-        for (int c = 0; c < kF8Block / 32; ++c) {
-          uint32_t p[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, p);
+        for (int c = 0; c < kF8Block / 16; ++c) {
+          uint32_t p[16];
+          tmem_ld_32x32b_x16(taddr + c * 16, p);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            acc[c * 32 + i] = __fadd_rn(acc[c * 32 + i], __fmul_rn(__uint_as_float(p[i]), sc));
+          for (int i = 0; i < 16; ++i)
+            acc[c * 16 + i] = __fadd_rn(acc[c * 16 + i], __fmul_rn(__uint_as_float(p[i]), sc));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty[j]);
       }
       if (!ok || !valid || *abort_flag) continue;
-      const int64_t base = (int64_t)row * args.N + (int64_t)nt * kF8Block;
+      const int64_t base = (int64_t)row * args.N + (int64_t)wblk * kF8Block;
       if (args.c_fp32) {
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.C) + base);
 #pragma unroll
@@ -329,7 +336,7 @@ bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, con
   const int a_rows = M < 128 ? (int)std::max<int64_t>(8, cdiv(M, 8) * 8) : 128;
   CUtensorMap ta, tb;
   if (!encode_tmap_2d_u8(&ta, Aq, K, M, K, kF8Block, a_rows) ||
-      !encode_tmap_2d_u8(&tb, Wq, K, N, K, kF8Block, kF8Block))
+      !encode_tmap_2d_u8(&tb, Wq, K, N, K, kF8Block, kF8BN))
     return fail(BI_ERR_CUDA, "bi_gemm_fp8: TMA descriptor failed");
   F8Args a;
   a.sa = sa;
@@ -340,12 +347,12 @@ bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, con
   a.N = (int)N;
   a.nkb = (int)(K / kF8Block);
   a.m_tiles = (int)cdiv(M, 128);
-  a.n_tiles = (int)(N / kF8Block);
+  a.n_tiles = (int)cdiv(N, kF8BN);
   a.a_box_rows = a_rows;
   a.c_fp32 = c_dtype == BI_DTYPE_FP32;
   const int64_t tiles = (int64_t)a.m_tiles * a.n_tiles;
   BI_REQUIRE_SHAPE(tiles < (1ll << 31), "too many tiles");
-  return launched(launch_pdl(gemm_fp8_kernel, dim3((unsigned)std::min<int64_t>(tiles, num_sms())), dim3(192),
+  return launched(launch_pdl(gemm_fp8_kernel, dim3((unsigned)std::min<int64_t>(tiles, num_sms())), dim3(kF8Threads),
                              kF8SmemBytes, as_stream(stream), ta, tb, a),
                   "bi_gemm_fp8");
 }

@@ -55,13 +55,16 @@ __host__ __device__ inline int64_t ssd_store_floats(int H, int /*G*/, int P, int
 __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) {
   extern __shared__ __align__(16) float sm[];
   const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
+  const int NS = N + 1;           // padded row stride of B and C: conflict-free column walks
   float* Hs = sm;                 // [N][P] state entering the chunk
-  float* Bs = Hs + N * P;         // [Q][N]
-  float* Cs = Bs + Q * N;         // [Q][N]
-  float* xs = Cs + Q * N;         // [Q][P]
+  float* Bs = Hs + N * P;         // [Q][NS]
+  float* Cs = Bs + Q * NS;        // [Q][NS]
+  float* xs = Cs + Q * NS;        // [Q][P]
   float* Gm = xs + Q * P;         // [Q][Q] (C_i . B_j) scaled by the decay
   float* ls = Gm + Q * Q;         // [Q] loga
   float* Ls = ls + Q;             // [Q] cumulative
+  float* eL = Ls + Q;             // [Q] exp(L_i)
+  float* dq = eL + Q;             // [Q] exp(L_{Q-1} - L_j), for the exit state
   pdl_trigger();
   pdl_wait();
   const int piece = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -82,6 +85,7 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
   float* st_l = st_x + (int64_t)Q * H * P;                     // [Q][H]
 
   for (int i = tid; i < N * P; i += kSsdThreads) Hs[i] = st_H[i];
+  bool advanced = false;  // some chunk completed in this call: the stored state changes
   const int64_t c_first = p0 / Q, c_last = (p1 - 1) / Q;
   for (int64_t c = c_first; c <= c_last; ++c) {
     const int64_t cs = c * Q;
@@ -90,11 +94,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
     for (int e = tid; e < i1 * N; e += kSsdThreads) {
       const int i = e / N, n = e % N;
       if (i < i0) {
-        Bs[e] = st_B[((int64_t)i * H + h) * N + n];
+        Bs[i * NS + n] = st_B[((int64_t)i * H + h) * N + n];
       } else {
         const int64_t r = row0 + (cs + i - p0);
-        Bs[e] = bf2f(a.B[(r * G + g) * N + n]);
-        Cs[e] = bf2f(a.C[(r * G + g) * N + n]);
+        Bs[i * NS + n] = bf2f(a.B[(r * G + g) * N + n]);
+        Cs[i * NS + n] = bf2f(a.C[(r * G + g) * N + n]);
       }
     }
     for (int e = tid; e < i1 * P; e += kSsdThreads) {
@@ -113,35 +117,107 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
       }
     }
     __syncthreads();
-    // decay-scaled (C_i . B_j) for the rows this call computes
-    for (int e = tid; e < (i1 - i0) * i1; e += kSsdThreads) {
-      const int i = i0 + e / i1, j = e % i1;
-      if (j > i) continue;
-      float d = 0.f;
-      for (int n = 0; n < N; ++n) d = __fmaf_rn(Cs[i * N + n], Bs[j * N + n], d);
-      Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), d);
+    for (int i = tid; i < i1; i += kSsdThreads) {
+      eL[i] = expf(Ls[i]);
+      if (i1 == Q) dq[i] = expf(__fsub_rn(Ls[Q - 1], Ls[i]));
+    }
+    // decay-scaled (C_i . B_j) for the rows this call computes; 4 x 4 tiles of (i, j)
+    {
+      const int ni = (i1 - i0 + 3) / 4, nj = (i1 + 3) / 4;
+      for (int e = tid; e < ni * nj; e += kSsdThreads) {
+        const int ib = i0 + (e / nj) * 4, jb = (e % nj) * 4;
+        if (jb > ib + 3) continue;  // above the diagonal
+        float acc[4][4] = {};
+        for (int n = 0; n < N; ++n) {
+          float c[4], bb[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            c[u] = ib + u < i1 ? Cs[(ib + u) * NS + n] : 0.f;
+            bb[u] = jb + u < i1 ? Bs[(jb + u) * NS + n] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(c[u], bb[v], acc[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int i = ib + u, j = jb + v;
+            if (i < i1 && j <= i) Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), acc[u][v]);
+          }
+      }
     }
     __syncthreads();
-    for (int e = tid; e < (i1 - i0) * P; e += kSsdThreads) {
-      const int i = i0 + e / P, p = e % P;
-      float inter = 0.f;
-      for (int n = 0; n < N; ++n) inter = __fmaf_rn(Cs[i * N + n], Hs[n * P + p], inter);
-      float intra = 0.f;
-      for (int j = 0; j <= i; ++j) intra = __fmaf_rn(Gm[i * Q + j], xs[j * P + p], intra);
-      const int64_t r = row0 + (cs + i - p0);
-      a.y[(r * H + h) * P + p] = __fadd_rn(__fmul_rn(expf(Ls[i]), inter), intra);
+    // rows: 4 x 4 tiles of (i, p)
+    {
+      const int ni = (i1 - i0 + 3) / 4, np4 = P / 4;
+      for (int e = tid; e < ni * np4; e += kSsdThreads) {
+        const int ib = i0 + (e / np4) * 4, pb = (e % np4) * 4;
+        float inter[4][4] = {}, intra[4][4] = {};
+        for (int n = 0; n < N; ++n) {
+          const float4 hv = *reinterpret_cast<const float4*>(&Hs[n * P + pb]);
+          const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float c = ib + u < i1 ? Cs[(ib + u) * NS + n] : 0.f;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) inter[u][v] = __fmaf_rn(c, hh[v], inter[u][v]);
+          }
+        }
+        const int jmax = ib + 3 < i1 - 1 ? ib + 3 : i1 - 1;
+        for (int j = 0; j <= jmax; ++j) {
+          const float4 xv = *reinterpret_cast<const float4*>(&xs[j * P + pb]);
+          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (j > ib + u) continue;  // row ib+u sums j = 0 .. ib+u only
+            const float gm = Gm[(ib + u) * Q + j];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) intra[u][v] = __fmaf_rn(gm, xx[v], intra[u][v]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = ib + u;
+          if (i >= i1) continue;
+          const int64_t r = row0 + (cs + i - p0);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            a.y[(r * H + h) * P + pb + v] = __fadd_rn(__fmul_rn(eL[i], inter[u][v]), intra[u][v]);
+        }
+      }
     }
     if (i1 == Q) {
-      // the chunk is complete: its exit state enters the next chunk
+      // the chunk is complete: its exit state enters the next chunk; 4 x 4 tiles of (n, p)
       __syncthreads();
-      const float eL = expf(Ls[Q - 1]);
-      for (int e = tid; e < N * P; e += kSsdThreads) {
-        const int n = e / P, p = e % P;
-        float acc = __fmul_rn(eL, Hs[e]);
-        for (int j = 0; j < Q; ++j)
-          acc = __fmaf_rn(__fmul_rn(expf(__fsub_rn(Ls[Q - 1], Ls[j])), Bs[j * N + n]), xs[j * P + p], acc);
-        Hs[e] = acc;
+      const float eLast = eL[Q - 1];
+      const int nn4 = N / 4, np4 = P / 4;
+      for (int e = tid; e < nn4 * np4; e += kSsdThreads) {
+        const int nb = (e / np4) * 4, pb = (e % np4) * 4;
+        float acc[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[u][v] = __fmul_rn(eLast, Hs[(nb + u) * P + pb + v]);
+        for (int j = 0; j < Q; ++j) {
+          const float4 xv = *reinterpret_cast<const float4*>(&xs[j * P + pb]);
+          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float wb = __fmul_rn(dq[j], Bs[j * NS + nb + u]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(wb, xx[v], acc[u][v]);
+          }
+        }
+        // a thread reads and writes only its own tile of Hs here
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) Hs[(nb + u) * P + pb + v] = acc[u][v];
       }
+      advanced = true;
     } else {
       // the chunk stays open: keep the inputs of the new offsets for the calls that finish it
       for (int e = tid; e < (i1 - i0) * P; e += kSsdThreads) {
@@ -150,14 +226,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
       }
       for (int e = tid; e < (i1 - i0) * N; e += kSsdThreads) {
         const int i = i0 + e / N, n = e % N;
-        st_B[((int64_t)i * H + h) * N + n] = Bs[i * N + n];
+        st_B[((int64_t)i * H + h) * N + n] = Bs[i * NS + n];
       }
       for (int i = i0 + tid; i < i1; i += kSsdThreads) st_l[(int64_t)i * H + h] = ls[i];
     }
     __syncthreads();
   }
-  // the state entering the sequence's next position
-  for (int i = tid; i < N * P; i += kSsdThreads) st_H[i] = Hs[i];
+  // the state entering the sequence's next position (unchanged unless a chunk completed)
+  if (advanced)
+    for (int i = tid; i < N * P; i += kSsdThreads) st_H[i] = Hs[i];
 }
 
 }  // namespace bi
@@ -178,15 +255,16 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
   if (pieces == 0) return BI_OK;
   BI_REQUIRE(x && B && C && loga && piece_seq && piece_row0 && piece_pos0 && state && y, "null pointer");
   BI_REQUIRE(H > 0 && G > 0 && H % G == 0, "H must be a positive multiple of G");
-  BI_REQUIRE_SHAPE(Q >= 1 && Q <= kSsdMaxQ && N >= 1 && N <= kSsdMaxN && P >= 1 && P <= kSsdMaxP,
-                   "chunk <= 64, state size <= 128 and head size <= 128");
+  BI_REQUIRE_SHAPE(Q >= 4 && Q <= kSsdMaxQ && Q % 4 == 0 && N >= 4 && N <= kSsdMaxN && N % 4 == 0 && P >= 4 &&
+                       P <= kSsdMaxP && P % 4 == 0,
+                   "chunk <= 64, state size <= 128 and head size <= 128, each a multiple of 4");
   BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0, "bad pieces / heads / sequences");
-  const int smem = (int)((size_t)(N * P + 2 * Q * N + Q * P + Q * Q + 2 * Q) * sizeof(float));
+  const int smem = (int)((size_t)(N * P + 2 * Q * (N + 1) + Q * P + Q * Q + 4 * Q) * sizeof(float));
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    const int mx = (kSsdMaxN * kSsdMaxP + 2 * kSsdMaxQ * kSsdMaxN + kSsdMaxQ * kSsdMaxP + kSsdMaxQ * kSsdMaxQ +
-                    2 * kSsdMaxQ) * (int)sizeof(float);
+    const int mx = (kSsdMaxN * kSsdMaxP + 2 * kSsdMaxQ * (kSsdMaxN + 1) + kSsdMaxQ * kSsdMaxP +
+                    kSsdMaxQ * kSsdMaxQ + 4 * kSsdMaxQ) * (int)sizeof(float);
     attr_err = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   });
   if (attr_err != cudaSuccess)
