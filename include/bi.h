@@ -231,6 +231,37 @@ bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, v
 bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, const void* Wq, const float* sw,
                       int64_t N, void* C, int c_dtype, int mode, void* stream);
 
+/* ---------------------------------------------------------- FP8 KV cache
+ * [Article] §4.2 ("FP8 KV cache: keep FP8 storage, unify the read path"): K
+ * and V are stored in FP8; prefill, decode and the training recompute all read
+ * them through one path, dequantise-and-gather into a bf16 workspace sized by
+ * limits, then the same bi_attention.  Readings: e4m3 codes, one power-of-two
+ * scale per (token, kv head) vector of hd values for K and for V (smallest s
+ * with 448 s >= amax, 1 for an all-zero vector); code x scale is exact in bf16.
+ *
+ * bi_kv_fp8_write: k, v bf16 [T, Hkv, hd] (device; rows grouped in pieces as in
+ * bi_attention) -> codes in k_cache8 / v_cache8 uint8 [n_blocks, Hkv, 64, hd]
+ * and scales in k_scale / v_scale fp32 [n_blocks, Hkv, 64] at each row's slot
+ * (block_table[seq][pos / 64], pos % 64).  hd in {64, 128}.  A row whose block
+ * is out of range is skipped and sets the device status. */
+bi_status bi_kv_fp8_write(const void* k, const void* v, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                          const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hkv, int hd,
+                          const int32_t* block_table, int64_t max_blocks_per_seq, int64_t n_blocks, void* k_cache8,
+                          void* v_cache8, float* k_scale, float* v_scale, void* stream);
+/* bi_kv_fp8_gather: for every piece p, the pages holding positions
+ * 0 .. piece_pos0[p] + (its rows) - 1 of its sequence, dequantised into the
+ * bf16 workspace page p * max_blocks_per_seq + l (k_ws, v_ws bf16
+ * [P * max_blocks_per_seq, Hkv, 64, hd], 16-byte aligned);
+ * ws_block_table int32 [P, max_blocks_per_seq] receives those page ids (-1
+ * after the last page).  Call bi_attention with the workspace as the cache,
+ * ws_block_table as the block table and piece p reading row p of it
+ * (piece_seq = 0 .. P-1), n_blocks = P * max_blocks_per_seq. */
+bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,
+                           int64_t n_blocks, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int Hkv, int hd, const int32_t* block_table,
+                           int64_t max_blocks_per_seq, void* k_ws, void* v_ws, int32_t* ws_block_table,
+                           void* stream);
+
 /* --------------------------------------------------- Mamba-2 chunked scan
  * [Article] §6 ("Transfer: Nemotron, a Mamba hybrid architecture + NVFP4"):
  * decode replays prefill's chunked arithmetic instead of its own single-step

@@ -79,6 +79,10 @@ _SIGS = {
     "bi_topk": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _int, _vp]),
     "bi_quantize_fp8": (_int, [_vp, _i64, _i64, _int, _vp, _vp, _vp]),
     "bi_ssd_state_bytes": (_sz, [_int, _int, _int, _int, _int]),
+    "bi_kv_fp8_write": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _i64, _i64, _vp, _vp, _vp,
+                               _vp, _vp]),
+    "bi_kv_fp8_gather": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _int, _int, _vp, _i64, _vp, _vp, _vp,
+                                _vp]),
     "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _int, _int, _vp, _i64,
                                  _vp, _int, _vp]),
     "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
@@ -238,6 +242,20 @@ def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_
 
 def bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split) -> int:
     return load().bi_attention_workspace_size(max_T, Hq, hd, max_ctx, kv_split)
+
+
+def bi_kv_fp8_write(k, v, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hkv, hd, block_table,
+                    max_blocks_per_seq, n_blocks, k_cache8, v_cache8, k_scale, v_scale, stream=None):
+    _check(load().bi_kv_fp8_write(_p(k), _p(v), T, _p(piece_seq), _p(piece_row0), _p(piece_pos0), P, max_q_len, Hkv,
+                                  hd, _p(block_table), max_blocks_per_seq, n_blocks, _p(k_cache8), _p(v_cache8),
+                                  _p(k_scale), _p(v_scale), _s(stream)))
+
+
+def bi_kv_fp8_gather(k_cache8, v_cache8, k_scale, v_scale, n_blocks, piece_seq, piece_row0, piece_pos0, P, Hkv, hd,
+                     block_table, max_blocks_per_seq, k_ws, v_ws, ws_block_table, stream=None):
+    _check(load().bi_kv_fp8_gather(_p(k_cache8), _p(v_cache8), _p(k_scale), _p(v_scale), n_blocks, _p(piece_seq),
+                                   _p(piece_row0), _p(piece_pos0), P, Hkv, hd, _p(block_table), max_blocks_per_seq,
+                                   _p(k_ws), _p(v_ws), _p(ws_block_table), _s(stream)))
 
 
 def bi_ssd_state_bytes(H, G, P, N, Q) -> int:
