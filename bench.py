@@ -432,7 +432,26 @@ def kernel_table(args):
                                             "16/4 heads x 128, split 512", "us": round(us, 1),
                                             "GB/s": round(nbytes / us / 1e3, 1), "frac": round(nbytes / us / 1e3 / hbm, 3),
                                             "bound": "hbm", "note": "KV (1.2 GB) exceeds L2"}
-    del kc, vc
+    # the same decode through an FP8 KV cache: dequantise-and-gather into a bf16 workspace, then the same attention
+    k8 = torch.randint(0, 0x7E, (nblk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+    v8 = torch.randint(0, 0x7E, (nblk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+    ks8 = torch.full((nblk, Hkv, 64), 2.0 ** -8, device=dev)
+    vs8 = torch.full_like(ks8, 2.0 ** -8)
+    kw = torch.empty((B * mb, Hkv, 64, hd), dtype=torch.bfloat16, device=dev)
+    vw = torch.empty_like(kw)
+    wbt = torch.empty((B, mb), dtype=torch.int32, device=dev)
+
+    def fp8_step():
+        bi.bi_kv_fp8_gather(k8, v8, ks8, vs8, nblk, seq, row0, pos0, B, Hkv, hd, bt, mb, kw, vw, wbt)
+        bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kw, vw, wbt, mb, B * mb, max_ctx, 512, hd ** -0.5,
+                        ws, ao)
+    us8 = _graph_us(fp8_step, n=5, reps=5)
+    b8 = int(lens.sum()) * Hkv * (hd + 4) * 2
+    out["attention_decode_long_context_fp8_kv"] = {
+        "us": round(us8, 1), "GB/s": round(b8 / us8 / 1e3, 1), "frac": round(b8 / us8 / 1e3 / hbm, 3), "bound": "hbm",
+        "note": "algorithmic bytes = the FP8 cache (codes + scales) read once; the gather writes and the attention "
+                "re-reads a bf16 copy (one read path for prefill and decode, as the pages do)"}
+    del kc, vc, k8, v8, kw, vw
     # vocab-wide logprob, large-vocab shape (8.47 GB of fp32 logits, > L2)
     T, Vv = 16384, 129280
     logits = torch.randn((T, Vv), device=dev)
@@ -483,8 +502,8 @@ def kernel_table(args):
         sq = torch.arange(n_seq, dtype=torch.int32, device=dev)
         r0 = torch.arange(0, T + 1, per, dtype=torch.int32, device=dev)
         p0 = torch.full((n_seq,), 0 if per > 1 else 40, dtype=torch.int32, device=dev)
-        us = _graph_us(lambda: bi.bi_ssd_chunk_scan(xs, Bs, Cs, la, sq, r0, p0, n_seq, Hs, Gs, Ps, Ns, Qs, st, n_seq,
-                                                    ys), n=3, reps=3)
+        us = _graph_us(lambda: bi.bi_ssd_chunk_scan(xs, Bs, Cs, la, sq, r0, p0, n_seq, per, Hs, Gs, Ps, Ns, Qs, st,
+                                                    n_seq, ys), n=3, reps=3)
         if per > 1:   # every chunk complete: rows + exit states
             fma = n_seq * Hs * (per // Qs) * (Qs * (Qs + 1) / 2 * Ns + Qs * Ps * (Ns + (Qs + 1) / 2) + Ns * Ps * Qs)
         else:         # one row at offset 40: its chunk row and no exit state

@@ -275,7 +275,9 @@ bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const flo
  * Inputs (device): x bf16 [T, H, P], B and C bf16 [T, G, N], loga fp32 [T, H]
  * (<= 0); pieces as in bi_attention (piece_seq [pieces], piece_row0
  * [pieces + 1], piece_pos0 [pieces]): at most one piece per sequence per call,
- * each sequence's pieces passed in position order over successive calls.
+ * each sequence's pieces passed in position order over successive calls;
+ * max_q_len (host) bounds the rows of any piece, and calls with max_q_len = 1
+ * (decode steps) run a lighter schedule of the same arithmetic.
  * state: fp32, bi_ssd_state_bytes(H, G, P, N, Q) bytes per sequence
  * (n_seq of them), zeroed by the caller for a new sequence; it holds the state
  * entering the current chunk and that chunk's earlier inputs.  y: fp32
@@ -283,8 +285,9 @@ bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const flo
  * runs the same kernel. */
 size_t bi_ssd_state_bytes(int H, int G, int P, int N, int Q);
 bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* loga, const int32_t* piece_seq,
-                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int H, int G,
-                            int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode, void* stream);
+                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int64_t max_q_len,
+                            int H, int G, int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode,
+                            void* stream);
 
 /* ------------------------------------------------------- deterministic Top-K
  * [Article] §4.3 ("Top-K in sparse attention: fix ties and order").

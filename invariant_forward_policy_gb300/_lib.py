@@ -83,8 +83,8 @@ _SIGS = {
                                _vp, _vp]),
     "bi_kv_fp8_gather": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _int, _int, _vp, _i64, _vp, _vp, _vp,
                                 _vp]),
-    "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _int, _int, _vp, _i64,
-                                 _vp, _int, _vp]),
+    "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _int, _vp,
+                                 _i64, _vp, _int, _vp]),
     "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
@@ -262,10 +262,10 @@ def bi_ssd_state_bytes(H, G, P, N, Q) -> int:
     return load().bi_ssd_state_bytes(H, G, P, N, Q)
 
 
-def bi_ssd_chunk_scan(x, B, C, loga, piece_seq, piece_row0, piece_pos0, pieces, H, G, P, N, Q, state, n_seq, y,
-                      mode=BI_INVARIANT, stream=None):
+def bi_ssd_chunk_scan(x, B, C, loga, piece_seq, piece_row0, piece_pos0, pieces, max_q_len, H, G, P, N, Q, state, n_seq,
+                      y, mode=BI_INVARIANT, stream=None):
     _check(load().bi_ssd_chunk_scan(_p(x), _p(B), _p(C), _p(loga), _p(piece_seq), _p(piece_row0), _p(piece_pos0),
-                                    pieces, H, G, P, N, Q, _p(state), n_seq, _p(y), mode, _s(stream)))
+                                    pieces, max_q_len, H, G, P, N, Q, _p(state), n_seq, _p(y), mode, _s(stream)))
 
 
 def bi_quantize_fp8(x, R, C, block_rows, q, scales, stream=None):

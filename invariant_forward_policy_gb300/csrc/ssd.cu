@@ -237,6 +237,89 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
     for (int i = tid; i < N * P; i += kSsdThreads) st_H[i] = Hs[i];
 }
 
+// Decode steps (one position per piece): the same row and exit-state
+// arithmetic as ssd_scan_kernel, term for term and in the same order, with the
+// entering state and the chunk's earlier inputs read straight from the store
+// instead of staged in shared memory, so that many CTAs share an SM.
+__global__ void __launch_bounds__(128) ssd_step_kernel(const SsdArgs a) {
+  __shared__ float c_s[kSsdMaxN], gm[kSsdMaxQ], Ls[kSsdMaxQ], dq[kSsdMaxQ], b_s[kSsdMaxN], x_s[kSsdMaxP];
+  __shared__ float l_s[kSsdMaxQ];
+  pdl_trigger();
+  pdl_wait();
+  const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
+  const int piece = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int g = h / (H / G);
+  const int row0 = a.row0[piece];
+  if (a.row0[piece + 1] - row0 != 1) {  // this kernel takes single-position pieces only
+    if (a.row0[piece + 1] - row0 > 1 && tid == 0) report(a.status, DEV_BAD_INDEX);
+    return;
+  }
+  const int s = a.seq[piece];
+  const int64_t pos = a.pos0[piece];
+  if (s < 0 || s >= a.n_seq || pos < 0) {
+    if (tid == 0) report(a.status, DEV_BAD_INDEX);
+    return;
+  }
+  float* st = a.store + (int64_t)s * a.store_floats;
+  float* st_H = st + (int64_t)h * N * P;
+  float* st_B = st + (int64_t)H * N * P;
+  float* st_x = st_B + (int64_t)Q * H * N;
+  float* st_l = st_x + (int64_t)Q * H * P;
+  const int i = (int)(pos % Q);
+  const int64_t r = row0;
+  for (int n = tid; n < N; n += 128) {
+    c_s[n] = bf2f(a.C[(r * G + g) * N + n]);
+    b_s[n] = bf2f(a.B[(r * G + g) * N + n]);
+  }
+  for (int p = tid; p < P; p += 128) x_s[p] = bf2f(a.x[(r * H + h) * P + p]);
+  for (int j = tid; j <= i; j += 128) l_s[j] = j < i ? st_l[(int64_t)j * H + h] : a.loga[r * H + h];
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int j = 0; j <= i; ++j) {
+      acc = __fadd_rn(acc, l_s[j]);
+      Ls[j] = acc;
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j <= i; j += 128) {
+    const float* bj = j < i ? st_B + ((int64_t)j * H + h) * N : b_s;
+    float d = 0.f;
+    for (int n = 0; n < N; ++n) d = __fmaf_rn(c_s[n], bj[n], d);
+    gm[j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), d);
+    if (i == Q - 1) dq[j] = expf(__fsub_rn(Ls[Q - 1], Ls[j]));
+  }
+  __syncthreads();
+  const float eLi = expf(Ls[i]);
+  for (int p = tid; p < P; p += 128) {
+    float inter = 0.f;
+    for (int n = 0; n < N; ++n) inter = __fmaf_rn(c_s[n], st_H[(int64_t)n * P + p], inter);
+    float intra = 0.f;
+    for (int j = 0; j <= i; ++j)
+      intra = __fmaf_rn(gm[j], j < i ? st_x[((int64_t)j * H + h) * P + p] : x_s[p], intra);
+    a.y[(r * H + h) * P + p] = __fadd_rn(__fmul_rn(eLi, inter), intra);
+  }
+  if (i == Q - 1) {
+    // the position completes its chunk: the exit state replaces the stored one
+    __syncthreads();  // every thread has read st_H for its row
+    const float eLast = eLi;
+    for (int e = tid; e < N * P; e += 128) {
+      const int n = e / P, p = e % P;
+      float acc = __fmul_rn(eLast, st_H[e]);
+      for (int j = 0; j < Q; ++j) {
+        const float bjn = j < i ? st_B[((int64_t)j * H + h) * N + n] : b_s[n];
+        const float xjp = j < i ? st_x[((int64_t)j * H + h) * P + p] : x_s[p];
+        acc = __fmaf_rn(__fmul_rn(dq[j], bjn), xjp, acc);
+      }
+      st_H[e] = acc;  // each element is read and written by its own thread only
+    }
+  } else {
+    for (int n = tid; n < N; n += 128) st_B[((int64_t)i * H + h) * N + n] = b_s[n];
+    for (int p = tid; p < P; p += 128) st_x[((int64_t)i * H + h) * P + p] = x_s[p];
+    if (tid == 0) st_l[(int64_t)i * H + h] = l_s[i];
+  }
+}
+
 }  // namespace bi
 
 extern "C" {
@@ -247,8 +330,9 @@ size_t bi_ssd_state_bytes(int H, int G, int P, int N, int Q) {
 }
 
 bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* loga, const int32_t* piece_seq,
-                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int H, int G,
-                            int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode, void* stream) {
+                            const int32_t* piece_row0, const int32_t* piece_pos0, int64_t pieces, int64_t max_q_len,
+                            int H, int G, int P, int N, int Q, void* state, int64_t n_seq, float* y, int mode,
+                            void* stream) {
   using namespace bi;
   BI_REQUIRE(pieces >= 0, "bad shape");
   BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
@@ -258,7 +342,8 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
   BI_REQUIRE_SHAPE(Q >= 4 && Q <= kSsdMaxQ && Q % 4 == 0 && N >= 4 && N <= kSsdMaxN && N % 4 == 0 && P >= 4 &&
                        P <= kSsdMaxP && P % 4 == 0,
                    "chunk <= 64, state size <= 128 and head size <= 128, each a multiple of 4");
-  BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0, "bad pieces / heads / sequences");
+  BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0 && max_q_len >= 1,
+             "bad pieces / heads / sequences / max_q_len");
   const int smem = (int)((size_t)(N * P + 2 * Q * (N + 1) + Q * P + Q * Q + 4 * Q) * sizeof(float));
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -287,6 +372,11 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
   a.P = P;
   a.N = N;
   a.Q = Q;
+  // single-position pieces (decode steps) take the lighter schedule: same arithmetic
+  if (max_q_len == 1)
+    return launched(launch_pdl(ssd_step_kernel, dim3((unsigned)pieces, (unsigned)H), dim3(128), 0, as_stream(stream),
+                               a),
+                    "bi_ssd_chunk_scan");
   return launched(launch_pdl(ssd_scan_kernel, dim3((unsigned)pieces, (unsigned)H), dim3(kSsdThreads), smem,
                              as_stream(stream), a),
                   "bi_ssd_chunk_scan");

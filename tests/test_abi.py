@@ -98,7 +98,7 @@ def test_ssd_validation_without_gpu():
     lib = bi.load()
     assert bi.bi_ssd_state_bytes(4, 3, 64, 128, 64) == 0                      # H % G != 0
     assert bi.bi_ssd_state_bytes(4, 2, 64, 128, 64) == 4 * (4 * 128 * 64 + 64 * 4 * 128 + 64 * 4 * 64 + 64 * 4)
-    args = [16, 16, 16, 16, 16, 16, 16, 1]
+    args = [16, 16, 16, 16, 16, 16, 16, 1, 1]
     assert lib.bi_ssd_chunk_scan(*args, 4, 2, 64, 256, 64, 16, 1, 16, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_ssd_chunk_scan(*args, 4, 3, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_ERR_INVALID_ARG
-    assert lib.bi_ssd_chunk_scan(None, 16, 16, 16, 16, 16, 16, 0, 4, 2, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_OK
+    assert lib.bi_ssd_chunk_scan(None, 16, 16, 16, 16, 16, 16, 0, 1, 4, 2, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_OK

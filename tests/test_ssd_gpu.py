@@ -45,8 +45,8 @@ class Scan:
                             device="cuda")
         pos0 = torch.tensor([p[1] for p in pieces], dtype=torch.int32, device="cuda")
         bi.bi_ssd_chunk_scan(dev_bf16(self.x[rows]), dev_bf16(self.B[rows]), dev_bf16(self.C[rows]),
-                             torch.from_numpy(self.l[rows]).cuda(), seq, row0, pos0, len(pieces), H, G, P, N, Q,
-                             self.state, len(self.lens), y)
+                             torch.from_numpy(self.l[rows]).cuda(), seq, row0, pos0, len(pieces),
+                             max(p[2] for p in pieces), H, G, P, N, Q, self.state, len(self.lens), y)
         yh = y.cpu().numpy()
         r = 0
         for s, p0, n in pieces:
