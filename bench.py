@@ -734,6 +734,63 @@ def run_kernel_case(name: str, reps: int):
         pd = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
         for _ in range(reps):
             ep.run(pd)
+    elif name == "gemm_fp8":
+        # block-FP8 W8A8 GEMM at a prefill FFN shape (operands quantised once, untimed)
+        M, N, K = 8192, 11264, 2048
+        A = torch.randn((M, K), device=dev).to(torch.bfloat16)
+        W = (0.02 * torch.randn((N, K), device=dev)).to(torch.bfloat16)
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((M, K // 128), device=dev)
+        qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        sw = torch.empty((N // 128, K // 128), device=dev)
+        bi.bi_quantize_fp8(A, M, K, 1, qa, sa)
+        bi.bi_quantize_fp8(W, N, K, 128, qw, sw)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            bi.bi_gemm_fp8(qa, sa, M, K, qw, sw, N, C)
+    elif name == "topk_decode":
+        # deterministic Top-K, K = 2048, one decode step of 64 rows with contexts 1K-32K
+        from synthetic import C5, make_c5_prompt_lengths
+        nv = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"]).astype(np.int32)
+        T, ld = len(nv), int(nv.max())
+        S = torch.randn((T, ld), device=dev)
+        idx = torch.empty((T, 2048), dtype=torch.int32, device=dev)
+        nvd = torch.from_numpy(nv).to(dev)
+        for _ in range(reps):
+            bi.bi_topk(S, T, ld, nvd, 2048, idx)
+    elif name == "ssd_prefill":
+        # Mamba-2 chunked scan: 16 sequences x 2048, 32 heads x 64, state 128, 8 groups, chunk 64
+        n_seq, per, Hs, Gs, Ps, Ns, Qs = 16, 2048, 32, 8, 64, 128, 64
+        T = n_seq * per
+        xs = torch.randn((T, Hs, Ps), device=dev).to(torch.bfloat16)
+        Bs = (torch.randn((T, Gs, Ns), device=dev) * Ns ** -0.5).to(torch.bfloat16)
+        Cs = (torch.randn((T, Gs, Ns), device=dev) * Ns ** -0.5).to(torch.bfloat16)
+        la = -torch.rand((T, Hs), device=dev) * 0.2
+        st = torch.zeros((n_seq, bi.bi_ssd_state_bytes(Hs, Gs, Ps, Ns, Qs) // 4), device=dev)
+        ys = torch.empty((T, Hs, Ps), device=dev)
+        sq = torch.arange(n_seq, dtype=torch.int32, device=dev)
+        r0 = torch.arange(0, T + 1, per, dtype=torch.int32, device=dev)
+        p0 = torch.zeros(n_seq, dtype=torch.int32, device=dev)
+        for _ in range(reps):
+            st.zero_()
+            bi.bi_ssd_chunk_scan(xs, Bs, Cs, la, sq, r0, p0, n_seq, per, Hs, Gs, Ps, Ns, Qs, st, n_seq, ys)
+    elif name == "kv_fp8_gather":
+        # FP8 KV read path: 16 sequences x 8192 context, 4 kv heads x 128 (0.27 GB of codes)
+        B, Hkv, hd, ctx = 16, 4, 128, 8192
+        mb = ctx // 64
+        k8 = torch.randint(0, 0x7E, (B * mb, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+        v8 = torch.randint(0, 0x7E, (B * mb, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+        ks = torch.full((B * mb, Hkv, 64), 2.0 ** -8, device=dev)
+        vs = torch.full_like(ks, 2.0 ** -8)
+        bt = torch.arange(B * mb, dtype=torch.int32, device=dev).view(B, mb)
+        kw = torch.empty((B * mb, Hkv, 64, hd), dtype=torch.bfloat16, device=dev)
+        vw = torch.empty_like(kw)
+        wbt = torch.empty((B, mb), dtype=torch.int32, device=dev)
+        seq = torch.arange(B, dtype=torch.int32, device=dev)
+        row0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        pos0 = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
+        for _ in range(reps):
+            bi.bi_kv_fp8_gather(k8, v8, ks, vs, B * mb, seq, row0, pos0, B, Hkv, hd, bt, mb, kw, vw, wbt)
     elif name == "attention_decode_long":
         # persistent decode schedule: 32 sequences x 4096 context, 16/4 heads x 128 (268 MB of KV > L2)
         B, Hq, Hkv, hd, ctx = 32, 16, 4, 128, 4096
@@ -761,7 +818,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
-                         "attention_decode, attention_decode_long) or the whole step (step) and exit; for profiling")
+                         "attention_decode, attention_decode_long, gemm_fp8, topk_decode, ssd_prefill, kv_fp8_gather) or "
+                         "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
