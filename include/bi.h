@@ -251,7 +251,7 @@ bi_status bi_kv_fp8_write(const void* k, const void* v, int64_t T, const int32_t
 /* bi_kv_fp8_gather: for every piece p, the pages holding positions
  * 0 .. piece_pos0[p] + (its rows) - 1 of its sequence, dequantised into the
  * bf16 workspace page p * max_blocks_per_seq + l (k_ws, v_ws bf16
- * [P * max_blocks_per_seq, Hkv, 64, hd], 16-byte aligned);
+ * [P * max_blocks_per_seq, Hkv, 64, hd]; workspace and cache 16-byte aligned);
  * ws_block_table int32 [P, max_blocks_per_seq] receives those page ids (-1
  * after the last page).  Call bi_attention with the workspace as the cache,
  * ws_block_table as the block table and piece p reading row p of it

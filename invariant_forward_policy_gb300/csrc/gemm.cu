@@ -588,14 +588,16 @@ static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUten
   return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: bad epilogue");
 }
 
-// Accumulator tile width for a weight: a function of its shape (N, K) only,
-// never of M.  Small weights (under 2M elements) take 64-wide tiles, so that a
-// decode-size call spreads over many CTAs; larger ones 128, and weights of
-// 16M+ elements or 32K+ rows 256, where the tensor pipe rather than shared
-// memory bandwidth bounds a prefill-size call.
-static int tile_n_for(int64_t n_rows_w, int64_t K, bool /*swiglu*/) {
+// Accumulator tile width for a weight: a function of its shape (N, K, number of
+// experts) only, never of M.  Small weights (under 2M elements) take 64-wide
+// tiles, so that a decode-size call spreads over many CTAs; larger ones 128,
+// and weights of 16M+ elements, 32K+ rows, or expert weights of 256+ rows
+// 256, where the tensor pipe rather than shared memory bandwidth bounds a
+// prefill-size call.
+static int tile_n_for(int64_t n_rows_w, int64_t K, bool /*swiglu*/, int64_t E = 1) {
   const int64_t elems = n_rows_w * K;
   if (elems < (int64_t(1) << 21)) return 64;
+  if (E > 1 && n_rows_w >= 256) return 256;  // expert weights: a layer's experts together are large
   if (elems < (int64_t(1) << 24) && n_rows_w < 32768) return 128;
   return 256;
 }
@@ -638,7 +640,7 @@ static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
 static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   const bool swiglu = g.epilogue == BI_EPI_SWIGLU;
   const int64_t n_out = swiglu ? g.n_rows_w / 2 : g.n_rows_w;
-  int bn = tile_n_for(g.n_rows_w, g.K, swiglu), splits = 1;
+  int bn = tile_n_for(g.n_rows_w, g.K, swiglu, g.E), splits = 1;
   if (g.mode == BI_FAST && g.E == 1) {
     fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
     if (g.lse || g.rope) splits = 1;  // fused epilogues keep whole K per tile; FAST narrows the tiles instead

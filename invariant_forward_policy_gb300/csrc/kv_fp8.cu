@@ -101,22 +101,31 @@ __global__ void __launch_bounds__(256) kv_fp8_gather_kernel(const uint8_t* __res
     return;
   }
   const int64_t n = (int64_t)Hkv * 64 * hd;  // one page of one of K / V
-  for (int64_t e = (int64_t)threadIdx.x * 4; e < 2 * n; e += 4 * blockDim.x) {
+  // 16 codes (one 16-byte load, one row: hd is a multiple of 16) per thread and step
+  for (int64_t e = (int64_t)threadIdx.x * 16; e < 2 * n; e += 16 * blockDim.x) {
     const int which = e >= n;
     const int64_t off = which ? e - n : e;
     const int64_t slot = off / hd;  // (kv head, slot in page)
     const uint8_t* src = (which ? v8 : k8) + (int64_t)blk * n + off;
     const float sc = (which ? vs : ks)[(int64_t)blk * Hkv * 64 + slot];
-    const uint32_t codes = *reinterpret_cast<const uint32_t*>(src);
-    __nv_bfloat16 out[4];
+    const uint4 raw = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t packed[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((codes >> (8 * u)) & 0xffu), __NV_E4M3);
-      // code x power-of-two scale is exact, so the bf16 rounding is exact too
-      out[u] = __float2bfloat16_rn(__fmul_rn(__half2float(__half(hr)), sc));
+    for (int u = 0; u < 16; u += 2) {
+      float f[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t code = (w[(u + t) >> 2] >> (8 * ((u + t) & 3))) & 0xffu;
+        const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+        // code x power-of-two scale is exact, so the bf16 rounding is exact too
+        f[t] = __fmul_rn(__half2float(__half(hr)), sc);
+      }
+      packed[u / 2] = pack_bf16x2(f[0], f[1]);
     }
-    __nv_bfloat16* dst = (which ? vw : kw) + wpage * n + off;
-    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(out);
+    uint4* dst = reinterpret_cast<uint4*>((which ? vw : kw) + wpage * n + off);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
   }
 }
 
@@ -161,8 +170,8 @@ bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const flo
   BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
   BI_REQUIRE(Hkv > 0 && P <= 65535 && max_blocks_per_seq > 0 && max_blocks_per_seq <= 0x7fffffff && n_blocks > 0,
              "bad arguments");
-  BI_REQUIRE(aligned16(k_ws) && aligned16(v_ws) && ((uintptr_t)k_cache8 & 3) == 0 && ((uintptr_t)v_cache8 & 3) == 0,
-             "workspace pages must be 16-byte and cache pages 4-byte aligned");
+  BI_REQUIRE(aligned16(k_ws) && aligned16(v_ws) && aligned16(k_cache8) && aligned16(v_cache8),
+             "workspace and cache pages must be 16-byte aligned");
   return launched(launch_pdl(kv_fp8_gather_kernel, dim3((unsigned)max_blocks_per_seq, (unsigned)P), dim3(256), 0,
                              as_stream(stream), static_cast<const uint8_t*>(k_cache8),
                              static_cast<const uint8_t*>(v_cache8), k_scale, v_scale, n_blocks,
