@@ -382,7 +382,9 @@ size_t bi_moe_combine_workspace_size(int64_t T, int64_t d, int mode);
 /* Whole MoE FFN layer: route, permute (contiguous layout), gather, grouped
  * gate_up GEMM with SwiGLU, grouped down GEMM, slot-order combine.
  * x: bf16 [T, d]; router_logits fp32 [T, E]; w13 bf16 [E, 2F, d]; w2 bf16 [E, d, F];
- * out bf16 [T, d].  workspace: bi_moe_layer_workspace_size() bytes. */
+ * out bf16 [T, d].  workspace: bi_moe_layer_workspace_size() bytes.  Both
+ * modes run the same kernels (the slot-order combine measured faster than the
+ * fp32-atomic one on this GPU, so the non-invariant layer uses it too). */
 bi_status bi_moe_layer(const void* x, const float* router_logits, int64_t T, int64_t d, int E, int k, int64_t F,
                        const void* w13, const void* w2, void* out, int mode, void* workspace, size_t ws_bytes,
                        void* stream);

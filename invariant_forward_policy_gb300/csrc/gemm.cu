@@ -768,7 +768,7 @@ bi_status bi_grouped_gemm(const void* A, int64_t M_rows, int64_t K, const void* 
   BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(C), "pointers must be 16-byte aligned");
   BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
   const bool swiglu = epilogue == BI_EPI_SWIGLU;
-  const int bn = tile_n_for(N, K, swiglu);
+  const int bn = tile_n_for(N, K, swiglu, E);
   BI_REQUIRE_SHAPE(swiglu ? (N / 2) % (bn / 2) == 0 : N % bn == 0,
                    "grouped GEMM needs the per-expert N to be a multiple of the tile width");
   BI_REQUIRE_SHAPE(M_rows < (1ll << 31) && N * E < (1ll << 31), "shape too large");

@@ -391,7 +391,12 @@ bi_status bi_moe_layer(const void* x, const float* router_logits, int64_t T, int
   BI_TRY(bi_moe_gather(x, ros, T, k, d, xp, stream));
   BI_TRY(bi_grouped_gemm(xp, rows, d, w13, E, 2 * F, tiles, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, stream));
   BI_TRY(bi_grouped_gemm(act, rows, F, w2, E, d, tiles, y, BI_DTYPE_BF16, BI_EPI_NONE, stream));
-  return bi_moe_combine(y, ros, wts, T, k, d, out, mode, cws, bi_moe_combine_workspace_size(T, d, mode), stream);
+  // Both modes combine in slot order: on this GPU the fp32-atomic combine (a
+  // separate pass, or folded into the down projection's epilogue) measured
+  // slower than the slot-order sum, so the non-invariant layer takes it too.
+  (void)mode;
+  return bi_moe_combine(y, ros, wts, T, k, d, out, BI_INVARIANT, cws, bi_moe_combine_workspace_size(T, d, mode),
+                        stream);
 }
 
 }  // extern "C"
