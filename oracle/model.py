@@ -18,11 +18,21 @@ Layer (pre-norm):
 Final: x = rmsnorm(r, final_norm); logits = x Wlm^T (fp32).
 
 Weights are dicts of fp32 arrays holding bf16 values (see ``weights_to_f32``).
+
+Block-FP8 model ("vLLM Achieves Bitwise-Consistent RL Training ..." §4.1 W8A8
+linear layers, §4.2 FP8 KV cache), weights from ``fp8_weights``: the four
+linear layers of every block become W8A8 GEMMs (the bf16 input rows quantised
+in 1 x 128 blocks, the weights in 128 x 128 blocks, bf16 output), and K (after
+RoPE) and V make the FP8 round trip of the cache (one power-of-two scale per
+token and kv head) before attention reads them.  Everything else, the lm_head
+included, is the bf16 model unchanged (the lm_head staying bf16 is a reading:
+the pages name the dense GEMMs of the blocks).
 """
 from __future__ import annotations
 
 import numpy as np
 
+from . import fp8 as ofp8
 from . import ops
 from .bf16 import bf16_bits_to_f32, round_bf16
 
@@ -36,6 +46,39 @@ def weights_to_f32(w_bits: dict) -> dict:
     return out
 
 
+FP8_LINEARS = ("wqkv", "wo", "w13", "w2")
+
+
+def fp8_weights(w: dict) -> dict:
+    """The block-FP8 model made from bf16 masters by the deployment rule
+    ([Article] §4.1: training quantises its bf16 master weights to block FP8
+    before the same GEMM): a copy of ``w`` whose layers also carry the codes
+    and 128 x 128 block scales of the four linear weights under key "fp8"."""
+    out = dict(w)
+    out["layers"] = []
+    for lw in w["layers"]:
+        l8 = dict(lw)
+        l8["fp8"] = {k: ofp8.quantize_weight(lw[k]) for k in FP8_LINEARS}
+        out["layers"].append(l8)
+    return out
+
+
+def linear_fp8(x, qw, sw):
+    """W8A8 linear layer: bf16 rows x quantised in 1 x 128 blocks, times the
+    block-FP8 weight, rounded once to bf16 ([Article] §4.1)."""
+    qa, sa = ofp8.quantize_act(x)
+    return ofp8.gemm_fp8(qa, sa, qw, sw, out="bf16")
+
+
+def kv_round_trip(t):
+    """K or V [L, Hkv, hd] as attention reads them from the FP8 cache: each
+    (token, kv head) vector quantised with its own power-of-two scale, then
+    dequantised ([Article] §4.2)."""
+    n, h, hd = t.shape
+    q, s = ofp8.quantize_blocks(np.asarray(t, F32).reshape(n * h, hd), 1, block_cols=hd)
+    return ofp8.dequantize_blocks(q, s, 1, block_cols=hd).reshape(n, h, hd)
+
+
 def layer(lw: dict, shape, r, pos, return_parts: bool = False):
     """One decoder layer on the residual stream r [L, d] of ONE sequence whose
     rows sit at positions ``pos`` (0 .. L-1, every earlier key is in r).
@@ -44,19 +87,27 @@ def layer(lw: dict, shape, r, pos, return_parts: bool = False):
     output projection o and the FFN output dn that were added)."""
     L = r.shape[0]
     hq, hkv, hd, F = shape.n_heads_q, shape.n_heads_kv, shape.head_dim, shape.ffn
+    w8 = lw.get("fp8")
     x, _ = ops.rmsnorm(r, lw["attn_norm"], shape.eps)
-    qkv = ops.linear(x, lw["wqkv"])
+    qkv = linear_fp8(x, *w8["wqkv"]) if w8 else ops.linear(x, lw["wqkv"])
     q = qkv[:, : hq * hd].reshape(L, hq, hd)
     k = qkv[:, hq * hd: (hq + hkv) * hd].reshape(L, hkv, hd)
     v = qkv[:, (hq + hkv) * hd:].reshape(L, hkv, hd)
     q = ops.rope(q, pos, shape.rope_theta)
     k = ops.rope(k, pos, shape.rope_theta)
+    if w8:
+        k, v = kv_round_trip(k), kv_round_trip(v)
     a = ops.attention(q, k, v, pos).reshape(L, hq * hd)
-    o = ops.linear(a, lw["wo"])
+    o = linear_fp8(a, *w8["wo"]) if w8 else ops.linear(a, lw["wo"])
     x, r = ops.rmsnorm(o, lw["ffn_norm"], shape.eps, residual=r)
-    g = ops.linear(x, lw["w13"][:F])
-    u = ops.linear(x, lw["w13"][F:])
-    dn = ops.linear(ops.silu_mul(g, u), lw["w2"])
+    if w8:
+        g13 = linear_fp8(x, *w8["w13"])
+        g, u = g13[:, :F], g13[:, F:]
+        dn = linear_fp8(ops.silu_mul(g, u), *w8["w2"])
+    else:
+        g = ops.linear(x, lw["w13"][:F])
+        u = ops.linear(x, lw["w13"][F:])
+        dn = ops.linear(ops.silu_mul(g, u), lw["w2"])
     out = round_bf16(r + dn)
     return (out, o, dn) if return_parts else out
 
