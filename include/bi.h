@@ -401,6 +401,9 @@ typedef struct {
   int64_t kv_block;   /* tokens per cache block: must be 64 */
   int64_t kv_split;   /* attention KV split, multiple of 64 (512) */
   int64_t max_pos;    /* rows of the RoPE table = maximum context length */
+  int64_t fp8;        /* 0: bf16 linear layers and KV cache.  1: block-FP8 W8A8 linear layers (the
+                         attention, FFN and their activations; not the embedding or lm_head) and
+                         an FP8 KV cache, [Article] §4.1-4.2 (see bi_gemm_fp8, bi_kv_fp8_write) */
 } bi_model_config;
 
 typedef struct {
@@ -410,6 +413,13 @@ typedef struct {
   const void* ffn_norm;  /* bf16 [d] */
   const void* w13;       /* bf16 [2F, d]: gate rows, then up rows */
   const void* w2;        /* bf16 [d, F] */
+  /* fp8 = 1 only: e4m3 codes and 128 x 128 block scales of the same weights
+   * (bi_quantize_fp8 with block_rows = 128; the training side requantises its
+   * bf16 masters by this rule before each forward, or keeps the copy) */
+  const void* wqkv8; const float* wqkv_s;
+  const void* wo8;   const float* wo_s;
+  const void* w138;  const float* w13_s;
+  const void* w28;   const float* w2_s;
 } bi_layer_weights;
 
 typedef struct {

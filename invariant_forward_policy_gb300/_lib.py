@@ -44,11 +44,13 @@ class BiError(RuntimeError):
 class bi_model_config(ctypes.Structure):
     _fields_ = [("n_layers", _i64), ("d", _i64), ("n_heads_q", _i64), ("n_heads_kv", _i64), ("head_dim", _i64),
                 ("ffn", _i64), ("vocab", _i64), ("eps", _f32), ("rope_theta", _f32), ("kv_block", _i64),
-                ("kv_split", _i64), ("max_pos", _i64)]
+                ("kv_split", _i64), ("max_pos", _i64), ("fp8", _i64)]
 
 
 class bi_layer_weights(ctypes.Structure):
-    _fields_ = [("attn_norm", _vp), ("wqkv", _vp), ("wo", _vp), ("ffn_norm", _vp), ("w13", _vp), ("w2", _vp)]
+    _fields_ = [("attn_norm", _vp), ("wqkv", _vp), ("wo", _vp), ("ffn_norm", _vp), ("w13", _vp), ("w2", _vp),
+                ("wqkv8", _vp), ("wqkv_s", _vp), ("wo8", _vp), ("wo_s", _vp), ("w138", _vp), ("w13_s", _vp),
+                ("w28", _vp), ("w2_s", _vp)]
 
 
 class bi_weights(ctypes.Structure):

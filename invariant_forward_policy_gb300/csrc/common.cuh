@@ -80,6 +80,16 @@ size_t lm_head_partial_bytes(int64_t T, int64_t V, int64_t K, int mode);
 // QKV projection whose epilogue applies RoPE (q, k) and writes k, v into the
 // paged cache at each row's (row_seq, row_pos): the same values as bi_gemm
 // followed by bi_rope_kv_write, without the bf16 qkv round trip.
+bi_status kv_fp8_gather_to(const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,
+                           int64_t n_blocks, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int Hkv, int hd, const int32_t* block_table,
+                           int64_t max_blocks_per_seq, int64_t ws_blk, void* k_ws, void* v_ws, int32_t* ws_block_table,
+                           cudaStream_t st);
+bi_status rope_kv_write_fp8(const void* qkv, int64_t T, const int32_t* row_seq, const int32_t* row_pos, int Hq,
+                            int Hkv, int hd, const float* table, int64_t max_pos, const int32_t* block_table,
+                            int64_t max_blk, int64_t n_blocks, void* q_out, void* k8, float* ks, void* v8, float* vs,
+                            cudaStream_t st);
+bi_status swiglu_rows(const void* g13, int64_t T, int64_t F, void* act, cudaStream_t st);
 bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int64_t N, const int32_t* row_seq,
                         const int32_t* row_pos, const float* rope_table, int64_t max_pos, const int32_t* block_table,
                         int64_t max_blk, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int Hq, int Hkv,

@@ -83,17 +83,18 @@ __global__ void __launch_bounds__(256) kv_fp8_gather_kernel(const uint8_t* __res
                                                             const float* __restrict__ vs, int64_t n_blocks,
                                                             KvPieces pm, int Hkv, int hd,
                                                             const int32_t* __restrict__ block_table, int64_t max_blk,
-                                                            __nv_bfloat16* __restrict__ kw, __nv_bfloat16* __restrict__ vw,
-                                                            int32_t* __restrict__ wbt, int* status) {
+                                                            int64_t ws_blk, __nv_bfloat16* __restrict__ kw,
+                                                            __nv_bfloat16* __restrict__ vw, int32_t* __restrict__ wbt,
+                                                            int* status) {
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
   const int64_t l = blockIdx.x;
   const int n_tok = pm.row0[p + 1] - pm.row0[p];
   const int64_t ctx = (int64_t)pm.pos0[p] + n_tok;  // positions 0 .. ctx-1 are read
-  const int64_t wpage = (int64_t)p * max_blk + l;
-  const bool live = n_tok > 0 && l * 64 < ctx;
-  if (threadIdx.x == 0) wbt[(int64_t)p * max_blk + l] = live ? (int32_t)wpage : -1;
+  const int64_t wpage = (int64_t)p * ws_blk + l;
+  const bool live = n_tok > 0 && l * 64 < ctx && l < max_blk;
+  if (threadIdx.x == 0) wbt[(int64_t)p * ws_blk + l] = live ? (int32_t)wpage : -1;
   if (!live) return;
   const int32_t blk = block_table[(int64_t)pm.seq[p] * max_blk + l];
   if (blk < 0 || blk >= n_blocks) {
@@ -156,6 +157,28 @@ bi_status bi_kv_fp8_write(const void* k, const void* v, int64_t T, const int32_t
                   "bi_kv_fp8_write");
 }
 
+}  // extern "C"
+
+namespace bi {
+// Gather into workspace pages p * ws_blk + l (ws_blk >= the pages any piece needs).
+bi_status kv_fp8_gather_to(const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,
+                           int64_t n_blocks, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int Hkv, int hd, const int32_t* block_table,
+                           int64_t max_blocks_per_seq, int64_t ws_blk, void* k_ws, void* v_ws, int32_t* ws_block_table,
+                           cudaStream_t st) {
+  if (P == 0) return BI_OK;
+  BI_REQUIRE(P <= 65535 && ws_blk > 0 && ws_blk <= 0x7fffffff, "bad pieces / workspace pages");
+  return launched(launch_pdl(kv_fp8_gather_kernel, dim3((unsigned)ws_blk, (unsigned)P), dim3(256), 0, st,
+                             static_cast<const uint8_t*>(k_cache8), static_cast<const uint8_t*>(v_cache8), k_scale,
+                             v_scale, n_blocks, KvPieces{piece_seq, piece_row0, piece_pos0}, Hkv, hd, block_table,
+                             max_blocks_per_seq, ws_blk, static_cast<__nv_bfloat16*>(k_ws),
+                             static_cast<__nv_bfloat16*>(v_ws), ws_block_table, device_status_ptr()),
+                  "bi_kv_fp8_gather");
+}
+}  // namespace bi
+
+extern "C" {
+
 bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,
                            int64_t n_blocks, const int32_t* piece_seq, const int32_t* piece_row0,
                            const int32_t* piece_pos0, int64_t P, int Hkv, int hd, const int32_t* block_table,
@@ -172,13 +195,9 @@ bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const flo
              "bad arguments");
   BI_REQUIRE(aligned16(k_ws) && aligned16(v_ws) && aligned16(k_cache8) && aligned16(v_cache8),
              "workspace and cache pages must be 16-byte aligned");
-  return launched(launch_pdl(kv_fp8_gather_kernel, dim3((unsigned)max_blocks_per_seq, (unsigned)P), dim3(256), 0,
-                             as_stream(stream), static_cast<const uint8_t*>(k_cache8),
-                             static_cast<const uint8_t*>(v_cache8), k_scale, v_scale, n_blocks,
-                             KvPieces{piece_seq, piece_row0, piece_pos0}, Hkv, hd, block_table, max_blocks_per_seq,
-                             static_cast<__nv_bfloat16*>(k_ws), static_cast<__nv_bfloat16*>(v_ws), ws_block_table,
-                             device_status_ptr()),
-                  "bi_kv_fp8_gather");
+  return kv_fp8_gather_to(k_cache8, v_cache8, k_scale, v_scale, n_blocks, piece_seq, piece_row0, piece_pos0, P, Hkv,
+                          hd, block_table, max_blocks_per_seq, max_blocks_per_seq, k_ws, v_ws, ws_block_table,
+                          as_stream(stream));
 }
 
 }  // extern "C"

@@ -48,6 +48,7 @@ struct DevMeta {
   int32_t* logit_tgt;  // target id of each logit row (or -1)
   int32_t* row_seq;    // sequence of every pass row
   int32_t* row_pos;    // absolute position of every pass row
+  int32_t* piece_ident;  // 0 .. pieces-1 (FP8 KV: row p of the gathered page table)
 };
 
 __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ tokens,
@@ -59,6 +60,7 @@ __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ 
       dm.piece_seq[p] = pm.seq[p];
       dm.piece_row0[p] = pm.row0[p];
       dm.piece_pos0[p] = pm.pos0[p];
+      dm.piece_ident[p] = p;
     }
     if (threadIdx.x == 0) dm.piece_row0[pm.n_pieces] = pm.row0[pm.n_pieces];
   }
@@ -95,6 +97,7 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
   if (threadIdx.x == 0) {
     if (b == 0) dm.piece_row0[B] = B;
     dm.piece_seq[b] = b;
+    dm.piece_ident[b] = b;
     dm.piece_row0[b] = b;
     dm.piece_pos0[b] = pos[b];
     dm.ids[b] = id;
@@ -113,9 +116,12 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
 
 // ------------------------------------------------------------- workspace plan
 struct FwdLayout {
-  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos;
+  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos, piece_ident;
   size_t h, x, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
   size_t attn_ws_bytes, gemm_ws_bytes, lp_ws_bytes;
+  // fp8 only: bf16 qkv and gate/up outputs, activation codes and scales, the gathered bf16 pages
+  size_t qkv, g13, qa, sa, kw, vw, wbt;
+  int64_t ws_blk;  // gathered pages per piece
   size_t total;
 };
 
@@ -138,6 +144,7 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   L.logit_tgt = take(std::max(Tm, Rm) * 4);
   L.row_seq = take(Tm * 4);
   L.row_pos = take(Tm * 4);
+  L.piece_ident = take(Pm * 4);
   L.h = take(Tm * c.d * 2);
   L.x = take(Tm * c.d * 2);
 
@@ -163,6 +170,18 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   }
   L.gemm_ws_bytes = g;
   L.gemm_ws = take(g);
+  if (c.fp8) {
+    const int64_t kmax = std::max(std::max(c.d, hq), c.ffn);
+    L.qkv = take(Tm * nqkv * 2);
+    L.g13 = take(Tm * 2 * c.ffn * 2);
+    L.qa = take(Tm * kmax);
+    L.sa = take(Tm * (kmax / 128) * 4);
+    L.ws_blk = cdiv(max_ctx, 64);
+    const size_t pages = (size_t)Pm * L.ws_blk;
+    L.kw = take(pages * c.n_heads_kv * 64 * c.head_dim * 2);
+    L.vw = take(pages * c.n_heads_kv * 64 * c.head_dim * 2);
+    L.wbt = take(pages * 4);
+  }
   L.total = off + 256;
   return L;
 }
@@ -199,7 +218,10 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
   void* tmp = at<void>(ws, L.tmp);
   void* act = at<void>(ws, L.act);
   void* gws = L.gemm_ws_bytes ? at<void>(ws, L.gemm_ws) : nullptr;
-  const size_t layer_cache = (size_t)n_blocks * Hkv * 64 * hd * 2;
+  // bf16: [n_blocks, Hkv, 64, hd] per layer; fp8: codes [n_blocks, Hkv, 64, hd] then fp32 scales [n_blocks, Hkv, 64]
+  const size_t layer_cache = (size_t)n_blocks * Hkv * 64 * (c.fp8 ? hd + 4 : hd * 2);
+  const size_t layer_codes = (size_t)n_blocks * Hkv * 64 * hd;
+  const cudaStream_t cst = as_stream(stream);
 
   const bool dumping = m->dump && T <= m->dump_rows;
   const size_t slot_bytes = (size_t)m->dump_rows * c.d * 2;
@@ -217,6 +239,39 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     const bi_layer_weights& lw = m->layers[li];
     void* kc = static_cast<uint8_t*>(k_cache) + li * layer_cache;
     void* vc = static_cast<uint8_t*>(v_cache) + li * layer_cache;
+    if (c.fp8) {
+      // block-FP8 W8A8 layer; K and V make the FP8 round trip through the one gather path
+      auto* qa = at<uint8_t>(ws, L.qa);
+      auto* sa = at<float>(ws, L.sa);
+      void* qkv = at<void>(ws, L.qkv);
+      float* ks = reinterpret_cast<float*>(static_cast<uint8_t*>(kc) + layer_codes);
+      float* vs = reinterpret_cast<float*>(static_cast<uint8_t*>(vc) + layer_codes);
+      BI_TRY(bi_quantize_fp8(x, T, c.d, 1, qa, sa, stream));
+      BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.wqkv8, lw.wqkv_s, nqkv, qkv, BI_DTYPE_BF16, mode, stream));
+      BI_TRY(rope_kv_write_fp8(qkv, T, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos), Hq, Hkv, hd,
+                               m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, ks, vc, vs, cst));
+      BI_TRY(kv_fp8_gather_to(kc, vc, ks, vs, n_blocks, piece_seq, piece_row0, piece_pos0, ps.pieces, Hkv, hd,
+                              block_table, max_blk, L.ws_blk, at<void>(ws, L.kw), at<void>(ws, L.vw),
+                              at<int32_t>(ws, L.wbt), cst));
+      BI_TRY(bi_attention(q, T, at<int32_t>(ws, L.piece_ident), piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq,
+                          Hkv, hd, at<void>(ws, L.kw), at<void>(ws, L.vw), at<int32_t>(ws, L.wbt), L.ws_blk,
+                          ps.pieces * L.ws_blk, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
+                          L.attn_ws_bytes, ao, mode, stream));
+      BI_TRY(bi_quantize_fp8(ao, T, hq, 1, qa, sa, stream));
+      BI_TRY(bi_gemm_fp8(qa, sa, T, hq, lw.wo8, lw.wo_s, c.d, tmp, BI_DTYPE_BF16, mode, stream));
+      BI_TRY(bi_rmsnorm(tmp, h, lw.ffn_norm, x, T, c.d, c.eps, mode, stream));
+      BI_TRY(bi_quantize_fp8(x, T, c.d, 1, qa, sa, stream));
+      BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.w138, lw.w13_s, 2 * c.ffn, at<void>(ws, L.g13), BI_DTYPE_BF16, mode,
+                         stream));
+      BI_TRY(swiglu_rows(at<void>(ws, L.g13), T, c.ffn, act, cst));
+      BI_TRY(bi_quantize_fp8(act, T, c.ffn, 1, qa, sa, stream));
+      BI_TRY(bi_gemm_fp8(qa, sa, T, c.ffn, lw.w28, lw.w2_s, c.d, tmp, BI_DTYPE_BF16, mode, stream));
+      if (li + 1 < c.n_layers) {
+        BI_TRY(bi_rmsnorm(tmp, h, m->layers[li + 1].attn_norm, x, T, c.d, c.eps, mode, stream));
+        BI_TRY(dump_copy(li + 1, h));
+      }
+      continue;
+    }
     // QKV projection with RoPE and the paged K/V write fused into its epilogue
     BI_TRY(gemm_qkv_rope(x, T, c.d, lw.wqkv, nqkv, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos),
                          m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd, mode,
@@ -271,6 +326,11 @@ static bi_status validate_cfg(const bi_model_config* c) {
   BI_REQUIRE_SHAPE(c->vocab % 8 == 0, "vocab must be a multiple of 8");
   BI_REQUIRE_SHAPE(64 % (c->n_heads_q / c->n_heads_kv) == 0, "Hq/Hkv must divide 64");
   BI_REQUIRE(c->eps > 0.f, "eps must be positive");
+  BI_REQUIRE(c->fp8 == 0 || c->fp8 == 1, "fp8 must be 0 or 1");
+  if (c->fp8)
+    BI_REQUIRE_SHAPE(c->d % 128 == 0 && c->ffn % 128 == 0 && (c->n_heads_q * c->head_dim) % 128 == 0 &&
+                         ((c->n_heads_q + 2 * c->n_heads_kv) * c->head_dim) % 128 == 0,
+                     "fp8 needs d, ffn, Hq*hd and (Hq + 2 Hkv)*hd multiples of 128");
   return BI_OK;
 }
 
@@ -285,6 +345,9 @@ bi_status bi_model_create(const bi_model_config* cfg, const bi_weights* w, void*
   for (int64_t i = 0; i < cfg->n_layers; ++i) {
     const bi_layer_weights& l = w->layers[i];
     BI_REQUIRE(l.attn_norm && l.wqkv && l.wo && l.ffn_norm && l.w13 && l.w2, "null layer weight");
+    if (cfg->fp8)
+      BI_REQUIRE(l.wqkv8 && l.wqkv_s && l.wo8 && l.wo_s && l.w138 && l.w13_s && l.w28 && l.w2_s,
+                 "fp8 model: null FP8 layer weight");
   }
   BI_TRY(bi_rope_table(w->rope_table, cfg->max_pos, (int)cfg->head_dim, (double)cfg->rope_theta, stream));
   bi_model* m = new bi_model;
@@ -310,7 +373,8 @@ bi_status bi_model_set_dump(bi_model* m, void* dump, int64_t max_rows) {
 
 size_t bi_kv_cache_bytes(const bi_model_config* cfg, int64_t n_blocks) {
   if (!cfg || n_blocks <= 0) return 0;
-  return (size_t)cfg->n_layers * n_blocks * cfg->n_heads_kv * 64 * cfg->head_dim * 2;
+  const int64_t per_slot = cfg->fp8 ? cfg->head_dim + 4 : cfg->head_dim * 2;  // fp8: codes + one fp32 scale
+  return (size_t)cfg->n_layers * n_blocks * cfg->n_heads_kv * 64 * per_slot;
 }
 
 size_t bi_forward_workspace_size(const bi_model_config* cfg, int64_t max_tokens, int64_t max_pieces, int64_t max_ctx,
@@ -402,7 +466,7 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
                at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids),
                at<int32_t>(workspace, L.logit_src), at<int32_t>(workspace, L.logit_dst),
                at<int32_t>(workspace, L.logit_tgt), at<int32_t>(workspace, L.row_seq),
-               at<int32_t>(workspace, L.row_pos)};
+               at<int32_t>(workspace, L.row_pos), at<int32_t>(workspace, L.piece_ident)};
     BI_TRY(launched(launch_pdl(pass_meta_kernel, dim3((unsigned)cdiv(std::max<int64_t>(rows, 1), 256)), dim3(256), 0,
                                st, pm, tokens, target_ids, dm),
                     "pass_meta_kernel"));
@@ -431,7 +495,8 @@ bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* p
   DevMeta dm{at<int32_t>(workspace, L.piece_seq), at<int32_t>(workspace, L.piece_row0),
              at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids), at<int32_t>(workspace, L.logit_src),
              at<int32_t>(workspace, L.logit_dst), at<int32_t>(workspace, L.logit_tgt),
-             at<int32_t>(workspace, L.row_seq), at<int32_t>(workspace, L.row_pos)};
+             at<int32_t>(workspace, L.row_seq), at<int32_t>(workspace, L.row_pos),
+             at<int32_t>(workspace, L.piece_ident)};
   const cudaStream_t st = as_stream(stream);
   BI_TRY(launched(launch_pdl(decode_embed_kernel, dim3((unsigned)B), dim3(128), 0, st, tokens, pos, (int)B, dm,
                              static_cast<const __nv_bfloat16*>(m->embed), m->cfg.vocab, m->cfg.d,

@@ -37,27 +37,53 @@ class KVCache:
 class Decoder:
     """A decoder whose weights live in caller-owned (torch) device memory."""
 
-    def __init__(self, shape, weight_bits: dict, max_pos: int, device="cuda"):
+    def __init__(self, shape, weight_bits: dict, max_pos: int, device="cuda", fp8: bool = False):
+        """fp8: block-FP8 W8A8 linear layers and an FP8 KV cache.  The FP8 copies
+        of the four linear weights of every layer are made here from the bf16
+        masters by the deployment rule (bi_quantize_fp8, 128 x 128 blocks) and
+        kept; a trainer that updates the masters re-runs `requantize()`."""
         self.shape = shape
         self.device = torch.device(device)
+        self.fp8 = bool(fp8)
         s = shape
         self.cfg = L.bi_model_config(n_layers=s.n_layers, d=s.d, n_heads_q=s.n_heads_q, n_heads_kv=s.n_heads_kv,
                                      head_dim=s.head_dim, ffn=s.ffn, vocab=s.vocab, eps=s.eps,
-                                     rope_theta=s.rope_theta, kv_block=64, kv_split=s.kv_split, max_pos=max_pos)
+                                     rope_theta=s.rope_theta, kv_block=64, kv_split=s.kv_split, max_pos=max_pos,
+                                     fp8=1 if fp8 else 0)
         dev = self.device
         self.w = {k: _bf16_tensor(weight_bits[k], dev) for k in ("embed", "final_norm", "lm_head")}
         self.layers = [{k: _bf16_tensor(v, dev) for k, v in lw.items()} for lw in weight_bits["layers"]]
         self.rope_table = torch.empty((max_pos, s.head_dim), dtype=torch.float32, device=dev)
+        if self.fp8:
+            for lw in self.layers:
+                for k in ("wqkv", "wo", "w13", "w2"):
+                    N, K = lw[k].shape
+                    lw[k + "8"] = torch.empty((N, K), dtype=torch.uint8, device=dev)
+                    lw[k + "_s"] = torch.empty((-(-N // 128), K // 128), dtype=torch.float32, device=dev)
+            self.requantize()
+
+        def ptr(lw, k):
+            return lw[k].data_ptr() if k in lw else None
+
         lw_arr = (L.bi_layer_weights * s.n_layers)()
         for i, lw in enumerate(self.layers):
             lw_arr[i] = L.bi_layer_weights(lw["attn_norm"].data_ptr(), lw["wqkv"].data_ptr(), lw["wo"].data_ptr(),
-                                           lw["ffn_norm"].data_ptr(), lw["w13"].data_ptr(), lw["w2"].data_ptr())
+                                           lw["ffn_norm"].data_ptr(), lw["w13"].data_ptr(), lw["w2"].data_ptr(),
+                                           ptr(lw, "wqkv8"), ptr(lw, "wqkv_s"), ptr(lw, "wo8"), ptr(lw, "wo_s"),
+                                           ptr(lw, "w138"), ptr(lw, "w13_s"), ptr(lw, "w28"), ptr(lw, "w2_s"))
         self._lw_arr = lw_arr
         self._weights = L.bi_weights(self.w["embed"].data_ptr(), self.w["final_norm"].data_ptr(),
                                      self.w["lm_head"].data_ptr(), ctypes.cast(lw_arr, ctypes.POINTER(L.bi_layer_weights)),
                                      self.rope_table.data_ptr())
         self.handle = L.bi_model_create(self.cfg, self._weights)
         self.max_pos = max_pos
+
+    def requantize(self):
+        """FP8 copies of the linear weights from the bf16 masters (128 x 128 blocks)."""
+        for lw in self.layers:
+            for k in ("wqkv", "wo", "w13", "w2"):
+                N, K = lw[k].shape
+                L.bi_quantize_fp8(lw[k], N, K, 128, lw[k + "8"], lw[k + "_s"])
 
     def close(self):
         if getattr(self, "handle", None):
@@ -73,6 +99,11 @@ class Decoder:
     # ------------------------------------------------------------ memory
     def alloc_cache(self, n_blocks: int) -> KVCache:
         s = self.shape
+        if self.fp8:
+            # per layer: e4m3 codes [n_blocks, Hkv, 64, hd], then fp32 scales [n_blocks, Hkv, 64]
+            per_layer = L.bi_kv_cache_bytes(self.cfg, n_blocks) // s.n_layers
+            return KVCache(torch.zeros((s.n_layers, per_layer), dtype=torch.uint8, device=self.device),
+                           torch.zeros((s.n_layers, per_layer), dtype=torch.uint8, device=self.device), n_blocks)
         shape = (s.n_layers, n_blocks, s.n_heads_kv, 64, s.head_dim)
         return KVCache(torch.zeros(shape, dtype=torch.bfloat16, device=self.device),
                        torch.zeros(shape, dtype=torch.bfloat16, device=self.device), n_blocks)

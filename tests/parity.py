@@ -24,6 +24,14 @@ from tests.gpu_util import bf16_close, host_f32
 E2E_MAX, E2E_MEAN = 2e-2, 5e-3            # dense decoder workload
 E2E_MAX_SMALL, E2E_MEAN_SMALL = 3e-2, 1e-2  # small 2-layer test models
 E2E_MAX_LONG, E2E_MEAN_LONG = 8e-2, 2.5e-2  # 8-layer d-2048 long-context decoder
+# Block-FP8 model: a one-ulp bf16 flip of a GEMM input moves its e4m3 code by a
+# whole e4m3 step (2^-3 relative) about one time in sixteen, so the same
+# measurement (the FP8 oracle against itself with P rounded to bf16, small
+# 2-layer model d 256) gives a free-running floor of max 1.8e-1, mean 4.4e-2, and
+# a layer-anchored floor of 0.15 of (|update| + row rms) per element, 0.015 on
+# average; the bounds are about twice and three times those.
+E2E_MAX_FP8, E2E_MEAN_FP8 = 0.4, 0.1
+FP8_LAYER_MAX, FP8_LAYER_MEAN = 0.5, 0.05
 
 
 def e2e_close(got, want, max_tol=E2E_MAX, mean_tol=E2E_MEAN):
@@ -32,12 +40,15 @@ def e2e_close(got, want, max_tol=E2E_MAX, mean_tol=E2E_MEAN):
     return err
 
 
-def anchored_parity(dec, wb, shape, seqs, seed=0):
+def anchored_parity(dec, wb, shape, seqs, seed=0, fp8=False):
     """Prefill `seqs` in one pass with the layer dump on, then check each layer
     against the oracle applied to the GPU's own layer input, the final norm, and
     the logprobs against the oracle's lm_head + log-softmax of the GPU's
-    final-norm rows.  Returns the worst errors seen."""
+    final-norm rows.  fp8: the block-FP8 model's oracle and bounds.  Returns the
+    worst errors seen."""
     W = omodel.weights_to_f32(wb)
+    if fp8:
+        W = omodel.fp8_weights(W)
     T = sum(len(s) for s in seqs)
     L_ = shape.n_layers
     mb = max(-(-len(s) // 64) for s in seqs)
@@ -72,7 +83,13 @@ def anchored_parity(dec, wb, shape, seqs, seed=0):
             upd = np.abs(o) + np.abs(dn)
             rms = np.sqrt(np.mean(o.astype(np.float64) ** 2, -1, keepdims=True)) + \
                 np.sqrt(np.mean(dn.astype(np.float64) ** 2, -1, keepdims=True))
-            bf16_close(got, want, ulps=2, frac_exact=0.25, atol=2.0 ** -5 * (upd + rms) + 1e-6)
+            if fp8:
+                scale = upd + rms + 1e-6
+                ratio = np.abs(got - want) / scale
+                assert ratio.max() <= FP8_LAYER_MAX, (l, ratio.max())
+                assert np.abs(got - want).mean() / scale.mean() <= FP8_LAYER_MEAN, l
+            else:
+                bf16_close(got, want, ulps=2, frac_exact=0.25, atol=2.0 ** -5 * (upd + rms) + 1e-6)
             worst["layer_max_rel_update"] = max(worst["layer_max_rel_update"],
                                                 float(np.max(np.abs(got - want) / (upd + 1e-3))))
             worst["layer_frac_exact_min"] = min(worst["layer_frac_exact_min"], float(np.mean(got == want)))
