@@ -689,6 +689,47 @@ def config_table(args):
     dec.close()
     del cache
     torch.cuda.empty_cache()
+
+    # block-FP8 dense decoder: the default workload's whole episode (prefill, 255
+    # graph-replayed decode steps, recompute) with W8A8 linear layers and the FP8
+    # KV cache; the bf16 model's episode is timed alongside for the ratio
+    from invariant_forward_policy_gb300.decoder import Episode
+    from synthetic import C2, make_prompts
+    shape2 = C2["shape"]
+    wb2 = make_decoder_weights(shape2, seed=C2["seed"], w_std=C2["w_std"])
+    prompts2 = make_prompts(C2["batch"], C2["prompt_min"], C2["prompt_max"], shape2.vocab, C2["seed"])
+    lens2 = [len(p) for p in prompts2]
+    pd2 = torch.from_numpy(np.concatenate(prompts2).astype(np.int32)).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    dec8 = Decoder(shape2, wb2, max_pos=1024, fp8=True)
+    dec16 = Decoder(shape2, wb2, max_pos=1024)
+    eps = {"invariant": Episode(dec8, lens2, C2["gen"], mode=bi.BI_INVARIANT),
+           "non_invariant": Episode(dec8, lens2, C2["gen"], mode=bi.BI_FAST),
+           "bf16_model": Episode(dec16, lens2, C2["gen"], mode=bi.BI_INVARIANT)}
+    for e in eps.values():
+        for _ in range(2):
+            e.run(pd2)
+    ts = {tag: [] for tag in eps}
+    diff0 = True
+    for _ in range(3):
+        for tag, e in eps.items():
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            _, lr, lt = e.run(pd2)
+            e1.record()
+            torch.cuda.synchronize()
+            ts[tag].append(e0.elapsed_time(e1) * 1000.0)
+            if tag == "invariant":
+                diff0 = diff0 and bool(torch.equal(lr.view(torch.int32), lt.view(torch.int32)))
+    t = {tag: float(np.median(v)) for tag, v in ts.items()}
+    toks = C2["batch"] * C2["gen"]
+    row("fp8_dense_decoder_episode_16x256", toks, "tokens/s", t,
+        {"bound": "latency", "bf16_model_tokens_per_s": round(toks / (t["bf16_model"] * 1e-6), 1),
+         "fp8_over_bf16": round(t["bf16_model"] / t["invariant"], 3), "rollout_equals_recompute": diff0,
+         "note": "W8A8 block-FP8 linear layers + FP8 KV cache (codes + per-(token, head) scales); L2 flushed"})
+    del eps, dec8, dec16, flush
+    torch.cuda.empty_cache()
     return out
 
 

@@ -230,6 +230,21 @@ bi_status bi_quantize_fp8(const void* x, int64_t R, int64_t C, int block_rows, v
  * (BI_FAST runs the same kernel). */
 bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, const void* Wq, const float* sw,
                       int64_t N, void* C, int c_dtype, int mode, void* stream);
+/* bi_rmsnorm_fp8: bi_rmsnorm (no mode argument: one schedule) whose bf16 output
+ * rows are also quantised as bi_quantize_fp8 with block_rows = 1 would: codes
+ * q uint8 [rows, d], scales q_scale fp32 [rows, d/128].  y (bf16 [rows, d]) may
+ * be NULL; residual as in bi_rmsnorm.  d % 128 == 0, 128 <= d <= 16384; x, gamma,
+ * y, residual 16-byte and q 8-byte aligned.  The codes and scales are bit-equal
+ * to bi_rmsnorm followed by bi_quantize_fp8 (one kernel instead of two).
+ *
+ * bi_swiglu_fp8 (the SiLU-mul-quant step, [Article] §4.4): g13 bf16 [T, 2F] holds
+ * a gate/up GEMM's output (gate columns 0..F-1, up columns F..2F-1);
+ * a = bf16(silu(g) u) in fp32, rounded once, silu(g) = g / (1 + exp(-g)), then a's
+ * 1 x 128 blocks to codes q uint8 [T, F] and scales q_scale fp32 [T, F/128], as
+ * bi_quantize_fp8 would.  F % 128 == 0; g13 16-byte and q 4-byte aligned. */
+bi_status bi_rmsnorm_fp8(const void* x, void* residual, const void* gamma, void* y, void* q, float* q_scale,
+                         int64_t rows, int64_t d, float eps, void* stream);
+bi_status bi_swiglu_fp8(const void* g13, int64_t T, int64_t F, void* q, float* q_scale, void* stream);
 
 /* ---------------------------------------------------------- FP8 KV cache
  * [Article] §4.2 ("FP8 KV cache: keep FP8 storage, unify the read path"): K

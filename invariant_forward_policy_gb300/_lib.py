@@ -88,6 +88,8 @@ _SIGS = {
     "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _int, _vp,
                                  _i64, _vp, _int, _vp]),
     "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
+    "bi_rmsnorm_fp8": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _vp]),
+    "bi_swiglu_fp8": (_int, [_vp, _i64, _i64, _vp, _vp, _vp]),
     "bi_embed": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp]),
     "bi_logprob_gather": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _int, _vp, _sz, _vp]),
     "bi_logprob_workspace_size": (_sz, [_i64, _i64, _int]),
@@ -276,6 +278,15 @@ def bi_quantize_fp8(x, R, C, block_rows, q, scales, stream=None):
 
 def bi_gemm_fp8(Aq, sa, M, K, Wq, sw, N, C, c_dtype=BI_DTYPE_BF16, mode=BI_INVARIANT, stream=None):
     _check(load().bi_gemm_fp8(_p(Aq), _p(sa), M, K, _p(Wq), _p(sw), N, _p(C), c_dtype, mode, _s(stream)))
+
+
+def bi_rmsnorm_fp8(x, residual, gamma, y, q, q_scale, rows, d, eps=1e-6, stream=None):
+    _check(load().bi_rmsnorm_fp8(_p(x), _p(residual), _p(gamma), _p(y), _p(q), _p(q_scale), rows, d, eps,
+                                 _s(stream)))
+
+
+def bi_swiglu_fp8(g13, T, F, q, q_scale, stream=None):
+    _check(load().bi_swiglu_fp8(_p(g13), T, F, _p(q), _p(q_scale), _s(stream)))
 
 
 def bi_topk(scores, T, ld, n_valid, K, idx_out, mode=BI_INVARIANT, stream=None):

@@ -89,7 +89,9 @@ bi_status rope_kv_write_fp8(const void* qkv, int64_t T, const int32_t* row_seq, 
                             int Hkv, int hd, const float* table, int64_t max_pos, const int32_t* block_table,
                             int64_t max_blk, int64_t n_blocks, void* q_out, void* k8, float* ks, void* v8, float* vs,
                             cudaStream_t st);
-bi_status swiglu_rows(const void* g13, int64_t T, int64_t F, void* act, cudaStream_t st);
+bi_status swiglu_fp8(const void* g13, int64_t T, int64_t F, void* q, float* qs, cudaStream_t st);
+bi_status rmsnorm_fp8_rows(const void* x, void* residual, const void* gamma, void* y, void* q, float* qs,
+                           int64_t rows, int64_t d, float eps, void* stream);
 bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int64_t N, const int32_t* row_seq,
                         const int32_t* row_pos, const float* rope_table, int64_t max_pos, const int32_t* block_table,
                         int64_t max_blk, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int Hq, int Hkv,

@@ -25,6 +25,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace bi {
 
@@ -35,13 +36,6 @@ constexpr int kF8TileBytes = 128 * kF8Block;       // A: 128 rows x 128 fp8
 constexpr int kF8BTileBytes = kF8BN * kF8Block;    // W: 256 rows x 128 fp8
 constexpr int kF8Threads = 320;                    // TMA, MMA, 8 promotion warps
 constexpr int kF8SmemBytes = 1024 + kF8Stages * (kF8TileBytes + kF8BTileBytes) + 256;
-
-// Smallest power of two s with 448 s >= amax (1 for amax = 0), exactly.
-__device__ __forceinline__ int fp8_scale_exp(float amax) {
-  if (!(amax > 0.f)) return 0;
-  const int e = ilogbf(amax);  // amax in [2^e, 2^(e+1))
-  return amax <= ldexpf(1.75f, e) ? e - 8 : e - 7;
-}
 
 // Activations (1 x 128 blocks): one warp per block, 4 consecutive elements per
 // lane, amax by warp shuffles; 8 blocks per CTA.
@@ -66,7 +60,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_rows_kernel(const __nv_bfloa
   uint32_t packed = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    packed |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[i], -e), __NV_SATFINITE, __NV_E4M3) << (8 * i);
+    packed |= fp8_code(v[i], e) << (8 * i);
   *reinterpret_cast<uint32_t*>(q + r * C + c0) = packed;
 }
 
@@ -103,7 +97,7 @@ __global__ void __launch_bounds__(256) quantize_fp8_blocks_kernel(const __nv_bfl
     uint32_t packed = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      packed |= (uint32_t)__nv_cvt_float_to_fp8(ldexpf(v[k], -e), __NV_SATFINITE, __NV_E4M3) << (8 * k);
+      packed |= fp8_code(v[k], e) << (8 * k);
     *reinterpret_cast<uint32_t*>(q + (r0 + i) * C + c0) = packed;
   }
 }

@@ -18,14 +18,9 @@
 #include <string>
 
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace bi {
-
-__device__ __forceinline__ int kv_scale_exp(float amax) {
-  if (!(amax > 0.f)) return 0;
-  const int e = ilogbf(amax);
-  return amax <= ldexpf(1.75f, e) ? e - 8 : e - 7;
-}
 
 struct KvPieces {
   const int32_t* seq;
@@ -66,11 +61,11 @@ __global__ void __launch_bounds__(256) kv_fp8_write_kernel(const __nv_bfloat16* 
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  const int e = kv_scale_exp(m);
+  const int e = fp8_scale_exp(m);
   const int64_t slot = ((int64_t)blk * Hkv + kh) * 64 + pos % 64;
   uint8_t* dst = (which ? v8 : k8) + slot * hd;
   for (int u = 0; u < per; ++u)
-    dst[lane * per + u] = (uint8_t)__nv_cvt_float_to_fp8(ldexpf(x[u], -e), __NV_SATFINITE, __NV_E4M3);
+    dst[lane * per + u] = (uint8_t)fp8_code(x[u], e);
   if (lane == 0) (which ? vs : ks)[slot] = ldexpf(1.f, e);
 }
 

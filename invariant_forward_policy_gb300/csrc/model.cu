@@ -234,19 +234,24 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
 
   if (!ps.embedded) BI_TRY(bi_embed(at<int32_t>(ws, L.ids), T, m->embed, c.vocab, c.d, h, stream));
   BI_TRY(dump_copy(0, h));
-  BI_TRY(bi_rmsnorm(h, nullptr, m->layers[0].attn_norm, x, T, c.d, c.eps, mode, stream));
+  if (c.fp8)
+    BI_TRY(rmsnorm_fp8_rows(h, nullptr, m->layers[0].attn_norm, nullptr, at<uint8_t>(ws, L.qa), at<float>(ws, L.sa),
+                            T, c.d, c.eps, stream));
+  else
+    BI_TRY(bi_rmsnorm(h, nullptr, m->layers[0].attn_norm, x, T, c.d, c.eps, mode, stream));
   for (int64_t li = 0; li < c.n_layers; ++li) {
     const bi_layer_weights& lw = m->layers[li];
     void* kc = static_cast<uint8_t*>(k_cache) + li * layer_cache;
     void* vc = static_cast<uint8_t*>(v_cache) + li * layer_cache;
     if (c.fp8) {
-      // block-FP8 W8A8 layer; K and V make the FP8 round trip through the one gather path
+      // block-FP8 W8A8 layer; K and V make the FP8 round trip through the one gather path.
+      // qa/sa hold the quantised input rows of the next GEMM (written by the
+      // preceding norm, or by the quantiser / SwiGLU in front of it).
       auto* qa = at<uint8_t>(ws, L.qa);
       auto* sa = at<float>(ws, L.sa);
       void* qkv = at<void>(ws, L.qkv);
       float* ks = reinterpret_cast<float*>(static_cast<uint8_t*>(kc) + layer_codes);
       float* vs = reinterpret_cast<float*>(static_cast<uint8_t*>(vc) + layer_codes);
-      BI_TRY(bi_quantize_fp8(x, T, c.d, 1, qa, sa, stream));
       BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.wqkv8, lw.wqkv_s, nqkv, qkv, BI_DTYPE_BF16, mode, stream));
       BI_TRY(rope_kv_write_fp8(qkv, T, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos), Hq, Hkv, hd,
                                m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, ks, vc, vs, cst));
@@ -259,15 +264,13 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
                           L.attn_ws_bytes, ao, mode, stream));
       BI_TRY(bi_quantize_fp8(ao, T, hq, 1, qa, sa, stream));
       BI_TRY(bi_gemm_fp8(qa, sa, T, hq, lw.wo8, lw.wo_s, c.d, tmp, BI_DTYPE_BF16, mode, stream));
-      BI_TRY(bi_rmsnorm(tmp, h, lw.ffn_norm, x, T, c.d, c.eps, mode, stream));
-      BI_TRY(bi_quantize_fp8(x, T, c.d, 1, qa, sa, stream));
+      BI_TRY(rmsnorm_fp8_rows(tmp, h, lw.ffn_norm, nullptr, qa, sa, T, c.d, c.eps, stream));
       BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.w138, lw.w13_s, 2 * c.ffn, at<void>(ws, L.g13), BI_DTYPE_BF16, mode,
                          stream));
-      BI_TRY(swiglu_rows(at<void>(ws, L.g13), T, c.ffn, act, cst));
-      BI_TRY(bi_quantize_fp8(act, T, c.ffn, 1, qa, sa, stream));
+      BI_TRY(swiglu_fp8(at<void>(ws, L.g13), T, c.ffn, qa, sa, cst));
       BI_TRY(bi_gemm_fp8(qa, sa, T, c.ffn, lw.w28, lw.w2_s, c.d, tmp, BI_DTYPE_BF16, mode, stream));
       if (li + 1 < c.n_layers) {
-        BI_TRY(bi_rmsnorm(tmp, h, m->layers[li + 1].attn_norm, x, T, c.d, c.eps, mode, stream));
+        BI_TRY(rmsnorm_fp8_rows(tmp, h, m->layers[li + 1].attn_norm, nullptr, qa, sa, T, c.d, c.eps, stream));
         BI_TRY(dump_copy(li + 1, h));
       }
       continue;

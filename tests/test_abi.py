@@ -56,6 +56,9 @@ def test_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.bi_quantize_fp8(16, 4, 128, 64, 16, 16, None) == bi.BI_ERR_INVALID_ARG        # block rows
     assert lib.bi_gemm_fp8(16, 16, 4, 100, 16, 16, 128, 16, 0, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_gemm_fp8(16, 16, 4, 128, 16, 16, 128, 16, 7, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_rmsnorm_fp8(16, None, 16, None, 16, 16, 4, 200, 1e-6, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_rmsnorm_fp8(16, None, 16, None, None, 16, 4, 256, 1e-6, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_swiglu_fp8(16, 4, 200, 16, 16, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_topk(16, 4, 64, 16, 0, 16, 0, None) == bi.BI_ERR_INVALID_ARG       # K < 1
     assert lib.bi_topk(16, 4, 64, 16, 4097, 16, 0, None) == bi.BI_ERR_INVALID_ARG    # K > 4096
     assert lib.bi_topk(None, 4, 64, 16, 8, 16, 0, None) == bi.BI_ERR_INVALID_ARG     # null scores

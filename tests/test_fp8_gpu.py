@@ -87,3 +87,50 @@ def test_training_side_requantisation_is_deterministic():
     q1, s1 = _quant(wb, 128)
     q2, s2 = _quant(wb, 128)
     assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("rows,d,resid", [(1, 128, False), (37, 512, True), (64, 2048, True), (5, 16384, False),
+                                          (130, 1408, True)])
+def test_rmsnorm_fp8_equals_norm_then_quantize(rows, d, resid):
+    """The fused norm + quantisation writes exactly what bi_rmsnorm followed by
+    bi_quantize_fp8 writes: codes, scales, the bf16 row and the residual."""
+    rng = np.random.default_rng(rows + d)
+    x = dev_bf16(normal_bf16(rng, (rows, d), 2.0))
+    g = dev_bf16(normal_bf16(rng, (d,), 1.0))
+    r0 = dev_bf16(normal_bf16(rng, (rows, d), 1.0))
+    r1, r2 = r0.clone(), r0.clone()
+    y1 = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    bi.bi_rmsnorm(x, r1 if resid else None, g, y1, rows, d, 1e-6)
+    q1 = torch.empty((rows, d), dtype=torch.uint8, device="cuda")
+    s1 = torch.empty((rows, d // 128), dtype=torch.float32, device="cuda")
+    bi.bi_quantize_fp8(y1, rows, d, 1, q1, s1)
+    y2 = torch.empty_like(y1)
+    q2, s2 = torch.empty_like(q1), torch.empty_like(s1)
+    bi.bi_rmsnorm_fp8(x, r2 if resid else None, g, y2, q2, s2, rows, d)
+    assert torch.equal(q1, q2) and same_bits(s1, s2) and same_bits(y1, y2) and same_bits(r1, r2)
+    q3, s3 = torch.empty_like(q1), torch.empty_like(s1)
+    r3 = r0.clone()
+    bi.bi_rmsnorm_fp8(x, r3 if resid else None, g, None, q3, s3, rows, d)      # no bf16 row written
+    assert torch.equal(q1, q3) and same_bits(s1, s3) and same_bits(r1, r3)
+
+
+@pytest.mark.parametrize("T,F", [(1, 128), (33, 1536), (300, 512), (7, 5632)])
+def test_swiglu_fp8_matches_oracle(T, F):
+    """SiLU-mul-quant: codes and scales of bf16(silu(g) u) by the oracle's rule; a
+    code may differ only where the kernel's exp and numpy's exp round the product
+    to different bf16 values (one e4m3 step at most, and rarely)."""
+    from oracle import ops
+    rng = np.random.default_rng(T * F)
+    g13 = normal_bf16(rng, (T, 2 * F), 2.0)
+    q = torch.empty((T, F), dtype=torch.uint8, device="cuda")
+    s = torch.empty((T, F // 128), dtype=torch.float32, device="cuda")
+    bi.bi_swiglu_fp8(dev_bf16(g13), T, F, q, s)
+    gf = bits_to_f32(g13)
+    a = ops.silu_mul(gf[:, :F], gf[:, F:])
+    wq, ws = ofp8.quantize_act(a)
+    gq, gs = q.cpu().numpy(), s.cpu().numpy()
+    assert np.mean(gs == ws) >= 0.999
+    same_scale = np.repeat(gs == ws, 128, axis=1)
+    diff = (gq != wq) & same_scale
+    assert np.mean(gq == wq) >= 0.999
+    assert np.all(np.abs(gq[diff].astype(np.int32) - wq[diff].astype(np.int32)) <= 1)
