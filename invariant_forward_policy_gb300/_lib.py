@@ -85,6 +85,8 @@ _SIGS = {
                                _vp, _vp]),
     "bi_kv_fp8_gather": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _int, _int, _vp, _i64, _vp, _vp, _vp,
                                 _vp]),
+    "bi_attention_fp8": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp, _vp, _vp,
+                                _i64, _i64, _i64, _int, _f32, _vp, _sz, _vp, _vp, _vp, _int, _vp]),
     "bi_ssd_chunk_scan": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _int, _vp,
                                  _i64, _vp, _int, _vp]),
     "bi_gemm_fp8": (_int, [_vp, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _int, _int, _vp]),
@@ -232,6 +234,15 @@ def bi_attention(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv,
     _check(load().bi_attention(_p(q), T, _p(piece_seq), _p(piece_row0), _p(piece_pos0), P, max_q_len, Hq, Hkv, hd,
                                _p(k_cache), _p(v_cache), _p(block_table), max_blocks_per_seq, n_blocks, max_ctx,
                                kv_split, scale, _p(workspace), _nb(workspace), _p(out), mode, _s(stream)))
+
+
+def bi_attention_fp8(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache8, v_cache8, k_scale,
+                     v_scale, block_table, max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, workspace, out,
+                     out_q=None, out_scale=None, mode=BI_INVARIANT, stream=None):
+    _check(load().bi_attention_fp8(_p(q), T, _p(piece_seq), _p(piece_row0), _p(piece_pos0), P, max_q_len, Hq, Hkv,
+                                   hd, _p(k_cache8), _p(v_cache8), _p(k_scale), _p(v_scale), _p(block_table),
+                                   max_blocks_per_seq, n_blocks, max_ctx, kv_split, scale, _p(workspace),
+                                   _nb(workspace), _p(out), _p(out_q), _p(out_scale), mode, _s(stream)))
 
 
 def bi_attention_static_scratch(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,

@@ -22,6 +22,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "fp8.cuh"
 
 namespace bi {
 
@@ -128,6 +129,12 @@ struct AttnArgs {
   const __nv_bfloat16* q;  // [T, Hq, hd]
   const __nv_bfloat16* k_cache;
   const __nv_bfloat16* v_cache;  // [n_blocks, Hkv, 64, hd]
+  // FP8 cache (the KV8 kernels): e4m3 codes [n_blocks, Hkv, 64, hd] and one
+  // fp32 scale per (block, kv head, slot)
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* ks;
+  const float* vs;
   const int32_t* block_table;
   float* part_o;  // [T, Hq, nsplit, hd]
   float* part_ml; // [T, Hq, nsplit, 2]
@@ -338,7 +345,17 @@ __device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row
 // DECODE (query tiles of at most 16 rows, short contexts): warp w computes
 // lane w of the split from its own one-tile buffer, then warp 0 merges the
 // lanes in order.
-template <int HD, bool DECODE>
+// KV8: the cache holds e4m3 codes and per-(slot, kv head) scales.  Each tile's
+// codes and scales are copied (cp.async) into a staging area, then expanded
+// into the same swizzled bf16 tile the bf16 cache gives (code x power-of-two
+// scale is exact in bf16), so every later step, and every bit, is unchanged.
+template <int HD>
+struct Kv8Stage {
+  static constexpr int kCodes = kKeys * HD;                  // one page of K or V codes
+  static constexpr int kBytes = 2 * kCodes + 2 * kKeys * 4;  // K codes, V codes, K scales, V scales
+};
+
+template <int HD, bool DECODE, bool KV8>
 __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
@@ -400,6 +417,59 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     cp_async_commit();
   };
 
+  // KV8: one tile's codes and scales into the staging area `stg`
+  // (zero-filled where the block-table entry is bad or the key is in the future)
+  auto load_tile8 = [&](int key0, uint8_t* stg, int t0, int nthr) {
+    constexpr int C16 = HD / 16;  // 16-code chunks per key row
+    const bool tab_ok = key0 / kKeys < a.max_blk;
+    const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
+    const bool blk_ok = blk >= 0 && blk < a.n_blocks;
+    if (!blk_ok && t0 == 0) report(a.status, DEV_BAD_INDEX);
+    const int64_t page = (int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh;
+    for (int c = t0; c < kKeys * C16; c += nthr) {
+      const bool valid = blk_ok && (key0 + c / C16) <= max_pos;
+      const int64_t src = page * Kv8Stage<HD>::kCodes + (int64_t)c * 16;
+      cp_async16(stg + c * 16, a.k8 + (valid ? src : 0), valid);
+      cp_async16(stg + Kv8Stage<HD>::kCodes + c * 16, a.v8 + (valid ? src : 0), valid);
+    }
+    for (int c = t0; c < kKeys / 4; c += nthr) {  // 64 scales = 16 chunks of 4
+      const int64_t src = page * kKeys + c * 4;
+      cp_async16(stg + 2 * Kv8Stage<HD>::kCodes + c * 16, a.ks + (blk_ok ? src : 0), blk_ok);
+      cp_async16(stg + 2 * Kv8Stage<HD>::kCodes + kKeys * 4 + c * 16, a.vs + (blk_ok ? src : 0), blk_ok);
+    }
+    cp_async_commit();
+  };
+  // KV8: expand a staged tile into the swizzled bf16 K and V tiles; keys after
+  // max_pos become zeros whatever their slot holds
+  auto expand_tile8 = [&](int key0, const uint8_t* stg, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
+    constexpr int C16 = HD / 16;
+    for (int c = t0; c < 2 * kKeys * C16; c += nthr) {
+      const int which = c >= kKeys * C16;
+      const int cc = which ? c - kKeys * C16 : c;
+      const int key = cc / C16, c16 = cc % C16;
+      const bool valid = (key0 + key) <= max_pos;
+      const uint4 raw = *reinterpret_cast<const uint4*>(stg + which * Kv8Stage<HD>::kCodes + cc * 16);
+      const float sc = *reinterpret_cast<const float*>(stg + 2 * Kv8Stage<HD>::kCodes + which * kKeys * 4 + key * 4);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t packed[8];
+#pragma unroll
+      for (int u = 0; u < 16; u += 2) {
+        float f[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t code = (w[(u + t) >> 2] >> (8 * ((u + t) & 3))) & 0xffu;
+          const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+          f[t] = __fmul_rn(__half2float(__half(hr)), sc);
+        }
+        packed[u / 2] = valid ? pack_bf16x2(f[0], f[1]) : 0u;
+      }
+      uint8_t* dst = which ? sv : sk;
+      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16 + 1)) =
+          make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+  };
+
   float m[2] = {-INFINITY, -INFINITY};
   float l[2] = {0.f, 0.f};
   float acc[HD / 8][4];
@@ -418,9 +488,17 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     uint8_t* sv = sk + TILE_BYTES;
     const int lb = kv_begin + warp * lane_len;
     const int le = min(lb + lane_len, kv_end);
+    uint8_t* stg = smem + 4 * 2 * TILE_BYTES + warp * Kv8Stage<HD>::kBytes;  // KV8 only
     for (int key0 = lb; key0 < le; key0 += kKeys) {
-      load_tile(key0, sk, sv, lane, 32);
-      cp_async_wait<0>();
+      if constexpr (KV8) {
+        load_tile8(key0, stg, lane, 32);
+        cp_async_wait<0>();
+        __syncwarp();
+        expand_tile8(key0, stg, sk, sv, lane, 32);
+      } else {
+        load_tile(key0, sk, sv, lane, 32);
+        cp_async_wait<0>();
+      }
       __syncwarp();
       attn_tile<HD>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
       __syncwarp();
@@ -445,23 +523,36 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     }
   } else {
     // ---- all warps share a two-stage ring; lanes are walked in order
-    LaneState<HD>* run = reinterpret_cast<LaneState<HD>*>(smem + 2 * 2 * TILE_BYTES) + tid;
+    // bf16: two K+V tiles (the ring), then the running states.  KV8: one K+V
+    // tile, the running states, then two staging areas (the ring).
+    constexpr int kTiles = KV8 ? 1 : 2;
+    LaneState<HD>* run = reinterpret_cast<LaneState<HD>*>(smem + kTiles * 2 * TILE_BYTES) + tid;
+    uint8_t* stg0 = smem + kTiles * 2 * TILE_BYTES + 128 * sizeof(LaneState<HD>);
     *run = P;
     const int t_begin = kv_begin / kKeys;
     const int n_tiles = (kv_end - kv_begin + kKeys - 1) / kKeys;
     const int tiles_per_lane = lane_len / kKeys;
-    load_tile(t_begin * kKeys, smem, smem + TILE_BYTES, tid, 128);
+    if constexpr (KV8) load_tile8(t_begin * kKeys, stg0, tid, 128);
+    else load_tile(t_begin * kKeys, smem, smem + TILE_BYTES, tid, 128);
     for (int t = 0; t < n_tiles; ++t) {
       const int stage = t & 1;
-      uint8_t* sk = smem + stage * 2 * TILE_BYTES;
+      uint8_t* sk = smem + (KV8 ? 0 : stage) * 2 * TILE_BYTES;
       if (t + 1 < n_tiles) {
-        uint8_t* nk = smem + (stage ^ 1) * 2 * TILE_BYTES;
-        load_tile((t_begin + t + 1) * kKeys, nk, nk + TILE_BYTES, tid, 128);
+        if constexpr (KV8) {
+          load_tile8((t_begin + t + 1) * kKeys, stg0 + (stage ^ 1) * Kv8Stage<HD>::kBytes, tid, 128);
+        } else {
+          uint8_t* nk = smem + (stage ^ 1) * 2 * TILE_BYTES;
+          load_tile((t_begin + t + 1) * kKeys, nk, nk + TILE_BYTES, tid, 128);
+        }
         cp_async_wait<1>();
       } else {
         cp_async_wait<0>();
       }
       __syncthreads();
+      if constexpr (KV8) {
+        expand_tile8((t_begin + t) * kKeys, stg0 + stage * Kv8Stage<HD>::kBytes, sk, sk + TILE_BYTES, tid, 128);
+        __syncthreads();
+      }
       if (t > 0 && t % tiles_per_lane == 0) {  // lane boundary: fold the finished lane in
         LaneState<HD> r = *run;
         lane_merge<HD>(r, m, l, acc);
@@ -792,10 +883,15 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
 // splits is bound by bandwidth rather than by one load latency per split.
 constexpr int kMergeBatch = 8;
 
+// q8 (optional): the output row is also quantised in 1 x 128 blocks (e4m3 codes
+// q8 [T, Hq*hd], scales qs [T, Hq*hd / 128]); each CTA holds exactly one block.
+// out may then be null.
 __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ part_o,
                                                               const float* __restrict__ part_ml, PieceMeta pm,
                                                               int Hq, int hd, int nsplit, int split,
-                                                              __nv_bfloat16* __restrict__ out, int* status) {
+                                                              __nv_bfloat16* __restrict__ out,
+                                                              uint8_t* __restrict__ q8, float* __restrict__ qs,
+                                                              int* status) {
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
@@ -803,7 +899,7 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   const int row0 = pm.row0[p];
   if (i >= pm.row0[p + 1] - row0) return;
   const int idx = blockIdx.z * 128 + threadIdx.x;
-  if (idx >= Hq * hd) return;
+  if (idx >= Hq * hd) return;  // never with q8 (Hq*hd is then a multiple of 128)
   const int64_t row = row0 + i;
   const int pos = pm.pos0[p] + i;
   int ns = pos / split + 1;
@@ -835,26 +931,45 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
       O = __fadd_rn(O, __fmul_rn(o[k], w));
     }
   }
-  out[row * (int64_t)Hq * hd + idx] = f2bf(__fdiv_rn(O, L));
+  const __nv_bfloat16 ob = f2bf(__fdiv_rn(O, L));
+  if (out) out[row * (int64_t)Hq * hd + idx] = ob;
+  if (q8) {
+    __shared__ float wmax[4];
+    const float v = bf2f(ob);
+    float mx = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    const int e = fp8_scale_exp(fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3])));
+    q8[row * (int64_t)Hq * hd + idx] = (uint8_t)fp8_code(v, e);
+    if (threadIdx.x == 0) qs[row * (int64_t)(Hq * hd / 128) + blockIdx.z] = ldexpf(1.f, e);
+  }
 }
 
-template <int HD, bool DECODE>
+template <int HD, bool DECODE, bool KV8>
 constexpr int attn_smem_bytes() {
-  // decode: one K+V tile per warp; prefill: a two-stage ring plus the running lane state
-  return DECODE ? 4 * 2 * kKeys * HD * 2 : 2 * 2 * kKeys * HD * 2 + 128 * (int)sizeof(LaneState<HD>);
+  // decode: one K+V tile per warp (+ one staging area per warp for KV8);
+  // prefill: a two-stage ring plus the running lane state (KV8: one K+V tile,
+  // the running states and two staging areas)
+  return DECODE ? 4 * 2 * kKeys * HD * 2 + (KV8 ? 4 * Kv8Stage<HD>::kBytes : 0)
+                : (KV8 ? 1 : 2) * 2 * kKeys * HD * 2 + 128 * (int)sizeof(LaneState<HD>) +
+                      (KV8 ? 2 * Kv8Stage<HD>::kBytes : 0);
 }
 
-template <int HD, bool DECODE>
+template <int HD, bool DECODE, bool KV8>
 static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t st) {
-  constexpr int smem = attn_smem_bytes<HD, DECODE>();
+  constexpr int smem = attn_smem_bytes<HD, DECODE, KV8>();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attention_kernel<HD, DECODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_err =
+        cudaFuncSetAttribute(attention_kernel<HD, DECODE, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(attention_kernel<HD, DECODE>, grid, dim3(128), smem, st, args), "attention_kernel");
+  return launched(launch_pdl(attention_kernel<HD, DECODE, KV8>, grid, dim3(128), smem, st, args),
+                  "attention_kernel");
 }
 
 // Persistent decode launch: as many CTAs as fit on the GPU at once (at most
@@ -947,27 +1062,39 @@ size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ct
   return per * hd * sizeof(float) + per * 2 * sizeof(float) + 256;
 }
 
-bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
-                       const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
-                       const void* k_cache, const void* v_cache, const int32_t* block_table,
-                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split, float scale,
-                       void* workspace, size_t ws_bytes, void* out, int mode, void* stream) {
-  using namespace bi;
+}  // extern "C"
+
+namespace bi {
+
+// Shared body of bi_attention (bf16 cache) and bi_attention_fp8 (k8 != null).
+static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                                const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                                const void* k_cache, const void* v_cache, const void* k8, const void* v8,
+                                const float* ks, const float* vs, const int32_t* block_table,
+                                int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split,
+                                float scale, void* workspace, size_t ws_bytes, void* out, void* out_q,
+                                float* out_scale, int mode, void* stream) {
   BI_REQUIRE(T >= 0 && P >= 0, "bad shape");
   if (T == 0 || P == 0) return BI_OK;
-  BI_REQUIRE(q && piece_seq && piece_row0 && piece_pos0 && k_cache && v_cache && block_table && out && workspace,
-             "null pointer");
+  const bool kv8 = k8 != nullptr;
+  BI_REQUIRE(q && piece_seq && piece_row0 && piece_pos0 && block_table && workspace, "null pointer");
+  BI_REQUIRE(kv8 ? (v8 && ks && vs) : (k_cache && v_cache), "null cache pointer");
+  BI_REQUIRE(out || out_q, "null output");
+  BI_REQUIRE(!out_q == !out_scale, "out_q and out_scale go together");
   BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
   BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
   BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  BI_REQUIRE_SHAPE(!out_q || (Hq * hd) % 128 == 0, "quantised output needs Hq*hd to be a multiple of 128");
   const int group = Hq / Hkv;
   BI_REQUIRE_SHAPE(kRows % group == 0, "64 must be a multiple of Hq/Hkv");
   BI_REQUIRE(kv_split >= 64 && kv_split % 64 == 0, "kv_split must be a positive multiple of 64");
   BI_REQUIRE(max_ctx > 0 && max_q_len > 0, "bad max_ctx / max_q_len");
   BI_REQUIRE(max_blocks_per_seq > 0 && n_blocks > 0 && n_blocks * Hkv * 64 < (int64_t(1) << 32),
              "bad cache shape (max_blocks_per_seq, n_blocks)");
-  BI_REQUIRE(aligned16(q) && aligned16(k_cache) && aligned16(v_cache) && aligned16(workspace) && aligned16(out),
-             "pointers must be 16-byte aligned");
+  BI_REQUIRE(aligned16(q) && aligned16(workspace) && (!out || aligned16(out)), "pointers must be 16-byte aligned");
+  BI_REQUIRE(kv8 ? (aligned16(k8) && aligned16(v8) && aligned16(ks) && aligned16(vs))
+                 : (aligned16(k_cache) && aligned16(v_cache)),
+             "cache pointers must be 16-byte aligned");
   const int split = choose_split(mode, kv_split, P, max_q_len, Hkv, group, max_ctx);
   const int64_t ns = n_splits(max_ctx, split);
   const size_t per = (size_t)T * Hq * ns;
@@ -981,6 +1108,10 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   args.q = static_cast<const __nv_bfloat16*>(q);
   args.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
   args.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
+  args.k8 = static_cast<const uint8_t*>(k8);
+  args.v8 = static_cast<const uint8_t*>(v8);
+  args.ks = ks;
+  args.vs = vs;
   args.block_table = block_table;
   args.part_o = part_o;
   args.part_ml = part_ml;
@@ -999,24 +1130,64 @@ bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const
   // query tiles of at most 16 rows (decode steps) take the lane-parallel
   // schedule, persistent with TMA page streaming once contexts span more than
   // kDecPersistentSplits splits (and the call has at most kDecMaxPieces
-  // sequences), one CTA per (sequence, kv head, split) otherwise; bigger query
-  // tiles take the row-parallel schedule.
+  // sequences; bf16 cache only), one CTA per (sequence, kv head, split)
+  // otherwise; bigger query tiles take the row-parallel schedule.
   const bool decode = max_q_len * group <= 16;
-  if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
+  if (decode && !kv8 && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
     BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
     BI_TRY(hd == 64 ? launch_attention_decode<64>(args, P, st) : launch_attention_decode<128>(args, P, st));
   } else if (decode) {
     dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)(Hkv * ns));
-    BI_TRY(hd == 64 ? launch_attention<64, true>(args, grid, st) : launch_attention<128, true>(args, grid, st));
+    if (kv8)
+      BI_TRY(hd == 64 ? launch_attention<64, true, true>(args, grid, st)
+                      : launch_attention<128, true, true>(args, grid, st));
+    else
+      BI_TRY(hd == 64 ? launch_attention<64, true, false>(args, grid, st)
+                      : launch_attention<128, true, false>(args, grid, st));
   } else {
     dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
-    BI_TRY(hd == 64 ? launch_attention<64, false>(args, grid, st) : launch_attention<128, false>(args, grid, st));
+    if (kv8)
+      BI_TRY(hd == 64 ? launch_attention<64, false, true>(args, grid, st)
+                      : launch_attention<128, false, true>(args, grid, st));
+    else
+      BI_TRY(hd == 64 ? launch_attention<64, false, false>(args, grid, st)
+                      : launch_attention<128, false, false>(args, grid, st));
   }
   dim3 mgrid((unsigned)max_q_len, (unsigned)P, (unsigned)cdiv(Hq * hd, 128));
   return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(128), 0, st, (const float*)part_o,
                              (const float*)part_ml, args.pm, Hq, hd, (int)ns, split, static_cast<__nv_bfloat16*>(out),
-                             args.status),
+                             static_cast<uint8_t*>(out_q), out_scale, args.status),
                   "attention_merge_kernel");
+}
+
+}  // namespace bi
+
+extern "C" {
+
+bi_status bi_attention(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                       const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table,
+                       int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx, int kv_split, float scale,
+                       void* workspace, size_t ws_bytes, void* out, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE(out || T == 0 || P == 0, "null pointer");
+  BI_REQUIRE((k_cache && v_cache) || T == 0 || P == 0, "null pointer");
+  return attention_impl(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,
+                        nullptr, nullptr, nullptr, nullptr, block_table, max_blocks_per_seq, n_blocks, max_ctx,
+                        kv_split, scale, workspace, ws_bytes, out, nullptr, nullptr, mode, stream);
+}
+
+bi_status bi_attention_fp8(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
+                           const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
+                           const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,
+                           const int32_t* block_table, int64_t max_blocks_per_seq, int64_t n_blocks, int64_t max_ctx,
+                           int kv_split, float scale, void* workspace, size_t ws_bytes, void* out, void* out_q,
+                           float* out_scale, int mode, void* stream) {
+  using namespace bi;
+  BI_REQUIRE((k_cache8 && v_cache8 && k_scale && v_scale) || T == 0 || P == 0, "null pointer");
+  return attention_impl(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, nullptr, nullptr,
+                        k_cache8, v_cache8, k_scale, v_scale, block_table, max_blocks_per_seq, n_blocks, max_ctx,
+                        kv_split, scale, workspace, ws_bytes, out, out_q, out_scale, mode, stream);
 }
 
 }  // extern "C"

@@ -48,7 +48,6 @@ struct DevMeta {
   int32_t* logit_tgt;  // target id of each logit row (or -1)
   int32_t* row_seq;    // sequence of every pass row
   int32_t* row_pos;    // absolute position of every pass row
-  int32_t* piece_ident;  // 0 .. pieces-1 (FP8 KV: row p of the gathered page table)
 };
 
 __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ tokens,
@@ -60,7 +59,6 @@ __global__ void pass_meta_kernel(const PassMeta pm, const int32_t* __restrict__ 
       dm.piece_seq[p] = pm.seq[p];
       dm.piece_row0[p] = pm.row0[p];
       dm.piece_pos0[p] = pm.pos0[p];
-      dm.piece_ident[p] = p;
     }
     if (threadIdx.x == 0) dm.piece_row0[pm.n_pieces] = pm.row0[pm.n_pieces];
   }
@@ -97,7 +95,6 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
   if (threadIdx.x == 0) {
     if (b == 0) dm.piece_row0[B] = B;
     dm.piece_seq[b] = b;
-    dm.piece_ident[b] = b;
     dm.piece_row0[b] = b;
     dm.piece_pos0[b] = pos[b];
     dm.ids[b] = id;
@@ -116,12 +113,11 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
 
 // ------------------------------------------------------------- workspace plan
 struct FwdLayout {
-  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos, piece_ident;
+  size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos;
   size_t h, x, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
   size_t attn_ws_bytes, gemm_ws_bytes, lp_ws_bytes;
-  // fp8 only: bf16 qkv and gate/up outputs, activation codes and scales, the gathered bf16 pages
-  size_t qkv, g13, qa, sa, kw, vw, wbt;
-  int64_t ws_blk;  // gathered pages per piece
+  // fp8 only: bf16 qkv and gate/up outputs, activation codes and scales
+  size_t qkv, g13, qa, sa;
   size_t total;
 };
 
@@ -144,7 +140,6 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   L.logit_tgt = take(std::max(Tm, Rm) * 4);
   L.row_seq = take(Tm * 4);
   L.row_pos = take(Tm * 4);
-  L.piece_ident = take(Pm * 4);
   L.h = take(Tm * c.d * 2);
   L.x = take(Tm * c.d * 2);
 
@@ -176,11 +171,6 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
     L.g13 = take(Tm * 2 * c.ffn * 2);
     L.qa = take(Tm * kmax);
     L.sa = take(Tm * (kmax / 128) * 4);
-    L.ws_blk = cdiv(max_ctx, 64);
-    const size_t pages = (size_t)Pm * L.ws_blk;
-    L.kw = take(pages * c.n_heads_kv * 64 * c.head_dim * 2);
-    L.vw = take(pages * c.n_heads_kv * 64 * c.head_dim * 2);
-    L.wbt = take(pages * 4);
   }
   L.total = off + 256;
   return L;
@@ -244,7 +234,7 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     void* kc = static_cast<uint8_t*>(k_cache) + li * layer_cache;
     void* vc = static_cast<uint8_t*>(v_cache) + li * layer_cache;
     if (c.fp8) {
-      // block-FP8 W8A8 layer; K and V make the FP8 round trip through the one gather path.
+      // block-FP8 W8A8 layer; K and V make the FP8 round trip through the one read path.
       // qa/sa hold the quantised input rows of the next GEMM (written by the
       // preceding norm, or by the quantiser / SwiGLU in front of it).
       auto* qa = at<uint8_t>(ws, L.qa);
@@ -255,14 +245,11 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
       BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.wqkv8, lw.wqkv_s, nqkv, qkv, BI_DTYPE_BF16, mode, stream));
       BI_TRY(rope_kv_write_fp8(qkv, T, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos), Hq, Hkv, hd,
                                m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, ks, vc, vs, cst));
-      BI_TRY(kv_fp8_gather_to(kc, vc, ks, vs, n_blocks, piece_seq, piece_row0, piece_pos0, ps.pieces, Hkv, hd,
-                              block_table, max_blk, L.ws_blk, at<void>(ws, L.kw), at<void>(ws, L.vw),
-                              at<int32_t>(ws, L.wbt), cst));
-      BI_TRY(bi_attention(q, T, at<int32_t>(ws, L.piece_ident), piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq,
-                          Hkv, hd, at<void>(ws, L.kw), at<void>(ws, L.vw), at<int32_t>(ws, L.wbt), L.ws_blk,
-                          ps.pieces * L.ws_blk, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
-                          L.attn_ws_bytes, ao, mode, stream));
-      BI_TRY(bi_quantize_fp8(ao, T, hq, 1, qa, sa, stream));
+      // attention reads the FP8 pages directly (bit-equal to gather + bf16 attention)
+      // and its split merge writes the quantised output rows for the O projection
+      BI_TRY(bi_attention_fp8(q, T, piece_seq, piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq, Hkv, hd, kc, vc,
+                              ks, vs, block_table, max_blk, n_blocks, ps.max_ctx, (int)c.kv_split, scale,
+                              at<void>(ws, L.attn_ws), L.attn_ws_bytes, nullptr, qa, sa, mode, stream));
       BI_TRY(bi_gemm_fp8(qa, sa, T, hq, lw.wo8, lw.wo_s, c.d, tmp, BI_DTYPE_BF16, mode, stream));
       BI_TRY(rmsnorm_fp8_rows(tmp, h, lw.ffn_norm, nullptr, qa, sa, T, c.d, c.eps, stream));
       BI_TRY(bi_gemm_fp8(qa, sa, T, c.d, lw.w138, lw.w13_s, 2 * c.ffn, at<void>(ws, L.g13), BI_DTYPE_BF16, mode,
@@ -469,7 +456,7 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
                at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids),
                at<int32_t>(workspace, L.logit_src), at<int32_t>(workspace, L.logit_dst),
                at<int32_t>(workspace, L.logit_tgt), at<int32_t>(workspace, L.row_seq),
-               at<int32_t>(workspace, L.row_pos), at<int32_t>(workspace, L.piece_ident)};
+               at<int32_t>(workspace, L.row_pos)};
     BI_TRY(launched(launch_pdl(pass_meta_kernel, dim3((unsigned)cdiv(std::max<int64_t>(rows, 1), 256)), dim3(256), 0,
                                st, pm, tokens, target_ids, dm),
                     "pass_meta_kernel"));
@@ -498,8 +485,7 @@ bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* p
   DevMeta dm{at<int32_t>(workspace, L.piece_seq), at<int32_t>(workspace, L.piece_row0),
              at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids), at<int32_t>(workspace, L.logit_src),
              at<int32_t>(workspace, L.logit_dst), at<int32_t>(workspace, L.logit_tgt),
-             at<int32_t>(workspace, L.row_seq), at<int32_t>(workspace, L.row_pos),
-             at<int32_t>(workspace, L.piece_ident)};
+             at<int32_t>(workspace, L.row_seq), at<int32_t>(workspace, L.row_pos)};
   const cudaStream_t st = as_stream(stream);
   BI_TRY(launched(launch_pdl(decode_embed_kernel, dim3((unsigned)B), dim3(128), 0, st, tokens, pos, (int)B, dm,
                              static_cast<const __nv_bfloat16*>(m->embed), m->cfg.vocab, m->cfg.d,

@@ -59,6 +59,13 @@ def test_validation_rejects_bad_arguments_without_launching(lib):
     assert lib.bi_rmsnorm_fp8(16, None, 16, None, 16, 16, 4, 200, 1e-6, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_rmsnorm_fp8(16, None, 16, None, None, 16, 4, 256, 1e-6, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_swiglu_fp8(16, 4, 200, 16, 16, None) == bi.BI_ERR_INVALID_ARG
+    # FP8 attention: scales missing; quantised output needs Hq*hd % 128 == 0 and both of out_q / out_scale
+    assert lib.bi_attention_fp8(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, None, 16, 16, 1, 1, 64, 512, 0.1, 16,
+                                1 << 20, 16, None, None, 0, None) == bi.BI_ERR_INVALID_ARG
+    assert lib.bi_attention_fp8(16, 4, 16, 16, 16, 1, 4, 1, 1, 64, 16, 16, 16, 16, 16, 1, 1, 64, 512, 0.1, 16,
+                                1 << 20, None, 16, 16, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
+    assert lib.bi_attention_fp8(16, 4, 16, 16, 16, 1, 4, 8, 8, 64, 16, 16, 16, 16, 16, 1, 1, 64, 512, 0.1, 16,
+                                1 << 20, 16, 16, None, 0, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_topk(16, 4, 64, 16, 0, 16, 0, None) == bi.BI_ERR_INVALID_ARG       # K < 1
     assert lib.bi_topk(16, 4, 64, 16, 4097, 16, 0, None) == bi.BI_ERR_INVALID_ARG    # K > 4096
     assert lib.bi_topk(None, 4, 64, 16, 8, 16, 0, None) == bi.BI_ERR_INVALID_ARG     # null scores

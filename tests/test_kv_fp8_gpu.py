@@ -54,6 +54,22 @@ class Fp8Cache:
                         vw, wbt, self.max_blk, P * self.max_blk, max_ctx, 512, 1.0 / math.sqrt(self.hd), ws, out)
         return out, kw, vw, wbt
 
+    def attend_direct(self, pieces, qb, Hq, max_ctx, quant=False, mode=0):
+        """bi_attention_fp8 over the FP8 pages themselves; with quant also the
+        quantised output rows.  Returns (out, codes, scales)."""
+        seq, row0, pos0 = _pieces(pieces)
+        P = len(pieces)
+        T = qb.shape[0]
+        out = torch.empty((T, Hq * self.hd), dtype=torch.bfloat16, device="cuda")
+        oq = torch.empty((T, Hq * self.hd), dtype=torch.uint8, device="cuda") if quant else None
+        osc = torch.empty((T, Hq * self.hd // 128), dtype=torch.float32, device="cuda") if quant else None
+        ws = torch.empty(bi.bi_attention_workspace_size(T, Hq, self.hd, max_ctx, 512), dtype=torch.uint8,
+                         device="cuda")
+        bi.bi_attention_fp8(dev_bf16(qb), T, seq, row0, pos0, P, max(p[2] for p in pieces), Hq, self.Hkv, self.hd,
+                            self.k8, self.v8, self.ks, self.vs, self.bt, self.max_blk, self.n_blocks, max_ctx, 512,
+                            1.0 / math.sqrt(self.hd), ws, out, oq, osc, mode)
+        return out, oq, osc
+
 
 def _pieces(pieces):
     seq = torch.tensor([p[0] for p in pieces], dtype=torch.int32, device="cuda")
@@ -128,3 +144,39 @@ def test_fp8_cache_decode_rows_equal_prefill_rows(Hq, Hkv, hd):
         for max_ctx in (2048, 8192):
             o, *_ = chunked.attend(pcs, qb[rows], Hq, max_ctx)
             assert same_bits(o, full[torch.tensor(rows, device="cuda")]), (pos, max_ctx)
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd", [(8, 8, 64), (16, 4, 128), (8, 1, 128)])
+def test_direct_fp8_attention_equals_gather_path(Hq, Hkv, hd):
+    """Reading the FP8 pages inside attention gives the bits of gather + bf16
+    attention: whole-sequence prefill, prefill chunks that start mid-sequence
+    (slots after them hold NaN codes and scales) and decode rows; the fused
+    output quantisation equals bi_quantize_fp8 of the bf16 output."""
+    rng = np.random.default_rng(11 + hd + Hkv)
+    lens = [300, 1, 129, 700, 64]
+    T = sum(lens)
+    kb, vb = normal_bf16(rng, (T, Hkv, hd), 1.0), normal_bf16(rng, (T, Hkv, hd), 1.0)
+    qb = normal_bf16(rng, (T, Hq, hd), 1.0)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    c = Fp8Cache(lens, Hkv, hd, rng)
+    # only the first part of each sequence is in the cache: the rest stays NaN
+    part = [max(1, n // 2) for n in lens]
+    c.write([(b, 0, n) for b, n in enumerate(part)], np.concatenate([kb[offs[b]:offs[b] + n] for b, n in enumerate(part)]),
+            np.concatenate([vb[offs[b]:offs[b] + n] for b, n in enumerate(part)]))
+    cases = {
+        "prefill": [(b, 0, n) for b, n in enumerate(part)],
+        "chunk": [(b, max(0, n - 37), min(37, n)) for b, n in enumerate(part)],
+        "decode": [(b, n - 1, 1) for b, n in enumerate(part)],
+    }
+    for name, pcs in cases.items():
+        rows = np.concatenate([offs[b] + np.arange(p0, p0 + n) for b, p0, n in pcs])
+        for max_ctx in (max(part), 4096):
+            ref, *_ = c.attend(pcs, qb[rows], Hq, max_ctx)
+            got, oq, osc = c.attend_direct(pcs, qb[rows], Hq, max_ctx, quant=True)
+            assert same_bits(got, ref), (name, max_ctx)
+            wq = torch.empty_like(oq)
+            ws_ = torch.empty_like(osc)
+            bi.bi_quantize_fp8(ref, ref.shape[0], ref.shape[1], 1, wq, ws_)
+            assert torch.equal(oq, wq) and same_bits(osc, ws_), (name, max_ctx)
+            assert not torch.isnan(got.float()).any()
+    assert bi.bi_device_status() == 0
