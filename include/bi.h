@@ -276,17 +276,20 @@ bi_status bi_kv_fp8_gather(const void* k_cache8, const void* v_cache8, const flo
                            const int32_t* piece_pos0, int64_t P, int Hkv, int hd, const int32_t* block_table,
                            int64_t max_blocks_per_seq, void* k_ws, void* v_ws, int32_t* ws_block_table,
                            void* stream);
-/* bi_attention_fp8: bi_attention reading the FP8 cache directly: the same
- * schedules (except the persistent decode one) and the same per-row arithmetic,
- * with each 64-key page's codes and scales copied to shared memory and
- * expanded there into the bf16 tile bi_kv_fp8_gather would have written (code x
- * power-of-two scale is exact), so the result is bit-equal to gather +
- * bi_attention for every row, in every phase.  k_cache8 / v_cache8 uint8 and
- * k_scale / v_scale fp32 as written by bi_kv_fp8_write (16-byte aligned); the
- * other arguments as in bi_attention.  out (bf16 [T, Hq*hd]) may be NULL when
- * out_q is given; out_q (uint8 [T, Hq*hd]) and out_scale (fp32 [T, Hq*hd/128]),
- * both NULL or both set, receive the output rows quantised as bi_quantize_fp8
- * with block_rows = 1 would (Hq*hd % 128 == 0), fused into the split merge. */
+/* bi_attention_fp8: bi_attention reading the FP8 cache directly, with the same
+ * three schedules and per-row arithmetic.  Each 64-key page's codes are expanded
+ * in shared memory into the bf16 values of the codes (unscaled, exact); the K
+ * scale then multiplies each score column and the V scale each P element
+ * before its bf16 rounding.  With power-of-two scales both products are exact,
+ * so every row's bits equal bi_kv_fp8_gather + bi_attention (outputs within a
+ * few ulps of fp32's smallest normal number excepted: there, P.V terms below
+ * 2^-126 may round differently).  Prefill, decode and recompute all read
+ * through this one path.  k_cache8 / v_cache8 uint8 and k_scale / v_scale fp32
+ * as written by bi_kv_fp8_write (16-byte aligned); the other arguments as in
+ * bi_attention.  out (bf16 [T, Hq*hd]) may be NULL when out_q is given; out_q
+ * (uint8 [T, Hq*hd]) and out_scale (fp32 [T, Hq*hd/128]), both NULL or both
+ * set, receive the output rows quantised as bi_quantize_fp8 with
+ * block_rows = 1 would (Hq*hd % 128 == 0), fused into the split merge. */
 bi_status bi_attention_fp8(const void* q, int64_t T, const int32_t* piece_seq, const int32_t* piece_row0,
                            const int32_t* piece_pos0, int64_t P, int64_t max_q_len, int Hq, int Hkv, int hd,
                            const void* k_cache8, const void* v_cache8, const float* k_scale, const float* v_scale,

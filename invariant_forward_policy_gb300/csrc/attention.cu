@@ -190,10 +190,13 @@ __device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD
 
 // Fold one tile's scores into the online-softmax state of the warp's rows:
 // masking by select, fp32 rescaling, then O += P V with P rounded to bf16.
+// vsm (FP8 cache only): the tile's V scales; P is then multiplied by its key's
+// scale before the bf16 rounding (exact: a power of two), so that P' V_codes has
+// the products P (V_codes scale) term for term.
 template <int HD>
 __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int key0, const bool (&row_valid)[2],
                                             const int (&row_pos)[2], float scale_log2, int lane, float (&m)[2],
-                                            float (&l)[2], float (&acc)[HD / 8][4]) {
+                                            float (&l)[2], float (&acc)[HD / 8][4], const float* vsm = nullptr) {
   const int tq = lane & 3;
   float pr[8][4];
 #pragma unroll
@@ -235,6 +238,16 @@ __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int 
       acc[j][h * 2 + 1] = __fmul_rn(acc[j][h * 2 + 1], alpha);
     }
   }
+  if (vsm) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 vv = *reinterpret_cast<const float2*>(vsm + j * 8 + tq * 2);
+      pr[j][0] = __fmul_rn(pr[j][0], vv.x);
+      pr[j][1] = __fmul_rn(pr[j][1], vv.y);
+      pr[j][2] = __fmul_rn(pr[j][2], vv.x);
+      pr[j][3] = __fmul_rn(pr[j][3], vv.y);
+    }
+  }
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
     uint32_t pa[4];
@@ -255,13 +268,28 @@ __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int 
 }
 
 // One 64-key tile into the online-softmax state of 16 query rows (one warp).
+// ksm / vsm (FP8 cache only): the tile holds unscaled e4m3 values and these are
+// its per-key K and V scales.  A score column is multiplied by its key's K
+// scale: Q (codes x 2^k)^T = 2^k (Q codes^T) exactly.
 template <int HD>
 __device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][4],
                                           const bool (&row_valid)[2], const int (&row_pos)[2], float scale_log2,
-                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4]) {
+                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4],
+                                          const float* ksm = nullptr, const float* vsm = nullptr) {
   float sc[8][4];
   attn_scores<HD>(sk, qf, lane, sc);
-  attn_update<HD>(sv, sc, key0, row_valid, row_pos, scale_log2, lane, m, l, acc);
+  if (ksm) {
+    const int tq = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 kk = *reinterpret_cast<const float2*>(ksm + j * 8 + tq * 2);
+      sc[j][0] = __fmul_rn(sc[j][0], kk.x);
+      sc[j][1] = __fmul_rn(sc[j][1], kk.y);
+      sc[j][2] = __fmul_rn(sc[j][2], kk.x);
+      sc[j][3] = __fmul_rn(sc[j][3], kk.y);
+    }
+  }
+  attn_update<HD>(sv, sc, key0, row_valid, row_pos, scale_log2, lane, m, l, acc, vsm);
 }
 
 // Per-thread state of one lane, as stored in shared memory between lanes.
@@ -439,35 +467,29 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
     }
     cp_async_commit();
   };
-  // KV8: expand a staged tile into the swizzled bf16 K and V tiles; keys after
-  // max_pos become zeros whatever their slot holds
-  auto expand_tile8 = [&](int key0, const uint8_t* stg, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
+  // KV8: expand a staged tile into swizzled bf16 K and V tiles of the unscaled
+  // e4m3 values (the scales are applied to the scores and to P); keys after
+  // max_pos become zeros with zero scales, whatever their slot holds
+  auto expand_tile8 = [&](int key0, uint8_t* stg, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
     constexpr int C16 = HD / 16;
     for (int c = t0; c < 2 * kKeys * C16; c += nthr) {
       const int which = c >= kKeys * C16;
       const int cc = which ? c - kKeys * C16 : c;
       const int key = cc / C16, c16 = cc % C16;
-      const bool valid = (key0 + key) <= max_pos;
       const uint4 raw = *reinterpret_cast<const uint4*>(stg + which * Kv8Stage<HD>::kCodes + cc * 16);
-      const float sc = *reinterpret_cast<const float*>(stg + 2 * Kv8Stage<HD>::kCodes + which * kKeys * 4 + key * 4);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t packed[8];
-#pragma unroll
-      for (int u = 0; u < 16; u += 2) {
-        float f[2];
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t code = (w[(u + t) >> 2] >> (8 * ((u + t) & 3))) & 0xffu;
-          const __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
-          f[t] = __fmul_rn(__half2float(__half(hr)), sc);
-        }
-        packed[u / 2] = valid ? pack_bf16x2(f[0], f[1]) : 0u;
-      }
+      uint2 b0 = e4m3x4_to_bf16x4(raw.x), b1 = e4m3x4_to_bf16x4(raw.y);
+      uint2 b2 = e4m3x4_to_bf16x4(raw.z), b3 = e4m3x4_to_bf16x4(raw.w);
+      if (key0 + key > max_pos) b0 = b1 = b2 = b3 = make_uint2(0u, 0u);
       uint8_t* dst = which ? sv : sk;
-      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16 + 1)) =
-          make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16)) = make_uint4(b0.x, b0.y, b1.x, b1.y);
+      *reinterpret_cast<uint4*>(dst + kv_off<HD>(key, 2 * c16 + 1)) = make_uint4(b2.x, b2.y, b3.x, b3.y);
     }
+    float* sc8 = reinterpret_cast<float*>(stg + 2 * Kv8Stage<HD>::kCodes);  // K scales, then V scales
+    for (int key = t0; key < kKeys; key += nthr)
+      if (key0 + key > max_pos) sc8[key] = sc8[kKeys + key] = 0.f;
+  };
+  auto stage_ks = [&](const uint8_t* stg) {
+    return reinterpret_cast<const float*>(stg + 2 * Kv8Stage<HD>::kCodes);
   };
 
   float m[2] = {-INFINITY, -INFINITY};
@@ -500,7 +522,8 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
         cp_async_wait<0>();
       }
       __syncwarp();
-      attn_tile<HD>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
+      attn_tile<HD>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
+                    KV8 ? stage_ks(stg) : nullptr, KV8 ? stage_ks(stg) + kKeys : nullptr);
       __syncwarp();
     }
     // lanes meet in shared memory (each warp reuses its buffer); warp 0 merges 0..3
@@ -562,8 +585,10 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 #pragma unroll
         for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
       }
+      const uint8_t* stg_t = stg0 + stage * Kv8Stage<HD>::kBytes;
       attn_tile<HD>(smem_u32(sk), smem_u32(sk + TILE_BYTES), (t_begin + t) * kKeys, qf, row_valid, row_pos,
-                    a.scale_log2, lane, m, l, acc);
+                    a.scale_log2, lane, m, l, acc, KV8 ? stage_ks(stg_t) : nullptr,
+                    KV8 ? stage_ks(stg_t) + kKeys : nullptr);
       __syncthreads();
     }
     P = *run;
@@ -595,14 +620,22 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 constexpr int kDecMaxPieces = 1024;      // larger decode calls take the per-CTA schedule (same bits)
 constexpr int kDecPersistentSplits = 4;  // shorter contexts take the per-CTA schedule (same bits)
 
-template <int HD>
+// KV8 (FP8 cache): a ring object is a page of e4m3 codes (64 rows x hd bytes,
+// unswizzled) followed by its 64 fp32 scales; each consumer warp expands the
+// object into its own bf16 page (the swizzled layout ldmatrix reads) and copies
+// the scales, zero past the item's last position, before releasing the slot.
+template <int HD, bool KV8 = false>
 struct DecLayout {
-  // ring depth per consumer warp: three 16 KB pages at hd 128 (one CTA per
-  // SM); two 8 KB pages at hd 64, so that two CTAs share an SM
+  // ring depth per consumer warp: three slots at hd 128 (one CTA per SM); two
+  // at hd 64, so that two CTAs share an SM
   static constexpr int kDecSlots = HD == 64 ? 2 : 3;
-  static constexpr int kTile = kKeys * HD * 2;                       // one K or V page
-  static constexpr int kRing = 4 * kDecSlots * kTile;                // four rings
-  static constexpr int kStates = kRing;                              // lane states of warps 1..3
+  static constexpr int kTile = kKeys * HD * 2;                       // one bf16 K or V page
+  static constexpr int kCodes = kKeys * HD;                          // one page of codes
+  static constexpr int kSlot = KV8 ? (kCodes + kKeys * 4 + 1023) / 1024 * 1024 : kTile;
+  static constexpr int kRing = 4 * kDecSlots * kSlot;                // four rings
+  static constexpr int kPriv = kRing;                                // KV8: bf16 page per consumer warp
+  static constexpr int kPrivScale = kPriv + (KV8 ? 4 * kTile : 0);   // KV8: [4][64] scales
+  static constexpr int kStates = kPrivScale + (KV8 ? 4 * kKeys * 4 : 0);  // lane states of warps 1..3
   static constexpr int kTable = kStates + 3 * 32 * (int)sizeof(LaneState<HD>);  // int [kDecMaxPieces + 1]
   static constexpr int kBars = kTable + (kDecMaxPieces + 2) * 4;
   static constexpr int kAbort = kBars + 2 * 4 * kDecSlots * 8;       // full[4][S], empty[4][S]
@@ -661,11 +694,12 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int HD>
+template <int HD, bool KV8>
 __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
     attention_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
-                            const __grid_constant__ CUtensorMap tmv, int P) {
-  using Lay = DecLayout<HD>;
+                            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmks,
+                            const __grid_constant__ CUtensorMap tmvs, int P) {
+  using Lay = DecLayout<HD, KV8>;
   constexpr int kDecSlots = Lay::kDecSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -685,6 +719,10 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
   if (tid == 128) {
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    if (KV8) {
+      prefetch_tmap(&tmks);
+      prefetch_tmap(&tmvs);
+    }
   }
   pdl_trigger();
   pdl_wait();  // q, the cache pages and the piece positions come from preceding kernels
@@ -749,8 +787,13 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
               const int n = issued[wj] + kv;
               const int slot = wj * kDecSlots + n % kDecSlots;
               if (!dec_wait(&empty[slot], ((n / kDecSlots) & 1) ^ 1, abort_flag, a.status)) break;
-              uint8_t* dst = smem + slot * Lay::kTile;
-              if (bj >= 0) {
+              uint8_t* dst = smem + slot * Lay::kSlot;
+              if (bj >= 0 && KV8) {
+                mbar_arrive_expect_tx(&full[slot], Lay::kCodes + kKeys * 4);
+                const int page = bj * a.Hkv + it.kvh;
+                tma_load_2d(dst, kv ? &tmv : &tmk, &full[slot], 0, page * kKeys);
+                tma_load_2d(dst + Lay::kCodes, kv ? &tmvs : &tmks, &full[slot], 0, page);
+              } else if (bj >= 0) {
                 mbar_arrive_expect_tx(&full[slot], Lay::kTile);
                 const int y = (bj * a.Hkv + it.kvh) * kKeys;
 #pragma unroll
@@ -812,11 +855,64 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
 
     const int lb = it.kv_begin + warp * lane_len;
     const int le = min(lb + lane_len, it.kv_end);
+    uint8_t* priv = smem + Lay::kPriv + warp * Lay::kTile;                       // KV8 only
+    float* pscale = reinterpret_cast<float*>(smem + Lay::kPrivScale) + warp * kKeys;  // KV8 only
+    // KV8: ring object -> this warp's bf16 page of unscaled values and its scales,
+    // keys at or after n_keys zeroed
+    auto expand = [&](const uint8_t* obj, int n_keys) {
+      constexpr int C16 = HD / 16;  // 16-code chunks per key row; a lane keeps chunk lane % C16
+      const int c16 = lane % C16;
+#pragma unroll
+      for (int i = 0; i < kKeys * C16 / 32; ++i) {
+        const int key = (lane + 32 * i) / C16;
+        const uint4 raw = *reinterpret_cast<const uint4*>(obj + (lane + 32 * i) * 16);
+        const uint2 b0 = e4m3x4_to_bf16x4(raw.x), b1 = e4m3x4_to_bf16x4(raw.y);
+        const uint2 b2 = e4m3x4_to_bf16x4(raw.z), b3 = e4m3x4_to_bf16x4(raw.w);
+        *reinterpret_cast<uint4*>(priv + kv_off<HD>(key, 2 * c16)) = make_uint4(b0.x, b0.y, b1.x, b1.y);
+        *reinterpret_cast<uint4*>(priv + kv_off<HD>(key, 2 * c16 + 1)) = make_uint4(b2.x, b2.y, b3.x, b3.y);
+      }
+      if (n_keys < kKeys) {  // the item's last page: rows after its last position become zeros
+        __syncwarp();
+        for (int c = n_keys * (HD / 8) + lane; c < kKeys * (HD / 8); c += 32)
+          *reinterpret_cast<uint4*>(priv + kv_off<HD>(c / (HD / 8), c % (HD / 8))) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      const float* sc_in = reinterpret_cast<const float*>(obj + Lay::kCodes);
+      pscale[lane] = lane < n_keys ? sc_in[lane] : 0.f;
+      pscale[lane + 32] = lane + 32 < n_keys ? sc_in[lane + 32] : 0.f;
+    };
     for (int key0 = lb; key0 < le; key0 += kKeys) {
       float sc[8][4];
+      const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
       // K page
       int slot = warp * kDecSlots + used % kDecSlots;
       bool ok = dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+      if constexpr (KV8) {
+        if (ok) expand(smem + slot * Lay::kSlot, n_keys);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (ok) {
+          attn_scores<HD>(smem_u32(priv), qf, lane, sc);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 kk = *reinterpret_cast<const float2*>(pscale + j * 8 + tq * 2);
+            sc[j][0] = __fmul_rn(sc[j][0], kk.x);
+            sc[j][1] = __fmul_rn(sc[j][1], kk.y);
+            sc[j][2] = __fmul_rn(sc[j][2], kk.x);
+            sc[j][3] = __fmul_rn(sc[j][3], kk.y);
+          }
+        }
+        __syncwarp();  // the K page and its scales are read before the V page replaces them
+        ++used;
+        slot = warp * kDecSlots + used % kDecSlots;
+        ok = ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+        if (ok) expand(smem + slot * Lay::kSlot, n_keys);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (ok) attn_update<HD>(smem_u32(priv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc, pscale);
+        __syncwarp();
+        ++used;
+        continue;
+      }
       if (ok) attn_scores<HD>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
@@ -826,7 +922,6 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
       ok = ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
       if (ok) {
         uint8_t* sv = smem + slot * Lay::kTile;
-        const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
         if (n_keys < kKeys) {
           for (int c = n_keys * (HD / 8) + lane; c < kKeys * (HD / 8); c += 32) {
             const int key = c / (HD / 8), ch = c % (HD / 8);
@@ -974,29 +1069,42 @@ static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t 
 
 // Persistent decode launch: as many CTAs as fit on the GPU at once (at most
 // one per work item).  K and V are viewed as 2-D bf16 tensors [n_blocks * Hkv
-// * 64 rows, hd] read in 64 x 64 boxes with 128-byte swizzle.
-template <int HD>
+// * 64 rows, hd] read in 64 x 64 boxes with 128-byte swizzle; an FP8 cache as
+// code rows [n_blocks * Hkv * 64, hd bytes] read in 64-row boxes and scale rows
+// [n_blocks * Hkv, 256 bytes] read one row per page, both unswizzled.
+template <int HD, bool KV8>
 static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaStream_t st) {
-  constexpr int smem = DecLayout<HD>::kBytes;
+  constexpr int smem = DecLayout<HD, KV8>::kBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int per_sm = 1;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attention_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_err =
+        cudaFuncSetAttribute(attention_decode_kernel<HD, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD>, 160, smem);
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8>, 160, smem);
     if (per_sm < 1) per_sm = 1;
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention decode attributes: ") + cudaGetErrorString(attr_err));
   const uint64_t rows = (uint64_t)args.n_blocks * args.Hkv * kKeys;
-  CUtensorMap tmk, tmv;
-  if (!encode_tmap_2d_bf16(&tmk, args.k_cache, HD, rows, HD * 2, 64, kKeys, true) ||
-      !encode_tmap_2d_bf16(&tmv, args.v_cache, HD, rows, HD * 2, 64, kKeys, true))
-    return fail(BI_ERR_CUDA, "attention decode: cuTensorMapEncodeTiled failed for the K/V cache");
+  CUtensorMap tmk, tmv, tmks, tmvs;
+  bool ok;
+  if (KV8) {
+    ok = encode_tmap_2d_u8(&tmk, args.k8, HD, rows, HD, HD, kKeys, false) &&
+         encode_tmap_2d_u8(&tmv, args.v8, HD, rows, HD, HD, kKeys, false) &&
+         encode_tmap_2d_u8(&tmks, args.ks, kKeys * 4, rows / kKeys, kKeys * 4, kKeys * 4, 1, false) &&
+         encode_tmap_2d_u8(&tmvs, args.vs, kKeys * 4, rows / kKeys, kKeys * 4, kKeys * 4, 1, false);
+  } else {
+    ok = encode_tmap_2d_bf16(&tmk, args.k_cache, HD, rows, HD * 2, 64, kKeys, true) &&
+         encode_tmap_2d_bf16(&tmv, args.v_cache, HD, rows, HD * 2, 64, kKeys, true);
+    tmks = tmk;
+    tmvs = tmv;
+  }
+  if (!ok) return fail(BI_ERR_CUDA, "attention decode: cuTensorMapEncodeTiled failed for the K/V cache");
   const int64_t grid = std::min<int64_t>(P * args.Hkv * args.nsplit, (int64_t)num_sms() * per_sm);
-  return launched(launch_pdl(attention_decode_kernel<HD>, dim3((unsigned)grid), dim3(160), smem, st, args, tmk, tmv,
-                             (int)P),
+  return launched(launch_pdl(attention_decode_kernel<HD, KV8>, dim3((unsigned)grid), dim3(160), smem, st, args, tmk,
+                             tmv, tmks, tmvs, (int)P),
                   "attention_decode_kernel");
 }
 
@@ -1130,12 +1238,17 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
   // query tiles of at most 16 rows (decode steps) take the lane-parallel
   // schedule, persistent with TMA page streaming once contexts span more than
   // kDecPersistentSplits splits (and the call has at most kDecMaxPieces
-  // sequences; bf16 cache only), one CTA per (sequence, kv head, split)
+  // sequences), one CTA per (sequence, kv head, split)
   // otherwise; bigger query tiles take the row-parallel schedule.
   const bool decode = max_q_len * group <= 16;
-  if (decode && !kv8 && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
+  if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
     BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
-    BI_TRY(hd == 64 ? launch_attention_decode<64>(args, P, st) : launch_attention_decode<128>(args, P, st));
+    if (kv8)
+      BI_TRY(hd == 64 ? launch_attention_decode<64, true>(args, P, st)
+                      : launch_attention_decode<128, true>(args, P, st));
+    else
+      BI_TRY(hd == 64 ? launch_attention_decode<64, false>(args, P, st)
+                      : launch_attention_decode<128, false>(args, P, st));
   } else if (decode) {
     dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)(Hkv * ns));
     if (kv8)

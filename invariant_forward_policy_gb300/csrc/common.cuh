@@ -101,9 +101,9 @@ bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int6
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                          bool swizzle128);
-// 8-bit elements (fp8 codes), 128-byte swizzle.
+// 8-bit elements (fp8 codes or raw bytes), 128-byte swizzle unless swizzle128 is false.
 bool encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
-                       uint32_t box_inner, uint32_t box_outer);
+                       uint32_t box_inner, uint32_t box_outer, bool swizzle128 = true);
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled
 // while its predecessor in the stream is still finishing; it must execute

@@ -180,3 +180,40 @@ def test_direct_fp8_attention_equals_gather_path(Hq, Hkv, hd):
             assert torch.equal(oq, wq) and same_bits(osc, ws_), (name, max_ctx)
             assert not torch.isnan(got.float()).any()
     assert bi.bi_device_status() == 0
+
+
+@pytest.mark.parametrize("hd,lo,hi", [(64, -12, 1), (128, -12, 1), (64, -30, 5), (128, -30, 5)])
+def test_direct_fp8_attention_every_code(hd, lo, hi):
+    """Every finite e4m3 code (zeros and subnormals included) under scales 2^lo ..
+    2^(hi-1), read directly by attention (per-CTA and persistent decode
+    schedules, prefill), against the gather path: the same bits wherever the
+    output is above 2^-100.  Below that, in outputs within a few ulps of fp32's
+    smallest normal number, P.V terms under 2^-126 (fp32 subnormals, which the
+    two paths form from differently scaled operands) may round differently; the
+    difference stays under 2^-124.  (Every phase reads through the direct path,
+    so decode, prefill and recompute still agree bit for bit.)"""
+    Hq, Hkv = 8, 2
+    rng = np.random.default_rng(hd)
+    lens = [2500, 700]
+    c = Fp8Cache(lens, Hkv, hd, rng)
+    codes = np.concatenate([np.arange(0x00, 0x7F), np.arange(0x80, 0xFF)]).astype(np.uint8)   # 254 finite codes
+    for t in (c.k8, c.v8):
+        fill = codes[rng.integers(0, len(codes), t.numel())]
+        fill[: len(codes)] = codes                       # every code at least once
+        t.copy_(torch.from_numpy(fill.reshape(t.shape)))
+    for t in (c.ks, c.vs):
+        t.copy_(torch.from_numpy((2.0 ** rng.integers(lo, hi, t.shape)).astype(np.float32)))
+    qb = normal_bf16(rng, (sum(lens), Hq, hd), 1.0)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    for pcs in ([(0, 0, lens[0]), (1, 0, lens[1])], [(0, lens[0] - 1, 1), (1, lens[1] - 1, 1)],
+                [(0, 1000, 200), (1, 500, 200)]):
+        rows = np.concatenate([offs[b] + np.arange(p0, p0 + n) for b, p0, n in pcs])
+        for max_ctx in (2560, 8192):
+            ref, *_ = c.attend(pcs, qb[rows], Hq, max_ctx)
+            got, *_ = c.attend_direct(pcs, qb[rows], Hq, max_ctx)
+            r, g = host_f32(ref), host_f32(got)
+            d = np.abs(r - g)
+            big = np.abs(r) >= 2.0 ** -100
+            assert np.array_equal(r[big].view(np.uint32), g[big].view(np.uint32)), (pcs[0], max_ctx)
+            assert d.max() <= 2.0 ** -124, (pcs[0], max_ctx, d.max())
+    assert bi.bi_device_status() == 0
