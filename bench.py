@@ -432,7 +432,9 @@ def kernel_table(args):
                                             "16/4 heads x 128, split 512", "us": round(us, 1),
                                             "GB/s": round(nbytes / us / 1e3, 1), "frac": round(nbytes / us / 1e3 / hbm, 3),
                                             "bound": "hbm", "note": "KV (1.2 GB) exceeds L2"}
-    # the same decode through an FP8 KV cache: dequantise-and-gather into a bf16 workspace, then the same attention
+    # the same decode through an FP8 KV cache: attention reads the codes and scales
+    # directly (the drivers' path), and the pages' literal form (dequantise-and-gather
+    # into a bf16 workspace, then the bf16 attention) for comparison
     k8 = torch.randint(0, 0x7E, (nblk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
     v8 = torch.randint(0, 0x7E, (nblk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
     ks8 = torch.full((nblk, Hkv, 64), 2.0 ** -8, device=dev)
@@ -440,17 +442,20 @@ def kernel_table(args):
     kw = torch.empty((B * mb, Hkv, 64, hd), dtype=torch.bfloat16, device=dev)
     vw = torch.empty_like(kw)
     wbt = torch.empty((B, mb), dtype=torch.int32, device=dev)
+    b8 = int(lens.sum()) * Hkv * (hd + 4) * 2
+    us8 = _graph_us(lambda: bi.bi_attention_fp8(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, k8, v8, ks8, vs8, bt, mb,
+                                                nblk, max_ctx, 512, hd ** -0.5, ws, ao), n=5, reps=5)
 
-    def fp8_step():
+    def gather_step():
         bi.bi_kv_fp8_gather(k8, v8, ks8, vs8, nblk, seq, row0, pos0, B, Hkv, hd, bt, mb, kw, vw, wbt)
         bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kw, vw, wbt, mb, B * mb, max_ctx, 512, hd ** -0.5,
                         ws, ao)
-    us8 = _graph_us(fp8_step, n=5, reps=5)
-    b8 = int(lens.sum()) * Hkv * (hd + 4) * 2
+    usg = _graph_us(gather_step, n=5, reps=5)
     out["attention_decode_long_context_fp8_kv"] = {
         "us": round(us8, 1), "GB/s": round(b8 / us8 / 1e3, 1), "frac": round(b8 / us8 / 1e3 / hbm, 3), "bound": "hbm",
-        "note": "algorithmic bytes = the FP8 cache (codes + scales) read once; the gather writes and the attention "
-                "re-reads a bf16 copy (one read path for prefill and decode, as the pages do)"}
+        "gather_path_us": round(usg, 1),
+        "note": "algorithmic bytes = the FP8 cache (codes + scales) read once; pages expanded to bf16 in shared "
+                "memory (bound by that expansion, not by HBM); gather_path_us = dequantise-and-gather + bf16 attention"}
     del kc, vc, k8, v8, kw, vw
     # vocab-wide logprob, large-vocab shape (8.47 GB of fp32 logits, > L2)
     T, Vv = 16384, 129280
@@ -656,39 +661,53 @@ def config_table(args):
     del H4, W4, I4, L4
     torch.cuda.empty_cache()
 
-    # long-context GQA decode step
+    # long-context GQA decode step, bf16 model, then the block-FP8 model (W8A8 linear
+    # layers, FP8 KV cache: half the weight and KV bytes)
     shape = C5["shape"]
     lens = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"])
     B = len(lens)
     wb = make_decoder_weights(shape, seed=C5["seed"], w_std=C5["w_std"])
     max_ctx = int(lens.max()) + 1
-    dec = Decoder(shape, wb, max_pos=max_ctx + 64)
-    mb = -(-max_ctx // 64)
-    bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
-    cache = dec.alloc_cache(nb)
     rng = np.random.default_rng(C5["seed"] + 3)
     prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
-    _, sm, cu = dec.prefill(prompts, cache, bt, logit_from=[int(n) - 1 for n in lens], chunk=C5["chunk"],
-                            max_tokens=16384, max_ctx=max_ctx, max_logit_rows=B)
-    tok = sm[torch.from_numpy(cu[1:] - 1).to(dev)].contiguous()
-    pos = torch.from_numpy(lens.astype(np.int32)).to(dev)
-    smp = torch.empty(B, dtype=torch.int32, device=dev)
-    lpd = torch.empty(B, device=dev)
+    for fp8 in (False, True):
+        dec = Decoder(shape, wb, max_pos=max_ctx + 64, fp8=fp8)
+        mb = -(-max_ctx // 64)
+        bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
+        cache = dec.alloc_cache(nb)
+        _, sm, cu = dec.prefill(prompts, cache, bt, logit_from=[int(n) - 1 for n in lens], chunk=C5["chunk"],
+                                max_tokens=16384, max_ctx=max_ctx, max_logit_rows=B)
+        tok = sm[torch.from_numpy(cu[1:] - 1).to(dev)].contiguous()
+        pos = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        smp = torch.empty(B, dtype=torch.int32, device=dev)
+        lpd = torch.empty(B, device=dev)
 
-    def step(mode):
-        ws = dec.workspace(B, B, max_ctx, B, mode)
-        return lambda: dec.decode(tok, pos, cache, bt, max_ctx, smp, lpd, ws, mode)
-    t = both(step, 3, 5)
-    kv = float(sum(int(n) + 1 for n in lens)) * shape.n_layers * shape.n_heads_kv * shape.head_dim * 2 * 2
-    wbytes = sum(a.nbytes for lw in wb["layers"] for a in lw.values()) + wb["lm_head"].nbytes + wb["final_norm"].nbytes
-    row("long_context_gqa_decode_step_64seq", B, "logprobs/s", t,
-        {"bound": "hbm", "GB/s": round((kv + wbytes) / t["invariant"] / 1e3, 1),
-         "frac": round((kv + wbytes) / t["invariant"] / 1e3 / hbm, 3),
-         "bytes_per_step": int(kv + wbytes),
-         "note": "KV of every context + all layer and lm_head weights read once per step (embedding rows excluded)"})
-    dec.close()
-    del cache
-    torch.cuda.empty_cache()
+        def step(mode):
+            ws = dec.workspace(B, B, max_ctx, B, mode)
+            return lambda: dec.decode(tok, pos, cache, bt, max_ctx, smp, lpd, ws, mode)
+        t = both(step, 3, 5)
+        per_kv = 2 * (shape.head_dim + 4) if fp8 else 2 * shape.head_dim * 2   # K and V bytes per token and kv head
+        kv = float(sum(int(n) + 1 for n in lens)) * shape.n_layers * shape.n_heads_kv * per_kv
+        if fp8:
+            wbytes = sum(lw[k + "8"].numel() + lw[k + "_s"].numel() * 4 for lw in dec.layers
+                         for k in ("wqkv", "wo", "w13", "w2"))
+            wbytes += sum(lw[k].numel() * 2 for lw in dec.layers for k in ("attn_norm", "ffn_norm"))
+            wbytes += wb["lm_head"].nbytes + wb["final_norm"].nbytes
+        else:
+            wbytes = sum(a.nbytes for lw in wb["layers"] for a in lw.values()) + wb["lm_head"].nbytes + \
+                wb["final_norm"].nbytes
+        name = "long_context_gqa_decode_step_64seq" + ("_fp8" if fp8 else "")
+        row(name, B, "logprobs/s", t,
+            {"bound": "hbm", "GB/s": round((kv + wbytes) / t["invariant"] / 1e3, 1),
+             "frac": round((kv + wbytes) / t["invariant"] / 1e3 / hbm, 3),
+             "bytes_per_step": int(kv + wbytes),
+             "note": ("FP8 codes + scales of the KV cache and of the linear weights (bf16 lm_head) read once per "
+                      "step; bound in practice by the in-shared-memory expansion of the FP8 pages" if fp8 else
+                      "KV of every context + all layer and lm_head weights read once per step (embedding rows "
+                      "excluded)")})
+        dec.close()
+        del cache
+        torch.cuda.empty_cache()
 
     # block-FP8 dense decoder: the default workload's whole episode (prefill, 255
     # graph-replayed decode steps, recompute) with W8A8 linear layers and the FP8
