@@ -851,6 +851,25 @@ def run_kernel_case(name: str, reps: int):
         pos0 = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
         for _ in range(reps):
             bi.bi_kv_fp8_gather(k8, v8, ks, vs, B * mb, seq, row0, pos0, B, Hkv, hd, bt, mb, kw, vw, wbt)
+    elif name == "attention_decode_long_fp8":
+        # persistent decode schedule over an FP8 cache: 32 sequences x 4096 context, 16/4 heads x 128
+        # (134 MB of codes + 2 MB of scales > L2)
+        B, Hq, Hkv, hd, ctx = 32, 16, 4, 128, 4096
+        max_blk = ctx // 64
+        k8 = torch.randint(0, 0x7E, (B * max_blk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+        v8 = torch.randint(0, 0x7E, (B * max_blk, Hkv, 64, hd), dtype=torch.uint8, device=dev)
+        ks = torch.full((B * max_blk, Hkv, 64), 2.0 ** -8, device=dev)
+        vs = torch.full_like(ks, 2.0 ** -8)
+        bt = torch.arange(B * max_blk, dtype=torch.int32, device=dev).view(B, max_blk)
+        q = (0.5 * torch.randn((B, Hq, hd), device=dev)).to(torch.bfloat16)
+        seq = torch.arange(B, dtype=torch.int32, device=dev)
+        row0 = torch.arange(B + 1, dtype=torch.int32, device=dev)
+        pos0 = torch.full((B,), ctx - 1, dtype=torch.int32, device=dev)
+        out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, ctx, 512), dtype=torch.uint8, device=dev)
+        for _ in range(reps):
+            bi.bi_attention_fp8(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, k8, v8, ks, vs, bt, max_blk, B * max_blk,
+                                ctx, 512, hd ** -0.5, ws, out)
     elif name == "attention_decode_long":
         # persistent decode schedule: 32 sequences x 4096 context, 16/4 heads x 128 (268 MB of KV > L2)
         B, Hq, Hkv, hd, ctx = 32, 16, 4, 128, 4096
@@ -878,7 +897,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
-                         "attention_decode, attention_decode_long, gemm_fp8, topk_decode, ssd_prefill, kv_fp8_gather) or "
+                         "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
+                         "kv_fp8_gather) or "
                          "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)

@@ -21,6 +21,7 @@
 #include <mutex>
 #include <string>
 
+#include "attn_merge.cuh"
 #include "common.cuh"
 #include "fp8.cuh"
 
@@ -972,13 +973,11 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
   if (warp != 0 && handed) named_bar_sync(2, 128);  // pairs with warp 0's last hand-back
 }
 
-// Merge of the split partials in ascending split order.  One thread per
-// output element (row, head, d), 128 per CTA; the split records are loaded in
-// batches of kMergeBatch ahead of the in-order accumulation, so a row with many
-// splits is bound by bandwidth rather than by one load latency per split.
-constexpr int kMergeBatch = 8;
-
-// q8 (optional): the output row is also quantised in 1 x 128 blocks (e4m3 codes
+// Merge of the split partials in ascending split order (attn_merge.cuh).  One
+// thread per output element (row, head, d), 128 per CTA; the split records are
+// loaded in batches of kMergeBatch ahead of the in-order accumulation, so a row
+// with many splits is bound by bandwidth rather than by one load latency per
+// split.  q8 (optional): the output row is also quantised in 1 x 128 blocks (e4m3 codes
 // q8 [T, Hq*hd], scales qs [T, Hq*hd / 128]); each CTA holds exactly one block.
 // out may then be null.
 __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ part_o,
@@ -997,36 +996,10 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   if (idx >= Hq * hd) return;  // never with q8 (Hq*hd is then a multiple of 128)
   const int64_t row = row0 + i;
   const int pos = pm.pos0[p] + i;
-  int ns = pos / split + 1;
-  if (ns > nsplit) {  // a position beyond the call's max_ctx bound
-    if (idx == 0) report(status, DEV_BAD_INDEX);
-    ns = nsplit;
-  }
+  const int ns = merge_split_count(pos, split, nsplit, status, idx == 0);
   const int h = idx / hd, d = idx % hd;
-  const int64_t base = (row * Hq + h) * nsplit;
-  const float2* ml = reinterpret_cast<const float2*>(part_ml) + base;
-  const float* po = part_o + base * hd + d;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[s].x);
-  float L = 0.f, O = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
-    float2 r[kMergeBatch];
-    float o[kMergeBatch];
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      const bool in = s0 + k < ns;
-      r[k] = in ? ml[s0 + k] : make_float2(-INFINITY, 0.f);
-      o[k] = in ? po[(int64_t)(s0 + k) * hd] : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < kMergeBatch; ++k) {
-      if (s0 + k >= ns) break;
-      const float w = exp2f(__fsub_rn(r[k].x, M));
-      L = __fadd_rn(L, __fmul_rn(r[k].y, w));
-      O = __fadd_rn(O, __fmul_rn(o[k], w));
-    }
-  }
-  const __nv_bfloat16 ob = f2bf(__fdiv_rn(O, L));
+  const float merged = merge_split_element(part_o, part_ml, (row * Hq + h) * nsplit, ns, hd, d);
+  const __nv_bfloat16 ob = f2bf(merged);
   if (out) out[row * (int64_t)Hq * hd + idx] = ob;
   if (q8) {
     __shared__ float wmax[4];

@@ -6,17 +6,12 @@
 // both the rollout and the training side).
 #include "common.cuh"
 #include "fp8.cuh"
+#include "norm.cuh"
 
 namespace bi {
 
-// Threads per row: d/8 (one 16-byte vector each) capped at 256; a thread walks
-// its vectors with stride 8*blockDim, so the per-thread order depends on d only.
-static int norm_threads(int64_t d) {
-  int64_t t = d / 8;
-  if (t > 256) t = 256;
-  if (t < 32) t = 32;
-  return (int)((t + 31) / 32 * 32);
-}
+// Threads per row: norm_threads(d) (norm.cuh); a thread walks its vectors with
+// stride 8*blockDim, so the per-thread order depends on d only.
 
 // Row r of y is the norm of row src(r) of x (+ residual), src(r) = idx ? idx[r] : r.
 // kFp8: the bf16 output row is also quantised in 1 x 128 blocks into codes q and
@@ -36,7 +31,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   const int nvec = d / 8;
-  constexpr int kMaxVec = 8;  // d <= 16384 -> at most 8 vectors per thread with 256 threads
+  constexpr int kMaxVec = kNormMaxVec;
   uint4 sv[kMaxVec];
   float ss = 0.f;
   const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
@@ -47,30 +42,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
     if (v < nvec) {
       uint4 a = xr[v];
       if (kResidual) {
-        uint4 b = rr[v];
-        uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
-        const uint32_t* pb = reinterpret_cast<const uint32_t*>(&b);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float lo = __fadd_rn(bf16lo(pb[j]), bf16lo(pa[j]));
-          float hi = __fadd_rn(bf16hi(pb[j]), bf16hi(pa[j]));
-          pa[j] = pack_bf16x2(lo, hi);
-        }
+        a = norm_residual_add(a, rr[v]);
         rr[v] = a;
       }
       sv[i] = a;
-      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&a);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float lo = bf16lo(pa[j]), hi = bf16hi(pa[j]);
-        ss = __fmaf_rn(lo, lo, ss);
-        ss = __fmaf_rn(hi, hi, ss);
-      }
+      ss = norm_ss_vec(a, ss);
     }
   }
   // fixed xor-butterfly inside the warp, then warps summed in index order
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  ss = norm_warp_sum(ss);
   __shared__ float warp_ss[8];
   __shared__ float s_inv;
   if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
@@ -78,8 +58,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   if (tid == 0) {
     float t = 0.f;
     for (int w = 0; w < nthr / 32; ++w) t += warp_ss[w];
-    const float ms = __fdiv_rn(t, (float)d);
-    s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    s_inv = norm_inv(t, d, eps);
   }
   __syncthreads();
   const float inv = s_inv;
@@ -91,16 +70,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
     const bool on = v < nvec;
     uint4 o = make_uint4(0, 0, 0, 0);
     if (on) {
-      const uint4 g = gr[v];
-      const uint32_t* pa = reinterpret_cast<const uint32_t*>(&sv[i]);
-      const uint32_t* pg = reinterpret_cast<const uint32_t*>(&g);
-      uint32_t* po = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float lo = __fmul_rn(__fmul_rn(bf16lo(pa[j]), inv), bf16lo(pg[j]));
-        float hi = __fmul_rn(__fmul_rn(bf16hi(pa[j]), inv), bf16hi(pg[j]));
-        po[j] = pack_bf16x2(lo, hi);
-      }
+      o = norm_apply(sv[i], gr[v], inv);
       if (y) reinterpret_cast<uint4*>(y + row * d)[v] = o;
     }
     if (kFp8) {
