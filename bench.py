@@ -794,6 +794,35 @@ def run_kernel_case(name: str, reps: int):
         pd = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
         for _ in range(reps):
             ep.run(pd)
+    elif name == "c5_decode":
+        # long-context GQA decode steps (8 layers, d 2048, 64 sequences, contexts 1K-32K) after an
+        # untimed prefill; the decode launches sit in the NVTX range "decode"
+        from invariant_forward_policy_gb300.decoder import Decoder
+        from synthetic import C5, make_c5_prompt_lengths, make_decoder_weights
+        shape = C5["shape"]
+        lens = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"])
+        B = len(lens)
+        wb = make_decoder_weights(shape, seed=C5["seed"], w_std=C5["w_std"])
+        max_ctx = int(lens.max()) + 1
+        rng = np.random.default_rng(C5["seed"] + 3)
+        prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
+        dec = Decoder(shape, wb, max_pos=max_ctx + 64, device=dev)
+        mb = -(-max_ctx // 64)
+        bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
+        cache = dec.alloc_cache(nb)
+        _, sm, cu = dec.prefill(prompts, cache, bt, logit_from=[int(n) - 1 for n in lens], chunk=C5["chunk"],
+                                max_tokens=16384, max_ctx=max_ctx, max_logit_rows=B)
+        tok = sm[torch.from_numpy(cu[1:] - 1).to(dev)].contiguous()
+        pos = torch.from_numpy(lens.astype(np.int32)).to(dev)
+        smp = torch.empty(B, dtype=torch.int32, device=dev)
+        lpd = torch.empty(B, device=dev)
+        ws = dec.workspace(B, B, max_ctx, B)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("decode")
+        for _ in range(reps):
+            dec.decode(tok, pos, cache, bt, max_ctx, smp, lpd, ws)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
     elif name == "gemm_fp8":
         # block-FP8 W8A8 GEMM at a prefill FFN shape (operands quantised once, untimed)
         M, N, K = 8192, 11264, 2048
@@ -898,7 +927,7 @@ def main():
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
-                         "kv_fp8_gather) or "
+                         "kv_fp8_gather, c5_decode) or "
                          "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)

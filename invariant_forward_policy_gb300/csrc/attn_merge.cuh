@@ -11,7 +11,7 @@
 
 namespace bi {
 
-constexpr int kMergeBatch = 8;  // split records loaded ahead of the in-order accumulation
+constexpr int kMergeBatch = 16;  // split records loaded ahead of the in-order accumulation
 
 // M = max_s m_s in ascending s
 __device__ __forceinline__ float merge_max(const float2* ml, int ns) {
