@@ -34,6 +34,18 @@ E2E_MAX_FP8, E2E_MEAN_FP8 = 0.4, 0.1
 FP8_LAYER_MAX, FP8_LAYER_MEAN = 0.5, 0.05
 
 
+def greedy_agrees(ids, logits, argmax, gap):
+    """GPU greedy ids against the oracle's argmax (teacher forced on the GPU's own
+    tokens) at every step whose oracle top-2 logit gap exceeds `gap` (twice the
+    free-running tolerance, so that numerical noise cannot flip the choice there).
+    Returns the number of steps checked."""
+    top2 = np.sort(np.asarray(logits, np.float64), axis=-1)[:, -2:]
+    sure = (top2[:, 1] - top2[:, 0]) > gap
+    ids = np.asarray(ids)
+    assert np.array_equal(ids[sure], np.asarray(argmax)[sure]), np.nonzero(ids[sure] != np.asarray(argmax)[sure])
+    return int(sure.sum())
+
+
 def e2e_close(got, want, max_tol=E2E_MAX, mean_tol=E2E_MEAN):
     err = np.abs(np.asarray(got, np.float64) - want)
     assert err.max() < max_tol and err.mean() < mean_tol, (err.max(), err.mean())

@@ -14,7 +14,7 @@ from oracle import model as omodel
 from oracle import ops
 from synthetic import C2, DecoderShape, make_decoder_weights, make_prompts
 from tests.gpu_util import same_bits
-from tests.parity import E2E_MAX_SMALL, E2E_MEAN_SMALL, anchored_parity, e2e_close
+from tests.parity import E2E_MAX, E2E_MAX_SMALL, E2E_MEAN_SMALL, anchored_parity, e2e_close, greedy_agrees
 
 pytestmark = pytest.mark.gpu
 
@@ -87,9 +87,12 @@ def test_small_decoder_rollout_equals_recompute_and_oracle():
     assert torch.equal(ids_s, ids_g) and same_bits(lp_s, lp_g)
     anchored_parity(dec, wb, shape, [np.concatenate([prompts[b], gens[b][:-1]]) for b in range(5)])
     W = omodel.weights_to_f32(wb)
+    checked = 0
     for b in range(5):
-        _, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
+        logits, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
         e2e_close(lp_g[b].cpu().numpy(), want, E2E_MAX_SMALL, E2E_MEAN_SMALL)
+        checked += greedy_agrees(gens[b], logits, am, 2 * E2E_MAX_SMALL)
+    assert checked > 0
 
 
 def test_gqa_decoder_rollout_equals_recompute_long_context():
@@ -146,9 +149,12 @@ def test_c2_dense_decoder_diff_zero_all_schedules():
         assert same_bits(lt, lp)
     W = omodel.weights_to_f32(wb)
     errs = []
+    checked = 0
     for b in (0, 5, 10, 15):
-        _, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
+        logits, want, am = omodel.score_generation(W, shape, prompts[b], gens[b])
         errs.append(e2e_close(lp[b].cpu().numpy(), want))
+        checked += greedy_agrees(gens[b], logits, am, 2 * E2E_MAX)
+    assert checked > 0
     errs = np.concatenate(errs)
     print("C2 free-running oracle error: max %.2e mean %.2e p99 %.2e" % (errs.max(), errs.mean(),
                                                                          np.quantile(errs, 0.99)))
