@@ -55,13 +55,15 @@ __host__ __device__ inline int64_t ssd_store_floats(int H, int /*G*/, int P, int
 __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) {
   extern __shared__ __align__(16) float sm[];
   const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
-  const int NS = N + 1;           // padded row stride of B and C: conflict-free column walks
-  float* Hs = sm;                 // [N][P] state entering the chunk
-  float* Bs = Hs + N * P;         // [Q][NS]
-  float* Cs = Bs + Q * NS;        // [Q][NS]
-  float* xs = Cs + Q * NS;        // [Q][P]
-  float* Gm = xs + Q * P;         // [Q][Q] (C_i . B_j) scaled by the decay
-  float* ls = Gm + Q * Q;         // [Q] loga
+  // B, C and x hold bf16 values (inputs, or their exact copies in the store):
+  // staged as bf16 and widened exactly on use, so that two CTAs share an SM
+  const int NS = N + 2;                      // padded bf16 row stride of B and C: conflict-free column walks
+  float* Hs = sm;                            // [N][P] state entering the chunk
+  float* Gm = Hs + N * P;                    // [Q][Q] (C_i . B_j) scaled by the decay
+  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(Gm + Q * Q);  // [Q][NS]
+  __nv_bfloat16* Cs = Bs + Q * NS;                                   // [Q][NS]
+  __nv_bfloat16* xs = Cs + Q * NS;                                   // [Q][P]
+  float* ls = reinterpret_cast<float*>(xs + Q * P);                  // [Q] loga
   float* Ls = ls + Q;             // [Q] cumulative
   float* eL = Ls + Q;             // [Q] exp(L_i)
   float* dq = eL + Q;             // [Q] exp(L_{Q-1} - L_j), for the exit state
@@ -94,17 +96,17 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
     for (int e = tid; e < i1 * N; e += kSsdThreads) {
       const int i = e / N, n = e % N;
       if (i < i0) {
-        Bs[i * NS + n] = st_B[((int64_t)i * H + h) * N + n];
+        Bs[i * NS + n] = f2bf(st_B[((int64_t)i * H + h) * N + n]);  // a bf16 value: exact
       } else {
         const int64_t r = row0 + (cs + i - p0);
-        Bs[i * NS + n] = bf2f(a.B[(r * G + g) * N + n]);
-        Cs[i * NS + n] = bf2f(a.C[(r * G + g) * N + n]);
+        Bs[i * NS + n] = a.B[(r * G + g) * N + n];
+        Cs[i * NS + n] = a.C[(r * G + g) * N + n];
       }
     }
     for (int e = tid; e < i1 * P; e += kSsdThreads) {
       const int i = e / P, p = e % P;
-      xs[e] = i < i0 ? st_x[((int64_t)i * H + h) * P + p]
-                     : bf2f(a.x[((row0 + (cs + i - p0)) * (int64_t)H + h) * P + p]);
+      xs[e] = i < i0 ? f2bf(st_x[((int64_t)i * H + h) * P + p])
+                     : a.x[((row0 + (cs + i - p0)) * (int64_t)H + h) * P + p];
     }
     for (int i = tid; i < i1; i += kSsdThreads)
       ls[i] = i < i0 ? st_l[(int64_t)i * H + h] : a.loga[(row0 + (cs + i - p0)) * (int64_t)H + h];
@@ -132,8 +134,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
           float c[4], bb[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            c[u] = ib + u < i1 ? Cs[(ib + u) * NS + n] : 0.f;
-            bb[u] = jb + u < i1 ? Bs[(jb + u) * NS + n] : 0.f;
+            c[u] = ib + u < i1 ? bf2f(Cs[(ib + u) * NS + n]) : 0.f;
+            bb[u] = jb + u < i1 ? bf2f(Bs[(jb + u) * NS + n]) : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -161,15 +163,15 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
           const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float c = ib + u < i1 ? Cs[(ib + u) * NS + n] : 0.f;
+            const float c = ib + u < i1 ? bf2f(Cs[(ib + u) * NS + n]) : 0.f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) inter[u][v] = __fmaf_rn(c, hh[v], inter[u][v]);
           }
         }
         const int jmax = ib + 3 < i1 - 1 ? ib + 3 : i1 - 1;
         for (int j = 0; j <= jmax; ++j) {
-          const float4 xv = *reinterpret_cast<const float4*>(&xs[j * P + pb]);
-          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+          const uint2 xr = *reinterpret_cast<const uint2*>(&xs[j * P + pb]);
+          const float xx[4] = {bf16lo(xr.x), bf16hi(xr.x), bf16lo(xr.y), bf16hi(xr.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             if (j > ib + u) continue;  // row ib+u sums j = 0 .. ib+u only
@@ -202,11 +204,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
 #pragma unroll
           for (int v = 0; v < 4; ++v) acc[u][v] = __fmul_rn(eLast, Hs[(nb + u) * P + pb + v]);
         for (int j = 0; j < Q; ++j) {
-          const float4 xv = *reinterpret_cast<const float4*>(&xs[j * P + pb]);
-          const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+          const uint2 xr = *reinterpret_cast<const uint2*>(&xs[j * P + pb]);
+          const float xx[4] = {bf16lo(xr.x), bf16hi(xr.x), bf16lo(xr.y), bf16hi(xr.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float wb = __fmul_rn(dq[j], Bs[j * NS + nb + u]);
+            const float wb = __fmul_rn(dq[j], bf2f(Bs[j * NS + nb + u]));
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(wb, xx[v], acc[u][v]);
           }
@@ -222,11 +224,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
       // the chunk stays open: keep the inputs of the new offsets for the calls that finish it
       for (int e = tid; e < (i1 - i0) * P; e += kSsdThreads) {
         const int i = i0 + e / P, p = e % P;
-        st_x[((int64_t)i * H + h) * P + p] = xs[i * P + p];
+        st_x[((int64_t)i * H + h) * P + p] = bf2f(xs[i * P + p]);
       }
       for (int e = tid; e < (i1 - i0) * N; e += kSsdThreads) {
         const int i = i0 + e / N, n = e % N;
-        st_B[((int64_t)i * H + h) * N + n] = Bs[i * NS + n];
+        st_B[((int64_t)i * H + h) * N + n] = bf2f(Bs[i * NS + n]);
       }
       for (int i = i0 + tid; i < i1; i += kSsdThreads) st_l[(int64_t)i * H + h] = ls[i];
     }
@@ -344,12 +346,13 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
                    "chunk <= 64, state size <= 128 and head size <= 128, each a multiple of 4");
   BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0 && max_q_len >= 1,
              "bad pieces / heads / sequences / max_q_len");
-  const int smem = (int)((size_t)(N * P + 2 * Q * (N + 1) + Q * P + Q * Q + 4 * Q) * sizeof(float));
+  // fp32 state, decayed C.B and the per-offset scalars; bf16 B, C (padded rows) and x
+  auto smem_bytes = [](int q, int n, int p) { return (n * p + q * q + 4 * q) * 4 + (2 * q * (n + 2) + q * p) * 2; };
+  const int smem = smem_bytes(Q, N, P);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    const int mx = (kSsdMaxN * kSsdMaxP + 2 * kSsdMaxQ * (kSsdMaxN + 1) + kSsdMaxQ * kSsdMaxP +
-                    kSsdMaxQ * kSsdMaxQ + 4 * kSsdMaxQ) * (int)sizeof(float);
+  std::call_once(once, [&] {
+    const int mx = smem_bytes(kSsdMaxQ, kSsdMaxN, kSsdMaxP);
     attr_err = cudaFuncSetAttribute(ssd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   });
   if (attr_err != cudaSuccess)
