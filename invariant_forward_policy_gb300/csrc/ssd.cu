@@ -29,6 +29,7 @@ namespace bi {
 
 constexpr int kSsdThreads = 256;
 constexpr int kSsdMaxQ = 64, kSsdMaxN = 128, kSsdMaxP = 128;
+constexpr int kSsdPrefetch = (2 * kSsdMaxQ * kSsdMaxN / 8 + kSsdMaxQ * kSsdMaxP / 8 + kSsdThreads - 1) / kSsdThreads;
 
 struct SsdArgs {
   const __nv_bfloat16* x;  // [T, H, P]
@@ -52,7 +53,7 @@ __host__ __device__ inline int64_t ssd_store_floats(int H, int /*G*/, int P, int
   return (int64_t)H * N * P + (int64_t)Q * H * N + (int64_t)Q * H * P + (int64_t)Q * H;
 }
 
-__global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) {
+__global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs a) {
   extern __shared__ __align__(16) float sm[];
   const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
   // B, C and x hold bf16 values (inputs, or their exact copies in the store):
@@ -89,9 +90,58 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
   for (int i = tid; i < N * P; i += kSsdThreads) Hs[i] = st_H[i];
   bool advanced = false;  // some chunk completed in this call: the stored state changes
   const int64_t c_first = p0 / Q, c_last = (p1 - 1) / Q;
+  // The next chunk's B, C and x (16-byte vectors: B rows, C rows, x rows) are
+  // loaded into registers while the current chunk computes; with N and P
+  // multiples of 8 (else every chunk is staged directly).
+  const bool vec = N % 8 == 0 && P % 8 == 0;
+  const int vb = Q * N / 8, vx = Q * P / 8;  // vectors of B (and of C), of x
+  uint4 pf[kSsdPrefetch];
+  auto prefetch = [&](int64_t c) {
+    const int64_t cs = c * Q;
+    const int i1 = (int)((p1 < cs + Q ? p1 : cs + Q) - cs);  // chunks after the first start at offset 0
+#pragma unroll
+    for (int k = 0; k < kSsdPrefetch; ++k) {
+      const int v = tid + k * kSsdThreads;
+      if (v < 2 * vb) {
+        const int w = v < vb ? v : v - vb, i = w / (N / 8), j = w % (N / 8);
+        if (i < i1) {
+          const int64_t r = row0 + (cs + i - p0);
+          pf[k] = __ldg(reinterpret_cast<const uint4*>((v < vb ? a.B : a.C) + (r * G + g) * N) + j);
+        }
+      } else if (v < 2 * vb + vx) {
+        const int w = v - 2 * vb, i = w / (P / 8), j = w % (P / 8);
+        if (i < i1) {
+          const int64_t r = row0 + (cs + i - p0);
+          pf[k] = __ldg(reinterpret_cast<const uint4*>(a.x + (r * (int64_t)H + h) * P) + j);
+        }
+      }
+    }
+  };
+  auto place = [&](int i1) {  // the prefetched vectors into Bs, Cs, xs
+#pragma unroll
+    for (int k = 0; k < kSsdPrefetch; ++k) {
+      const int v = tid + k * kSsdThreads;
+      if (v < 2 * vb) {
+        const int w = v < vb ? v : v - vb, i = w / (N / 8), j = w % (N / 8);
+        if (i < i1) {
+          uint32_t* d = reinterpret_cast<uint32_t*>((v < vb ? Bs : Cs) + i * NS + j * 8);
+          d[0] = pf[k].x;
+          d[1] = pf[k].y;
+          d[2] = pf[k].z;
+          d[3] = pf[k].w;
+        }
+      } else if (v < 2 * vb + vx) {
+        const int w = v - 2 * vb, i = w / (P / 8), j = w % (P / 8);
+        if (i < i1) *reinterpret_cast<uint4*>(xs + i * P + j * 8) = pf[k];
+      }
+    }
+  };
   for (int64_t c = c_first; c <= c_last; ++c) {
     const int64_t cs = c * Q;
     const int i0 = (int)((p0 > cs ? p0 : cs) - cs), i1 = (int)((p1 < cs + Q ? p1 : cs + Q) - cs);
+    if (vec && c > c_first) {
+      place(i1);  // i0 == 0 here
+    } else {
     // chunk inputs: earlier offsets from the store (first chunk of the call only), new ones from the call
     for (int e = tid; e < i1 * N; e += kSsdThreads) {
       const int i = e / N, n = e % N;
@@ -108,9 +158,11 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_scan_kernel(const SsdArgs a) 
       xs[e] = i < i0 ? f2bf(st_x[((int64_t)i * H + h) * P + p])
                      : a.x[((row0 + (cs + i - p0)) * (int64_t)H + h) * P + p];
     }
+    }
     for (int i = tid; i < i1; i += kSsdThreads)
       ls[i] = i < i0 ? st_l[(int64_t)i * H + h] : a.loga[(row0 + (cs + i - p0)) * (int64_t)H + h];
     __syncthreads();
+    if (vec && c < c_last) prefetch(c + 1);  // in flight while this chunk computes
     if (tid == 0) {
       float acc = 0.f;
       for (int i = 0; i < i1; ++i) {
