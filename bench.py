@@ -850,6 +850,15 @@ def run_kernel_case(name: str, reps: int):
         nvd = torch.from_numpy(nv).to(dev)
         for _ in range(reps):
             bi.bi_topk(S, T, ld, nvd, 2048, idx)
+    elif name == "topk_prefill":
+        # deterministic Top-K, K = 2048, a 2048-row prefill chunk at positions 30K-32K (one CTA per row)
+        nv = np.arange(30721, 32769, dtype=np.int32)
+        T, ld = len(nv), int(nv.max())
+        S = torch.randn((T, ld), device=dev)
+        idx = torch.empty((T, 2048), dtype=torch.int32, device=dev)
+        nvd = torch.from_numpy(nv).to(dev)
+        for _ in range(reps):
+            bi.bi_topk(S, T, ld, nvd, 2048, idx)
     elif name == "ssd_prefill":
         # Mamba-2 chunked scan: 16 sequences x 2048, 32 heads x 64, state 128, 8 groups, chunk 64
         n_seq, per, Hs, Gs, Ps, Ns, Qs = 16, 2048, 32, 8, 64, 128, 64
@@ -930,7 +939,7 @@ def main():
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
-                         "kv_fp8_gather, c5_decode) or "
+                         "kv_fp8_gather, c5_decode, topk_prefill) or "
                          "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
