@@ -102,3 +102,19 @@ def test_topk_row_and_cluster_schedules_agree():
     fast = _run(S, n, K, bi.BI_FAST)
     for t in range(0, T, 37):
         assert np.array_equal(np.sort(S[t][full[t][full[t] >= 0]]), np.sort(S[t][fast[t][fast[t] >= 0]]))
+
+
+@pytest.mark.parametrize("dist", ["normal", "coarse", "bf16_ties"])
+def test_topk_row_kernel_long_rows(dist):
+    """One CTA per row over 32K-position rows: the kept-candidate passes (normal
+    scores: the first byte's candidates fit in shared memory) and the full-row
+    fallback (coarse scores: most keys share a byte) both give the oracle's result."""
+    rng = np.random.default_rng(len(dist) + 99)
+    T, ld, K = 320, 32768, 2048
+    S = _scores(rng, T, ld, dist)
+    n = rng.integers(K, ld + 1, T)
+    n[:3] = [ld, K, K + 1]
+    got = _run(S, n, K)
+    rows = np.r_[0:3, rng.choice(np.arange(3, T), 29, replace=False)]
+    assert np.array_equal(got[rows], otk.topk(S[rows], n[rows], K))
+    assert bi.bi_device_status() == 0
