@@ -58,12 +58,14 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
   const int Q = a.Q, N = a.N, P = a.P, H = a.H, G = a.G;
   // B, C and x hold bf16 values (inputs, or their exact copies in the store):
   // staged as bf16 and widened exactly on use, so that two CTAs share an SM
-  const int NS = N + 2;                      // padded bf16 row stride of B and C: conflict-free column walks
+  // B and C are kept transposed, [n][offset] with row stride QS: a thread's four
+  // offsets at one n are one 8-byte load, and a warp's 16 row blocks hit distinct banks
+  const int QS = Q + 4;
   float* Hs = sm;                            // [N][P] state entering the chunk
   float* Gm = Hs + N * P;                    // [Q][Q] (C_i . B_j) scaled by the decay
-  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(Gm + Q * Q);  // [Q][NS]
-  __nv_bfloat16* Cs = Bs + Q * NS;                                   // [Q][NS]
-  __nv_bfloat16* xs = Cs + Q * NS;                                   // [Q][P]
+  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(Gm + Q * Q);  // [N][QS]
+  __nv_bfloat16* Cs = Bs + N * QS;                                   // [N][QS]
+  __nv_bfloat16* xs = Cs + N * QS;                                   // [Q][P]
   float* ls = reinterpret_cast<float*>(xs + Q * P);                  // [Q] loga
   float* Ls = ls + Q;             // [Q] cumulative
   float* eL = Ls + Q;             // [Q] exp(L_i)
@@ -92,7 +94,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
   const int64_t c_first = p0 / Q, c_last = (p1 - 1) / Q;
   // The next chunk's B, C and x (16-byte vectors: B rows, C rows, x rows) are
   // loaded into registers while the current chunk computes; with N and P
-  // multiples of 8 (else every chunk is staged directly).
+  // multiples of 8 (else every chunk is staged directly).  A warp loads whole
+  // rows: that measured faster than 16-row groups, whose transposed stores into
+  // shared memory would be conflict-free but whose loads span 16 rows.
   const bool vec = N % 8 == 0 && P % 8 == 0;
   const int vb = Q * N / 8, vx = Q * P / 8;  // vectors of B (and of C), of x
   uint4 pf[kSsdPrefetch];
@@ -124,11 +128,11 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
       if (v < 2 * vb) {
         const int w = v < vb ? v : v - vb, i = w / (N / 8), j = w % (N / 8);
         if (i < i1) {
-          uint32_t* d = reinterpret_cast<uint32_t*>((v < vb ? Bs : Cs) + i * NS + j * 8);
-          d[0] = pf[k].x;
-          d[1] = pf[k].y;
-          d[2] = pf[k].z;
-          d[3] = pf[k].w;
+          __nv_bfloat16* d = (v < vb ? Bs : Cs) + (j * 8) * QS + i;
+          const uint32_t wd[4] = {pf[k].x, pf[k].y, pf[k].z, pf[k].w};
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            d[t * QS] = __ushort_as_bfloat16((unsigned short)(wd[t >> 1] >> (16 * (t & 1))));
         }
       } else if (v < 2 * vb + vx) {
         const int w = v - 2 * vb, i = w / (P / 8), j = w % (P / 8);
@@ -146,11 +150,11 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
     for (int e = tid; e < i1 * N; e += kSsdThreads) {
       const int i = e / N, n = e % N;
       if (i < i0) {
-        Bs[i * NS + n] = f2bf(st_B[((int64_t)i * H + h) * N + n]);  // a bf16 value: exact
+        Bs[n * QS + i] = f2bf(st_B[((int64_t)i * H + h) * N + n]);  // a bf16 value: exact
       } else {
         const int64_t r = row0 + (cs + i - p0);
-        Bs[i * NS + n] = a.B[(r * G + g) * N + n];
-        Cs[i * NS + n] = a.C[(r * G + g) * N + n];
+        Bs[n * QS + i] = a.B[(r * G + g) * N + n];
+        Cs[n * QS + i] = a.C[(r * G + g) * N + n];
       }
     }
     for (int e = tid; e < i1 * P; e += kSsdThreads) {
@@ -176,19 +180,19 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
       if (i1 == Q) dq[i] = expf(__fsub_rn(Ls[Q - 1], Ls[i]));
     }
     // decay-scaled (C_i . B_j) for the rows this call computes; 4 x 4 tiles of (i, j)
+    // (row tiles start at a multiple of 4: rows below i0 are computed and dropped)
+    const int ia = i0 & ~3;
     {
-      const int ni = (i1 - i0 + 3) / 4, nj = (i1 + 3) / 4;
+      const int ni = (i1 - ia + 3) / 4, nj = (i1 + 3) / 4;
       for (int e = tid; e < ni * nj; e += kSsdThreads) {
-        const int ib = i0 + (e / nj) * 4, jb = (e % nj) * 4;
+        const int ib = ia + (e / nj) * 4, jb = (e % nj) * 4;
         if (jb > ib + 3) continue;  // above the diagonal
         float acc[4][4] = {};
         for (int n = 0; n < N; ++n) {
-          float c[4], bb[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            c[u] = ib + u < i1 ? bf2f(Cs[(ib + u) * NS + n]) : 0.f;
-            bb[u] = jb + u < i1 ? bf2f(Bs[(jb + u) * NS + n]) : 0.f;
-          }
+          const uint2 cw = *reinterpret_cast<const uint2*>(Cs + n * QS + ib);
+          const uint2 bw = *reinterpret_cast<const uint2*>(Bs + n * QS + jb);
+          const float c[4] = {bf16lo(cw.x), bf16hi(cw.x), bf16lo(cw.y), bf16hi(cw.y)};
+          const float bb[4] = {bf16lo(bw.x), bf16hi(bw.x), bf16lo(bw.y), bf16hi(bw.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -199,26 +203,26 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int i = ib + u, j = jb + v;
-            if (i < i1 && j <= i) Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), acc[u][v]);
+            if (i >= i0 && i < i1 && j <= i) Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), acc[u][v]);
           }
       }
     }
     __syncthreads();
     // rows: 4 x 4 tiles of (i, p)
     {
-      const int ni = (i1 - i0 + 3) / 4, np4 = P / 4;
+      const int ni = (i1 - ia + 3) / 4, np4 = P / 4;
       for (int e = tid; e < ni * np4; e += kSsdThreads) {
-        const int ib = i0 + (e / np4) * 4, pb = (e % np4) * 4;
+        const int ib = ia + (e / np4) * 4, pb = (e % np4) * 4;
         float inter[4][4] = {}, intra[4][4] = {};
         for (int n = 0; n < N; ++n) {
           const float4 hv = *reinterpret_cast<const float4*>(&Hs[n * P + pb]);
           const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
+          const uint2 cw = *reinterpret_cast<const uint2*>(Cs + n * QS + ib);
+          const float c4[4] = {bf16lo(cw.x), bf16hi(cw.x), bf16lo(cw.y), bf16hi(cw.y)};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float c = ib + u < i1 ? bf2f(Cs[(ib + u) * NS + n]) : 0.f;
+          for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) inter[u][v] = __fmaf_rn(c, hh[v], inter[u][v]);
-          }
+            for (int v = 0; v < 4; ++v) inter[u][v] = __fmaf_rn(c4[u], hh[v], inter[u][v]);
         }
         const int jmax = ib + 3 < i1 - 1 ? ib + 3 : i1 - 1;
         for (int j = 0; j <= jmax; ++j) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = ib + u;
-          if (i >= i1) continue;
+          if (i < i0 || i >= i1) continue;
           const int64_t r = row0 + (cs + i - p0);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
           const float xx[4] = {bf16lo(xr.x), bf16hi(xr.x), bf16lo(xr.y), bf16hi(xr.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float wb = __fmul_rn(dq[j], bf2f(Bs[j * NS + nb + u]));
+            const float wb = __fmul_rn(dq[j], bf2f(Bs[(nb + u) * QS + j]));
 #pragma unroll
             for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(wb, xx[v], acc[u][v]);
           }
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
       }
       for (int e = tid; e < (i1 - i0) * N; e += kSsdThreads) {
         const int i = i0 + e / N, n = e % N;
-        st_B[((int64_t)i * H + h) * N + n] = bf2f(Bs[i * NS + n]);
+        st_B[((int64_t)i * H + h) * N + n] = bf2f(Bs[n * QS + i]);
       }
       for (int i = i0 + tid; i < i1; i += kSsdThreads) st_l[(int64_t)i * H + h] = ls[i];
     }
@@ -398,8 +402,8 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
                    "chunk <= 64, state size <= 128 and head size <= 128, each a multiple of 4");
   BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0 && max_q_len >= 1,
              "bad pieces / heads / sequences / max_q_len");
-  // fp32 state, decayed C.B and the per-offset scalars; bf16 B, C (padded rows) and x
-  auto smem_bytes = [](int q, int n, int p) { return (n * p + q * q + 4 * q) * 4 + (2 * q * (n + 2) + q * p) * 2; };
+  // fp32 state, decayed C.B and the per-offset scalars; bf16 B, C (transposed, padded) and x
+  auto smem_bytes = [](int q, int n, int p) { return (n * p + q * q + 4 * q) * 4 + (2 * n * (q + 4) + q * p) * 2; };
   const int smem = smem_bytes(Q, N, P);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
