@@ -62,8 +62,9 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
   // offsets at one n are one 8-byte load, and a warp's 16 row blocks hit distinct banks
   const int QS = Q + 4;
   float* Hs = sm;                            // [N][P] state entering the chunk
-  float* Gm = Hs + N * P;                    // [Q][Q] (C_i . B_j) scaled by the decay
-  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(Gm + Q * Q);  // [N][QS]
+  const int GS = Q + 1;                      // Gm row stride: rows ib and ib + 4 on different banks
+  float* Gm = Hs + N * P;                    // [Q][GS] (C_i . B_j) scaled by the decay
+  __nv_bfloat16* Bs = reinterpret_cast<__nv_bfloat16*>(Gm + Q * GS);  // [N][QS]
   __nv_bfloat16* Cs = Bs + N * QS;                                   // [N][QS]
   __nv_bfloat16* xs = Cs + N * QS;                                   // [Q][P]
   float* ls = reinterpret_cast<float*>(xs + Q * P);                  // [Q] loga
@@ -128,11 +129,30 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
       if (v < 2 * vb) {
         const int w = v < vb ? v : v - vb, i = w / (N / 8), j = w % (N / 8);
         if (i < i1) {
+          // the vector's 8 values go to 8 rows n of the transposed array; lanes
+          // start at different rows (r = (j / 2) mod 8) so that a warp's 2-byte
+          // stores of one step fall on distinct banks: rotate the values by r first
           __nv_bfloat16* d = (v < vb ? Bs : Cs) + (j * 8) * QS + i;
-          const uint32_t wd[4] = {pf[k].x, pf[k].y, pf[k].z, pf[k].w};
+          const int r = (j >> 1) & 7;
+          uint32_t w0 = pf[k].x, w1 = pf[k].y, w2 = pf[k].z, w3 = pf[k].w, t0;
+          if (r & 2) {  // by one word
+            t0 = w0; w0 = w1; w1 = w2; w2 = w3; w3 = t0;
+          }
+          if (r & 4) {  // by two words
+            t0 = w0; w0 = w2; w2 = t0;
+            t0 = w1; w1 = w3; w3 = t0;
+          }
+          if (r & 1) {  // by one value
+            t0 = w0;
+            w0 = __funnelshift_r(w0, w1, 16);
+            w1 = __funnelshift_r(w1, w2, 16);
+            w2 = __funnelshift_r(w2, w3, 16);
+            w3 = __funnelshift_r(w3, t0, 16);
+          }
+          const uint32_t wd[4] = {w0, w1, w2, w3};
 #pragma unroll
-          for (int t = 0; t < 8; ++t)
-            d[t * QS] = __ushort_as_bfloat16((unsigned short)(wd[t >> 1] >> (16 * (t & 1))));
+          for (int t = 0; t < 8; ++t)  // wd's value t is the vector's value (t + r) mod 8
+            d[((t + r) & 7) * QS] = __ushort_as_bfloat16((unsigned short)(wd[t >> 1] >> (16 * (t & 1))));
         }
       } else if (v < 2 * vb + vx) {
         const int w = v - 2 * vb, i = w / (P / 8), j = w % (P / 8);
@@ -203,7 +223,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int i = ib + u, j = jb + v;
-            if (i >= i0 && i < i1 && j <= i) Gm[i * Q + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), acc[u][v]);
+            if (i >= i0 && i < i1 && j <= i) Gm[i * GS + j] = __fmul_rn(expf(__fsub_rn(Ls[i], Ls[j])), acc[u][v]);
           }
       }
     }
@@ -231,7 +251,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             if (j > ib + u) continue;  // row ib+u sums j = 0 .. ib+u only
-            const float gm = Gm[(ib + u) * Q + j];
+            const float gm = Gm[(ib + u) * GS + j];
 #pragma unroll
             for (int v = 0; v < 4; ++v) intra[u][v] = __fmaf_rn(gm, xx[v], intra[u][v]);
           }
@@ -403,7 +423,9 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
   BI_REQUIRE(pieces <= 0x7fffffff && H <= 65535 && n_seq > 0 && max_q_len >= 1,
              "bad pieces / heads / sequences / max_q_len");
   // fp32 state, decayed C.B and the per-offset scalars; bf16 B, C (transposed, padded) and x
-  auto smem_bytes = [](int q, int n, int p) { return (n * p + q * q + 4 * q) * 4 + (2 * n * (q + 4) + q * p) * 2; };
+  auto smem_bytes = [](int q, int n, int p) {
+    return (n * p + q * (q + 1) + 4 * q) * 4 + (2 * n * (q + 4) + q * p) * 2;
+  };
   const int smem = smem_bytes(Q, N, P);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
