@@ -22,6 +22,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -245,8 +246,11 @@ def run_ours(args):
 
     results = []
     barrier()
-    with Clocks(os.path.join(ROOT, "gpurun_out", "clocks_bench.csv") if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                else "/tmp/clocks_bench.csv") as ck:
+    clocks_path = args.clocks_csv
+    if not clocks_path:
+        fd, clocks_path = tempfile.mkstemp(prefix="clocks_bench_", suffix=".csv")
+        os.close(fd)
+    with Clocks(clocks_path) as ck:
         t_inv = timed(ep, args.steps, results, "invariant")
         t_fast = timed(ep_fast, args.steps, None, "fast")
     barrier()
@@ -950,6 +954,8 @@ def main():
     ap.add_argument("--no-kernels", action="store_true", help="skip the per-kernel rate table")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' timed units")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi samples of the timed region in this file (default: a temporary file)")
     args = ap.parse_args()
     if args.kernel_case:
         run_kernel_case(args.kernel_case, args.reps)
