@@ -58,6 +58,23 @@ __device__ __forceinline__ float norm_inv(float t, int d, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
 }
 
+// inv of a row from each thread's own sum of squares: the warps' butterflies,
+// then thread 0 adds the warp sums in warp order.  Every thread of the block
+// calls it; warp_ss holds blockDim / 32 floats, s_inv one.
+__device__ __forceinline__ float norm_row_inv(float ss, int d, float eps, float* warp_ss, float* s_inv) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  ss = norm_warp_sum(ss);
+  if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int w = 0; w < nthr / 32; ++w) t += warp_ss[w];
+    *s_inv = norm_inv(t, d, eps);
+  }
+  __syncthreads();
+  return *s_inv;
+}
+
 // y = bf16((r * inv) * g) of one vector
 __device__ __forceinline__ uint4 norm_apply(const uint4& r, const uint4& g, float inv) {
   const uint32_t* pa = reinterpret_cast<const uint32_t*>(&r);

@@ -50,18 +50,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
     }
   }
   // fixed xor-butterfly inside the warp, then warps summed in index order
-  ss = norm_warp_sum(ss);
   __shared__ float warp_ss[8];
   __shared__ float s_inv;
-  if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int w = 0; w < nthr / 32; ++w) t += warp_ss[w];
-    s_inv = norm_inv(t, d, eps);
-  }
-  __syncthreads();
-  const float inv = s_inv;
+  const float inv = norm_row_inv(ss, d, eps, warp_ss, &s_inv);
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
 #pragma unroll
   for (int i = 0; i < kMaxVec; ++i) {
