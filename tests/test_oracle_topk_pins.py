@@ -2,6 +2,8 @@
 the pages' own two-way tie example, closed forms, brute force on tiny rows, and an
 independent restatement through the 64-bit (score, position) key the pages describe."""
 import itertools
+import json
+import os
 
 import numpy as np
 import pytest
@@ -25,13 +27,28 @@ def _topk_by_key(scores, n, k):
     return np.concatenate([pos, -np.ones(k - len(pos), np.int64)]).astype(np.int32)
 
 
+def golden_tie_cases():
+    """The pages' two-way tie example (tests/golden/topk_tie_example.json, with its
+    citation): (scores, n_valid, k, want) per case."""
+    with open(os.path.join(os.path.dirname(__file__), "golden", "topk_tie_example.json")) as f:
+        g = json.load(f)
+    out = []
+    for c in g["cases"]:
+        s = np.full(max(64, c["n_valid"]), c["default"], np.float32)
+        for p, v in c["scores"].items():
+            s[int(p)] = v
+        out.append((s, c["n_valid"], c["k"], c["want"]))
+    return out
+
+
 def test_pages_tie_example_selects_larger_position():
-    # K = 2; positions 17 and 42 tie for second place: the position bits select 42,
-    # and the output lists selected positions by descending position.
-    s = np.full(64, -1.0, np.float32)
-    s[5], s[17], s[42] = 3.0, 2.0, 2.0
-    assert otk.topk_row(s, 64, 2).tolist() == [42, 5]
-    assert otk.topk_row(s, 64, 3).tolist() == [42, 17, 5]
+    # K = 2; positions 17 and 42 tie: the position bits select 42, and the output
+    # lists selected positions by descending position, invalid entries last
+    cases = golden_tie_cases()
+    assert len(cases) >= 2 and cases[0][3] == [42, 5]
+    for s, n, k, want in cases:
+        assert otk.topk_row(s, n, k).tolist() == want, (n, k)
+        assert _topk_by_key(s, n, k).tolist() == want, (n, k)
 
 
 def test_fewer_candidates_than_k_pads_with_invalid_last():

@@ -49,6 +49,22 @@ def test_topk_matches_oracle(dist, T, ld, K):
     assert bi.bi_device_status() == 0
 
 
+def test_topk_pages_tie_example():
+    """The pages' two-way tie example, every case of the golden fixture in one batch."""
+    from tests.test_oracle_topk_pins import golden_tie_cases
+    cases = golden_tie_cases()
+    ld = max(len(c[0]) for c in cases)
+    K = max(c[2] for c in cases)
+    S = np.full((len(cases), ld), -1.0, np.float32)
+    for t, (s, n, k, want) in enumerate(cases):
+        S[t, :len(s)] = s
+    n = np.array([c[1] for c in cases])
+    for t, (s, nv, k, want) in enumerate(cases):
+        got = _run(S[t:t + 1], n[t:t + 1], k)
+        assert got[0].tolist() == want, (t, got[0].tolist(), want)
+    assert bi.bi_device_status() == 0
+
+
 def test_topk_edge_rows():
     S = np.full((5, 4096), 0.5, np.float32)
     n = np.array([0, 1, 4096, 2047, 2048])
