@@ -112,3 +112,33 @@ def test_ssd_validation_without_gpu():
     assert lib.bi_ssd_chunk_scan(*args, 4, 2, 64, 256, 64, 16, 1, 16, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_ssd_chunk_scan(*args, 4, 3, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_ssd_chunk_scan(None, 16, 16, 16, 16, 16, 16, 0, 1, 4, 2, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_OK
+
+
+def test_product_path_does_not_reach_the_oracle():
+    """The package (binding, decoder, build) imports neither the oracle nor the
+    input generators: every step of the path runs in libbi.so (numpy serves the
+    host bookkeeping only: index arrays, block tables)."""
+    import ast
+    pkg = os.path.join(ROOT, "invariant_forward_policy_gb300")
+    for f in sorted(os.listdir(pkg)):
+        if not f.endswith(".py"):
+            continue
+        tree = ast.parse(open(os.path.join(pkg, f)).read())
+        for node in ast.walk(tree):
+            names = []
+            if isinstance(node, ast.Import):
+                names = [a.name for a in node.names]
+            elif isinstance(node, ast.ImportFrom) and node.level == 0:
+                names = [node.module or ""]
+            for n in names:
+                assert n.split(".")[0] not in ("oracle", "synthetic"), (f, n)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without libbi.so the first call raises; nothing falls back to the CPU."""
+    monkeypatch.setattr(_lib, "_L", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libbi.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.load()
+    with pytest.raises(RuntimeError):
+        bi.bi_version()
