@@ -313,8 +313,8 @@ bi_status bi_attention_fp8(const void* q, int64_t T, const int32_t* piece_seq, c
  * each sequence's pieces passed in position order over successive calls;
  * max_q_len (host) bounds the rows of any piece, and calls with max_q_len = 1
  * (decode steps) run a lighter schedule of the same arithmetic.
- * state: fp32, bi_ssd_state_bytes(H, G, P, N, Q) bytes per sequence
- * (n_seq of them), zeroed by the caller for a new sequence; it holds the state
+ * state: fp32, 16-byte aligned, bi_ssd_state_bytes(H, G, P, N, Q) bytes per
+ * sequence (n_seq of them), zeroed by the caller for a new sequence; it holds the state
  * entering the current chunk and that chunk's earlier inputs.  y: fp32
  * [T, H, P].  Q <= 64, N <= 128, P <= 128, each a multiple of 4.  BI_FAST
  * runs the same kernel. */

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kSsdThreads, 2) ssd_scan_kernel(const SsdArgs 
 // arithmetic as ssd_scan_kernel, term for term and in the same order, with the
 // entering state and the chunk's earlier inputs read straight from the store
 // instead of staged in shared memory, so that many CTAs share an SM.
-__global__ void __launch_bounds__(128) ssd_step_kernel(const SsdArgs a) {
+__global__ void __launch_bounds__(128, 8) ssd_step_kernel(const SsdArgs a) {
   __shared__ float c_s[kSsdMaxN], gm[kSsdMaxQ], Ls[kSsdMaxQ], dq[kSsdMaxQ], b_s[kSsdMaxN], x_s[kSsdMaxP];
   __shared__ float l_s[kSsdMaxQ];
   pdl_trigger();
@@ -380,16 +380,39 @@ __global__ void __launch_bounds__(128) ssd_step_kernel(const SsdArgs a) {
   if (i == Q - 1) {
     // the position completes its chunk: the exit state replaces the stored one
     __syncthreads();  // every thread has read st_H for its row
+    // 4 x 4 tiles of (n, p), each element's terms in ascending j as in the scan
+    // kernel; a tile reads 4 B and 4 x values per j as two 16-byte loads
     const float eLast = eLi;
-    for (int e = tid; e < N * P; e += 128) {
-      const int n = e / P, p = e % P;
-      float acc = __fmul_rn(eLast, st_H[e]);
+    const int nn4 = N / 4, np4 = P / 4;
+    for (int e = tid; e < nn4 * np4; e += 128) {
+      const int nb = (e / np4) * 4, pb = (e % np4) * 4;
+      float acc[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[u][v] = __fmul_rn(eLast, st_H[(nb + u) * P + pb + v]);
       for (int j = 0; j < Q; ++j) {
-        const float bjn = j < i ? st_B[((int64_t)j * H + h) * N + n] : b_s[n];
-        const float xjp = j < i ? st_x[((int64_t)j * H + h) * P + p] : x_s[p];
-        acc = __fmaf_rn(__fmul_rn(dq[j], bjn), xjp, acc);
+        float4 bv, xv;
+        if (j < i) {
+          bv = *reinterpret_cast<const float4*>(st_B + ((int64_t)j * H + h) * N + nb);
+          xv = *reinterpret_cast<const float4*>(st_x + ((int64_t)j * H + h) * P + pb);
+        } else {
+          bv = make_float4(b_s[nb], b_s[nb + 1], b_s[nb + 2], b_s[nb + 3]);
+          xv = make_float4(x_s[pb], x_s[pb + 1], x_s[pb + 2], x_s[pb + 3]);
+        }
+        const float bb[4] = {bv.x, bv.y, bv.z, bv.w}, xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float wb = __fmul_rn(dq[j], bb[u]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[u][v] = __fmaf_rn(wb, xx[v], acc[u][v]);
+        }
       }
-      st_H[e] = acc;  // each element is read and written by its own thread only
+      // each element is read and written by its own thread only
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) st_H[(nb + u) * P + pb + v] = acc[u][v];
     }
   } else {
     for (int n = tid; n < N; n += 128) st_B[((int64_t)i * H + h) * N + n] = b_s[n];
@@ -417,6 +440,7 @@ bi_status bi_ssd_chunk_scan(const void* x, const void* B, const void* C, const f
   if (pieces == 0) return BI_OK;
   BI_REQUIRE(x && B && C && loga && piece_seq && piece_row0 && piece_pos0 && state && y, "null pointer");
   BI_REQUIRE(H > 0 && G > 0 && H % G == 0, "H must be a positive multiple of G");
+  BI_REQUIRE(aligned16(state), "state must be 16-byte aligned");
   BI_REQUIRE_SHAPE(Q >= 4 && Q <= kSsdMaxQ && Q % 4 == 0 && N >= 4 && N <= kSsdMaxN && N % 4 == 0 && P >= 4 &&
                        P <= kSsdMaxP && P % 4 == 0,
                    "chunk <= 64, state size <= 128 and head size <= 128, each a multiple of 4");

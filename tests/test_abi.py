@@ -112,6 +112,8 @@ def test_ssd_validation_without_gpu():
     assert lib.bi_ssd_chunk_scan(*args, 4, 2, 64, 256, 64, 16, 1, 16, 0, None) == bi.BI_ERR_UNSUPPORTED_SHAPE
     assert lib.bi_ssd_chunk_scan(*args, 4, 3, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_ERR_INVALID_ARG
     assert lib.bi_ssd_chunk_scan(None, 16, 16, 16, 16, 16, 16, 0, 1, 4, 2, 64, 128, 64, 16, 1, 16, 0, None) == bi.BI_OK
+    misaligned = [16, 16, 16, 16, 16, 16, 16, 1, 1, 4, 2, 64, 128, 64, 20, 1, 16, 0, None]   # state at byte 20
+    assert lib.bi_ssd_chunk_scan(*misaligned) == bi.BI_ERR_INVALID_ARG
 
 
 def test_product_path_does_not_reach_the_oracle():
