@@ -27,6 +27,67 @@ def _bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
     return t.to(device)
 
 
+# ------------------------------------------------------------ host bookkeeping
+def block_ids(n_seq: int, max_blocks: int, seed: int | None = None, base: int = 0) -> np.ndarray:
+    """Physical block ids [n_seq, max_blocks] (int32): base .. base + n_seq * max_blocks - 1,
+    scattered over the cache by a seeded permutation (in order when seed is None)."""
+    n = n_seq * max_blocks
+    ids = np.arange(n, dtype=np.int32) + base
+    if seed is not None:
+        ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
+    return ids.reshape(n_seq, max_blocks)
+
+
+def paged_block_ids(ctx_lens, max_blocks: int, seed: int | None = None):
+    """Block table giving sequence b only ceil(ctx_lens[b] / 64) physical blocks
+    (entries past that are -1), scattered over the cache by a seeded permutation.
+    Returns (table [n_seq, max_blocks] int32, n_blocks)."""
+    need = [-(-int(n) // 64) for n in ctx_lens]
+    total = int(sum(need))
+    ids = np.arange(total, dtype=np.int32)
+    if seed is not None:
+        ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
+    tab = np.full((len(need), max_blocks), -1, dtype=np.int32)
+    o = 0
+    for b, n in enumerate(need):
+        tab[b, :n] = ids[o:o + n]
+        o += n
+    return tab, total
+
+
+def recompute_pack(prompts, gens, order):
+    """The training side's packed batch, sequence by sequence in `order`: tokens
+    [prompt, gen[:-1]], targets (gen from row len(prompt) - 1 on, 0 before) and the
+    first scored row len(prompt) - 1."""
+    seqs, tg, lf = [], [], []
+    for b in order:
+        p = np.asarray(prompts[b], np.int32)
+        g = np.asarray(gens[b], np.int32)
+        s = np.concatenate([p, g[:-1]])
+        t = np.zeros(len(s), np.int32)
+        t[len(p) - 1:] = g
+        seqs.append(s)
+        tg.append(t)
+        lf.append(len(p) - 1)
+    return seqs, tg, lf
+
+
+def recompute_rows(prompt_lens, n_gen: int):
+    """Rows of the same packed batch on static buffers, sequences in order: cu
+    (B + 1 offsets), p_dst (the prompts' rows, concatenated), g_dst [B, n_gen - 1]
+    (the rows of the fed-back generated tokens; None when n_gen == 1) and t_dst
+    [B, n_gen] (the rows whose target is generated token k)."""
+    lens = np.asarray(prompt_lens, dtype=np.int64)
+    cu = np.concatenate([[0], np.cumsum(lens + n_gen - 1)])
+    pd, gd, td = [], [], []
+    for b in range(len(lens)):
+        o = cu[b]
+        pd.append(o + np.arange(lens[b]))
+        gd.append(o + lens[b] + np.arange(n_gen - 1))
+        td.append(o + lens[b] - 1 + np.arange(n_gen))
+    return cu, np.concatenate(pd), (np.stack(gd) if n_gen > 1 else None), np.stack(td)
+
+
 @dataclasses.dataclass
 class KVCache:
     k: torch.Tensor
@@ -110,26 +171,13 @@ class Decoder:
 
     def block_table(self, n_seq: int, max_blocks: int, seed: int | None = None, base: int = 0) -> torch.Tensor:
         """Physical blocks for n_seq sequences; a seeded permutation scatters them over the cache."""
-        n = n_seq * max_blocks
-        ids = np.arange(n, dtype=np.int32) + base
-        if seed is not None:
-            ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
-        return torch.from_numpy(ids.reshape(n_seq, max_blocks)).to(self.device)
+        return torch.from_numpy(block_ids(n_seq, max_blocks, seed, base)).to(self.device)
 
     def paged_block_table(self, ctx_lens, max_blocks: int, seed: int | None = None):
         """Block table giving sequence b only ceil(ctx_lens[b] / 64) physical blocks
         (entries past that are -1 and never touched), scattered over the cache by a
         seeded permutation.  Returns (table [n_seq, max_blocks] int32, n_blocks)."""
-        need = [-(-int(n) // 64) for n in ctx_lens]
-        total = int(sum(need))
-        ids = np.arange(total, dtype=np.int32)
-        if seed is not None:
-            ids = np.random.default_rng(seed).permutation(ids).astype(np.int32)
-        tab = np.full((len(need), max_blocks), -1, dtype=np.int32)
-        o = 0
-        for b, n in enumerate(need):
-            tab[b, :n] = ids[o:o + n]
-            o += n
+        tab, total = paged_block_ids(ctx_lens, max_blocks, seed)
         return torch.from_numpy(tab).to(self.device), total
 
     def workspace(self, max_tokens, max_pieces, max_ctx, max_logit_rows, mode=L.BI_INVARIANT) -> torch.Tensor:
@@ -226,15 +274,7 @@ class Decoder:
         B = len(prompts)
         order = list(range(B)) if order is None else list(order)
         gens = [np.asarray(g, np.int32) for g in gens]
-        seqs, tg, lf = [], [], []
-        for b in order:
-            p = np.asarray(prompts[b], np.int32)
-            s = np.concatenate([p, gens[b][:-1]])
-            t = np.zeros(len(s), np.int32)
-            t[len(p) - 1:] = gens[b]
-            seqs.append(s)
-            tg.append(t)
-            lf.append(len(p) - 1)
+        seqs, tg, lf = recompute_pack(prompts, gens, order)
         bt = block_table[torch.as_tensor(order, device=block_table.device)]
         lp, _, cu = self.prefill(seqs, cache, bt, logit_from=lf, targets=tg, chunk=chunk, max_tokens=max_tokens,
                                  max_logit_rows=max_logit_rows, mode=mode)
@@ -280,18 +320,11 @@ class Episode:
         self.hist_ids = torch.zeros((n_gen, B), dtype=torch.int32, device=dev)
         self.hist_lp = torch.zeros((n_gen, B), dtype=torch.float32, device=dev)
         # recompute: packed [prompt_b, gen_b[:-1]] per sequence
-        rl = lens + n_gen - 1
-        self.cu_r = np.concatenate([[0], np.cumsum(rl)])
+        self.cu_r, pd, gd, td = recompute_rows(lens, n_gen)
         self.T_r = int(self.cu_r[-1])
-        pd, gd, td = [], [], []
-        for b in range(B):
-            o = self.cu_r[b]
-            pd.append(o + np.arange(lens[b]))
-            gd.append(o + lens[b] + np.arange(n_gen - 1))
-            td.append(o + lens[b] - 1 + np.arange(n_gen))
-        self.p_dst = torch.from_numpy(np.concatenate(pd)).to(dev)
-        self.g_dst = torch.from_numpy(np.stack(gd)).to(dev) if n_gen > 1 else None
-        self.t_dst = torch.from_numpy(np.stack(td)).to(dev)
+        self.p_dst = torch.from_numpy(pd).to(dev)
+        self.g_dst = torch.from_numpy(gd).to(dev) if gd is not None else None
+        self.t_dst = torch.from_numpy(td).to(dev)
         self.rec_tok = torch.zeros(self.T_r, dtype=torch.int32, device=dev)
         self.rec_tgt = torch.zeros(self.T_r, dtype=torch.int32, device=dev)
         self.rec_lp = torch.zeros(self.T_r, dtype=torch.float32, device=dev)
