@@ -137,3 +137,37 @@ def test_fp8_layer_first_token_reads_its_own_round_tripped_v():
     q, s = fp8.quantize_act(v_read)
     assert np.array_equal(o, fp8.dequantize_blocks(q, s, 1))
     assert not np.array_equal(model.kv_round_trip(v), v)          # the round trip is not the identity here
+
+
+def test_fp8_layer_attention_mixes_round_tripped_k_and_v():
+    """With several keys the attention output mixes V vectors, so the FP8 round
+    trips of K (after RoPE) and V are visible through the O projection's own
+    1 x 128 quantisation: with Wo the identity, the attention sub-layer output is
+    the activation round trip of attention(q, rt(rope(k)), rt(v)), and neither the
+    bf16 V, the bf16 K nor K quantised before its rotation gives it."""
+    shape = DecoderShape(1, 256, 4, 2, 64, 256, 512)
+    W = model.weights_to_f32(make_decoder_weights(shape, seed=9, w_std=0.05))
+    lw = dict(W["layers"][0])
+    lw["wo"] = np.eye(256, dtype=np.float32)
+    l8 = model.fp8_weights({"layers": [lw]})["layers"][0]
+    L = 5
+    pos = np.arange(L)
+    r = round_bf16(np.random.default_rng(10).standard_normal((L, 256)).astype(np.float32))
+    _, o, _ = model.layer(l8, shape, r, pos, return_parts=True)
+    x, _ = ops.rmsnorm(r, lw["attn_norm"], shape.eps)
+    qkv = model.linear_fp8(x, *l8["fp8"]["wqkv"])
+    q = ops.rope(qkv[:, :256].reshape(L, 4, 64), pos, shape.rope_theta)
+    k_raw = qkv[:, 256:384].reshape(L, 2, 64)
+    k = ops.rope(k_raw, pos, shape.rope_theta)
+    v = qkv[:, 384:].reshape(L, 2, 64)
+
+    def o_of(kk, vv):
+        a = ops.attention(q, kk, vv, pos).reshape(L, 256)
+        qa, sa = fp8.quantize_act(a)
+        return fp8.dequantize_blocks(qa, sa, 1)
+
+    rt = model.kv_round_trip
+    assert np.array_equal(o, o_of(rt(k), rt(v)))
+    assert not np.array_equal(o, o_of(rt(k), v))
+    assert not np.array_equal(o, o_of(k, rt(v)))
+    assert not np.array_equal(o, o_of(ops.rope(rt(k_raw), pos, shape.rope_theta), rt(v)))
