@@ -58,6 +58,28 @@ MUTATIONS = [
     ("model.py", "k, v = kv_round_trip(k), kv_round_trip(v)", "k = kv_round_trip(k)", "fp8"),
     ("model.py", "    k = ops.rope(k, pos, shape.rope_theta)\n    if w8:\n        k, v = kv_round_trip(k), kv_round_trip(v)",
      "    if w8:\n        k, v = kv_round_trip(k), kv_round_trip(v)\n    k = ops.rope(k, pos, shape.rope_theta)", "fp8"),
+    # FP8 codes: subnormal exponent, the sign of zero
+    ("fp8.py", "v[code] = sign * (m / 8.0) * 2.0 ** -6", "v[code] = sign * (m / 8.0) * 2.0 ** -7", "fp8"),
+    ("fp8.py", "np.where(np.signbit(x), 0x80, 0)", "np.where(x < 0, 0x80, 0)", "fp8"),
+    # logprob: target index, normaliser without the max, greedy ties to the highest id
+    ("ops.py", "return x[np.arange(x.shape[0]), ids] - lse", "return x[np.arange(x.shape[0]), ids - 1] - lse", "ops"),
+    ("ops.py", "lse = m[..., 0] + np.log(np.sum(np.exp(x - m), axis=-1))",
+     "lse = np.log(np.sum(np.exp(x - m), axis=-1))", "ops"),
+    ("ops.py", "return np.argmax(np.asarray(logits, dtype=F32), axis=-1).astype(np.int32)",
+     "x = np.asarray(logits, dtype=F32)\n    return (x.shape[-1] - 1 - np.argmax(x[..., ::-1], axis=-1)).astype(np.int32)", "ops"),
+    # acceptance statistics: sample std instead of the population std
+    ("ops.py", '"std": float(d.std())', '"std": float(d.std(ddof=1)) if d.size > 1 else 0.0', "ops"),
+    # MoE routing: ties to the highest expert id, normaliser of one slot only
+    ("moe.py", 'order = np.argsort(-x, axis=1, kind="stable")[:, :k].astype(np.int32)',
+     'order = (E - 1 - np.argsort(-x[:, ::-1], axis=1, kind="stable"))[:, :k].astype(np.int32)', "ops"),
+    ("moe.py", "den = den + e[:, s: s + 1]", "den = den + e[:, 0:1]", "ops"),
+    # scoring: rows shifted by one, no final norm
+    ("model.py", "rows = np.arange(len(prompt) - 1, len(seq))", "rows = np.arange(len(prompt) - 2, len(seq) - 1)", "ops"),
+    ("model.py", 'x, _ = ops.rmsnorm(r, w["final_norm"], shape.eps)\n    if return_layers:',
+     'x = r\n    if return_layers:', "ops"),
+    # Mamba-2: the entering state ignored
+    ("ssd.py", "state = np.zeros((H, N, P)) if state0 is None else np.array(state0, np.float64)",
+     "state = np.zeros((H, N, P))", "ssd"),
     # Mamba-2: decay applied after the input, group map, output read before the update
     ("ssd.py", "state[h] = np.exp(loga[t, h]) * state[h] + np.outer(B[t, g], x[t, h])",
      "state[h] = np.exp(loga[t, h]) * (state[h] + np.outer(B[t, g], x[t, h]))", "ssd"),

@@ -279,6 +279,14 @@ def test_diff_stats_closed_forms():
     s = ops.diff_stats(np.zeros(2), np.full(2, math.log(2.0)))
     assert abs(s["k3"] - (1.0 - math.log(2.0))) < 1e-15
     assert abs(s["max"] - math.log(2.0)) < 1e-15 and s["std"] == 0.0
+    # diffs 0, 0, 0, 2: mean 1/2, population std sqrt(3)/2 (the reading: std over the
+    # tokens compared, not a sample estimate, which would give 1)
+    s = ops.diff_stats(np.zeros(4), np.array([0.0, 0.0, 0.0, 2.0]))
+    assert s["max"] == 2.0 and s["mean"] == 0.5
+    assert abs(s["std"] - math.sqrt(3.0) / 2.0) < 1e-15
+    # k3 per token is r - 1 - log r >= 0 with r = exp(lp_train - lp_rollout): its mean
+    # here is (e^2 - 3) / 4
+    assert abs(s["k3"] - (math.exp(2.0) - 3.0) / 4.0) < 1e-14
 
 
 # ----------------------------------------------------------------------------- MoE
