@@ -144,3 +144,72 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         _lib.load()
     with pytest.raises(RuntimeError):
         bi.bi_version()
+
+
+def _header_no_comments():
+    src = open(os.path.join(ROOT, "include", "bi.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.sub(r"//[^\n]*", "", src)
+
+
+def _ctype_of(decl):
+    """The ctypes type the binding must use for one C parameter / field / result type."""
+    decl = " ".join(decl.replace("const", " ").split())
+    if "*" in decl:
+        return "char_p" if decl.startswith("char") and decl.count("*") == 1 else "ptr"
+    base = decl.split()[0]
+    return {"int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t, "int": ctypes.c_int, "float": ctypes.c_float,
+            "double": ctypes.c_double, "bi_status": ctypes.c_int, "void": None}[base]
+
+
+def _same(want, got):
+    if want == "ptr":
+        return got is ctypes.c_void_p or (isinstance(got, type) and issubclass(got, ctypes._Pointer))
+    if want == "char_p":
+        return got is ctypes.c_char_p
+    return got is want
+
+
+def test_binding_types_match_the_header_prototypes():
+    """Every ctypes signature has the header's arity and, parameter by parameter,
+    the same width: a 32-bit int bound as 64 (or a pointer as an int) would be
+    silent undefined behaviour."""
+    src = _header_no_comments()
+    protos = {}
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(bi_[a-z0-9_]+)\s*\(([^;{()]*)\)\s*;", src):
+        res, name, args = m.group(1).strip(), m.group(2), m.group(3).strip()
+        params = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
+        # drop the parameter name: the type is everything before the last identifier
+        types = [re.sub(r"\b[A-Za-z_]\w*\s*$", "", p).strip() or p for p in params]
+        protos[name] = (res, types)
+    assert sorted(protos) == sorted(_lib._SIGS)
+    for name, (res, types) in protos.items():
+        want_res, want_args = _ctype_of(res), [_ctype_of(t) for t in types]
+        got_res, got_args = _lib._SIGS[name]
+        assert (want_res is None and got_res is None) or _same(want_res, got_res), (name, res, got_res)
+        assert len(got_args) == len(want_args), (name, len(got_args), len(want_args))
+        for i, (w, g) in enumerate(zip(want_args, got_args)):
+            assert _same(w, g), (name, i, types[i], g)
+
+
+def test_binding_structs_and_constants_match_the_header():
+    src = _header_no_comments()
+    for cls in (_lib.bi_model_config, _lib.bi_layer_weights, _lib.bi_weights):
+        body = re.search(r"typedef struct \{([^}]*)\}\s*" + cls.__name__ + r"\s*;", src).group(1)
+        fields = []
+        for stmt in body.split(";"):
+            stmt = stmt.strip()
+            if not stmt:
+                continue
+            m = re.match(r"((?:const\s+)?[A-Za-z_]\w*\s*\**)\s*(.*)$", stmt)
+            base, names = m.group(1), m.group(2)
+            for nm in names.split(","):
+                nm = nm.strip()
+                stars = nm.count("*")
+                fields.append((nm.strip("* "), _ctype_of(base + "*" * stars)))
+        got = cls._fields_
+        assert [f[0] for f in got] == [f[0] for f in fields], cls.__name__
+        for (n, w), (_, g) in zip(fields, got):
+            assert _same(w, g), (cls.__name__, n, g)
+    for name, value in re.findall(r"\b(BI_[A-Z0-9_]+)\s*=\s*(\d+)", src):
+        assert getattr(_lib, name) == int(value), name
