@@ -130,3 +130,34 @@ def test_ssd_rows_do_not_depend_on_the_batch():
             alone.call([(s, p, n)])
             p += n
         assert np.array_equal(alone.y[s].view(np.uint32), together.y[s].view(np.uint32)), s
+
+
+def test_ssd_full_size_sampled_against_recurrence():
+    """The timed prefill workload in its launch configuration (16 sequences x 2048
+    positions in one call; 32 heads x 64, state 128, 8 groups, chunk 64), sampled
+    (sequence, head) pairs against the fp64 recurrence run for that head alone."""
+    Hf, Gf, n_seq, per = 32, 8, 16, 2048
+    T = n_seq * per
+    rng = np.random.default_rng(8)
+    xb = normal_bf16(rng, (T, Hf, P), 1.0)
+    Bb = normal_bf16(rng, (T, Gf, N), N ** -0.5)
+    Cb = normal_bf16(rng, (T, Gf, N), N ** -0.5)
+    loga = (-np.abs(rng.standard_normal((T, Hf))) * 0.15).astype(np.float32)
+    state = torch.zeros((n_seq, bi.bi_ssd_state_bytes(Hf, Gf, P, N, Q) // 4), dtype=torch.float32, device="cuda")
+    y = torch.empty((T, Hf, P), dtype=torch.float32, device="cuda")
+    seq = torch.arange(n_seq, dtype=torch.int32, device="cuda")
+    row0 = torch.arange(0, T + 1, per, dtype=torch.int32, device="cuda")
+    pos0 = torch.zeros(n_seq, dtype=torch.int32, device="cuda")
+    bi.bi_ssd_chunk_scan(dev_bf16(xb), dev_bf16(Bb), dev_bf16(Cb), torch.from_numpy(loga).cuda(), seq, row0, pos0,
+                         n_seq, per, Hf, Gf, P, N, Q, state, n_seq, y)
+    yh = y.cpu().numpy()
+    assert np.isfinite(yh).all()
+    for s, h in ((0, 0), (7, 13), (15, 31)):
+        g = h // (Hf // Gf)
+        r = slice(s * per, (s + 1) * per)
+        want, _ = ossd.ssd_scan(bits_to_f32(xb[r, h:h + 1]), bits_to_f32(Bb[r, g:g + 1]), bits_to_f32(Cb[r, g:g + 1]),
+                                loga[r, h:h + 1], n_groups=1)
+        err = np.abs(yh[r, h:h + 1] - want)
+        assert err.max() <= 1e-4 * max(1.0, np.abs(want).max()), (s, h, err.max())
+        assert err.mean() <= 1e-5 * max(1.0, np.abs(want).mean()), (s, h, err.mean())
+    assert bi.bi_device_status() == 0
