@@ -38,13 +38,53 @@ WORKLOAD = ("dense decoder 4 layers, d=512, 8 heads x 64, SwiGLU 1408, vocab 320
             "decode) + training recompute (packed prefill, chunk 2048) of all 4096 sampled-token logprobs")
 
 
+def _flat_numbers(d, prefix=""):
+    """(dotted key, number) pairs of a JSON object, nested objects included."""
+    out = []
+    if isinstance(d, dict):
+        for k, v in d.items():
+            out += _flat_numbers(v, f"{prefix}.{k}" if prefix else str(k))
+    elif isinstance(d, (int, float)) and not isinstance(d, bool):
+        out.append((prefix.lower(), float(d)))
+    return out
+
+
+def parse_peaks(d):
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained) from the measured-peaks
+    record, or None.  Keys are matched by what they name (hbm / bf16 / sustained),
+    flat or nested (a "value" leaf under the named key counts), TB/s and PFLOP/s
+    converted."""
+    nums = _flat_numbers(d)
+
+    def pick(want, avoid=()):
+        for k, v in nums:
+            if all(w in k for w in want) and not any(a in k for a in avoid) and v > 0:
+                return k, v
+        return None, None
+
+    kh, hbm = pick(("hbm",), ("clock", "mhz", "util", "pct", "frac"))
+    kb, bf = pick(("bf16",), ("sustain", "clock", "mhz", "util", "pct", "frac"))
+    ks, bs = pick(("bf16", "sustain"), ("clock", "mhz", "util", "pct", "frac"))
+    if hbm is None or bf is None:
+        return None
+    if "tb" in kh or hbm < 100:          # TB/s
+        hbm *= 1000.0
+    if "pflop" in kb or bf < 50:         # PFLOP/s
+        bf *= 1000.0
+    if bs is None:
+        bs = bf
+    elif "pflop" in ks or bs < 50:
+        bs *= 1000.0
+    return hbm, bf, bs
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
-            d = json.load(open(p))
-            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
-            return float(hbm), float(d.get("bf16_tflops")), float(d.get("bf16_tflops_sustained", d.get("bf16_tflops"))), "measured"
+            got = parse_peaks(json.load(open(p)))
+            if got:
+                return got[0], got[1], got[2], "measured"
         except Exception:
             pass
     return 6800.0, 1900.0, 1700.0, "fallback"

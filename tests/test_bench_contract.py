@@ -38,3 +38,17 @@ def test_reference_arm_prints_one_contract_line():
 def test_reference_arm_other_ranks_exit_quietly():
     r = _bench({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--steps", "1", "--warmup", "0")
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_measured_peaks_record_is_read_flat_or_nested():
+    sys.path.insert(0, ROOT)
+    from bench import parse_peaks
+    want = (7100.0, 2050.0, 1740.0)
+    flat = {"hbm_gbs": 7100, "bf16_tflops": 2050, "bf16_tflops_sustained": 1740, "sm_clock_mhz": 2070}
+    nested = {"gpu": "GB300", "hbm_gbs": {"value": 7100, "pct_of_nominal": 90},
+              "bf16_tflops": {"value": 2050}, "bf16_tflops_sustained": {"value": 1740, "clock_mhz": 1900}}
+    units = {"hbm_tbs": 7.1, "bf16_pflops": 2.05, "bf16_pflops_sustained": 1.74}
+    for rec in (flat, nested, units):
+        assert parse_peaks(rec) == want, rec
+    assert parse_peaks({"hbm_gbs": 7100, "bf16_tflops": 2050}) == (7100.0, 2050.0, 2050.0)
+    assert parse_peaks({"note": "no measurement"}) is None
