@@ -19,6 +19,10 @@ Readings where the pages are silent (the plainest ones the rest supports):
     the product of the dequantised operands (the block-wise promotion a kernel
     does is the same sum regrouped, exact for power-of-two scales); fp32
     output, or bf16 rounded once.
+
+[Article] is "vLLM Achieves Bitwise-Consistent RL Training: Eliminating Numerical
+Drift to Zero KL Divergence on DeepSeek-V4-Flash at 91% Throughput"; section numbers
+are its own.
 """
 from __future__ import annotations
 

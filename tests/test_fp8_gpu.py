@@ -1,6 +1,10 @@
 """Block-FP8 quantisation and the W8A8 tcgen05 GEMM ([Article] §4.1) through the C ABI:
 codes and scales bit-exact against the oracle, the GEMM within fp32 accumulation of
-the oracle's exact product, and every row's result independent of the batch."""
+the oracle's exact product, and every row's result independent of the batch.
+
+[Article] is "vLLM Achieves Bitwise-Consistent RL Training: Eliminating Numerical
+Drift to Zero KL Divergence on DeepSeek-V4-Flash at 91% Throughput"; section numbers
+are its own."""
 import numpy as np
 import pytest
 import torch

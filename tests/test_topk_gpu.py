@@ -1,6 +1,10 @@
 """Deterministic Top-K ([Article] §4.3) on the GPU through the C ABI: bit-exact
 against the oracle, rows independent of the batch they run in, and the
-non-deterministic BI_FAST variant selecting the same scores."""
+non-deterministic BI_FAST variant selecting the same scores.
+
+[Article] is "vLLM Achieves Bitwise-Consistent RL Training: Eliminating Numerical
+Drift to Zero KL Divergence on DeepSeek-V4-Flash at 91% Throughput"; section numbers
+are its own."""
 import numpy as np
 import pytest
 import torch
