@@ -971,6 +971,46 @@ def run_kernel_case(name: str, reps: int):
         for _ in range(reps):
             bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, B * max_blk, ctx, 512,
                             hd ** -0.5, ws, out)
+    elif name == "rmsnorm":
+        # residual add + norm, 16384 rows x 2048 (4 x 67 MB: above L2)
+        R, d = 16384, 2048
+        x = torch.randn((R, d), device=dev).to(torch.bfloat16)
+        r = torch.randn((R, d), device=dev).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        g = torch.ones(d, device=dev).to(torch.bfloat16)
+        for _ in range(reps):
+            bi.bi_rmsnorm(x, r, g, y, R, d)
+    elif name == "logprob":
+        # vocab-wide log-softmax + gather, 2048 rows x 129280 (1.06 GB of fp32 logits)
+        T, V = 2048, 129280
+        logits = torch.randn((T, V), device=dev)
+        lp = torch.empty(T, device=dev)
+        ids = torch.randint(0, V, (T,), dtype=torch.int32, device=dev)
+        for _ in range(reps):
+            bi.bi_logprob_gather(logits, ids, T, V, lp)
+    elif name == "lm_head_fused":
+        # fused lm_head + log-softmax records + merge, 2048 rows x 4096 -> 129280
+        T, d, V = 2048, 4096, 129280
+        H = torch.randn((T, d), device=dev).to(torch.bfloat16)
+        W = (0.01 * torch.randn((V, d), device=dev)).to(torch.bfloat16)
+        ids = torch.randint(0, V, (T,), dtype=torch.int32, device=dev)
+        lp = torch.empty(T, device=dev)
+        ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(T, V, d, bi.BI_INVARIANT), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(reps):
+            bi.bi_lm_head_logprob(H, T, d, W, V, ids, lp, None, bi.BI_INVARIANT, ws)
+    elif name == "moe_layer":
+        # MoE layer: router top-8, permutation, grouped expert GEMMs, slot-order combine (4096 x 2048, 64 experts)
+        T, dm, E, k, F = 4096, 2048, 64, 8, 1024
+        x = torch.randn((T, dm), device=dev).to(torch.bfloat16)
+        lg = torch.randn((T, E), device=dev)
+        w13 = (0.02 * torch.randn((E, 2 * F, dm), device=dev)).to(torch.bfloat16)
+        w2 = (0.02 * torch.randn((E, dm, F), device=dev)).to(torch.bfloat16)
+        y = torch.empty((T, dm), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(bi.bi_moe_layer_workspace_size(T, dm, E, k, F, bi.BI_INVARIANT), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(reps):
+            bi.bi_moe_layer(x, lg, T, dm, E, k, F, w13, w2, y, bi.BI_INVARIANT, ws)
     else:
         raise SystemExit(f"unknown kernel case {name}")
     torch.cuda.synchronize()
@@ -983,7 +1023,7 @@ def main():
     ap.add_argument("--kernel-case", default=None,
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
-                         "kv_fp8_gather, c5_decode, topk_prefill) or "
+                         "kv_fp8_gather, c5_decode, topk_prefill, rmsnorm, logprob, lm_head_fused, moe_layer) or "
                          "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
