@@ -513,6 +513,16 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
                              void* k_cache, void* v_cache, int64_t n_blocks, float* logprob_out,
                              int32_t* sampled_out, void* workspace, size_t ws_bytes, int64_t max_tokens,
                              int64_t max_ctx, int64_t max_logit_rows, int mode, void* stream);
+/* The pass schedule bi_forward_prefill runs for these sequences (host only, no
+ * GPU; a diagnostic).  Arguments as in bi_forward_prefill (cu_seqlens, start_pos,
+ * logit_from HOST int64; B sequences; chunk; max_tokens).  Writes one record of 8
+ * int64 per piece, in launch order, to out (HOST int64 [out_rows, 8]; may be
+ * NULL): (pass, sequence, first row in the pass, rows, first position, first
+ * packed token, first row with logits relative to the piece, first logit row in
+ * the pass).  Returns the number of pieces (records beyond out_rows are not
+ * written), or -1 for invalid arguments. */
+int64_t bi_prefill_plan(const int64_t* cu_seqlens, const int64_t* start_pos, const int64_t* logit_from, int64_t B,
+                        int64_t chunk, int64_t max_tokens, int64_t* out, int64_t out_rows);
 
 /* One greedy decode step for B sequences: token b (device int32 [B]) sits at
  * position pos[b] (device int32 [B]); its K/V are written to the cache, and the

@@ -115,6 +115,8 @@ _SIGS = {
     "bi_forward_prefill": (_int, [_vp, _vp, _vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64),
                                   _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _i64, _i64, _i64, _int,
                                   _vp]),
+    "bi_prefill_plan": (_i64, [ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64), _i64, _i64, _i64,
+                               ctypes.POINTER(_i64), _i64]),
     "bi_forward_decode": (_int, [_vp, _vp, _vp, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _sz, _int,
                                  _vp]),
     "bi_decode_advance": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp]),
@@ -408,6 +410,19 @@ def bi_forward_prefill(model, tokens, target_ids, cu_seqlens, start_pos, logit_f
                                      max_blocks_per_seq, _p(k_cache), _p(v_cache), n_blocks, _p(logprob_out),
                                      _p(sampled_out), _p(workspace), _nb(workspace), max_tokens, max_ctx,
                                      max_logit_rows, mode, _s(stream)))
+
+
+def bi_prefill_plan(cu_seqlens, start_pos, logit_from, chunk, max_tokens):
+    """The pass schedule bi_forward_prefill runs (host only): a list of records
+    (pass, seq, row0, rows, pos0, tok0, lfirst, loff), one per piece, in launch order."""
+    B = len(cu_seqlens) - 1
+    cu, sp, lf = _i64_array(cu_seqlens), _i64_array(start_pos), _i64_array(logit_from)
+    n = load().bi_prefill_plan(cu, sp, lf, B, chunk, max_tokens, None, 0)
+    if n < 0:
+        raise BiError(BI_ERR_INVALID_ARG, "bi_prefill_plan: invalid arguments")
+    out = (_i64 * (8 * max(n, 1)))()
+    load().bi_prefill_plan(cu, sp, lf, B, chunk, max_tokens, out, n)
+    return [tuple(out[8 * r: 8 * r + 8]) for r in range(n)]
 
 
 def bi_forward_decode(model, tokens, pos, B, block_table, max_blocks_per_seq, k_cache, v_cache, n_blocks, max_ctx,

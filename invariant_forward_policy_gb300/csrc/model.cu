@@ -186,6 +186,76 @@ struct PassShape {
   bool embedded;  // the embedding rows are already in the residual buffer
 };
 
+// One layer pass of a prefill call: the pieces it holds and its shape.
+struct PassPlan {
+  PassMeta pm;
+  PassShape ps;
+};
+
+// The pass schedule of a prefill call (host only).  Pieces in chunk-major order
+// (every sequence's chunk 0, then chunk 1, ...), each at most `chunk` rows;
+// passes take pieces in that order up to max_tokens rows and Pm pieces; a piece
+// larger than a whole pass is split.  logit_from (or NULL: every row) gives each
+// sequence's first row with logits.
+static std::vector<PassPlan> plan_prefill(const int64_t* cu_seqlens, const int64_t* start_pos,
+                                          const int64_t* logit_from, int64_t B, int64_t chunk, int64_t max_tokens,
+                                          int64_t Pm) {
+  struct Piece { int64_t seq, start, len; };
+  std::vector<Piece> pieces;
+  int64_t max_len = 0;
+  for (int64_t b = 0; b < B; ++b) max_len = std::max(max_len, cu_seqlens[b + 1] - cu_seqlens[b]);
+  for (int64_t c0 = 0; c0 < max_len; c0 += chunk)
+    for (int64_t b = 0; b < B; ++b) {
+      const int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
+      if (c0 < n) pieces.push_back({b, c0, std::min(chunk, n - c0)});
+    }
+  std::vector<PassPlan> plan;
+  size_t i = 0;
+  while (i < pieces.size()) {
+    PassMeta pm{};
+    PassShape ps{};
+    int64_t rows = 0, nlog = 0;
+    int np = 0;
+    while (i < pieces.size() && np < Pm) {
+      const Piece& pc = pieces[i];
+      int64_t len = pc.len;
+      if (rows + len > max_tokens) {
+        if (rows > 0) break;
+        len = max_tokens;  // a single piece larger than the pass limit: split it
+      }
+      const int64_t lf_call = logit_from ? logit_from[pc.seq] : 0;
+      const int64_t lfirst = std::min(std::max<int64_t>(lf_call - pc.start, 0), len);
+      pm.seq[np] = (int)pc.seq;
+      pm.row0[np] = (int)rows;
+      pm.pos0[np] = (int)(start_pos[pc.seq] + pc.start);
+      pm.tok0[np] = (int)(cu_seqlens[pc.seq] + pc.start);
+      pm.lfirst[np] = (int)lfirst;
+      pm.loff[np] = (int)nlog;
+      nlog += len - lfirst;
+      rows += len;
+      ps.max_q_len = std::max(ps.max_q_len, len);
+      ps.max_ctx = std::max(ps.max_ctx, start_pos[pc.seq] + pc.start + len);
+      ++np;
+      if (len < pieces[i].len) {
+        pieces[i].start += len;
+        pieces[i].len -= len;
+      } else {
+        ++i;
+      }
+    }
+    pm.n_pieces = np;
+    pm.n_rows = (int)rows;
+    pm.n_logit = (int)nlog;
+    pm.row0[np] = (int)rows;
+    pm.loff[np] = (int)nlog;
+    ps.rows = rows;
+    ps.pieces = np;
+    ps.n_logit = nlog;
+    plan.push_back({pm, ps});
+  }
+  return plan;
+}
+
 // The layer stack over the rows of one pass (identical for prefill and decode).
 static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassShape& ps, int64_t Rm,
                           const int32_t* block_table, int64_t max_blk, void* k_cache, void* v_cache,
@@ -400,58 +470,12 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
   }
   BI_REQUIRE(cu_seqlens[B] < (1ll << 31), "too many tokens");
 
-  // pieces in chunk-major order: every sequence's chunk 0, then chunk 1, ...
-  struct Piece { int64_t seq, start, len; };
-  std::vector<Piece> pieces;
-  int64_t max_len = 0;
-  for (int64_t b = 0; b < B; ++b) max_len = std::max(max_len, cu_seqlens[b + 1] - cu_seqlens[b]);
-  for (int64_t c0 = 0; c0 < max_len; c0 += chunk)
-    for (int64_t b = 0; b < B; ++b) {
-      const int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
-      if (c0 < n) pieces.push_back({b, c0, std::min(chunk, n - c0)});
-    }
-  size_t i = 0;
+  const std::vector<PassPlan> plan = plan_prefill(cu_seqlens, start_pos, logit_from, B, chunk, max_tokens, Pm);
   const cudaStream_t st = as_stream(stream);
-  while (i < pieces.size()) {
-    PassMeta pm{};
-    PassShape ps{};
-    int64_t rows = 0, nlog = 0;
-    int np = 0;
-    while (i < pieces.size() && np < Pm) {
-      const Piece& pc = pieces[i];
-      int64_t len = pc.len;
-      if (rows + len > max_tokens) {
-        if (rows > 0) break;
-        len = max_tokens;  // a single piece larger than the pass limit: split it
-      }
-      const int64_t lf_call = logit_from ? logit_from[pc.seq] : 0;
-      const int64_t lfirst = std::min(std::max<int64_t>(lf_call - pc.start, 0), len);
-      pm.seq[np] = (int)pc.seq;
-      pm.row0[np] = (int)rows;
-      pm.pos0[np] = (int)(start_pos[pc.seq] + pc.start);
-      pm.tok0[np] = (int)(cu_seqlens[pc.seq] + pc.start);
-      pm.lfirst[np] = (int)lfirst;
-      pm.loff[np] = (int)nlog;
-      nlog += len - lfirst;
-      rows += len;
-      ps.max_q_len = std::max(ps.max_q_len, len);
-      ps.max_ctx = std::max(ps.max_ctx, start_pos[pc.seq] + pc.start + len);
-      ++np;
-      if (len < pieces[i].len) {
-        pieces[i].start += len;
-        pieces[i].len -= len;
-      } else {
-        ++i;
-      }
-    }
-    pm.n_pieces = np;
-    pm.n_rows = (int)rows;
-    pm.n_logit = (int)nlog;
-    pm.row0[np] = (int)rows;
-    pm.loff[np] = (int)nlog;
-    ps.rows = rows;
-    ps.pieces = np;
-    ps.n_logit = nlog;
+  for (const PassPlan& pp : plan) {
+    const PassMeta& pm = pp.pm;
+    const PassShape& ps = pp.ps;
+    const int64_t rows = ps.rows;
     DevMeta dm{at<int32_t>(workspace, L.piece_seq), at<int32_t>(workspace, L.piece_row0),
                at<int32_t>(workspace, L.piece_pos0), at<int32_t>(workspace, L.ids),
                at<int32_t>(workspace, L.logit_src), at<int32_t>(workspace, L.logit_dst),
@@ -464,6 +488,33 @@ bi_status bi_forward_prefill(bi_model* m, const int32_t* tokens, const int32_t* 
                     target_ids == nullptr, logprob_out, sampled_out, mode, stream));
   }
   return BI_OK;
+}
+
+int64_t bi_prefill_plan(const int64_t* cu_seqlens, const int64_t* start_pos, const int64_t* logit_from, int64_t B,
+                        int64_t chunk, int64_t max_tokens, int64_t* out, int64_t out_rows) {
+  using namespace bi;
+  if (!cu_seqlens || !start_pos || B < 0 || chunk <= 0 || max_tokens <= 0 || cu_seqlens[0] != 0) return -1;
+  for (int64_t b = 0; b < B; ++b)
+    if (cu_seqlens[b + 1] < cu_seqlens[b] || start_pos[b] < 0) return -1;
+  const int64_t Pm = std::min<int64_t>(kMaxPiecesPerPass, std::max<int64_t>(B, 1));
+  const std::vector<PassPlan> plan = plan_prefill(cu_seqlens, start_pos, logit_from, B, chunk, max_tokens, Pm);
+  int64_t n = 0;
+  for (size_t p = 0; p < plan.size(); ++p) {
+    const PassMeta& pm = plan[p].pm;
+    for (int k = 0; k < pm.n_pieces; ++k, ++n) {
+      if (!out || n >= out_rows) continue;
+      int64_t* r = out + n * 8;
+      r[0] = (int64_t)p;
+      r[1] = pm.seq[k];
+      r[2] = pm.row0[k];
+      r[3] = pm.row0[k + 1] - pm.row0[k];
+      r[4] = pm.pos0[k];
+      r[5] = pm.tok0[k];
+      r[6] = pm.lfirst[k];
+      r[7] = pm.loff[k];
+    }
+  }
+  return n;
 }
 
 bi_status bi_forward_decode(bi_model* m, const int32_t* tokens, const int32_t* pos, int64_t B,

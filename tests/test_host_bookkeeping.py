@@ -69,3 +69,70 @@ def test_static_rows_build_the_same_batch_as_the_list_form():
         assert np.array_equal(tok, np.concatenate(seqs))                      # every row written once
         assert np.array_equal(tgt, np.concatenate(tg))
         assert np.array_equal(t_dst[:, 0], cu[:-1] + np.array(lf))
+
+
+def _check_plan(lens, start_pos, logit_from, chunk, max_tokens):
+    from invariant_forward_policy_gb300 import bi_prefill_plan
+    B = len(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    plan = bi_prefill_plan(cu.tolist(), list(start_pos), None if logit_from is None else list(logit_from), chunk,
+                           max_tokens)
+    seen = [0] * B                        # rows of each sequence scheduled so far
+    logits = [0] * B
+    passes = {}
+    last_chunk = -1
+    for p, seq, row0, rows, pos0, tok0, lfirst, loff in plan:
+        off = seen[seq]
+        assert rows >= 1 and tok0 == cu[seq] + off and pos0 == start_pos[seq] + off   # in order, no gap, no repeat
+        assert off // chunk == (off + rows - 1) // chunk and rows <= chunk              # inside one chunk
+        assert off // chunk >= last_chunk - 1                                          # chunk-major order
+        last_chunk = max(last_chunk, off // chunk)
+        lf = 0 if logit_from is None else logit_from[seq]
+        assert lfirst == min(max(lf - off, 0), rows)
+        seen[seq] += rows
+        logits[seq] += rows - lfirst
+        passes.setdefault(p, []).append((row0, rows, lfirst, loff))
+    assert seen == list(lens)                                                          # every row once
+    for b in range(B):
+        lf = 0 if logit_from is None else logit_from[b]
+        assert logits[b] == lens[b] - min(max(lf, 0), lens[b])
+    assert sorted(passes) == list(range(len(passes)))
+    for pieces in passes.values():
+        assert len(pieces) <= min(128, max(B, 1))
+        r = lo = 0
+        for row0, rows, lfirst, loff in pieces:                                         # packed back to back
+            assert row0 == r and loff == lo
+            r += rows
+            lo += rows - lfirst
+        assert r <= max_tokens
+    return plan
+
+
+def test_prefill_plan_schedules_every_row_once_within_the_limits():
+    rng = np.random.default_rng(3)
+    for trial in range(300):
+        B = int(rng.integers(1, 200 if trial % 7 == 0 else 10))
+        lens = rng.integers(0, 2500, B)
+        sp = rng.integers(0, 300, B)
+        lf = (rng.integers(0, 2500, B) * rng.integers(0, 2, B)) if trial % 2 else None
+        chunk = int(rng.choice([1, 64, 97, 512, 2048, 1 << 30]))
+        mt = int(rng.choice([3, 64, 500, 2048, 8192]))
+        _check_plan(lens, sp, lf, chunk, mt)
+
+
+def test_prefill_plan_small_cases_and_errors():
+    import pytest
+    import invariant_forward_policy_gb300 as bi
+    # two sequences, chunk 4, passes of at most 6 rows filled greedily in chunk-major
+    # order: chunk 0 of each (4 + 4 > 6: two passes), then chunk 1 of each
+    plan = _check_plan([6, 5], [0, 10], None, 4, 6)
+    assert [(p, s, r) for p, s, _, r, *_ in plan] == [(0, 0, 4), (1, 1, 4), (1, 0, 2), (2, 1, 1)]
+    assert plan[1][4] == 10 and plan[3][4] == 14                                          # positions follow start_pos
+    # a piece longer than a pass is split across passes
+    plan = _check_plan([10], [0], None, 1 << 20, 4)
+    assert [r for _, _, _, r, *_ in plan] == [4, 4, 2]
+    assert bi.bi_prefill_plan([0], [], None, 64, 64) == []                                 # no sequences
+    with pytest.raises(bi.BiError):
+        bi.bi_prefill_plan([1, 5], [0], None, 64, 64)                                      # cu_seqlens[0] != 0
+    with pytest.raises(bi.BiError):
+        bi.bi_prefill_plan([0, 5, 3], [0, 0], None, 64, 64)                                # decreasing
