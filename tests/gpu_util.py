@@ -31,9 +31,19 @@ def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
     return torch.equal(a, b)
 
 
+def bf16_ulp(x) -> np.ndarray:
+    """One bf16 ulp at each |x|: 2^(e - 7) for |x| in [2^e, 2^(e+1)) (8 significant
+    bits), and 2^-133 (the smallest subnormal step) below 2^-126 and at zero."""
+    a = np.abs(np.asarray(x, np.float64))
+    _, e = np.frexp(a)                       # a = f * 2^e with f in [0.5, 1)
+    e = np.where(a == 0, -125, np.maximum(e, -125))
+    return np.ldexp(1.0, e - 8)
+
+
 def bf16_close(got: np.ndarray, want: np.ndarray, ulps: float = 1.0, frac_exact: float = 0.95, atol: float = 0.0):
-    """got within `ulps` bf16 ulps (relative 2^-8 per ulp) of want, and mostly bit-equal."""
-    tol = ulps * 2.0 ** -7 * np.abs(want) + atol
-    bad = np.abs(got - want) > tol
+    """got within `ulps` bf16 ulps of want (one ulp measured exactly at |want|), plus
+    atol, and at least `frac_exact` of the elements bit-equal."""
+    tol = ulps * bf16_ulp(want) + atol
+    bad = np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64)) > tol
     assert not bad.any(), f"{bad.sum()} elements beyond {ulps} bf16 ulp; max err {np.max(np.abs(got - want))}"
     assert np.mean(got == want) >= frac_exact, f"only {np.mean(got == want):.3f} bit-equal"

@@ -2,17 +2,21 @@
 
 Free-running tolerance: two implementations of the same numerical contract
 (fp32 accumulation, bf16 at the same boundaries) that only sum in a different
-order already differ by a model-dependent amount, because one-ulp bf16 flips
-in the residual stream propagate.  Measured with the oracle against its own
-fp64-accumulation variant (same tokens, teacher forced):
-  dense decoder (4 layers, d 512):            max 7.5e-3, mean 2.2e-3
-  long-context GQA decoder (8 layers, d 2048): max 3.8e-2, mean 1.0e-2
-  small 2-layer test models (d 128 / 256):     max 6.7e-3, mean 2.6e-3
-and rounding P to bf16 before P.V (the kernel does, the oracle does not) adds
-about 3e-3 to the mean on the small models (max 7.9e-3, mean 3.0e-3 alone).
-The free-running bounds are about twice those floors; the strict check is the
-layer-anchored one (every layer from the GPU's own input; the logprob from its
-final norm within 1e-4).
+order, or round the attention probabilities P to bf16 before P.V (the kernel
+does, the oracle does not), already differ by a model-dependent amount,
+because one-ulp bf16 flips in the residual stream propagate.
+tests/test_tolerance_floor.py measures that floor on the CPU, per model, as
+the oracle against variants of itself (fp64 accumulation; bf16 P in a 64-key
+online softmax; both), teacher forced, and requires every bound below to lie
+between the largest floor and 2.5 times it.  Measured (max / mean of |dlp|):
+  small 2-layer models (d 128 and d 256):    1.0e-2 / 3.2e-3
+  dense decoder (4 layers, d 512):           1.1e-2 / 2.8e-3  (4 x 256 tokens)
+  long-context GQA (8 layers, d 2048):       4.2e-2 / 1.3e-2  (1 x 64 tokens)
+  block-FP8 2-layer model (d 256):           2.0e-1 / 3.6e-2
+the benchmark spec's 5e-3 is therefore met as a mean on the dense decoder, and is
+below the contract's own floor on the 8-layer long-context model; the strict
+check on every model is the layer-anchored one (each layer from the GPU's own
+input; the logprob from the GPU's final-norm rows within 1e-4).
 """
 import numpy as np
 import torch
@@ -22,15 +26,15 @@ from oracle import ops
 from tests.gpu_util import bf16_close, host_f32
 
 E2E_MAX, E2E_MEAN = 2e-2, 5e-3            # dense decoder workload
-E2E_MAX_SMALL, E2E_MEAN_SMALL = 3e-2, 1e-2  # small 2-layer test models
+E2E_MAX_SMALL, E2E_MEAN_SMALL = 2.5e-2, 7e-3  # small 2-layer test models
 E2E_MAX_LONG, E2E_MEAN_LONG = 8e-2, 2.5e-2  # 8-layer d-2048 long-context decoder
 # Block-FP8 model: a one-ulp bf16 flip of a GEMM input moves its e4m3 code by a
-# whole e4m3 step (2^-3 relative) about one time in sixteen, so the same
-# measurement (the FP8 oracle against itself with P rounded to bf16, small
-# 2-layer model d 256) gives a free-running floor of max 1.8e-1, mean 4.4e-2, and
-# a layer-anchored floor of 0.15 of (|update| + row rms) per element, 0.015 on
-# average; the bounds are about twice and three times those.
-E2E_MAX_FP8, E2E_MEAN_FP8 = 0.4, 0.1
+# whole e4m3 step (2^-3 relative) about one time in sixteen, so its floor is an
+# order of magnitude above the bf16 one.  The layer-anchored floor (the FP8
+# oracle with P rounded to bf16 against the FP8 oracle) is 0.15 of (|update| +
+# row rms) per element, 0.015 on average; the layer bounds are about three
+# times those.
+E2E_MAX_FP8, E2E_MEAN_FP8 = 0.4, 0.08
 FP8_LAYER_MAX, FP8_LAYER_MEAN = 0.5, 0.05
 
 

@@ -120,8 +120,9 @@ def test_gqa_decoder_rollout_equals_recompute_long_context():
 def test_c2_dense_decoder_diff_zero_all_schedules():
     """The 4-layer d=512 dense decoder workload: 16 prompts of 128-512 tokens,
     256 greedy tokens.  Rollout under three batch schedules and recompute under
-    three packings/chunkings all give identical logprobs; the oracle agrees
-    within 5e-3 on the sampled tokens of four sequences."""
+    three packings/chunkings all give identical logprobs; on the sampled tokens
+    of four sequences the oracle agrees within max 2e-2 and mean 5e-3 (the
+    contract's own floor here is max 1.1e-2, mean 2.8e-3: tests/parity.py)."""
     cfg = C2
     shape = cfg["shape"]
     wb = make_decoder_weights(shape, seed=cfg["seed"], w_std=cfg["w_std"])
