@@ -193,7 +193,13 @@ size_t bi_attention_workspace_size(int64_t max_T, int Hq, int hd, int64_t max_ct
  *  - It allocates nothing: no cudaMalloc / cudaFree, no library allocator.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept with the unique id of the
+ *    context it was found in: after cudaDeviceReset, or from another context,
+ *    the next call looks it up again (so make that call outside a capture too).
+ *  - The sizes are checked against the array on the host before any CUDA
+ *    call; the check cannot wrap around for huge T or max_ctx.  As with
+ *    bi_attention, the kernels take row indices from piece_row0, so every
+ *    piece's rows must lie below T.
  *  - Every call on a device shares the one array and the array keeps the last
  *    call's contents; nothing in it needs to start at zero, because every
  *    partial that the merge reads is written earlier in the same call.  Calls

@@ -43,20 +43,61 @@ int num_sms() {
   return cached[dev];
 }
 
-int* device_status_ptr() {
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static int* cached[64] = {nullptr};
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!cached[dev]) {
+// Driver calls reached through the runtime's entry-point table (the library
+// links no libcuda): the current context and its unique id.
+static PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+static PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+
+bool current_context_id(unsigned long long* id) {
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    cached[dev] = static_cast<int*>(p);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!g_ctx_get_current || !g_ctx_get_id) return false;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+bool module_symbol_address(const void* symbol, void** out, ModuleAddressCache* cache) {
+  *out = nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return false;
   }
-  return cached[dev];
+  unsigned long long ctx = 0;
+  bool have_ctx = current_context_id(&ctx);
+  std::lock_guard<std::mutex> lock(cache->mu);
+  if (have_ctx && cache->addr[dev] && cache->ctx[dev] == ctx) {
+    *out = cache->addr[dev];
+    return true;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return false;
+  }
+  // the lookup makes the device's primary context current if none was
+  if (!have_ctx) have_ctx = current_context_id(&ctx);
+  cache->addr[dev] = have_ctx ? p : nullptr;
+  cache->ctx[dev] = have_ctx ? ctx : 0;
+  *out = p;
+  return true;
+}
+
+int* device_status_ptr() {
+  static ModuleAddressCache cache;
+  void* p = nullptr;
+  return module_symbol_address(&g_device_status, &p, &cache) ? static_cast<int*>(p) : nullptr;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {

@@ -1286,25 +1286,26 @@ namespace bi {
 constexpr size_t kAttnStaticScratchBytes = size_t(32) << 20;  // 32 MiB per device
 static __device__ __align__(256) unsigned char g_attn_static_scratch[kAttnStaticScratchBytes];
 
-// Device address of the array on the current device, looked up once per device.
+// Device address of the array in the current context: looked up on a device's
+// first call and again whenever the context has changed since (a reset device,
+// or a context the caller made), never reused across contexts.
 static bi_status attn_static_scratch_addr(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(BI_ERR_CUDA, std::string("bi_attention_static_scratch: ") + cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return fail(BI_ERR_CUDA, "bi_attention_static_scratch: device index out of range");
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
-    if (e != cudaSuccess || !p)
-      return fail(BI_ERR_CUDA, std::string("bi_attention_static_scratch: cudaGetSymbolAddress failed: ") +
-                                   cudaGetErrorString(e));
-    addr[dev] = p;
-  }
-  *out = addr[dev];
+  static ModuleAddressCache cache;
+  if (!module_symbol_address(&g_attn_static_scratch, out, &cache))
+    return fail(BI_ERR_CUDA, "bi_attention_static_scratch: cudaGetSymbolAddress of the scratch array failed");
   return BI_OK;
+}
+
+// Bytes of split partials a call needs, T * Hq * ns * (hd + 2) * 4, or false
+// when that product does not fit in 64 bits (so huge sizes cannot wrap around
+// to a small one).
+static bool attn_partials_bytes(int64_t T, int Hq, int64_t ns, int hd, uint64_t* need) {
+  uint64_t b = (uint64_t)(hd + 2) * sizeof(float);
+  const uint64_t factors[3] = {(uint64_t)Hq, (uint64_t)ns, (uint64_t)T};
+  for (uint64_t f : factors)
+    if (__builtin_mul_overflow(b, f, &b)) return false;
+  *need = b;
+  return true;
 }
 
 }  // namespace bi
@@ -1321,15 +1322,19 @@ extern "C" bi_status bi_attention_static_scratch(const void* q, int64_t T, const
   BI_REQUIRE(Hq > 0 && Hkv > 0 && Hq % Hkv == 0, "Hq must be a multiple of Hkv");
   BI_REQUIRE(hd > 0 && kv_split >= 64 && kv_split % 64 == 0 && max_ctx > 0 && max_q_len > 0,
              "bad head_dim / kv_split / max_ctx / max_q_len");
+  BI_REQUIRE(mode == BI_INVARIANT || mode == BI_FAST, "bad mode");
   // the partials this call needs, computed the way bi_attention sizes them
   const int split = choose_split(mode, kv_split, P, max_q_len, Hkv, Hq / Hkv, max_ctx);
-  const size_t per = (size_t)T * Hq * n_splits(max_ctx, split);
-  const size_t need = per * hd * sizeof(float) + per * 2 * sizeof(float);
-  if (need > kAttnStaticScratchBytes)
-    return fail(BI_ERR_INVALID_ARG, "bi_attention_static_scratch: this call needs " + std::to_string(need) +
-                                        " bytes of split partials but the static scratch array holds " +
-                                        std::to_string(kAttnStaticScratchBytes) +
-                                        " bytes; use bi_attention with a caller workspace");
+  const int64_t ns = n_splits(max_ctx, split);
+  uint64_t need = 0;
+  const bool exact = attn_partials_bytes(T, Hq, ns, hd, &need);
+  if (!exact || need > kAttnStaticScratchBytes)
+    return fail(BI_ERR_INVALID_ARG,
+                "bi_attention_static_scratch: this call needs " +
+                    (exact ? std::to_string(need) : std::string("more than 2^64")) +
+                    " bytes of split partials (T " + std::to_string(T) + " x Hq " + std::to_string(Hq) + " x splits " +
+                    std::to_string(ns) + " x (hd + 2) x 4) but the static scratch array holds " +
+                    std::to_string(kAttnStaticScratchBytes) + " bytes; use bi_attention with a caller workspace");
   void* scratch = nullptr;
   BI_TRY(attn_static_scratch_addr(&scratch));
   return bi_attention(q, T, piece_seq, piece_row0, piece_pos0, P, max_q_len, Hq, Hkv, hd, k_cache, v_cache,

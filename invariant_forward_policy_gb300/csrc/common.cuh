@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <string>
 #include <utility>
 
@@ -47,7 +48,24 @@ int num_sms();
 // Device status word: kernels that give up a bounded wait, or that see an
 // out-of-range index, record a code here instead of trapping.
 enum DeviceCode : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
-int* device_status_ptr();  // device address of the status word (current device)
+int* device_status_ptr();  // device address of the status word (current device and context)
+
+// Device addresses of a module's __device__ symbol, remembered per device
+// together with the unique id of the context they were looked up in: a
+// context made again (after cudaDeviceReset, or a context the caller created)
+// loads the module at a new address, and the changed id makes the next call
+// look it up again instead of handing a kernel the stale one.
+struct ModuleAddressCache {
+  std::mutex mu;
+  void* addr[64] = {nullptr};
+  unsigned long long ctx[64] = {0};
+};
+// The current context's unique id (false when none is current or the driver
+// lacks cuCtxGetId).
+bool current_context_id(unsigned long long* id);
+// Address of `symbol` on the current device in the current context, through
+// `cache`; false (no address) when the lookup fails.
+bool module_symbol_address(const void* symbol, void** out, ModuleAddressCache* cache);
 
 // Internal launchers shared between translation units (same kernels as the
 // public entry points, with a row indirection the model driver uses).

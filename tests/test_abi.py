@@ -104,6 +104,30 @@ def test_workspace_queries_are_limit_sized(lib):
     assert bi.bi_gemm_workspace_size(16, 1536, 512, 0, bi.BI_FAST) > 0
 
 
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="passes dummy addresses; the refusal must be observed where nothing can launch")
+def test_static_scratch_attention_refuses_oversized_calls_before_any_cuda_call(lib):
+    # The size check of bi_attention_static_scratch runs on the host before any
+    # CUDA call, so on a machine without a GPU a refused call returns
+    # BI_ERR_INVALID_ARG, and a regressed check would show up as BI_ERR_CUDA
+    # (no device), never as a launch.  Arguments: q T seq row0 pos0 P max_q_len
+    # Hq Hkv hd k v block_table max_blk n_blocks max_ctx split scale out mode stream.
+    def call(T, max_ctx, Hq=16, hd=128, mode=0):
+        return lib.bi_attention_static_scratch(16, T, 16, 16, 16, 1, 64, Hq, 4, hd, 16, 16, 16, 1024, 1024, max_ctx,
+                                               512, 0.088, 16, mode, None)
+    # 64 rows x 16 heads x 128 splits x 130 x 4 bytes = 68 MB > 32 MiB
+    assert call(64, 65536) == bi.BI_ERR_INVALID_ARG
+    msg = bi.bi_last_error()
+    assert "static scratch array holds 33554432 bytes" in msg and "68157440 bytes" in msg, msg
+    # a product that does not fit in 64 bits is refused the same way (no wrap-around)
+    assert call(1 << 40, 1 << 50) == bi.BI_ERR_INVALID_ARG
+    assert "more than 2^64 bytes" in bi.bi_last_error()
+    assert call(1 << 62, 1 << 62, Hq=1 << 30) == bi.BI_ERR_INVALID_ARG
+    # bad mode and bad shapes are refused before the size check
+    assert call(64, 4096, mode=3) == bi.BI_ERR_INVALID_ARG
+    assert call(64, 4096, hd=0) == bi.BI_ERR_INVALID_ARG
+
+
 def test_ssd_validation_without_gpu():
     lib = bi.load()
     assert bi.bi_ssd_state_bytes(4, 3, 64, 128, 64) == 0                      # H % G != 0

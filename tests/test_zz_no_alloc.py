@@ -7,8 +7,13 @@ the attention split partials in a fixed array of its own.  This test calls that
 entry point through the C ABI twice in a row, on two different problems (the
 second one finds the first one's partials still in the array), and checks each
 result against the ordinary workspace entry point; it also checks that a call
-too large for the array is refused with a clear error.  The file is named so
-that pytest collects it last.
+too large for the array is refused with a clear error (that check runs on the
+host before any CUDA call, and is tested on the CPU in test_abi.py, so that a
+regression shows up as a wrong status rather than an out-of-bounds launch).
+Decode-shaped calls take the other two schedules (one CTA per split for short
+contexts, the persistent one beyond four splits) and BI_FAST takes smaller
+splits, i.e. more partials; each is compared with a caller workspace too.  The
+file is named so that pytest collects it last.
 """
 import math
 
@@ -48,21 +53,34 @@ def _problem(seq_lens, Hq, Hkv, hd, seed):
                 hd=hd, kc=kc, vc=vc, bt=bt, max_blk=max_blk, max_ctx=max(seq_lens))
 
 
-def _with_workspace(pb):
+def _decode_rows(pb, seq_lens, pos):
+    """Single-token pieces at position `pos` of every sequence longer than it (a decode step)."""
+    keep = [b for b, n in enumerate(seq_lens) if pos < n]
+    offs = np.concatenate([[0], np.cumsum(seq_lens)])
+    rows = torch.tensor([int(offs[b]) + pos for b in keep], device="cuda")
+    d = dict(pb)
+    d.update(q=pb["q"][rows].contiguous(), T=len(keep), P=len(keep), max_q_len=1,
+             seq=torch.tensor(keep, dtype=torch.int32, device="cuda"),
+             row0=torch.arange(len(keep) + 1, dtype=torch.int32, device="cuda"),
+             pos0=torch.full((len(keep),), pos, dtype=torch.int32, device="cuda"))
+    return d
+
+
+def _with_workspace(pb, mode=bi.BI_INVARIANT):
     out = torch.empty((pb["T"], pb["Hq"] * pb["hd"]), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(bi.bi_attention_workspace_size(pb["T"], pb["Hq"], pb["hd"], pb["max_ctx"], 512),
                      dtype=torch.uint8, device="cuda")
     bi.bi_attention(pb["q"], pb["T"], pb["seq"], pb["row0"], pb["pos0"], pb["P"], pb["max_q_len"], pb["Hq"],
                     pb["Hkv"], pb["hd"], pb["kc"], pb["vc"], pb["bt"], pb["max_blk"], pb["kc"].shape[0],
-                    pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), ws, out)
+                    pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), ws, out, mode)
     return out
 
 
-def _static(pb):
+def _static(pb, mode=bi.BI_INVARIANT):
     out = torch.full((pb["T"], pb["Hq"] * pb["hd"]), float("nan"), dtype=torch.bfloat16, device="cuda")
     bi.bi_attention_static_scratch(pb["q"], pb["T"], pb["seq"], pb["row0"], pb["pos0"], pb["P"], pb["max_q_len"],
                                    pb["Hq"], pb["Hkv"], pb["hd"], pb["kc"], pb["vc"], pb["bt"], pb["max_blk"],
-                                   pb["kc"].shape[0], pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), out)
+                                   pb["kc"].shape[0], pb["max_ctx"], 512, 1.0 / math.sqrt(pb["hd"]), out, mode)
     return out
 
 
@@ -79,12 +97,17 @@ def test_static_scratch_attention_matches_workspace_attention_twice():
     assert bi.bi_device_status() == 0
 
 
-def test_static_scratch_refuses_calls_larger_than_the_array():
-    pb = _problem([64], 16, 4, 128, seed=3)
-    with pytest.raises(bi.BiError) as e:
-        # T rows whose partials would exceed 32 MiB: 20000 * 16 * 8 splits * 130 * 4 bytes
-        bi.bi_attention_static_scratch(pb["q"], 20000, pb["seq"], pb["row0"], pb["pos0"], 1, 64, 16, 4, 128,
-                                       pb["kc"], pb["vc"], pb["bt"], pb["max_blk"],
-                                       pb["kc"].shape[0], 4096, 512, 0.088, pb["q"])
-    assert e.value.status == bi.BI_ERR_INVALID_ARG
-    assert "static scratch array holds" in str(e.value)
+def test_static_scratch_decode_schedules_and_fast_mode_match_workspace():
+    lens = [3000, 2600, 700, 1]
+    pb = _problem(lens, 16, 4, 128, seed=4)
+    short = dict(_decode_rows(pb, lens, 650), max_ctx=2048)    # <= 4 splits: one CTA per (seq, kv head, split)
+    long_ = _decode_rows(pb, lens, 2999)                       # 6 splits: persistent schedule, TMA page streaming
+    for d in (short, long_, short):
+        want, got = _with_workspace(d), _static(d)
+        torch.cuda.synchronize()
+        assert same_bits(got, want)
+    # BI_FAST shrinks the split for decode-sized calls (more partials per row)
+    want, got = _with_workspace(long_, bi.BI_FAST), _static(long_, bi.BI_FAST)
+    torch.cuda.synchronize()
+    assert same_bits(got, want)
+    assert bi.bi_device_status() == 0
