@@ -163,7 +163,8 @@ def test_long_context_gqa_decoder_diff_zero():
     chunk 2048.  Rollout of 64 greedy tokens as one decode batch of 64 and as
     subsets of 1, 7 and 33 sequences in shuffled order; prefill chunks 2048 and
     1536; recompute with chunk 2048 and with 4096 in another packing order.
-    Every logprob is bit-equal; the oracle agrees on the two shortest sequences."""
+    Every logprob is bit-equal; the oracle agrees on the two shortest sequences
+    and on the one whose prompt is nearest 4096 tokens."""
     c = C5
     shape = c["shape"]
     n_gen = 64
@@ -204,9 +205,11 @@ def test_long_context_gqa_decoder_diff_zero():
     W = omodel.weights_to_f32(wb)
     errs = []
     short = np.argsort(lens)[:2]
-    for b in short:
+    near_4k = int(np.argmin(np.abs(lens - 4096)))           # 9 splits deep, scored by the oracle too
+    for b in list(short) + [near_4k]:
         _, want, _ = omodel.score_generation(W, shape, prompts[b], gens[b])
         errs.append(e2e_close(lp[b].cpu().numpy(), want, E2E_MAX_LONG, E2E_MEAN_LONG))
+        print("  sequence %d (prompt %d): max %.2e mean %.2e" % (b, lens[b], errs[-1].max(), errs[-1].mean()))
     errs = np.concatenate(errs)
     print("GQA long-context free-running oracle error: max %.2e mean %.2e" % (errs.max(), errs.mean()))
     anchored_parity(dec, wb, shape, [np.concatenate([prompts[short[0]], gens[short[0]][:-1]])], seed=5)
