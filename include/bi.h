@@ -103,7 +103,8 @@ bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, 
 bi_status bi_gemm(const void* A, int64_t M, int64_t K, const void* W, int64_t N, void* C, int c_dtype,
                   int epilogue, int mode, void* workspace, size_t ws_bytes, void* stream);
 size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int epilogue, int mode);
-/* The N tile width bi_gemm uses for a weight of shape (N, K) (diagnostic). */
+/* The N tile width bi_gemm uses for a weight of shape (N, K) (diagnostic):
+ * 16, 32, 64, 128 or 256, a function of (N, K, epilogue) only. */
 int bi_gemm_tile_n(int64_t N, int64_t K, int epilogue);
 
 /* Grouped GEMM over 128-row tiles, each tile owned by one expert

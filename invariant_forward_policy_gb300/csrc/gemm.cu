@@ -49,11 +49,12 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kATileBytes = kBM * kBK * 2;
 
-// TMA ring depth per tile width (about 144-192 KB of stages): deep enough that
-// a decode-size K range is mostly in flight at once.  It never changes results.
+// TMA ring depth per tile width (about 190-220 KB of stages): deep enough that
+// a decode-size K range of a small weight is in flight at once, all of it
+// requested before the dependency wait.  It never changes results.
 template <int BN>
 struct GemmSmem {
-  static constexpr int kStages = BN == 64 ? 6 : (BN == 128 ? 5 : 4);
+  static constexpr int kStages = BN == 16 ? 12 : (BN == 32 ? 11 : (BN == 64 ? 9 : (BN == 128 ? 5 : 4)));
   static constexpr int kBTileBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
   static constexpr int kBytes = 1024 + kStages * kStageBytes + 256;
@@ -100,24 +101,32 @@ __device__ __forceinline__ void tile_lse_step4(float& m, float& s, float& best, 
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
+// CW consecutive accumulator columns of this warp's 32 TMEM lanes (CW = 16 or 32).
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) tmem_ld_32x32b_x32(taddr, r);
+  else tmem_ld_32x32b_x16(taddr, r);
+}
+
 // Epilogue of one 128 x BN accumulator tile: this warp drains TMEM lanes
 // 32q..32q+31 (tile rows) from column base t_row and writes its rows.
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_row, int row, bool row_ok,
                                               bool do_store, int n_tile, int split) {
-  if (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU) {
+  if constexpr (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU) {
     const int j0 = n_tile * (BN / 2);
+    constexpr int CW = BN / 2 < 32 ? BN / 2 : 32;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
-      uint32_t g[32], u[32];
-      tmem_ld_32x32b_x32(t_row + c, g);
-      tmem_ld_32x32b_x32(t_row + BN / 2 + c, u);
+    for (int c = 0; c < BN / 2; c += CW) {
+      uint32_t g[CW], u[CW];
+      tmem_ld_cols<CW>(t_row + c, g);
+      tmem_ld_cols<CW>(t_row + BN / 2 + c, u);
       tmem_ld_wait();
       if (!(do_store && row_ok)) continue;
       if (EPI == EPI_SWIGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.C) + (size_t)row * args.ldc;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CW / 8; ++q) {
           const int col = j0 + c + q * 8;
           if (col >= args.n_out) break;
           uint4 v;
@@ -140,7 +149,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         float* pg = args.partial + ((size_t)split * args.M + row) * args.ldp;
         float* pu = pg + args.n_out;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < CW / 4; ++q) {
           const int col = j0 + c + q * 4;
           if (col >= args.n_out) break;
           *reinterpret_cast<float4*>(pg + col) =
@@ -152,7 +161,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         }
       }
     }
-  } else if (EPI == EPI_ROPE) {
+  } else if constexpr (EPI == EPI_ROPE) {
     // q/k heads: rotate-half pairs (j, j + hd/2) of bf16(acc) in fp32, rounded
     // to bf16; q to q_out, k and v into the paged cache at the row's position.
     const RopeKvArgs& ra = args.rope;
@@ -228,7 +237,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         }
       }
     }
-  } else if (EPI == EPI_LSE) {
+  } else if constexpr (EPI == EPI_LSE) {
+    static_assert(EPI != EPI_LSE || BN >= 64, "the fused log-softmax keeps 64+ wide vocab tiles");
     // fp32 logits of this row's BN columns, visited in column order
     const int n0 = n_tile * BN;
     const int tgt = (row_ok && args.ids) ? args.ids[row] : -1;
@@ -264,16 +274,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
     }
   } else {
     const int n0 = n_tile * BN;
+    constexpr int CW = BN < 32 ? BN : 32;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(t_row + c, r);
+    for (int c = 0; c < BN; c += CW) {
+      uint32_t r[CW];
+      tmem_ld_cols<CW>(t_row + c, r);
       tmem_ld_wait();
       if (!(do_store && row_ok)) continue;
       if (EPI == EPI_BF16) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.C) + (size_t)row * args.ldc;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < CW / 8; ++q) {
           const int col = n0 + c + q * 8;
           if (col >= args.n_out) break;
           uint4 v;
@@ -287,7 +298,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         float* out = (EPI == EPI_F32) ? static_cast<float*>(args.C) + (size_t)row * args.ldc
                                       : args.partial + ((size_t)split * args.M + row) * args.ldp;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < CW / 4; ++q) {
           const int col = n0 + c + q * 4;
           if (col >= args.n_out) break;
           *reinterpret_cast<float4*>(out + col) =
@@ -567,6 +578,13 @@ template <int EPI>
 static bi_status dispatch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2,
                              const GemmArgs& args, dim3 grid, cudaStream_t st) {
   switch (bn) {
+    case 16:
+      if constexpr (EPI != EPI_LSE && EPI != EPI_ROPE && EPI != EPI_SWIGLU && EPI != EPI_PARTIAL_SWIGLU)
+        return launch_tc<16, EPI>(a, b, b2, args, grid, st);
+      break;
+    case 32:
+      if constexpr (EPI != EPI_LSE && EPI != EPI_ROPE) return launch_tc<32, EPI>(a, b, b2, args, grid, st);
+      break;
     case 64: return launch_tc<64, EPI>(a, b, b2, args, grid, st);
     case 128: return launch_tc<128, EPI>(a, b, b2, args, grid, st);
     case 256: return launch_tc<256, EPI>(a, b, b2, args, grid, st);
@@ -589,13 +607,18 @@ static bi_status dispatch_epi(int epi, int bn, const CUtensorMap& a, const CUten
 }
 
 // Accumulator tile width for a weight: a function of its shape (N, K, number of
-// experts) only, never of M.  Small weights (under 2M elements) take 64-wide
-// tiles, so that a decode-size call spreads over many CTAs; larger ones 128,
-// and weights of 16M+ elements, 32K+ rows, or expert weights of 256+ rows
-// 256, where the tensor pipe rather than shared memory bandwidth bounds a
-// prefill-size call.
-static int tile_n_for(int64_t n_rows_w, int64_t K, bool /*swiglu*/, int64_t E = 1) {
+// experts) and of the epilogue only, never of M.  Dense weights under 1M
+// elements take 16-wide tiles, and SwiGLU weights under 2M elements 32-wide
+// ones (16 gate and 16 up columns), so that a decode-size call spreads a small
+// weight over many CTAs and each CTA's slice of it is in flight before the
+// dependency wait; other weights under 2M elements 64; then 128, and weights of 16M+ elements, 32K+ rows, or
+// expert weights of 256+ rows 256, where the tensor pipe rather than shared
+// memory bandwidth bounds a prefill-size call.  The fused log-softmax keeps
+// 64+ and the fused RoPE whole heads (both raised by the caller).
+static int tile_n_for(int64_t n_rows_w, int64_t K, bool swiglu, int64_t E = 1) {
   const int64_t elems = n_rows_w * K;
+  if (E == 1 && !swiglu && elems < (int64_t(1) << 20)) return 16;
+  if (E == 1 && swiglu && elems < (int64_t(1) << 21)) return 32;
   if (elems < (int64_t(1) << 21)) return 64;
   if (E > 1 && n_rows_w >= 256) return 256;  // expert weights: a layer's experts together are large
   if (elems < (int64_t(1) << 24) && n_rows_w < 32768) return 128;
@@ -607,9 +630,9 @@ static void fast_plan(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, int* 
   *bn = tile_n_for(n_rows_w, K, swiglu);
   *splits = 1;
   if (M > 128) return;
-  *bn = 64;
+  *bn = std::min(*bn, 64);
   const int64_t n_cols = swiglu ? n_rows_w / 2 : n_rows_w;
-  const int64_t tiles = cdiv(n_cols, swiglu ? 32 : 64);
+  const int64_t tiles = cdiv(n_cols, swiglu ? *bn / 2 : *bn);
   const int64_t kblocks = K / kBK;
   int64_t s = cdiv((int64_t)num_sms(), tiles);
   s = std::min<int64_t>(s, kblocks / 2 > 0 ? kblocks / 2 : 1);
@@ -645,6 +668,7 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
     fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
     if (g.lse || g.rope) splits = 1;  // fused epilogues keep whole K per tile; FAST narrows the tiles instead
   }
+  if (g.lse && bn < 64) bn = 64;  // the fused log-softmax records are per 64+ vocab columns
   if (g.rope) {
     // a tile must hold whole heads so that rotate-half pairs meet in one thread
     while (bn < g.rope->hd) bn *= 2;
@@ -786,7 +810,7 @@ namespace bi {
 static int lm_head_tile_n(int64_t T, int64_t V, int64_t K, int mode) {
   int bn = tile_n_for(V, K, false), splits = 1;
   if (mode == BI_FAST) fast_plan(T, V, K, false, &bn, &splits);
-  return bn;
+  return std::max(bn, 64);  // the records are per 64+ vocab columns (as run_gemm raises it)
 }
 
 size_t lm_head_partial_bytes(int64_t T, int64_t V, int64_t K, int mode) {

@@ -71,5 +71,5 @@ def test_plain_c_program_calls_the_library(tmp_path, lib_path):
     assert out["version"] == "100"
     assert out["rmsnorm_null"] == "1 msg"                                   # BI_ERR_INVALID_ARG with a message
     assert out["ssd_state_bytes"] == str(4 * (4 * 128 * 64 + 64 * 4 * 128 + 64 * 4 * 64 + 64 * 4))
-    assert int(out["gemm_tile_n"]) in (64, 128, 256)
+    assert int(out["gemm_tile_n"]) in (16, 32, 64, 128, 256)
     assert out["plan"] == "4 (0 0 4) (1 1 4) (1 0 2) (2 1 1)"               # the schedule of the Python test

@@ -60,9 +60,11 @@ def test_rmsnorm_rows_do_not_depend_on_batch():
 
 
 # ---------------------------------------------------------------------------- GEMM
-# tile widths: 64 below 2M weight elements, 128 below 16M (and N < 32768), else 256
+# tile widths: 16 below 1M weight elements (SwiGLU: 32 below 2M), 64 below 2M, 128 below 16M (and
+# N < 32768), else 256
 GEMM_SHAPES = [(1, 64, 64), (5, 1536, 512), (128, 512, 512), (129, 4096, 256), (300, 200, 576), (17, 32000, 512),
-               (260, 2816, 512), (131, 3072, 1024), (200, 8192, 2048), (3, 40000, 128)]
+               (260, 2816, 512), (131, 3072, 1024), (200, 8192, 2048), (3, 40000, 128), (16, 512, 1408),
+               (33, 2048, 768)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
@@ -96,7 +98,7 @@ def test_gemm_swiglu_epilogue(M, F, K):
     bf16_close(host_f32(C), want, ulps=2, frac_exact=0.9, atol=2e-2 * absdot * 2.0 ** -7)
 
 
-@pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408), (3072, 2048), (8192, 2048)])
+@pytest.mark.parametrize("N,K", [(1536, 512), (32000, 512), (512, 1408), (3072, 2048), (8192, 2048), (2048, 768)])
 def test_gemm_rows_invariant_to_M_and_order(N, K):
     rng = np.random.default_rng(N)
     ab, _ = rng_bf16(rng, (300, K))
@@ -112,6 +114,26 @@ def test_gemm_rows_invariant_to_M_and_order(N, K):
     perm = torch.from_numpy(rng.permutation(300)).cuda()
     outp = torch.empty_like(full)
     bi.bi_gemm(A[perm].contiguous(), 300, K, W, N, outp, bi.BI_DTYPE_FP32)
+    assert same_bits(outp, full[perm])
+
+
+@pytest.mark.parametrize("F,K", [(1408, 512), (64, 128), (5632, 2048)])
+def test_gemm_swiglu_rows_invariant_to_M_and_order(F, K):
+    """The SwiGLU epilogue's 32-, 128- and 256-wide tiles: a row's output bits do not
+    depend on how many rows the call has or where the row sits."""
+    rng = np.random.default_rng(F + K)
+    ab, _ = rng_bf16(rng, (300, K))
+    wb, _ = rng_bf16(rng, (2 * F, K), 0.05)
+    A, W = dev_bf16(ab), dev_bf16(wb)
+    full = torch.empty((300, F), dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm(A, 300, K, W, 2 * F, full, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
+    for M in (1, 16, 64, 129):
+        part = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
+        bi.bi_gemm(A[300 - M:].contiguous(), M, K, W, 2 * F, part, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
+        assert same_bits(part, full[300 - M:]), M
+    perm = torch.from_numpy(rng.permutation(300)).cuda()
+    outp = torch.empty_like(full)
+    bi.bi_gemm(A[perm].contiguous(), 300, K, W, 2 * F, outp, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
     assert same_bits(outp, full[perm])
 
 
@@ -363,6 +385,65 @@ def test_moe_route_topk_matches_oracle_and_ties():
     oi, ow = omoe.route_topk(x, k)
     assert np.array_equal(ids.cpu().numpy(), oi)
     assert np.max(np.abs(w.cpu().numpy() - ow)) < 1e-6
+
+
+def _stable_layout(ids, E, cap=0):
+    """Host reference: the rank of each (token, slot) pair among the earlier pairs of its
+    expert (a stable counting sort), then its row in the contiguous layout (expert ranges
+    padded to 128, in expert order) or the masked one (cap rows per expert, -1 beyond)."""
+    ids = np.asarray(ids).ravel()
+    seen = np.zeros(E, np.int64)
+    rank = np.empty(len(ids), np.int64)
+    for i, e in enumerate(ids):
+        rank[i] = seen[e]
+        seen[e] += 1
+    if cap:
+        rows = np.where(rank < cap, ids * cap + rank, -1)
+        return rows, None, np.arange(E * cap // 128) // (cap // 128)
+    off = np.concatenate([[0], np.cumsum((seen + 127) // 128 * 128)])
+    return off[ids] + rank, off, off
+
+
+@pytest.mark.parametrize("case", ["uniform", "skewed", "one_expert", "wide"])
+def test_moe_permute_is_a_stable_counting_sort(case):
+    """bi_moe_permute / bi_moe_permute_masked against a host stable counting sort, bit for bit:
+    ragged pair counts (not a multiple of the 1024-pair chunk), empty experts, one expert
+    taking every pair, E up to 1000, and masked capacity overflow (dropped and reported)."""
+    rng = np.random.default_rng({"uniform": 1, "skewed": 2, "one_expert": 3, "wide": 4}[case])
+    T, k, E = {"uniform": (4096, 8, 64), "skewed": (777, 8, 64), "one_expert": (300, 1, 64),
+               "wide": (2500, 4, 1000)}[case]
+    if case == "skewed":
+        ids = np.minimum(rng.geometric(0.15, (T, k)) - 1, E - 1)           # many empty experts
+    elif case == "one_expert":
+        ids = np.full((T, k), 17)
+    else:
+        ids = rng.integers(0, E, (T, k))
+    ids = ids.astype(np.int32)
+    d_ids = torch.from_numpy(ids).cuda()
+    max_rows = 128 * math.ceil((T * k + 127 * E) / 128)
+    ros = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+    tiles = torch.full((max_rows // 128,), -7, dtype=torch.int32, device="cuda")
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    pws = torch.empty(bi.bi_moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+    bi.bi_moe_permute(d_ids, T, k, E, max_rows, ros, tiles, offs, pws)
+    rows, off, _ = _stable_layout(ids, E)
+    assert np.array_equal(ros.cpu().numpy(), rows)
+    assert np.array_equal(offs.cpu().numpy(), off)
+    t_start = np.arange(max_rows // 128) * 128
+    owner = np.where(t_start < off[-1], np.searchsorted(off[1:], t_start, side="right"), -1)
+    assert np.array_equal(tiles.cpu().numpy(), owner)
+    assert bi.bi_device_status() == 0
+    # masked layout; the smallest capacity that holds every pair first, then one that drops some
+    need = int(np.bincount(ids.ravel(), minlength=E).max())
+    for cap, overflow in ((128 * math.ceil(need / 128), False), (128, need > 128)):
+        ros_m = torch.full((T * k,), -7, dtype=torch.int32, device="cuda")
+        tiles_m = torch.full((E * cap // 128,), -7, dtype=torch.int32, device="cuda")
+        bi.bi_moe_permute_masked(d_ids, T, k, E, cap, ros_m, tiles_m, pws)
+        rows_m, _, owner_m = _stable_layout(ids, E, cap)
+        assert np.array_equal(ros_m.cpu().numpy(), rows_m)
+        assert np.array_equal(tiles_m.cpu().numpy(), owner_m)
+        st = bi.bi_device_status()                     # reading it also clears it
+        assert (st == bi.BI_ERR_DEVICE_CHECK) == overflow, st
 
 
 @pytest.mark.parametrize("T", [1, 37, 512])
