@@ -13,6 +13,8 @@
 // function of the routing.  Row results do not depend on the layout anyway
 // because the grouped GEMM is row-invariant.
 #include <algorithm>
+#include <mutex>
+#include <string>
 
 #include "common.cuh"
 
@@ -64,121 +66,171 @@ __global__ void route_topk_kernel(const float* __restrict__ logits, int64_t T, i
 }
 
 // ------------------------------------------------------------------ layouts
-// rank[pair] = number of earlier pairs (in (token, slot) order) routed to the
-// same expert; counts[e] = pairs of expert e.  One CTA per expert.
+// The (token, slot) pairs are cut into chunks of kPermThreads in pair order.
+// Pass 1, one CTA per chunk: each pair's rank among the earlier pairs of its
+// chunk routed to the same expert (lanes of a warp by __match_any_sync, warps
+// by a scan in warp order) and the chunk's per-expert counts.  Pass 2, one CTA
+// per chunk: each CTA sums the counts of the earlier chunks, so a pair's rank
+// in its expert is its order in the whole (token, slot) sequence (a stable
+// counting sort), and places the pair in the contiguous layout (expert row
+// ranges padded to 128, in expert order) or the masked one (capacity rows per
+// expert).  Both passes are pure functions of the routing.
 constexpr int kPermThreads = 1024;
-__global__ void __launch_bounds__(kPermThreads) expert_rank_kernel(const int32_t* __restrict__ ids, int64_t n, int E,
-                                                                   int32_t* __restrict__ rank,
-                                                                   int32_t* __restrict__ counts, int* status) {
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads) expert_chunk_rank_kernel(const int32_t* __restrict__ ids, int64_t n,
+                                                                         int E, int32_t* __restrict__ rank,
+                                                                         int32_t* __restrict__ chunk_counts,
+                                                                         int* status) {
   pdl_trigger();
+  extern __shared__ int32_t hist[];  // [kPermWarps][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int j = tid; j < kPermWarps * E; j += kPermThreads) hist[j] = 0;
   pdl_wait();
-  const int e = blockIdx.x;
-  const int tid = threadIdx.x;
-  const int64_t per = (n + kPermThreads - 1) / kPermThreads;
-  const int64_t b = tid * per, en = min(n, b + per);
-  int c = 0;
-  for (int64_t i = b; i < en; ++i) {
-    const int32_t x = ids[i];
-    if (x == e) ++c;
-    if (e == 0 && (x < 0 || x >= E)) report(status, DEV_BAD_INDEX);
-  }
-  // exclusive block scan of c in thread order
-  __shared__ int warp_tot[32];
-  int incl = c;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if ((tid & 31) >= o) incl += y;
-  }
-  if ((tid & 31) == 31) warp_tot[tid >> 5] = incl;
-  __syncthreads();
-  if (tid < 32) {
-    int w = warp_tot[tid];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (tid >= o) wi += y;
+  const int64_t i = (int64_t)blockIdx.x * kPermThreads + tid;
+  int e = -1;
+  if (i < n) {
+    e = ids[i];
+    if (e < 0 || e >= E) {
+      report(status, DEV_BAD_INDEX);
+      e = -1;
     }
-    warp_tot[tid] = wi - w;  // exclusive prefix over warps
-    if (tid == 31) counts[e] = wi;
   }
   __syncthreads();
-  int r = warp_tot[tid >> 5] + incl - c;
-  for (int64_t i = b; i < en; ++i)
-    if (ids[i] == e) rank[i] = r++;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const int in_warp = __popc(same & ((1u << lane) - 1u));
+  if (e >= 0 && in_warp == 0) hist[warp * E + e] = __popc(same);
+  __syncthreads();
+  for (int x = tid; x < E; x += kPermThreads) {  // exclusive scan over the warps, in warp order
+    int run = 0;
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = hist[w * E + x];
+      hist[w * E + x] = run;
+      run += c;
+    }
+    chunk_counts[(int64_t)blockIdx.x * E + x] = run;
+  }
+  __syncthreads();
+  if (i < n) rank[i] = e >= 0 ? hist[warp * E + e] + in_warp : -1;
 }
 
-// Contiguous layout: expert offsets padded to 128 rows, and the tile owner map.
-__global__ void expert_offsets_kernel(const int32_t* __restrict__ counts, int E, int64_t max_tiles,
-                                      int32_t* __restrict__ offsets, int32_t* __restrict__ tile_expert, int* status) {
+// capacity == 0: contiguous layout (offsets written, expert ranges padded to
+// 128 rows); capacity > 0: masked layout (expert e owns rows [e*capacity,
+// (e+1)*capacity), pairs beyond it are dropped and reported).
+__global__ void __launch_bounds__(kPermThreads) expert_layout_kernel(
+    const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_counts,
+    int64_t n, int64_t n_chunks, int E, int64_t capacity, int64_t max_rows, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ tile_expert, int32_t* __restrict__ row_of_slot, int* status) {
   pdl_trigger();
+  extern __shared__ int32_t lay[];  // before[E], off[E + 1]
+  int32_t* before = lay;
+  int32_t* off = lay + E;
+  __shared__ int32_t warp_sum[kPermWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t chunk = blockIdx.x;
   pdl_wait();
-  __shared__ int32_t off[1025];
-  if (threadIdx.x == 0) {
-    int32_t o = 0;
-    for (int e = 0; e < E; ++e) {
-      off[e] = o;
-      o += (counts[e] + 127) / 128 * 128;
+  // pairs of each expert in the earlier chunks, and in all chunks (padded to 128)
+  int padded = 0;
+  for (int x = tid; x < E; x += kPermThreads) {
+    int p = 0, tot = 0;
+    for (int64_t c = 0; c < n_chunks; ++c) {
+      const int v = chunk_counts[c * E + x];
+      if (c < chunk) p += v;
+      tot += v;
     }
-    off[E] = o;
-    if ((int64_t)o > max_tiles * 128) report(status, DEV_BAD_INDEX);
+    before[x] = p;
+    if (x == tid) padded = (tot + 127) / 128 * 128;
+  }
+  if (capacity == 0) {  // block-wide exclusive scan of the padded sizes in expert order (E <= kPermThreads)
+    int incl = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = warp_sum[lane];
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      warp_sum[lane] = wi - w;
+    }
+    __syncthreads();
+    const int ex = warp_sum[warp] + incl - padded;
+    if (tid < E) off[tid] = ex;
+    if (tid == E - 1) off[E] = ex + padded;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = off[e];
-  for (int64_t t = threadIdx.x; t < max_tiles; t += blockDim.x) {
-    const int64_t r = t * 128;
+  if (capacity == 0 && chunk == 0) {
+    for (int x = tid; x <= E; x += kPermThreads) offsets[x] = off[x];
+    if (tid == 0 && (int64_t)off[E] > max_rows) report(status, DEV_BAD_INDEX);
+  }
+  // tile owners: CTA c writes tiles c, c + grid, ...
+  const int64_t max_tiles = max_rows / 128;
+  for (int64_t t = chunk * kPermThreads + tid; t < max_tiles; t += (int64_t)gridDim.x * kPermThreads) {
     int owner = -1;
-    if (r < off[E]) {
-      int lo = 0, hi = E - 1;  // last e with off[e] <= r
+    if (capacity > 0) {
+      owner = (int)(t / (capacity / 128));
+    } else if (t * 128 < off[E]) {
+      int lo = 0, hi = E - 1;  // last e with off[e] <= t * 128
       while (lo < hi) {
         const int mid = (lo + hi + 1) / 2;
-        if (off[mid] <= r) lo = mid; else hi = mid - 1;
+        if (off[mid] <= t * 128) lo = mid;
+        else hi = mid - 1;
       }
       owner = lo;
     }
     tile_expert[t] = owner;
   }
-}
-
-__global__ void row_of_slot_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, int64_t n,
-                                   const int32_t* __restrict__ offsets, int64_t capacity, int64_t max_rows,
-                                   int32_t* __restrict__ row_of_slot, int* status) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  const int32_t e = ids[i];
-  int64_t row;
-  if (capacity > 0) {  // masked layout
-    row = (rank[i] < capacity) ? e * capacity + rank[i] : -1;
-  } else {
-    row = offsets[e] + rank[i];
+  const int64_t i = chunk * kPermThreads + tid;
+  if (i < n) {
+    const int32_t e = ids[i];
+    const int32_t r = rank[i];
+    int64_t row = -1;
+    if (e >= 0 && e < E && r >= 0) {
+      const int64_t q = (int64_t)before[e] + r;
+      if (capacity > 0) row = q < capacity ? e * capacity + q : -1;
+      else row = off[e] + q;
+    }
+    if (row < 0 || row >= max_rows) {
+      report(status, DEV_BAD_INDEX);
+      row = -1;
+    }
+    row_of_slot[i] = (int32_t)row;
   }
-  if (row < 0 || row >= max_rows) {
-    report(status, DEV_BAD_INDEX);
-    row = -1;
-  }
-  row_of_slot[i] = (int32_t)row;
 }
 
-__global__ void masked_tiles_kernel(int32_t* tile_expert, int64_t n_tiles, int64_t tiles_per_expert) {
+// One warp per (token, slot) pair, kGatherWarps pairs per CTA; each lane keeps
+// four 16-byte loads in flight before its stores.
+constexpr int kGatherWarps = 8;
+__global__ void __launch_bounds__(kGatherWarps * 32) moe_gather_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                        const int32_t* __restrict__ row_of_slot,
+                                                                        int k, int64_t d, int64_t n_pairs,
+                                                                        __nv_bfloat16* __restrict__ xp) {
   pdl_trigger();
   pdl_wait();
-  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (t < n_tiles) tile_expert[t] = (int32_t)(t / tiles_per_expert);
-}
-
-__global__ void moe_gather_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_of_slot, int k,
-                                  int64_t d, __nv_bfloat16* __restrict__ xp) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t pair = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int64_t pair = (int64_t)blockIdx.x * kGatherWarps + (threadIdx.x >> 5);
+  if (pair >= n_pairs) return;
   const int32_t row = row_of_slot[pair];
   if (row < 0) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + (pair / k) * d);
   uint4* dst = reinterpret_cast<uint4*>(xp + (int64_t)row * d);
-  for (int64_t v = threadIdx.x; v < d / 8; v += blockDim.x) dst[v] = src[v];
+  const int64_t nv = d / 8;
+  for (int64_t v0 = lane; v0 < nv; v0 += 4 * 32) {
+    uint4 t[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (v0 + 32 * u < nv) t[u] = src[v0 + 32 * u];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (v0 + 32 * u < nv) dst[v0 + 32 * u] = t[u];
+  }
 }
 
 // out[t] = bf16( sum_s w[t,s] * y[row(t,s)] ), slots in order, fp32.
@@ -257,17 +309,38 @@ bi_status bi_moe_route_topk(const float* logits, int64_t T, int E, int k, int32_
 
 size_t bi_moe_permute_workspace_size(int64_t T, int k, int E) {
   if (T <= 0 || k <= 0 || E <= 0) return 0;
-  return ((size_t)T * k + (size_t)E + 64) * sizeof(int32_t);
+  const int64_t n = T * k, chunks = bi::cdiv(n, bi::kPermThreads);
+  return ((size_t)n + (size_t)chunks * E + 64) * sizeof(int32_t);
 }
 
-static bi_status permute_common(const int32_t* ids, int64_t T, int k, int E, void* workspace, size_t ws_bytes,
-                                int32_t** rank, int32_t** counts, cudaStream_t st) {
+// Both layouts: chunk ranks, then the layout pass (capacity 0 = contiguous).
+static bi_status permute_impl(const int32_t* ids, int64_t T, int k, int E, int64_t capacity, int64_t max_rows,
+                              int32_t* row_of_slot, int32_t* tile_expert, int32_t* expert_offsets, void* workspace,
+                              size_t ws_bytes, cudaStream_t st) {
   using namespace bi;
   BI_REQUIRE(workspace && ws_bytes >= bi_moe_permute_workspace_size(T, k, E), "permute workspace too small");
-  BI_REQUIRE(E >= 1 && E <= 1024, "E must be in [1, 1024]");
-  *rank = static_cast<int32_t*>(workspace);
-  *counts = *rank + T * k;
-  return launched(launch_pdl(expert_rank_kernel, dim3(E), dim3(kPermThreads), 0, st, ids, T * k, E, *rank, *counts, device_status_ptr()), "expert_rank_kernel");
+  BI_REQUIRE(E >= 1 && E <= kPermThreads, "E must be in [1, 1024]");
+  const int64_t n = T * k, chunks = cdiv(n, kPermThreads);
+  BI_REQUIRE(chunks < (int64_t(1) << 31) && max_rows < (int64_t(1) << 31), "too many pairs");
+  int32_t* rank = static_cast<int32_t*>(workspace);
+  int32_t* chunk_counts = rank + n;
+  const size_t hist_bytes = (size_t)kPermWarps * E * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(expert_chunk_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(kPermWarps * kPermThreads * sizeof(int32_t)));
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("permute smem attribute: ") + cudaGetErrorString(attr_err));
+  BI_TRY(launched(launch_pdl(expert_chunk_rank_kernel, dim3((unsigned)chunks), dim3(kPermThreads), hist_bytes, st, ids,
+                             n, E, rank, chunk_counts, device_status_ptr()),
+                  "expert_chunk_rank_kernel"));
+  const size_t lay_bytes = (size_t)(2 * E + 1) * sizeof(int32_t);
+  return launched(launch_pdl(expert_layout_kernel, dim3((unsigned)chunks), dim3(kPermThreads), lay_bytes, st, ids,
+                             (const int32_t*)rank, (const int32_t*)chunk_counts, n, chunks, E, capacity, max_rows,
+                             expert_offsets, tile_expert, row_of_slot, device_status_ptr()),
+                  "expert_layout_kernel");
 }
 
 bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t max_rows, int32_t* row_of_slot,
@@ -278,13 +351,8 @@ bi_status bi_moe_permute(const int32_t* ids, int64_t T, int k, int E, int64_t ma
   if (T == 0) return BI_OK;
   BI_REQUIRE(ids && row_of_slot && tile_expert && expert_offsets, "null pointer");
   BI_REQUIRE(max_rows % 128 == 0 && max_rows >= contiguous_rows(T, k, E), "max_rows too small");
-  cudaStream_t st = as_stream(stream);
-  int32_t *rank, *counts;
-  BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
-  BI_TRY(launched(launch_pdl(expert_offsets_kernel, dim3(1), dim3(256), 0, st, counts, E, max_rows / 128, expert_offsets, tile_expert,
-                                           device_status_ptr()), "expert_offsets_kernel"));
-  return launched(launch_pdl(row_of_slot_kernel, dim3((unsigned)cdiv(T * k, 256)), dim3(256), 0, st, ids, rank, T * k, expert_offsets, 0, max_rows,
-                                                                   row_of_slot, device_status_ptr()), "row_of_slot_kernel");
+  return permute_impl(ids, T, k, E, 0, max_rows, row_of_slot, tile_expert, expert_offsets, workspace, ws_bytes,
+                      as_stream(stream));
 }
 
 bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int64_t capacity, int32_t* row_of_slot,
@@ -294,13 +362,8 @@ bi_status bi_moe_permute_masked(const int32_t* ids, int64_t T, int k, int E, int
   if (T == 0) return BI_OK;
   BI_REQUIRE(ids && row_of_slot && tile_expert, "null pointer");
   BI_REQUIRE(capacity > 0 && capacity % 128 == 0, "capacity must be a positive multiple of 128");
-  cudaStream_t st = as_stream(stream);
-  int32_t *rank, *counts;
-  BI_TRY(permute_common(ids, T, k, E, workspace, ws_bytes, &rank, &counts, st));
-  const int64_t n_tiles = E * capacity / 128;
-  BI_TRY(launched(launch_pdl(masked_tiles_kernel, dim3((unsigned)cdiv(n_tiles, 256)), dim3(256), 0, st, tile_expert, n_tiles, capacity / 128), "masked_tiles_kernel"));
-  return launched(launch_pdl(row_of_slot_kernel, dim3((unsigned)cdiv(T * k, 256)), dim3(256), 0, st, ids, rank, T * k, nullptr, capacity, E * capacity,
-                                                                   row_of_slot, device_status_ptr()), "row_of_slot_kernel");
+  return permute_impl(ids, T, k, E, capacity, (int64_t)E * capacity, row_of_slot, tile_expert, nullptr, workspace,
+                      ws_bytes, as_stream(stream));
 }
 
 bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, int k, int64_t d, void* xp,
@@ -310,9 +373,10 @@ bi_status bi_moe_gather(const void* x, const int32_t* row_of_slot, int64_t T, in
   if (T == 0) return BI_OK;
   BI_REQUIRE(x && row_of_slot && xp, "null pointer");
   BI_REQUIRE(d % 8 == 0 && aligned16(x) && aligned16(xp), "d % 8 and 16-byte alignment required");
-  return launched(launch_pdl(moe_gather_kernel, dim3((unsigned)(T * k)), dim3(128), 0, as_stream(stream), static_cast<const __nv_bfloat16*>(x),
-                                                                      row_of_slot, k, d,
-                                                                      static_cast<__nv_bfloat16*>(xp)), "bi_moe_gather");
+  return launched(launch_pdl(moe_gather_kernel, dim3((unsigned)cdiv(T * k, kGatherWarps)), dim3(kGatherWarps * 32), 0,
+                             as_stream(stream), static_cast<const __nv_bfloat16*>(x), row_of_slot, k, d, T * k,
+                             static_cast<__nv_bfloat16*>(xp)),
+                  "bi_moe_gather");
 }
 
 size_t bi_moe_combine_workspace_size(int64_t T, int64_t d, int mode) {
