@@ -886,7 +886,8 @@ def config_table(args):
     rng = np.random.default_rng(C5["seed"] + 3)
     prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
     for fp8 in (False, True):
-        dec = Decoder(shape, wb, max_pos=max_ctx + 64, fp8=fp8)
+        # positions up to the longest prompt + the generated tokens (the recompute leg needs them)
+        dec = Decoder(shape, wb, max_pos=int(lens.max()) + C5["gen"] + 64, fp8=fp8)
         mb = -(-max_ctx // 64)
         bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
         cache = dec.alloc_cache(nb)
@@ -921,8 +922,6 @@ def config_table(args):
                       "KV of every context + all layer and lm_head weights read once per step (embedding rows "
                       "excluded)")})
         if not fp8:
-            del cache
-            torch.cuda.empty_cache()
             row("long_context_gqa_recompute_64seq", *_c5_recompute(dec, shape, lens, prompts, tf_s))
         dec.close()
         del cache
