@@ -598,6 +598,404 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   write_partial<HD>(a, P, row_valid, row_pos, row_tok, row_head, kv_begin, s, tq);
 }
 
+// ------------------------------------------------- tensor-memory prefill schedule
+// PREFILL on the 5th-generation tensor cores, for bf16 caches: a CTA owns
+// (piece, 128-row query tile, kv head, split); rows are the (token, q head of
+// the group) pairs as above.  S = Q K^T (K = hd in 16-wide steps, ascending)
+// and O += P V (K = 64 keys in 16-wide steps, ascending) accumulate in TMEM;
+// tcgen05.mma and mma.sync give the same fp32 bits step for step, so each row
+// gets exactly the arithmetic of the mma.sync schedules.  Each row belongs to
+// one thread of warps 0..3 (TMEM lane = row), which repeats attn_update's
+// operations in its order: scale and select-mask, the tile max, alpha, P =
+// exp2(v - m) with the row sum taken in the mma.sync quad order
+// ((s0 + s1) + (s2 + s3), s_q the sequential sum of keys 8j + 2q + {0, 1}),
+// l = l alpha + sum, O = O alpha (skipped when alpha is exactly 1, where it is
+// the identity), P rounded to bf16; and at every lane boundary the finished
+// lane folds into the running state with lane_merge's formula.
+// Warp 4 lane 0 streams the split's K and V pages by TMA (the persistent
+// decode kernel's tensor maps) into a ring; warp 5 owns TMEM and lane 0 issues
+// the MMAs, S of the next tile ahead of P V of this one.  V rows after the
+// CTA's last query position are zeroed in shared memory before P V (TMA copies
+// whole pages, and slots not yet written may hold anything); K rows there only
+// feed scores that the select-mask replaces.
+template <int HD>
+struct TcAttnLayout {
+  static constexpr int kQ = 128 * HD * 2;           // HD/64 boxes of 128 rows x 128 bytes
+  static constexpr int kPage = kKeys * HD * 2;      // one K or V page
+  static constexpr int kStages = HD == 128 ? 3 : 4;
+  static constexpr int kP = 128 * kKeys * 2;        // one P tile, 128 rows x 64 keys
+  static constexpr int kOffKV = kQ;
+  static constexpr int kOffP = kOffKV + kStages * 2 * kPage;
+  static constexpr int kOffBar = kOffP + 2 * kP;
+  static constexpr int kBytes = kOffBar + 256 + 1024;   // + barriers, + alignment slack
+  static constexpr uint32_t kCols = HD == 128 ? 512 : 256;  // S0, S1 (64 each), O, R (HD each)
+  static constexpr uint32_t kColS = 0, kColO = 128, kColR = 128 + HD;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
+                                                               const __grid_constant__ CUtensorMap tmk,
+                                                               const __grid_constant__ CUtensorMap tmv) {
+  using Lay = TcAttnLayout<HD>;
+  constexpr int NS = Lay::kStages;
+  constexpr int KB = HD / 64;  // 64-dim boxes per row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + Lay::kOffKV;  // stage st: K page at st * 2 * kPage, V page after it
+  uint8_t* sP = smem + Lay::kOffP;
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
+  uint64_t* kv_empty = kv_full + NS;
+  uint64_t* s_full = kv_empty + NS;   // [2] MMA -> softmax: S of a tile is in TMEM
+  uint64_t* s_empty = s_full + 2;     // [2] softmax -> MMA: S read (4 warp arrivals)
+  uint64_t* p_full = s_empty + 2;     // [2] softmax -> MMA: P written, O rescaled (4 warp arrivals)
+  uint64_t* o_done = p_full + 2;      // MMA -> softmax: P V of a tile has completed
+  uint64_t* q_full = o_done + 1;      // softmax -> MMA: Q tile loaded (128 thread arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int p = blockIdx.y;
+  const int kvh = blockIdx.z % a.Hkv;
+  const int s = blockIdx.z / a.Hkv;
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(q_full, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, Lay::kCols);
+    tmem_relinquish();
+  }
+  if (tid == 128) {
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // dependents may launch only once this CTA holds its TMEM columns
+  pdl_trigger();
+  pdl_wait();
+
+  const int row0 = a.pm.row0[p];
+  const int n_tok = a.pm.row0[p + 1] - row0;
+  const int tok_per_tile = 128 / a.group;
+  const int tok0 = blockIdx.x * tok_per_tile;
+  const int pos_first = a.pm.pos0[p];
+  const int kv_begin = s * a.split;
+  int n_tiles = 0, max_pos = -1;
+  if (tok0 < n_tok) {
+    max_pos = pos_first + min(n_tok, tok0 + tok_per_tile) - 1;
+    if (kv_begin <= max_pos) n_tiles = (min(kv_begin + a.split, max_pos + 1) - kv_begin + kKeys - 1) / kKeys;
+  }
+  const int tpl = (((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys) / kKeys;  // tiles per lane
+  const int seq = a.pm.seq[p];
+  const int32_t* bt = a.block_table + (int64_t)seq * a.max_blk;
+  const int t_begin = kv_begin / kKeys;
+
+  if (n_tiles > 0 && warp == 4) {
+    if (lane == 0) {
+      // ---------------- TMA producer: K and V pages of the split's tiles, in order
+      const int rows_total = (int)(a.n_blocks * a.Hkv * kKeys);
+      int t = 0;
+      for (; t < n_tiles && !*abort_flag; ++t) {
+        const int st = t % NS;
+        if (t >= NS && !mbar_wait(&kv_empty[st], ((t / NS) - 1) & 1)) {
+          report(a.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        const int blk_i = t_begin + t;
+        const int32_t blk = blk_i < a.max_blk ? bt[blk_i] : -1;
+        int row = rows_total;  // past the end: the copy reads zeros
+        if (blk >= 0 && blk < a.n_blocks) row = (int)((blk * a.Hkv + kvh) * kKeys);
+        else report(a.status, DEV_BAD_INDEX);
+        uint8_t* sk = sKV + st * 2 * Lay::kPage;
+        mbar_arrive_expect_tx(&kv_full[st], 2 * Lay::kPage);
+#pragma unroll
+        for (int b = 0; b < KB; ++b) {
+          tma_load_2d(sk + b * (kKeys * 128), &tmk, &kv_full[st], b * 64, row);
+          tma_load_2d(sk + Lay::kPage + b * (kKeys * 128), &tmv, &kv_full[st], b * 64, row);
+        }
+      }
+      // the copies this CTA started land before it can exit
+      for (int i = 0; i < NS && i < t; ++i) {
+        const int tt = t - 1 - i;
+        mbar_wait(&kv_full[tt % NS], (tt / NS) & 1);
+      }
+    }
+  } else if (n_tiles > 0 && warp == 5) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD) | (1u << 16);  // V read MN-major
+      bool ok = mbar_wait(q_full, 0);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % NS;
+        if (!mbar_wait(&kv_full[st], (j / NS) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&s_empty[j & 1], ((j - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sQ), ka = smem_u32(sKV + st * 2 * Lay::kPage);
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32, koff = (k >> 2) * (kKeys * 128) + (k & 3) * 32;
+          tc_mma_bf16(tmem + Lay::kColS + (j & 1) * kKeys, sw128_kmajor_desc(qa + off),
+                      sw128_kmajor_desc(ka + koff), idesc_s, k != 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int t = 0; ok && t < n_tiles && !*abort_flag; ++t) {
+        if (t + 1 < n_tiles && !issue_s(t + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(&p_full[t & 1], (t >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int st = t % NS;
+        const uint32_t pa = smem_u32(sP + (t & 1) * Lay::kP), va = smem_u32(sKV + st * 2 * Lay::kPage + Lay::kPage);
+#pragma unroll
+        for (int k = 0; k < kKeys / 16; ++k)
+          tc_mma_bf16(tmem + Lay::kColO, sw128_kmajor_desc(pa + k * 32),
+                      sw128_mnmajor_desc(va + k * 16 * 128, kKeys * 128, 1024), idesc_o, 1u);
+        tc_commit(o_done);
+        tc_commit(&kv_empty[st]);
+      }
+      if (!ok) {
+        report(a.status, DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  } else if (n_tiles > 0 && warp < 4) {
+    // ---------------- softmax warps: thread = row = TMEM lane
+    const int r = tid;
+    const int ti = tok0 + r / a.group;
+    const bool row_valid = ti < n_tok;
+    const int row_tok = row0 + ti, row_pos = pos_first + ti, row_head = kvh * a.group + (r % a.group);
+    // Q row into the swizzled tile (zeros for rows past the piece)
+    {
+      const __nv_bfloat16* qr = a.q + ((int64_t)row_tok * a.Hq + row_head) * HD;
+#pragma unroll
+      for (int ch = 0; ch < HD / 8; ++ch) {
+        const int within = ch & 7;
+        uint8_t* dst = sQ + (ch >> 3) * (128 * 128) + r * 128 + ((within ^ (r & 7)) << 4);
+        cp_async16(dst, row_valid ? qr + ch * 8 : a.q, row_valid);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async();
+      mbar_arrive(q_full);
+    }
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tO = trow + Lay::kColO, tR = trow + Lay::kColR;
+    auto zero_o = [&]() {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) tmem_st_32x32b_x32(tO + c, z);
+      tmem_st_wait();
+    };
+    float m = -INFINITY, l = 0.f, Rm = -INFINITY, Rl = 0.f;
+    // R <- lane_merge(R, (m, l, O)): P.acc = P.acc a + acc b, or a copy into an empty R
+    auto fold_lane = [&]() {
+      const bool has = m != -INFINITY;
+      const bool copy = has && Rm == -INFINITY;
+      const float M = fmaxf(Rm, m);
+      const float fa = (Rm == M) ? 1.0f : exp2f(__fsub_rn(Rm, M));
+      const float fb = (m == M) ? 1.0f : exp2f(__fsub_rn(m, M));
+      if (__any_sync(0xffffffffu, has)) {
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t rr[32], oo[32];
+          tmem_ld_32x32b_x32(tR + c, rr);
+          tmem_ld_32x32b_x32(tO + c, oo);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float rv = __uint_as_float(rr[i]), ov = __uint_as_float(oo[i]);
+            const float nv = copy ? ov : (has ? __fadd_rn(__fmul_rn(rv, fa), __fmul_rn(ov, fb)) : rv);
+            rr[i] = __float_as_uint(nv);
+          }
+          tmem_st_32x32b_x32(tR + c, rr);
+        }
+        tmem_st_wait();
+      }
+      if (copy) {
+        Rm = m;
+        Rl = l;
+      } else if (has) {
+        Rl = __fadd_rn(__fmul_rn(Rl, fa), __fmul_rn(l, fb));
+        Rm = M;
+      }
+    };
+    // every decision that gates a warp-collective tcgen05.ld / st is taken for the
+    // whole warp at once (a wait that gives up on any lane stops all of them)
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool got = mbar_wait(bar, parity) && !*abort_flag;
+      return __all_sync(0xffffffffu, got);
+    };
+    zero_o();
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int key0 = (t_begin + t) * kKeys;
+      const bool lane_start = t > 0 && t % tpl == 0;
+      if (!warp_wait(&s_full[t & 1], (t >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[kKeys];
+      {
+        uint32_t sr[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld_32x32b_x32(trow + Lay::kColS + (t & 1) * kKeys + h * 32, sr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(sr[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[t & 1]);
+      if (t > 0) {  // P V of the previous tile has landed in O
+        if (!warp_wait(o_done, (t - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if (lane_start) {
+        fold_lane();
+        zero_o();
+        m = -INFINITY;
+        l = 0.f;
+      }
+      // scale and mask, tile max
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        const bool okc = row_valid && key0 + c <= row_pos;
+        v[c] = okc ? __fmul_rn(v[c], a.scale_log2) : -INFINITY;
+        tmax = fmaxf(tmax, v[c]);
+      }
+      const float m_new = fmaxf(m, tmax);
+      const float alpha = (m_new == m) ? 1.0f : exp2f(__fsub_rn(m, m_new));
+      // P and the row sum in the quad order of the mma.sync fragments
+      float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = j * 8 + q * 2 + e;
+            const float pv = (v[c] == -INFINITY) ? 0.f : exp2f(__fsub_rn(v[c], m_new));
+            v[c] = pv;
+            sq[q] = __fadd_rn(sq[q], pv);
+          }
+        }
+      }
+      const float rs = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
+      l = __fadd_rn(__fmul_rn(l, alpha), rs);
+      m = m_new;
+      // O = O alpha (identity where alpha == 1; O is +0 at a lane's first tile)
+      if (t > 0 && !lane_start && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t oo[32];
+          tmem_ld_32x32b_x32(tO + c, oo);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha));
+          tmem_st_32x32b_x32(tO + c, oo);
+        }
+        tmem_st_wait();
+      }
+      // the last tile may hold keys after the CTA's last position: zero those V rows
+      const int st = t % NS;
+      if (key0 + kKeys - 1 > max_pos) {
+        if (!warp_wait(&kv_full[st], (t / NS) & 1)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sv = sKV + st * 2 * Lay::kPage + Lay::kPage;
+        for (int i = tid; i < kKeys * KB * 8; i += 128) {  // (key, 16-byte chunk): whole rows, any chunk order
+          const int key = i / (KB * 8), ch = i % (KB * 8);
+          if (key0 + key > max_pos)
+            *reinterpret_cast<uint4*>(sv + (ch >> 3) * (kKeys * 128) + key * 128 + ((ch & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P row in bf16 into the swizzled P tile
+      uint8_t* prow = sP + (t & 1) * Lay::kP + r * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 w;
+        w.x = pack_bf16x2(v[ch * 8 + 0], v[ch * 8 + 1]);
+        w.y = pack_bf16x2(v[ch * 8 + 2], v[ch * 8 + 3]);
+        w.z = pack_bf16x2(v[ch * 8 + 4], v[ch * 8 + 5]);
+        w.w = pack_bf16x2(v[ch * 8 + 6], v[ch * 8 + 7]);
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = w;
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      // this warp's P rows (and its share of the zeroed V rows) are written; the
+      // MMA waits for all four warps
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t & 1]);
+    }
+    if (ok && warp_wait(o_done, (n_tiles - 1) & 1)) {
+      tc_fence_after();
+      fold_lane();
+      // the split partial (m, l, acc) of this row; every lane loads, rows that
+      // have no key in this split store nothing
+      const bool store = row_valid && row_pos >= kv_begin;
+      const int64_t pidx = ((int64_t)row_tok * a.Hq + row_head) * a.nsplit + s;
+      float* po = a.part_o + pidx * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t rr[32];
+        tmem_ld_32x32b_x32(tR + c, rr);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(po + c + i) = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
+                                                               __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+        }
+      }
+      if (store) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
+    } else {
+      report(a.status, DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Lay::kCols);
+  }
+}
+
 // ----------------------------------------------------------- decode schedule
 // Persistent DECODE schedule, for query tiles of at most 16 rows over long
 // contexts: the same per-row arithmetic as above, with the four lanes of a
@@ -1081,6 +1479,27 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
                   "attention_decode_kernel");
 }
 
+// Tensor-memory prefill launch: K and V viewed as the persistent decode kernel
+// views them (2-D bf16 [n_blocks * Hkv * 64, hd], 64 x 64 boxes, 128-byte swizzle).
+template <int HD>
+static bi_status launch_attention_tc(const AttnArgs& args, dim3 grid, cudaStream_t st) {
+  constexpr int smem = TcAttnLayout<HD>::kBytes;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attention_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("attention prefill attributes: ") + cudaGetErrorString(attr_err));
+  const uint64_t rows = (uint64_t)args.n_blocks * args.Hkv * kKeys;
+  CUtensorMap tmk, tmv;
+  if (!encode_tmap_2d_bf16(&tmk, args.k_cache, HD, rows, HD * 2, 64, kKeys, true) ||
+      !encode_tmap_2d_bf16(&tmv, args.v_cache, HD, rows, HD * 2, 64, kKeys, true))
+    return fail(BI_ERR_CUDA, "attention prefill: cuTensorMapEncodeTiled failed for the K/V cache");
+  return launched(launch_pdl(attention_tc_kernel<HD>, grid, dim3(192), smem, st, args, tmk, tmv),
+                  "attention_tc_kernel");
+}
+
 // Positions per split: the fixed kv_split, or (BI_FAST) a size chosen from the
 // batch so that the decode grid fills the GPU (flash-decoding heuristic).
 static int choose_split(int mode, int kv_split, int64_t P, int64_t max_q_len, int Hkv, int group, int64_t max_ctx) {
@@ -1207,12 +1626,13 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
   args.split = split;
   args.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = as_stream(stream);
-  // Three schedules with the same per-row arithmetic (so the same bits):
+  // Four schedules with the same per-row arithmetic (so the same bits):
   // query tiles of at most 16 rows (decode steps) take the lane-parallel
   // schedule, persistent with TMA page streaming once contexts span more than
   // kDecPersistentSplits splits (and the call has at most kDecMaxPieces
-  // sequences), one CTA per (sequence, kv head, split)
-  // otherwise; bigger query tiles take the row-parallel schedule.
+  // sequences), one CTA per (sequence, kv head, split) otherwise; bigger query
+  // tiles take the tensor-memory prefill schedule (bf16 caches) or the
+  // mma.sync row-parallel one (FP8 caches).
   const bool decode = max_q_len * group <= 16;
   if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
     BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
@@ -1230,6 +1650,10 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
     else
       BI_TRY(hd == 64 ? launch_attention<64, true, false>(args, grid, st)
                       : launch_attention<128, true, false>(args, grid, st));
+  } else if (!kv8 && n_blocks * Hkv * kKeys < (int64_t(1) << 31)) {
+    // bf16 cache: 128-row query tiles on the tensor cores (TMA page coordinates are 32-bit)
+    dim3 grid((unsigned)cdiv(max_q_len * group, 128), (unsigned)P, (unsigned)(Hkv * ns));
+    BI_TRY(hd == 64 ? launch_attention_tc<64>(args, grid, st) : launch_attention_tc<128>(args, grid, st));
   } else {
     dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
     if (kv8)

@@ -49,6 +49,14 @@ int num_sms();
 // out-of-range index, record a code here instead of trapping.
 enum DeviceCode : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 int* device_status_ptr();  // device address of the status word (current device and context)
+// Grouped GEMM whose A rows are gathered by TMA: row r of the M_rows-row
+// operand is row a_rows[r] of A [a_src_rows, K] (int32 [M_rows], 16-byte
+// aligned).  Same tiles, K order and bits as bi_grouped_gemm on the gathered
+// copy; the MoE layer's gate/up projection reads the token rows in place.
+bi_status grouped_gemm_rows(const void* A, int64_t a_src_rows, const int32_t* a_rows, int64_t M_rows, int64_t K,
+                            const void* W, int64_t E, int64_t N, const int32_t* tile_expert, void* C, int c_dtype,
+                            int epilogue, cudaStream_t st);
+
 
 // Device addresses of a module's __device__ symbol, remembered per device
 // together with the unique id of the context they were looked up in: a
@@ -222,6 +230,15 @@ BI_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// Four rows r0..r3 of a 2-D tensor (box: one row of box_inner columns from
+// column c0) into consecutive rows at dst; the tensor map's box is one row high.
+BI_DEV void tma_gather4_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
 BI_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -283,6 +300,18 @@ BI_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 BI_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 32 lanes x 32 bit, 32 consecutive columns: thread i of the warp writes lane (base + i).
+BI_DEV void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+BI_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand written by TMA with
 // 128-byte swizzle: 8-row core groups 1024 bytes apart (stride byte offset),
@@ -294,6 +323,21 @@ BI_DEV uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset
   d |= (uint64_t)1 << 46;                           // version
   d |= (uint64_t)2 << 61;                           // SWIZZLE_128B
+  return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand with 128-byte
+// swizzle: rows of 64 consecutive MN elements (128 bytes) per K index, 8 K rows
+// per 1024-byte swizzle atom; `lbo` = bytes between 64-element groups along MN,
+// `sbo` = bytes between 8-row groups along K.  (A V page as the paged cache's
+// TMA copy leaves it: key rows of 64 head dims, one box per 64 dims.)
+BI_DEV uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 
