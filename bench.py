@@ -976,8 +976,9 @@ def run_kernel_case(name: str, reps: int):
     import invariant_forward_policy_gb300 as bi
     torch.manual_seed(0)
     dev = torch.device("cuda")
-    if name in ("gemm_decode_qkv", "gemm_decode_lm_head", "gemm_prefill"):
+    if name in ("gemm_decode_qkv", "gemm_decode_down", "gemm_decode_lm_head", "gemm_prefill"):
         M, N, K, dt = {"gemm_decode_qkv": (16, 1536, 512, bi.BI_DTYPE_BF16),
+                       "gemm_decode_down": (16, 512, 1408, bi.BI_DTYPE_BF16),
                        "gemm_decode_lm_head": (16, 32000, 512, bi.BI_DTYPE_FP32),
                        "gemm_prefill": (8192, 5632 * 2, 2048, bi.BI_DTYPE_BF16)}[name]
         A = (0.5 * torch.randn((M, K), device=dev)).to(torch.bfloat16)
@@ -1177,6 +1178,17 @@ def run_kernel_case(name: str, reps: int):
         ids = torch.randint(0, V, (T,), dtype=torch.int32, device=dev)
         for _ in range(reps):
             bi.bi_logprob_gather(logits, ids, T, V, lp)
+    elif name == "lm_head_fused_decode":
+        # the dense decoder's decode-step head: 16 rows x 512 -> 32000, fused log-softmax records + merge
+        T, d, V = 16, 512, 32000
+        H = torch.randn((T, d), device=dev).to(torch.bfloat16)
+        W = (0.02 * torch.randn((V, d), device=dev)).to(torch.bfloat16)
+        lp = torch.empty(T, device=dev)
+        am = torch.empty(T, dtype=torch.int32, device=dev)
+        ws = torch.empty(bi.bi_lm_head_logprob_workspace_size(T, V, d, bi.BI_INVARIANT), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(reps):
+            bi.bi_lm_head_logprob(H, T, d, W, V, None, lp, am, bi.BI_INVARIANT, ws)
     elif name == "lm_head_fused":
         # fused lm_head + log-softmax records + merge, 2048 rows x 4096 -> 129280
         T, d, V = 2048, 4096, 129280
@@ -1210,7 +1222,8 @@ def run_kernel_case(name: str, reps: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", default=None,
-                    help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_lm_head, gemm_prefill, "
+                    help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_down, gemm_decode_lm_head, "
+                         "lm_head_fused_decode, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
                          "kv_fp8_gather, c5_decode, topk_prefill, attention_prefill_long, rmsnorm, logprob, lm_head_fused, "
                          "moe_layer) or "
