@@ -34,6 +34,15 @@ constexpr int kF8BN = 256;      // output tile width: two weight blocks
 constexpr int kF8Stages = 4;
 constexpr int kF8TileBytes = 128 * kF8Block;       // A: 128 rows x 128 fp8
 constexpr int kF8BTileBytes = kF8BN * kF8Block;    // W: 256 rows x 128 fp8
+// acc (two fp32 lanes) += (x0, x1) * (s, s) with one rounding each: a packed fp32 FMA.
+__device__ __forceinline__ void fma2_acc(unsigned long long& acc, uint32_t x0, uint32_t x1, unsigned long long ss) {
+  unsigned long long x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(x0), "r"(x1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(ss));
+}
+__device__ __forceinline__ float lo_f32(unsigned long long v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32(unsigned long long v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
 constexpr int kF8Threads = 320;                    // TMA, MMA, 8 promotion warps
 constexpr int kF8SmemBytes = 1024 + kF8Stages * (kF8TileBytes + kF8BTileBytes) + 256;
 
@@ -228,9 +237,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
       const int row = mt * 128 + q * 32 + lane;
       const int wblk = nt * 2 + hf;                       // weight block row of this half
       const bool valid = row < args.M && wblk * kF8Block < args.N;
-      float acc[kF8Block];
+      unsigned long long acc2[kF8Block / 2];  // fp32 pairs (columns 2i, 2i + 1)
 #pragma unroll
-      for (int c = 0; c < kF8Block; ++c) acc[c] = 0.f;
+      for (int c = 0; c < kF8Block / 2; ++c) acc2[c] = 0ull;
       for (int kb = 0; kb < nk; ++kb, ++pb) {
         const int j = pb & 1;
         const float sc = valid ? args.sa[(int64_t)row * nk + kb] * args.sw[(int64_t)wblk * nk + kb] : 0.f;
@@ -242,14 +251,16 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + j * kF8BN + hf * kF8Block + ((uint32_t)(q * 32) << 16);
+        // acc += partial * (scale_a * scale_w), one rounding per element (paired fp32 FMA);
+        // 16 columns per TMEM round trip
+        const unsigned long long sc2 = ((unsigned long long)__float_as_uint(sc) << 32) | __float_as_uint(sc);
 #pragma unroll
         for (int c = 0; c < kF8Block / 16; ++c) {
           uint32_t p[16];
           tmem_ld_32x32b_x16(taddr + c * 16, p);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            acc[c * 16 + i] = __fadd_rn(acc[c * 16 + i], __fmul_rn(__uint_as_float(p[i]), sc));
+          for (int i = 0; i < 16; i += 2) fma2_acc(acc2[(c * 16 + i) / 2], p[i], p[i + 1], sc2);
         }
         tc_fence_before();
         __syncwarp();
@@ -261,14 +272,16 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.C) + base);
 #pragma unroll
         for (int v = 0; v < kF8Block / 4; ++v)
-          dst[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+          dst[v] = make_float4(lo_f32(acc2[2 * v]), hi_f32(acc2[2 * v]), lo_f32(acc2[2 * v + 1]),
+                               hi_f32(acc2[2 * v + 1]));
       } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.C) + base);
 #pragma unroll
         for (int v = 0; v < kF8Block / 8; ++v)
-          dst[v] = make_uint4(pack_bf16x2(acc[8 * v], acc[8 * v + 1]), pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                              pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
-                              pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
+          dst[v] = make_uint4(pack_bf16x2(lo_f32(acc2[4 * v]), hi_f32(acc2[4 * v])),
+                              pack_bf16x2(lo_f32(acc2[4 * v + 1]), hi_f32(acc2[4 * v + 1])),
+                              pack_bf16x2(lo_f32(acc2[4 * v + 2]), hi_f32(acc2[4 * v + 2])),
+                              pack_bf16x2(lo_f32(acc2[4 * v + 3]), hi_f32(acc2[4 * v + 3])));
       }
     }
   }
