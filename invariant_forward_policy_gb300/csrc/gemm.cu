@@ -57,31 +57,8 @@ struct GemmSmem {
   static constexpr int kStages = BN == 16 ? 12 : (BN == 32 ? 11 : (BN == 64 ? 9 : (BN == 128 ? 5 : 4)));
   static constexpr int kBTileBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kATileBytes + kBTileBytes;
-  static constexpr int kData = kStages * kStageBytes;     // the A and W rings
-  static constexpr int kBytes = 1024 + 1024 + kData;     // + alignment slack + barriers
+  static constexpr int kBytes = 1024 + kStages * kStageBytes + 256;
 };
-
-// A call with fewer than 128 rows copies only its rows of A (a_box_rows,
-// rounded up to 8) and packs the A stages at that pitch (1024-byte aligned,
-// as the 128-byte swizzle needs).  The MMA still reads a 128-row window from
-// each stage; its rows past the copied ones fall on the next stages' data and
-// only feed accumulator rows that are never stored (MMA rows never mix).  The
-// ring then holds far more stages in the same shared memory, so a small
-// weight's whole K range is requested before the dependency wait.  Ring depth
-// and A pitch change which bytes sit where, never a stored value.
-constexpr int kMaxStages = 48;
-template <int BN>
-__host__ __device__ constexpr int gemm_a_pitch(int a_box_rows) {
-  return a_box_rows >= kBM ? kATileBytes : (a_box_rows * kBK * 2 + 1023) / 1024 * 1024;
-}
-template <int BN>
-__host__ __device__ constexpr int gemm_stages(int a_box_rows) {
-  using S = GemmSmem<BN>;
-  const int pitch = gemm_a_pitch<BN>(a_box_rows);
-  if (pitch == kATileBytes) return S::kStages;
-  const int n = (S::kData - (kATileBytes - pitch)) / (pitch + S::kBTileBytes);
-  return n < kMaxStages ? n : kMaxStages;
-}
 
 struct GemmArgs {
   void* C;
@@ -100,7 +77,6 @@ struct GemmArgs {
   int m_tiles, n_tiles_grid, splits;  // tile space walked by the persistent CTAs
   int a_box_rows;                     // rows of A one TMA copy brings in (128, or M rounded up to 8 when M < 128)
   int group_m;                        // M-tiles per rasterisation group
-  const int32_t* a_rows;              // grouped only: A row of each tile row (A gathered by TMA), or NULL
   RopeKvArgs rope;                    // EPI_ROPE only
 };
 
@@ -371,18 +347,16 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmB2,
                                                          const GemmArgs args) {
   using S = GemmSmem<BN>;
-  const int kStages = gemm_stages<BN>(args.a_box_rows);
-  const int a_pitch = gemm_a_pitch<BN>(args.a_box_rows);
+  constexpr int kStages = S::kStages;
   constexpr bool kSwiglu = (EPI == EPI_SWIGLU || EPI == EPI_PARTIAL_SWIGLU);
   constexpr uint32_t kTmemCols = 2 * BN;  // two accumulator buffers
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // [barriers, 1 KB][A ring: stages x a_pitch, then the last 128-row window][W ring]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* sA = smem + 1024;
-  uint8_t* sB = sA + (kStages - 1) * a_pitch + kATileBytes;
-  uint64_t* empty = full + kMaxStages;
-  uint64_t* acc_full = empty + kMaxStages;  // [2] MMA -> epilogue
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * S::kBTileBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;   // [2] MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA (4 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -422,57 +396,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   // expert of an M-tile (grouped GEMM); -1 tiles are skipped by every role alike
   auto tile_expert = [&](int m_tile) { return args.tile_expert ? args.tile_expert[m_tile] : 0; };
 
-  if (warp == 0 && args.a_rows) {
-    // ---------------- TMA producer, A gathered row by row: lane l copies tile rows
-    // 4l..4l+3 from the rows args.a_rows names, lane 0 runs the ring and the W loads
-    const uint32_t stage_bytes = (uint32_t)kBM * kBK * 2 + S::kBTileBytes;
-    int kb_total = 0;
-    pdl_wait();
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      if (__shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0)) break;
-      const TileCoord tc = tile_coord(t, m_tiles, n_tiles, args.group_m);
-      const int expert = tile_expert(tc.m_tile);
-      if (expert < 0) continue;
-      const int4 rows = reinterpret_cast<const int4*>(args.a_rows + (int64_t)tc.m_tile * kBM)[lane];
-      bool ok = true;
-      for (int kb = 0; kb < nk; ++kb, ++kb_total) {
-        const int s = kb_total % kStages;
-        const uint32_t ph = (kb_total / kStages) & 1;
-        int go = 1;
-        if (lane == 0) {
-          go = mbar_wait(&empty[s], ph ^ 1) && !*abort_flag;
-          if (go) mbar_arrive_expect_tx(&full[s], stage_bytes);
-          else {
-            report(args.status, DEV_TIMEOUT);
-            *abort_flag = 1;
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, go, 0)) {
-          ok = false;
-          break;
-        }
-        const int kc = (tc.split * nk + kb) * kBK;
-        tma_gather4_2d(sA + s * a_pitch + lane * 4 * (kBK * 2), &tmA, &full[s], kc, rows.x, rows.y, rows.z, rows.w);
-        if (lane == 0) {
-          const int wbase = expert * args.w_rows_per_expert;
-          if (kSwiglu) {
-            const int j0 = tc.n_tile * (BN / 2);
-            tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + j0);
-            tma_load_2d(sB + s * S::kBTileBytes + (BN / 2) * kBK * 2, &tmB2, &full[s], kc,
-                        wbase + args.up_offset + j0);
-          } else {
-            tma_load_2d(sB + s * S::kBTileBytes, &tmB, &full[s], kc, wbase + tc.n_tile * BN);
-          }
-        }
-      }
-      if (!ok) break;
-    }
-    if (lane == 0)  // let the last copies this CTA started land before it can exit
-      for (int i = 0; i < kStages && i < kb_total; ++i) {
-        const int kb = kb_total - 1 - i;
-        mbar_wait(&full[kb % kStages], (kb / kStages) & 1);
-      }
-  } else if (warp == 0) {
+  if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       auto load_w = [&](int expert, int n_tile, int kc, int s) {
@@ -512,7 +436,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           if (expert < 0) continue;
         }
         for (int kb = 0; kb < pre; ++kb)
-          tma_load_2d(sA + kb * a_pitch, &tmA, &full[kb], (tc.split * nk + kb) * kBK, tc.m_tile * kBM);
+          tma_load_2d(sA + kb * kATileBytes, &tmA, &full[kb], (tc.split * nk + kb) * kBK, tc.m_tile * kBM);
         kb_total += pre;
         for (int kb = pre; kb < nk; ++kb, ++kb_total) {
           const int s = kb_total % kStages;
@@ -524,7 +448,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           }
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           const int kc = (tc.split * nk + kb) * kBK;
-          tma_load_2d(sA + s * a_pitch, &tmA, &full[s], kc, tc.m_tile * kBM);
+          tma_load_2d(sA + s * kATileBytes, &tmA, &full[s], kc, tc.m_tile * kBM);
           load_w(expert, tc.n_tile, kc, s);
         }
       }
@@ -564,7 +488,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + s * a_pitch);
+          const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
           const uint32_t b_addr = smem_u32(sB + s * S::kBTileBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
@@ -734,8 +658,6 @@ struct GemmCall {
   const int32_t* ids = nullptr;  // fused log-softmax: targets (NULL = greedy)
   TileLse* lse = nullptr;        // fused log-softmax: tile partials (non-NULL selects it)
   const RopeKvArgs* rope = nullptr;  // fused RoPE + paged KV write (non-NULL selects it)
-  const int32_t* a_rows = nullptr;   // grouped: A row of each of the M rows (A = [a_src_rows, K], gathered by TMA)
-  int64_t a_src_rows = 0;
 };
 
 static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
@@ -762,9 +684,8 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   // a dense call with M < 128 copies only its M rows (rounded up to 8) of A per stage
   const int a_box_rows = (g.M < kBM && g.E == 1 && !g.tile_expert) ? (int)std::max<int64_t>(8, cdiv(g.M, 8) * 8)
                                                                     : kBM;
-  const bool a_ok = g.a_rows ? encode_tmap_2d_bf16(&ta, g.A, g.K, g.a_src_rows, g.K * 2, kBK, 1, true)
-                             : encode_tmap_2d_bf16(&ta, g.A, g.K, g.M, g.K * 2, kBK, (uint32_t)a_box_rows, true);
-  if (!a_ok) return fail(BI_ERR_CUDA, "gemm: TMA descriptor for A failed");
+  if (!encode_tmap_2d_bf16(&ta, g.A, g.K, g.M, g.K * 2, kBK, (uint32_t)a_box_rows, true))
+    return fail(BI_ERR_CUDA, "gemm: TMA descriptor for A failed");
   const uint32_t box_b = swiglu ? bn / 2 : bn;
   if (g.E == 1 && swiglu) {
     const char* w = static_cast<const char*>(g.W);
@@ -801,7 +722,6 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   args.splits = splits;
   args.a_box_rows = a_box_rows;
   args.group_m = g.tile_expert ? 1 : kGroupM;
-  args.a_rows = g.a_rows;
   const int64_t tiles = (int64_t)args.m_tiles * n_tiles * splits;
   BI_REQUIRE_SHAPE(tiles < (1ll << 31), "too many tiles");
   dim3 grid((unsigned)std::min<int64_t>(tiles, num_sms()));
@@ -886,30 +806,6 @@ bi_status bi_grouped_gemm(const void* A, int64_t M_rows, int64_t K, const void* 
 }
 
 }  // extern "C"
-
-namespace bi {
-
-bi_status grouped_gemm_rows(const void* A, int64_t a_src_rows, const int32_t* a_rows, int64_t M_rows, int64_t K,
-                            const void* W, int64_t E, int64_t N, const int32_t* tile_expert, void* C, int c_dtype,
-                            int epilogue, cudaStream_t st) {
-  BI_REQUIRE(M_rows >= 0 && N > 0 && K > 0 && E > 0 && a_src_rows > 0, "bad shape");
-  if (M_rows == 0) return BI_OK;
-  BI_REQUIRE(A && W && C && tile_expert && a_rows, "null pointer");
-  BI_REQUIRE(M_rows % 128 == 0, "M_rows must be a multiple of 128");
-  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(C) && aligned16(a_rows), "pointers must be 16-byte aligned");
-  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
-  const bool swiglu = epilogue == BI_EPI_SWIGLU;
-  const int bn = tile_n_for(N, K, swiglu, E);
-  BI_REQUIRE_SHAPE(swiglu ? (N / 2) % (bn / 2) == 0 : N % bn == 0,
-                   "grouped GEMM needs the per-expert N to be a multiple of the tile width");
-  BI_REQUIRE_SHAPE(M_rows < (1ll << 31) && N * E < (1ll << 31) && a_src_rows < (1ll << 31), "shape too large");
-  GemmCall g{A, M_rows, K, W, N, E, tile_expert, C, c_dtype, epilogue, BI_INVARIANT, nullptr, 0};
-  g.a_rows = a_rows;
-  g.a_src_rows = a_src_rows;
-  return run_gemm(g, st);
-}
-
-}  // namespace bi
 
 // ----------------------------------------------- fused lm_head + log-softmax
 namespace bi {

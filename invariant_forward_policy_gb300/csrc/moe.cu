@@ -81,16 +81,12 @@ constexpr int kPermWarps = kPermThreads / 32;
 __global__ void __launch_bounds__(kPermThreads) expert_chunk_rank_kernel(const int32_t* __restrict__ ids, int64_t n,
                                                                          int E, int32_t* __restrict__ rank,
                                                                          int32_t* __restrict__ chunk_counts,
-                                                                         int32_t* __restrict__ row_token,
-                                                                         int64_t max_rows, int* status) {
+                                                                         int* status) {
   pdl_trigger();
   extern __shared__ int32_t hist[];  // [kPermWarps][E]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int j = tid; j < kPermWarps * E; j += kPermThreads) hist[j] = 0;
   pdl_wait();
-  if (row_token)  // padding rows read token 0 (their results are never combined)
-    for (int64_t r = (int64_t)blockIdx.x * kPermThreads + tid; r < max_rows; r += (int64_t)gridDim.x * kPermThreads)
-      row_token[r] = 0;
   const int64_t i = (int64_t)blockIdx.x * kPermThreads + tid;
   int e = -1;
   if (i < n) {
@@ -123,9 +119,8 @@ __global__ void __launch_bounds__(kPermThreads) expert_chunk_rank_kernel(const i
 // (e+1)*capacity), pairs beyond it are dropped and reported).
 __global__ void __launch_bounds__(kPermThreads) expert_layout_kernel(
     const int32_t* __restrict__ ids, const int32_t* __restrict__ rank, const int32_t* __restrict__ chunk_counts,
-    int64_t n, int64_t n_chunks, int E, int k, int64_t capacity, int64_t max_rows, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ tile_expert, int32_t* __restrict__ row_of_slot, int32_t* __restrict__ row_token,
-    int* status) {
+    int64_t n, int64_t n_chunks, int E, int64_t capacity, int64_t max_rows, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ tile_expert, int32_t* __restrict__ row_of_slot, int* status) {
   pdl_trigger();
   extern __shared__ int32_t lay[];  // before[E], off[E + 1]
   int32_t* before = lay;
@@ -207,7 +202,6 @@ __global__ void __launch_bounds__(kPermThreads) expert_layout_kernel(
       row = -1;
     }
     row_of_slot[i] = (int32_t)row;
-    if (row_token && row >= 0) row_token[row] = (int32_t)(i / k);
   }
 }
 
@@ -322,7 +316,7 @@ size_t bi_moe_permute_workspace_size(int64_t T, int k, int E) {
 // Both layouts: chunk ranks, then the layout pass (capacity 0 = contiguous).
 static bi_status permute_impl(const int32_t* ids, int64_t T, int k, int E, int64_t capacity, int64_t max_rows,
                               int32_t* row_of_slot, int32_t* tile_expert, int32_t* expert_offsets, void* workspace,
-                              size_t ws_bytes, cudaStream_t st, int32_t* row_token = nullptr) {
+                              size_t ws_bytes, cudaStream_t st) {
   using namespace bi;
   BI_REQUIRE(workspace && ws_bytes >= bi_moe_permute_workspace_size(T, k, E), "permute workspace too small");
   BI_REQUIRE(E >= 1 && E <= kPermThreads, "E must be in [1, 1024]");
@@ -340,12 +334,12 @@ static bi_status permute_impl(const int32_t* ids, int64_t T, int k, int E, int64
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("permute smem attribute: ") + cudaGetErrorString(attr_err));
   BI_TRY(launched(launch_pdl(expert_chunk_rank_kernel, dim3((unsigned)chunks), dim3(kPermThreads), hist_bytes, st, ids,
-                             n, E, rank, chunk_counts, row_token, max_rows, device_status_ptr()),
+                             n, E, rank, chunk_counts, device_status_ptr()),
                   "expert_chunk_rank_kernel"));
   const size_t lay_bytes = (size_t)(2 * E + 1) * sizeof(int32_t);
   return launched(launch_pdl(expert_layout_kernel, dim3((unsigned)chunks), dim3(kPermThreads), lay_bytes, st, ids,
-                             (const int32_t*)rank, (const int32_t*)chunk_counts, n, chunks, E, k, capacity, max_rows,
-                             expert_offsets, tile_expert, row_of_slot, row_token, device_status_ptr()),
+                             (const int32_t*)rank, (const int32_t*)chunk_counts, n, chunks, E, capacity, max_rows,
+                             expert_offsets, tile_expert, row_of_slot, device_status_ptr()),
                   "expert_layout_kernel");
 }
 
@@ -423,7 +417,7 @@ size_t bi_moe_layer_workspace_size(int64_t T, int64_t d, int E, int k, int64_t F
   add((size_t)(rows / 128) * 4);                 // tile_expert
   add((size_t)(E + 1) * 4);                      // offsets
   add(bi_moe_permute_workspace_size(T, k, E));   // rank + counts
-  add((size_t)rows * 4);                         // token of each layout row
+  add((size_t)rows * d * 2);                     // gathered x
   add((size_t)rows * F * 2);                     // activation
   add((size_t)rows * d * 2);                     // expert outputs
   add(bi_moe_combine_workspace_size(T, d, mode));
@@ -452,16 +446,14 @@ bi_status bi_moe_layer(const void* x, const float* router_logits, int64_t T, int
   auto* offs = static_cast<int32_t*>(take((size_t)(E + 1) * 4));
   const size_t pws = bi_moe_permute_workspace_size(T, k, E);
   void* perm_ws = take(pws);
-  auto* row_token = static_cast<int32_t*>(take((size_t)rows * 4));
+  void* xp = take((size_t)rows * d * 2);
   void* act = take((size_t)rows * F * 2);
   void* y = take((size_t)rows * d * 2);
   void* cws = take(bi_moe_combine_workspace_size(T, d, mode));
   BI_TRY(bi_moe_route_topk(router_logits, T, E, k, ids, wts, stream));
-  cudaStream_t st = as_stream(stream);
-  BI_REQUIRE(E >= 1 && E <= kPermThreads && k >= 1, "bad expert count / top-k");
-  BI_TRY(permute_impl(ids, T, k, E, 0, rows, ros, tiles, offs, perm_ws, pws, st, row_token));
-  // gate/up reads each layout row's token row of x in place (TMA row gather): no permuted copy
-  BI_TRY(grouped_gemm_rows(x, T, row_token, rows, d, w13, E, 2 * F, tiles, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, st));
+  BI_TRY(bi_moe_permute(ids, T, k, E, rows, ros, tiles, offs, perm_ws, pws, stream));
+  BI_TRY(bi_moe_gather(x, ros, T, k, d, xp, stream));
+  BI_TRY(bi_grouped_gemm(xp, rows, d, w13, E, 2 * F, tiles, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, stream));
   BI_TRY(bi_grouped_gemm(act, rows, F, w2, E, d, tiles, y, BI_DTYPE_BF16, BI_EPI_NONE, stream));
   // Both modes combine in slot order: on this GPU the fp32-atomic combine (a
   // separate pass, or folded into the down projection's epilogue) measured
