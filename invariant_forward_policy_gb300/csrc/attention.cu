@@ -605,19 +605,22 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 // and O += P V (K = 64 keys in 16-wide steps, ascending) accumulate in TMEM;
 // tcgen05.mma and mma.sync give the same fp32 bits step for step, so each row
 // gets exactly the arithmetic of the mma.sync schedules.  Each row belongs to
-// one thread of warps 0..3 (TMEM lane = row), which repeats attn_update's
-// operations in its order: scale and select-mask, the tile max, alpha, P =
-// exp2(v - m) with the row sum taken in the mma.sync quad order
-// ((s0 + s1) + (s2 + s3), s_q the sequential sum of keys 8j + 2q + {0, 1}),
-// l = l alpha + sum, O = O alpha (skipped when alpha is exactly 1, where it is
-// the identity), P rounded to bf16; and at every lane boundary the finished
-// lane folds into the running state with lane_merge's formula.
-// Warp 4 lane 0 streams the split's K and V pages by TMA (the persistent
-// decode kernel's tensor maps) into a ring; warp 5 owns TMEM and lane 0 issues
-// the MMAs, S of the next tile ahead of P V of this one.  V rows after the
-// CTA's last query position are zeroed in shared memory before P V (TMA copies
-// whole pages, and slots not yet written may hold anything); K rows there only
-// feed scores that the select-mask replaces.
+// four threads of the sixteen softmax warps (warps w, w + 4, w + 8, w + 12
+// read TMEM lane quarter w): thread q holds the keys 8j + 2q + {0, 1} of the
+// tile, i.e. exactly the keys of the mma.sync fragment's quad sum s_q.  They
+// repeat attn_update's operations in its order: scale and select-mask, the
+// tile max (exchanged), alpha, P = exp2(v - m), s_q summed over its keys in
+// order and the row sum formed as (s0 + s1) + (s2 + s3), l = l alpha + sum,
+// O = O alpha (skipped when alpha is exactly 1, where it is the identity), P
+// rounded to bf16; and at every lane boundary the finished lane folds into the
+// running state with lane_merge's formula.  Each of the four threads keeps
+// the row's (m, l) and rescales, folds and writes its quarter of the O columns.
+// Warp 16 lane 0 streams the split's K and V pages by TMA (the persistent
+// decode kernel's tensor maps) into a ring; warp 17 owns TMEM and lane 0
+// issues the MMAs, S of the next tile ahead of P V of this one.  V rows after
+// the CTA's last query position are zeroed in shared memory before P V (TMA
+// copies whole pages, and slots not yet written may hold anything); K rows
+// there only feed scores that the select-mask replaces.
 template <int HD>
 struct TcAttnLayout {
   static constexpr int kQ = 128 * HD * 2;           // HD/64 boxes of 128 rows x 128 bytes
@@ -626,32 +629,42 @@ struct TcAttnLayout {
   static constexpr int kP = 128 * kKeys * 2;        // one P tile, 128 rows x 64 keys
   static constexpr int kOffKV = kQ;
   static constexpr int kOffP = kOffKV + kStages * 2 * kPage;
-  static constexpr int kOffBar = kOffP + 2 * kP;
+  static constexpr int kOffX = kOffP + 2 * kP;      // max and sum exchange, [4 quads][128 rows] each
+  static constexpr int kOffBar = kOffX + 2 * 4 * 128 * 4;
   static constexpr int kBytes = kOffBar + 256 + 1024;   // + barriers, + alignment slack
   static constexpr uint32_t kCols = HD == 128 ? 512 : 256;  // S0, S1 (64 each), O, R (HD each)
   static constexpr uint32_t kColS = 0, kColO = 128, kColR = 128 + HD;
+  static constexpr int kSoftmaxWarps = 16;
+  static constexpr int kThreads = 32 * kSoftmaxWarps + 64;  // + TMA warp, MMA warp
 };
 
 template <int HD>
-__global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
-                                                               const __grid_constant__ CUtensorMap tmk,
-                                                               const __grid_constant__ CUtensorMap tmv) {
+__global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
+    attention_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv) {
   using Lay = TcAttnLayout<HD>;
   constexpr int NS = Lay::kStages;
-  constexpr int KB = HD / 64;  // 64-dim boxes per row
+  constexpr int KB = HD / 64;        // 64-dim boxes per row
+  constexpr int OQ = HD / 4;         // O columns per thread
+  constexpr int CW = 16;             // TMEM columns per load or store in the O and R passes
+  constexpr int kSM = Lay::kSoftmaxWarps * 32;
+  constexpr int kWarpTma = Lay::kSoftmaxWarps, kWarpMma = Lay::kSoftmaxWarps + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + Lay::kOffKV;  // stage st: K page at st * 2 * kPage, V page after it
   uint8_t* sP = smem + Lay::kOffP;
+  float* xmax = reinterpret_cast<float*>(smem + Lay::kOffX);  // [4][128]
+  float* xsum = xmax + 4 * 128;                                // [4][128]
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;   // [2] MMA -> softmax: S of a tile is in TMEM
-  uint64_t* s_empty = s_full + 2;     // [2] softmax -> MMA: S read (4 warp arrivals)
-  uint64_t* p_full = s_empty + 2;     // [2] softmax -> MMA: P written, O rescaled (4 warp arrivals)
+  uint64_t* s_empty = s_full + 2;     // [2] softmax -> MMA: S read (16 warp arrivals)
+  uint64_t* p_full = s_empty + 2;     // [2] softmax -> MMA: P written, O rescaled (16 warp arrivals)
   uint64_t* o_done = p_full + 2;      // MMA -> softmax: P V of a tile has completed
-  uint64_t* q_full = o_done + 1;      // softmax -> MMA: Q tile loaded (128 thread arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
+  uint64_t* q_full = o_done + 1;      // softmax -> MMA: Q tile loaded (kSM thread arrivals)
+  uint64_t* xbar = q_full + 1;        // [4 lane quarters][2]: the four warps of a quarter met (max, sum)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -665,19 +678,20 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_empty[i], Lay::kSoftmaxWarps);
+      mbar_init(&p_full[i], Lay::kSoftmaxWarps);
     }
     mbar_init(o_done, 1);
-    mbar_init(q_full, 128);
+    mbar_init(q_full, kSM);
+    for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(tmem_slot, Lay::kCols);
     tmem_relinquish();
   }
-  if (tid == 128) {
+  if (warp == kWarpTma && lane == 0) {
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
   }
@@ -705,7 +719,7 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
   const int32_t* bt = a.block_table + (int64_t)seq * a.max_blk;
   const int t_begin = kv_begin / kKeys;
 
-  if (n_tiles > 0 && warp == 4) {
+  if (n_tiles > 0 && warp == kWarpTma) {
     if (lane == 0) {
       // ---------------- TMA producer: K and V pages of the split's tiles, in order
       const int rows_total = (int)(a.n_blocks * a.Hkv * kKeys);
@@ -736,7 +750,7 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
         mbar_wait(&kv_full[tt % NS], (tt / NS) & 1);
       }
     }
-  } else if (n_tiles > 0 && warp == 5) {
+  } else if (n_tiles > 0 && warp == kWarpMma) {
     if (lane == 0) {
       // ---------------- MMA issuer
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kKeys);
@@ -782,19 +796,21 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
         *abort_flag = 1;
       }
     }
-  } else if (n_tiles > 0 && warp < 4) {
-    // ---------------- softmax warps: thread = row = TMEM lane
-    const int r = tid;
+  } else if (n_tiles > 0 && warp < Lay::kSoftmaxWarps) {
+    // ---------------- softmax warps: row r = TMEM lane; quad group qd of its keys, quarter qd of O
+    const int qw = warp & 3, qd = warp >> 2;
+    const int r = qw * 32 + lane;
     const int ti = tok0 + r / a.group;
     const bool row_valid = ti < n_tok;
     const int row_tok = row0 + ti, row_pos = pos_first + ti, row_head = kvh * a.group + (r % a.group);
-    // Q row into the swizzled tile (zeros for rows past the piece)
+    uint64_t* xb = xbar + 2 * qw;  // where the four warps that share these rows meet
+    // a quarter of the Q row into the swizzled tile (zeros for rows past the piece)
     {
       const __nv_bfloat16* qr = a.q + ((int64_t)row_tok * a.Hq + row_head) * HD;
 #pragma unroll
-      for (int ch = 0; ch < HD / 8; ++ch) {
-        const int within = ch & 7;
-        uint8_t* dst = sQ + (ch >> 3) * (128 * 128) + r * 128 + ((within ^ (r & 7)) << 4);
+      for (int c = 0; c < HD / 32; ++c) {
+        const int ch = qd * (HD / 32) + c;
+        uint8_t* dst = sQ + (ch >> 3) * (128 * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
         cp_async16(dst, row_valid ? qr + ch * 8 : a.q, row_valid);
       }
       cp_async_commit();
@@ -802,19 +818,20 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
       fence_proxy_async();
       mbar_arrive(q_full);
     }
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t tO = trow + Lay::kColO, tR = trow + Lay::kColR;
+    const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
+    const uint32_t tO = trow + Lay::kColO + qd * OQ, tR = trow + Lay::kColR + qd * OQ;
     auto zero_o = [&]() {
-      uint32_t z[32];
+      uint32_t z[CW];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = 0u;
+      for (int i = 0; i < CW; ++i) z[i] = 0u;
 #pragma unroll
-      for (int c = 0; c < HD; c += 32) tmem_st_32x32b_x32(tO + c, z);
+      for (int c = 0; c < OQ; c += CW) tmem_st_cols<CW>(tO + c, z);
       tmem_st_wait();
     };
     float m = -INFINITY, l = 0.f, Rm = -INFINITY, Rl = 0.f;
-    // R <- lane_merge(R, (m, l, O)): P.acc = P.acc a + acc b, or a copy into an empty R
-    auto fold_lane = [&]() {
+    // R <- lane_merge(R, (m, l, O)) on this thread's quarter of the columns:
+    // P.acc = P.acc a + acc b, or a copy into an empty R
+    auto fold_lane = [&](const float m, const float l) {
       const bool has = m != -INFINITY;
       const bool copy = has && Rm == -INFINITY;
       const float M = fmaxf(Rm, m);
@@ -822,18 +839,18 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
       const float fb = (m == M) ? 1.0f : exp2f(__fsub_rn(m, M));
       if (__any_sync(0xffffffffu, has)) {
 #pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t rr[32], oo[32];
-          tmem_ld_32x32b_x32(tR + c, rr);
-          tmem_ld_32x32b_x32(tO + c, oo);
+        for (int c = 0; c < OQ; c += CW) {
+          uint32_t rr[CW], oo[CW];
+          tmem_ld_cols_attn<CW>(tR + c, rr);
+          tmem_ld_cols_attn<CW>(tO + c, oo);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < CW; ++i) {
             const float rv = __uint_as_float(rr[i]), ov = __uint_as_float(oo[i]);
             const float nv = copy ? ov : (has ? __fadd_rn(__fmul_rn(rv, fa), __fmul_rn(ov, fb)) : rv);
             rr[i] = __float_as_uint(nv);
           }
-          tmem_st_32x32b_x32(tR + c, rr);
+          tmem_st_cols<CW>(tR + c, rr);
         }
         tmem_st_wait();
       }
@@ -853,6 +870,7 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
     };
     zero_o();
     bool ok = true;
+    // v[2j + e] is the score of key 8j + 2qd + e of the tile
     for (int t = 0; t < n_tiles; ++t) {
       const int key0 = (t_begin + t) * kKeys;
       const bool lane_start = t > 0 && t % tpl == 0;
@@ -861,20 +879,83 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
         break;
       }
       tc_fence_after();
-      float v[kKeys];
+      float v[16];
       {
-        uint32_t sr[32];
+        uint32_t g[8][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld_32x32b_x32(trow + Lay::kColS + (t & 1) * kKeys + h * 32, sr);
-          tmem_ld_wait();
+        for (int j = 0; j < 8; ++j) tmem_ld_32x32b_x2(trow + Lay::kColS + (t & 1) * kKeys + 8 * j + 2 * qd, g[j]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(sr[i]);
+        for (int j = 0; j < 8; ++j) {
+          v[2 * j] = __uint_as_float(g[j][0]);
+          v[2 * j + 1] = __uint_as_float(g[j][1]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[t & 1]);
+      // a new lane starts from a fresh state; the finished one is folded into R
+      // once its last P V has landed (below), so this tile's softmax runs while
+      // the tensor core finishes the previous tile
+      const float m_done = m, l_done = l;
+      if (lane_start) {
+        m = -INFINITY;
+        l = 0.f;
+      }
+      // scale and mask (a tile wholly at or before the row's position needs no
+      // mask), the tile max over the four quads (the max of a set does not depend
+      // on the order it is taken in)
+      const bool open = row_valid && key0 + kKeys - 1 <= row_pos;
+      if (open) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = __fmul_rn(v[c], a.scale_log2);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int key = key0 + 8 * (c >> 1) + 2 * qd + (c & 1);
+          v[c] = (row_valid && key <= row_pos) ? __fmul_rn(v[c], a.scale_log2) : -INFINITY;
+        }
+      }
+      float mx[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+      for (int c = 4; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], v[c]);
+      xmax[qd * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xb[0]);
+      if (!warp_wait(&xb[0], t & 1)) {
+        ok = false;
+        break;
+      }
+      const float tmax = fmaxf(fmaxf(xmax[r], xmax[128 + r]), fmaxf(xmax[256 + r], xmax[384 + r]));
+      const float m_new = fmaxf(m, tmax);
+      const float alpha = (m_new == m) ? 1.0f : exp2f(__fsub_rn(m, m_new));
+      // P and this thread's quad sum s_qd over its keys in order (a score of an
+      // open tile is never -inf, so the select is the identity there)
+      float sq = 0.f;
+      if (open) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          v[c] = exp2f(__fsub_rn(v[c], m_new));
+          sq = __fadd_rn(sq, v[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          v[c] = (v[c] == -INFINITY) ? 0.f : exp2f(__fsub_rn(v[c], m_new));
+          sq = __fadd_rn(sq, v[c]);
+        }
+      }
+      xsum[qd * 128 + r] = sq;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xb[1]);
+      if (!warp_wait(&xb[1], t & 1)) {
+        ok = false;
+        break;
+      }
+      const float rs =
+          __fadd_rn(__fadd_rn(xsum[r], xsum[128 + r]), __fadd_rn(xsum[256 + r], xsum[384 + r]));
+      l = __fadd_rn(__fmul_rn(l, alpha), rs);
+      m = m_new;
       if (t > 0) {  // P V of the previous tile has landed in O
         if (!warp_wait(o_done, (t - 1) & 1)) {
           ok = false;
@@ -883,49 +964,19 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
         tc_fence_after();
       }
       if (lane_start) {
-        fold_lane();
+        fold_lane(m_done, l_done);
         zero_o();
-        m = -INFINITY;
-        l = 0.f;
       }
-      // scale and mask, tile max
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const bool okc = row_valid && key0 + c <= row_pos;
-        v[c] = okc ? __fmul_rn(v[c], a.scale_log2) : -INFINITY;
-        tmax = fmaxf(tmax, v[c]);
-      }
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = (m_new == m) ? 1.0f : exp2f(__fsub_rn(m, m_new));
-      // P and the row sum in the quad order of the mma.sync fragments
-      float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = j * 8 + q * 2 + e;
-            const float pv = (v[c] == -INFINITY) ? 0.f : exp2f(__fsub_rn(v[c], m_new));
-            v[c] = pv;
-            sq[q] = __fadd_rn(sq[q], pv);
-          }
-        }
-      }
-      const float rs = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
-      l = __fadd_rn(__fmul_rn(l, alpha), rs);
-      m = m_new;
-      // O = O alpha (identity where alpha == 1; O is +0 at a lane's first tile)
+      // O = O alpha on this quarter (identity where alpha == 1; O is +0 at a lane's first tile)
       if (t > 0 && !lane_start && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t oo[32];
-          tmem_ld_32x32b_x32(tO + c, oo);
+        for (int c = 0; c < OQ; c += CW) {
+          uint32_t oo[CW];
+          tmem_ld_cols_attn<CW>(tO + c, oo);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha));
-          tmem_st_32x32b_x32(tO + c, oo);
+          for (int i = 0; i < CW; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha));
+          tmem_st_cols<CW>(tO + c, oo);
         }
         tmem_st_wait();
       }
@@ -937,52 +988,47 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
           break;
         }
         uint8_t* sv = sKV + st * 2 * Lay::kPage + Lay::kPage;
-        for (int i = tid; i < kKeys * KB * 8; i += 128) {  // (key, 16-byte chunk): whole rows, any chunk order
+        for (int i = tid; i < kKeys * KB * 8; i += kSM) {  // (key, 16-byte chunk): whole rows, any chunk order
           const int key = i / (KB * 8), ch = i % (KB * 8);
           if (key0 + key > max_pos)
             *reinterpret_cast<uint4*>(sv + (ch >> 3) * (kKeys * 128) + key * 128 + ((ch & 7) << 4)) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // P row in bf16 into the swizzled P tile
+      // this quad of the P row in bf16: keys 8j + 2qd + {0, 1} are bytes 4qd .. 4qd + 3
+      // of the row's 16-byte chunk j in the swizzled P tile
       uint8_t* prow = sP + (t & 1) * Lay::kP + r * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 w;
-        w.x = pack_bf16x2(v[ch * 8 + 0], v[ch * 8 + 1]);
-        w.y = pack_bf16x2(v[ch * 8 + 2], v[ch * 8 + 3]);
-        w.z = pack_bf16x2(v[ch * 8 + 4], v[ch * 8 + 5]);
-        w.w = pack_bf16x2(v[ch * 8 + 6], v[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = w;
-      }
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint32_t*>(prow + ((j ^ (r & 7)) << 4) + 4 * qd) = pack_bf16x2(v[2 * j], v[2 * j + 1]);
       fence_proxy_async();
       tc_fence_before();
-      // this warp's P rows (and its share of the zeroed V rows) are written; the
-      // MMA waits for all four warps
+      // this warp's quads of P (and its share of the zeroed V rows) are written;
+      // the MMA waits for all sixteen warps
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t & 1]);
     }
     if (ok && warp_wait(o_done, (n_tiles - 1) & 1)) {
       tc_fence_after();
-      fold_lane();
-      // the split partial (m, l, acc) of this row; every lane loads, rows that
-      // have no key in this split store nothing
+      fold_lane(m, l);
+      // this quarter of the split partial (m, l, acc) of the row; every lane loads,
+      // rows that have no key in this split store nothing
       const bool store = row_valid && row_pos >= kv_begin;
       const int64_t pidx = ((int64_t)row_tok * a.Hq + row_head) * a.nsplit + s;
-      float* po = a.part_o + pidx * HD;
+      float* po = a.part_o + pidx * HD + qd * OQ;
 #pragma unroll 1
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t rr[32];
-        tmem_ld_32x32b_x32(tR + c, rr);
+      for (int c = 0; c < OQ; c += CW) {
+        uint32_t rr[CW];
+        tmem_ld_cols_attn<CW>(tR + c, rr);
         tmem_ld_wait();
         if (store) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
+          for (int i = 0; i < CW; i += 4)
             *reinterpret_cast<float4*>(po + c + i) = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
                                                                __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
         }
       }
-      if (store) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
+      if (store && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
     } else {
       report(a.status, DEV_TIMEOUT);
       *abort_flag = 1;
@@ -990,7 +1036,7 @@ __global__ void __launch_bounds__(192, 1) attention_tc_kernel(const AttnArgs a,
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::kCols);
   }
@@ -1496,7 +1542,8 @@ static bi_status launch_attention_tc(const AttnArgs& args, dim3 grid, cudaStream
   if (!encode_tmap_2d_bf16(&tmk, args.k_cache, HD, rows, HD * 2, 64, kKeys, true) ||
       !encode_tmap_2d_bf16(&tmv, args.v_cache, HD, rows, HD * 2, 64, kKeys, true))
     return fail(BI_ERR_CUDA, "attention prefill: cuTensorMapEncodeTiled failed for the K/V cache");
-  return launched(launch_pdl(attention_tc_kernel<HD>, grid, dim3(192), smem, st, args, tmk, tmv),
+  return launched(launch_pdl(attention_tc_kernel<HD>, grid, dim3(TcAttnLayout<HD>::kThreads), smem, st, args, tmk,
+                             tmv),
                   "attention_tc_kernel");
 }
 

@@ -49,13 +49,6 @@ int num_sms();
 // out-of-range index, record a code here instead of trapping.
 enum DeviceCode : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_BAD_INDEX = 2 };
 int* device_status_ptr();  // device address of the status word (current device and context)
-// Grouped GEMM whose A rows are gathered by TMA: row r of the M_rows-row
-// operand is row a_rows[r] of A [a_src_rows, K] (int32 [M_rows], 16-byte
-// aligned).  Same tiles, K order and bits as bi_grouped_gemm on the gathered
-// copy; the MoE layer's gate/up projection reads the token rows in place.
-bi_status grouped_gemm_rows(const void* A, int64_t a_src_rows, const int32_t* a_rows, int64_t M_rows, int64_t K,
-                            const void* W, int64_t E, int64_t N, const int32_t* tile_expert, void* C, int c_dtype,
-                            int epilogue, cudaStream_t st);
 
 
 // Device addresses of a module's __device__ symbol, remembered per device
@@ -230,15 +223,6 @@ BI_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0
       ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
-// Four rows r0..r3 of a 2-D tensor (box: one row of box_inner columns from
-// column c0) into consecutive rows at dst; the tensor map's box is one row high.
-BI_DEV void tma_gather4_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
-      "%5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
 BI_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -291,6 +275,25 @@ BI_DEV void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 32 bit, 2 consecutive columns.
+BI_DEV void tmem_ld_32x32b_x2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
+// 32 lanes x 32 bit, 16 consecutive columns: thread i of the warp writes lane (base + i).
+BI_DEV void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+// 32 lanes x 32 bit, 4 consecutive columns.
+BI_DEV void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
 // 32 lanes x 32 bit, 16 consecutive columns.
 BI_DEV void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -312,6 +315,17 @@ BI_DEV void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 BI_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// CW (16 or 32) consecutive columns of a warp's 32 TMEM lanes, loaded or stored.
+template <int CW>
+BI_DEV void tmem_ld_cols_attn(uint32_t taddr, uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) tmem_ld_32x32b_x32(taddr, r);
+  else tmem_ld_32x32b_x16(taddr, r);
+}
+template <int CW>
+BI_DEV void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[CW]) {
+  if constexpr (CW == 32) tmem_st_32x32b_x32(taddr, r);
+  else tmem_st_32x32b_x16(taddr, r);
+}
 
 // Shared-memory matrix descriptor for a K-major operand written by TMA with
 // 128-byte swizzle: 8-row core groups 1024 bytes apart (stride byte offset),
