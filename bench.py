@@ -1042,6 +1042,34 @@ def run_kernel_case(name: str, reps: int):
             dec.decode(tok, pos, cache, bt, max_ctx, smp, lpd, ws)
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
+    elif name == "c5_recompute":
+        # training-side recompute of the long-context workload: one packed chunk-2048 prefill over
+        # prompt + 127 fed-back tokens of all 64 sequences (the bench's recompute row)
+        from invariant_forward_policy_gb300 import _lib as L
+        from invariant_forward_policy_gb300.decoder import Decoder, recompute_pack
+        from synthetic import C5, make_c5_prompt_lengths, make_decoder_weights
+        shape = C5["shape"]
+        lens = make_c5_prompt_lengths(C5["batch"], C5["ctx_min"], C5["ctx_max"], C5["seed"])
+        B, n_gen = len(lens), C5["gen"]
+        wb = make_decoder_weights(shape, seed=C5["seed"], w_std=C5["w_std"])
+        rng = np.random.default_rng(C5["seed"] + 3)
+        prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
+        gens = [np.random.default_rng(C5["seed"] + 9 + b).integers(0, shape.vocab, n_gen).astype(np.int32)
+                for b in range(B)]
+        seqs, tg, lf = recompute_pack(prompts, gens, range(B))
+        tot = [len(x) for x in seqs]
+        max_ctx = max(tot)
+        dec = Decoder(shape, wb, max_pos=max_ctx + 64, device=dev)
+        bt, nb = dec.paged_block_table(tot, -(-max_ctx // 64), seed=7)
+        cache = dec.alloc_cache(nb)
+        tok = torch.from_numpy(np.concatenate(seqs).astype(np.int32)).to(dev)
+        tgt = torch.from_numpy(np.concatenate(tg).astype(np.int32)).to(dev)
+        cu = np.concatenate([[0], np.cumsum(tot)]).astype(np.int64)
+        lp = torch.empty(int(cu[-1]), dtype=torch.float32, device=dev)
+        ws = dec.workspace(16384, min(B, 128), max_ctx, 2048, bi.BI_INVARIANT)
+        for _ in range(reps):
+            L.bi_forward_prefill(dec.handle, tok, tgt, cu, [0] * B, lf, B, C5["chunk"], bt, bt.shape[1], cache.k,
+                                 cache.v, cache.n_blocks, lp, None, ws, 16384, max_ctx, 2048, bi.BI_INVARIANT)
     elif name == "gemm_fp8":
         # block-FP8 W8A8 GEMM at a prefill FFN shape (operands quantised once, untimed)
         M, N, K = 8192, 11264, 2048
@@ -1225,7 +1253,8 @@ def main():
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_down, gemm_decode_lm_head, "
                          "lm_head_fused_decode, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
-                         "kv_fp8_gather, c5_decode, topk_prefill, attention_prefill_long, rmsnorm, logprob, lm_head_fused, "
+                         "kv_fp8_gather, c5_decode, c5_recompute, topk_prefill, attention_prefill_long, rmsnorm, "
+                         "logprob, lm_head_fused, "
                          "moe_layer) or "
                          "the whole step (step) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)

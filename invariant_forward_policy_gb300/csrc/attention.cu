@@ -169,6 +169,15 @@ __device__ __forceinline__ uint32_t kv_off(int key, int ch) {
   return (uint32_t)((ch >> 3) * (kKeys * 128) + key * 128 + (((ch & 7) ^ (key & 7)) << 4));
 }
 
+// P = 2^x for the attention probabilities: the hardware's ex2 with results
+// below 2^-126 flushed to zero (and 2^-inf = +0).  Every schedule, decode and
+// prefill, takes P through this one instruction, so their bits stay equal.
+__device__ __forceinline__ float exp2_p(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // S = Q K^T for the warp's 16 query rows and one 64-key tile (fp32, unscaled).
 template <int HD>
 __device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD / 16][4], int lane,
@@ -224,7 +233,7 @@ __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int 
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float v = sc[j][h * 2 + e];
-        const float pv = (v == -INFINITY) ? 0.f : exp2f(__fsub_rn(v, m_new));
+        const float pv = (v == -INFINITY) ? 0.f : exp2_p(__fsub_rn(v, m_new));
         pr[j][h * 2 + e] = pv;
         rs = __fadd_rn(rs, pv);
       }
@@ -615,12 +624,17 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 // rounded to bf16; and at every lane boundary the finished lane folds into the
 // running state with lane_merge's formula.  Each of the four threads keeps
 // the row's (m, l) and rescales, folds and writes its quarter of the O columns.
-// Warp 16 lane 0 streams the split's K and V pages by TMA (the persistent
-// decode kernel's tensor maps) into a ring; warp 17 owns TMEM and lane 0
-// issues the MMAs, S of the next tile ahead of P V of this one.  V rows after
+// A CTA walks up to kTcSplitsPerCta consecutive splits of its query tile, one
+// after another (each split's partial is written when the next one starts), so
+// the Q tile, TMEM and the page pipeline serve many tiles.
+// Warp 16 lane 0 streams the K and V pages by TMA (the persistent decode
+// kernel's tensor maps) into a ring; warp 17 owns TMEM and lane 0 issues the
+// MMAs, S of the next tile ahead of P V of this one.  V rows after
 // the CTA's last query position are zeroed in shared memory before P V (TMA
 // copies whole pages, and slots not yet written may hold anything); K rows
 // there only feed scores that the select-mask replaces.
+constexpr int kTcSplitsPerCta = 4;
+
 template <int HD>
 struct TcAttnLayout {
   static constexpr int kQ = 128 * HD * 2;           // HD/64 boxes of 128 rows x 128 bytes
@@ -670,7 +684,7 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p = blockIdx.y;
   const int kvh = blockIdx.z % a.Hkv;
-  const int s = blockIdx.z / a.Hkv;
+  const int s0 = (blockIdx.z / a.Hkv) * kTcSplitsPerCta;  // first split of this CTA
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&kv_full[i], 1);
@@ -708,16 +722,23 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
   const int tok_per_tile = 128 / a.group;
   const int tok0 = blockIdx.x * tok_per_tile;
   const int pos_first = a.pm.pos0[p];
-  const int kv_begin = s * a.split;
+  // tiles of this CTA's splits in order: every split before the last live one is
+  // whole (ntf tiles), so tile k is tile k % ntf of split s0 + k / ntf
+  const int ntf = a.split / kKeys;
   int n_tiles = 0, max_pos = -1;
   if (tok0 < n_tok) {
     max_pos = pos_first + min(n_tok, tok0 + tok_per_tile) - 1;
-    if (kv_begin <= max_pos) n_tiles = (min(kv_begin + a.split, max_pos + 1) - kv_begin + kKeys - 1) / kKeys;
+    const int s_last = min(min(s0 + kTcSplitsPerCta, a.nsplit) - 1, max_pos / a.split);
+    if (s_last >= s0) {
+      const int kb = s_last * a.split;
+      n_tiles = (s_last - s0) * ntf + (min(kb + a.split, max_pos + 1) - kb + kKeys - 1) / kKeys;
+    }
   }
   const int tpl = (((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys) / kKeys;  // tiles per lane
   const int seq = a.pm.seq[p];
   const int32_t* bt = a.block_table + (int64_t)seq * a.max_blk;
-  const int t_begin = kv_begin / kKeys;
+  // first key of tile k (absolute position)
+  auto tile_key0 = [&](int k) { return (s0 + k / ntf) * a.split + (k % ntf) * kKeys; };
 
   if (n_tiles > 0 && warp == kWarpTma) {
     if (lane == 0) {
@@ -731,7 +752,7 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
           *abort_flag = 1;
           break;
         }
-        const int blk_i = t_begin + t;
+        const int blk_i = tile_key0(t) / kKeys;
         const int32_t blk = blk_i < a.max_blk ? bt[blk_i] : -1;
         int row = rows_total;  // past the end: the copy reads zeros
         if (blk >= 0 && blk < a.n_blocks) row = (int)((blk * a.Hkv + kvh) * kKeys);
@@ -871,9 +892,31 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
     zero_o();
     bool ok = true;
     // v[2j + e] is the score of key 8j + 2qd + e of the tile
+    // this row's partial (m, l, acc) of split s from R; every lane loads, rows
+    // that have no key in the split store nothing
+    auto write_partial = [&](int s) {
+      const bool store = row_valid && row_pos >= s * a.split;
+      const int64_t pidx = ((int64_t)row_tok * a.Hq + row_head) * a.nsplit + s;
+      float* po = a.part_o + pidx * HD + qd * OQ;
+#pragma unroll 1
+      for (int c = 0; c < OQ; c += CW) {
+        uint32_t rr[CW];
+        tmem_ld_cols_attn<CW>(tR + c, rr);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < CW; i += 4)
+            *reinterpret_cast<float4*>(po + c + i) = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
+                                                               __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
+        }
+      }
+      if (store && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
+    };
     for (int t = 0; t < n_tiles; ++t) {
-      const int key0 = (t_begin + t) * kKeys;
-      const bool lane_start = t > 0 && t % tpl == 0;
+      const int key0 = tile_key0(t);
+      const int tt = t % ntf;                                  // tile within its split
+      const bool split_start = t > 0 && tt == 0;               // a new split: finish the previous one
+      const bool lane_start = split_start || (tt > 0 && tt % tpl == 0);
       if (!warp_wait(&s_full[t & 1], (t >> 1) & 1)) {
         ok = false;
         break;
@@ -935,13 +978,13 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       if (open) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          v[c] = exp2f(__fsub_rn(v[c], m_new));
+          v[c] = exp2_p(__fsub_rn(v[c], m_new));
           sq = __fadd_rn(sq, v[c]);
         }
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          v[c] = (v[c] == -INFINITY) ? 0.f : exp2f(__fsub_rn(v[c], m_new));
+          v[c] = (v[c] == -INFINITY) ? 0.f : exp2_p(__fsub_rn(v[c], m_new));
           sq = __fadd_rn(sq, v[c]);
         }
       }
@@ -965,6 +1008,11 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       }
       if (lane_start) {
         fold_lane(m_done, l_done);
+        if (split_start) {
+          write_partial(s0 + t / ntf - 1);
+          Rm = -INFINITY;  // the next fold copies into R
+          Rl = 0.f;
+        }
         zero_o();
       }
       // O = O alpha on this quarter (identity where alpha == 1; O is +0 at a lane's first tile)
@@ -1011,24 +1059,7 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
     if (ok && warp_wait(o_done, (n_tiles - 1) & 1)) {
       tc_fence_after();
       fold_lane(m, l);
-      // this quarter of the split partial (m, l, acc) of the row; every lane loads,
-      // rows that have no key in this split store nothing
-      const bool store = row_valid && row_pos >= kv_begin;
-      const int64_t pidx = ((int64_t)row_tok * a.Hq + row_head) * a.nsplit + s;
-      float* po = a.part_o + pidx * HD + qd * OQ;
-#pragma unroll 1
-      for (int c = 0; c < OQ; c += CW) {
-        uint32_t rr[CW];
-        tmem_ld_cols_attn<CW>(tR + c, rr);
-        tmem_ld_wait();
-        if (store) {
-#pragma unroll
-          for (int i = 0; i < CW; i += 4)
-            *reinterpret_cast<float4*>(po + c + i) = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
-                                                               __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-        }
-      }
-      if (store && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
+      write_partial(s0 + (n_tiles - 1) / ntf);
     } else {
       report(a.status, DEV_TIMEOUT);
       *abort_flag = 1;
@@ -1699,7 +1730,7 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
                       : launch_attention<128, true, false>(args, grid, st));
   } else if (!kv8 && n_blocks * Hkv * kKeys < (int64_t(1) << 31)) {
     // bf16 cache: 128-row query tiles on the tensor cores (TMA page coordinates are 32-bit)
-    dim3 grid((unsigned)cdiv(max_q_len * group, 128), (unsigned)P, (unsigned)(Hkv * ns));
+    dim3 grid((unsigned)cdiv(max_q_len * group, 128), (unsigned)P, (unsigned)(Hkv * cdiv(ns, kTcSplitsPerCta)));
     BI_TRY(hd == 64 ? launch_attention_tc<64>(args, grid, st) : launch_attention_tc<128>(args, grid, st));
   } else {
     dim3 grid((unsigned)qtiles, (unsigned)P, (unsigned)(Hkv * ns));
