@@ -1455,38 +1455,91 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
 // split.  q8 (optional): the output row is also quantised in 1 x 128 blocks (e4m3 codes
 // q8 [T, Hq*hd], scales qs [T, Hq*hd / 128]); each CTA holds exactly one block.
 // out may then be null.
-__global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ part_o,
-                                                              const float* __restrict__ part_ml, PieceMeta pm,
-                                                              int Hq, int hd, int nsplit, int split,
-                                                              __nv_bfloat16* __restrict__ out,
-                                                              uint8_t* __restrict__ q8, float* __restrict__ qs,
-                                                              int* status) {
+// Split merge: one warp per 128 output columns of a row (one head at hd 128,
+// two at hd 64), four columns per lane read as one 16-byte load per split.
+// The lanes of a head load its split records (m_s, l_s) once, take M = max_s
+// m_s, and hand each split's weight 2^(m_s - M) and l_s to every column by
+// shuffles; each column then sums L and O over the splits in ascending order
+// with the formula of merge_split_element, so its bits are unchanged.
+constexpr int kMergeWarps = 4;
+__global__ void __launch_bounds__(kMergeWarps * 32) attention_merge_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_ml, PieceMeta pm, int Hq, int hd, int nsplit,
+    int split, __nv_bfloat16* __restrict__ out, uint8_t* __restrict__ q8, float* __restrict__ qs, int* status) {
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
   const int i = blockIdx.x;
   const int row0 = pm.row0[p];
   if (i >= pm.row0[p + 1] - row0) return;
-  const int idx = blockIdx.z * 128 + threadIdx.x;
-  if (idx >= Hq * hd) return;  // never with q8 (Hq*hd is then a multiple of 128)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.z * kMergeWarps + warp;  // 128-column block of the row
+  const int width = Hq * hd;
+  if (chunk * 128 >= width) return;
+  const int G = hd / 4;                 // lanes per head (a power of two: 16 or 32)
+  const int col = chunk * 128 + 4 * lane;
+  const bool live = col < width;
+  const int h = (live ? col : chunk * 128) / hd, d = col % hd;
+  const int gl = lane % G;              // lane within its head's group
   const int64_t row = row0 + i;
   const int pos = pm.pos0[p] + i;
-  const int ns = merge_split_count(pos, split, nsplit, status, idx == 0);
-  const int h = idx / hd, d = idx % hd;
-  const float merged = merge_split_element(part_o, part_ml, (row * Hq + h) * nsplit, ns, hd, d);
-  const __nv_bfloat16 ob = f2bf(merged);
-  if (out) out[row * (int64_t)Hq * hd + idx] = ob;
-  if (q8) {
-    __shared__ float wmax[4];
-    const float v = bf2f(ob);
-    float mx = fabsf(v);
+  const int ns = merge_split_count(pos, split, nsplit, status, chunk == 0 && lane == 0);
+  const int64_t base = (row * Hq + h) * nsplit;
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + base;
+  // M = max_s m_s (the max of a set does not depend on the order it is taken in)
+  float M = -INFINITY;
+  for (int s = gl; s < ns; s += G) M = fmaxf(M, ml[s].x);
+  for (int o = G / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, G));
+  float L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+  const float4* po = reinterpret_cast<const float4*>(part_o + base * hd + d);
+  for (int s0 = 0; s0 < ns; s0 += G) {
+    // lane gl of the head holds split s0 + gl: its weight and l
+    float wv = 0.f, lv = 0.f;
+    if (s0 + gl < ns) {
+      const float2 r = ml[s0 + gl];
+      wv = merge_weight(r.x, M);
+      lv = r.y;
+    }
+    const int nb = min(G, ns - s0);
+    for (int k0 = 0; k0 < nb; k0 += 8) {
+      float4 ov[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        ov[k] = (k0 + k < nb && live) ? po[(int64_t)(s0 + k0 + k) * (hd / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wv, k0 + k, G);
+        const float lk = __shfl_sync(0xffffffffu, lv, k0 + k, G);
+        if (k0 + k < nb) {
+          L = merge_term(L, lk, w);
+          O[0] = merge_term(O[0], ov[k].x, w);
+          O[1] = merge_term(O[1], ov[k].y, w);
+          O[2] = merge_term(O[2], ov[k].z, w);
+          O[3] = merge_term(O[3], ov[k].w, w);
+        }
+      }
+    }
+  }
+  __nv_bfloat16 ob[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) ob[e] = f2bf(__fdiv_rn(O[e], L));
+  if (out && live) {
+    uint2 v;
+    v.x = (uint32_t)__bfloat16_as_ushort(ob[0]) | ((uint32_t)__bfloat16_as_ushort(ob[1]) << 16);
+    v.y = (uint32_t)__bfloat16_as_ushort(ob[2]) | ((uint32_t)__bfloat16_as_ushort(ob[3]) << 16);
+    *reinterpret_cast<uint2*>(out + row * (int64_t)width + col) = v;
+  }
+  if (q8) {  // (Hq * hd is then a multiple of 128: every lane is live)
+    float mx = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(bf2f(ob[e])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    const int e = fp8_scale_exp(fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3])));
-    q8[row * (int64_t)Hq * hd + idx] = (uint8_t)fp8_code(v, e);
-    if (threadIdx.x == 0) qs[row * (int64_t)(Hq * hd / 128) + blockIdx.z] = ldexpf(1.f, e);
+    const int ex = fp8_scale_exp(mx);
+    uint32_t c = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c |= (uint32_t)fp8_code(bf2f(ob[e]), ex) << (8 * e);
+    *reinterpret_cast<uint32_t*>(q8 + row * (int64_t)width + col) = c;
+    if (lane == 0) qs[row * (int64_t)(width / 128) + chunk] = ldexpf(1.f, ex);
   }
 }
 
@@ -1741,8 +1794,8 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
       BI_TRY(hd == 64 ? launch_attention<64, false, false>(args, grid, st)
                       : launch_attention<128, false, false>(args, grid, st));
   }
-  dim3 mgrid((unsigned)max_q_len, (unsigned)P, (unsigned)cdiv(Hq * hd, 128));
-  return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(128), 0, st, (const float*)part_o,
+  dim3 mgrid((unsigned)max_q_len, (unsigned)P, (unsigned)cdiv(cdiv(Hq * hd, 128), kMergeWarps));
+  return launched(launch_pdl(attention_merge_kernel, mgrid, dim3(kMergeWarps * 32), 0, st, (const float*)part_o,
                              (const float*)part_ml, args.pm, Hq, hd, (int)ns, split, static_cast<__nv_bfloat16*>(out),
                              static_cast<uint8_t*>(out_q), out_scale, args.status),
                   "attention_merge_kernel");
