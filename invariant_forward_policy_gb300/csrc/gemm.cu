@@ -102,6 +102,18 @@ __device__ __forceinline__ void tile_lse_step4(float& m, float& s, float& best, 
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
 
+// Per-element epilogue arithmetic, shared by every GEMM schedule.
+// SwiGLU: silu(bf16(gate)) * bf16(up) in fp32, from the fp32 accumulators.
+__device__ __forceinline__ float swiglu_elem(float g, float u) {
+  return __fmul_rn(silu_f(bf2f(f2bf(g))), bf2f(f2bf(u)));
+}
+// RoPE rotate-half of the pair (x1, x2) = bf16 of the accumulators (j, j + hd/2).
+__device__ __forceinline__ void rope_pair(float x1, float x2, float c, float s, float& o1, float& o2) {
+  const float v1 = bf2f(f2bf(x1)), v2 = bf2f(f2bf(x2));
+  o1 = __fsub_rn(__fmul_rn(v1, c), __fmul_rn(v2, s));
+  o2 = __fadd_rn(__fmul_rn(v2, c), __fmul_rn(v1, s));
+}
+
 // CW consecutive accumulator columns of this warp's 32 TMEM lanes (CW = 16 or 32).
 template <int CW>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CW]) {
@@ -138,9 +150,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int i = q * 8 + e * 2 + h;
-              const float gb = bf2f(f2bf(__uint_as_float(g[i])));
-              const float ub = bf2f(f2bf(__uint_as_float(u[i])));
-              a2[h] = __fmul_rn(silu_f(gb), ub);
+              a2[h] = swiglu_elem(__uint_as_float(g[i]), __uint_as_float(u[i]));
             }
             pv[e] = pack_bf16x2(a2[0], a2[1]);
           }
@@ -204,13 +214,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         for (int i = 0; i < 32; i += 2) {
           float a1[2], a2[2];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float v1 = bf2f(f2bf(__uint_as_float(x1[i + e])));
-            const float v2 = bf2f(f2bf(__uint_as_float(x2[i + e])));
-            const float cc = cs[j0 + i + e], ss = cs[half + j0 + i + e];
-            a1[e] = __fsub_rn(__fmul_rn(v1, cc), __fmul_rn(v2, ss));
-            a2[e] = __fadd_rn(__fmul_rn(v2, cc), __fmul_rn(v1, ss));
-          }
+          for (int e = 0; e < 2; ++e)
+            rope_pair(__uint_as_float(x1[i + e]), __uint_as_float(x2[i + e]), cs[j0 + i + e], cs[half + j0 + i + e],
+                      a1[e], a2[e]);
           o1[i / 2] = pack_bf16x2(a1[0], a1[1]);
           o2[i / 2] = pack_bf16x2(a2[0], a2[1]);
         }
@@ -537,6 +543,203 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   }
 }
 
+// ------------------------------------------------------------------ decode-size rows
+// Calls with M <= 16 rows (a decode step) of a dense weight.  One CTA per
+// TN-wide output tile; MMA warp w accumulates the 16 x 8 slice of the tile's W
+// rows 8w..8w+7 over the whole K in ascending 16-wide mma.sync steps
+// (m16n8k16, fp32 accumulator starting at -0, the identity of the first add),
+// while four loader warps stream the operands into shared memory.
+// Each step is the same 16-term bf16 tensor-core dot product added to the
+// accumulator as one tcgen05.mma K-step, which gives the same fp32 bits; the
+// epilogue applies the same per-element formulas.  So every element equals
+// the tcgen05 kernel's bit for bit (the row-invariance tests compare rows on
+// both sides of M = 16).  What changes is the schedule for a tile of 16 rows:
+// no TMEM, no stage ring, the whole W slice requested (cp.async) before the
+// dependency wait, A after it, both consumed in 256-column K chunks as they
+// land.  (Per-row bulk copies cost about 70 cycles each in the copy engine,
+// more than these 16-row tiles' data takes through cp.async.)
+constexpr int kRowsM = 16;
+constexpr int kRowsKC = 256;
+constexpr int kRowsMaxK = 4096;
+constexpr size_t kRowsMaxSmem = 220 * 1024;
+
+__host__ __device__ constexpr int rows_stride(int K) { return K * 2 + 16; }  // bytes; ldmatrix rows hit distinct banks
+__host__ constexpr size_t rows_smem_bytes(int K, int TN) {
+  return 256 + (size_t)(kRowsM + TN) * rows_stride(K) + (size_t)kRowsM * (TN + 4) * 4;
+}
+
+constexpr int kRowsLoadWarps = 4;
+template <int TN>
+constexpr int rows_threads() { return (TN / 8 + kRowsLoadWarps) * 32; }
+
+template <int EPI, int TN>
+__global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __nv_bfloat16* __restrict__ A,
+                                                                       const __nv_bfloat16* __restrict__ W,
+                                                                       const GemmArgs args) {
+  constexpr bool kSwiglu = EPI == EPI_SWIGLU;
+  constexpr int kTS = TN + 4;  // staged accumulator row (floats)
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
+  const int K = args.K, M = args.M, stride = rows_stride(K);
+  uint8_t* sA = smem_raw + 256;
+  uint8_t* sW = sA + kRowsM * stride;
+  float* sT = reinterpret_cast<float*>(sW + TN * stride);
+  const int nch = (K + kRowsKC - 1) / kRowsKC;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  pdl_trigger();
+
+  // global W row of tile row r (SwiGLU: gate rows, then the matching up rows), -1 past the weight
+  auto w_row = [&](int r) -> int64_t {
+    if (kSwiglu) {
+      const int j = tile * (TN / 2) + (r % (TN / 2));
+      if (j >= args.n_out) return -1;
+      return r < TN / 2 ? j : (int64_t)args.n_out + j;
+    }
+    const int n = tile * TN + r;
+    return n < args.n_out ? n : -1;
+  };
+  auto chunk_cols = [&](int c) { return min(kRowsKC, K - c * kRowsKC); };
+
+  constexpr int kMmaWarps = TN / 8, kLoaders = kRowsLoadWarps * 32;
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < nch; ++c) mbar_init(&bar[c], kLoaders);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (warp >= kMmaWarps) {
+    // loader warps: warp lw copies rows lw, lw + 4, ... in 16-byte cp.async
+    // pieces, lane by lane along the row.  The weights never come from the
+    // preceding kernel and are in flight before the dependency wait; A follows
+    // it chunk by chunk, each chunk's barrier completing once every loader's
+    // copies up to it have landed.  Rows past the weight or past M are not
+    // copied: MMA rows never mix, and those rows are never stored.
+    const int lw = warp - kMmaWarps;
+    for (int c = 0; c < nch; ++c) {
+      const int pc = chunk_cols(c) / 8, k0 = c * kRowsKC;
+      for (int r = lw; r < TN; r += kRowsLoadWarps) {
+        const int64_t gr = w_row(r);
+        if (gr < 0) continue;
+        const __nv_bfloat16* src = W + gr * K + k0;
+        uint8_t* dst = sW + r * stride + k0 * 2;
+        for (int p = lane; p < pc; p += 32) cp_async16(dst + p * 16, src + p * 8, true);
+      }
+    }
+    pdl_wait();
+    for (int c = 0; c < nch; ++c) {
+      const int pc = chunk_cols(c) / 8, k0 = c * kRowsKC;
+      for (int r = lw; r < M; r += kRowsLoadWarps) {
+        const __nv_bfloat16* src = A + (int64_t)r * K + k0;
+        uint8_t* dst = sA + r * stride + k0 * 2;
+        for (int p = lane; p < pc; p += 32) cp_async16(dst + p * 16, src + p * 8, true);
+      }
+      cp_async_mbar_arrive(&bar[c]);
+    }
+  } else {
+    pdl_wait();  // the outputs below are written only after the preceding kernel is done
+  }
+
+  // MMA warps 0 .. TN/8-1 start on each chunk as soon as it has landed
+  float d[4] = {-0.f, -0.f, -0.f, -0.f};
+  bool ok = true;
+  const uint32_t a_lane = smem_u32(sA) + (lane & 15) * stride + (lane >> 4) * 16;
+  const uint32_t w_lane = smem_u32(sW) + (warp * 8 + (lane & 7)) * stride + (lane >> 3) * 16;
+  for (int c = 0; c < nch && ok && warp < kMmaWarps; ++c) {
+    if (!mbar_wait(&bar[c], 0)) {
+      ok = false;
+      break;
+    }
+    const int k_end = c * kRowsKC + chunk_cols(c);
+#pragma unroll 2
+    for (int k = c * kRowsKC; k < k_end; k += 32) {
+      uint32_t a0[4], a1[4], b0, b1, b2, b3;
+      ldsm_x4(a_lane + k * 2, a0[0], a0[1], a0[2], a0[3]);
+      ldsm_x4(a_lane + k * 2 + 32, a1[0], a1[1], a1[2], a1[3]);
+      ldsm_x4(w_lane + k * 2, b0, b1, b2, b3);
+      mma_bf16_16816(d, a0, b0, b1);
+      mma_bf16_16816(d, a1, b2, b3);
+    }
+  }
+  if (!ok) report(args.status, DEV_TIMEOUT);
+  cp_async_wait<0>();  // this thread's copies have landed before it can leave
+  ok = __syncthreads_and(ok);
+  if (!ok) return;
+
+  const int g = lane >> 2, t2 = 2 * (lane & 3);
+  if constexpr (EPI == EPI_BF16 || EPI == EPI_F32) {
+    const int col = tile * TN + warp * 8 + t2;
+    if (warp < kMmaWarps && col < args.n_out) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = g + 8 * h;
+        if (row >= M) continue;
+        if (EPI == EPI_BF16)
+          *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(args.C) + (size_t)row * args.ldc + col) =
+              pack_bf16x2(d[2 * h], d[2 * h + 1]);
+        else
+          *reinterpret_cast<float2*>(static_cast<float*>(args.C) + (size_t)row * args.ldc + col) =
+              make_float2(d[2 * h], d[2 * h + 1]);
+      }
+    }
+  } else {
+    // stage the 16 x TN accumulators, then apply the pairwise epilogue
+    if (warp < kMmaWarps) {
+      sT[g * kTS + warp * 8 + t2] = d[0];
+      sT[g * kTS + warp * 8 + t2 + 1] = d[1];
+      sT[(g + 8) * kTS + warp * 8 + t2] = d[2];
+      sT[(g + 8) * kTS + warp * 8 + t2 + 1] = d[3];
+    }
+    __syncthreads();
+    if constexpr (kSwiglu) {
+      constexpr int H = TN / 2;
+      const int j0 = tile * H;
+      for (int i = threadIdx.x; i < kRowsM * H; i += blockDim.x) {
+        const int row = i / H, j = i % H;
+        if (row >= M || j0 + j >= args.n_out) continue;
+        static_cast<__nv_bfloat16*>(args.C)[(size_t)row * args.ldc + j0 + j] =
+            f2bf(swiglu_elem(sT[row * kTS + j], sT[row * kTS + H + j]));
+      }
+    } else if constexpr (EPI == EPI_ROPE) {
+      // the tile is head `tile`: q and k heads rotate-half, v heads copied; rows as the tcgen05 epilogue
+      const RopeKvArgs& ra = args.rope;
+      constexpr int half = TN / 2;
+      const int h = tile;
+      for (int i = threadIdx.x; i < kRowsM * half; i += blockDim.x) {
+        const int row = i / half, j = i % half;
+        if (row >= M) continue;
+        const int seq = ra.row_seq[row];
+        const int64_t pos = ra.row_pos[row];
+        if (pos < 0 || pos >= ra.max_pos) {
+          if (j == 0) report(args.status, DEV_BAD_INDEX);
+          continue;
+        }
+        int64_t blk = -1;
+        const int32_t b = (pos / 64 < ra.max_blk) ? ra.block_table[(int64_t)seq * ra.max_blk + pos / 64] : -1;
+        if (b >= 0 && b < ra.n_blocks) blk = b;
+        else if (j == 0) report(args.status, DEV_BAD_INDEX);
+        const int slot = (int)(pos % 64);
+        const float x1 = sT[row * kTS + j], x2 = sT[row * kTS + half + j];
+        __nv_bfloat16* dst;
+        if (h < ra.Hq + ra.Hkv) {
+          if (h < ra.Hq) dst = ra.q_out + ((int64_t)row * ra.Hq + h) * TN;
+          else if (blk >= 0) dst = ra.k_cache + ((blk * ra.Hkv + (h - ra.Hq)) * 64 + slot) * TN;
+          else continue;
+          const float* cs = ra.table + pos * TN;
+          float o1, o2;
+          rope_pair(x1, x2, cs[j], cs[half + j], o1, o2);
+          dst[j] = f2bf(o1);
+          dst[half + j] = f2bf(o2);
+        } else {
+          if (blk < 0) continue;
+          dst = ra.v_cache + ((blk * ra.Hkv + (h - ra.Hq - ra.Hkv)) * 64 + slot) * TN;
+          dst[j] = f2bf(x1);
+          dst[half + j] = f2bf(x2);
+        }
+      }
+    }
+  }
+}
+
 // Split-K reduction of the non-invariant path: sums partials in split order.
 template <int EPI>
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int M, int n_out, int ldp,
@@ -660,6 +863,61 @@ struct GemmCall {
   const RopeKvArgs* rope = nullptr;  // fused RoPE + paged KV write (non-NULL selects it)
 };
 
+template <int EPI, int TN>
+static bi_status launch_rows(const void* A, const void* W, const GemmArgs& args, int n_tiles, size_t smem,
+                             cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_rows_kernel<EPI, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kRowsMaxSmem);
+  });
+  if (attr_err != cudaSuccess)
+    return fail(BI_ERR_CUDA, std::string("gemm rows smem attribute: ") + cudaGetErrorString(attr_err));
+  return launched(launch_pdl(gemm_rows_kernel<EPI, TN>, dim3(n_tiles), dim3(rows_threads<TN>()), smem, st,
+                             static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(W), args),
+                  "gemm_rows_kernel");
+}
+
+// Output columns per CTA of the decode-size schedule (never changes results):
+// 16 (SwiGLU: 16 gate + 16 up), whole heads for the fused RoPE.
+static int rows_tile(const GemmCall& g, bool swiglu) {
+  if (g.rope) return g.rope->hd;
+  return swiglu ? 32 : 16;
+}
+
+// The decode-size schedule takes invariant dense calls of at most 16 rows whose
+// W slice and rows fit shared memory; BI_FAST keeps its M-dependent plan.
+static bool rows_path(const GemmCall& g, int64_t n_out, bool swiglu) {
+  if (g.mode != BI_INVARIANT || g.M < 1 || g.M > kRowsM || g.E != 1 || g.tile_expert || g.lse) return false;
+  if (g.K % 64 || g.K > kRowsMaxK || n_out % 8) return false;
+  if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.W)) & 15) return false;
+  if (g.rope && ((g.rope->hd != 64 && g.rope->hd != 128) || g.n_rows_w % g.rope->hd)) return false;
+  return rows_smem_bytes((int)g.K, rows_tile(g, swiglu)) <= kRowsMaxSmem;
+}
+
+static bi_status run_rows(const GemmCall& g, int64_t n_out, bool swiglu, cudaStream_t st) {
+  GemmArgs args = {};
+  args.C = g.C;
+  args.status = device_status_ptr();
+  args.M = (int)g.M;
+  args.K = (int)g.K;
+  args.ldc = (int)n_out;
+  args.n_out = (int)n_out;
+  const int tn = rows_tile(g, swiglu);
+  const size_t smem = rows_smem_bytes((int)g.K, tn);
+  if (g.rope) {
+    args.rope = *g.rope;
+    const int heads = (int)(g.n_rows_w / tn);
+    return tn == 64 ? launch_rows<EPI_ROPE, 64>(g.A, g.W, args, heads, smem, st)
+                    : launch_rows<EPI_ROPE, 128>(g.A, g.W, args, heads, smem, st);
+  }
+  const int n_tiles = (int)cdiv(n_out, 16);
+  if (swiglu) return launch_rows<EPI_SWIGLU, 32>(g.A, g.W, args, n_tiles, smem, st);
+  return g.c_dtype == BI_DTYPE_FP32 ? launch_rows<EPI_F32, 16>(g.A, g.W, args, n_tiles, smem, st)
+                                    : launch_rows<EPI_BF16, 16>(g.A, g.W, args, n_tiles, smem, st);
+}
+
 static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
   return splits > 1 ? (size_t)splits * M * n_rows_w * sizeof(float) : 0;
 }
@@ -667,6 +925,7 @@ static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
 static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   const bool swiglu = g.epilogue == BI_EPI_SWIGLU;
   const int64_t n_out = swiglu ? g.n_rows_w / 2 : g.n_rows_w;
+  if (rows_path(g, n_out, swiglu)) return run_rows(g, n_out, swiglu, st);
   int bn = tile_n_for(g.n_rows_w, g.K, swiglu, g.E), splits = 1;
   if (g.mode == BI_FAST && g.E == 1) {
     fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);

@@ -531,3 +531,46 @@ def test_fused_qkv_rope_kv_write_equals_gemm_then_rope(Hq, Hkv, hd):
     assert same_bits(q2, q1)
     assert same_bits(kc2, kc1) and same_bits(vc2, vc1)
     assert bi.bi_device_status() == 0
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd,K", [(8, 8, 64, 512), (16, 4, 128, 512), (16, 4, 128, 2048)])
+def test_fused_qkv_rope_rows_invariant_to_M(Hq, Hkv, hd, K):
+    """The fused QKV + RoPE + paged K/V write: a decode-size call (M <= 16 rows)
+    writes the same q and cache bits for its rows as a 300-row call, whichever
+    schedule each call takes."""
+    rng = np.random.default_rng(Hq * K + hd)
+    seq_lens = [130, 1, 77, 92]
+    T = sum(seq_lens)
+    N = (Hq + 2 * Hkv) * hd
+    xb, _ = rng_bf16(rng, (T, K))
+    wb, _ = rng_bf16(rng, (N, K), 0.05)
+    X, W = dev_bf16(xb), dev_bf16(wb)
+    max_pos = 1024
+    table = torch.empty((max_pos, hd), dtype=torch.float32, device="cuda")
+    bi.bi_rope_table(table, max_pos, hd, 10000.0)
+    starts = [3, 0, 200, 64]
+    bt, kc, vc, max_blk, n_blocks = _paged_setup([s + n for s, n in zip(starts, seq_lens)], Hq, Hkv, hd, rng)
+    kc.zero_()
+    vc.zero_()
+    seqs = np.repeat(np.arange(len(seq_lens)), seq_lens).astype(np.int32)
+    poss = np.concatenate([starts[b] + np.arange(n) for b, n in enumerate(seq_lens)]).astype(np.int32)
+    row_seq, row_pos = torch.from_numpy(seqs).cuda(), torch.from_numpy(poss).cuda()
+    q = torch.empty((T, Hq, hd), dtype=torch.bfloat16, device="cuda")
+    bi.bi_qkv_rope_kv_write(X, T, K, W, Hq, Hkv, hd, row_seq, row_pos, table, max_pos, bt, max_blk, n_blocks, q,
+                            kc, vc)
+    btc = bt.cpu().numpy()
+    for M in (1, 5, 16, 17):
+        idx = np.sort(rng.choice(T, M, replace=False))
+        kp, vp = torch.zeros_like(kc), torch.zeros_like(vc)
+        qp = torch.empty((M, Hq, hd), dtype=torch.bfloat16, device="cuda")
+        it = torch.from_numpy(idx).cuda()
+        bi.bi_qkv_rope_kv_write(X[it].contiguous(), M, K, W, Hq, Hkv, hd, row_seq[it].contiguous(),
+                                row_pos[it].contiguous(), table, max_pos, bt, max_blk, n_blocks, qp, kp, vp)
+        assert same_bits(qp, q[it]), M
+        blk = torch.from_numpy(btc[seqs[idx], poss[idx] // 64].astype(np.int64)).cuda()
+        slot = torch.from_numpy((poss[idx] % 64).astype(np.int64)).cuda()
+        assert same_bits(kp[blk, :, slot], kc[blk, :, slot]) and same_bits(vp[blk, :, slot], vc[blk, :, slot]), M
+        written = torch.zeros(kp.shape[0], kp.shape[2], dtype=torch.bool, device="cuda")
+        written[blk, slot] = True
+        assert not kp.permute(0, 2, 1, 3)[~written].any() and not vp.permute(0, 2, 1, 3)[~written].any(), M
+    assert bi.bi_device_status() == 0
