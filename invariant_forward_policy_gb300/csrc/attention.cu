@@ -125,6 +125,7 @@ struct AttnArgs {
   int64_t max_blk, n_blocks;
   int Hq, Hkv, group, nsplit, split;  // split = positions per split
   float scale_log2;
+  __nv_bfloat16* out;  // [T, Hq * hd]: FUSED decode only (the splits merged in the kernel)
 };
 
 constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
@@ -357,6 +358,43 @@ __device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row
   }
 }
 
+// FUSED decode: the output of the two rows a thread holds from the partials of
+// split 0 (P0) and split 1 (P1), with the split merge's arithmetic: M = max_s
+// m_s, then L and O summed over s = 0, 1 in that order (a row whose position
+// is before split 1 has only split 0), out = bf16(O / L).
+template <int HD>
+__device__ __forceinline__ void fused_split_merge(const AttnArgs& a, const LaneState<HD>& P0,
+                                                  const LaneState<HD>* P1, const bool (&row_valid)[2],
+                                                  const int (&row_pos)[2], const int (&row_tok)[2],
+                                                  const int (&row_head)[2], int tq) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (!row_valid[h]) continue;
+    const int ns = merge_split_count(row_pos[h], a.split, a.nsplit, a.status, tq == 0);
+    float M = fmaxf(-INFINITY, P0.m[h]);
+    if (ns > 1) M = fmaxf(M, P1->m[h]);
+    const float w0 = merge_weight(P0.m[h], M);
+    const float w1 = ns > 1 ? merge_weight(P1->m[h], M) : 0.f;
+    float L = merge_term(0.f, P0.l[h], w0);
+    if (ns > 1) L = merge_term(L, P1->l[h], w1);
+    __nv_bfloat16* orow = a.out + ((int64_t)row_tok[h] * a.Hq + row_head[h]) * HD;
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) {
+      float o[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        o[e] = merge_term(0.f, P0.acc[j][h * 2 + e], w0);
+        if (ns > 1) o[e] = merge_term(o[e], P1->acc[j][h * 2 + e], w1);
+        o[e] = __fdiv_rn(o[e], L);
+      }
+      __nv_bfloat162 v;
+      v.x = f2bf(o[0]);
+      v.y = f2bf(o[1]);
+      *reinterpret_cast<__nv_bfloat162*>(orow + j * 8 + tq * 2) = v;
+    }
+  }
+}
+
 // One CTA per (piece, query tile, kv head, split), two schedules:
 // PREFILL (64-row query tiles): warp w owns rows 16w..16w+15 and walks the
 // split's tiles in order from a shared two-stage cp.async ring, folding each
@@ -364,6 +402,12 @@ __device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row
 // DECODE (query tiles of at most 16 rows, short contexts): warp w computes
 // lane w of the split from its own one-tile buffer, then warp 0 merges the
 // lanes in order.
+// FUSED (DECODE with at most two splits): one CTA per (piece, query tile, kv
+// head) covers both splits with eight warps, warp w computing lane w % 4 of
+// split w / 4; warps 0 and 4 fold their split's lanes in order, and warp 0
+// merges the two split partials with the split merge's formulas (ascending
+// split order) and writes the output rows: no partials leave the CTA and no
+// merge kernel runs.
 // KV8: the cache holds e4m3 codes and per-(slot, kv head) scales.  Each tile's
 // codes and scales are copied (cp.async) into a staging area, then expanded
 // into the same swizzled bf16 tile the bf16 cache gives (code x power-of-two
@@ -374,16 +418,17 @@ struct Kv8Stage {
   static constexpr int kBytes = 2 * kCodes + 2 * kKeys * 4;  // K codes, V codes, K scales, V scales
 };
 
-template <int HD, bool DECODE, bool KV8>
-__global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
+template <int HD, bool DECODE, bool KV8, bool FUSED = false>
+__global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const AttnArgs a) {
+  static_assert(!FUSED || DECODE, "the fused split merge is a decode schedule");
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   pdl_trigger();
   pdl_wait();
   const int p = blockIdx.y;
-  const int kvh = blockIdx.z % a.Hkv;
-  const int s = blockIdx.z / a.Hkv;
+  const int kvh = FUSED ? (int)blockIdx.z : (int)blockIdx.z % a.Hkv;
+  const int s = FUSED ? (int)(threadIdx.x >> 7) : (int)blockIdx.z / a.Hkv;
   const int row0 = a.pm.row0[p];
   const int n_tok = a.pm.row0[p + 1] - row0;
   const int tok_per_tile = (DECODE ? 16 : kRows) / a.group;
@@ -393,7 +438,10 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   const int tok_last = min(n_tok, tok0 + tok_per_tile) - 1;
   const int max_pos = pos_first + tok_last;  // last query position in this CTA
   const int kv_begin = s * a.split;
-  if (kv_begin > max_pos) return;  // split entirely in the future of every row here
+  // a split entirely in the future of every row here: nothing to do (FUSED: this
+  // half of the CTA only skips its lanes; split 0 always holds position 0)
+  if (!FUSED && kv_begin > max_pos) return;
+  const bool split_live = kv_begin <= max_pos;
   const int kv_end = min(kv_begin + a.split, max_pos + 1);  // exclusive
   const int lane_len = ((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys;
   const int seq = a.pm.seq[p];
@@ -496,12 +544,13 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
   for (int j = 0; j < HD / 8; ++j) P.acc[j][0] = P.acc[j][1] = P.acc[j][2] = P.acc[j][3] = 0.f;
 
   if (DECODE) {
-    // ---- lane `warp`, from this warp's own one-tile buffer
+    // ---- lane `warp` (FUSED: lane warp % 4 of split warp / 4), from this warp's own one-tile buffer
+    constexpr int kWarps = FUSED ? 8 : 4;
     uint8_t* sk = smem + warp * 2 * TILE_BYTES;
     uint8_t* sv = sk + TILE_BYTES;
-    const int lb = kv_begin + warp * lane_len;
-    const int le = min(lb + lane_len, kv_end);
-    uint8_t* stg = smem + 4 * 2 * TILE_BYTES + warp * Kv8Stage<HD>::kBytes;  // KV8 only
+    const int lb = kv_begin + (warp & 3) * lane_len;
+    const int le = split_live ? min(lb + lane_len, kv_end) : lb;
+    uint8_t* stg = smem + kWarps * 2 * TILE_BYTES + warp * Kv8Stage<HD>::kBytes;  // KV8 only
     for (int key0 = lb; key0 < le; key0 += kKeys) {
       if constexpr (KV8) {
         load_tile8(key0, stg, lane, 32);
@@ -529,6 +578,21 @@ __global__ void __launch_bounds__(128) attention_kernel(const AttnArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) st->acc[j][c] = acc[j][c];
     __syncthreads();
+    if constexpr (FUSED) {
+      // warps 0 and 4 fold the lanes of splits 0 and 1; warp 4 leaves its partial in its buffer
+      if ((warp & 3) == 0 && split_live) {
+        const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
+        for (int w = 0; w < n_lanes; ++w) {
+          const LaneState<HD>* q = reinterpret_cast<const LaneState<HD>*>(smem + (warp + w) * 2 * TILE_BYTES) + lane;
+          lane_merge<HD>(P, q->m, q->l, q->acc);
+        }
+        if (warp == 4) *(reinterpret_cast<LaneState<HD>*>(smem + 4 * 2 * TILE_BYTES) + lane) = P;
+      }
+      __syncthreads();
+      if (warp == 0) fused_split_merge<HD>(a, P, reinterpret_cast<const LaneState<HD>*>(smem + 4 * 2 * TILE_BYTES) + lane,
+                                           row_valid, row_pos, row_tok, row_head, tq);
+      return;
+    }
     if (warp != 0) return;
     const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
     for (int w = 0; w < n_lanes; ++w) {
@@ -1524,28 +1588,28 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attention_merge_kernel(
   }
 }
 
-template <int HD, bool DECODE, bool KV8>
+template <int HD, bool DECODE, bool KV8, bool FUSED = false>
 constexpr int attn_smem_bytes() {
-  // decode: one K+V tile per warp (+ one staging area per warp for KV8);
-  // prefill: a two-stage ring plus the running lane state (KV8: one K+V tile,
-  // the running states and two staging areas)
-  return DECODE ? 4 * 2 * kKeys * HD * 2 + (KV8 ? 4 * Kv8Stage<HD>::kBytes : 0)
+  // decode: one K+V tile per warp (+ one staging area per warp for KV8), four
+  // warps or (FUSED) eight; prefill: a two-stage ring plus the running lane
+  // state (KV8: one K+V tile, the running states and two staging areas)
+  return DECODE ? (FUSED ? 8 : 4) * (2 * kKeys * HD * 2 + (KV8 ? Kv8Stage<HD>::kBytes : 0))
                 : (KV8 ? 1 : 2) * 2 * kKeys * HD * 2 + 128 * (int)sizeof(LaneState<HD>) +
                       (KV8 ? 2 * Kv8Stage<HD>::kBytes : 0);
 }
 
-template <int HD, bool DECODE, bool KV8>
+template <int HD, bool DECODE, bool KV8, bool FUSED = false>
 static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t st) {
-  constexpr int smem = attn_smem_bytes<HD, DECODE, KV8>();
+  constexpr int smem = attn_smem_bytes<HD, DECODE, KV8, FUSED>();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err =
-        cudaFuncSetAttribute(attention_kernel<HD, DECODE, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_err = cudaFuncSetAttribute(attention_kernel<HD, DECODE, KV8, FUSED>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(attention_kernel<HD, DECODE, KV8>, grid, dim3(128), smem, st, args),
+  return launched(launch_pdl(attention_kernel<HD, DECODE, KV8, FUSED>, grid, dim3(FUSED ? 256 : 128), smem, st, args),
                   "attention_kernel");
 }
 
@@ -1746,6 +1810,13 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
   // tiles take the tensor-memory prefill schedule (bf16 caches) or the
   // mma.sync row-parallel one (FP8 caches).
   const bool decode = max_q_len * group <= 16;
+  args.out = static_cast<__nv_bfloat16*>(out);
+  if (decode && ns <= 2 && hd == 64 && out && !out_q) {
+    // short contexts: both splits in one CTA, merged there (no partials, no merge kernel)
+    dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)Hkv);
+    return kv8 ? launch_attention<64, true, true, true>(args, grid, st)
+               : launch_attention<64, true, false, true>(args, grid, st);
+  }
   if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
     BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
     if (kv8)

@@ -367,6 +367,59 @@ def test_attention_decode_schedules_agree(Hq, Hkv, hd, B):
     assert same_bits(outs[1], outs[0])
 
 
+@pytest.mark.parametrize("Hq,Hkv,hd,B", [(8, 8, 64, 16), (8, 2, 64, 300), (4, 1, 64, 37), (16, 4, 128, 40)])
+def test_attention_decode_two_split_schedule(Hq, Hkv, hd, B):
+    """Decode calls whose contexts fit two splits (max_ctx <= 1024) take, at hd 64,
+    the schedule that covers both splits in one CTA and merges them there.  Its
+    rows equal, bit for bit, those of the per-split schedule (max_ctx 2048) and of
+    the persistent one (max_ctx 16384), and match the oracle's explicit softmax
+    (rows before, at and after the split boundary).  Slots after each sequence's
+    last position hold NaN."""
+    rng = np.random.default_rng(B + 5 * hd + Hkv)
+    ctx = rng.integers(1, 1025, B)
+    ctx[: min(B, 4)] = [1, 512, 513, 1024][: min(B, 4)]
+    max_blk = 16
+    n_blocks = B * max_blk
+    bt = torch.from_numpy(rng.permutation(n_blocks).astype(np.int32).reshape(B, max_blk)).cuda()
+    kb = normal_bf16(rng, (n_blocks, Hkv, 64, hd), 0.5)
+    vb = normal_bf16(rng, (n_blocks, Hkv, 64, hd), 0.5)
+    kc, vc = dev_bf16(kb), dev_bf16(vb)
+    stale = np.zeros((n_blocks, 64), dtype=bool)
+    tab = bt.cpu().numpy()
+    for b in range(B):
+        last = (ctx[b] - 1) // 64
+        stale[tab[b, last], ctx[b] - last * 64:] = True
+        stale[tab[b, last + 1:]] = True
+    m = torch.from_numpy(stale).cuda()
+    kc.permute(0, 2, 1, 3)[m] = float("nan")
+    vc.permute(0, 2, 1, 3)[m] = float("nan")
+    qb = normal_bf16(rng, (B, Hq, hd), 0.5)
+    q = dev_bf16(qb)
+    seq = torch.arange(B, dtype=torch.int32, device="cuda")
+    row0 = torch.arange(B + 1, dtype=torch.int32, device="cuda")
+    pos0 = torch.from_numpy((ctx - 1).astype(np.int32)).cuda()
+    outs = []
+    for max_ctx in (1024, 2048, 16384):
+        out = torch.empty((B, Hq * hd), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(bi.bi_attention_workspace_size(B, Hq, hd, max_ctx, 512), dtype=torch.uint8, device="cuda")
+        bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, n_blocks, max_ctx, 512,
+                        hd ** -0.5, ws, out)
+        outs.append(out)
+    assert bi.bi_device_status() == 0
+    assert not torch.isnan(outs[0].float()).any()
+    assert same_bits(outs[1], outs[0]) and same_bits(outs[2], outs[0])
+    got = host_f32(outs[0]).reshape(B, Hq, hd)
+    kf, vf = bits_to_f32(kb), bits_to_f32(vb)
+    for b in range(min(B, 4)):
+        n = int(ctx[b])
+        blocks = tab[b, : (n + 63) // 64]
+        k = kf[blocks].transpose(0, 2, 1, 3).reshape(-1, Hkv, hd)[:n]
+        v = vf[blocks].transpose(0, 2, 1, 3).reshape(-1, Hkv, hd)[:n]
+        want = ops.attention(bits_to_f32(qb[b:b + 1]), k, v, np.array([n - 1]))
+        err = np.abs(got[b] - want[0])
+        assert err.max() < 2e-2 and err.mean() < 2e-3, (b, n, err.max(), err.mean())
+
+
 # ---------------------------------------------------------------------------- MoE
 def _moe_dev(T, d, F, E, seed):
     inp = make_moe_layer(T, d, F, E, 0.05, seed)
