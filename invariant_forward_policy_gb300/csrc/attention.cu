@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <mutex>
 #include <string>
+#include <type_traits>
 
 #include "attn_merge.cuh"
 #include "common.cuh"
@@ -129,6 +130,8 @@ struct AttnArgs {
 };
 
 constexpr int kRows = 64;   // query rows per CTA (4 warps x 16)
+constexpr std::integral_constant<int, 32> kThr32{};    // copy loops of one warp
+constexpr std::integral_constant<int, 128> kThr128{};  // copy loops of four warps
 constexpr int kKeys = 64;   // keys per tile = cache block
 
 // Per-row arithmetic (shared by the decode and the prefill schedule below):
@@ -466,14 +469,19 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
   load_q_frags<HD>(a, row_valid, row_tok, row_head, tq, qf);
 
   // copy one 64-key tile of K and V into (sk, sv) with threads t0, t0 + nthr, ...;
-  // keys after max_pos are zero-filled
-  auto load_tile = [&](int key0, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
+  // keys after max_pos are zero-filled.  nthr is a compile-time constant
+  // (std::integral_constant) so that the copy loops unroll: a loop with
+  // run-time bounds around each copy costs more issue slots than the copies.
+  auto load_tile = [&](int key0, uint8_t* sk, uint8_t* sv, int t0, auto nthr_c) {
+    constexpr int nthr = decltype(nthr_c)::value;
     const bool tab_ok = key0 / kKeys < a.max_blk;
     const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
     const bool blk_ok = blk >= 0 && blk < a.n_blocks;
     if (!blk_ok && t0 == 0) report(a.status, DEV_BAD_INDEX);
     const int64_t base = ((int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh) * kKeys * HD;
-    for (int c = t0; c < kKeys * CH; c += nthr) {
+#pragma unroll
+    for (int i = 0; i < kKeys * CH / nthr; ++i) {
+      const int c = t0 + i * nthr;
       const int key = c / CH, ch = c % CH;
       const bool valid = blk_ok && (key0 + key) <= max_pos;
       const int off = (int)kv_off<HD>(key, ch);
@@ -486,14 +494,17 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
 
   // KV8: one tile's codes and scales into the staging area `stg`
   // (zero-filled where the block-table entry is bad or the key is in the future)
-  auto load_tile8 = [&](int key0, uint8_t* stg, int t0, int nthr) {
+  auto load_tile8 = [&](int key0, uint8_t* stg, int t0, auto nthr_c) {
+    constexpr int nthr = decltype(nthr_c)::value;
     constexpr int C16 = HD / 16;  // 16-code chunks per key row
     const bool tab_ok = key0 / kKeys < a.max_blk;
     const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
     const bool blk_ok = blk >= 0 && blk < a.n_blocks;
     if (!blk_ok && t0 == 0) report(a.status, DEV_BAD_INDEX);
     const int64_t page = (int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh;
-    for (int c = t0; c < kKeys * C16; c += nthr) {
+#pragma unroll
+    for (int i = 0; i < kKeys * C16 / nthr; ++i) {
+      const int c = t0 + i * nthr;
       const bool valid = blk_ok && (key0 + c / C16) <= max_pos;
       const int64_t src = page * Kv8Stage<HD>::kCodes + (int64_t)c * 16;
       cp_async16(stg + c * 16, a.k8 + (valid ? src : 0), valid);
@@ -509,9 +520,12 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
   // KV8: expand a staged tile into swizzled bf16 K and V tiles of the unscaled
   // e4m3 values (the scales are applied to the scores and to P); keys after
   // max_pos become zeros with zero scales, whatever their slot holds
-  auto expand_tile8 = [&](int key0, uint8_t* stg, uint8_t* sk, uint8_t* sv, int t0, int nthr) {
+  auto expand_tile8 = [&](int key0, uint8_t* stg, uint8_t* sk, uint8_t* sv, int t0, auto nthr_c) {
+    constexpr int nthr = decltype(nthr_c)::value;
     constexpr int C16 = HD / 16;
-    for (int c = t0; c < 2 * kKeys * C16; c += nthr) {
+#pragma unroll 4
+    for (int i = 0; i < 2 * kKeys * C16 / nthr; ++i) {
+      const int c = t0 + i * nthr;
       const int which = c >= kKeys * C16;
       const int cc = which ? c - kKeys * C16 : c;
       const int key = cc / C16, c16 = cc % C16;
@@ -553,12 +567,12 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
     uint8_t* stg = smem + kWarps * 2 * TILE_BYTES + warp * Kv8Stage<HD>::kBytes;  // KV8 only
     for (int key0 = lb; key0 < le; key0 += kKeys) {
       if constexpr (KV8) {
-        load_tile8(key0, stg, lane, 32);
+        load_tile8(key0, stg, lane, kThr32);
         cp_async_wait<0>();
         __syncwarp();
-        expand_tile8(key0, stg, sk, sv, lane, 32);
+        expand_tile8(key0, stg, sk, sv, lane, kThr32);
       } else {
-        load_tile(key0, sk, sv, lane, 32);
+        load_tile(key0, sk, sv, lane, kThr32);
         cp_async_wait<0>();
       }
       __syncwarp();
@@ -610,17 +624,17 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
     const int t_begin = kv_begin / kKeys;
     const int n_tiles = (kv_end - kv_begin + kKeys - 1) / kKeys;
     const int tiles_per_lane = lane_len / kKeys;
-    if constexpr (KV8) load_tile8(t_begin * kKeys, stg0, tid, 128);
-    else load_tile(t_begin * kKeys, smem, smem + TILE_BYTES, tid, 128);
+    if constexpr (KV8) load_tile8(t_begin * kKeys, stg0, tid, kThr128);
+    else load_tile(t_begin * kKeys, smem, smem + TILE_BYTES, tid, kThr128);
     for (int t = 0; t < n_tiles; ++t) {
       const int stage = t & 1;
       uint8_t* sk = smem + (KV8 ? 0 : stage) * 2 * TILE_BYTES;
       if (t + 1 < n_tiles) {
         if constexpr (KV8) {
-          load_tile8((t_begin + t + 1) * kKeys, stg0 + (stage ^ 1) * Kv8Stage<HD>::kBytes, tid, 128);
+          load_tile8((t_begin + t + 1) * kKeys, stg0 + (stage ^ 1) * Kv8Stage<HD>::kBytes, tid, kThr128);
         } else {
           uint8_t* nk = smem + (stage ^ 1) * 2 * TILE_BYTES;
-          load_tile((t_begin + t + 1) * kKeys, nk, nk + TILE_BYTES, tid, 128);
+          load_tile((t_begin + t + 1) * kKeys, nk, nk + TILE_BYTES, tid, kThr128);
         }
         cp_async_wait<1>();
       } else {
@@ -628,7 +642,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
       }
       __syncthreads();
       if constexpr (KV8) {
-        expand_tile8((t_begin + t) * kKeys, stg0 + stage * Kv8Stage<HD>::kBytes, sk, sk + TILE_BYTES, tid, 128);
+        expand_tile8((t_begin + t) * kKeys, stg0 + stage * Kv8Stage<HD>::kBytes, sk, sk + TILE_BYTES, tid, kThr128);
         __syncthreads();
       }
       if (t > 0 && t % tiles_per_lane == 0) {  // lane boundary: fold the finished lane in

@@ -564,6 +564,7 @@ constexpr int kRowsMaxK = 4096;
 constexpr size_t kRowsMaxSmem = 220 * 1024;
 
 __host__ __device__ constexpr int rows_stride(int K) { return K * 2 + 16; }  // bytes; ldmatrix rows hit distinct banks
+// barriers | A rows | W rows | staged accumulators [16][TN + 4]
 __host__ constexpr size_t rows_smem_bytes(int K, int TN) {
   return 256 + (size_t)(kRowsM + TN) * rows_stride(K) + (size_t)kRowsM * (TN + 4) * 4;
 }
@@ -614,24 +615,27 @@ __global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __n
     // it chunk by chunk, each chunk's barrier completing once every loader's
     // copies up to it have landed.  Rows past the weight or past M are not
     // copied: MMA rows never mix, and those rows are never stored.
+    // (One piece per lane per row and chunk, the row loop unrolled: a loop with
+    // run-time bounds around each copy costs more issue slots than the copies.)
     const int lw = warp - kMmaWarps;
     for (int c = 0; c < nch; ++c) {
-      const int pc = chunk_cols(c) / 8, k0 = c * kRowsKC;
-      for (int r = lw; r < TN; r += kRowsLoadWarps) {
+      const bool on = lane * 8 < chunk_cols(c);
+      const int k = c * kRowsKC + lane * 8;
+#pragma unroll 4
+      for (int rr = 0; rr < TN / kRowsLoadWarps; ++rr) {
+        const int r = lw + rr * kRowsLoadWarps;
         const int64_t gr = w_row(r);
-        if (gr < 0) continue;
-        const __nv_bfloat16* src = W + gr * K + k0;
-        uint8_t* dst = sW + r * stride + k0 * 2;
-        for (int p = lane; p < pc; p += 32) cp_async16(dst + p * 16, src + p * 8, true);
+        if (on && gr >= 0) cp_async16(sW + r * stride + k * 2, W + gr * K + k, true);
       }
     }
     pdl_wait();
     for (int c = 0; c < nch; ++c) {
-      const int pc = chunk_cols(c) / 8, k0 = c * kRowsKC;
-      for (int r = lw; r < M; r += kRowsLoadWarps) {
-        const __nv_bfloat16* src = A + (int64_t)r * K + k0;
-        uint8_t* dst = sA + r * stride + k0 * 2;
-        for (int p = lane; p < pc; p += 32) cp_async16(dst + p * 16, src + p * 8, true);
+      const bool on = lane * 8 < chunk_cols(c);
+      const int k = c * kRowsKC + lane * 8;
+#pragma unroll
+      for (int rr = 0; rr < kRowsM / kRowsLoadWarps; ++rr) {
+        const int r = lw + rr * kRowsLoadWarps;
+        if (on && r < M) cp_async16(sA + r * stride + k * 2, A + (int64_t)r * K + k, true);
       }
       cp_async_mbar_arrive(&bar[c]);
     }
@@ -886,10 +890,14 @@ static int rows_tile(const GemmCall& g, bool swiglu) {
   return swiglu ? 32 : 16;
 }
 
-// The decode-size schedule takes invariant dense calls of at most 16 rows whose
-// W slice and rows fit shared memory; BI_FAST keeps its M-dependent plan.
+// The decode-size schedule takes invariant dense calls of at most 16 rows of a
+// weight under 4M elements (a decoder layer's projections; larger weights,
+// such as a vocabulary head, stream faster through the tcgen05 kernel's TMA
+// ring) whose W slice and rows fit shared memory; BI_FAST keeps its
+// M-dependent plan, and the fused log-softmax stays on the tcgen05 kernel.
 static bool rows_path(const GemmCall& g, int64_t n_out, bool swiglu) {
   if (g.mode != BI_INVARIANT || g.M < 1 || g.M > kRowsM || g.E != 1 || g.tile_expert || g.lse) return false;
+  if (g.n_rows_w * g.K >= (int64_t(1) << 22)) return false;
   if (g.K % 64 || g.K > kRowsMaxK || n_out % 8) return false;
   if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.W)) & 15) return false;
   if (g.rope && ((g.rope->hd != 64 && g.rope->hd != 128) || g.n_rows_w % g.rope->hd)) return false;

@@ -8,7 +8,7 @@ import torch
 import invariant_forward_policy_gb300 as bi
 from oracle import moe as omoe
 from oracle import ops
-from synthetic import bits_to_f32, make_moe_layer, normal_bf16
+from synthetic import bits_to_f32, make_moe_layer, normal_bf16, to_bf16_bits
 from tests.gpu_util import bf16_close, dev_bf16, host_f32, same_bits
 
 pytestmark = pytest.mark.gpu
@@ -213,6 +213,39 @@ def test_fused_lm_head_logprob_parity_and_row_invariance(T, K, V):
         assert same_bits(l1, lp[t0:t0 + 1]) and torch.equal(a1, am[t0:t0 + 1])
     lf, _ = _fused_head(X, W, I, bi.BI_FAST)                   # the non-invariant path agrees closely
     assert np.max(np.abs(lf.cpu().numpy() - lp.cpu().numpy())) < 1e-4
+
+
+@pytest.mark.parametrize("K,V", [(256, 4096), (512, 32000)])
+def test_fused_lm_head_decode_rows_equal_large_calls_on_ties_and_rising_maxima(K, V):
+    """Decode-size calls of the fused head (1, 7 and 16 rows) give the bits of a
+    40-row call for every row: logits tied exactly (duplicated
+    weight rows, within and across vocab tiles) and maxima that rise step after
+    step inside a tile (weight rows scaled up column by column), targets on the
+    tied and rising columns, and greedy decoding."""
+    rng = np.random.default_rng(K + V)
+    T = 40
+    xb, _ = rng_bf16(rng, (T, K))
+    wb, wf = rng_bf16(rng, (V, K), 0.05)
+    wf = wf.copy()
+    # exact ties: column 3 equals column 1 (one tile), column 200 equals column 1 (another tile)
+    wf[3] = wf[1]
+    wf[200] = wf[1]
+    # rising maxima: columns 64..127 of the second tile scaled up 1.05x per column
+    wf[64:128] = wf[1][None, :] * (1.05 ** np.arange(1, 65))[:, None]
+    wb = to_bf16_bits(wf)
+    ids = rng.integers(0, V, T).astype(np.int32)
+    ids[:8] = [1, 3, 200, 64, 127, 100, V - 1, 0]
+    X, W, I = dev_bf16(xb), dev_bf16(wb), torch.from_numpy(ids).cuda()
+    lp, am = _fused_head(X, W, I)
+    lpg, amg = _fused_head(X, W, None)
+    for M in (1, 7, 16):
+        for t0 in (0, 13, T - M):
+            sl = slice(t0, t0 + M)
+            l1, a1 = _fused_head(X[sl].contiguous(), W, I[sl].contiguous())
+            assert same_bits(l1, lp[sl]) and torch.equal(a1, am[sl]), (M, t0)
+            l2, a2 = _fused_head(X[sl].contiguous(), W, None)
+            assert same_bits(l2, lpg[sl]) and torch.equal(a2, amg[sl]), (M, t0)
+    assert bi.bi_device_status() == 0
 
 
 # ---------------------------------------------------------------------------- RoPE + attention
