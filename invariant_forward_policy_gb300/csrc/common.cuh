@@ -73,6 +73,10 @@ bool module_symbol_address(const void* symbol, void** out, ModuleAddressCache* c
 // RMSNorm of rows idx[0..rows) of x / residual into the compact y[0..rows).
 bi_status rmsnorm_rows(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d, float eps,
                        const int32_t* idx, void* stream);
+// The same with x + residual written to res_out (NULL iff residual is NULL), which
+// may be the residual rows themselves or another buffer.
+bi_status rmsnorm_rows_to(const void* x, const void* residual, void* res_out, const void* gamma, void* y, int64_t rows,
+                          int64_t d, float eps, const int32_t* idx, void* stream);
 // Logprob / argmax of each logits row, written to out index dst[row] (dst may be NULL).
 bi_status logprob_gather_to(const float* logits, const int32_t* ids, int64_t T, int64_t V, float* logprob_out,
                             int32_t* argmax_out, const int32_t* dst, int mode, void* workspace, size_t ws_bytes,
@@ -115,6 +119,27 @@ bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int6
                         const int32_t* row_pos, const float* rope_table, int64_t max_pos, const int32_t* block_table,
                         int64_t max_blk, int64_t n_blocks, void* q_out, void* k_cache, void* v_cache, int Hq, int Hkv,
                         int hd, int mode, void* stream);
+
+// RMSNorm in front of a GEMM: the GEMM's A rows are y = RMSNorm(x (+ res_in)) *
+// gamma (the norm kernels' arithmetic) and res_out receives x + res_in.  A
+// decode-size call computes y inside the GEMM; otherwise the norm kernel runs
+// first and writes y.
+struct NormIn {
+  const void* x;       // [M, K] bf16
+  const void* res_in;  // [M, K] bf16 residual stream, or NULL (the norm of x alone)
+  void* res_out;       // [M, K] bf16 x + res_in, a buffer other than res_in; NULL iff res_in is
+  const void* gamma;   // [K] bf16
+  float eps;
+  void* y;             // [M, K] bf16 rows of the norm when it runs as its own kernel
+};
+// Dense GEMM (BI_EPI_NONE or BI_EPI_SWIGLU, bf16 out) of the normalised rows.
+bi_status gemm_norm(const NormIn& norm, int64_t M, int64_t K, const void* W, int64_t N, void* C, int epilogue,
+                    int mode, void* workspace, size_t ws_bytes, void* stream);
+// gemm_qkv_rope of the normalised rows.
+bi_status gemm_qkv_rope_norm(const NormIn& norm, int64_t M, int64_t K, const void* W, int64_t N,
+                             const int32_t* row_seq, const int32_t* row_pos, const float* rope_table, int64_t max_pos,
+                             const int32_t* block_table, int64_t max_blk, int64_t n_blocks, void* q_out,
+                             void* k_cache, void* v_cache, int Hq, int Hkv, int hd, int mode, void* stream);
 
 // TMA descriptor encode (driver entry point looked up through the runtime).
 bool encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

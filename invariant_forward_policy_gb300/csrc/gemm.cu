@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "norm.cuh"
 
 namespace bi {
 
@@ -78,6 +79,12 @@ struct GemmArgs {
   int a_box_rows;                     // rows of A one TMA copy brings in (128, or M rounded up to 8 when M < 128)
   int group_m;                        // M-tiles per rasterisation group
   RopeKvArgs rope;                    // EPI_ROPE only
+  // decode-size schedule with the RMSNorm folded in: A = norm(nx (+ nres_in)) * ngamma
+  const __nv_bfloat16* nx;
+  const __nv_bfloat16* nres_in;
+  __nv_bfloat16* nres_out;
+  const __nv_bfloat16* ngamma;
+  float neps;
 };
 
 // Online (max, sum-exp, argmax) over 4 consecutive logits, in column order.
@@ -573,7 +580,55 @@ constexpr int kRowsLoadWarps = 4;
 template <int TN>
 constexpr int rows_threads() { return (TN / 8 + kRowsLoadWarps) * 32; }
 
-template <int EPI, int TN>
+// The normalised A rows of a fused-norm call, into the padded shared rows sA:
+// warp w of nw takes rows w, w + nw, ... (< M), lane l the 16-byte vectors
+// l + 32 j (j < NJ) of a row.  K = 256 NJ, so each of the norm kernels' K/8
+// threads owns exactly one vector and their warps are the j's: the sum of
+// squares per vector, the xor butterfly per j and the j sums added in order
+// are the norm kernels' operations (norm.cuh).  With write_res, x + res_in
+// goes to res_out.  RB rows' loads are in flight together.
+template <int NJ>
+__device__ __forceinline__ void rows_norm(const GemmArgs& args, uint8_t* sA, int stride, int M, int w, int nw,
+                                          int lane, bool write_res) {
+  constexpr int RB = NJ >= 8 ? 1 : 2;
+  const int K = args.K;
+  const uint4* gam = reinterpret_cast<const uint4*>(args.ngamma);
+  for (int r0 = w; r0 < M; r0 += RB * nw) {
+    uint4 a[RB][NJ], h[RB][NJ];
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      const int r = r0 + b * nw;
+      if (r >= M) continue;
+      const uint4* xr = reinterpret_cast<const uint4*>(args.nx + (int64_t)r * K);
+      const uint4* hr = args.nres_in ? reinterpret_cast<const uint4*>(args.nres_in + (int64_t)r * K) : nullptr;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        a[b][j] = xr[lane + 32 * j];
+        if (args.nres_in) h[b][j] = hr[lane + 32 * j];
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      const int r = r0 + b * nw;
+      if (r >= M) continue;
+      float t = 0.f;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        if (args.nres_in) {
+          a[b][j] = norm_residual_add(a[b][j], h[b][j]);
+          if (write_res) reinterpret_cast<uint4*>(args.nres_out + (int64_t)r * K)[lane + 32 * j] = a[b][j];
+        }
+        t += norm_warp_sum(norm_ss_vec(a[b][j], 0.f));
+      }
+      const float inv = norm_inv(t, K, args.neps);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j)
+        *reinterpret_cast<uint4*>(sA + r * stride + (lane + 32 * j) * 16) = norm_apply(a[b][j], gam[lane + 32 * j], inv);
+    }
+  }
+}
+
+template <int EPI, int TN, int NJ = 0>
 __global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __nv_bfloat16* __restrict__ A,
                                                                        const __nv_bfloat16* __restrict__ W,
                                                                        const GemmArgs args) {
@@ -604,6 +659,7 @@ __global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __n
 
   constexpr int kMmaWarps = TN / 8, kLoaders = kRowsLoadWarps * 32;
   if (threadIdx.x == 0) {
+    // every loader arrives once per chunk when its copies have landed
     for (int c = 0; c < nch; ++c) mbar_init(&bar[c], kLoaders);
     fence_barrier_init();
   }
@@ -629,18 +685,28 @@ __global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __n
       }
     }
     pdl_wait();
-    for (int c = 0; c < nch; ++c) {
-      const bool on = lane * 8 < chunk_cols(c);
-      const int k = c * kRowsKC + lane * 8;
+    if constexpr (NJ == 0) {
+      for (int c = 0; c < nch; ++c) {
+        const bool on = lane * 8 < chunk_cols(c);
+        const int k = c * kRowsKC + lane * 8;
 #pragma unroll
-      for (int rr = 0; rr < kRowsM / kRowsLoadWarps; ++rr) {
-        const int r = lw + rr * kRowsLoadWarps;
-        if (on && r < M) cp_async16(sA + r * stride + k * 2, A + (int64_t)r * K + k, true);
+        for (int rr = 0; rr < kRowsM / kRowsLoadWarps; ++rr) {
+          const int r = lw + rr * kRowsLoadWarps;
+          if (on && r < M) cp_async16(sA + r * stride + k * 2, A + (int64_t)r * K + k, true);
+        }
+        cp_async_mbar_arrive(&bar[c]);
       }
-      cp_async_mbar_arrive(&bar[c]);
+    } else {
+      for (int c = 0; c < nch; ++c) cp_async_mbar_arrive(&bar[c]);  // the W copies only
     }
   } else {
     pdl_wait();  // the outputs below are written only after the preceding kernel is done
+  }
+  if constexpr (NJ != 0) {
+    // every warp normalises its share of the rows (whole rows: the MMA starts
+    // once all are written); CTA 0 also writes the new residual rows
+    rows_norm<NJ>(args, sA, stride, M, warp, blockDim.x >> 5, lane, tile == 0);
+    __syncthreads();
   }
 
   // MMA warps 0 .. TN/8-1 start on each chunk as soon as it has landed
@@ -865,20 +931,21 @@ struct GemmCall {
   const int32_t* ids = nullptr;  // fused log-softmax: targets (NULL = greedy)
   TileLse* lse = nullptr;        // fused log-softmax: tile partials (non-NULL selects it)
   const RopeKvArgs* rope = nullptr;  // fused RoPE + paged KV write (non-NULL selects it)
+  const NormIn* norm = nullptr;      // RMSNorm in front (A unused; non-NULL selects it)
 };
 
-template <int EPI, int TN>
+template <int EPI, int TN, int NJ = 0>
 static bi_status launch_rows(const void* A, const void* W, const GemmArgs& args, int n_tiles, size_t smem,
                              cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_rows_kernel<EPI, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(gemm_rows_kernel<EPI, TN, NJ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kRowsMaxSmem);
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("gemm rows smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(gemm_rows_kernel<EPI, TN>, dim3(n_tiles), dim3(rows_threads<TN>()), smem, st,
+  return launched(launch_pdl(gemm_rows_kernel<EPI, TN, NJ>, dim3(n_tiles), dim3(rows_threads<TN>()), smem, st,
                              static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(W), args),
                   "gemm_rows_kernel");
 }
@@ -904,8 +971,34 @@ static bool rows_path(const GemmCall& g, int64_t n_out, bool swiglu) {
   return rows_smem_bytes((int)g.K, rows_tile(g, swiglu)) <= kRowsMaxSmem;
 }
 
+// The RMSNorm folds into the decode-size schedule for the SwiGLU and fused-RoPE
+// (head_dim 64) epilogues when K is 512, 1024 or 2048 (norm_nj = K / 256).
+static int norm_nj(const GemmCall& g, bool swiglu) {
+  if (!(swiglu || (g.rope && g.rope->hd == 64))) return 0;
+  return (g.K == 512 || g.K == 1024 || g.K == 2048) ? (int)(g.K / 256) : 0;
+}
+
+template <int EPI, int TN>
+static bi_status launch_rows_nj(int nj, const GemmCall& g, const GemmArgs& args, int n_tiles, size_t smem,
+                                cudaStream_t st) {
+  switch (nj) {
+    case 2: return launch_rows<EPI, TN, 2>(g.A, g.W, args, n_tiles, smem, st);
+    case 4: return launch_rows<EPI, TN, 4>(g.A, g.W, args, n_tiles, smem, st);
+    case 8: return launch_rows<EPI, TN, 8>(g.A, g.W, args, n_tiles, smem, st);
+  }
+  return fail(BI_ERR_UNSUPPORTED_SHAPE, "gemm: norm width");
+}
+
 static bi_status run_rows(const GemmCall& g, int64_t n_out, bool swiglu, cudaStream_t st) {
   GemmArgs args = {};
+  const int nj = g.norm ? norm_nj(g, swiglu) : 0;
+  if (nj) {
+    args.nx = static_cast<const __nv_bfloat16*>(g.norm->x);
+    args.nres_in = static_cast<const __nv_bfloat16*>(g.norm->res_in);
+    args.nres_out = static_cast<__nv_bfloat16*>(g.norm->res_out);
+    args.ngamma = static_cast<const __nv_bfloat16*>(g.norm->gamma);
+    args.neps = g.norm->eps;
+  }
   args.C = g.C;
   args.status = device_status_ptr();
   args.M = (int)g.M;
@@ -917,11 +1010,15 @@ static bi_status run_rows(const GemmCall& g, int64_t n_out, bool swiglu, cudaStr
   if (g.rope) {
     args.rope = *g.rope;
     const int heads = (int)(g.n_rows_w / tn);
+    if (nj) return launch_rows_nj<EPI_ROPE, 64>(nj, g, args, heads, smem, st);
     return tn == 64 ? launch_rows<EPI_ROPE, 64>(g.A, g.W, args, heads, smem, st)
                     : launch_rows<EPI_ROPE, 128>(g.A, g.W, args, heads, smem, st);
   }
   const int n_tiles = (int)cdiv(n_out, 16);
-  if (swiglu) return launch_rows<EPI_SWIGLU, 32>(g.A, g.W, args, n_tiles, smem, st);
+  if (swiglu) {
+    if (nj) return launch_rows_nj<EPI_SWIGLU, 32>(nj, g, args, n_tiles, smem, st);
+    return launch_rows<EPI_SWIGLU, 32>(g.A, g.W, args, n_tiles, smem, st);
+  }
   return g.c_dtype == BI_DTYPE_FP32 ? launch_rows<EPI_F32, 16>(g.A, g.W, args, n_tiles, smem, st)
                                     : launch_rows<EPI_BF16, 16>(g.A, g.W, args, n_tiles, smem, st);
 }
@@ -933,6 +1030,16 @@ static size_t partial_bytes(int64_t M, int64_t n_rows_w, int splits) {
 static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   const bool swiglu = g.epilogue == BI_EPI_SWIGLU;
   const int64_t n_out = swiglu ? g.n_rows_w / 2 : g.n_rows_w;
+  if (g.norm) {
+    if (rows_path(g, n_out, swiglu) && norm_nj(g, swiglu)) return run_rows(g, n_out, swiglu, st);
+    // the norm as its own kernel, then the GEMM of its rows
+    const NormIn& n = *g.norm;
+    BI_TRY(rmsnorm_rows_to(n.x, n.res_in, n.res_out, n.gamma, n.y, g.M, g.K, n.eps, nullptr, st));
+    GemmCall plain = g;
+    plain.norm = nullptr;
+    plain.A = n.y;
+    return run_gemm(plain, st);
+  }
   if (rows_path(g, n_out, swiglu)) return run_rows(g, n_out, swiglu, st);
   int bn = tile_n_for(g.n_rows_w, g.K, swiglu, g.E), splits = 1;
   if (g.mode == BI_FAST && g.E == 1) {
@@ -1147,6 +1254,54 @@ bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int6
                 n_blocks, Hq, Hkv, hd};
   GemmCall g{A, M, K, W, N, 1, nullptr, q_out, BI_DTYPE_BF16, BI_EPI_NONE, mode, nullptr, 0};
   g.rope = &ra;
+  return run_gemm(g, as_stream(stream));
+}
+
+static bi_status check_norm(const NormIn& n, int64_t K) {
+  BI_REQUIRE(n.x && n.gamma && n.y, "null pointer");
+  BI_REQUIRE(!n.res_in == !n.res_out, "res_in and res_out go together");
+  BI_REQUIRE(!n.res_in || n.res_in != n.res_out, "res_out must be another buffer than res_in");
+  BI_REQUIRE(aligned16(n.x) && aligned16(n.gamma) && aligned16(n.y) &&
+                 (!n.res_in || (aligned16(n.res_in) && aligned16(n.res_out))),
+             "pointers must be 16-byte aligned");
+  BI_REQUIRE(n.eps > 0.f, "eps must be positive");
+  BI_REQUIRE_SHAPE(K <= 16384, "K must be at most 16384 for the norm");
+  return BI_OK;
+}
+
+bi_status gemm_norm(const NormIn& norm, int64_t M, int64_t K, const void* W, int64_t N, void* C, int epilogue,
+                    int mode, void* workspace, size_t ws_bytes, void* stream) {
+  BI_REQUIRE(M >= 0 && K > 0 && N > 0, "bad shape");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(W && C, "null pointer");
+  BI_REQUIRE(epilogue == BI_EPI_NONE || epilogue == BI_EPI_SWIGLU, "bad epilogue");
+  BI_REQUIRE_SHAPE(K % 64 == 0 && (epilogue != BI_EPI_SWIGLU || N % 2 == 0), "bad GEMM shape");
+  BI_REQUIRE(aligned16(W) && aligned16(C), "pointers must be 16-byte aligned");
+  BI_TRY(check_norm(norm, K));
+  GemmCall g{nullptr, M, K, W, N, 1, nullptr, C, BI_DTYPE_BF16, epilogue, mode, workspace, ws_bytes};
+  g.norm = &norm;
+  return run_gemm(g, as_stream(stream));
+}
+
+bi_status gemm_qkv_rope_norm(const NormIn& norm, int64_t M, int64_t K, const void* W, int64_t N,
+                             const int32_t* row_seq, const int32_t* row_pos, const float* rope_table, int64_t max_pos,
+                             const int32_t* block_table, int64_t max_blk, int64_t n_blocks, void* q_out,
+                             void* k_cache, void* v_cache, int Hq, int Hkv, int hd, int mode, void* stream) {
+  BI_REQUIRE(M >= 0 && K > 0 && N > 0, "bad shape");
+  if (M == 0) return BI_OK;
+  BI_REQUIRE(W && row_seq && row_pos && rope_table && block_table && q_out && k_cache && v_cache, "null pointer");
+  BI_REQUIRE(N == (int64_t)(Hq + 2 * Hkv) * hd, "N must be (Hq + 2 Hkv) * head_dim");
+  BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
+  BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
+  BI_REQUIRE(aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache),
+             "pointers must be 16-byte aligned");
+  BI_TRY(check_norm(norm, K));
+  RopeKvArgs ra{row_seq, row_pos, rope_table, block_table, static_cast<__nv_bfloat16*>(q_out),
+                static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), max_pos, max_blk,
+                n_blocks, Hq, Hkv, hd};
+  GemmCall g{nullptr, M, K, W, N, 1, nullptr, q_out, BI_DTYPE_BF16, BI_EPI_NONE, mode, nullptr, 0};
+  g.rope = &ra;
+  g.norm = &norm;
   return run_gemm(g, as_stream(stream));
 }
 

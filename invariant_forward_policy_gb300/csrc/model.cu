@@ -112,9 +112,13 @@ __global__ void decode_embed_kernel(const int32_t* __restrict__ tokens, const in
 }
 
 // ------------------------------------------------------------- workspace plan
+// Passes of at most this many rows (decode steps) fold each RMSNorm into the
+// GEMM after it (gemm_norm, gemm_qkv_rope_norm), which writes the new residual
+// rows to the other of two buffers; longer passes run the norm kernel in place.
+constexpr int64_t kFoldRows = 16;
 struct FwdLayout {
   size_t piece_seq, piece_row0, piece_pos0, ids, logit_src, logit_dst, logit_tgt, row_seq, row_pos;
-  size_t h, x, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
+  size_t h, h2, x, q, ao, tmp, act, attn_ws, xsel, logits, gemm_ws;
   size_t attn_ws_bytes, gemm_ws_bytes, lp_ws_bytes;
   // fp8 only: bf16 qkv and gate/up outputs, activation codes and scales
   size_t qkv, g13, qa, sa;
@@ -141,6 +145,8 @@ static FwdLayout plan_layout(const bi_model_config& c, int64_t Tm, int64_t Pm, i
   L.row_seq = take(Tm * 4);
   L.row_pos = take(Tm * 4);
   L.h = take(Tm * c.d * 2);
+  // passes of at most kFoldRows rows alternate the residual stream between h and h2
+  L.h2 = take(std::min<int64_t>(Tm, kFoldRows) * c.d * 2);
   L.x = take(Tm * c.d * 2);
 
   L.q = take(Tm * hq * 2);
@@ -294,10 +300,17 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
 
   if (!ps.embedded) BI_TRY(bi_embed(at<int32_t>(ws, L.ids), T, m->embed, c.vocab, c.d, h, stream));
   BI_TRY(dump_copy(0, h));
+  // bf16 passes of at most kFoldRows rows (decode steps) fold each norm into
+  // the next GEMM; the residual stream then alternates between h and h2 (res
+  // is the current one), every row keeping the norm kernel's arithmetic
+  const bool fold = !c.fp8 && !dumping && T <= kFoldRows;
+  void* res = h;
+  void* h2 = at<void>(ws, L.h2);
+  auto other = [&](void* r) { return r == h ? h2 : h; };
   if (c.fp8)
     BI_TRY(rmsnorm_fp8_rows(h, nullptr, m->layers[0].attn_norm, nullptr, at<uint8_t>(ws, L.qa), at<float>(ws, L.sa),
                             T, c.d, c.eps, stream));
-  else
+  else if (!fold)
     BI_TRY(bi_rmsnorm(h, nullptr, m->layers[0].attn_norm, x, T, c.d, c.eps, mode, stream));
   for (int64_t li = 0; li < c.n_layers; ++li) {
     const bi_layer_weights& lw = m->layers[li];
@@ -333,18 +346,34 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
       continue;
     }
     // QKV projection with RoPE and the paged K/V write fused into its epilogue
-    BI_TRY(gemm_qkv_rope(x, T, c.d, lw.wqkv, nqkv, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos),
-                         m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd, mode,
-                         stream));
+    if (fold) {
+      // the layer's input norm: of the embeddings (layer 0), else of the last down projection + residual
+      const NormIn n = li == 0 ? NormIn{h, nullptr, nullptr, lw.attn_norm, c.eps, x}
+                               : NormIn{tmp, res, other(res), lw.attn_norm, c.eps, x};
+      if (li > 0) res = other(res);
+      BI_TRY(gemm_qkv_rope_norm(n, T, c.d, lw.wqkv, nqkv, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos),
+                                m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd,
+                                mode, stream));
+    } else {
+      BI_TRY(gemm_qkv_rope(x, T, c.d, lw.wqkv, nqkv, at<int32_t>(ws, L.row_seq), at<int32_t>(ws, L.row_pos),
+                           m->rope_table, c.max_pos, block_table, max_blk, n_blocks, q, kc, vc, Hq, Hkv, hd, mode,
+                           stream));
+    }
     BI_TRY(bi_attention(q, T, piece_seq, piece_row0, piece_pos0, ps.pieces, ps.max_q_len, Hq, Hkv, hd, kc, vc,
                         block_table, max_blk, n_blocks, ps.max_ctx, (int)c.kv_split, scale, at<void>(ws, L.attn_ws),
                         L.attn_ws_bytes, ao, mode, stream));
     BI_TRY(bi_gemm(ao, T, hq, lw.wo, c.d, tmp, BI_DTYPE_BF16, BI_EPI_NONE, mode, gws, L.gemm_ws_bytes, stream));
-    BI_TRY(bi_rmsnorm(tmp, h, lw.ffn_norm, x, T, c.d, c.eps, mode, stream));
-    BI_TRY(bi_gemm(x, T, c.d, lw.w13, 2 * c.ffn, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, mode, gws, L.gemm_ws_bytes,
-                   stream));
+    if (fold) {
+      const NormIn n{tmp, res, other(res), lw.ffn_norm, c.eps, x};
+      res = other(res);
+      BI_TRY(gemm_norm(n, T, c.d, lw.w13, 2 * c.ffn, act, BI_EPI_SWIGLU, mode, gws, L.gemm_ws_bytes, stream));
+    } else {
+      BI_TRY(bi_rmsnorm(tmp, h, lw.ffn_norm, x, T, c.d, c.eps, mode, stream));
+      BI_TRY(bi_gemm(x, T, c.d, lw.w13, 2 * c.ffn, act, BI_DTYPE_BF16, BI_EPI_SWIGLU, mode, gws, L.gemm_ws_bytes,
+                     stream));
+    }
     BI_TRY(bi_gemm(act, T, c.ffn, lw.w2, c.d, tmp, BI_DTYPE_BF16, BI_EPI_NONE, mode, gws, L.gemm_ws_bytes, stream));
-    if (li + 1 < c.n_layers) {
+    if (li + 1 < c.n_layers && !fold) {
       BI_TRY(bi_rmsnorm(tmp, h, m->layers[li + 1].attn_norm, x, T, c.d, c.eps, mode, stream));
       BI_TRY(dump_copy(li + 1, h));
     }
@@ -362,7 +391,7 @@ static bi_status run_pass(bi_model* m, void* ws, const FwdLayout& L, const PassS
     const int32_t* src = at<int32_t>(ws, L.logit_src) + r0;
     void* xsel = at<void>(ws, L.xsel);
     // rows src[j] of (down-proj out + residual) -> final norm -> compact row j
-    BI_TRY(rmsnorm_rows(tmp, h, m->final_norm, xsel, R, c.d, c.eps, src, stream));
+    BI_TRY(rmsnorm_rows(tmp, res, m->final_norm, xsel, R, c.d, c.eps, src, stream));
     // lm_head + log-softmax + gather fused; results land at the call's row index
     const int32_t* tgt = greedy ? nullptr : at<int32_t>(ws, L.logit_tgt) + r0;
     BI_TRY(lm_head_logprob_to(xsel, R, c.d, m->lm_head, c.vocab, tgt, logprob_out, sampled_out,

@@ -13,13 +13,15 @@ namespace bi {
 // Threads per row: norm_threads(d) (norm.cuh); a thread walks its vectors with
 // stride 8*blockDim, so the per-thread order depends on d only.
 
-// Row r of y is the norm of row src(r) of x (+ residual), src(r) = idx ? idx[r] : r.
+// Row r of y is the norm of row src(r) of x (+ residual), src(r) = idx ? idx[r] : r;
+// x + residual goes to res_out (the residual rows themselves, or another buffer).
 // kFp8: the bf16 output row is also quantised in 1 x 128 blocks into codes q and
 // scales qs (the 16 threads holding a block's 16 vectors reduce its amax); y may
 // then be null.
 template <bool kResidual, bool kFp8>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                      __nv_bfloat16* __restrict__ residual,
+                                                      const __nv_bfloat16* residual,
+                                                      __nv_bfloat16* res_out,
                                                       const __nv_bfloat16* __restrict__ gamma,
                                                       __nv_bfloat16* __restrict__ y, int d, float eps,
                                                       const int32_t* __restrict__ idx, uint8_t* __restrict__ q,
@@ -35,7 +37,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   uint4 sv[kMaxVec];
   float ss = 0.f;
   const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
-  uint4* rr = reinterpret_cast<uint4*>(residual + src * d);
+  const uint4* rr = reinterpret_cast<const uint4*>(residual + src * d);
+  uint4* ro = reinterpret_cast<uint4*>(res_out + src * d);
 #pragma unroll
   for (int i = 0; i < kMaxVec; ++i) {
     const int v = tid + i * nthr;
@@ -43,7 +46,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
       uint4 a = xr[v];
       if (kResidual) {
         a = norm_residual_add(a, rr[v]);
-        rr[v] = a;
+        ro[v] = a;
       }
       sv[i] = a;
       ss = norm_ss_vec(a, ss);
@@ -88,24 +91,31 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
 
 bi_status rmsnorm_rows(const void* x, void* residual, const void* gamma, void* y, int64_t rows, int64_t d, float eps,
                        const int32_t* idx, void* stream) {
+  return rmsnorm_rows_to(x, residual, residual, gamma, y, rows, d, eps, idx, stream);
+}
+
+bi_status rmsnorm_rows_to(const void* x, const void* residual, void* res_out, const void* gamma, void* y, int64_t rows,
+                          int64_t d, float eps, const int32_t* idx, void* stream) {
   BI_REQUIRE(rows >= 0, "rows < 0");
   if (rows == 0) return BI_OK;
   BI_REQUIRE(x && gamma && y, "null pointer");
   BI_REQUIRE(d >= 8 && d <= 16384 && d % 8 == 0, "d must be a multiple of 8 in [8, 16384]");
-  BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y) && (!residual || aligned16(residual)),
+  BI_REQUIRE(!residual == !res_out, "residual and res_out go together");
+  BI_REQUIRE(aligned16(x) && aligned16(gamma) && aligned16(y) && (!residual || (aligned16(residual) && aligned16(res_out))),
              "pointers must be 16-byte aligned");
   BI_REQUIRE(rows <= 0x7fffffff, "rows too large");
   const int thr = norm_threads(d);
   auto* xp = static_cast<const __nv_bfloat16*>(x);
-  auto* rp = static_cast<__nv_bfloat16*>(residual);
+  auto* rp = static_cast<const __nv_bfloat16*>(residual);
+  auto* op = static_cast<__nv_bfloat16*>(res_out);
   auto* gp = static_cast<const __nv_bfloat16*>(gamma);
   auto* yp = static_cast<__nv_bfloat16*>(y);
   cudaError_t e;
   if (residual)
-    e = launch_pdl(rmsnorm_kernel<true, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp,
+    e = launch_pdl(rmsnorm_kernel<true, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, op, gp,
                    yp, (int)d, eps, idx, nullptr, nullptr);
   else
-    e = launch_pdl(rmsnorm_kernel<false, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp,
+    e = launch_pdl(rmsnorm_kernel<false, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, op, gp,
                    yp, (int)d, eps, idx, nullptr, nullptr);
   return launched(e, "rmsnorm_kernel");
 }
@@ -128,10 +138,10 @@ bi_status rmsnorm_fp8_rows(const void* x, void* residual, const void* gamma, voi
   auto* qp = static_cast<uint8_t*>(q);
   cudaError_t e;
   if (residual)
-    e = launch_pdl(rmsnorm_kernel<true, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp, yp,
-                   (int)d, eps, nullptr, qp, qs);
+    e = launch_pdl(rmsnorm_kernel<true, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, rp, gp,
+                   yp, (int)d, eps, nullptr, qp, qs);
   else
-    e = launch_pdl(rmsnorm_kernel<false, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, gp,
+    e = launch_pdl(rmsnorm_kernel<false, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, rp, gp,
                    yp, (int)d, eps, nullptr, qp, qs);
   return launched(e, "rmsnorm_fp8_kernel");
 }
