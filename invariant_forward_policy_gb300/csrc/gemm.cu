@@ -957,13 +957,13 @@ static int rows_tile(const GemmCall& g, bool swiglu) {
   return swiglu ? 32 : 16;
 }
 
-// The decode-size schedule takes invariant dense calls of at most 16 rows of a
-// weight under 4M elements (a decoder layer's projections; larger weights,
-// such as a vocabulary head, stream faster through the tcgen05 kernel's TMA
-// ring) whose W slice and rows fit shared memory; BI_FAST keeps its
-// M-dependent plan, and the fused log-softmax stays on the tcgen05 kernel.
+// The decode-size schedule takes dense calls of at most 16 rows of a weight
+// under 4M elements (a decoder layer's projections; larger weights, such as a
+// vocabulary head, stream faster through the tcgen05 kernel's TMA ring) whose
+// W slice and rows fit shared memory, in either mode (BI_FAST has nothing
+// faster for them); the fused log-softmax stays on the tcgen05 kernel.
 static bool rows_path(const GemmCall& g, int64_t n_out, bool swiglu) {
-  if (g.mode != BI_INVARIANT || g.M < 1 || g.M > kRowsM || g.E != 1 || g.tile_expert || g.lse) return false;
+  if (g.M < 1 || g.M > kRowsM || g.E != 1 || g.tile_expert || g.lse) return false;
   if (g.n_rows_w * g.K >= (int64_t(1) << 22)) return false;
   if (g.K % 64 || g.K > kRowsMaxK || n_out % 8) return false;
   if ((reinterpret_cast<uintptr_t>(g.A) | reinterpret_cast<uintptr_t>(g.W)) & 15) return false;

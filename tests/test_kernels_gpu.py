@@ -138,8 +138,10 @@ def test_gemm_swiglu_rows_invariant_to_M_and_order(F, K):
 
 
 def test_gemm_fast_mode_is_close_but_split():
+    """BI_FAST splits K for 17..128 rows (its M-dependent plan; at most 16 rows it
+    takes the decode-size schedule like the invariant mode): close to the oracle."""
     rng = np.random.default_rng(9)
-    M, N, K = 16, 1536, 512
+    M, N, K = 48, 1536, 512
     ab, af = rng_bf16(rng, (M, K))
     wb, wf = rng_bf16(rng, (N, K), 0.05)
     ws = torch.empty(bi.bi_gemm_workspace_size(M, N, K, 0, bi.BI_FAST), dtype=torch.uint8, device="cuda")
