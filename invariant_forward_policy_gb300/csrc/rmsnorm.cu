@@ -18,10 +18,11 @@ namespace bi {
 // kFp8: the bf16 output row is also quantised in 1 x 128 blocks into codes q and
 // scales qs (the 16 threads holding a block's 16 vectors reduce its amax); y may
 // then be null.
-template <bool kResidual, bool kFp8>
+// kOut: res_out is a buffer of its own; otherwise the sum goes back to the residual rows.
+template <bool kResidual, bool kFp8, bool kOut = false>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                      const __nv_bfloat16* residual,
-                                                      __nv_bfloat16* res_out,
+                                                      __nv_bfloat16* __restrict__ residual,
+                                                      __nv_bfloat16* __restrict__ res_out,
                                                       const __nv_bfloat16* __restrict__ gamma,
                                                       __nv_bfloat16* __restrict__ y, int d, float eps,
                                                       const int32_t* __restrict__ idx, uint8_t* __restrict__ q,
@@ -37,8 +38,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const __nv_bfloat16* __res
   uint4 sv[kMaxVec];
   float ss = 0.f;
   const uint4* xr = reinterpret_cast<const uint4*>(x + src * d);
-  const uint4* rr = reinterpret_cast<const uint4*>(residual + src * d);
-  uint4* ro = reinterpret_cast<uint4*>(res_out + src * d);
+  uint4* rr = reinterpret_cast<uint4*>(residual + src * d);
+  uint4* ro = kOut ? reinterpret_cast<uint4*>(res_out + src * d) : rr;
 #pragma unroll
   for (int i = 0; i < kMaxVec; ++i) {
     const int v = tid + i * nthr;
@@ -106,17 +107,20 @@ bi_status rmsnorm_rows_to(const void* x, const void* residual, void* res_out, co
   BI_REQUIRE(rows <= 0x7fffffff, "rows too large");
   const int thr = norm_threads(d);
   auto* xp = static_cast<const __nv_bfloat16*>(x);
-  auto* rp = static_cast<const __nv_bfloat16*>(residual);
+  auto* rp = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(residual));  // written only in place
   auto* op = static_cast<__nv_bfloat16*>(res_out);
   auto* gp = static_cast<const __nv_bfloat16*>(gamma);
   auto* yp = static_cast<__nv_bfloat16*>(y);
   cudaError_t e;
-  if (residual)
-    e = launch_pdl(rmsnorm_kernel<true, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, op, gp,
-                   yp, (int)d, eps, idx, nullptr, nullptr);
+  if (residual && res_out != residual)
+    e = launch_pdl(rmsnorm_kernel<true, false, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp,
+                   op, gp, yp, (int)d, eps, idx, nullptr, nullptr);
+  else if (residual)
+    e = launch_pdl(rmsnorm_kernel<true, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp,
+                   static_cast<__nv_bfloat16*>(nullptr), gp, yp, (int)d, eps, idx, nullptr, nullptr);
   else
-    e = launch_pdl(rmsnorm_kernel<false, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, op, gp,
-                   yp, (int)d, eps, idx, nullptr, nullptr);
+    e = launch_pdl(rmsnorm_kernel<false, false>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp,
+                   static_cast<__nv_bfloat16*>(nullptr), gp, yp, (int)d, eps, idx, nullptr, nullptr);
   return launched(e, "rmsnorm_kernel");
 }
 
@@ -138,11 +142,11 @@ bi_status rmsnorm_fp8_rows(const void* x, void* residual, const void* gamma, voi
   auto* qp = static_cast<uint8_t*>(q);
   cudaError_t e;
   if (residual)
-    e = launch_pdl(rmsnorm_kernel<true, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, rp, gp,
-                   yp, (int)d, eps, nullptr, qp, qs);
+    e = launch_pdl(rmsnorm_kernel<true, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp,
+                   static_cast<__nv_bfloat16*>(nullptr), gp, yp, (int)d, eps, nullptr, qp, qs);
   else
-    e = launch_pdl(rmsnorm_kernel<false, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp, rp, gp,
-                   yp, (int)d, eps, nullptr, qp, qs);
+    e = launch_pdl(rmsnorm_kernel<false, true>, dim3((unsigned)rows), dim3(thr), 0, as_stream(stream), xp, rp,
+                   static_cast<__nv_bfloat16*>(nullptr), gp, yp, (int)d, eps, nullptr, qp, qs);
   return launched(e, "rmsnorm_fp8_kernel");
 }
 
