@@ -702,12 +702,11 @@ struct TcAttnLayout {
   static constexpr int kP = 128 * kKeys * 2;        // one P tile, 128 rows x 64 keys
   static constexpr int kOffKV = kQ;
   static constexpr int kOffP = kOffKV + kStages * 2 * kPage;
-  static constexpr int kOffX = kOffP + 2 * kP;      // max and sum exchange, [4 quads][128 rows] each
-  static constexpr int kOffBar = kOffX + 2 * 4 * 128 * 4;
+  static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kBytes = kOffBar + 256 + 1024;   // + barriers, + alignment slack
   static constexpr uint32_t kCols = HD == 128 ? 512 : 256;  // S0, S1 (64 each), O, R (HD each)
   static constexpr uint32_t kColS = 0, kColO = 128, kColR = 128 + HD;
-  static constexpr int kSoftmaxWarps = 16;
+  static constexpr int kSoftmaxWarps = 8;
   static constexpr int kThreads = 32 * kSoftmaxWarps + 64;  // + TMA warp, MMA warp
 };
 
@@ -718,8 +717,6 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
   using Lay = TcAttnLayout<HD>;
   constexpr int NS = Lay::kStages;
   constexpr int KB = HD / 64;        // 64-dim boxes per row
-  constexpr int OQ = HD / 4;         // O columns per thread
-  constexpr int CW = 16;             // TMEM columns per load or store in the O and R passes
   constexpr int kSM = Lay::kSoftmaxWarps * 32;
   constexpr int kWarpTma = Lay::kSoftmaxWarps, kWarpMma = Lay::kSoftmaxWarps + 1;
   extern __shared__ uint8_t smem_raw[];
@@ -727,8 +724,6 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sKV = smem + Lay::kOffKV;  // stage st: K page at st * 2 * kPage, V page after it
   uint8_t* sP = smem + Lay::kOffP;
-  float* xmax = reinterpret_cast<float*>(smem + Lay::kOffX);  // [4][128]
-  float* xsum = xmax + 4 * 128;                                // [4][128]
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + Lay::kOffBar);
   uint64_t* kv_empty = kv_full + NS;
   uint64_t* s_full = kv_empty + NS;   // [2] MMA -> softmax: S of a tile is in TMEM
@@ -736,8 +731,7 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
   uint64_t* p_full = s_empty + 2;     // [2] softmax -> MMA: P written, O rescaled (16 warp arrivals)
   uint64_t* o_done = p_full + 2;      // MMA -> softmax: P V of a tile has completed
   uint64_t* q_full = o_done + 1;      // softmax -> MMA: Q tile loaded (kSM thread arrivals)
-  uint64_t* xbar = q_full + 1;        // [4 lane quarters][2]: the four warps of a quarter met (max, sum)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -756,7 +750,6 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
     }
     mbar_init(o_done, 1);
     mbar_init(q_full, kSM);
-    for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -877,69 +870,95 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       }
     }
   } else if (n_tiles > 0 && warp < Lay::kSoftmaxWarps) {
-    // ---------------- softmax warps: row r = TMEM lane; quad group qd of its keys, quarter qd of O
-    const int qw = warp & 3, qd = warp >> 2;
-    const int r = qw * 32 + lane;
-    const int ti = tok0 + r / a.group;
-    const bool row_valid = ti < n_tok;
-    const int row_tok = row0 + ti, row_pos = pos_first + ti, row_head = kvh * a.group + (r % a.group);
-    uint64_t* xb = xbar + 2 * qw;  // where the four warps that share these rows meet
-    // a quarter of the Q row into the swizzled tile (zeros for rows past the piece)
-    {
-      const __nv_bfloat16* qr = a.q + ((int64_t)row_tok * a.Hq + row_head) * HD;
+    // ---------------- softmax warps.  Warp w holds the 16 rows rb .. rb + 15, rb =
+    // 32 (w % 4) + 16 (w / 4) (TMEM lanes; a warp reads only its lane quarter), in the
+    // mma.sync accumulator layout that the 16x256b TMEM shape gives: thread (g, qd) =
+    // (lane / 4, lane % 4) holds rows rb + g and rb + g + 8 and, of every 8-column group
+    // of S, O and R, the columns 2 qd + {0, 1}.  So a row's keys 8j + 2qd + {0, 1} are this
+    // thread's, the quad's four threads are the row, and the row max and sum are quad
+    // shuffles, exactly as in the mma.sync schedules.
+    const int g = lane >> 2, qd = lane & 3;
+    const int rb = 32 * (warp & 3) + 16 * (warp >> 2);
+    int r[2], row_tok[2], row_pos[2], row_head[2];
+    bool row_valid[2];
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        const int ch = qd * (HD / 32) + c;
-        uint8_t* dst = sQ + (ch >> 3) * (128 * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        cp_async16(dst, row_valid ? qr + ch * 8 : a.q, row_valid);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async();
-      mbar_arrive(q_full);
+    for (int h = 0; h < 2; ++h) {
+      r[h] = rb + g + 8 * h;
+      const int ti = tok0 + r[h] / a.group;
+      row_valid[h] = ti < n_tok;
+      row_tok[h] = row0 + ti;
+      row_pos[h] = pos_first + ti;
+      row_head[h] = kvh * a.group + (r[h] % a.group);
     }
-    const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
-    const uint32_t tO = trow + Lay::kColO + qd * OQ, tR = trow + Lay::kColR + qd * OQ;
+    // the Q tile into the swizzled layout (zeros for rows past the piece), 16-byte
+    // chunks spread over the softmax threads
+    for (int i = tid; i < 128 * (HD / 8); i += kSM) {
+      const int qrow = i / (HD / 8), ch = i % (HD / 8);
+      const int ti = tok0 + qrow / a.group;
+      const bool valid = ti < n_tok;
+      const __nv_bfloat16* src =
+          a.q + ((int64_t)(row0 + ti) * a.Hq + kvh * a.group + (qrow % a.group)) * HD + ch * 8;
+      uint8_t* dst = sQ + (ch >> 3) * (128 * 128) + qrow * 128 + (((ch & 7) ^ (qrow & 7)) << 4);
+      cp_async16(dst, valid ? src : a.q, valid);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async();
+    mbar_arrive(q_full);
+
+    const uint32_t tblk = tmem + ((uint32_t)rb << 16);
+    const uint32_t tS = tblk + Lay::kColS, tO = tblk + Lay::kColO, tR = tblk + Lay::kColR;
+    // register i of a 16-register O or R group at column c0 is row (i >> 1) & 1, column
+    // c0 + 8 (i >> 2) + 2 qd + (i & 1)
     auto zero_o = [&]() {
-      uint32_t z[CW];
+      uint32_t z[16];
 #pragma unroll
-      for (int i = 0; i < CW; ++i) z[i] = 0u;
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-      for (int c = 0; c < OQ; c += CW) tmem_st_cols<CW>(tO + c, z);
+      for (int c = 0; c < HD; c += 32) tmem_st_16x256b_x4(tO + c, z);
       tmem_st_wait();
     };
-    float m = -INFINITY, l = 0.f, Rm = -INFINITY, Rl = 0.f;
-    // R <- lane_merge(R, (m, l, O)) on this thread's quarter of the columns:
-    // P.acc = P.acc a + acc b, or a copy into an empty R
-    auto fold_lane = [&](const float m, const float l) {
-      const bool has = m != -INFINITY;
-      const bool copy = has && Rm == -INFINITY;
-      const float M = fmaxf(Rm, m);
-      const float fa = (Rm == M) ? 1.0f : exp2f(__fsub_rn(Rm, M));
-      const float fb = (m == M) ? 1.0f : exp2f(__fsub_rn(m, M));
-      if (__any_sync(0xffffffffu, has)) {
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float Rm[2] = {-INFINITY, -INFINITY}, Rl[2] = {0.f, 0.f};
+    // R <- lane_merge(R, (m, l, O)) per row: R a + O b, or a copy into an empty R
+    auto fold_lane = [&](const float (&mq)[2], const float (&lq)[2]) {
+      bool has[2], copy[2];
+      float M[2], fa[2], fb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        has[h] = mq[h] != -INFINITY;
+        copy[h] = has[h] && Rm[h] == -INFINITY;
+        M[h] = fmaxf(Rm[h], mq[h]);
+        fa[h] = (Rm[h] == M[h]) ? 1.0f : exp2f(__fsub_rn(Rm[h], M[h]));
+        fb[h] = (mq[h] == M[h]) ? 1.0f : exp2f(__fsub_rn(mq[h], M[h]));
+      }
+      if (__any_sync(0xffffffffu, has[0] || has[1])) {
 #pragma unroll 1
-        for (int c = 0; c < OQ; c += CW) {
-          uint32_t rr[CW], oo[CW];
-          tmem_ld_cols_attn<CW>(tR + c, rr);
-          tmem_ld_cols_attn<CW>(tO + c, oo);
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t rr[16], oo[16];
+          tmem_ld_16x256b_x4(tR + c, rr);
+          tmem_ld_16x256b_x4(tO + c, oo);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < CW; ++i) {
+          for (int i = 0; i < 16; ++i) {
+            const int h = (i >> 1) & 1;
             const float rv = __uint_as_float(rr[i]), ov = __uint_as_float(oo[i]);
-            const float nv = copy ? ov : (has ? __fadd_rn(__fmul_rn(rv, fa), __fmul_rn(ov, fb)) : rv);
+            const float nv = copy[h] ? ov : (has[h] ? __fadd_rn(__fmul_rn(rv, fa[h]), __fmul_rn(ov, fb[h])) : rv);
             rr[i] = __float_as_uint(nv);
           }
-          tmem_st_cols<CW>(tR + c, rr);
+          tmem_st_16x256b_x4(tR + c, rr);
         }
         tmem_st_wait();
       }
-      if (copy) {
-        Rm = m;
-        Rl = l;
-      } else if (has) {
-        Rl = __fadd_rn(__fmul_rn(Rl, fa), __fmul_rn(l, fb));
-        Rm = M;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (copy[h]) {
+          Rm[h] = mq[h];
+          Rl[h] = lq[h];
+        } else if (has[h]) {
+          Rl[h] = __fadd_rn(__fmul_rn(Rl[h], fa[h]), __fmul_rn(lq[h], fb[h]));
+          Rm[h] = M[h];
+        }
       }
     };
     // every decision that gates a warp-collective tcgen05.ld / st is taken for the
@@ -948,29 +967,35 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       const bool got = mbar_wait(bar, parity) && !*abort_flag;
       return __all_sync(0xffffffffu, got);
     };
+    // the rows' partials (m, l, acc) of split s from R; every lane loads, rows that
+    // have no key in the split store nothing
+    auto write_partial = [&](int s) {
+      bool store[2];
+      int64_t pidx[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        store[h] = row_valid[h] && row_pos[h] >= s * a.split;
+        pidx[h] = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
+      }
+#pragma unroll 1
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t rr[16];
+        tmem_ld_16x256b_x4(tR + c, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            if (store[h])
+              *reinterpret_cast<float2*>(a.part_o + pidx[h] * HD + c + 8 * k + 2 * qd) =
+                  make_float2(__uint_as_float(rr[4 * k + 2 * h]), __uint_as_float(rr[4 * k + 2 * h + 1]));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if (store[h] && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx[h] * 2) = make_float2(Rm[h], Rl[h]);
+    };
     zero_o();
     bool ok = true;
-    // v[2j + e] is the score of key 8j + 2qd + e of the tile
-    // this row's partial (m, l, acc) of split s from R; every lane loads, rows
-    // that have no key in the split store nothing
-    auto write_partial = [&](int s) {
-      const bool store = row_valid && row_pos >= s * a.split;
-      const int64_t pidx = ((int64_t)row_tok * a.Hq + row_head) * a.nsplit + s;
-      float* po = a.part_o + pidx * HD + qd * OQ;
-#pragma unroll 1
-      for (int c = 0; c < OQ; c += CW) {
-        uint32_t rr[CW];
-        tmem_ld_cols_attn<CW>(tR + c, rr);
-        tmem_ld_wait();
-        if (store) {
-#pragma unroll
-          for (int i = 0; i < CW; i += 4)
-            *reinterpret_cast<float4*>(po + c + i) = make_float4(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1]),
-                                                               __uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3]));
-        }
-      }
-      if (store && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx * 2) = make_float2(Rm, Rl);
-    };
     for (int t = 0; t < n_tiles; ++t) {
       const int key0 = tile_key0(t);
       const int tt = t % ntf;                                  // tile within its split
@@ -981,17 +1006,22 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      float v[16];
+      // v[h][2j + e] is the score of key 8j + 2qd + e of the tile for row h
+      float v[2][16];
       {
-        uint32_t g[8][2];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) tmem_ld_32x32b_x2(trow + Lay::kColS + (t & 1) * kKeys + 8 * j + 2 * qd, g[j]);
+        uint32_t sa[16], sb[16];
+        tmem_ld_16x256b_x4(tS + (t & 1) * kKeys, sa);
+        tmem_ld_16x256b_x4(tS + (t & 1) * kKeys + 32, sb);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[2 * j] = __uint_as_float(g[j][0]);
-          v[2 * j + 1] = __uint_as_float(g[j][1]);
-        }
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              v[h][2 * j + e] = __uint_as_float(sa[4 * j + 2 * h + e]);
+              v[h][8 + 2 * j + e] = __uint_as_float(sb[4 * j + 2 * h + e]);
+            }
       }
       tc_fence_before();
       __syncwarp();
@@ -999,65 +1029,57 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       // a new lane starts from a fresh state; the finished one is folded into R
       // once its last P V has landed (below), so this tile's softmax runs while
       // the tensor core finishes the previous tile
-      const float m_done = m, l_done = l;
+      const float m_done[2] = {m[0], m[1]}, l_done[2] = {l[0], l[1]};
       if (lane_start) {
-        m = -INFINITY;
-        l = 0.f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
       }
-      // scale and mask (a tile wholly at or before the row's position needs no
-      // mask), the tile max over the four quads (the max of a set does not depend
-      // on the order it is taken in)
-      const bool open = row_valid && key0 + kKeys - 1 <= row_pos;
-      if (open) {
+      float alpha[2];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = __fmul_rn(v[c], a.scale_log2);
-      } else {
+      for (int h = 0; h < 2; ++h) {
+        // scale and mask (a tile wholly at or before the row's position needs no
+        // mask), the tile max over the quad (the max of a set does not depend on
+        // the order it is taken in)
+        const bool open = row_valid[h] && key0 + kKeys - 1 <= row_pos[h];
+        if (open) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int key = key0 + 8 * (c >> 1) + 2 * qd + (c & 1);
-          v[c] = (row_valid && key <= row_pos) ? __fmul_rn(v[c], a.scale_log2) : -INFINITY;
+          for (int c = 0; c < 16; ++c) v[h][c] = __fmul_rn(v[h][c], a.scale_log2);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int key = key0 + 8 * (c >> 1) + 2 * qd + (c & 1);
+            v[h][c] = (row_valid[h] && key <= row_pos[h]) ? __fmul_rn(v[h][c], a.scale_log2) : -INFINITY;
+          }
         }
-      }
-      float mx[4] = {v[0], v[1], v[2], v[3]};
+        float mx = v[h][0];
 #pragma unroll
-      for (int c = 4; c < 16; ++c) mx[c & 3] = fmaxf(mx[c & 3], v[c]);
-      xmax[qd * 128 + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xb[0]);
-      if (!warp_wait(&xb[0], t & 1)) {
-        ok = false;
-        break;
-      }
-      const float tmax = fmaxf(fmaxf(xmax[r], xmax[128 + r]), fmaxf(xmax[256 + r], xmax[384 + r]));
-      const float m_new = fmaxf(m, tmax);
-      const float alpha = (m_new == m) ? 1.0f : exp2f(__fsub_rn(m, m_new));
-      // P and this thread's quad sum s_qd over its keys in order (a score of an
-      // open tile is never -inf, so the select is the identity there)
-      float sq = 0.f;
-      if (open) {
+        for (int c = 1; c < 16; ++c) mx = fmaxf(mx, v[h][c]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m[h], mx);
+        alpha[h] = (m_new == m[h]) ? 1.0f : exp2f(__fsub_rn(m[h], m_new));
+        // P and this thread's quad sum s_qd over its keys in order (a score of an
+        // open tile is never -inf, so the select is the identity there); the row
+        // sum is (s0 + s1) + (s2 + s3)
+        float sq = 0.f;
+        if (open) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          v[c] = exp2_p(__fsub_rn(v[c], m_new));
-          sq = __fadd_rn(sq, v[c]);
+          for (int c = 0; c < 16; ++c) {
+            v[h][c] = exp2_p(__fsub_rn(v[h][c], m_new));
+            sq = __fadd_rn(sq, v[h][c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            v[h][c] = (v[h][c] == -INFINITY) ? 0.f : exp2_p(__fsub_rn(v[h][c], m_new));
+            sq = __fadd_rn(sq, v[h][c]);
+          }
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          v[c] = (v[c] == -INFINITY) ? 0.f : exp2_p(__fsub_rn(v[c], m_new));
-          sq = __fadd_rn(sq, v[c]);
-        }
+        const float s2 = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));
+        const float rs = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, 2));
+        l[h] = __fadd_rn(__fmul_rn(l[h], alpha[h]), rs);
+        m[h] = m_new;
       }
-      xsum[qd * 128 + r] = sq;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&xb[1]);
-      if (!warp_wait(&xb[1], t & 1)) {
-        ok = false;
-        break;
-      }
-      const float rs =
-          __fadd_rn(__fadd_rn(xsum[r], xsum[128 + r]), __fadd_rn(xsum[256 + r], xsum[384 + r]));
-      l = __fadd_rn(__fmul_rn(l, alpha), rs);
-      m = m_new;
       if (t > 0) {  // P V of the previous tile has landed in O
         if (!warp_wait(o_done, (t - 1) & 1)) {
           ok = false;
@@ -1069,21 +1091,21 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
         fold_lane(m_done, l_done);
         if (split_start) {
           write_partial(s0 + t / ntf - 1);
-          Rm = -INFINITY;  // the next fold copies into R
-          Rl = 0.f;
+          Rm[0] = Rm[1] = -INFINITY;  // the next fold copies into R
+          Rl[0] = Rl[1] = 0.f;
         }
         zero_o();
       }
-      // O = O alpha on this quarter (identity where alpha == 1; O is +0 at a lane's first tile)
-      if (t > 0 && !lane_start && __any_sync(0xffffffffu, alpha != 1.0f)) {
+      // O = O alpha (identity where alpha == 1; O is +0 at a lane's first tile)
+      if (t > 0 && !lane_start && __any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
 #pragma unroll 1
-        for (int c = 0; c < OQ; c += CW) {
-          uint32_t oo[CW];
-          tmem_ld_cols_attn<CW>(tO + c, oo);
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t oo[16];
+          tmem_ld_16x256b_x4(tO + c, oo);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < CW; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha));
-          tmem_st_cols<CW>(tO + c, oo);
+          for (int i = 0; i < 16; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha[(i >> 1) & 1]));
+          tmem_st_16x256b_x4(tO + c, oo);
         }
         tmem_st_wait();
       }
@@ -1102,16 +1124,20 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
                 make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      // this quad of the P row in bf16: keys 8j + 2qd + {0, 1} are bytes 4qd .. 4qd + 3
-      // of the row's 16-byte chunk j in the swizzled P tile
-      uint8_t* prow = sP + (t & 1) * Lay::kP + r * 128;
+      // the rows' P in bf16: keys 8j + 2qd + {0, 1} are bytes 4qd .. 4qd + 3 of the
+      // row's 16-byte chunk j in the swizzled P tile
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint32_t*>(prow + ((j ^ (r & 7)) << 4) + 4 * qd) = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+      for (int h = 0; h < 2; ++h) {
+        uint8_t* prow = sP + (t & 1) * Lay::kP + r[h] * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint32_t*>(prow + ((j ^ (r[h] & 7)) << 4) + 4 * qd) =
+              pack_bf16x2(v[h][2 * j], v[h][2 * j + 1]);
+      }
       fence_proxy_async();
       tc_fence_before();
-      // this warp's quads of P (and its share of the zeroed V rows) are written;
-      // the MMA waits for all sixteen warps
+      // this warp's rows of P (and its share of the zeroed V rows) are written;
+      // the MMA waits for all the softmax warps
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[t & 1]);
     }
