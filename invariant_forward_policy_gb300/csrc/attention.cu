@@ -704,8 +704,8 @@ struct TcAttnLayout {
   static constexpr int kOffP = kOffKV + kStages * 2 * kPage;
   static constexpr int kOffBar = kOffP + 2 * kP;
   static constexpr int kBytes = kOffBar + 256 + 1024;   // + barriers, + alignment slack
-  static constexpr uint32_t kCols = HD == 128 ? 512 : 256;  // S0, S1 (64 each), O, R (HD each)
-  static constexpr uint32_t kColS = 0, kColO = 128, kColR = 128 + HD;
+  static constexpr uint32_t kCols = 256;  // S0, S1 (64 each), O (HD); the lane accumulator R is in registers
+  static constexpr uint32_t kColS = 0, kColO = 128;
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kThreads = 32 * kSoftmaxWarps + 64;  // + TMA warp, MMA warp
 };
@@ -907,9 +907,14 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
     mbar_arrive(q_full);
 
     const uint32_t tblk = tmem + ((uint32_t)rb << 16);
-    const uint32_t tS = tblk + Lay::kColS, tO = tblk + Lay::kColO, tR = tblk + Lay::kColR;
-    // register i of a 16-register O or R group at column c0 is row (i >> 1) & 1, column
-    // c0 + 8 (i >> 2) + 2 qd + (i & 1)
+    const uint32_t tS = tblk + Lay::kColS, tO = tblk + Lay::kColO;
+    // register i of a 16-register O group at column c0 is row (i >> 1) & 1, column
+    // c0 + 8 (i >> 2) + 2 qd + (i & 1); the lane accumulator R holds the same elements,
+    // R[c0 / 2 + i], in registers
+    constexpr int NR = HD / 2;
+    float R[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) R[i] = 0.f;
     auto zero_o = [&]() {
       uint32_t z[16];
 #pragma unroll
@@ -933,22 +938,21 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
         fb[h] = (mq[h] == M[h]) ? 1.0f : exp2f(__fsub_rn(mq[h], M[h]));
       }
       if (__any_sync(0xffffffffu, has[0] || has[1])) {
-#pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t rr[16], oo[16];
-          tmem_ld_16x256b_x4(tR + c, rr);
-          tmem_ld_16x256b_x4(tO + c, oo);
+#pragma unroll
+        for (int c = 0; c < HD; c += 64) {  // two O groups per TMEM round trip
+          uint32_t oo[2][16];
+          tmem_ld_16x256b_x4(tO + c, oo[0]);
+          tmem_ld_16x256b_x4(tO + c + 32, oo[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int h = (i >> 1) & 1;
-            const float rv = __uint_as_float(rr[i]), ov = __uint_as_float(oo[i]);
-            const float nv = copy[h] ? ov : (has[h] ? __fadd_rn(__fmul_rn(rv, fa[h]), __fmul_rn(ov, fb[h])) : rv);
-            rr[i] = __float_as_uint(nv);
-          }
-          tmem_st_16x256b_x4(tR + c, rr);
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int h = (i >> 1) & 1, ri = (c + 32 * b) / 2 + i;
+              const float rv = R[ri], ov = __uint_as_float(oo[b][i]);
+              R[ri] = copy[h] ? ov : (has[h] ? __fadd_rn(__fmul_rn(rv, fa[h]), __fmul_rn(ov, fb[h])) : rv);
+            }
         }
-        tmem_st_wait();
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -977,19 +981,15 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
         store[h] = row_valid[h] && row_pos[h] >= s * a.split;
         pidx[h] = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
       }
-#pragma unroll 1
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t rr[16];
-        tmem_ld_16x256b_x4(tR + c, rr);
-        tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < HD; c += 32)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             if (store[h])
               *reinterpret_cast<float2*>(a.part_o + pidx[h] * HD + c + 8 * k + 2 * qd) =
-                  make_float2(__uint_as_float(rr[4 * k + 2 * h]), __uint_as_float(rr[4 * k + 2 * h + 1]));
-      }
+                  make_float2(R[c / 2 + 4 * k + 2 * h], R[c / 2 + 4 * k + 2 * h + 1]);
 #pragma unroll
       for (int h = 0; h < 2; ++h)
         if (store[h] && qd == 0) *reinterpret_cast<float2*>(a.part_ml + pidx[h] * 2) = make_float2(Rm[h], Rl[h]);
@@ -1098,14 +1098,19 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
       }
       // O = O alpha (identity where alpha == 1; O is +0 at a lane's first tile)
       if (t > 0 && !lane_start && __any_sync(0xffffffffu, alpha[0] != 1.0f || alpha[1] != 1.0f)) {
-#pragma unroll 1
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t oo[16];
-          tmem_ld_16x256b_x4(tO + c, oo);
+#pragma unroll
+        for (int c = 0; c < HD; c += 64) {  // two O groups per TMEM round trip
+          uint32_t oo[2][16];
+          tmem_ld_16x256b_x4(tO + c, oo[0]);
+          tmem_ld_16x256b_x4(tO + c + 32, oo[1]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) oo[i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[i]), alpha[(i >> 1) & 1]));
-          tmem_st_16x256b_x4(tO + c, oo);
+          for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              oo[b][i] = __float_as_uint(__fmul_rn(__uint_as_float(oo[b][i]), alpha[(i >> 1) & 1]));
+            tmem_st_16x256b_x4(tO + c + 32 * b, oo[b]);
+          }
         }
         tmem_st_wait();
       }
