@@ -1451,7 +1451,8 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
       const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
       // K page
       int slot = warp * kDecSlots + used % kDecSlots;
-      bool ok = dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+      // decided for the whole warp: ldmatrix and mma.sync below are warp-collective
+      bool ok = __all_sync(0xffffffffu, dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
       if constexpr (KV8) {
         if (ok) expand(smem + slot * Lay::kSlot, n_keys);
         __syncwarp();
@@ -1470,7 +1471,7 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
         __syncwarp();  // the K page and its scales are read before the V page replaces them
         ++used;
         slot = warp * kDecSlots + used % kDecSlots;
-        ok = ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+        ok = __all_sync(0xffffffffu, ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
         if (ok) expand(smem + slot * Lay::kSlot, n_keys);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
@@ -1485,7 +1486,7 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
       ++used;
       // V page
       slot = warp * kDecSlots + used % kDecSlots;
-      ok = ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status);
+      ok = __all_sync(0xffffffffu, ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
       if (ok) {
         uint8_t* sv = smem + slot * Lay::kTile;
         if (n_keys < kKeys) {

@@ -525,7 +525,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       if (args.tile_expert && tile_expert(tc.m_tile) < 0) continue;
       const int b = local & 1;
       const uint32_t bph = (local >> 1) & 1;
-      const bool acc_ok = mbar_wait(&acc_full[b], bph);
+      // decided for the whole warp: the TMEM loads below are warp-collective
+      const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[b], bph));
       tc_fence_after();
       if (!acc_ok) {
         report(args.status, DEV_TIMEOUT);
@@ -715,7 +716,8 @@ __global__ void __launch_bounds__(rows_threads<TN>()) gemm_rows_kernel(const __n
   const uint32_t a_lane = smem_u32(sA) + (lane & 15) * stride + (lane >> 4) * 16;
   const uint32_t w_lane = smem_u32(sW) + (warp * 8 + (lane & 7)) * stride + (lane >> 3) * 16;
   for (int c = 0; c < nch && ok && warp < kMmaWarps; ++c) {
-    if (!mbar_wait(&bar[c], 0)) {
+    // decided for the whole warp: ldmatrix and mma.sync below are warp-collective
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar[c], 0))) {
       ok = false;
       break;
     }

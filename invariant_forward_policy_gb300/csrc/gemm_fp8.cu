@@ -243,7 +243,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
       for (int kb = 0; kb < nk; ++kb, ++pb) {
         const int j = pb & 1;
         const float sc = valid ? args.sa[(int64_t)row * nk + kb] * args.sw[(int64_t)wblk * nk + kb] : 0.f;
-        if (!mbar_wait(&pfull[j], (pb >> 1) & 1)) {
+        // decided for the whole warp: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(&pfull[j], (pb >> 1) & 1))) {
           report(args.status, DEV_TIMEOUT);
           *abort_flag = 1;
           ok = false;
