@@ -904,6 +904,29 @@ static int tile_n_for(int64_t n_rows_w, int64_t K, bool swiglu, int64_t E = 1) {
   return 256;
 }
 
+// Tile width of a decode-size call (17..128 rows) of a dense weight without the
+// fused log-softmax or RoPE: an element's bits do not depend on the tile width
+// (only the log-softmax records do, and RoPE needs whole heads), so the width
+// that minimises the bytes the busiest CTA reads (its tiles x (the call's A
+// rows + its W slice)) is taken, spreading a large weight over the GPU.
+static int decode_tile_n(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, int bn_weight) {
+  const int64_t n_out = swiglu ? n_rows_w / 2 : n_rows_w;
+  const int64_t a_rows = std::max<int64_t>(8, cdiv(M, 8) * 8);
+  int best = bn_weight;
+  double best_bytes = 0.0;
+  for (int bn : {256, 128, 64, 32, 16}) {
+    if (swiglu && bn < 32) continue;
+    const int64_t tiles = cdiv(n_out, swiglu ? bn / 2 : bn);
+    const int64_t per_cta = cdiv(tiles, (int64_t)num_sms());
+    const double bytes = (double)per_cta * (double)(a_rows + bn) * (double)K * 2.0;
+    if (best_bytes == 0.0 || bytes < best_bytes) {
+      best = bn;
+      best_bytes = bytes;
+    }
+  }
+  return best;
+}
+
 // Non-invariant choices (BI_FAST): tile width and split count chosen from M.
 static void fast_plan(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, int* bn, int* splits) {
   *bn = tile_n_for(n_rows_w, K, swiglu);
@@ -1048,6 +1071,8 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
     fast_plan(g.M, g.n_rows_w, g.K, swiglu, &bn, &splits);
     if (g.lse || g.rope) splits = 1;  // fused epilogues keep whole K per tile; FAST narrows the tiles instead
   }
+  if (!g.lse && !g.rope && g.E == 1 && !g.tile_expert && g.M <= kBM && splits == 1)
+    bn = decode_tile_n(g.M, g.n_rows_w, g.K, swiglu, bn);
   if (g.lse && bn < 64) bn = 64;  // the fused log-softmax records are per 64+ vocab columns
   if (g.rope) {
     // a tile must hold whole heads so that rotate-half pairs meet in one thread
