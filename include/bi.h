@@ -89,10 +89,14 @@ bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, 
 /* --------------------------------------------------------------------- GEMM
  * [Article] §4.1 "Dense GEMM: one accumulation order for every M".
  * C[m, n] = sum_k A[m, k] * W[n, k] with bf16 inputs and fp32 accumulation on
- * the tcgen05 tensor cores (TMEM accumulator, TMA-fed 128B-swizzled tiles).
- * In BI_INVARIANT mode the tile is 128 x BN x 64 with BN a function of (N, K,
- * epilogue) only, K is consumed in ascending 16-wide steps, never split: the
- * bits of row m do not depend on M or on the other rows.
+ * the tensor cores.  In BI_INVARIANT mode every element is the sum, in ascending
+ * order, of 16-wide K steps (bf16 products, fp32 accumulator), never split: the
+ * bits of row m do not depend on M or on the other rows.  Schedules: tcgen05
+ * with a TMEM accumulator and TMA-fed 128B-swizzled 128 x BN x 64 tiles; for at
+ * most 16 rows of a weight under 4M elements, mma.sync m16n8k16 with loader
+ * warps (the same fp32 bits per K step).  BN does not change an element's bits;
+ * it is bi_gemm_tile_n's width, or for 17..128 rows (without a fused RoPE) the
+ * width that spreads the weight over the GPU.
  * A: bf16 [M, K]; W: bf16 [N, K] (nn.Linear layout); C: bf16 or fp32 [M, N]
  * (c_dtype), or for BI_EPI_SWIGLU: W holds 2F rows (gate rows then up rows)
  * and C is bf16 [M, F] with C = bf16( silu(bf16(g)) * bf16(u) ) computed in
@@ -103,8 +107,10 @@ bi_status bi_rmsnorm(const void* x, void* residual, const void* gamma, void* y, 
 bi_status bi_gemm(const void* A, int64_t M, int64_t K, const void* W, int64_t N, void* C, int c_dtype,
                   int epilogue, int mode, void* workspace, size_t ws_bytes, void* stream);
 size_t bi_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int epilogue, int mode);
-/* The N tile width bi_gemm uses for a weight of shape (N, K) (diagnostic):
- * 16, 32, 64, 128 or 256, a function of (N, K, epilogue) only. */
+/* The N tile width bi_gemm uses for a weight of shape (N, K) at prefill size
+ * (more than 128 rows; diagnostic): 16, 32, 64, 128 or 256, a function of (N, K,
+ * epilogue) only.  The fused log-softmax (bi_lm_head_logprob) keeps this width
+ * at every M, since its records are per tile. */
 int bi_gemm_tile_n(int64_t N, int64_t K, int epilogue);
 
 /* Grouped GEMM over 128-row tiles, each tile owned by one expert
