@@ -106,7 +106,7 @@ def test_gemm_rows_invariant_to_M_and_order(N, K):
     A, W = dev_bf16(ab), dev_bf16(wb)
     full = torch.empty((300, N), dtype=torch.float32, device="cuda")
     bi.bi_gemm(A, 300, K, W, N, full, bi.BI_DTYPE_FP32)
-    for M in (1, 2, 7, 16, 64, 127, 128, 129, 255):
+    for M in (1, 2, 7, 16, 17, 33, 64, 65, 127, 128, 129, 255):
         part = torch.empty((M, N), dtype=torch.float32, device="cuda")
         off = 300 - M
         bi.bi_gemm(A[off:].contiguous(), M, K, W, N, part, bi.BI_DTYPE_FP32)
@@ -127,7 +127,7 @@ def test_gemm_swiglu_rows_invariant_to_M_and_order(F, K):
     A, W = dev_bf16(ab), dev_bf16(wb)
     full = torch.empty((300, F), dtype=torch.bfloat16, device="cuda")
     bi.bi_gemm(A, 300, K, W, 2 * F, full, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
-    for M in (1, 16, 64, 129):
+    for M in (1, 16, 17, 40, 64, 129):
         part = torch.empty((M, F), dtype=torch.bfloat16, device="cuda")
         bi.bi_gemm(A[300 - M:].contiguous(), M, K, W, 2 * F, part, bi.BI_DTYPE_BF16, bi.BI_EPI_SWIGLU)
         assert same_bits(part, full[300 - M:]), M
@@ -647,7 +647,7 @@ def test_fused_qkv_rope_rows_invariant_to_M(Hq, Hkv, hd, K):
     bi.bi_qkv_rope_kv_write(X, T, K, W, Hq, Hkv, hd, row_seq, row_pos, table, max_pos, bt, max_blk, n_blocks, q,
                             kc, vc)
     btc = bt.cpu().numpy()
-    for M in (1, 5, 16, 17):
+    for M in (1, 5, 16, 17, 40, 64):
         idx = np.sort(rng.choice(T, M, replace=False))
         kp, vp = torch.zeros_like(kc), torch.zeros_like(vc)
         qp = torch.empty((M, Hq, hd), dtype=torch.bfloat16, device="cuda")
