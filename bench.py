@@ -503,8 +503,9 @@ def _graph_us(fn, n=20, reps=10):
 
 
 def roofline_probe(dec, ep, args):
-    """Roofline of the step's dominant kernel class, the decode-size tcgen05 GEMMs
-    (QKV, O, gate/up+SwiGLU, down of every layer and the fused lm_head+logprob):
+    """Roofline of the step's dominant kernel class, the decode-size GEMMs (QKV, O,
+    gate/up+SwiGLU, down of every layer on the mma.sync rows schedule, and the
+    fused lm_head+logprob on the tcgen05 tile schedule with its LSE epilogue):
     each is launched at its decode shape (M = 16) from a CUDA graph, the way the
     decode step runs it, and timed with CUDA events.  achieved = the algorithmic
     bytes of one decode step's GEMMs (weights + activations in + out) / their
@@ -543,13 +544,13 @@ def roofline_probe(dec, ep, args):
     per_step_us += us
     per_step_bytes += V * d * 2 + B * d * 2 + B * 8
     achieved = per_step_bytes / (per_step_us * 1e-6) / 1e9
-    return {"kernel": "gemm_tc_kernel, decode-size launches of one decode step (M 16: QKV, O, gate/up+SwiGLU, "
-                      "down per layer; fused lm_head + log-softmax)",
+    return {"kernel": "decode-size GEMM launches of one decode step (M 16): gemm_rows_kernel for QKV, O, "
+                      "gate/up+SwiGLU and down per layer; gemm_tc_kernel<EPI_LSE> for the fused lm_head + log-softmax",
             "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": None, "us_per_decode_step": round(per_step_us, 2), "us_per_launch": detail,
             "algorithmic_bytes_per_decode_step": per_step_bytes, "peak_source": src,
-            "note": "weights L2-resident across decode steps; launches are latency-bound (one 128-row tile, "
-                    "16 valid rows); frac of the HBM copy peak"}
+            "note": "weights L2-resident across decode steps; launches are latency-bound (a few us each, "
+                    "16 rows); frac of the HBM copy peak"}
 
 
 def kernel_table(args):
@@ -1001,14 +1002,15 @@ def run_kernel_case(name: str, reps: int):
         for _ in range(reps):
             bi.bi_attention(q, B, seq, row0, pos0, B, 1, Hq, Hkv, hd, kc, vc, bt, max_blk, B * max_blk, ctx, 512, 0.125,
                             ws, out)
-    elif name == "step":
+    elif name in ("step", "fp8_step"):
         # the timed unit of the default run: rollout + recompute of the dense-decoder workload
+        # (fp8_step: the same episode with W8A8 block-FP8 layers and the FP8 KV cache)
         from invariant_forward_policy_gb300.decoder import Decoder, Episode
         from synthetic import C2, make_decoder_weights, make_prompts
         shape = C2["shape"]
         wb = make_decoder_weights(shape, seed=C2["seed"], w_std=C2["w_std"])
         prompts = make_prompts(C2["batch"], C2["prompt_min"], C2["prompt_max"], shape.vocab, C2["seed"])
-        dec = Decoder(shape, wb, max_pos=1024, device=dev)
+        dec = Decoder(shape, wb, max_pos=1024, device=dev, fp8=name == "fp8_step")
         ep = Episode(dec, [len(p) for p in prompts], C2["gen"], mode=bi.BI_INVARIANT)
         pd = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
         for _ in range(reps):
@@ -1256,7 +1258,7 @@ def main():
                          "kv_fp8_gather, c5_decode, c5_recompute, topk_prefill, attention_prefill_long, rmsnorm, "
                          "logprob, lm_head_fused, "
                          "moe_layer) or "
-                         "the whole step (step) and exit; for profiling")
+                         "the whole step (step, or fp8_step with the block-FP8 model) and exit; for profiling")
     ap.add_argument("--reps", type=int, default=5)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)

@@ -17,7 +17,9 @@
 // 128-column half, i.e. per weight block) add each finished partial, times
 // the exact power-of-two scale product, to an fp32 accumulator held in
 // registers, in ascending kb.  The tile shape and the K order are the same for
-// every M, so every row's result is batch invariant.
+// every M, so every row's result is batch invariant.  Calls of at most 16
+// rows run the same MMA with the operands' roles exchanged (weight tiles as its
+// M side; see gemm_fp8_dec_kernel), which leaves every element's bits as they are.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -294,6 +296,188 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
   }
 }
 
+// ------------------------------------------------------------------ decode-size calls
+// Calls of at most 16 rows (a decode step) on the same tensor-core MMA with the
+// operands' roles exchanged: a tile of BM (64 or 128) weight rows is the MMA's
+// M side and the call's rows, zero-filled by the TMA copy up to 16, are its N
+// side, so one CTA per BM output columns streams its weight rows once (N / BM
+// CTAs where the 128-row tile above gives N / 256).  An element's partial per K
+// block is the same sum of the same products in the same K order as in the
+// large kernel (which operand is which does not enter a product), and the
+// promotion is the same fp32 fma in ascending kb, so the rows are the same bits
+// (the row-invariance test compares them across M).  Weights are copied before
+// the dependency wait and the call's codes after it; a ring of up to
+// f8dec_max_stages K blocks holds the whole K of the usual decode shapes, so
+// every copy is in flight at once.
+constexpr int kF8DecRows = 16;   // the MMA's N: rows of the call, zero past M
+constexpr int kF8DecBufs = 4;    // TMEM partial buffers (16 columns each)
+constexpr int kF8DecThreads = 192;  // TMA, MMA, four promotion warps (one per lane quarter)
+__host__ __device__ constexpr int f8dec_max_stages(int bm) { return bm == 64 ? 16 : 8; }
+__host__ __device__ constexpr int f8dec_stage_bytes(int bm) { return bm * kF8Block + kF8DecRows * kF8Block; }
+__host__ constexpr size_t f8dec_smem(int bm, int stages) {
+  return 1024 + (size_t)stages * f8dec_stage_bytes(bm) + 512;
+}
+
+struct F8DecArgs {
+  const float* sa;  // [M, nkb]
+  const float* sw;  // [N / 128, nkb]
+  void* C;
+  int* status;
+  int M, N, nkb, stages, c_fp32;
+};
+
+template <int BM>
+__global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __grid_constant__ CUtensorMap tmW,
+                                                                 const __grid_constant__ CUtensorMap tmX,
+                                                                 const F8DecArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = args.stages, nk = args.nkb;
+  uint8_t* sW = smem;                              // [S][BM rows x 128 codes], 128-byte swizzle
+  uint8_t* sX = smem + S * BM * kF8Block;          // [S][16 rows x 128 codes]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sX + S * kF8DecRows * kF8Block);
+  uint64_t* empty = full + S;
+  uint64_t* pfull = empty + S;                     // [kF8DecBufs] MMA -> promotion
+  uint64_t* pempty = pfull + kF8DecBufs;           // [kF8DecBufs] promotion -> MMA (4 warp arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + kF8DecBufs);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  constexpr uint32_t kTmemCols = kF8DecBufs * kF8DecRows;
+  constexpr uint32_t kStageW = BM * kF8Block, kStageX = kF8DecRows * kF8Block;
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BM;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kF8DecBufs; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmX);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: the first ring's weights before the
+      // dependency wait, its codes after it; later blocks reuse freed stages
+      const int first = min(nk, S);
+      for (int kb = 0; kb < first; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], kStageW + kStageX);
+        tma_load_2d(sW + kb * kStageW, &tmW, &full[kb], kb * kF8Block, n0);
+      }
+      pdl_wait();
+      for (int kb = 0; kb < first; ++kb) tma_load_2d(sX + kb * kStageX, &tmX, &full[kb], kb * kF8Block, 0);
+      for (int kb = first; kb < nk; ++kb) {
+        const int s = kb % S;
+        if (!mbar_wait(&empty[s], ((kb / S) & 1) ^ 1) || *abort_flag) {
+          report(args.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kStageW + kStageX);
+        tma_load_2d(sW + s * kStageW, &tmW, &full[s], kb * kF8Block, n0);
+        tma_load_2d(sX + s * kStageX, &tmX, &full[s], kb * kF8Block, 0);
+      }
+      for (int i = 0; i < S && i < nk; ++i) {  // let the last copies land
+        const int kb = nk - 1 - i;
+        mbar_wait(&full[kb % S], (kb / S) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: one TMEM partial (BM x 16) per K block
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, kF8DecRows);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int j = kb % kF8DecBufs, s = kb % S;
+        if (!mbar_wait(&pempty[j], ((kb / kF8DecBufs) & 1) ^ 1) || !mbar_wait(&full[s], (kb / S) & 1) ||
+            *abort_flag) {
+          report(args.status, DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t w_addr = smem_u32(sW + s * kStageW), x_addr = smem_u32(sX + s * kStageX);
+#pragma unroll
+        for (int k = 0; k < kF8Block / 32; ++k)
+          tc_mma_f8(tmem_base + j * kF8DecRows, sw128_kmajor_desc(w_addr + k * 32), sw128_kmajor_desc(x_addr + k * 32),
+                    idesc, k != 0 ? 1u : 0u);
+        tc_commit(&empty[s]);
+        tc_commit(&pfull[j]);
+      }
+    }
+  } else {
+    // ---------------- promotion and store: warps 2..5, lane quarter q = warp % 4;
+    // thread (q, lane) owns output column n0 + c (c = its tile row) for the 16 rows
+    const int q = warp & 3;
+    const int c = BM == 128 ? 32 * q + lane : 16 * q + lane;
+    const bool col_ok = (BM == 128 || lane < 16) && n0 + c < args.N;
+    const int wblk = n0 / kF8Block;  // BM divides 128: the tile lies in one weight block
+    const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
+    float acc[kF8DecRows];
+#pragma unroll
+    for (int m = 0; m < kF8DecRows; ++m) acc[m] = 0.f;
+    pdl_wait();  // the row scales come from the preceding kernel
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int j = kb % kF8DecBufs;
+      const float swk = args.sw[(int64_t)wblk * nk + kb];
+      float sc[kF8DecRows];
+#pragma unroll
+      for (int m = 0; m < kF8DecRows; ++m) sc[m] = m < args.M ? __fmul_rn(args.sa[(int64_t)m * nk + kb], swk) : 0.f;
+      // decided for the whole warp: the TMEM load below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&pfull[j], (kb / kF8DecBufs) & 1) && !*abort_flag)) {
+        report(args.status, DEV_TIMEOUT);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t p[16];
+      tmem_ld_32x32b_x16(tq + j * kF8DecRows, p);
+      tmem_ld_wait();
+      // acc += partial * (scale_a * scale_w), one rounding per element
+#pragma unroll
+      for (int m = 0; m < kF8DecRows; ++m) acc[m] = __fmaf_rn(__uint_as_float(p[m]), sc[m], acc[m]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pempty[j]);
+    }
+    if (ok && col_ok && !*abort_flag) {
+      const int col = n0 + c;
+#pragma unroll
+      for (int m = 0; m < kF8DecRows; ++m) {
+        if (m >= args.M) break;
+        if (args.c_fp32)
+          static_cast<float*>(args.C)[(int64_t)m * args.N + col] = acc[m];
+        else
+          static_cast<__nv_bfloat16*>(args.C)[(int64_t)m * args.N + col] = __float2bfloat16_rn(acc[m]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace bi
 
 extern "C" {
@@ -333,6 +517,36 @@ bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, con
   BI_REQUIRE(K > 0 && Aq && sa && Wq && sw && C, "null pointer");
   BI_REQUIRE(aligned16(Aq) && aligned16(Wq) && aligned16(C), "pointers must be 16-byte aligned");
   BI_REQUIRE(M <= 0x7fffffff && N <= 0x7fffffff, "shape too large");
+  if (M <= kF8DecRows) {
+    // decode size: weight tiles as the MMA's M side (the same bits); 128-row
+    // tiles once 64-row ones would fill the GPU twice over
+    const int bm = N / 64 >= 2 * (int64_t)num_sms() ? 128 : 64;
+    const int nkb = (int)(K / kF8Block);
+    const int stages = std::min(nkb, f8dec_max_stages(bm));
+    static std::once_flag once_dec;
+    static cudaError_t attr_dec = cudaSuccess;
+    std::call_once(once_dec, [] {
+      attr_dec = cudaFuncSetAttribute(gemm_fp8_dec_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)f8dec_smem(64, f8dec_max_stages(64)));
+      if (attr_dec == cudaSuccess)
+        attr_dec = cudaFuncSetAttribute(gemm_fp8_dec_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)f8dec_smem(128, f8dec_max_stages(128)));
+    });
+    if (attr_dec != cudaSuccess)
+      return fail(BI_ERR_CUDA, std::string("bi_gemm_fp8 decode smem attribute: ") + cudaGetErrorString(attr_dec));
+    CUtensorMap tw, tx;
+    if (!encode_tmap_2d_u8(&tw, Wq, K, N, K, kF8Block, bm) ||
+        !encode_tmap_2d_u8(&tx, Aq, K, M, K, kF8Block, kF8DecRows))
+      return fail(BI_ERR_CUDA, "bi_gemm_fp8: TMA descriptor failed");
+    F8DecArgs da{sa, sw, C, device_status_ptr(), (int)M, (int)N, nkb, stages, c_dtype == BI_DTYPE_FP32};
+    const dim3 grid((unsigned)(N / bm));
+    const size_t smem = f8dec_smem(bm, stages);
+    return launched(bm == 64 ? launch_pdl(gemm_fp8_dec_kernel<64>, grid, dim3(kF8DecThreads), smem, as_stream(stream),
+                                          tw, tx, da)
+                             : launch_pdl(gemm_fp8_dec_kernel<128>, grid, dim3(kF8DecThreads), smem,
+                                          as_stream(stream), tw, tx, da),
+                    "bi_gemm_fp8");
+  }
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {

@@ -66,7 +66,7 @@ def test_gemm_fp8_parity(M, N, K):
     assert bi.bi_device_status() == 0
 
 
-@pytest.mark.parametrize("N,K", [(256, 512), (3072, 2048)])
+@pytest.mark.parametrize("N,K", [(256, 512), (512, 1408), (3072, 2048), (20480, 256)])
 def test_gemm_fp8_rows_invariant_to_M_and_order(N, K):
     rng = np.random.default_rng(N)
     qa, sa, qw, sw = _fp8_operands(rng, 300, N, K)
