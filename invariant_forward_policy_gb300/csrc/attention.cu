@@ -1186,26 +1186,39 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
 constexpr int kDecMaxPieces = 1024;      // larger decode calls take the per-CTA schedule (same bits)
 constexpr int kDecPersistentSplits = 4;  // shorter contexts take the per-CTA schedule (same bits)
 
-// KV8 (FP8 cache): a ring object is a page of e4m3 codes (64 rows x hd bytes,
-// unswizzled) followed by its 64 fp32 scales; each consumer warp expands the
-// object into its own bf16 page (the swizzled layout ldmatrix reads) and copies
-// the scales, zero past the item's last position, before releasing the slot.
+// KV8 (FP8 cache): warps 4..7 replace the producer, warp 4 + w serving
+// consumer w alone.  It walks the items as consumer w does and copies each
+// page's e4m3 codes (64 rows x hd bytes, unswizzled) and 64 fp32 scales with
+// TMA into its two-slot code ring, two pages ahead; it then expands a landed
+// page into the consumer's two-slot bf16 ring (the swizzled layout ldmatrix
+// reads), rows and scales after the item's last position zero.  The consumer
+// runs the bf16 schedule on that page with the scales applied.  Each ring
+// involves one loader warp and one consumer warp only.
 template <int HD, bool KV8 = false>
 struct DecLayout {
-  // ring depth per consumer warp: three slots at hd 128 (one CTA per SM); two
-  // at hd 64, so that two CTAs share an SM
-  static constexpr int kDecSlots = HD == 64 ? 2 : 3;
+  static constexpr int kThreads = KV8 ? 256 : 160;  // consumers, then producer (KV8: four loaders)
+  // bf16 ring depth per consumer warp: three slots at hd 128 (one CTA per SM);
+  // two at hd 64 (two CTAs share an SM) and on an FP8 cache (two code slots
+  // more per ring)
+  static constexpr int kDecSlots = (HD == 64 || KV8) ? 2 : 3;
+  static constexpr int kCodeSlots = 2;
   static constexpr int kTile = kKeys * HD * 2;                       // one bf16 K or V page
   static constexpr int kCodes = kKeys * HD;                          // one page of codes
-  static constexpr int kSlot = KV8 ? (kCodes + kKeys * 4 + 1023) / 1024 * 1024 : kTile;
-  static constexpr int kRing = 4 * kDecSlots * kSlot;                // four rings
-  static constexpr int kPriv = kRing;                                // KV8: bf16 page per consumer warp
-  static constexpr int kPrivScale = kPriv + (KV8 ? 4 * kTile : 0);   // KV8: [4][64] scales
-  static constexpr int kStates = kPrivScale + (KV8 ? 4 * kKeys * 4 : 0);  // lane states of warps 1..3
+  static constexpr int kCodeSlot = kCodes + kKeys * 4;               // codes, then scales
+  static constexpr int kRing = 4 * kDecSlots * kTile;                // four bf16 rings
+  static constexpr int kScales = kRing;                              // KV8: [4][kDecSlots][64] fp32
+  static constexpr int kCodeRing = kScales + (KV8 ? 4 * kDecSlots * kKeys * 4 : 0);  // KV8: [4][2] code slots
+  static constexpr int kStates = kCodeRing + (KV8 ? 4 * kCodeSlots * kCodeSlot : 0);  // lane states of warps 1..3
   static constexpr int kTable = kStates + 3 * 32 * (int)sizeof(LaneState<HD>);  // int [kDecMaxPieces + 1]
   static constexpr int kBars = kTable + (kDecMaxPieces + 2) * 4;
-  static constexpr int kAbort = kBars + 2 * 4 * kDecSlots * 8;       // full[4][S], empty[4][S]
+  // full[4][S] (bf16: TMA -> consumer; KV8: code TMA -> loader, [4][2]), empty[4][S]
+  // (consumer -> producer / loader), KV8 conv[4][S] (loader -> consumer)
+  static constexpr int kNBars = (KV8 ? 3 : 2) * 4 * kDecSlots;
+  static constexpr int kAbort = kBars + kNBars * 8;
   static constexpr int kBytes = kAbort + 16 + 1024;                  // + alignment slack
+  static_assert(kBars % 8 == 0 && kCodeSlot % 128 == 0, "alignment");
+  static_assert(!KV8 || kCodeSlots == kDecSlots, "one full barrier per code slot");
+  static_assert(kBytes <= 232448, "decode schedule exceeds the shared-memory limit");
 };
 
 // Work items are (piece, split, kv head) with the split at or before the
@@ -1260,8 +1273,37 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
+// KV8 loader step: the codes of one page (64 rows x hd bytes) as this lane's
+// uint4 chunks lane + 32 u, and their expansion into the swizzled bf16 page of
+// unscaled values, rows at or after nk zero.  One warp.
+template <int HD>
+struct DecCodes {
+  static constexpr int C16 = HD / 16;            // 16-code chunks per key row
+  static constexpr int kPer = kKeys * C16 / 32;  // chunks per lane
+  uint4 raw[kPer];
+  __device__ __forceinline__ void load(const uint8_t* codes, int lane) {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) raw[u] = *reinterpret_cast<const uint4*>(codes + (lane + 32 * u) * 16);
+  }
+  __device__ __forceinline__ void expand(uint8_t* page, int nk, int lane) const {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = lane + 32 * u, key = i / C16, c16 = i % C16;
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (key < nk) {
+        const uint2 b0 = e4m3x4_to_bf16x4(raw[u].x), b1 = e4m3x4_to_bf16x4(raw[u].y);
+        const uint2 b2 = e4m3x4_to_bf16x4(raw[u].z), b3 = e4m3x4_to_bf16x4(raw[u].w);
+        lo = make_uint4(b0.x, b0.y, b1.x, b1.y);
+        hi = make_uint4(b2.x, b2.y, b3.x, b3.y);
+      }
+      *reinterpret_cast<uint4*>(page + kv_off<HD>(key, 2 * c16)) = lo;
+      *reinterpret_cast<uint4*>(page + kv_off<HD>(key, 2 * c16 + 1)) = hi;
+    }
+  }
+};
+
 template <int HD, bool KV8>
-__global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
+__global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV8) ? 2 : 1)
     attention_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmks,
                             const __grid_constant__ CUtensorMap tmvs, int P) {
@@ -1269,8 +1311,12 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
   constexpr int kDecSlots = Lay::kDecSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);  // [4][kDecSlots]
-  uint64_t* empty = full + 4 * kDecSlots;                           // [4][kDecSlots]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBars);  // [4][kDecSlots] TMA -> converter / consumer
+  uint64_t* empty = full + 4 * kDecSlots;                           // [4][kDecSlots] consumer -> producer
+  uint64_t* conv = empty + 4 * kDecSlots;                           // KV8: [4][kDecSlots] loader -> consumer
+  uint64_t* ready = KV8 ? conv : full;                              // what a consumer waits for
+  float* scl = reinterpret_cast<float*>(smem + Lay::kScales);       // KV8: [4][kDecSlots][64] page scales
+  uint8_t* codes = smem + Lay::kCodeRing;                           // KV8: [4][2] code slots
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kAbort);
   int* first = reinterpret_cast<int*>(smem + Lay::kTable);          // [P + 1]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1278,6 +1324,7 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
     for (int i = 0; i < 4 * kDecSlots; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      if (KV8) mbar_init(&conv[i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -1320,7 +1367,7 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
   const int lane_len = ((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys;
   const int tpl = lane_len / kKeys;  // tiles per lane
 
-  if (warp == 4) {
+  if (!KV8 && warp == 4) {
     // ------------------------------------------------------------ producer
     int issued[4] = {0, 0, 0, 0};
     for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
@@ -1353,13 +1400,8 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
               const int n = issued[wj] + kv;
               const int slot = wj * kDecSlots + n % kDecSlots;
               if (!dec_wait(&empty[slot], ((n / kDecSlots) & 1) ^ 1, abort_flag, a.status)) break;
-              uint8_t* dst = smem + slot * Lay::kSlot;
-              if (bj >= 0 && KV8) {
-                mbar_arrive_expect_tx(&full[slot], Lay::kCodes + kKeys * 4);
-                const int page = bj * a.Hkv + it.kvh;
-                tma_load_2d(dst, kv ? &tmv : &tmk, &full[slot], 0, page * kKeys);
-                tma_load_2d(dst + Lay::kCodes, kv ? &tmvs : &tmks, &full[slot], 0, page);
-              } else if (bj >= 0) {
+              uint8_t* dst = smem + slot * Lay::kTile;
+              if (bj >= 0) {
                 mbar_arrive_expect_tx(&full[slot], Lay::kTile);
                 const int y = (bj * a.Hkv + it.kvh) * kKeys;
 #pragma unroll
@@ -1385,6 +1427,105 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
           mbar_wait(&full[w * kDecSlots + n % kDecSlots], (n / kDecSlots) & 1);
         }
     }
+    return;
+  }
+
+  if (KV8 && warp >= 4) {
+    // ------------------------------------------------- loader of ring w (KV8)
+    // objects in consumer w's order: items of this CTA, the ring's pages of each
+    // (keys lb .. le), K then V
+    const int w = warp - 4;
+    int item = blockIdx.x, lb = 0, le = 0, key0 = 0, kv = 0, kv_end = 0, seq = 0, kvh = 0, blk_all = -1;
+    bool more = false;
+    auto enter = [&]() {  // the first item from `item` on with pages for this ring
+      for (; item < n_items; item += gridDim.x) {
+        const DecItem it = dec_item(a, first, item, P);
+        lb = it.kv_begin + w * lane_len;
+        le = min(lb + lane_len, it.kv_end);
+        if (lb < le) {
+          key0 = lb;
+          kv = 0;
+          kv_end = it.kv_end;
+          seq = it.seq;
+          kvh = it.kvh;
+          // block-table entries of the first 32 pages, one per lane
+          const int bi = lb / kKeys + lane;
+          blk_all = (lb + lane * kKeys < le && bi < a.max_blk) ? a.block_table[(int64_t)seq * a.max_blk + bi] : -1;
+          more = true;
+          return;
+        }
+      }
+      more = false;
+    };
+    auto advance = [&]() {
+      if (kv == 0) {
+        kv = 1;
+        return;
+      }
+      kv = 0;
+      key0 += kKeys;
+      if (key0 >= le) {
+        item += gridDim.x;
+        enter();
+      }
+    };
+    int nk0 = 0, nk1 = 0;  // keys at or before the item's last position, per code slot
+    auto issue = [&](int n) {  // the cursor's object into code slot n % 2 (whole warp)
+      const int cs = n & 1;
+      if (cs) nk1 = kv_end - key0;
+      else nk0 = kv_end - key0;
+      const int t = (key0 - lb) / kKeys;
+      int blk = __shfl_sync(0xffffffffu, blk_all, t & 31);
+      if (lane == 0) {
+        if (t >= 32) {
+          const int bi = key0 / kKeys;
+          blk = bi < a.max_blk ? a.block_table[(int64_t)seq * a.max_blk + bi] : -1;
+        }
+        if (blk < 0 || blk >= a.n_blocks) {
+          report(a.status, DEV_BAD_INDEX);
+          blk = -1;
+        }
+        uint64_t* bar = &full[w * kDecSlots + cs];
+        uint8_t* dst = codes + (w * kDecSlots + cs) * Lay::kCodeSlot;
+        if (blk >= 0) {
+          mbar_arrive_expect_tx(bar, Lay::kCodeSlot);
+          const int page = blk * a.Hkv + kvh;
+          tma_load_2d(dst, kv ? &tmv : &tmk, bar, 0, page * kKeys);
+          tma_load_2d(dst + Lay::kCodes, kv ? &tmvs : &tmks, bar, 0, page);
+        } else {
+          mbar_arrive(bar);  // bad block (reported): the slot's old codes are expanded
+        }
+      }
+    };
+    int n_issued = 0, c = 0;
+    enter();
+    for (; n_issued < 2 && more; advance()) issue(n_issued++);
+    DecCodes<HD> cd;
+    for (; c < n_issued; ++c) {
+      const int cs = c & 1, nk = cs ? nk1 : nk0;
+      if (!__all_sync(0xffffffffu, dec_wait(&full[w * kDecSlots + cs], (c >> 1) & 1, abort_flag, a.status))) break;
+      const uint8_t* src = codes + (w * kDecSlots + cs) * Lay::kCodeSlot;
+      cd.load(src, lane);
+      const float* ssrc = reinterpret_cast<const float*>(src + Lay::kCodes);
+      const float s0 = lane < nk ? ssrc[lane] : 0.f, s1 = lane + 32 < nk ? ssrc[lane + 32] : 0.f;
+      fence_proxy_async();  // the reads above before the slot's next TMA copy
+      __syncwarp();
+      if (more) {
+        issue(n_issued++);
+        advance();
+      }
+      // bf16 slot: consumer w has released the object kDecSlots before this one
+      const int bs = w * kDecSlots + c % kDecSlots;
+      if (!__all_sync(0xffffffffu, dec_wait(&empty[bs], ((c / kDecSlots) & 1) ^ 1, abort_flag, a.status))) break;
+      cd.expand(smem + bs * Lay::kTile, nk, lane);
+      scl[bs * kKeys + lane] = s0;
+      scl[bs * kKeys + lane + 32] = s1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&conv[bs]);
+    }
+    // every copy this warp started lands before it can exit
+    if (lane == 0)
+      for (int d = c; d < n_issued; ++d) mbar_wait(&full[w * kDecSlots + (d & 1)], (d >> 1) & 1);
     return;
   }
 
@@ -1421,83 +1562,45 @@ __global__ void __launch_bounds__(160, HD == 64 ? 2 : 1)
 
     const int lb = it.kv_begin + warp * lane_len;
     const int le = min(lb + lane_len, it.kv_end);
-    uint8_t* priv = smem + Lay::kPriv + warp * Lay::kTile;                       // KV8 only
-    float* pscale = reinterpret_cast<float*>(smem + Lay::kPrivScale) + warp * kKeys;  // KV8 only
-    // KV8: ring object -> this warp's bf16 page of unscaled values and its scales,
-    // keys at or after n_keys zeroed
-    auto expand = [&](const uint8_t* obj, int n_keys) {
-      constexpr int C16 = HD / 16;  // 16-code chunks per key row; a lane keeps chunk lane % C16
-      const int c16 = lane % C16;
-#pragma unroll
-      for (int i = 0; i < kKeys * C16 / 32; ++i) {
-        const int key = (lane + 32 * i) / C16;
-        const uint4 raw = *reinterpret_cast<const uint4*>(obj + (lane + 32 * i) * 16);
-        const uint2 b0 = e4m3x4_to_bf16x4(raw.x), b1 = e4m3x4_to_bf16x4(raw.y);
-        const uint2 b2 = e4m3x4_to_bf16x4(raw.z), b3 = e4m3x4_to_bf16x4(raw.w);
-        *reinterpret_cast<uint4*>(priv + kv_off<HD>(key, 2 * c16)) = make_uint4(b0.x, b0.y, b1.x, b1.y);
-        *reinterpret_cast<uint4*>(priv + kv_off<HD>(key, 2 * c16 + 1)) = make_uint4(b2.x, b2.y, b3.x, b3.y);
-      }
-      if (n_keys < kKeys) {  // the item's last page: rows after its last position become zeros
-        __syncwarp();
-        for (int c = n_keys * (HD / 8) + lane; c < kKeys * (HD / 8); c += 32)
-          *reinterpret_cast<uint4*>(priv + kv_off<HD>(c / (HD / 8), c % (HD / 8))) = make_uint4(0u, 0u, 0u, 0u);
-      }
-      const float* sc_in = reinterpret_cast<const float*>(obj + Lay::kCodes);
-      pscale[lane] = lane < n_keys ? sc_in[lane] : 0.f;
-      pscale[lane + 32] = lane + 32 < n_keys ? sc_in[lane + 32] : 0.f;
-    };
     for (int key0 = lb; key0 < le; key0 += kKeys) {
       float sc[8][4];
       const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
       // K page
       int slot = warp * kDecSlots + used % kDecSlots;
       // decided for the whole warp: ldmatrix and mma.sync below are warp-collective
-      bool ok = __all_sync(0xffffffffu, dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
-      if constexpr (KV8) {
-        if (ok) expand(smem + slot * Lay::kSlot, n_keys);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (ok) {
-          attn_scores<HD>(smem_u32(priv), qf, lane, sc);
+      bool ok = __all_sync(0xffffffffu, dec_wait(&ready[slot], (used / kDecSlots) & 1, abort_flag, a.status));
+      if (ok) {
+        attn_scores<HD>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
+        if (KV8) {  // a score column times its key's K scale
+          const float* ks = scl + slot * kKeys;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float2 kk = *reinterpret_cast<const float2*>(pscale + j * 8 + tq * 2);
+            const float2 kk = *reinterpret_cast<const float2*>(ks + j * 8 + tq * 2);
             sc[j][0] = __fmul_rn(sc[j][0], kk.x);
             sc[j][1] = __fmul_rn(sc[j][1], kk.y);
             sc[j][2] = __fmul_rn(sc[j][2], kk.x);
             sc[j][3] = __fmul_rn(sc[j][3], kk.y);
           }
         }
-        __syncwarp();  // the K page and its scales are read before the V page replaces them
-        ++used;
-        slot = warp * kDecSlots + used % kDecSlots;
-        ok = __all_sync(0xffffffffu, ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
-        if (ok) expand(smem + slot * Lay::kSlot, n_keys);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (ok) attn_update<HD>(smem_u32(priv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc, pscale);
-        __syncwarp();
-        ++used;
-        continue;
       }
-      if (ok) attn_scores<HD>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       ++used;
       // V page
       slot = warp * kDecSlots + used % kDecSlots;
-      ok = __all_sync(0xffffffffu, ok && dec_wait(&full[slot], (used / kDecSlots) & 1, abort_flag, a.status));
+      ok = __all_sync(0xffffffffu, ok && dec_wait(&ready[slot], (used / kDecSlots) & 1, abort_flag, a.status));
       if (ok) {
         uint8_t* sv = smem + slot * Lay::kTile;
-        if (n_keys < kKeys) {
+        if (!KV8 && n_keys < kKeys) {  // (the converter has zeroed an FP8 page's tail)
           for (int c = n_keys * (HD / 8) + lane; c < kKeys * (HD / 8); c += 32) {
             const int key = c / (HD / 8), ch = c % (HD / 8);
             *reinterpret_cast<uint4*>(sv + kv_off<HD>(key, ch)) = make_uint4(0u, 0u, 0u, 0u);
           }
           __syncwarp();
         }
-        attn_update<HD>(smem_u32(sv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
-        fence_proxy_async();  // generic writes above before the next TMA write of this slot
+        attn_update<HD>(smem_u32(sv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
+                        KV8 ? scl + slot * kKeys : nullptr);
+        if (!KV8) fence_proxy_async();  // generic writes above before the next TMA write of this slot
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
@@ -1674,7 +1777,8 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
     attr_err =
         cudaFuncSetAttribute(attention_decode_kernel<HD, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8>, 160, smem);
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8>,
+                                                               DecLayout<HD, KV8>::kThreads, smem);
     if (per_sm < 1) per_sm = 1;
   });
   if (attr_err != cudaSuccess)
@@ -1695,7 +1799,8 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
   }
   if (!ok) return fail(BI_ERR_CUDA, "attention decode: cuTensorMapEncodeTiled failed for the K/V cache");
   const int64_t grid = std::min<int64_t>(P * args.Hkv * args.nsplit, (int64_t)num_sms() * per_sm);
-  return launched(launch_pdl(attention_decode_kernel<HD, KV8>, dim3((unsigned)grid), dim3(160), smem, st, args, tmk,
+  return launched(launch_pdl(attention_decode_kernel<HD, KV8>, dim3((unsigned)grid), dim3(DecLayout<HD, KV8>::kThreads),
+                             smem, st, args, tmk,
                              tmv, tmks, tmvs, (int)P),
                   "attention_decode_kernel");
 }
