@@ -1015,9 +1015,10 @@ def run_kernel_case(name: str, reps: int):
         pd = torch.from_numpy(np.concatenate(prompts).astype(np.int32)).to(dev)
         for _ in range(reps):
             ep.run(pd)
-    elif name == "c5_decode":
+    elif name in ("c5_decode", "c5_decode_fp8"):
         # long-context GQA decode steps (8 layers, d 2048, 64 sequences, contexts 1K-32K) after an
-        # untimed prefill; the decode launches sit in the NVTX range "decode"
+        # untimed prefill; the decode launches sit in the NVTX range "decode" (c5_decode_fp8: W8A8
+        # block-FP8 layers and the FP8 KV cache)
         from invariant_forward_policy_gb300.decoder import Decoder
         from synthetic import C5, make_c5_prompt_lengths, make_decoder_weights
         shape = C5["shape"]
@@ -1027,7 +1028,7 @@ def run_kernel_case(name: str, reps: int):
         max_ctx = int(lens.max()) + 1
         rng = np.random.default_rng(C5["seed"] + 3)
         prompts = [rng.integers(0, shape.vocab, int(n)).astype(np.int32) for n in lens]
-        dec = Decoder(shape, wb, max_pos=max_ctx + 64, device=dev)
+        dec = Decoder(shape, wb, max_pos=max_ctx + 64, device=dev, fp8=name == "c5_decode_fp8")
         mb = -(-max_ctx // 64)
         bt, nb = dec.paged_block_table([int(n) + 1 for n in lens], mb, seed=5)
         cache = dec.alloc_cache(nb)
@@ -1255,7 +1256,7 @@ def main():
                     help="run one kernel at its step shape (gemm_decode_qkv, gemm_decode_down, gemm_decode_lm_head, "
                          "lm_head_fused_decode, gemm_prefill, "
                          "attention_decode, attention_decode_long, attention_decode_long_fp8, gemm_fp8, topk_decode, ssd_prefill, "
-                         "kv_fp8_gather, c5_decode, c5_recompute, topk_prefill, attention_prefill_long, rmsnorm, "
+                         "kv_fp8_gather, c5_decode, c5_decode_fp8, c5_recompute, topk_prefill, attention_prefill_long, rmsnorm, "
                          "logprob, lm_head_fused, "
                          "moe_layer) or "
                          "the whole step (step, or fp8_step with the block-FP8 model) and exit; for profiling")
