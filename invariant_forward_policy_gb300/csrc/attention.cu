@@ -163,12 +163,36 @@ __device__ __forceinline__ float exp2_p(float x) {
   return y;
 }
 
-// S = Q K^T for the warp's 16 query rows and one 64-key tile (fp32, unscaled).
-template <int HD>
-__device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD / 16][4], int lane,
-                                            float (&sc)[8][4]) {
+// The warp's query rows: NH = 2 holds 16 rows per tile (thread (g, qd) rows g and
+// g + 8), NH = 1 only rows 0..7 (decode tiles of at most 8 rows: GQA group x
+// tokens).  At NH = 1 the m16n8k16 MMAs get zero A rows 8..15 and their D rows
+// 8..15 are discarded; a D element depends only on its own A row and B column, so
+// rows 0..7 are the same bits either way.
+template <int NH>
+__device__ __forceinline__ void mma_rows(float (&d)[2 * NH], const uint32_t (&a)[2 * NH], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (NH == 2) {
+    mma_bf16_16816(d, a, b0, b1);
+  } else {
+    float t2, t3;  // rows 8..15 of D: discarded
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%10,%11};"
+        : "+f"(d[0]), "+f"(d[1]), "=f"(t2), "=f"(t3)
+        : "r"(a[0]), "r"(0u), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f), "f"(0.f));
+  }
+}
+
+// S = Q K^T for the warp's query rows and one 64-key tile (fp32, unscaled).
+// qf[kk]: the rows' A fragment of head dims 16 kk .. 16 kk + 15 (h-th row half
+// at [h] for dims + 0..7 and at [NH + h] for dims + 8..15).
+template <int HD, int NH = 2>
+__device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD / 16][2 * NH], int lane,
+                                            float (&sc)[8][2 * NH]) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int c = 0; c < 2 * NH; ++c) sc[j][c] = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
 #pragma unroll
@@ -177,8 +201,8 @@ __device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD
       const int ch = kk * 2 + (lane >> 3);
       uint32_t b0, b1, b2, b3;
       ldsm_x4(sk + kv_off<HD>(key, ch), b0, b1, b2, b3);
-      mma_bf16_16816(sc[j], qf[kk], b0, b1);
-      mma_bf16_16816(sc[j], qf[kk + 1], b2, b3);
+      mma_rows<NH>(sc[j], qf[kk], b0, b1);
+      mma_rows<NH>(sc[j], qf[kk + 1], b2, b3);
     }
   }
 }
@@ -188,14 +212,15 @@ __device__ __forceinline__ void attn_scores(uint32_t sk, const uint32_t (&qf)[HD
 // vsm (FP8 cache only): the tile's V scales; P is then multiplied by its key's
 // scale before the bf16 rounding (exact: a power of two), so that P' V_codes has
 // the products P (V_codes scale) term for term.
-template <int HD>
-__device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int key0, const bool (&row_valid)[2],
+template <int HD, int NH = 2>
+__device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][2 * NH], int key0, const bool (&row_valid)[2],
                                             const int (&row_pos)[2], float scale_log2, int lane, float (&m)[2],
-                                            float (&l)[2], float (&acc)[HD / 8][4], const float* vsm = nullptr) {
+                                            float (&l)[2], float (&acc)[HD / 8][2 * NH],
+                                            const float* vsm = nullptr) {
   const int tq = lane & 3;
-  float pr[8][4];
+  float pr[8][2 * NH];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     float tmax = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -237,27 +262,29 @@ __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float2 vv = *reinterpret_cast<const float2*>(vsm + j * 8 + tq * 2);
-      pr[j][0] = __fmul_rn(pr[j][0], vv.x);
-      pr[j][1] = __fmul_rn(pr[j][1], vv.y);
-      pr[j][2] = __fmul_rn(pr[j][2], vv.x);
-      pr[j][3] = __fmul_rn(pr[j][3], vv.y);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        pr[j][h * 2] = __fmul_rn(pr[j][h * 2], vv.x);
+        pr[j][h * 2 + 1] = __fmul_rn(pr[j][h * 2 + 1], vv.y);
+      }
     }
   }
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {  // 64 keys = 4 k-steps of 16
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(pr[2 * kk][0], pr[2 * kk][1]);
-    pa[1] = pack_bf16x2(pr[2 * kk][2], pr[2 * kk][3]);
-    pa[2] = pack_bf16x2(pr[2 * kk + 1][0], pr[2 * kk + 1][1]);
-    pa[3] = pack_bf16x2(pr[2 * kk + 1][2], pr[2 * kk + 1][3]);
+    uint32_t pa[2 * NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      pa[h] = pack_bf16x2(pr[2 * kk][h * 2], pr[2 * kk][h * 2 + 1]);
+      pa[NH + h] = pack_bf16x2(pr[2 * kk + 1][h * 2], pr[2 * kk + 1][h * 2 + 1]);
+    }
 #pragma unroll
     for (int j = 0; j < HD / 8; j += 2) {
       const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
       const int ch = j + (lane >> 4);
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(sv + kv_off<HD>(key, ch), b0, b1, b2, b3);
-      mma_bf16_16816(acc[j], pa, b0, b1);
-      mma_bf16_16816(acc[j + 1], pa, b2, b3);
+      mma_rows<NH>(acc[j], pa, b0, b1);
+      mma_rows<NH>(acc[j + 1], pa, b2, b3);
     }
   }
 }
@@ -266,41 +293,43 @@ __device__ __forceinline__ void attn_update(uint32_t sv, float (&sc)[8][4], int 
 // ksm / vsm (FP8 cache only): the tile holds unscaled e4m3 values and these are
 // its per-key K and V scales.  A score column is multiplied by its key's K
 // scale: Q (codes x 2^k)^T = 2^k (Q codes^T) exactly.
-template <int HD>
-__device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][4],
+template <int HD, int NH = 2>
+__device__ __forceinline__ void attn_tile(uint32_t sk, uint32_t sv, int key0, const uint32_t (&qf)[HD / 16][2 * NH],
                                           const bool (&row_valid)[2], const int (&row_pos)[2], float scale_log2,
-                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][4],
+                                          int lane, float (&m)[2], float (&l)[2], float (&acc)[HD / 8][2 * NH],
                                           const float* ksm = nullptr, const float* vsm = nullptr) {
-  float sc[8][4];
-  attn_scores<HD>(sk, qf, lane, sc);
+  float sc[8][2 * NH];
+  attn_scores<HD, NH>(sk, qf, lane, sc);
   if (ksm) {
     const int tq = lane & 3;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float2 kk = *reinterpret_cast<const float2*>(ksm + j * 8 + tq * 2);
-      sc[j][0] = __fmul_rn(sc[j][0], kk.x);
-      sc[j][1] = __fmul_rn(sc[j][1], kk.y);
-      sc[j][2] = __fmul_rn(sc[j][2], kk.x);
-      sc[j][3] = __fmul_rn(sc[j][3], kk.y);
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        sc[j][h * 2] = __fmul_rn(sc[j][h * 2], kk.x);
+        sc[j][h * 2 + 1] = __fmul_rn(sc[j][h * 2 + 1], kk.y);
+      }
     }
   }
-  attn_update<HD>(sv, sc, key0, row_valid, row_pos, scale_log2, lane, m, l, acc, vsm);
+  attn_update<HD, NH>(sv, sc, key0, row_valid, row_pos, scale_log2, lane, m, l, acc, vsm);
 }
 
-// Per-thread state of one lane, as stored in shared memory between lanes.
-template <int HD>
+// Per-thread state of one lane (its NH row halves), as stored in shared memory
+// between lanes.
+template <int HD, int NH = 2>
 struct LaneState {
-  float m[2], l[2];
-  float acc[HD / 8][4];
+  float m[NH], l[NH];
+  float acc[HD / 8][2 * NH];
 };
 
-// P <- P (+) Q for the two rows a thread holds; an empty Q leaves P unchanged,
-// an empty P takes Q as it is.
-template <int HD>
-__device__ __forceinline__ void lane_merge(LaneState<HD>& P, const float (&mq)[2], const float (&lq)[2],
-                                           const float (&accq)[HD / 8][4]) {
+// P <- P (+) Q for the rows a thread holds; an empty Q leaves P unchanged, an
+// empty P takes Q as it is.
+template <int HD, int NH = 2>
+__device__ __forceinline__ void lane_merge(LaneState<HD, NH>& P, const float* mq, const float* lq,
+                                           const float (&accq)[HD / 8][2 * NH]) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     if (mq[h] == -INFINITY) continue;
     if (P.m[h] == -INFINITY) {
       P.m[h] = mq[h];
@@ -328,13 +357,13 @@ __device__ __forceinline__ void lane_merge(LaneState<HD>& P, const float (&mq)[2
   }
 }
 
-// Split partial of one row pair (the two rows a thread holds) to the workspace.
-template <int HD>
-__device__ __forceinline__ void write_partial(const AttnArgs& a, const LaneState<HD>& P, const bool (&row_valid)[2],
+// Split partial of the rows a thread holds to the workspace.
+template <int HD, int NH = 2>
+__device__ __forceinline__ void write_partial(const AttnArgs& a, const LaneState<HD, NH>& P, const bool (&row_valid)[2],
                                               const int (&row_pos)[2], const int (&row_tok)[2],
                                               const int (&row_head)[2], int kv_begin, int s, int tq) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     if (!row_valid[h] || row_pos[h] < kv_begin) continue;
     const int64_t pidx = ((int64_t)row_tok[h] * a.Hq + row_head[h]) * a.nsplit + s;
     float* po = a.part_o + pidx * HD;
@@ -346,17 +375,17 @@ __device__ __forceinline__ void write_partial(const AttnArgs& a, const LaneState
   }
 }
 
-// Query fragments (mma A layout) of the two rows a thread holds; zero for invalid rows.
-template <int HD>
+// Query fragments (mma A layout) of the rows a thread holds; zero for invalid rows.
+template <int HD, int NH = 2>
 __device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row_valid)[2], const int (&row_tok)[2],
-                                             const int (&row_head)[2], int tq, uint32_t (&qf)[HD / 16][4]) {
+                                             const int (&row_head)[2], int tq, uint32_t (&qf)[HD / 16][2 * NH]) {
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       const __nv_bfloat16* qr = a.q + ((int64_t)row_tok[h] * a.Hq + row_head[h]) * HD + kk * 16 + tq * 2;
       qf[kk][h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-      qf[kk][2 + h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+      qf[kk][NH + h] = row_valid[h] ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
     }
   }
 }
@@ -365,13 +394,13 @@ __device__ __forceinline__ void load_q_frags(const AttnArgs& a, const bool (&row
 // split 0 (P0) and split 1 (P1), with the split merge's arithmetic: M = max_s
 // m_s, then L and O summed over s = 0, 1 in that order (a row whose position
 // is before split 1 has only split 0), out = bf16(O / L).
-template <int HD>
-__device__ __forceinline__ void fused_split_merge(const AttnArgs& a, const LaneState<HD>& P0,
-                                                  const LaneState<HD>* P1, const bool (&row_valid)[2],
+template <int HD, int NH = 2>
+__device__ __forceinline__ void fused_split_merge(const AttnArgs& a, const LaneState<HD, NH>& P0,
+                                                  const LaneState<HD, NH>* P1, const bool (&row_valid)[2],
                                                   const int (&row_pos)[2], const int (&row_tok)[2],
                                                   const int (&row_head)[2], int tq) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < NH; ++h) {
     if (!row_valid[h]) continue;
     const int ns = merge_split_count(row_pos[h], a.split, a.nsplit, a.status, tq == 0);
     float M = fmaxf(-INFINITY, P0.m[h]);
@@ -421,9 +450,10 @@ struct Kv8Stage {
   static constexpr int kBytes = 2 * kCodes + 2 * kKeys * 4;  // K codes, V codes, K scales, V scales
 };
 
-template <int HD, bool DECODE, bool KV8, bool FUSED = false>
+template <int HD, bool DECODE, bool KV8, bool FUSED = false, int NH = 2>
 __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const AttnArgs a) {
   static_assert(!FUSED || DECODE, "the fused split merge is a decode schedule");
+  static_assert(NH == 2 || DECODE, "one row half only in decode tiles (at most 8 rows)");
   constexpr int CH = HD / 8;  // 16-byte chunks per key row
   constexpr int TILE_BYTES = kKeys * HD * 2;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
   const int s = FUSED ? (int)(threadIdx.x >> 7) : (int)blockIdx.z / a.Hkv;
   const int row0 = a.pm.row0[p];
   const int n_tok = a.pm.row0[p + 1] - row0;
-  const int tok_per_tile = (DECODE ? 16 : kRows) / a.group;
+  const int tok_per_tile = (DECODE ? 8 * NH : kRows) / a.group;
   const int tok0 = blockIdx.x * tok_per_tile;
   if (tok0 >= n_tok) return;
   const int pos_first = a.pm.pos0[p];
@@ -460,13 +490,13 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
   for (int h = 0; h < 2; ++h) {
     const int r = (DECODE ? 0 : warp * 16) + g + h * 8;
     const int ti = tok0 + r / a.group;
-    row_valid[h] = ti < n_tok && (r / a.group) < tok_per_tile;
+    row_valid[h] = h < NH && ti < n_tok && (r / a.group) < tok_per_tile;
     row_tok[h] = row0 + ti;
     row_pos[h] = pos_first + ti;
     row_head[h] = kvh * a.group + (r % a.group);
   }
-  uint32_t qf[HD / 16][4];
-  load_q_frags<HD>(a, row_valid, row_tok, row_head, tq, qf);
+  uint32_t qf[HD / 16][2 * NH];
+  load_q_frags<HD, NH>(a, row_valid, row_tok, row_head, tq, qf);
 
   // copy one 64-key tile of K and V into (sk, sv) with threads t0, t0 + nthr, ...;
   // keys after max_pos are zero-filled.  nthr is a compile-time constant
@@ -547,17 +577,24 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
 
   float m[2] = {-INFINITY, -INFINITY};
   float l[2] = {0.f, 0.f};
-  float acc[HD / 8][4];
+  float acc[HD / 8][2 * NH];
 #pragma unroll
-  for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-  LaneState<HD> P;
-  P.m[0] = P.m[1] = -INFINITY;
-  P.l[0] = P.l[1] = 0.f;
+  for (int j = 0; j < HD / 8; ++j)
 #pragma unroll
-  for (int j = 0; j < HD / 8; ++j) P.acc[j][0] = P.acc[j][1] = P.acc[j][2] = P.acc[j][3] = 0.f;
+    for (int c = 0; c < 2 * NH; ++c) acc[j][c] = 0.f;
 
-  if (DECODE) {
+  LaneState<HD, NH> P;
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    P.m[h] = -INFINITY;
+    P.l[h] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < HD / 8; ++j)
+#pragma unroll
+    for (int c = 0; c < 2 * NH; ++c) P.acc[j][c] = 0.f;
+
+  if constexpr (DECODE) {
     // ---- lane `warp` (FUSED: lane warp % 4 of split warp / 4), from this warp's own one-tile buffer
     constexpr int kWarps = FUSED ? 8 : 4;
     uint8_t* sk = smem + warp * 2 * TILE_BYTES;
@@ -576,42 +613,44 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
         cp_async_wait<0>();
       }
       __syncwarp();
-      attn_tile<HD>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
-                    KV8 ? stage_ks(stg) : nullptr, KV8 ? stage_ks(stg) + kKeys : nullptr);
+      attn_tile<HD, NH>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
+                        KV8 ? stage_ks(stg) : nullptr, KV8 ? stage_ks(stg) + kKeys : nullptr);
       __syncwarp();
     }
     // lanes meet in shared memory (each warp reuses its buffer); warp 0 merges 0..3
-    LaneState<HD>* st = reinterpret_cast<LaneState<HD>*>(smem + warp * 2 * TILE_BYTES) + lane;
+    LaneState<HD, NH>* st = reinterpret_cast<LaneState<HD, NH>*>(smem + warp * 2 * TILE_BYTES) + lane;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NH; ++h) {
       st->m[h] = m[h];
       st->l[h] = l[h];
     }
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) st->acc[j][c] = acc[j][c];
+      for (int c = 0; c < 2 * NH; ++c) st->acc[j][c] = acc[j][c];
     __syncthreads();
     if constexpr (FUSED) {
       // warps 0 and 4 fold the lanes of splits 0 and 1; warp 4 leaves its partial in its buffer
       if ((warp & 3) == 0 && split_live) {
         const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
         for (int w = 0; w < n_lanes; ++w) {
-          const LaneState<HD>* q = reinterpret_cast<const LaneState<HD>*>(smem + (warp + w) * 2 * TILE_BYTES) + lane;
-          lane_merge<HD>(P, q->m, q->l, q->acc);
+          const LaneState<HD, NH>* q =
+              reinterpret_cast<const LaneState<HD, NH>*>(smem + (warp + w) * 2 * TILE_BYTES) + lane;
+          lane_merge<HD, NH>(P, q->m, q->l, q->acc);
         }
-        if (warp == 4) *(reinterpret_cast<LaneState<HD>*>(smem + 4 * 2 * TILE_BYTES) + lane) = P;
+        if (warp == 4) *(reinterpret_cast<LaneState<HD, NH>*>(smem + 4 * 2 * TILE_BYTES) + lane) = P;
       }
       __syncthreads();
-      if (warp == 0) fused_split_merge<HD>(a, P, reinterpret_cast<const LaneState<HD>*>(smem + 4 * 2 * TILE_BYTES) + lane,
-                                           row_valid, row_pos, row_tok, row_head, tq);
+      if (warp == 0)
+        fused_split_merge<HD, NH>(a, P, reinterpret_cast<const LaneState<HD, NH>*>(smem + 4 * 2 * TILE_BYTES) + lane,
+                                  row_valid, row_pos, row_tok, row_head, tq);
       return;
     }
     if (warp != 0) return;
     const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
     for (int w = 0; w < n_lanes; ++w) {
-      const LaneState<HD>* q = reinterpret_cast<const LaneState<HD>*>(smem + w * 2 * TILE_BYTES) + lane;
-      lane_merge<HD>(P, q->m, q->l, q->acc);
+      const LaneState<HD, NH>* q = reinterpret_cast<const LaneState<HD, NH>*>(smem + w * 2 * TILE_BYTES) + lane;
+      lane_merge<HD, NH>(P, q->m, q->l, q->acc);
     }
   } else {
     // ---- all warps share a two-stage ring; lanes are walked in order
@@ -663,7 +702,7 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
     P = *run;
     lane_merge<HD>(P, m, l, acc);
   }
-  write_partial<HD>(a, P, row_valid, row_pos, row_tok, row_head, kv_begin, s, tq);
+  write_partial<HD, NH>(a, P, row_valid, row_pos, row_tok, row_head, kv_begin, s, tq);
 }
 
 // ------------------------------------------------- tensor-memory prefill schedule
@@ -1194,7 +1233,7 @@ constexpr int kDecPersistentSplits = 4;  // shorter contexts take the per-CTA sc
 // reads), rows and scales after the item's last position zero.  The consumer
 // runs the bf16 schedule on that page with the scales applied.  Each ring
 // involves one loader warp and one consumer warp only.
-template <int HD, bool KV8 = false>
+template <int HD, bool KV8 = false, int NH = 2>
 struct DecLayout {
   static constexpr int kThreads = KV8 ? 256 : 160;  // consumers, then producer (KV8: four loaders)
   // bf16 ring depth per consumer warp: three slots at hd 128 (one CTA per SM);
@@ -1209,7 +1248,7 @@ struct DecLayout {
   static constexpr int kScales = kRing;                              // KV8: [4][kDecSlots][64] fp32
   static constexpr int kCodeRing = kScales + (KV8 ? 4 * kDecSlots * kKeys * 4 : 0);  // KV8: [4][2] code slots
   static constexpr int kStates = kCodeRing + (KV8 ? 4 * kCodeSlots * kCodeSlot : 0);  // lane states of warps 1..3
-  static constexpr int kTable = kStates + 3 * 32 * (int)sizeof(LaneState<HD>);  // int [kDecMaxPieces + 1]
+  static constexpr int kTable = kStates + 3 * 32 * (int)sizeof(LaneState<HD, NH>);  // int [kDecMaxPieces + 1]
   static constexpr int kBars = kTable + (kDecMaxPieces + 2) * 4;
   // full[4][S] (bf16: TMA -> consumer; KV8: code TMA -> loader, [4][2]), empty[4][S]
   // (consumer -> producer / loader), KV8 conv[4][S] (loader -> consumer)
@@ -1302,12 +1341,12 @@ struct DecCodes {
   }
 };
 
-template <int HD, bool KV8>
-__global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV8) ? 2 : 1)
+template <int HD, bool KV8, int NH>
+__global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 && !KV8) ? 2 : 1)
     attention_decode_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmks,
                             const __grid_constant__ CUtensorMap tmvs, int P) {
-  using Lay = DecLayout<HD, KV8>;
+  using Lay = DecLayout<HD, KV8, NH>;
   constexpr int kDecSlots = Lay::kDecSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1531,7 +1570,7 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, tq = lane & 3;
-  LaneState<HD>* states = reinterpret_cast<LaneState<HD>*>(smem + Lay::kStates);  // [3][32]
+  LaneState<HD, NH>* states = reinterpret_cast<LaneState<HD, NH>*>(smem + Lay::kStates);  // [3][32]
   int used = 0;  // objects taken from this warp's ring
   bool handed = false;
   DecItem nxt;
@@ -1542,44 +1581,47 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV
     if (item + (int)gridDim.x < n_items) nxt = dec_item(a, first, item + gridDim.x, P);
     int row_pos[2], row_tok[2], row_head[2];
     bool row_valid[2];
-    const int tok_per_tile = 16 / a.group;
+    const int tok_per_tile = 8 * NH / a.group;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < 2; ++h) {  // (row half 1 is empty at NH = 1)
       const int r = g + h * 8;
       const int ti = r / a.group;
-      row_valid[h] = ti < it.n_tok && (r / a.group) < tok_per_tile;
+      row_valid[h] = h < NH && ti < it.n_tok && ti < tok_per_tile;
       row_tok[h] = it.row0 + ti;
       row_pos[h] = it.pos_first + ti;
       row_head[h] = it.kvh * a.group + (r % a.group);
     }
-    uint32_t qf[HD / 16][4];
-    load_q_frags<HD>(a, row_valid, row_tok, row_head, tq, qf);
+    uint32_t qf[HD / 16][2 * NH];
+    load_q_frags<HD, NH>(a, row_valid, row_tok, row_head, tq, qf);
     float m[2] = {-INFINITY, -INFINITY};
     float l[2] = {0.f, 0.f};
-    float acc[HD / 8][4];
+    float acc[HD / 8][2 * NH];
 #pragma unroll
-    for (int j = 0; j < HD / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int j = 0; j < HD / 8; ++j)
+#pragma unroll
+      for (int c = 0; c < 2 * NH; ++c) acc[j][c] = 0.f;
 
     const int lb = it.kv_begin + warp * lane_len;
     const int le = min(lb + lane_len, it.kv_end);
     for (int key0 = lb; key0 < le; key0 += kKeys) {
-      float sc[8][4];
+      float sc[8][2 * NH];
       const int n_keys = it.kv_end - key0;  // keys of this page at or before max_pos
       // K page
       int slot = warp * kDecSlots + used % kDecSlots;
       // decided for the whole warp: ldmatrix and mma.sync below are warp-collective
       bool ok = __all_sync(0xffffffffu, dec_wait(&ready[slot], (used / kDecSlots) & 1, abort_flag, a.status));
       if (ok) {
-        attn_scores<HD>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
+        attn_scores<HD, NH>(smem_u32(smem + slot * Lay::kTile), qf, lane, sc);
         if (KV8) {  // a score column times its key's K scale
           const float* ks = scl + slot * kKeys;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float2 kk = *reinterpret_cast<const float2*>(ks + j * 8 + tq * 2);
-            sc[j][0] = __fmul_rn(sc[j][0], kk.x);
-            sc[j][1] = __fmul_rn(sc[j][1], kk.y);
-            sc[j][2] = __fmul_rn(sc[j][2], kk.x);
-            sc[j][3] = __fmul_rn(sc[j][3], kk.y);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+              sc[j][h * 2] = __fmul_rn(sc[j][h * 2], kk.x);
+              sc[j][h * 2 + 1] = __fmul_rn(sc[j][h * 2 + 1], kk.y);
+            }
           }
         }
       }
@@ -1598,8 +1640,8 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV
           }
           __syncwarp();
         }
-        attn_update<HD>(smem_u32(sv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
-                        KV8 ? scl + slot * kKeys : nullptr);
+        attn_update<HD, NH>(smem_u32(sv), sc, key0, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
+                            KV8 ? scl + slot * kKeys : nullptr);
         if (!KV8) fence_proxy_async();  // generic writes above before the next TMA write of this slot
       }
       __syncwarp();
@@ -1610,33 +1652,38 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8>::kThreads, (HD == 64 && !KV
     // lanes meet: warps 1..3 hand over, warp 0 merges in lane order
     if (warp != 0) {
       if (handed) named_bar_sync(2, 128);  // warp 0 has read the previous item's states
-      LaneState<HD>* st = states + (warp - 1) * 32 + lane;
+      LaneState<HD, NH>* st = states + (warp - 1) * 32 + lane;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NH; ++h) {
         st->m[h] = m[h];
         st->l[h] = l[h];
       }
 #pragma unroll
       for (int j = 0; j < HD / 8; ++j)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) st->acc[j][c] = acc[j][c];
+        for (int c = 0; c < 2 * NH; ++c) st->acc[j][c] = acc[j][c];
       named_bar_arrive(1, 128);
       handed = true;
     } else {
-      LaneState<HD> Pm;
-      Pm.m[0] = Pm.m[1] = -INFINITY;
-      Pm.l[0] = Pm.l[1] = 0.f;
+      LaneState<HD, NH> Pm;
 #pragma unroll
-      for (int j = 0; j < HD / 8; ++j) Pm.acc[j][0] = Pm.acc[j][1] = Pm.acc[j][2] = Pm.acc[j][3] = 0.f;
-      lane_merge<HD>(Pm, m, l, acc);
+      for (int h = 0; h < NH; ++h) {
+        Pm.m[h] = -INFINITY;
+        Pm.l[h] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < HD / 8; ++j)
+#pragma unroll
+        for (int c = 0; c < 2 * NH; ++c) Pm.acc[j][c] = 0.f;
+      lane_merge<HD, NH>(Pm, m, l, acc);
       named_bar_sync(1, 128);
 #pragma unroll 1
       for (int w = 1; w < 4; ++w) {
-        const LaneState<HD>* q = states + (w - 1) * 32 + lane;
-        lane_merge<HD>(Pm, q->m, q->l, q->acc);
+        const LaneState<HD, NH>* q = states + (w - 1) * 32 + lane;
+        lane_merge<HD, NH>(Pm, q->m, q->l, q->acc);
       }
       named_bar_arrive(2, 128);
-      write_partial<HD>(a, Pm, row_valid, row_pos, row_tok, row_head, it.kv_begin, it.s, tq);
+      write_partial<HD, NH>(a, Pm, row_valid, row_pos, row_tok, row_head, it.kv_begin, it.s, tq);
     }
   }
   if (warp != 0 && handed) named_bar_sync(2, 128);  // pairs with warp 0's last hand-back
@@ -1747,19 +1794,20 @@ constexpr int attn_smem_bytes() {
                       (KV8 ? 2 * Kv8Stage<HD>::kBytes : 0);
 }
 
-template <int HD, bool DECODE, bool KV8, bool FUSED = false>
+template <int HD, bool DECODE, bool KV8, bool FUSED = false, int NH = 2>
 static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t st) {
   constexpr int smem = attn_smem_bytes<HD, DECODE, KV8, FUSED>();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attention_kernel<HD, DECODE, KV8, FUSED>,
+    attr_err = cudaFuncSetAttribute(attention_kernel<HD, DECODE, KV8, FUSED, NH>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention smem attribute: ") + cudaGetErrorString(attr_err));
-  return launched(launch_pdl(attention_kernel<HD, DECODE, KV8, FUSED>, grid, dim3(FUSED ? 256 : 128), smem, st, args),
-                  "attention_kernel");
+  return launched(
+      launch_pdl(attention_kernel<HD, DECODE, KV8, FUSED, NH>, grid, dim3(FUSED ? 256 : 128), smem, st, args),
+      "attention_kernel");
 }
 
 // Persistent decode launch: as many CTAs as fit on the GPU at once (at most
@@ -1767,18 +1815,18 @@ static bi_status launch_attention(const AttnArgs& args, dim3 grid, cudaStream_t 
 // * 64 rows, hd] read in 64 x 64 boxes with 128-byte swizzle; an FP8 cache as
 // code rows [n_blocks * Hkv * 64, hd bytes] read in 64-row boxes and scale rows
 // [n_blocks * Hkv, 256 bytes] read one row per page, both unswizzled.
-template <int HD, bool KV8>
+template <int HD, bool KV8, int NH>
 static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaStream_t st) {
-  constexpr int smem = DecLayout<HD, KV8>::kBytes;
+  constexpr int smem = DecLayout<HD, KV8, NH>::kBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int per_sm = 1;
   std::call_once(once, [] {
     attr_err =
-        cudaFuncSetAttribute(attention_decode_kernel<HD, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(attention_decode_kernel<HD, KV8, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8>,
-                                                               DecLayout<HD, KV8>::kThreads, smem);
+      attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8, NH>,
+                                                               DecLayout<HD, KV8, NH>::kThreads, smem);
     if (per_sm < 1) per_sm = 1;
   });
   if (attr_err != cudaSuccess)
@@ -1799,7 +1847,7 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
   }
   if (!ok) return fail(BI_ERR_CUDA, "attention decode: cuTensorMapEncodeTiled failed for the K/V cache");
   const int64_t grid = std::min<int64_t>(P * args.Hkv * args.nsplit, (int64_t)num_sms() * per_sm);
-  return launched(launch_pdl(attention_decode_kernel<HD, KV8>, dim3((unsigned)grid), dim3(DecLayout<HD, KV8>::kThreads),
+  return launched(launch_pdl(attention_decode_kernel<HD, KV8, NH>, dim3((unsigned)grid), dim3(DecLayout<HD, KV8, NH>::kThreads),
                              smem, st, args, tmk,
                              tmv, tmks, tmvs, (int)P),
                   "attention_decode_kernel");
@@ -1961,26 +2009,46 @@ static bi_status attention_impl(const void* q, int64_t T, const int32_t* piece_s
   // tiles take the tensor-memory prefill schedule (bf16 caches) or the
   // mma.sync row-parallel one (FP8 caches).
   const bool decode = max_q_len * group <= 16;
+  // decode tiles of at most 8 query rows (GQA group x tokens) keep one row half
+  // of the 16-row MMA tiles: the same bits, half the softmax and state work
+  const bool half = max_q_len * group <= 8;
   args.out = static_cast<__nv_bfloat16*>(out);
   if (decode && ns <= 2 && hd == 64 && out && !out_q) {
     // short contexts: both splits in one CTA, merged there (no partials, no merge kernel)
     dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)Hkv);
+    if (half)
+      return kv8 ? launch_attention<64, true, true, true, 1>(args, grid, st)
+                 : launch_attention<64, true, false, true, 1>(args, grid, st);
     return kv8 ? launch_attention<64, true, true, true>(args, grid, st)
                : launch_attention<64, true, false, true>(args, grid, st);
   }
   if (decode && ns > kDecPersistentSplits && P <= kDecMaxPieces) {
     BI_REQUIRE(P * Hkv * ns < (int64_t(1) << 31), "too many attention work items");
-    if (kv8)
-      BI_TRY(hd == 64 ? launch_attention_decode<64, true>(args, P, st)
-                      : launch_attention_decode<128, true>(args, P, st));
+    // tiles of at most 8 query rows (GQA group x tokens) keep one row half
+    const bool half = max_q_len * group <= 8;
+    if (kv8 && half)
+      BI_TRY(hd == 64 ? launch_attention_decode<64, true, 1>(args, P, st)
+                      : launch_attention_decode<128, true, 1>(args, P, st));
+    else if (kv8)
+      BI_TRY(hd == 64 ? launch_attention_decode<64, true, 2>(args, P, st)
+                      : launch_attention_decode<128, true, 2>(args, P, st));
+    else if (half)
+      BI_TRY(hd == 64 ? launch_attention_decode<64, false, 1>(args, P, st)
+                      : launch_attention_decode<128, false, 1>(args, P, st));
     else
-      BI_TRY(hd == 64 ? launch_attention_decode<64, false>(args, P, st)
-                      : launch_attention_decode<128, false>(args, P, st));
+      BI_TRY(hd == 64 ? launch_attention_decode<64, false, 2>(args, P, st)
+                      : launch_attention_decode<128, false, 2>(args, P, st));
   } else if (decode) {
     dim3 grid((unsigned)cdiv(max_q_len * group, 16), (unsigned)P, (unsigned)(Hkv * ns));
-    if (kv8)
+    if (kv8 && half)
+      BI_TRY(hd == 64 ? launch_attention<64, true, true, false, 1>(args, grid, st)
+                      : launch_attention<128, true, true, false, 1>(args, grid, st));
+    else if (kv8)
       BI_TRY(hd == 64 ? launch_attention<64, true, true>(args, grid, st)
                       : launch_attention<128, true, true>(args, grid, st));
+    else if (half)
+      BI_TRY(hd == 64 ? launch_attention<64, true, false, false, 1>(args, grid, st)
+                      : launch_attention<128, true, false, false, 1>(args, grid, st));
     else
       BI_TRY(hd == 64 ? launch_attention<64, true, false>(args, grid, st)
                       : launch_attention<128, true, false>(args, grid, st));
