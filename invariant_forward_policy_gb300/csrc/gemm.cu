@@ -61,6 +61,19 @@ struct GemmSmem {
   static constexpr int kBytes = 1024 + kStages * kStageBytes + 256;
 };
 
+// The fused log-softmax at 64 and 128 columns keeps two staging buffers of a
+// 16-row tile ([16][BN + 4] fp32 each) for tiles of at most 16 rows.
+template <int BN, int EPI>
+struct LseStage {
+  static constexpr bool kOn = EPI == 5 && (BN == 64 || BN == 128);  // EPI_LSE
+  static constexpr int kFloats = 16 * (BN + 4);
+  static constexpr int kBytes = kOn ? 2 * kFloats * 4 : 0;
+};
+template <int BN, int EPI>
+constexpr int gemm_tc_smem() {
+  return GemmSmem<BN>::kBytes + LseStage<BN, EPI>::kBytes;
+}
+
 struct GemmArgs {
   void* C;
   float* partial;           // split-K partials [splits, M, ldp]
@@ -105,6 +118,130 @@ __device__ __forceinline__ void tile_lse_step4(float& m, float& s, float& best, 
   if (x1 > best) { best = x1; idx = col + 1; }
   if (x2 > best) { best = x2; idx = col + 2; }
   if (x3 > best) { best = x3; idx = col + 3; }
+}
+
+// The same (max, sum-exp, argmax) record of one tile row, with the row's BN
+// logits staged in shared memory and shared by 8 threads (16-row tiles: 128
+// threads).  Each thread takes BN/8 consecutive columns.  The running max after
+// each 4-column group is a prefix max (order-free), so every exponential and
+// every rescale factor of the column-order recurrence is computed in parallel;
+// only the fp32 fold of s is sequential, carried from chunk to chunk by
+// shuffles, with the recurrence's operations in its order (s reset to 0 when the
+// running max was -inf, s * expf(m - mx) when a group raises it, then its four
+// terms added in column order).  The argmax of a later chunk replaces that of an
+// earlier one only when strictly greater, as the sequential scan does.  So the
+// record equals tile_lse_step4's over the row, bit for bit.
+constexpr int kLseSmallRows = 16;
+template <int BN>
+__device__ __forceinline__ void lse_small_tile_row(const GemmArgs& args, const float* stg, int m_tile, int n_tile,
+                                                   int u, bool do_store) {
+  constexpr int CPC = BN / 8;  // columns per chunk
+  constexpr int G = CPC / 4;   // 4-column groups per chunk
+  const int r = u >> 3, k = u & 7;
+  const int row = m_tile * kBM + r;
+  const bool row_ok = row < args.M;
+  const int n0 = n_tile * BN, c0 = n0 + k * CPC;
+  float x[CPC];
+#pragma unroll
+  for (int i = 0; i < CPC; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(stg + r * (BN + 4) + k * CPC + i);
+    x[i] = v.x;
+    x[i + 1] = v.y;
+    x[i + 2] = v.z;
+    x[i + 3] = v.w;
+  }
+  bool gv[G];
+  float gm[G];
+  float cm = -INFINITY;  // this chunk's max over its groups
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    gv[g] = c0 + 4 * g < args.n_out;
+    gm[g] = fmaxf(fmaxf(x[4 * g], x[4 * g + 1]), fmaxf(x[4 * g + 2], x[4 * g + 3]));
+    if (gv[g]) cm = fmaxf(cm, gm[g]);
+  }
+  // the running max entering this chunk: max over the row's earlier chunks
+  float incl = cm;
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    const float v = __shfl_up_sync(0xffffffffu, incl, d, 8);
+    if (k >= d) incl = fmaxf(incl, v);
+  }
+  float m = __shfl_up_sync(0xffffffffu, incl, 1, 8);
+  if (k == 0) m = -INFINITY;
+  // per group: does it raise the max, from -inf, the rescale factor, the terms
+  bool up[G], from_inf[G];
+  float rs[G], e[CPC];
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    up[g] = false;
+    from_inf[g] = false;
+    rs[g] = 1.f;
+    if (!gv[g]) continue;
+    if (gm[g] > m) {
+      up[g] = true;
+      from_inf[g] = m == -INFINITY;
+      if (!from_inf[g]) rs[g] = expf(__fsub_rn(m, gm[g]));
+      m = gm[g];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e[4 * g + i] = expf(__fsub_rn(x[4 * g + i], m));
+      if (x[4 * g + i] > best) {
+        best = x[4 * g + i];
+        idx = c0 + 4 * g + i;
+      }
+    }
+  }
+  // the fold of s, chunk after chunk
+  float s_out = 0.f;
+#pragma unroll 1
+  for (int step = 0; step < 8; ++step) {
+    const float s_in = __shfl_up_sync(0xffffffffu, s_out, 1, 8);
+    if (k == step) {
+      float s = k == 0 ? 0.f : s_in;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (!gv[g]) continue;
+        if (up[g]) s = from_inf[g] ? 0.f : __fmul_rn(s, rs[g]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s = __fadd_rn(s, e[4 * g + i]);
+      }
+      s_out = s;
+    }
+  }
+  // argmax over the chunks in order: a later chunk wins only when strictly greater
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    const float vb = __shfl_up_sync(0xffffffffu, best, d, 8);
+    const int vi = __shfl_up_sync(0xffffffffu, idx, d, 8);
+    if (k >= d && !(best > vb)) {
+      best = vb;
+      idx = vi;
+    }
+  }
+  // the target's logit, from the chunk that holds it
+  const int tgt = (row_ok && args.ids) ? args.ids[row] : -1;
+  const int off = tgt - n0;
+  float xt = __int_as_float(0x7fc00000);
+  if (off >= 0 && off < BN && off / CPC == k) {
+#pragma unroll
+    for (int i = 0; i < CPC; ++i)
+      if (i == off - k * CPC) xt = x[i];
+  }
+  const int owner = (off >= 0 && off < BN) ? off / CPC : 7;
+  const float xt_row = __shfl_sync(0xffffffffu, xt, (threadIdx.x & 24) + owner);
+  if (k == 7 && do_store && row_ok) {
+    TileLse t;
+    t.m = incl;
+    t.s = s_out;
+    t.best = best;
+    t.xt = xt_row;
+    t.idx = idx;
+    t.pad[0] = t.pad[1] = t.pad[2] = 0;
+    args.lse[(size_t)row * args.n_tiles + n_tile] = t;
+  }
 }
 
 __device__ __forceinline__ float silu_f(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g))); }
@@ -373,6 +510,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA (4 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* lse_ready = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // [2] LseStage: a 16-row tile is staged
+  float* lse_stage = reinterpret_cast<float*>(sB + kStages * S::kBTileBytes + 256);  // LseStage only
+  static_assert((2 * kStages + 4) * 8 + 8 + 16 <= 256, "barrier area");
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -388,6 +528,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
+      if (LseStage<BN, EPI>::kOn) mbar_init(&lse_ready[b], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -534,8 +675,49 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         break;
       }
       const int row = tc.m_tile * kBM + q * 32 + lane;
-      epilogue_tile<BN, EPI>(args, tmem_base + b * BN + ((uint32_t)(q * 32) << 16), row, row < args.M,
-                             !*abort_flag, tc.n_tile, tc.split);
+      bool small = false;
+      if constexpr (LseStage<BN, EPI>::kOn) {
+        small = args.M - tc.m_tile * kBM <= kLseSmallRows;
+        if (small) {
+          // a tile of at most 16 rows: TMEM lanes 0..15 staged by warp q = 0, then all
+          // four epilogue warps (8 threads per row) form the rows' records
+          float* stg = lse_stage + b * LseStage<BN, EPI>::kFloats;
+          if (q == 0) {
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(tmem_base + b * BN + c, r);
+              tmem_ld_wait();
+              if (lane < kLseSmallRows) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                  *reinterpret_cast<float4*>(stg + lane * (BN + 4) + c + i) =
+                      make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                  __uint_as_float(r[i + 3]));
+              }
+            }
+          }
+          // the other warps wait for the staged rows (bounded; a stage buffer is
+          // rewritten only after every epilogue warp has released its accumulator)
+          bool staged = true;
+          if (q == 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&lse_ready[b]);
+          } else {
+            staged = __all_sync(0xffffffffu, mbar_wait(&lse_ready[b], bph));
+            if (!staged) {
+              report(args.status, DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+          }
+          if (staged)
+            lse_small_tile_row<BN>(args, stg, tc.m_tile, tc.n_tile, (warp - 2) * 32 + lane, !*abort_flag);
+        }
+      }
+      if (!small) {
+        epilogue_tile<BN, EPI>(args, tmem_base + b * BN + ((uint32_t)(q * 32) << 16), row, row < args.M,
+                               !*abort_flag, tc.n_tile, tc.split);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
@@ -843,7 +1025,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
 template <int BN, int EPI>
 static bi_status launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmArgs& args,
                            dim3 grid, cudaStream_t st) {
-  constexpr int smem = GemmSmem<BN>::kBytes;
+  constexpr int smem = gemm_tc_smem<BN, EPI>();
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
