@@ -450,6 +450,11 @@ struct Kv8Stage {
   static constexpr int kBytes = 2 * kCodes + 2 * kKeys * 4;  // K codes, V codes, K scales, V scales
 };
 
+// Decode schedules: 64-key tiles of shared memory per warp (bf16 caches: a
+// three-tile K/V ring; FP8 caches: the expanded K and V of one page).
+template <bool KV8>
+constexpr int kDecWarpTiles = KV8 ? 2 : 3;
+
 template <int HD, bool DECODE, bool KV8, bool FUSED = false, int NH = 2>
 __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const AttnArgs a) {
   static_assert(!FUSED || DECODE, "the fused split merge is a decode schedule");
@@ -518,6 +523,26 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
       const int64_t src = base + (int64_t)key * HD + ch * 8;
       cp_async16(sk + off, a.k_cache + (valid ? src : 0), valid);
       cp_async16(sv + off, a.v_cache + (valid ? src : 0), valid);
+    }
+    cp_async_commit();
+  };
+
+  // one 64-key tile of K (v false) or V into dst (bf16 decode ring), as load_tile
+  auto load_one = [&](int key0, uint8_t* dst, bool v, int t0, auto nthr_c) {
+    constexpr int nthr = decltype(nthr_c)::value;
+    const bool tab_ok = key0 / kKeys < a.max_blk;
+    const int32_t blk = tab_ok ? bt[key0 / kKeys] : -1;
+    const bool blk_ok = blk >= 0 && blk < a.n_blocks;
+    if (!blk_ok && t0 == 0) report(a.status, DEV_BAD_INDEX);
+    const int64_t base = ((int64_t)(blk_ok ? blk : 0) * a.Hkv + kvh) * kKeys * HD;
+    const __nv_bfloat16* cache = v ? a.v_cache : a.k_cache;
+#pragma unroll
+    for (int i = 0; i < kKeys * CH / nthr; ++i) {
+      const int c = t0 + i * nthr;
+      const int key = c / CH, ch = c % CH;
+      const bool valid = blk_ok && (key0 + key) <= max_pos;
+      const int64_t src = base + (int64_t)key * HD + ch * 8;
+      cp_async16(dst + kv_off<HD>(key, ch), cache + (valid ? src : 0), valid);
     }
     cp_async_commit();
   };
@@ -595,30 +620,48 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
     for (int c = 0; c < 2 * NH; ++c) P.acc[j][c] = 0.f;
 
   if constexpr (DECODE) {
-    // ---- lane `warp` (FUSED: lane warp % 4 of split warp / 4), from this warp's own one-tile buffer
+    // ---- lane `warp` (FUSED: lane warp % 4 of split warp / 4), from this warp's own buffers
     constexpr int kWarps = FUSED ? 8 : 4;
-    uint8_t* sk = smem + warp * 2 * TILE_BYTES;
-    uint8_t* sv = sk + TILE_BYTES;
+    constexpr int kRegion = kDecWarpTiles<KV8> * TILE_BYTES;  // this warp's shared memory
     const int lb = kv_begin + (warp & 3) * lane_len;
     const int le = split_live ? min(lb + lane_len, kv_end) : lb;
-    uint8_t* stg = smem + kWarps * 2 * TILE_BYTES + warp * Kv8Stage<HD>::kBytes;  // KV8 only
-    for (int key0 = lb; key0 < le; key0 += kKeys) {
-      if constexpr (KV8) {
+    if constexpr (KV8) {
+      uint8_t* sk = smem + warp * kRegion;
+      uint8_t* sv = sk + TILE_BYTES;
+      uint8_t* stg = smem + kWarps * kRegion + warp * Kv8Stage<HD>::kBytes;
+      for (int key0 = lb; key0 < le; key0 += kKeys) {
         load_tile8(key0, stg, lane, kThr32);
         cp_async_wait<0>();
         __syncwarp();
         expand_tile8(key0, stg, sk, sv, lane, kThr32);
-      } else {
-        load_tile(key0, sk, sv, lane, kThr32);
-        cp_async_wait<0>();
+        __syncwarp();
+        attn_tile<HD, NH>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
+                          stage_ks(stg), stage_ks(stg) + kKeys);
+        __syncwarp();
       }
-      __syncwarp();
-      attn_tile<HD, NH>(smem_u32(sk), smem_u32(sv), key0, qf, row_valid, row_pos, a.scale_log2, lane, m, l, acc,
-                        KV8 ? stage_ks(stg) : nullptr, KV8 ? stage_ks(stg) + kKeys : nullptr);
-      __syncwarp();
+    } else {
+      // the lane's tiles K, V of each page in turn, tile j in buffer j % 3: two tiles
+      // are in flight while one is used, and a buffer is refilled once it is read
+      uint8_t* buf = smem + warp * kRegion;
+      const int n_t = le > lb ? 2 * ((le - lb + kKeys - 1) / kKeys) : 0;
+      auto issue = [&](int j) { load_one(lb + (j >> 1) * kKeys, buf + (j % 3) * TILE_BYTES, j & 1, lane, kThr32); };
+      for (int j = 0; j < 3 && j < n_t; ++j) issue(j);
+      float sc[8][2 * NH];
+      for (int j = 0; j < n_t; ++j) {
+        const int ahead = min(n_t, j + 3) - (j + 1);  // copy groups issued after tile j
+        if (ahead >= 2) cp_async_wait<2>();
+        else if (ahead == 1) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncwarp();
+        const uint32_t t = smem_u32(buf + (j % 3) * TILE_BYTES);
+        if ((j & 1) == 0) attn_scores<HD, NH>(t, qf, lane, sc);
+        else attn_update<HD, NH>(t, sc, lb + (j >> 1) * kKeys, row_valid, row_pos, a.scale_log2, lane, m, l, acc);
+        __syncwarp();  // every lane has read tile j before its buffer takes tile j + 3
+        if (j + 3 < n_t) issue(j + 3);
+      }
     }
-    // lanes meet in shared memory (each warp reuses its buffer); warp 0 merges 0..3
-    LaneState<HD, NH>* st = reinterpret_cast<LaneState<HD, NH>*>(smem + warp * 2 * TILE_BYTES) + lane;
+    // lanes meet in shared memory (each warp reuses its buffers); warp 0 merges 0..3
+    LaneState<HD, NH>* st = reinterpret_cast<LaneState<HD, NH>*>(smem + warp * kRegion) + lane;
 #pragma unroll
     for (int h = 0; h < NH; ++h) {
       st->m[h] = m[h];
@@ -635,21 +678,21 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
         const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
         for (int w = 0; w < n_lanes; ++w) {
           const LaneState<HD, NH>* q =
-              reinterpret_cast<const LaneState<HD, NH>*>(smem + (warp + w) * 2 * TILE_BYTES) + lane;
+              reinterpret_cast<const LaneState<HD, NH>*>(smem + (warp + w) * kRegion) + lane;
           lane_merge<HD, NH>(P, q->m, q->l, q->acc);
         }
-        if (warp == 4) *(reinterpret_cast<LaneState<HD, NH>*>(smem + 4 * 2 * TILE_BYTES) + lane) = P;
+        if (warp == 4) *(reinterpret_cast<LaneState<HD, NH>*>(smem + 4 * kRegion) + lane) = P;
       }
       __syncthreads();
       if (warp == 0)
-        fused_split_merge<HD, NH>(a, P, reinterpret_cast<const LaneState<HD, NH>*>(smem + 4 * 2 * TILE_BYTES) + lane,
+        fused_split_merge<HD, NH>(a, P, reinterpret_cast<const LaneState<HD, NH>*>(smem + 4 * kRegion) + lane,
                                   row_valid, row_pos, row_tok, row_head, tq);
       return;
     }
     if (warp != 0) return;
     const int n_lanes = (kv_end - kv_begin + lane_len - 1) / lane_len;
     for (int w = 0; w < n_lanes; ++w) {
-      const LaneState<HD, NH>* q = reinterpret_cast<const LaneState<HD, NH>*>(smem + w * 2 * TILE_BYTES) + lane;
+      const LaneState<HD, NH>* q = reinterpret_cast<const LaneState<HD, NH>*>(smem + w * kRegion) + lane;
       lane_merge<HD, NH>(P, q->m, q->l, q->acc);
     }
   } else {
@@ -1789,7 +1832,7 @@ constexpr int attn_smem_bytes() {
   // decode: one K+V tile per warp (+ one staging area per warp for KV8), four
   // warps or (FUSED) eight; prefill: a two-stage ring plus the running lane
   // state (KV8: one K+V tile, the running states and two staging areas)
-  return DECODE ? (FUSED ? 8 : 4) * (2 * kKeys * HD * 2 + (KV8 ? Kv8Stage<HD>::kBytes : 0))
+  return DECODE ? (FUSED ? 8 : 4) * (kDecWarpTiles<KV8> * kKeys * HD * 2 + (KV8 ? Kv8Stage<HD>::kBytes : 0))
                 : (KV8 ? 1 : 2) * 2 * kKeys * HD * 2 + 128 * (int)sizeof(LaneState<HD>) +
                       (KV8 ? 2 * Kv8Stage<HD>::kBytes : 0);
 }
