@@ -297,25 +297,32 @@ __global__ void __launch_bounds__(kF8Threads, 1) gemm_fp8_kernel(const __grid_co
 }
 
 // ------------------------------------------------------------------ decode-size calls
-// Calls of at most 16 rows (a decode step) on the same tensor-core MMA with the
+// Calls of at most 16 rows (decode steps) on the same tensor-core MMA with the
 // operands' roles exchanged: a tile of BM (64 or 128) weight rows is the MMA's
-// M side and the call's rows, zero-filled by the TMA copy up to 16, are its N
-// side, so one CTA per BM output columns streams its weight rows once (N / BM
-// CTAs where the 128-row tile above gives N / 256).  An element's partial per K
+// M side and the call's rows, zero-filled by the TMA copy up to R = 16, are its
+// N side, so one CTA per BM output columns streams its weight rows once (N / BM
+// CTAs where the 128-row tile above gives N / 256).  (R = 32 and 64 were
+// measured at 64-row calls of the long-context decoder: slower there than the
+// 128 x 256 tiles, whose 44 and 8 CTAs stream the weights at least as fast.)  An element's partial per K
 // block is the same sum of the same products in the same K order as in the
 // large kernel (which operand is which does not enter a product), and the
 // promotion is the same fp32 fma in ascending kb, so the rows are the same bits
 // (the row-invariance test compares them across M).  Weights are copied before
 // the dependency wait and the call's codes after it; a ring of up to
 // f8dec_max_stages K blocks holds the whole K of the usual decode shapes, so
-// every copy is in flight at once.
-constexpr int kF8DecRows = 16;   // the MMA's N: rows of the call, zero past M
-constexpr int kF8DecBufs = 4;    // TMEM partial buffers (16 columns each)
+// every copy is in flight at once.  The scale products sa[m, kb] sw[n/128, kb]
+// of the CTA's weight block are formed once, before the K loop, into shared
+// memory (the same fp32 product the large kernel forms per block).
+constexpr int kF8DecMaxRows = 16;   // the MMA's N: rows of the call, zero past M
+constexpr int kF8DecBufs = 4;       // TMEM partial buffers (R columns each)
 constexpr int kF8DecThreads = 192;  // TMA, MMA, four promotion warps (one per lane quarter)
-__host__ __device__ constexpr int f8dec_max_stages(int bm) { return bm == 64 ? 16 : 8; }
-__host__ __device__ constexpr int f8dec_stage_bytes(int bm) { return bm * kF8Block + kF8DecRows * kF8Block; }
-__host__ constexpr size_t f8dec_smem(int bm, int stages) {
-  return 1024 + (size_t)stages * f8dec_stage_bytes(bm) + 512;
+constexpr size_t kF8DecMaxSmem = 220 * 1024;
+__host__ __device__ constexpr int f8dec_stage_bytes(int bm, int r) { return (bm + r) * kF8Block; }
+__host__ __device__ constexpr int f8dec_max_stages(int bm, int r) {
+  return 196608 / f8dec_stage_bytes(bm, r) < 16 ? 196608 / f8dec_stage_bytes(bm, r) : 16;
+}
+__host__ constexpr size_t f8dec_smem(int bm, int r, int stages, int nkb) {
+  return 1024 + (size_t)stages * f8dec_stage_bytes(bm, r) + (size_t)r * nkb * 4 + 512;
 }
 
 struct F8DecArgs {
@@ -326,7 +333,7 @@ struct F8DecArgs {
   int M, N, nkb, stages, c_fp32;
 };
 
-template <int BM>
+template <int BM, int R>
 __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __grid_constant__ CUtensorMap tmW,
                                                                  const __grid_constant__ CUtensorMap tmX,
                                                                  const F8DecArgs args) {
@@ -335,14 +342,15 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
   const int S = args.stages, nk = args.nkb;
   uint8_t* sW = smem;                              // [S][BM rows x 128 codes], 128-byte swizzle
   uint8_t* sX = smem + S * BM * kF8Block;          // [S][16 rows x 128 codes]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sX + S * kF8DecRows * kF8Block);
+  float* sc_s = reinterpret_cast<float*>(sX + S * R * kF8Block);  // [nk][R] scale products
+  uint64_t* full = reinterpret_cast<uint64_t*>(sc_s + nk * R);
   uint64_t* empty = full + S;
   uint64_t* pfull = empty + S;                     // [kF8DecBufs] MMA -> promotion
   uint64_t* pempty = pfull + kF8DecBufs;           // [kF8DecBufs] promotion -> MMA (4 warp arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pempty + kF8DecBufs);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  constexpr uint32_t kTmemCols = kF8DecBufs * kF8DecRows;
-  constexpr uint32_t kStageW = BM * kF8Block, kStageX = kF8DecRows * kF8Block;
+  constexpr uint32_t kTmemCols = kF8DecBufs * R;
+  constexpr uint32_t kStageW = BM * kF8Block, kStageX = R * kF8Block;
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer: one TMEM partial (BM x 16) per K block
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, kF8DecRows);
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, R);
       for (int kb = 0; kb < nk; ++kb) {
         const int j = kb % kF8DecBufs, s = kb % S;
         if (!mbar_wait(&pempty[j], ((kb / kF8DecBufs) & 1) ^ 1) || !mbar_wait(&full[s], (kb / S) & 1) ||
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
         const uint32_t w_addr = smem_u32(sW + s * kStageW), x_addr = smem_u32(sX + s * kStageX);
 #pragma unroll
         for (int k = 0; k < kF8Block / 32; ++k)
-          tc_mma_f8(tmem_base + j * kF8DecRows, sw128_kmajor_desc(w_addr + k * 32), sw128_kmajor_desc(x_addr + k * 32),
+          tc_mma_f8(tmem_base + j * R, sw128_kmajor_desc(w_addr + k * 32), sw128_kmajor_desc(x_addr + k * 32),
                     idesc, k != 0 ? 1u : 0u);
         tc_commit(&empty[s]);
         tc_commit(&pfull[j]);
@@ -423,23 +431,25 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
     }
   } else {
     // ---------------- promotion and store: warps 2..5, lane quarter q = warp % 4;
-    // thread (q, lane) owns output column n0 + c (c = its tile row) for the 16 rows
+    // thread (q, lane) owns output column n0 + c (c = its tile row) for the R rows
     const int q = warp & 3;
     const int c = BM == 128 ? 32 * q + lane : 16 * q + lane;
     const bool col_ok = (BM == 128 || lane < 16) && n0 + c < args.N;
     const int wblk = n0 / kF8Block;  // BM divides 128: the tile lies in one weight block
     const uint32_t tq = tmem_base + ((uint32_t)(32 * q) << 16);
-    float acc[kF8DecRows];
+    float acc[R];
 #pragma unroll
-    for (int m = 0; m < kF8DecRows; ++m) acc[m] = 0.f;
+    for (int m = 0; m < R; ++m) acc[m] = 0.f;
     pdl_wait();  // the row scales come from the preceding kernel
+    // the scale products of every (kb, row): sa * sw, one rounding (0 past M)
+    for (int i = threadIdx.x - 64; i < nk * R; i += 128) {
+      const int kb = i / R, m = i % R;
+      sc_s[i] = m < args.M ? __fmul_rn(args.sa[(int64_t)m * nk + kb], args.sw[(int64_t)wblk * nk + kb]) : 0.f;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four promotion warps
     bool ok = true;
     for (int kb = 0; kb < nk; ++kb) {
       const int j = kb % kF8DecBufs;
-      const float swk = args.sw[(int64_t)wblk * nk + kb];
-      float sc[kF8DecRows];
-#pragma unroll
-      for (int m = 0; m < kF8DecRows; ++m) sc[m] = m < args.M ? __fmul_rn(args.sa[(int64_t)m * nk + kb], swk) : 0.f;
       // decided for the whole warp: the TMEM load below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(&pfull[j], (kb / kF8DecBufs) & 1) && !*abort_flag)) {
         report(args.status, DEV_TIMEOUT);
@@ -448,12 +458,23 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
         break;
       }
       tc_fence_after();
-      uint32_t p[16];
-      tmem_ld_32x32b_x16(tq + j * kF8DecRows, p);
-      tmem_ld_wait();
-      // acc += partial * (scale_a * scale_w), one rounding per element
+      // acc += partial * (scale_a * scale_w), one rounding per element; 16 rows per
+      // TMEM load
 #pragma unroll
-      for (int m = 0; m < kF8DecRows; ++m) acc[m] = __fmaf_rn(__uint_as_float(p[m]), sc[m], acc[m]);
+      for (int c16 = 0; c16 < R; c16 += 16) {
+        uint32_t p[16];
+        tmem_ld_32x32b_x16(tq + j * R + c16, p);
+        tmem_ld_wait();
+        const float4* sc4 = reinterpret_cast<const float4*>(sc_s + kb * R + c16);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 sc = sc4[i / 4];
+          acc[c16 + i] = __fmaf_rn(__uint_as_float(p[i]), sc.x, acc[c16 + i]);
+          acc[c16 + i + 1] = __fmaf_rn(__uint_as_float(p[i + 1]), sc.y, acc[c16 + i + 1]);
+          acc[c16 + i + 2] = __fmaf_rn(__uint_as_float(p[i + 2]), sc.z, acc[c16 + i + 2]);
+          acc[c16 + i + 3] = __fmaf_rn(__uint_as_float(p[i + 3]), sc.w, acc[c16 + i + 3]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pempty[j]);
@@ -461,7 +482,7 @@ __global__ void __launch_bounds__(kF8DecThreads, 1) gemm_fp8_dec_kernel(const __
     if (ok && col_ok && !*abort_flag) {
       const int col = n0 + c;
 #pragma unroll
-      for (int m = 0; m < kF8DecRows; ++m) {
+      for (int m = 0; m < R; ++m) {
         if (m >= args.M) break;
         if (args.c_fp32)
           static_cast<float*>(args.C)[(int64_t)m * args.N + col] = acc[m];
@@ -517,35 +538,37 @@ bi_status bi_gemm_fp8(const void* Aq, const float* sa, int64_t M, int64_t K, con
   BI_REQUIRE(K > 0 && Aq && sa && Wq && sw && C, "null pointer");
   BI_REQUIRE(aligned16(Aq) && aligned16(Wq) && aligned16(C), "pointers must be 16-byte aligned");
   BI_REQUIRE(M <= 0x7fffffff && N <= 0x7fffffff, "shape too large");
-  if (M <= kF8DecRows) {
-    // decode size: weight tiles as the MMA's M side (the same bits); 128-row
-    // tiles once 64-row ones would fill the GPU twice over
-    const int bm = N / 64 >= 2 * (int64_t)num_sms() ? 128 : 64;
-    const int nkb = (int)(K / kF8Block);
-    const int stages = std::min(nkb, f8dec_max_stages(bm));
+  const int nkb = (int)(K / kF8Block);
+  // decode sizes: weight tiles as the MMA's M side (the same bits); 128-row tiles
+  // once 64-row ones would fill the GPU twice
+  const int bm = N / 64 >= 2 * (int64_t)num_sms() ? 128 : 64;
+  constexpr int rr = kF8DecMaxRows;
+  const int dec_stages = std::min(nkb, f8dec_max_stages(bm, rr));
+  if (M <= kF8DecMaxRows && f8dec_smem(bm, rr, dec_stages, nkb) <= kF8DecMaxSmem) {
     static std::once_flag once_dec;
     static cudaError_t attr_dec = cudaSuccess;
     std::call_once(once_dec, [] {
-      attr_dec = cudaFuncSetAttribute(gemm_fp8_dec_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)f8dec_smem(64, f8dec_max_stages(64)));
-      if (attr_dec == cudaSuccess)
-        attr_dec = cudaFuncSetAttribute(gemm_fp8_dec_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)f8dec_smem(128, f8dec_max_stages(128)));
+      const int smax = (int)kF8DecMaxSmem;
+      cudaError_t e = cudaSuccess;
+      auto set = [&](auto fn) {
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smax);
+      };
+      set(gemm_fp8_dec_kernel<64, rr>);
+      set(gemm_fp8_dec_kernel<128, rr>);
+      attr_dec = e;
     });
     if (attr_dec != cudaSuccess)
       return fail(BI_ERR_CUDA, std::string("bi_gemm_fp8 decode smem attribute: ") + cudaGetErrorString(attr_dec));
     CUtensorMap tw, tx;
-    if (!encode_tmap_2d_u8(&tw, Wq, K, N, K, kF8Block, bm) ||
-        !encode_tmap_2d_u8(&tx, Aq, K, M, K, kF8Block, kF8DecRows))
+    if (!encode_tmap_2d_u8(&tw, Wq, K, N, K, kF8Block, bm) || !encode_tmap_2d_u8(&tx, Aq, K, M, K, kF8Block, rr))
       return fail(BI_ERR_CUDA, "bi_gemm_fp8: TMA descriptor failed");
-    F8DecArgs da{sa, sw, C, device_status_ptr(), (int)M, (int)N, nkb, stages, c_dtype == BI_DTYPE_FP32};
-    const dim3 grid((unsigned)(N / bm));
-    const size_t smem = f8dec_smem(bm, stages);
-    return launched(bm == 64 ? launch_pdl(gemm_fp8_dec_kernel<64>, grid, dim3(kF8DecThreads), smem, as_stream(stream),
-                                          tw, tx, da)
-                             : launch_pdl(gemm_fp8_dec_kernel<128>, grid, dim3(kF8DecThreads), smem,
-                                          as_stream(stream), tw, tx, da),
-                    "bi_gemm_fp8");
+    F8DecArgs da{sa, sw, C, device_status_ptr(), (int)M, (int)N, nkb, dec_stages, c_dtype == BI_DTYPE_FP32};
+    const dim3 grid((unsigned)(N / bm)), block(kF8DecThreads);
+    const size_t smem = f8dec_smem(bm, rr, dec_stages, nkb);
+    cudaStream_t st = as_stream(stream);
+    const cudaError_t le = bm == 64 ? launch_pdl(gemm_fp8_dec_kernel<64, rr>, grid, block, smem, st, tw, tx, da)
+                                    : launch_pdl(gemm_fp8_dec_kernel<128, rr>, grid, block, smem, st, tw, tx, da);
+    return launched(le, "bi_gemm_fp8");
   }
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

@@ -72,7 +72,7 @@ def test_gemm_fp8_rows_invariant_to_M_and_order(N, K):
     qa, sa, qw, sw = _fp8_operands(rng, 300, N, K)
     full = torch.empty((300, N), dtype=torch.float32, device="cuda")
     bi.bi_gemm_fp8(qa, sa, 300, K, qw, sw, N, full, bi.BI_DTYPE_FP32)
-    for M in (1, 7, 16, 127, 128, 129, 255):
+    for M in (1, 7, 16, 17, 33, 64, 65, 127, 128, 129, 255):
         off = 300 - M
         part = torch.empty((M, N), dtype=torch.float32, device="cuda")
         bi.bi_gemm_fp8(qa[off:].contiguous(), sa[off:].contiguous(), M, K, qw, sw, N, part, bi.BI_DTYPE_FP32)
