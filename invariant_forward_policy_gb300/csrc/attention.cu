@@ -432,8 +432,9 @@ __device__ __forceinline__ void fused_split_merge(const AttnArgs& a, const LaneS
 // split's tiles in order from a shared two-stage cp.async ring, folding each
 // finished lane into a running state at every lane boundary.
 // DECODE (query tiles of at most 16 rows, short contexts): warp w computes
-// lane w of the split from its own one-tile buffer, then warp 0 merges the
-// lanes in order.
+// lane w of the split from its own buffers (bf16 caches: a three-tile cp.async
+// ring of the lane's K and V tiles, two ahead of the one in use), then warp 0
+// merges the lanes in order.  Tiles of at most 8 rows keep one row half.
 // FUSED (DECODE with at most two splits): one CTA per (piece, query tile, kv
 // head) covers both splits with eight warps, warp w computing lane w % 4 of
 // split w / 4; warps 0 and 4 fold their split's lanes in order, and warp 0
