@@ -217,13 +217,14 @@ def test_fused_lm_head_logprob_parity_and_row_invariance(T, K, V):
     assert np.max(np.abs(lf.cpu().numpy() - lp.cpu().numpy())) < 1e-4
 
 
-@pytest.mark.parametrize("K,V", [(256, 4096), (512, 32000)])
+@pytest.mark.parametrize("K,V", [(256, 4096), (512, 32000), (256, 1000)])
 def test_fused_lm_head_decode_rows_equal_large_calls_on_ties_and_rising_maxima(K, V):
     """Decode-size calls of the fused head (1, 7 and 16 rows) give the bits of a
     40-row call for every row: logits tied exactly (duplicated
     weight rows, within and across vocab tiles) and maxima that rise step after
     step inside a tile (weight rows scaled up column by column), targets on the
-    tied and rising columns, and greedy decoding."""
+    tied and rising columns, and greedy decoding.  V = 1000 ends inside a vocab
+    tile (the groups past the last column are skipped)."""
     rng = np.random.default_rng(K + V)
     T = 40
     xb, _ = rng_bf16(rng, (T, K))
