@@ -1269,17 +1269,24 @@ __global__ void __launch_bounds__(TcAttnLayout<HD>::kThreads, 1)
 constexpr int kDecMaxPieces = 1024;      // larger decode calls take the per-CTA schedule (same bits)
 constexpr int kDecPersistentSplits = 4;  // shorter contexts take the per-CTA schedule (same bits)
 
-// KV8 (FP8 cache): warps 4..7 replace the producer, warp 4 + w serving
-// consumer w alone.  It walks the items as consumer w does and copies each
-// page's e4m3 codes (64 rows x hd bytes, unswizzled) and 64 fp32 scales with
-// TMA into its two-slot code ring, two pages ahead; it then expands a landed
-// page into the consumer's two-slot bf16 ring (the swizzled layout ldmatrix
-// reads), rows and scales after the item's last position zero.  The consumer
-// runs the bf16 schedule on that page with the scales applied.  Each ring
-// involves one loader warp and one consumer warp only.
+// KV8 (FP8 cache): eight loader warps replace the producer, two per consumer
+// ring: warp 4 + w loads consumer w's K pages, warp 8 + w its V pages.  A
+// loader walks the items as consumer w does and copies each of its pages' e4m3
+// codes (64 rows x hd bytes, unswizzled) and 64 fp32 scales with TMA into its
+// code slot, one page ahead; it expands the landed page a quarter at a time
+// into its slot of the consumer's bf16 ring (the swizzled layout ldmatrix
+// reads), rows and scales after the item's last position zero, and copies the
+// next page into the code slot as soon as the last quarter and the scales are
+// read.  The consumer runs the bf16 schedule on that page with the scales
+// applied.  The consumers' warpgroup takes kConsumerRegs registers a thread and
+// the two loader warpgroups kLoaderRegs (setmaxnreg), within the 168 a thread
+// that 384 threads launch with (the host checks the compiled count).
 template <int HD, bool KV8 = false, int NH = 2>
 struct DecLayout {
-  static constexpr int kThreads = KV8 ? 256 : 160;  // consumers, then producer (KV8: four loaders)
+  static constexpr int kThreads = KV8 ? 384 : 160;  // consumers, then producer (KV8: eight loaders)
+  static constexpr int kLaunchRegs = 168;           // KV8: 65536 / 384, rounded down to a multiple of 8
+  static constexpr int kConsumerRegs = 240, kLoaderRegs = 128;
+  static_assert(!KV8 || 128 * kConsumerRegs + 256 * kLoaderRegs <= kThreads * kLaunchRegs, "register split");
   // bf16 ring depth per consumer warp: three slots at hd 128 (one CTA per SM);
   // two at hd 64 (two CTAs share an SM) and on an FP8 cache (two code slots
   // more per ring)
@@ -1356,22 +1363,24 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// KV8 loader step: the codes of one page (64 rows x hd bytes) as this lane's
-// uint4 chunks lane + 32 u, and their expansion into the swizzled bf16 page of
-// unscaled values, rows at or after nk zero.  One warp.
+// KV8 loader step: a quarter of the codes of one page (64 rows x hd bytes), as
+// this lane's uint4 chunks lane + 32 u of the quarter, and their expansion into
+// the swizzled bf16 page of unscaled values, rows at or after nk zero.  One warp.
 template <int HD>
 struct DecCodes {
-  static constexpr int C16 = HD / 16;            // 16-code chunks per key row
-  static constexpr int kPer = kKeys * C16 / 32;  // chunks per lane
-  uint4 raw[kPer];
-  __device__ __forceinline__ void load(const uint8_t* codes, int lane) {
+  static constexpr int C16 = HD / 16;              // 16-code chunks per key row
+  static constexpr int kParts = 4;
+  static constexpr int kPart = kKeys * C16 / (32 * kParts);  // chunks per lane and part
+  uint4 raw[kPart];
+  __device__ __forceinline__ void load(const uint8_t* codes, int lane, int part) {
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) raw[u] = *reinterpret_cast<const uint4*>(codes + (lane + 32 * u) * 16);
+    for (int u = 0; u < kPart; ++u)
+      raw[u] = *reinterpret_cast<const uint4*>(codes + (lane + 32 * (part * kPart + u)) * 16);
   }
-  __device__ __forceinline__ void expand(uint8_t* page, int nk, int lane) const {
+  __device__ __forceinline__ void expand(uint8_t* page, int nk, int lane, int part) const {
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = lane + 32 * u, key = i / C16, c16 = i % C16;
+    for (int u = 0; u < kPart; ++u) {
+      const int i = lane + 32 * (part * kPart + u), key = i / C16, c16 = i % C16;
       uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
       if (key < nk) {
         const uint2 b0 = e4m3x4_to_bf16x4(raw[u].x), b1 = e4m3x4_to_bf16x4(raw[u].y);
@@ -1449,6 +1458,12 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 &&
   const int n_items = first[P];
   const int lane_len = ((a.split + 3) / 4 + kKeys - 1) / kKeys * kKeys;
   const int tpl = lane_len / kKeys;  // tiles per lane
+  if constexpr (KV8) {
+    // warpgroup 0 consumes, warpgroups 1 and 2 load: the loaders give up their
+    // registers first thing, before any of their warps can return
+    if (warp < 4) reg_alloc_inc<Lay::kConsumerRegs>();
+    else reg_alloc_dec<Lay::kLoaderRegs>();
+  }
 
   if (!KV8 && warp == 4) {
     // ------------------------------------------------------------ producer
@@ -1514,11 +1529,14 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 &&
   }
 
   if (KV8 && warp >= 4) {
-    // ------------------------------------------------- loader of ring w (KV8)
+    // ------------------------------------ loader of ring w, K or V pages (KV8)
     // objects in consumer w's order: items of this CTA, the ring's pages of each
-    // (keys lb .. le), K then V
-    const int w = warp - 4;
-    int item = blockIdx.x, lb = 0, le = 0, key0 = 0, kv = 0, kv_end = 0, seq = 0, kvh = 0, blk_all = -1;
+    // (keys lb .. le); this warp takes the K (kv 0) or the V (kv 1) page of each.
+    // With two bf16 slots per ring, consumer w's K pages always take slot 0 and
+    // its V pages slot 1, so a loader owns one code slot and one bf16 slot.
+    const int w = (warp - 4) & 3, kv = (warp - 4) >> 2;
+    const int cs = w * kDecSlots + kv;
+    int item = blockIdx.x, lb = 0, le = 0, key0 = 0, kv_end = 0, seq = 0, kvh = 0, blk_all = -1;
     bool more = false;
     auto enter = [&]() {  // the first item from `item` on with pages for this ring
       for (; item < n_items; item += gridDim.x) {
@@ -1527,7 +1545,6 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 &&
         le = min(lb + lane_len, it.kv_end);
         if (lb < le) {
           key0 = lb;
-          kv = 0;
           kv_end = it.kv_end;
           seq = it.seq;
           kvh = it.kvh;
@@ -1541,22 +1558,18 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 &&
       more = false;
     };
     auto advance = [&]() {
-      if (kv == 0) {
-        kv = 1;
-        return;
-      }
-      kv = 0;
       key0 += kKeys;
       if (key0 >= le) {
         item += gridDim.x;
         enter();
       }
     };
-    int nk0 = 0, nk1 = 0;  // keys at or before the item's last position, per code slot
-    auto issue = [&](int n) {  // the cursor's object into code slot n % 2 (whole warp)
-      const int cs = n & 1;
-      if (cs) nk1 = kv_end - key0;
-      else nk0 = kv_end - key0;
+    // the cursor's page, looked up before the slot is free (block-table entry, in
+    // lane 0, and its keys at or before the item's last position); the code slot's
+    // page is issued from these, so the lookups run while no codes are held
+    int blk_next = -1, page_next = 0, nk_next = 0, nk_slot = 0;
+    auto prepare = [&]() {  // whole warp
+      nk_next = kv_end - key0;
       const int t = (key0 - lb) / kKeys;
       int blk = __shfl_sync(0xffffffffu, blk_all, t & 31);
       if (lane == 0) {
@@ -1568,47 +1581,70 @@ __global__ void __launch_bounds__(DecLayout<HD, KV8, NH>::kThreads, (HD == 64 &&
           report(a.status, DEV_BAD_INDEX);
           blk = -1;
         }
-        uint64_t* bar = &full[w * kDecSlots + cs];
-        uint8_t* dst = codes + (w * kDecSlots + cs) * Lay::kCodeSlot;
-        if (blk >= 0) {
-          mbar_arrive_expect_tx(bar, Lay::kCodeSlot);
-          const int page = blk * a.Hkv + kvh;
-          tma_load_2d(dst, kv ? &tmv : &tmk, bar, 0, page * kKeys);
-          tma_load_2d(dst + Lay::kCodes, kv ? &tmvs : &tmks, bar, 0, page);
+        blk_next = blk;
+        page_next = blk * a.Hkv + kvh;
+      }
+    };
+    auto issue = [&]() {  // the prepared page into the code slot
+      nk_slot = nk_next;
+      if (lane == 0) {
+        uint8_t* dst = codes + cs * Lay::kCodeSlot;
+        if (blk_next >= 0) {
+          mbar_arrive_expect_tx(&full[cs], Lay::kCodeSlot);
+          tma_load_2d(dst, kv ? &tmv : &tmk, &full[cs], 0, page_next * kKeys);
+          tma_load_2d(dst + Lay::kCodes, kv ? &tmvs : &tmks, &full[cs], 0, page_next);
         } else {
-          mbar_arrive(bar);  // bad block (reported): the slot's old codes are expanded
+          mbar_arrive(&full[cs]);  // bad block (reported): the slot's old codes are expanded
         }
       }
     };
     int n_issued = 0, c = 0;
     enter();
-    for (; n_issued < 2 && more; advance()) issue(n_issued++);
+    if (more) {
+      prepare();
+      issue();
+      ++n_issued;
+      advance();
+      if (more) prepare();
+    }
     DecCodes<HD> cd;
+    uint8_t* bpage = smem + cs * Lay::kTile;
     for (; c < n_issued; ++c) {
-      const int cs = c & 1, nk = cs ? nk1 : nk0;
-      if (!__all_sync(0xffffffffu, dec_wait(&full[w * kDecSlots + cs], (c >> 1) & 1, abort_flag, a.status))) break;
-      const uint8_t* src = codes + (w * kDecSlots + cs) * Lay::kCodeSlot;
-      cd.load(src, lane);
+      const int nk = nk_slot;
+      if (!__all_sync(0xffffffffu, dec_wait(&full[cs], c & 1, abort_flag, a.status))) break;
+      const uint8_t* src = codes + cs * Lay::kCodeSlot;
+      cd.load(src, lane, 0);
+      // bf16 slot: consumer w has released this loader's previous page
+      if (!__all_sync(0xffffffffu, dec_wait(&empty[cs], (c & 1) ^ 1, abort_flag, a.status))) break;
+      // all but the last part expanded straight from the slot; the last part and
+      // the scales are read before the slot takes the next page
+#pragma unroll 1
+      for (int part = 0; part < DecCodes<HD>::kParts - 1; ++part) {
+        cd.expand(bpage, nk, lane, part);
+        cd.load(src, lane, part + 1);
+      }
       const float* ssrc = reinterpret_cast<const float*>(src + Lay::kCodes);
       const float s0 = lane < nk ? ssrc[lane] : 0.f, s1 = lane + 32 < nk ? ssrc[lane + 32] : 0.f;
       fence_proxy_async();  // the reads above before the slot's next TMA copy
       __syncwarp();
-      if (more) {
-        issue(n_issued++);
-        advance();
+      const bool issued = more;
+      if (issued) {
+        issue();
+        ++n_issued;
       }
-      // bf16 slot: consumer w has released the object kDecSlots before this one
-      const int bs = w * kDecSlots + c % kDecSlots;
-      if (!__all_sync(0xffffffffu, dec_wait(&empty[bs], ((c / kDecSlots) & 1) ^ 1, abort_flag, a.status))) break;
-      cd.expand(smem + bs * Lay::kTile, nk, lane);
-      scl[bs * kKeys + lane] = s0;
-      scl[bs * kKeys + lane + 32] = s1;
+      cd.expand(bpage, nk, lane, DecCodes<HD>::kParts - 1);
+      scl[cs * kKeys + lane] = s0;
+      scl[cs * kKeys + lane + 32] = s1;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&conv[bs]);
+      if (lane == 0) mbar_arrive(&conv[cs]);
+      if (issued) {
+        advance();
+        if (more) prepare();
+      }
     }
     // every copy this warp started lands before it can exit
     if (lane == 0)
-      for (int d = c; d < n_issued; ++d) mbar_wait(&full[w * kDecSlots + (d & 1)], (d >> 1) & 1);
+      for (int d = c; d < n_issued; ++d) mbar_wait(&full[cs], d & 1);
     return;
   }
 
@@ -1864,7 +1900,7 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
   constexpr int smem = DecLayout<HD, KV8, NH>::kBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  static int per_sm = 1;
+  static int per_sm = 1, launch_regs = 0;
   std::call_once(once, [] {
     attr_err =
         cudaFuncSetAttribute(attention_decode_kernel<HD, KV8, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1872,9 +1908,18 @@ static bi_status launch_attention_decode(const AttnArgs& args, int64_t P, cudaSt
       attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_decode_kernel<HD, KV8, NH>,
                                                                DecLayout<HD, KV8, NH>::kThreads, smem);
     if (per_sm < 1) per_sm = 1;
+    if (KV8 && attr_err == cudaSuccess) {
+      cudaFuncAttributes fa{};
+      attr_err = cudaFuncGetAttributes(&fa, attention_decode_kernel<HD, KV8, NH>);
+      launch_regs = fa.numRegs;
+    }
   });
   if (attr_err != cudaSuccess)
     return fail(BI_ERR_CUDA, std::string("attention decode attributes: ") + cudaGetErrorString(attr_err));
+  // the warpgroups' register split must fit what the block launches with, or the
+  // consumers' increase would never be granted
+  if (KV8 && launch_regs < DecLayout<HD, KV8, NH>::kLaunchRegs)
+    return fail(BI_ERR_CUDA, "attention decode (FP8): compiled with fewer registers than its warpgroup split needs");
   const uint64_t rows = (uint64_t)args.n_blocks * args.Hkv * kKeys;
   CUtensorMap tmk, tmv, tmks, tmvs;
   bool ok;

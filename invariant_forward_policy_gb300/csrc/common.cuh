@@ -188,6 +188,15 @@ BI_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::
 // (returns at once when the kernel was launched without the attribute).
 BI_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Move registers between warpgroups: every warp of a warpgroup executes the same
+// one.  An increase waits until decreases elsewhere in the block have freed
+// enough of the registers the block launched with, so the block's split must fit
+// that total and every decrease must run before any warp can stop.
+template <int N>
+BI_DEV void reg_alloc_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory"); }
+template <int N>
+BI_DEV void reg_alloc_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory"); }
+
 // Bounded waits give up after this many nanoseconds (global timer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
