@@ -755,23 +755,23 @@ __global__ void __launch_bounds__(FUSED ? 256 : 128) attention_kernel(const Attn
 // the group) pairs as above.  S = Q K^T (K = hd in 16-wide steps, ascending)
 // and O += P V (K = 64 keys in 16-wide steps, ascending) accumulate in TMEM;
 // tcgen05.mma and mma.sync give the same fp32 bits step for step, so each row
-// gets exactly the arithmetic of the mma.sync schedules.  Each row belongs to
-// four threads of the sixteen softmax warps (warps w, w + 4, w + 8, w + 12
-// read TMEM lane quarter w): thread q holds the keys 8j + 2q + {0, 1} of the
-// tile, i.e. exactly the keys of the mma.sync fragment's quad sum s_q.  They
-// repeat attn_update's operations in its order: scale and select-mask, the
-// tile max (exchanged), alpha, P = exp2(v - m), s_q summed over its keys in
-// order and the row sum formed as (s0 + s1) + (s2 + s3), l = l alpha + sum,
-// O = O alpha (skipped when alpha is exactly 1, where it is the identity), P
-// rounded to bf16; and at every lane boundary the finished lane folds into the
-// running state with lane_merge's formula.  Each of the four threads keeps
-// the row's (m, l) and rescales, folds and writes its quarter of the O columns.
+// gets exactly the arithmetic of the mma.sync schedules.  The eight softmax
+// warps read S and O through the 16x256b TMEM shape, which gives a warp 16 rows
+// in the mma.sync accumulator layout: the four threads of a quad are one row and
+// thread q holds the keys 8j + 2q + {0, 1} of the tile, i.e. exactly the keys of
+// the mma.sync fragment's quad sum s_q.  They repeat attn_update's operations in
+// its order: scale and select-mask, the tile max (quad shuffles), alpha,
+// P = exp2(v - m), s_q summed over its keys in order and the row sum formed as
+// (s0 + s1) + (s2 + s3), l = l alpha + sum, O = O alpha (skipped when alpha is
+// exactly 1, where it is the identity), P rounded to bf16; and at every lane
+// boundary the finished lane folds into the running state (held in registers)
+// with lane_merge's formula.
 // A CTA walks up to kTcSplitsPerCta consecutive splits of its query tile, one
 // after another (each split's partial is written when the next one starts), so
 // the Q tile, TMEM and the page pipeline serve many tiles.
-// Warp 16 lane 0 streams the K and V pages by TMA (the persistent decode
-// kernel's tensor maps) into a ring; warp 17 owns TMEM and lane 0 issues the
-// MMAs, S of the next tile ahead of P V of this one.  V rows after
+// The warp after the softmax warps streams the K and V pages by TMA (lane 0; the
+// persistent decode kernel's tensor maps) into a ring; the next one owns TMEM and
+// its lane 0 issues the MMAs, S of the next tile ahead of P V of this one.  V rows after
 // the CTA's last query position are zeroed in shared memory before P V (TMA
 // copies whole pages, and slots not yet written may hold anything); K rows
 // there only feed scores that the select-mask replaces.
