@@ -6,8 +6,9 @@ numerical contract may change: the accumulation order (here fp64) and the bf16
 rounding of the attention probabilities before P.V (see tests/noise_floor.py).
 Every bound must lie between the largest floor measured for its model and
 2.5 times it: large enough that a correct kernel passes, small enough that the
-bound still means something.  (the benchmark spec's 5e-3 sits below the maximum of this
-floor on every multi-layer model; it is met as a mean on the dense decoder.)
+bound still means something.  (The 5e-3 target for GPU logprobs against the
+oracle sits below the maximum of this floor on every multi-layer model; it is
+met as a mean on the dense decoder.)
 """
 import numpy as np
 import pytest
