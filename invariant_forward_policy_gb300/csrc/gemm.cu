@@ -340,6 +340,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       const int n = n0 + c;
+      if (n >= args.n_out) break;  // a last tile past the final head
       const int h = n / hd, j0 = n % hd;
       if (h < ra.Hq + ra.Hkv) {
         if (j0 >= half) continue;  // done together with its partner chunk
@@ -1109,6 +1110,30 @@ static int decode_tile_n(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, in
   return best;
 }
 
+// Tile width of a call of more than 128 rows on a weight whose own width is
+// narrow (below 128: a small weight spread over the GPU at decode size).  Bits do
+// not depend on the width, so a prefill pass takes the width that minimises the
+// bytes its busiest CTA reads over all its tiles (tiles x (128 A rows + the W
+// slice)) instead of re-reading its A rows once per 16 or 32 columns.  min_bn:
+// SwiGLU pairs need 32, RoPE whole heads (and a width that divides N).
+static int wide_tile_n(int64_t M, int64_t n_rows_w, bool swiglu, int min_bn, bool divides, int bn_weight) {
+  const int64_t n_out = swiglu ? n_rows_w / 2 : n_rows_w;
+  const int64_t m_tiles = cdiv(M, kBM);
+  int best = bn_weight;
+  double best_bytes = 0.0;
+  for (int bn : {256, 128, 64, 32, 16}) {
+    if (bn < min_bn || (divides && (n_out % bn || bn % min_bn))) continue;
+    const int64_t tiles = m_tiles * cdiv(n_out, swiglu ? bn / 2 : bn);
+    const int64_t per_cta = cdiv(tiles, (int64_t)num_sms());
+    const double bytes = (double)per_cta * (double)(kBM + bn);
+    if (best_bytes == 0.0 || bytes < best_bytes) {
+      best = bn;
+      best_bytes = bytes;
+    }
+  }
+  return best;
+}
+
 // Non-invariant choices (BI_FAST): tile width and split count chosen from M.
 static void fast_plan(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, int* bn, int* splits) {
   *bn = tile_n_for(n_rows_w, K, swiglu);
@@ -1255,6 +1280,8 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   }
   if (!g.lse && !g.rope && g.E == 1 && !g.tile_expert && g.M <= kBM && splits == 1)
     bn = decode_tile_n(g.M, g.n_rows_w, g.K, swiglu, bn);
+  if (!g.lse && g.E == 1 && !g.tile_expert && g.M > kBM && splits == 1 && bn < 128)
+    bn = wide_tile_n(g.M, g.n_rows_w, swiglu, g.rope ? g.rope->hd : (swiglu ? 32 : 16), g.rope != nullptr, bn);
   if (g.lse && bn < 64) bn = 64;  // the fused log-softmax records are per 64+ vocab columns
   if (g.rope) {
     // a tile must hold whole heads so that rotate-half pairs meet in one thread
