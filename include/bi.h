@@ -147,7 +147,8 @@ bi_status bi_rope_kv_write(const void* qkv, int64_t T, const int32_t* piece_seq,
  * bf16 as bi_gemm would, then q and k rotated and everything written exactly as
  * bi_rope_kv_write does for row t at (row_seq[t], row_pos[t]) (device int32
  * [T]).  Same bits as the two calls, without the bf16 qkv round trip.  The
- * GEMM tile width is a multiple of hd (a tile holds whole heads).  The caller
+ * GEMM tile width is a multiple of hd (a tile holds whole heads).  x, wqkv,
+ * rope_table, q_out and the caches must be 16-byte aligned.  The caller
  * guarantees 0 <= row_seq[t] < rows of block_table; a position outside
  * [0, max_pos) or a block id outside [0, n_blocks) skips that row's writes and
  * sets the device status (bi_device_status). */

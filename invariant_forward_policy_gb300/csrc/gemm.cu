@@ -353,17 +353,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& args, uint32_t t_r
         if (h < ra.Hq) dst = ra.q_out + ((int64_t)row * ra.Hq + h) * hd;
         else if (blk >= 0) dst = ra.k_cache + (((int64_t)blk * ra.Hkv + (h - ra.Hq)) * 64 + slot) * hd;
         else continue;
-        const float* cs = ra.table + pos * hd;
+        // the row's cos and sin runs as 16-byte loads (a thread is a row: one line per lane)
+        const float4* c4 = reinterpret_cast<const float4*>(ra.table + pos * hd + j0);
+        const float4* s4 = reinterpret_cast<const float4*>(ra.table + pos * hd + half + j0);
         uint32_t o1[16], o2[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float a1[2], a2[2];
+        for (int i = 0; i < 32; i += 4) {
+          const float4 cv = c4[i / 4], sv = s4[i / 4];
+          const float cc[4] = {cv.x, cv.y, cv.z, cv.w}, ss[4] = {sv.x, sv.y, sv.z, sv.w};
+          float a1[4], a2[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            rope_pair(__uint_as_float(x1[i + e]), __uint_as_float(x2[i + e]), cs[j0 + i + e], cs[half + j0 + i + e],
-                      a1[e], a2[e]);
+          for (int e = 0; e < 4; ++e)
+            rope_pair(__uint_as_float(x1[i + e]), __uint_as_float(x2[i + e]), cc[e], ss[e], a1[e], a2[e]);
           o1[i / 2] = pack_bf16x2(a1[0], a1[1]);
+          o1[i / 2 + 1] = pack_bf16x2(a1[2], a1[3]);
           o2[i / 2] = pack_bf16x2(a2[0], a2[1]);
+          o2[i / 2 + 1] = pack_bf16x2(a2[2], a2[3]);
         }
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
@@ -1483,7 +1488,8 @@ bi_status gemm_qkv_rope(const void* A, int64_t M, int64_t K, const void* W, int6
   BI_REQUIRE(N == (int64_t)(Hq + 2 * Hkv) * hd, "N must be (Hq + 2 Hkv) * head_dim");
   BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
   BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
-  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache),
+  BI_REQUIRE(aligned16(A) && aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache) &&
+                 aligned16(rope_table),
              "pointers must be 16-byte aligned");
   RopeKvArgs ra{row_seq, row_pos, rope_table, block_table, static_cast<__nv_bfloat16*>(q_out),
                 static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), max_pos, max_blk,
@@ -1529,7 +1535,8 @@ bi_status gemm_qkv_rope_norm(const NormIn& norm, int64_t M, int64_t K, const voi
   BI_REQUIRE(N == (int64_t)(Hq + 2 * Hkv) * hd, "N must be (Hq + 2 Hkv) * head_dim");
   BI_REQUIRE_SHAPE(hd == 64 || hd == 128, "head_dim must be 64 or 128");
   BI_REQUIRE_SHAPE(K % 64 == 0, "K must be a multiple of 64");
-  BI_REQUIRE(aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache),
+  BI_REQUIRE(aligned16(W) && aligned16(q_out) && aligned16(k_cache) && aligned16(v_cache) &&
+                 aligned16(rope_table),
              "pointers must be 16-byte aligned");
   BI_TRY(check_norm(norm, K));
   RopeKvArgs ra{row_seq, row_pos, rope_table, block_table, static_cast<__nv_bfloat16*>(q_out),
