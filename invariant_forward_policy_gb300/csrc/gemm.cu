@@ -1116,11 +1116,13 @@ static int decode_tile_n(int64_t M, int64_t n_rows_w, int64_t K, bool swiglu, in
 }
 
 // Tile width of a call of more than 128 rows on a weight whose own width is
-// narrow (below 128: a small weight spread over the GPU at decode size).  Bits do
-// not depend on the width, so a prefill pass takes the width that minimises the
-// bytes its busiest CTA reads over all its tiles (tiles x (128 A rows + the W
-// slice)) instead of re-reading its A rows once per 16 or 32 columns.  min_bn:
-// SwiGLU pairs need 32, RoPE whole heads (and a width that divides N).
+// below 256 (the width that spreads the weight over the GPU at decode size).
+// Bits do not depend on the width, so a prefill pass takes the width that
+// minimises the bytes its busiest CTA reads over all its tiles (tiles x (128 A
+// rows + the W slice)): 16- or 32-wide tiles would re-read the A rows once per 16
+// or 32 columns, and at thousands of rows 256-wide tiles carry twice the MMA work
+// per staged byte of 128-wide ones.  min_bn: SwiGLU pairs need 32, RoPE whole
+// heads (and a width that divides N).
 static int wide_tile_n(int64_t M, int64_t n_rows_w, bool swiglu, int min_bn, bool divides, int bn_weight) {
   const int64_t n_out = swiglu ? n_rows_w / 2 : n_rows_w;
   const int64_t m_tiles = cdiv(M, kBM);
@@ -1285,7 +1287,7 @@ static bi_status run_gemm(const GemmCall& g, cudaStream_t st) {
   }
   if (!g.lse && !g.rope && g.E == 1 && !g.tile_expert && g.M <= kBM && splits == 1)
     bn = decode_tile_n(g.M, g.n_rows_w, g.K, swiglu, bn);
-  if (!g.lse && g.E == 1 && !g.tile_expert && g.M > kBM && splits == 1 && bn < 128)
+  if (!g.lse && g.E == 1 && !g.tile_expert && g.M > kBM && splits == 1 && bn < 256)
     bn = wide_tile_n(g.M, g.n_rows_w, swiglu, g.rope ? g.rope->hd : (swiglu ? 32 : 16), g.rope != nullptr, bn);
   if (g.lse && bn < 64) bn = 64;  // the fused log-softmax records are per 64+ vocab columns
   if (g.rope) {
